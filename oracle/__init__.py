@@ -1,0 +1,145 @@
+"""Oracle for jagged attention: plain fp64 CPU definition (see ``oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  The CUDA
+library never loads it and shares no code with it.
+
+Inputs are numpy arrays: values ``[T, H, D]`` (any float dtype; widened to fp64
+exactly), offsets ``int32[B+1]``, bias table ``[H, 32]`` or ``None``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+SOFTMAX, GELU_TANH, SILU = 0, 1, 2
+MODES = {"softmax": SOFTMAX, "gelu_tanh": GELU_TANH, "silu": SILU}
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` beside it (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O3", "-std=c11", "-D_DEFAULT_SOURCE", "-fopenmp", "-fPIC", "-shared",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.POINTER
+            d, i32 = ctypes.c_double, ctypes.c_int32
+            lib.oracle_relpos_bucket.argtypes = [ctypes.c_int64]
+            lib.oracle_relpos_bucket.restype = ctypes.c_int
+            lib.oracle_act.argtypes = [ctypes.c_int, d]
+            lib.oracle_act.restype = d
+            lib.oracle_act_grad.argtypes = [ctypes.c_int, d]
+            lib.oracle_act_grad.restype = d
+            lib.oracle_max_threads.restype = ctypes.c_int
+            common = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(i32), P(i32)]
+            lib.oracle_fwd.argtypes = common + [P(d)] * 3 + [ctypes.c_int, ctypes.c_int, P(d), d,
+                                                             P(d), P(d), ctypes.c_int]
+            lib.oracle_fwd.restype = ctypes.c_int
+            lib.oracle_bwd.argtypes = common + [P(d)] * 4 + [ctypes.c_int, ctypes.c_int, P(d), d,
+                                                             P(d), P(d), P(d), ctypes.c_int]
+            lib.oracle_bwd.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _check(q_off, kv_off, Q, K, V):
+    q_off = np.ascontiguousarray(np.asarray(q_off, dtype=np.int32))
+    kv_off = np.ascontiguousarray(np.asarray(kv_off, dtype=np.int32))
+    if q_off.ndim != 1 or q_off.shape != kv_off.shape or q_off.size < 1:
+        raise ValueError("offsets must be 1-D of equal length B+1")
+    if np.any(np.diff(q_off) < 0) or np.any(np.diff(kv_off) < 0) or q_off[0] < 0 or kv_off[0] < 0:
+        raise ValueError("offsets must be non-negative and non-decreasing")
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    if Q.ndim != 3 or K.shape != V.shape or K.ndim != 3 or Q.shape[1:] != K.shape[1:]:
+        raise ValueError("Q [Tq,H,D], K and V [Tkv,H,D] expected")
+    if Q.shape[0] < q_off[-1] or K.shape[0] < kv_off[-1]:
+        raise ValueError("offsets exceed the value tensors")
+    return q_off, kv_off, Q, K, V
+
+
+def relpos_bucket(r: int) -> int:
+    return int(_load().oracle_relpos_bucket(int(r)))
+
+
+def act(mode: str, x: float) -> float:
+    return float(_load().oracle_act(MODES[mode], float(x)))
+
+
+def act_grad(mode: str, x: float) -> float:
+    return float(_load().oracle_act_grad(MODES[mode], float(x)))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def fwd(q_off, kv_off, Q, K, V, *, mode="softmax", causal=False, bias=None, scale=None,
+        nthreads=0):
+    """Returns (O [Tq,H,D] fp64, LSE [Tq,H] fp64)."""
+    lib = _load()
+    q_off, kv_off, Q, K, V = _check(q_off, kv_off, Q, K, V)
+    B = q_off.size - 1
+    _, H, D = Q.shape
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    b = None if bias is None else _f64(bias).reshape(H, 32)
+    O = np.zeros_like(Q)
+    LSE = np.zeros((Q.shape[0], H), dtype=np.float64)
+    rc = lib.oracle_fwd(B, H, D, _ptr(q_off, ctypes.c_int32), _ptr(kv_off, ctypes.c_int32),
+                        _ptr(Q), _ptr(K), _ptr(V), MODES[mode], int(bool(causal)),
+                        None if b is None else _ptr(b), scale, _ptr(O), _ptr(LSE), int(nthreads))
+    if rc != 0:
+        raise MemoryError("oracle_fwd failed")
+    return O, LSE
+
+
+def bwd(q_off, kv_off, Q, K, V, dO, *, mode="softmax", causal=False, bias=None, scale=None,
+        nthreads=0):
+    """Returns (dQ, dK, dV), fp64, same shapes as Q, K, V."""
+    lib = _load()
+    q_off, kv_off, Q, K, V = _check(q_off, kv_off, Q, K, V)
+    dO = _f64(dO)
+    if dO.shape != Q.shape:
+        raise ValueError("dO must match Q")
+    B = q_off.size - 1
+    _, H, D = Q.shape
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    b = None if bias is None else _f64(bias).reshape(H, 32)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    rc = lib.oracle_bwd(B, H, D, _ptr(q_off, ctypes.c_int32), _ptr(kv_off, ctypes.c_int32),
+                        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), MODES[mode], int(bool(causal)),
+                        None if b is None else _ptr(b), scale, _ptr(dQ), _ptr(dK), _ptr(dV),
+                        int(nthreads))
+    if rc != 0:
+        raise MemoryError("oracle_bwd failed")
+    return dQ, dK, dV
