@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Benchmark: jagged attention forward+backward TFLOP/s (unpadded FLOPs) on GB300.
+
+One step = one forward and one backward pass over one seeded synthetic jagged batch
+(the hot path end to end: planner output reused, forward kernel, backward
+preprocess, backward main kernel, dQ convert).  Default workload: the long-sequence
+causal self-attention batch (64 sequences, lengths U{4096..32768}, 8 heads,
+head_dim 128, bf16, relative-position bias) -- the configuration the >=50%-of-peak
+target names.  Every input tensor (~2.5 GB each) is larger than the 129 MB L2, so no
+flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead, on a
+bounded sample of the same workload.  Under torchrun each rank runs its own batch
+(seeded per rank; weak scaling) with no collective in the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from jagged_sequence_attention_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "jagged attention fwd+bwd TFLOPS (unpadded) and % of GB300 BF16 tensor peak"
+UNIT = "TFLOP/s"
+
+
+# ----------------------------------------------------------------------------- FLOPs / bytes
+
+
+def allowed_pairs(q_lens, kv_lens, causal):
+    q = np.asarray(q_lens, dtype=np.int64)
+    kv = np.asarray(kv_lens, dtype=np.int64)
+    if not causal:
+        return int(np.sum(q * kv))
+    tot = 0
+    for a, b in zip(q.tolist(), kv.tolist()):
+        # rows i = 0..a-1 see min(b, i + 1 + b - a) keys (at least 0)
+        i = np.arange(a, dtype=np.int64)
+        tot += int(np.clip(i + 1 + b - a, 0, b).sum())
+    return tot
+
+
+def flops_of(batch):
+    pairs = allowed_pairs(batch.q_lens, batch.kv_lens, batch.causal)
+    fwd = 4.0 * batch.D * batch.H * pairs
+    return fwd, 2.5 * fwd
+
+
+def algorithmic_bytes(batch, elem=2):
+    Tq, Tkv, H, D = int(batch.q_off[-1]), int(batch.kv_off[-1]), batch.H, batch.D
+    fwd = elem * H * D * (2 * Tq + 2 * Tkv) + 4 * H * Tq
+    bwd = elem * H * D * (3 * Tq + 4 * Tkv) + 8 * H * Tq
+    return fwd, bwd
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "jagged_sequence_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}/{workload}")
+    if not e or e.get("kernel_digest") != kernel_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- reference (oracle)
+
+
+def oracle_sample(batch, target_seconds=15.0):
+    """The shortest sequences of the batch (all heads), as a CPU batch: a bounded sample
+    of the same workload for the oracle."""
+    order = np.argsort(batch.q_lens * batch.kv_lens)
+    # ~40 GFLOP of fp64 work per 15 s on the host cores is the planning figure
+    budget = 2.7e9 * target_seconds
+    seqs, tot = [], 0.0
+    for b in order:
+        f = 3.5 * 4.0 * batch.D * batch.H * allowed_pairs([batch.q_lens[b]], [batch.kv_lens[b]], batch.causal)
+        if seqs and tot + f > budget:
+            break
+        seqs.append(int(b))
+        tot += f
+    sub = wl.subset(batch, seqs)
+    cpu = wl.Batch(sub.name, sub.q_off, sub.kv_off, sub.Q.cpu(), sub.K.cpu(), sub.V.cpu(), sub.dO.cpu(),
+                   None if sub.bias is None else sub.bias.cpu(), sub.scale, sub.mode, sub.causal, sub.H, sub.D)
+    return cpu, seqs
+
+
+def run_oracle_once(cpu_batch):
+    import oracle
+    f64 = lambda t: t.detach().to(torch.float32).numpy().astype(np.float64)  # noqa: E731
+    b = None if cpu_batch.bias is None else f64(cpu_batch.bias)
+    t0 = time.perf_counter()
+    oracle.fwd(cpu_batch.q_off, cpu_batch.kv_off, f64(cpu_batch.Q), f64(cpu_batch.K), f64(cpu_batch.V),
+               mode=cpu_batch.mode, causal=cpu_batch.causal, bias=b, scale=cpu_batch.scale)
+    oracle.bwd(cpu_batch.q_off, cpu_batch.kv_off, f64(cpu_batch.Q), f64(cpu_batch.K), f64(cpu_batch.V),
+               f64(cpu_batch.dO), mode=cpu_batch.mode, causal=cpu_batch.causal, bias=b, scale=cpu_batch.scale)
+    return time.perf_counter() - t0
+
+
+def oracle_cores(cpu_batch):
+    import oracle
+    return int(min(oracle.max_threads(), cpu_batch.B * cpu_batch.H))
+
+
+# ----------------------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_causal", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    w = wl.WORKLOADS[args.workload]
+    cfg = {"workload": args.workload, "description": w.description, "B": w.B, "H": w.H, "D": w.D,
+           "mode": w.mode, "causal": w.causal, "bias": w.bias, "seed": wl.seed_of(w),
+           "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"dp{world} (independent batches)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            if dist:
+                dist.barrier()
+            return
+        batch = wl.make(args.workload, device="cpu")
+        cpu, seqs = oracle_sample(batch, args.cpu_seconds)
+        fl_f, fl_b = flops_of(cpu)
+        for _ in range(args.warmup if args.steps > 1 else 0):
+            break  # the oracle has no warm-up effects beyond the first load
+        run_oracle_once(wl.subset(cpu, [0], [0]))  # load / build once
+        times = [run_oracle_once(cpu) for _ in range(args.steps)]
+        t = sum(times) / len(times)
+        v = (fl_f + fl_b) / t / 1e12
+        sample = (f"{len(seqs)} shortest sequences of the workload (lengths {sorted(batch.q_lens[seqs].tolist())}), "
+                  f"all {cpu.H} heads, forward+backward in fp64")
+        cfg.update({"tokens": int(batch.q_off[-1]), "sample_tokens": int(cpu.q_off[-1])})
+        line = {"metric": METRIC, "value": v, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": oracle_cores(cpu), "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        if dist:
+            dist.barrier()
+        return
+
+    from jagged_sequence_attention_gb300 import _build
+    from jagged_sequence_attention_gb300 import jfa
+    _build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    seed = wl.seed_of(w) + 7919 * rank
+    batch = wl.make(args.workload, device=dev, seed=seed)
+    fl_f, fl_b = flops_of(batch)
+    by_f, by_b = algorithmic_bytes(batch)
+    cfg.update({"tokens": int(batch.q_off[-1]), "kv_tokens": int(batch.kv_off[-1]),
+                "unpadded_fwd_flop": fl_f, "unpadded_bwd_flop": fl_b})
+
+    stream = torch.cuda.current_stream()
+    plan = jfa.jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal)
+    O = torch.empty_like(batch.Q)
+    lse = torch.empty((batch.Q.shape[0], batch.H), dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(batch.Q), torch.empty_like(batch.K), torch.empty_like(batch.V)
+    ws = torch.empty(jfa.jfa_bwd_workspace_size(plan, batch.Q.dtype), dtype=torch.uint8, device=dev)
+
+    def step():
+        jfa.jfa_fwd(plan, batch.Q, batch.K, batch.V, batch.bias, batch.scale, O=O, lse=lse)
+        jfa.jfa_bwd(plan, batch.Q, batch.K, batch.V, O, batch.dO, lse, batch.bias, batch.scale, dQ=dQ, dK=dK,
+                    dV=dV, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = jfa.jfa_plan_device_status(plan)
+    if status != 0:
+        raise RuntimeError(f"device status after warm-up: {jfa.jfa_status_string(status)}")
+
+    jfa.jfa_plan_set_timing(plan, True)
+    jfa.jfa_plan_kernel_times(plan)
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else torch.cuda.current_device())
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    kt = jfa.jfa_plan_kernel_times(plan)
+    jfa.jfa_plan_set_timing(plan, False)
+    status = jfa.jfa_plan_device_status(plan)
+    if status != 0:
+        raise RuntimeError(f"device status after timing: {jfa.jfa_status_string(status)}")
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * (fl_f + fl_b) / (ms_step / 1e3) / 1e12
+    peaks = load_peaks()
+
+    # dominant kernel: the larger share of device time among the two tensor-core kernels
+    per = {k: (v[0] / v[1] if v[1] else 0.0, v[1], v[0]) for k, v in kt.items()}
+    dom = max(("fwd", "bwd_main"), key=lambda k: per[k][2])
+    dom_flop = fl_f if dom == "fwd" else fl_b
+    dom_ms = per[dom][0]
+    achieved = dom_flop / (dom_ms / 1e3) / 1e12 if dom_ms > 0 else 0.0
+    kname = {"fwd": "jfa_fwd_kernel", "bwd_main": "jfa_bwd_kernel"}[dom]
+    roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
+                "peak_kind": f"bf16 dense, sustained, {peaks['source']}", "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "traffic": measured_traffic(kname, args.workload),
+                "algorithmic_bytes_per_launch": by_f if dom == "fwd" else by_b,
+                "flop_per_launch": dom_flop}
+    kernels = {k: {"ms_per_launch": v[0], "launches": v[1], "share": v[2] / max(1e-9, sum(x[2] for x in per.values()))}
+               for k, v in per.items()}
+    launches = int(sum(v[1] for v in per.values()))
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+            "pct_of_bf16_peak_sustained": 100.0 * value / world / peaks["bf16_tflops_sustained"],
+            "fwd_tflops": fl_f / (kt["fwd"][0] / max(1, kt["fwd"][1]) / 1e3) / 1e12 if kt["fwd"][1] else None,
+            "roofline": roofline, "kernels": kernels, "gpu_launches": launches, "clocks": clocks}
+
+    # ---------------------------------------------------------------- end to end through the API
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        hQ, hK, hV, hdO = pin(batch.Q), pin(batch.K), pin(batch.V), pin(batch.dO)
+        hbias = None if batch.bias is None else pin(batch.bias)
+        hO, hdQ = torch.empty_like(hQ).pin_memory(), torch.empty_like(hQ).pin_memory()
+        hdK, hdV = torch.empty_like(hK).pin_memory(), torch.empty_like(hV).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        q_off, kv_off = batch.q_off.copy(), batch.kv_off.copy()
+        dQd, dKd, dVd, dOd = batch.Q, batch.K, batch.V, batch.dO
+        bias_d = batch.bias
+        h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hdO)) + (
+            0 if hbias is None else hbias.numel() * 4) + q_off.nbytes + kv_off.nbytes
+        d2h = sum(t.numel() * t.element_size() for t in (hO, hdQ, hdK, hdV, hlse))
+
+        def e2e_step():
+            dQd.copy_(hQ, non_blocking=True)
+            dKd.copy_(hK, non_blocking=True)
+            dVd.copy_(hV, non_blocking=True)
+            dOd.copy_(hdO, non_blocking=True)
+            if hbias is not None:
+                bias_d.copy_(hbias, non_blocking=True)
+            p2 = jfa.jfa_plan_create(q_off, kv_off, batch.H, batch.D, batch.mode, batch.causal)
+            jfa.jfa_fwd(p2, dQd, dKd, dVd, bias_d, batch.scale, O=O, lse=lse)
+            jfa.jfa_bwd(p2, dQd, dKd, dVd, O, dOd, lse, bias_d, batch.scale, dQ=dQ, dK=dK, dV=dV, workspace=ws)
+            hO.copy_(O, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            hdQ.copy_(dQ, non_blocking=True)
+            hdK.copy_(dK, non_blocking=True)
+            hdV.copy_(dV, non_blocking=True)
+            torch.cuda.synchronize()
+            jfa.jfa_plan_destroy(p2)
+
+        e2e_step()
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        el = (time.perf_counter() - t0) / args.e2e_steps
+        if dist:
+            t = torch.tensor([el], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            el = float(t.item())
+        line["e2e"] = {"value": world * (fl_f + fl_b) / el / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                       "d2h_bytes_per_step": int(d2h), "ms_per_step": el * 1e3, "steps": args.e2e_steps,
+                       "includes": "pinned H2D of Q,K,V,dO,bias,offsets; jfa_plan_create; jfa_fwd; jfa_bwd; "
+                                   "D2H of O,lse,dQ,dK,dV"}
+
+    # ---------------------------------------------------------------- CPU baseline (oracle)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu, seqs = oracle_sample(batch, args.cpu_seconds)
+        cf, cb = flops_of(cpu)
+        run_oracle_once(wl.subset(cpu, [0], [0]))
+        t = run_oracle_once(cpu)
+        line["cpu_baseline"] = {"value": (cf + cb) / t / 1e12, "unit": UNIT, "cores": oracle_cores(cpu),
+                                "kind": "oracle", "seconds": t,
+                                "sample": f"{len(seqs)} shortest sequences (lengths "
+                                          f"{sorted(batch.q_lens[seqs].tolist())}), all {cpu.H} heads, fwd+bwd fp64"}
+
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

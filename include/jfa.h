@@ -1,0 +1,167 @@
+/*
+ * libjfa -- Jagged Flash Attention and GDPA for GB300 (sm_103a).
+ *
+ * The operation (GEM training-efficiency article, aihot.vn, section "Jagged
+ * Sequence Flash Attention"; vibekk.com GEM article, FAQ "Jagged tensor 是什么"):
+ * attention computed directly on jagged tensors -- packed values plus offsets --
+ * with no padding, where every sequence b attends only within itself.  Query and
+ * key/value lengths may differ per sequence ("asymmetric query/key-value
+ * lengths"), an additive per-head bias may apply ("custom attention bias"), and the
+ * backward pass is provided.  The GDPA mode (same article, section "Generalized
+ * Dot-Product Attention (GDPA)") replaces softmax by an elementwise GELU or SiLU
+ * with no row normalisation.
+ *
+ * For sequence b, head h, query row i (0-based within the sequence), key row j:
+ *   s_ij   = scale * <q_i, k_j> + bias[h, bucket(|i + (kv_len - q_len) - j|)]
+ *   allowed(i, j) = !causal || j <= i + (kv_len - q_len)        (bottom-right causal)
+ *   SOFTMAX: o_i = sum_j softmax_j(s_ij) v_j over allowed j;  lse_i = log sum exp s_ij
+ *   GDPA:    o_i = sum_j act(s_ij) v_j over allowed j, act = tanh-GELU or SiLU
+ *   bucket(r) = min(31, floor(log2((1 + r)^2)))   (exact integer arithmetic)
+ * A row with no allowed key gets o = 0 (and lse = -inf); its gradients are 0.
+ *
+ * Layout and conventions (all calls):
+ *  - Q, O, dO, dQ are [T_q, H, D] row-major (token-major), T_q = q_offsets[B];
+ *    K, V, dK, dV are [T_kv, H, D], T_kv = kv_offsets[B].  Contiguous, 16-byte
+ *    aligned DEVICE pointers owned by the caller.  lse is fp32 [T_q, H].
+ *  - Element type: JFA_BF16 (bfloat16, head_dim 64 or 128) or JFA_F32 (float,
+ *    head_dim 32 or 64; the tensor cores compute in TF32).  Accumulation is fp32.
+ *  - Values must be finite: a key/value row of a neighbouring sequence is read
+ *    (and multiplied by an exact zero weight) at jagged tile edges.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *    stream).  jfa_plan_create (which uploads the work lists), jfa_plan_destroy,
+ *    jfa_plan_device_status and jfa_plan_kernel_times synchronise; jfa_fwd and
+ *    jfa_bwd never do.
+ *  - Every call returns a jfa_status; argument errors are detected on the host
+ *    before anything is launched.  No call aborts the process.
+ *  - A plan is not thread-safe: do not use one plan from two host threads at once.
+ */
+#ifndef JFA_H
+#define JFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    JFA_OK = 0,
+    JFA_ERR_INVALID_ARG = 1,    /* null pointer, bad offsets, misaligned pointer, bad size */
+    JFA_ERR_UNSUPPORTED = 2,    /* head_dim / dtype / mode combination not built */
+    JFA_ERR_CUDA = 3,           /* a CUDA runtime or driver call failed */
+    JFA_ERR_TIMEOUT = 4,        /* a kernel pipeline wait exceeded its limit (device status) */
+    JFA_ERR_DEVICE_BOUNDS = 5,  /* a kernel's own bounds check fired (device status) */
+    JFA_ERR_PLAN_MISMATCH = 6,  /* the call does not match the plan (mode, head_dim) */
+    JFA_ERR_NO_DEVICE = 7       /* no usable sm_100-family GPU */
+} jfa_status;
+
+typedef enum { JFA_SOFTMAX = 0, JFA_GDPA_GELU_TANH = 1, JFA_GDPA_SILU = 2 } jfa_mode;
+typedef enum { JFA_BF16 = 0, JFA_F32 = 1 } jfa_dtype;
+typedef enum { JFA_BIAS_NONE = 0, JFA_BIAS_RELPOS32 = 1 } jfa_bias_kind;
+
+typedef struct jfa_plan_t* jfa_plan;
+
+/*
+ * Builds the work lists for one batch shape (the planner): validates offsets,
+ * splits every (sequence, head) into query tiles (forward) and key/value tiles
+ * (backward), costs each tile by the number of score tiles it visits (causal
+ * tiles stop at the diagonal), and assigns them longest-first to the least loaded
+ * CTA of a persistent grid, so that short sequences never leave SMs idle while a
+ * long one finishes (the article's point that padding-free kernels otherwise idle
+ * SMs when short sequences end early).
+ *   q_offsets, kv_offsets: int32[B+1], non-decreasing, offsets[0] == 0; host
+ *     pointers, or device pointers when offsets_on_device != 0 (then copied to the
+ *     host on `stream`).  Copied; the caller keeps ownership.
+ *   The plan's device memory (offsets, work lists, status word) is allocated here
+ *   and uploaded on `stream`, which this call synchronises.
+ *   B >= 0 sequences, H >= 1 heads, D head_dim, mode a jfa_mode, causal 0/1.
+ *   out: receives a library-owned plan; free with jfa_plan_destroy.
+ * Errors: INVALID_ARG (bad offsets or sizes), UNSUPPORTED (D not 32/64/128),
+ * NO_DEVICE, CUDA.
+ */
+jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
+                           int32_t H, int32_t D, int32_t mode, int32_t causal,
+                           int32_t offsets_on_device, void* stream, jfa_plan* out);
+
+/* Frees a plan and its device memory (cudaFree synchronises the device, so launches
+ * still using the plan finish first).  NULL is accepted. */
+jfa_status jfa_plan_destroy(jfa_plan plan);
+
+/*
+ * Plan facts for callers and tests, written to info[0..n): T_q, T_kv, B, H, D,
+ * mode, causal, forward work items, forward grid, backward work items, backward
+ * grid, SM count.  n may be smaller than 12.
+ */
+jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
+
+/*
+ * Forward pass.
+ *   Q [T_q,H,D], K, V [T_kv,H,D] (dtype); bias_table fp32 [H,32] when bias_kind is
+ *   JFA_BIAS_RELPOS32, else ignored; scale multiplies <q,k> (typically 1/sqrt(D)).
+ *   O [T_q,H,D] is written for every row covered by the offsets, in o_dtype:
+ *   JFA_F32 (the fp32 accumulator, no output rounding) or JFA_BF16 (rounded to
+ *   nearest even); with dtype JFA_F32, o_dtype must be JFA_F32.
+ *   lse fp32 [T_q,H]: written in SOFTMAX mode (natural log, -inf for a row with
+ *   no allowed key) and required there; ignored and may be NULL in GDPA modes.
+ * Errors: INVALID_ARG, UNSUPPORTED, PLAN_MISMATCH, CUDA (launch failure).
+ */
+jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, const void* V,
+                   int32_t bias_kind, const float* bias_table, float scale, void* O, int32_t o_dtype,
+                   float* lse, void* stream);
+
+/* Bytes of device workspace jfa_bwd needs for this plan and dtype (fp32 dQ
+ * accumulator [T_q,H,D] plus fp32 row terms [T_q,H]); 0 on a bad plan. */
+size_t jfa_bwd_workspace_size(jfa_plan plan, int32_t dtype);
+
+/*
+ * Backward pass of L = sum(O * dO) for the forward with the same arguments.
+ *   O (in o_dtype) and lse are the forward's outputs (both ignored in GDPA modes);
+ *   dO is the upstream gradient [T_q,H,D] (dtype).  Writes dQ [T_q,H,D], dK, dV
+ *   [T_kv,H,D] (dtype).
+ *   workspace: caller-owned device memory of at least jfa_bwd_workspace_size bytes,
+ *   256-byte aligned; its contents need not be initialised and are clobbered.
+ * Errors: INVALID_ARG (incl. too small a workspace), UNSUPPORTED, PLAN_MISMATCH,
+ * CUDA.
+ */
+jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, const void* V,
+                   const void* O, int32_t o_dtype, const void* dO, const float* lse,
+                   int32_t bias_kind, const float* bias_table, float scale, void* dQ, void* dK,
+                   void* dV, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then reads and clears the plan's device status word, which
+ * the kernels set when a pipeline wait times out (TIMEOUT) or a bounds check fires
+ * (DEVICE_BOUNDS).  Returns JFA_OK when no kernel reported anything. */
+jfa_status jfa_plan_device_status(jfa_plan plan, void* stream);
+
+/* Host-only planner, usable without a GPU (the same code jfa_plan_create runs).
+ * pass 0 = forward (query tiles of 128 rows), 1 = backward (key/value tiles of 128
+ * rows).  jfa_worklist_size gives the number of work items; jfa_worklist_build
+ * writes items as int32 quadruples (sequence, head, tile index, inner tiles
+ * visited) grouped by CTA, cta_offsets[n_ctas+1] delimiting each CTA's items, and
+ * optionally each CTA's total cost in score-tile units. */
+jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
+                             int32_t H, int32_t causal, int32_t pass, int64_t* n_items);
+jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
+                              int32_t H, int32_t causal, int32_t pass, int32_t n_ctas,
+                              int32_t* items, int32_t* cta_offsets, int64_t* cta_cost);
+
+/* Kernel timing for measurement.  With timing enabled, every kernel launch made for
+ * this plan is bracketed by a pair of CUDA events recorded on the launch stream.
+ * jfa_plan_kernel_times synchronises those events and returns, per kernel kind
+ * (0 forward, 1 backward preprocess, 2 backward main, 3 backward dQ convert), the
+ * summed milliseconds and the number of launches since the previous query, then
+ * forgets them.  Timing is off by default; enabling it adds one event record before
+ * and after each launch.  total_ms and launches point to arrays of 4 (either may be
+ * NULL). */
+jfa_status jfa_plan_set_timing(jfa_plan plan, int32_t enable);
+jfa_status jfa_plan_kernel_times(jfa_plan plan, double* total_ms, int64_t* launches);
+
+/* Static description of a status code. */
+const char* jfa_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JFA_H */

@@ -1,0 +1,417 @@
+// C-ABI of libjfa: argument validation, plans, tensor maps and kernel launches.
+// Semantics of every entry point are documented in include/jfa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "jfa_internal.h"
+
+using namespace jfa;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t elem_bytes(int dtype) { return dtype == JFA_F32 ? 4 : 2; }
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// 2-D view [rows, H*D] of a token-major [T, H, D] tensor, box = 128 bytes x box_rows,
+// 128-byte swizzle, zero fill beyond the last row.
+jfa_status make_map(CUtensorMap* map, int dtype, const void* base, int64_t rows, int H, int D,
+                    const void* dummy, int box_rows = 128) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return JFA_ERR_CUDA;
+    const size_t E = elem_bytes(dtype);
+    if (rows <= 0) {  // never read; keep the descriptor well-formed
+        rows = 1;
+        base = dummy;
+    }
+    cuuint64_t dims[2] = {cuuint64_t(H) * cuuint64_t(D), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(H) * cuuint64_t(D) * E};
+    cuuint32_t box[2] = {cuuint32_t(128 / E), cuuint32_t(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(map, dtype == JFA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? JFA_OK : JFA_ERR_CUDA;
+}
+
+cudaEvent_t take_event(jfa_plan plan) {
+    if (!plan->ev_pool.empty()) {
+        cudaEvent_t e = plan->ev_pool.back();
+        plan->ev_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Records a start event before a kernel launch when timing is enabled.
+struct KernelTimer {
+    jfa_plan plan;
+    int kind;
+    cudaStream_t st;
+    cudaEvent_t a = nullptr, b = nullptr;
+    KernelTimer(jfa_plan p, int k, cudaStream_t s) : plan(p), kind(k), st(s) {
+        if (!plan->timing) return;
+        a = take_event(plan);
+        b = take_event(plan);
+        if (a && b) cudaEventRecord(a, st);
+    }
+    void done() {
+        if (!plan->timing || !a || !b) return;
+        cudaEventRecord(b, st);
+        plan->ev_pending.push_back({kind, {a, b}});
+        a = b = nullptr;
+    }
+};
+
+jfa_status check_plan_call(jfa_plan plan, int dtype, int bias_kind, const float* bias_table) {
+    if (!plan) return JFA_ERR_INVALID_ARG;
+    if (dtype != JFA_BF16 && dtype != JFA_F32) return JFA_ERR_INVALID_ARG;
+    if (!supported(dtype, plan->D)) return JFA_ERR_UNSUPPORTED;
+    if (bias_kind != JFA_BIAS_NONE && bias_kind != JFA_BIAS_RELPOS32) return JFA_ERR_INVALID_ARG;
+    if (bias_kind == JFA_BIAS_RELPOS32 && !bias_table) return JFA_ERR_INVALID_ARG;
+    return JFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* jfa_status_string(int32_t s) {
+    switch (s) {
+        case JFA_OK: return "ok";
+        case JFA_ERR_INVALID_ARG: return "invalid argument";
+        case JFA_ERR_UNSUPPORTED: return "unsupported head_dim/dtype/mode";
+        case JFA_ERR_CUDA: return "CUDA error";
+        case JFA_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+        case JFA_ERR_DEVICE_BOUNDS: return "kernel bounds check fired";
+        case JFA_ERR_PLAN_MISMATCH: return "call does not match the plan";
+        case JFA_ERR_NO_DEVICE: return "no usable sm_100-family GPU";
+        default: return "unknown status";
+    }
+}
+
+jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H,
+                             int32_t causal, int32_t pass, int64_t* n_items) {
+    if (!n_items || H < 1 || (pass != 0 && pass != 1)) return JFA_ERR_INVALID_ARG;
+    jfa_status s = validate_offsets(q_offsets, kv_offsets, B);
+    if (s != JFA_OK) return s;
+    *n_items = count_items(q_offsets, kv_offsets, B, H, causal, pass);
+    return JFA_OK;
+}
+
+jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H,
+                              int32_t causal, int32_t pass, int32_t n_ctas, int32_t* items,
+                              int32_t* cta_offsets, int64_t* cta_cost) {
+    if (H < 1 || n_ctas < 1 || !cta_offsets || (pass != 0 && pass != 1)) return JFA_ERR_INVALID_ARG;
+    jfa_status s = validate_offsets(q_offsets, kv_offsets, B);
+    if (s != JFA_OK) return s;
+    const int64_t n = count_items(q_offsets, kv_offsets, B, H, causal, pass);
+    if (n > 0 && !items) return JFA_ERR_INVALID_ARG;
+    build_worklist(q_offsets, kv_offsets, B, H, causal, pass, n_ctas, reinterpret_cast<WorkItem*>(items),
+                   cta_offsets, cta_cost);
+    return JFA_OK;
+}
+
+jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H, int32_t D,
+                           int32_t mode, int32_t causal, int32_t offsets_on_device, void* stream, jfa_plan* out) {
+    if (!out) return JFA_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!q_offsets || !kv_offsets || B < 0 || H < 1 || H > 65535) return JFA_ERR_INVALID_ARG;
+    if (mode != JFA_SOFTMAX && mode != JFA_GDPA_GELU_TANH && mode != JFA_GDPA_SILU) return JFA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return JFA_ERR_INVALID_ARG;
+    if (D != 32 && D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_NO_DEVICE;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return JFA_ERR_NO_DEVICE;
+    if (prop.major != 10) return JFA_ERR_NO_DEVICE;
+
+    std::vector<int32_t> qo(size_t(B) + 1), ko(size_t(B) + 1);
+    if (offsets_on_device) {
+        if (cudaMemcpyAsync(qo.data(), q_offsets, qo.size() * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            cudaMemcpyAsync(ko.data(), kv_offsets, ko.size() * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return JFA_ERR_CUDA;
+    } else {
+        std::memcpy(qo.data(), q_offsets, qo.size() * 4);
+        std::memcpy(ko.data(), kv_offsets, ko.size() * 4);
+    }
+    jfa_status s = validate_offsets(qo.data(), ko.data(), B);
+    if (s != JFA_OK) return s;
+
+    jfa_plan_t* p = new (std::nothrow) jfa_plan_t();
+    if (!p) return JFA_ERR_CUDA;
+    p->B = B;
+    p->H = H;
+    p->D = D;
+    p->mode = mode;
+    p->causal = causal;
+    p->Tq = qo[size_t(B)];
+    p->Tkv = ko[size_t(B)];
+    p->device = dev;
+    p->num_sms = prop.multiProcessorCount;
+    p->q_off = qo;
+    p->kv_off = ko;
+    p->timing = false;
+
+    p->n_fwd_items = count_items(qo.data(), ko.data(), B, H, causal, 0);
+    p->n_bwd_items = count_items(qo.data(), ko.data(), B, H, causal, 1);
+    p->fwd_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_fwd_items)));
+    p->bwd_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_bwd_items)));
+    std::vector<WorkItem> fi(size_t(std::max<int64_t>(1, p->n_fwd_items)));
+    std::vector<WorkItem> bi(size_t(std::max<int64_t>(1, p->n_bwd_items)));
+    std::vector<int32_t> fo(size_t(p->fwd_grid) + 1), bo(size_t(p->bwd_grid) + 1);
+    build_worklist(qo.data(), ko.data(), B, H, causal, 0, p->fwd_grid, fi.data(), fo.data(), nullptr);
+    build_worklist(qo.data(), ko.data(), B, H, causal, 1, p->bwd_grid, bi.data(), bo.data(), nullptr);
+
+    // One device block: offsets, status word, work lists (16-byte aligned pieces).
+    const size_t off_bytes = round_up((size_t(B) + 1) * 4, 256);
+    size_t cur = 0;
+    const size_t o_q = cur; cur += off_bytes;
+    const size_t o_kv = cur; cur += off_bytes;
+    const size_t o_st = cur; cur += 256;
+    const size_t o_fi = cur; cur += round_up(fi.size() * 16, 256);
+    const size_t o_fo = cur; cur += round_up(fo.size() * 4, 256);
+    const size_t o_bi = cur; cur += round_up(bi.size() * 16, 256);
+    const size_t o_bo = cur; cur += round_up(bo.size() * 4, 256);
+    if (cudaMalloc(&p->dev_block, cur) != cudaSuccess) {
+        delete p;
+        return JFA_ERR_CUDA;
+    }
+    char* base = static_cast<char*>(p->dev_block);
+    p->d_q_off = reinterpret_cast<int32_t*>(base + o_q);
+    p->d_kv_off = reinterpret_cast<int32_t*>(base + o_kv);
+    p->d_status = reinterpret_cast<int*>(base + o_st);
+    p->d_fwd_items = reinterpret_cast<int4*>(base + o_fi);
+    p->d_fwd_cta_off = reinterpret_cast<int32_t*>(base + o_fo);
+    p->d_bwd_items = reinterpret_cast<int4*>(base + o_bi);
+    p->d_bwd_cta_off = reinterpret_cast<int32_t*>(base + o_bo);
+    bool ok = cudaMemcpyAsync(p->d_q_off, qo.data(), qo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(p->d_kv_off, ko.data(), ko.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemsetAsync(p->d_status, 0, 256, st) == cudaSuccess &&
+              cudaMemcpyAsync(p->d_fwd_items, fi.data(), fi.size() * 16, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(p->d_fwd_cta_off, fo.data(), fo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(p->d_bwd_items, bi.data(), bi.size() * 16, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(p->d_bwd_cta_off, bo.data(), bo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    // The host vectors are pageable: the copies above are staged before returning,
+    // but keep the stream ordered before the vectors go out of scope.
+    if (!ok || cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaFree(p->dev_block);
+        delete p;
+        return JFA_ERR_CUDA;
+    }
+    *out = p;
+    return JFA_OK;
+}
+
+jfa_status jfa_plan_destroy(jfa_plan plan) {
+    if (!plan) return JFA_OK;
+    for (auto& pr : plan->ev_pending) {
+        cudaEventDestroy(pr.second.first);
+        cudaEventDestroy(pr.second.second);
+    }
+    for (cudaEvent_t e : plan->ev_pool) cudaEventDestroy(e);
+    cudaError_t e = cudaFree(plan->dev_block);
+    delete plan;
+    return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
+    if (!plan || !info || n < 0) return JFA_ERR_INVALID_ARG;
+    const int64_t v[12] = {plan->Tq, plan->Tkv, plan->B, plan->H, plan->D, plan->mode, plan->causal,
+                           plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items, plan->bwd_grid, plan->num_sms};
+    for (int32_t i = 0; i < n && i < 12; ++i) info[i] = v[i];
+    return JFA_OK;
+}
+
+jfa_status jfa_plan_set_timing(jfa_plan plan, int32_t enable) {
+    if (!plan) return JFA_ERR_INVALID_ARG;
+    plan->timing = enable != 0;
+    return JFA_OK;
+}
+
+jfa_status jfa_plan_kernel_times(jfa_plan plan, double* total_ms, int64_t* launches) {
+    if (!plan) return JFA_ERR_INVALID_ARG;
+    double t[4] = {0, 0, 0, 0};
+    int64_t n[4] = {0, 0, 0, 0};
+    jfa_status st = JFA_OK;
+    for (auto& pr : plan->ev_pending) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(pr.second.second) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, pr.second.first, pr.second.second) != cudaSuccess)
+            st = JFA_ERR_CUDA;
+        t[pr.first] += ms;
+        n[pr.first] += 1;
+        plan->ev_pool.push_back(pr.second.first);
+        plan->ev_pool.push_back(pr.second.second);
+    }
+    plan->ev_pending.clear();
+    for (int i = 0; i < 4; ++i) {
+        if (total_ms) total_ms[i] = t[i];
+        if (launches) launches[i] = n[i];
+    }
+    return st;
+}
+
+jfa_status jfa_plan_device_status(jfa_plan plan, void* stream) {
+    if (!plan) return JFA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    if (cudaMemcpyAsync(&h, plan->d_status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemsetAsync(plan->d_status, 0, 4, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+        return JFA_ERR_CUDA;
+    if (h & kStatusTimeout) return JFA_ERR_TIMEOUT;
+    if (h & kStatusBounds) return JFA_ERR_DEVICE_BOUNDS;
+    return JFA_OK;
+}
+
+jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, const void* V, int32_t bias_kind,
+                   const float* bias_table, float scale, void* O, int32_t o_dtype, float* lse, void* stream) {
+    jfa_status s = check_plan_call(plan, dtype, bias_kind, bias_table);
+    if (s != JFA_OK) return s;
+    if (o_dtype != JFA_BF16 && o_dtype != JFA_F32) return JFA_ERR_INVALID_ARG;
+    if (dtype == JFA_F32 && o_dtype != JFA_F32) return JFA_ERR_UNSUPPORTED;
+    const bool softmax = plan->mode == JFA_SOFTMAX;
+    if (plan->Tq > 0 && (!Q || !O || (softmax && !lse))) return JFA_ERR_INVALID_ARG;
+    if (plan->Tkv > 0 && (!K || !V)) return JFA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(bias_table) & 3u))
+        return JFA_ERR_INVALID_ARG;
+    if (plan->Tq == 0 || plan->n_fwd_items == 0) return JFA_OK;
+    CUtensorMap mq, mk, mv;
+    if (dtype == JFA_BF16 &&
+        ((s = make_map(&mq, dtype, Q, plan->Tq, plan->H, plan->D, plan->dev_block)) != JFA_OK ||
+         (s = make_map(&mk, dtype, K, plan->Tkv, plan->H, plan->D, plan->dev_block)) != JFA_OK ||
+         (s = make_map(&mv, dtype, V, plan->Tkv, plan->H, plan->D, plan->dev_block)) != JFA_OK))
+        return s;
+    FwdParams p;
+    p.items = plan->d_fwd_items;
+    p.cta_off = plan->d_fwd_cta_off;
+    p.q_off = plan->d_q_off;
+    p.kv_off = plan->d_kv_off;
+    p.H = plan->H;
+    p.mode = plan->mode;
+    p.causal = plan->causal;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.bias = bias_kind == JFA_BIAS_RELPOS32 ? bias_table : nullptr;
+    p.O = O;
+    p.lse = softmax ? lse : nullptr;
+    p.status = plan->d_status;
+    KernelTimer tm(plan, 0, static_cast<cudaStream_t>(stream));
+    cudaError_t e = dtype == JFA_BF16
+                        ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, plan->fwd_grid, static_cast<cudaStream_t>(stream))
+                        : launch_fwd_f32(plan->D, Q, K, V, p, plan->n_fwd_items, static_cast<cudaStream_t>(stream));
+    tm.done();
+    return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+size_t jfa_bwd_workspace_size(jfa_plan plan, int32_t dtype) {
+    if (!plan || (dtype != JFA_BF16 && dtype != JFA_F32)) return 0;
+    const size_t rows = size_t(plan->Tq) * size_t(plan->H);
+    return round_up(rows * size_t(plan->D) * 4, 256) + round_up(rows * 4, 256);
+}
+
+jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, const void* V, const void* O,
+                   int32_t o_dtype, const void* dO, const float* lse, int32_t bias_kind, const float* bias_table,
+                   float scale, void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+    jfa_status s = check_plan_call(plan, dtype, bias_kind, bias_table);
+    if (s != JFA_OK) return s;
+    if (o_dtype != JFA_BF16 && o_dtype != JFA_F32) return JFA_ERR_INVALID_ARG;
+    if (dtype == JFA_F32 && o_dtype != JFA_F32) return JFA_ERR_UNSUPPORTED;
+    const bool softmax = plan->mode == JFA_SOFTMAX;
+    if (plan->Tq > 0 && (!Q || !O || !dO || !dQ || (softmax && !lse))) return JFA_ERR_INVALID_ARG;
+    if (plan->Tkv > 0 && (!K || !V || !dK || !dV)) return JFA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(dQ) ||
+        !aligned16(dK) || !aligned16(dV) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+        (reinterpret_cast<uintptr_t>(bias_table) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return JFA_ERR_INVALID_ARG;
+    const size_t need = jfa_bwd_workspace_size(plan, dtype);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return JFA_ERR_INVALID_ARG;
+    if (plan->Tkv == 0 && plan->Tq == 0) return JFA_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t rows = size_t(plan->Tq) * size_t(plan->H);
+    float* dq_acc = static_cast<float*>(workspace);
+    float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * size_t(plan->D) * 4, 256));
+
+    cudaError_t e = cudaSuccess;
+    if (plan->Tq > 0) {
+        KernelTimer tm(plan, 1, st);
+        e = launch_bwd_pre(dtype, o_dtype, plan->D, O, dO, delta, dq_acc, plan->Tq, plan->H, plan->mode, st);
+        tm.done();
+        if (e != cudaSuccess) return JFA_ERR_CUDA;
+    }
+    if (plan->n_bwd_items > 0) {
+        CUtensorMap mq, mk, mv, mdo;
+        if (dtype == JFA_BF16 &&
+            ((s = make_map(&mq, dtype, Q, plan->Tq, plan->H, plan->D, plan->dev_block, kBwdBM)) != JFA_OK ||
+             (s = make_map(&mk, dtype, K, plan->Tkv, plan->H, plan->D, plan->dev_block, kBwdBN)) != JFA_OK ||
+             (s = make_map(&mv, dtype, V, plan->Tkv, plan->H, plan->D, plan->dev_block, kBwdBN)) != JFA_OK ||
+             (s = make_map(&mdo, dtype, dO, plan->Tq, plan->H, plan->D, plan->dev_block, kBwdBM)) != JFA_OK))
+            return s;
+        BwdParams p;
+        p.items = plan->d_bwd_items;
+        p.cta_off = plan->d_bwd_cta_off;
+        p.q_off = plan->d_q_off;
+        p.kv_off = plan->d_kv_off;
+        p.H = plan->H;
+        p.mode = plan->mode;
+        p.causal = plan->causal;
+        p.scale = scale;
+        p.scale_log2 = scale * 1.4426950408889634f;
+        p.bias = bias_kind == JFA_BIAS_RELPOS32 ? bias_table : nullptr;
+        p.lse = softmax ? lse : nullptr;
+        p.delta = delta;
+        p.dq_acc = dq_acc;
+        p.dK = dK;
+        p.dV = dV;
+        p.status = plan->d_status;
+        KernelTimer tm(plan, 2, st);
+        e = dtype == JFA_BF16 ? launch_bwd_main(dtype, plan->D, mq, mk, mv, mdo, p, plan->bwd_grid, st)
+                              : launch_bwd_f32(plan->D, Q, K, V, dO, p, plan->n_bwd_items, st);
+        tm.done();
+        if (e != cudaSuccess) return JFA_ERR_CUDA;
+    }
+    if (plan->Tq > 0) {
+        KernelTimer tm(plan, 3, st);
+        e = launch_bwd_post(dtype, plan->D, dq_acc, dQ, plan->Tq, plan->H, scale, st);
+        tm.done();
+        if (e != cudaSuccess) return JFA_ERR_CUDA;
+    }
+    return JFA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,262 @@
+// fp32 path: jagged attention forward and backward on the CUDA cores in fp32.
+//
+// Same operation, work items and conventions as the bf16 tensor-core kernels (the
+// GEM articles' jagged flash attention and GDPA), for float inputs.  The tensor
+// cores' fp32-input format (TF32) drops 13 mantissa bits and tcgen05 takes TF32
+// operands only K-major, while V, dO and Q enter the products MN-major; for the
+// float element type the kernels therefore use plain fp32 FMA, one thread per
+// row, with K/V (forward) or Q/dO (backward) tiles staged in shared memory.
+#include "jfa_internal.h"
+
+#include <math.h>
+
+namespace jfa {
+
+namespace {
+
+constexpr int kF32Rows = 128;   // threads per CTA = rows of the outer tile
+constexpr int kF32Inner = 64;   // rows of the staged inner tile (forward)
+constexpr int kF32InnerB = 32;  // rows of the staged inner tile (backward)
+
+__device__ __forceinline__ int bucket_f32(int r) {
+    r = r < 0 ? -r : r;
+    if (r >= 46340) return 31;
+    const uint32_t v = uint32_t(r + 1) * uint32_t(r + 1);
+    return 31 - __clz(v);
+}
+
+__device__ __forceinline__ float act_f32(int mode, float x) {
+    if (mode == JFA_GDPA_GELU_TANH) {
+        const float c = 0.7978845608028654f;
+        return 0.5f * x * (1.f + tanhf(c * (x + 0.044715f * x * x * x)));
+    }
+    return x / (1.f + expf(-x));
+}
+
+__device__ __forceinline__ float act_grad_f32(int mode, float x) {
+    if (mode == JFA_GDPA_GELU_TANH) {
+        const float c = 0.7978845608028654f;
+        const float t = tanhf(c * (x + 0.044715f * x * x * x));
+        return 0.5f * (1.f + t) + 0.5f * x * (1.f - t * t) * c * (1.f + 3.f * 0.044715f * x * x);
+    }
+    const float sg = 1.f / (1.f + expf(-x));
+    return sg * (1.f + x * (1.f - sg));
+}
+
+// One CTA per forward work item (query tile of 128 rows); thread = query row.
+template <int D>
+__global__ void __launch_bounds__(kF32Rows) jfa_fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
+                                                                const float* __restrict__ V, const FwdParams p) {
+    __shared__ float sK[kF32Inner][D];
+    __shared__ float sV[kF32Inner][D];
+    __shared__ float sB[32];
+    const int4 w = p.items[blockIdx.x];
+    const int b = w.x, h = w.y, mt = w.z, n_tiles = w.w;
+    const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
+    const int k0 = p.kv_off[b], kv_len = p.kv_off[b + 1] - k0;
+    const int t = threadIdx.x, row = mt * kF32Rows + t;
+    const bool valid = row < q_len;
+    const int diag = kv_len - q_len;
+    const bool softmax = p.mode == JFA_SOFTMAX;
+    if (t < 32) sB[t] = p.bias ? p.bias[h * 32 + t] : 0.f;
+    float q[D], o[D];
+    const size_t rq = (size_t(q0) + size_t(valid ? row : 0)) * p.H + h;
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+        q[d] = valid ? Q[rq * D + d] : 0.f;
+        o[d] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    // keys up to the causal limit of the tile's last row (the planner's count, in
+    // 128-key units), staged 64 at a time
+    const int kv_end = min(kv_len, n_tiles * kFwdBN);
+    const int lim = p.causal ? min(kv_len, row + diag + 1) : kv_len;  // keys [0, lim) allowed
+    for (int c0 = 0; c0 < kv_end; c0 += kF32Inner) {
+        __syncthreads();
+        for (int e = t; e < kF32Inner * D; e += kF32Rows) {
+            const int r = e / D, d = e % D;
+            const bool in = c0 + r < kv_len;
+            const size_t rk = (size_t(k0) + size_t(in ? c0 + r : 0)) * p.H + h;
+            sK[r][d] = in ? K[rk * D + d] : 0.f;
+            sV[r][d] = in ? V[rk * D + d] : 0.f;
+        }
+        __syncthreads();
+        float s[kF32Inner];
+        float mx = -INFINITY;
+#pragma unroll 4
+        for (int j = 0; j < kF32Inner; ++j) {
+            float acc = 0.f;
+#pragma unroll
+            for (int d = 0; d < D; ++d) acc = fmaf(q[d], sK[j][d], acc);
+            float x = acc * p.scale;
+            if (p.bias) x += sB[bucket_f32(row + diag - (c0 + j))];
+            const bool ok = valid && (c0 + j) < lim;
+            s[j] = ok ? x : -INFINITY;
+            mx = fmaxf(mx, s[j]);
+        }
+        if (softmax) {
+            const float m_new = fmaxf(m, mx);
+            if (m_new == -INFINITY) continue;
+            const float alpha = (m == -INFINITY) ? 0.f : expf(m - m_new);
+            l *= alpha;
+#pragma unroll
+            for (int d = 0; d < D; ++d) o[d] *= alpha;
+            for (int j = 0; j < kF32Inner; ++j) {
+                const float pj = expf(s[j] - m_new);
+                l += pj;
+#pragma unroll
+                for (int d = 0; d < D; ++d) o[d] = fmaf(pj, sV[j][d], o[d]);
+            }
+            m = m_new;
+        } else {
+            for (int j = 0; j < kF32Inner; ++j) {
+                if (s[j] == -INFINITY) continue;
+                const float a = act_f32(p.mode, s[j]);
+#pragma unroll
+                for (int d = 0; d < D; ++d) o[d] = fmaf(a, sV[j][d], o[d]);
+            }
+        }
+    }
+    if (!valid) return;
+    float* O = static_cast<float*>(p.O) + rq * D;
+    const float inv = softmax ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
+#pragma unroll
+    for (int d = 0; d < D; ++d) O[d] = o[d] * inv;
+    if (softmax && p.lse) p.lse[rq] = l > 0.f ? m + logf(l) : -INFINITY;
+}
+
+// One CTA per backward work item (key tile of 128 rows); thread = key row.  Query
+// rows stream through shared memory 64 at a time; dS for the chunk is kept in
+// shared memory so that dQ is reduced over the CTA's keys before one atomic add per
+// (query row, d).
+template <int D>
+__global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
+                                                                const float* __restrict__ V, const float* __restrict__ dO,
+                                                                const BwdParams p) {
+    __shared__ float sQ[kF32InnerB][D];
+    __shared__ float sdO[kF32InnerB][D];
+    __shared__ float sDS[kF32InnerB][kF32Rows + 1];
+    __shared__ float sL[kF32InnerB], sDel[kF32InnerB];
+    __shared__ float sB[32];
+    const int4 w = p.items[blockIdx.x];
+    const int b = w.x, h = w.y, nt = w.z, n = w.w;
+    const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
+    const int k0 = p.kv_off[b], kv_len = p.kv_off[b + 1] - k0;
+    const int t = threadIdx.x, j = nt * kBwdBN + t;
+    const bool kvalid = j < kv_len;
+    const int diag = kv_len - q_len;
+    const bool softmax = p.mode == JFA_SOFTMAX;
+    if (t < 32) sB[t] = p.bias ? p.bias[h * 32 + t] : 0.f;
+    const size_t rk = (size_t(k0) + size_t(kvalid ? j : 0)) * p.H + h;
+    float k[D], v[D], dk[D], dv[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+        k[d] = kvalid ? K[rk * D + d] : 0.f;
+        v[d] = kvalid ? V[rk * D + d] : 0.f;
+        dk[d] = 0.f;
+        dv[d] = 0.f;
+    }
+    const int nq = (q_len + kBwdBM - 1) / kBwdBM;
+    const int row_begin = (nq - n) * kBwdBM;
+    const int n_keys = min(kBwdBN, kv_len - nt * kBwdBN);
+    for (int r0 = row_begin; r0 < q_len; r0 += kF32InnerB) {
+        __syncthreads();
+        for (int e = t; e < kF32InnerB * D; e += kF32Rows) {
+            const int r = e / D, d = e % D;
+            const bool in = r0 + r < q_len;
+            const size_t rq = (size_t(q0) + size_t(in ? r0 + r : 0)) * p.H + h;
+            sQ[r][d] = in ? Q[rq * D + d] : 0.f;
+            sdO[r][d] = in ? dO[rq * D + d] : 0.f;
+        }
+        if (t < kF32InnerB) {
+            const bool in = r0 + t < q_len;
+            const size_t rq = (size_t(q0) + size_t(in ? r0 + t : 0)) * p.H + h;
+            sL[t] = (in && softmax) ? p.lse[rq] : 0.f;
+            sDel[t] = (in && softmax) ? p.delta[rq] : 0.f;
+        }
+        __syncthreads();
+        for (int i = 0; i < kF32InnerB; ++i) {
+            const int row = r0 + i;
+            const bool ok = kvalid && row < q_len && (!p.causal || j <= row + diag);
+            float ds = 0.f;
+            if (ok) {
+                float acc = 0.f, dp = 0.f;
+#pragma unroll
+                for (int d = 0; d < D; ++d) {
+                    acc = fmaf(sQ[i][d], k[d], acc);
+                    dp = fmaf(sdO[i][d], v[d], dp);
+                }
+                float x = acc * p.scale;
+                if (p.bias) x += sB[bucket_f32(row + diag - j)];
+                float pij;
+                if (softmax) {
+                    pij = expf(x - sL[i]);
+                    ds = pij * (dp - sDel[i]);
+                } else {
+                    pij = act_f32(p.mode, x);
+                    ds = act_grad_f32(p.mode, x) * dp;
+                }
+#pragma unroll
+                for (int d = 0; d < D; ++d) {
+                    dv[d] = fmaf(pij, sdO[i][d], dv[d]);
+                    dk[d] = fmaf(ds, sQ[i][d], dk[d]);
+                }
+            }
+            sDS[i][t] = ds;
+        }
+        __syncthreads();
+        // dQ rows of this chunk: sum over the CTA's keys (K rows re-read through the
+        // cache), then one atomic per element
+        for (int e = t; e < kF32InnerB * D; e += kF32Rows) {
+            const int i = e / D, d = e % D;
+            if (r0 + i >= q_len) continue;
+            float acc = 0.f;
+            for (int jj = 0; jj < n_keys; ++jj)
+                acc = fmaf(sDS[i][jj], __ldg(K + ((size_t(k0) + size_t(nt * kBwdBN + jj)) * p.H + h) * D + d), acc);
+            const size_t rq = (size_t(q0) + size_t(r0 + i)) * p.H + h;
+            atomicAdd(p.dq_acc + rq * D + d, acc);
+        }
+    }
+    if (!kvalid) return;
+    float* dK = static_cast<float*>(p.dK) + rk * D;
+    float* dV = static_cast<float*>(p.dV) + rk * D;
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+        dK[d] = dk[d] * p.scale;
+        dV[d] = dv[d];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_f32(int D, const void* Q, const void* K, const void* V, const FwdParams& p, int64_t n_items,
+                           cudaStream_t st) {
+    if (n_items <= 0) return cudaSuccess;
+    const unsigned g = unsigned(n_items);
+    if (D == 32)
+        jfa_fwd_f32_kernel<32><<<g, kF32Rows, 0, st>>>(static_cast<const float*>(Q), static_cast<const float*>(K),
+                                                       static_cast<const float*>(V), p);
+    else if (D == 64)
+        jfa_fwd_f32_kernel<64><<<g, kF32Rows, 0, st>>>(static_cast<const float*>(Q), static_cast<const float*>(K),
+                                                       static_cast<const float*>(V), p);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_f32(int D, const void* Q, const void* K, const void* V, const void* dO, const BwdParams& p,
+                           int64_t n_items, cudaStream_t st) {
+    if (n_items <= 0) return cudaSuccess;
+    const unsigned g = unsigned(n_items);
+    if (D == 32)
+        jfa_bwd_f32_kernel<32><<<g, kF32Rows, 0, st>>>(static_cast<const float*>(Q), static_cast<const float*>(K),
+                                                       static_cast<const float*>(V), static_cast<const float*>(dO), p);
+    else if (D == 64)
+        jfa_bwd_f32_kernel<64><<<g, kF32Rows, 0, st>>>(static_cast<const float*>(Q), static_cast<const float*>(K),
+                                                       static_cast<const float*>(V), static_cast<const float*>(dO), p);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace jfa

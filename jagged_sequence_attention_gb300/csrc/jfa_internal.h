@@ -1,0 +1,116 @@
+// Internal declarations shared by the C-ABI layer, the planner and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+#include <vector>
+
+#include "jfa.h"
+
+namespace jfa {
+
+// Forward tiles: 128 query rows x 128 key rows.  Backward tiles: 128 key rows
+// (resident) x 64 query rows (streamed).
+constexpr int kFwdBM = 128;
+constexpr int kFwdBN = 128;
+constexpr int kBwdBN = 128;
+constexpr int kBwdBM = 64;
+
+// One unit of persistent-grid work: sequence, head, tile index (query tile for the
+// forward, key/value tile for the backward) and the number of inner tiles visited.
+struct WorkItem {
+    int32_t b, h, tile, n_inner;
+};
+static_assert(sizeof(WorkItem) == 16, "WorkItem must match int4");
+
+// Status bits the kernels OR into the plan's device status word.
+enum : int { kStatusTimeout = 1, kStatusBounds = 2 };
+
+struct FwdParams {
+    const int4* items;
+    const int32_t* cta_off;
+    const int32_t* q_off;
+    const int32_t* kv_off;
+    int H;
+    int mode;       // jfa_mode
+    int causal;
+    float scale;        // multiplies <q,k>
+    float scale_log2;   // scale * log2(e)
+    const float* bias;  // [H,32] fp32 or nullptr
+    void* O;
+    float* lse;         // [T_q,H] or nullptr (GDPA)
+    int* status;
+};
+
+struct BwdParams {
+    const int4* items;
+    const int32_t* cta_off;
+    const int32_t* q_off;
+    const int32_t* kv_off;
+    int H;
+    int mode;
+    int causal;
+    float scale;
+    float scale_log2;
+    const float* bias;
+    const float* lse;    // [T_q,H] (softmax)
+    const float* delta;  // [T_q,H] rowsum(dO*O) (softmax)
+    float* dq_acc;       // [T_q,H,D] fp32, zeroed by the preprocess kernel
+    void* dK;
+    void* dV;
+    int* status;
+};
+
+// Host planner (plan.cpp).  Returns JFA_OK or an error for bad offsets.
+jfa_status validate_offsets(const int32_t* q_off, const int32_t* kv_off, int32_t B);
+int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
+                    int32_t causal, int32_t pass);
+void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
+                    int32_t causal, int32_t pass, int32_t n_ctas, WorkItem* items,
+                    int32_t* cta_off, int64_t* cta_cost);
+
+// Kernel launchers (fwd.cu, bwd.cu).  Return cudaSuccess or the launch error.
+cudaError_t launch_fwd(int dtype, int o_dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                       const CUtensorMap& tmV, const FwdParams& p, int grid, cudaStream_t st);
+cudaError_t launch_bwd_pre(int dtype, int o_dtype, int D, const void* O, const void* dO, float* delta,
+                           float* dq_acc, int64_t Tq, int H, int mode, cudaStream_t st);
+cudaError_t launch_bwd_main(int dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdParams& p,
+                            int grid, cudaStream_t st);
+cudaError_t launch_bwd_post(int dtype, int D, const float* dq_acc, void* dQ, int64_t Tq, int H,
+                            float scale, cudaStream_t st);
+
+// fp32 element type: CUDA-core kernels, one CTA per work item (f32.cu).
+cudaError_t launch_fwd_f32(int D, const void* Q, const void* K, const void* V, const FwdParams& p, int64_t n_items,
+                           cudaStream_t st);
+cudaError_t launch_bwd_f32(int D, const void* Q, const void* K, const void* V, const void* dO, const BwdParams& p,
+                           int64_t n_items, cudaStream_t st);
+
+bool supported(int dtype, int D);
+
+}  // namespace jfa
+
+struct jfa_plan_t {
+    int32_t B, H, D, mode, causal;
+    int64_t Tq, Tkv;
+    int device, num_sms;
+    std::vector<int32_t> q_off, kv_off;   // host copies
+    // one device allocation holding everything below
+    void* dev_block;
+    int32_t* d_q_off;
+    int32_t* d_kv_off;
+    int* d_status;
+    int4* d_fwd_items;
+    int32_t* d_fwd_cta_off;
+    int4* d_bwd_items;
+    int32_t* d_bwd_cta_off;
+    int64_t n_fwd_items, n_bwd_items;
+    int fwd_grid, bwd_grid;
+    // optional per-kernel timing (jfa_plan_set_timing)
+    bool timing;
+    std::vector<cudaEvent_t> ev_pool;                 // reusable events
+    std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> ev_pending;  // kind, (start, stop)
+};

@@ -1,0 +1,136 @@
+// Host planner: turns jagged offsets into LPT-balanced work lists for the
+// persistent kernels.
+//
+// Once padding is gone, the GEM articles note that tile scheduling and load balance
+// become the bottleneck (vibekk.com GEM article, section 第一轮瓶颈迁移: short sequences
+// finish early, long ones keep computing; aihot.vn article, "Jagged Sequence Flash
+// Attention": padding-free kernels otherwise leave SMs idle).  Each (sequence, head,
+// tile) is costed by the score tiles it visits and placed, longest first, on the
+// CTA with the least accumulated cost (Graham's LPT rule), so every CTA of the
+// persistent grid ends within one item of the others.
+#include <algorithm>
+#include <cstring>
+#include <numeric>
+#include <queue>
+#include <utility>
+#include <vector>
+
+#include "jfa_internal.h"
+
+namespace jfa {
+
+jfa_status validate_offsets(const int32_t* q_off, const int32_t* kv_off, int32_t B) {
+    if (B < 0 || !q_off || !kv_off) return JFA_ERR_INVALID_ARG;
+    if (q_off[0] != 0 || kv_off[0] != 0) return JFA_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < B; ++b) {
+        if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return JFA_ERR_INVALID_ARG;
+    }
+    return JFA_OK;
+}
+
+namespace {
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Inner tiles visited by an outer tile; see the comments in build_items.
+inline int64_t fwd_inner(int64_t q_len, int64_t kv_len, int64_t mt, int causal) {
+    int64_t n = ceil_div(kv_len, kFwdBN);
+    if (causal) {
+        const int64_t last_row = std::min(q_len, (mt + 1) * kFwdBM) - 1;
+        const int64_t max_col = last_row + (kv_len - q_len);
+        n = max_col < 0 ? 0 : std::min(n, max_col / kFwdBN + 1);
+    }
+    return n;
+}
+
+inline int64_t bwd_inner(int64_t q_len, int64_t kv_len, int64_t nt, int causal) {
+    const int64_t nq = ceil_div(q_len, kBwdBM);
+    if (!causal) return nq;
+    // Row i sees the tile iff its first column nt*BN <= i + (kv_len - q_len).
+    const int64_t first_row = std::max<int64_t>(0, nt * kBwdBN - (kv_len - q_len));
+    if (first_row >= q_len) return 0;
+    return nq - first_row / kBwdBM;
+}
+
+struct Costed {
+    WorkItem w;
+    int64_t cost;
+};
+
+void build_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
+                 int32_t causal, int32_t pass, std::vector<Costed>* out) {
+    for (int32_t b = 0; b < B; ++b) {
+        const int64_t q_len = q_off[b + 1] - q_off[b];
+        const int64_t kv_len = kv_off[b + 1] - kv_off[b];
+        if (pass == 0) {
+            // Forward: one item per query tile; it visits key tiles from 0 up to the
+            // causal diagonal of its last row (or all of them).
+            const int64_t nt = ceil_div(q_len, kFwdBM);
+            for (int32_t h = 0; h < H; ++h)
+                for (int64_t t = 0; t < nt; ++t) {
+                    const int64_t n = fwd_inner(q_len, kv_len, t, causal);
+                    out->push_back({{b, h, int32_t(t), int32_t(n)}, 2 * n + 1});
+                }
+        } else {
+            // Backward: one item per key tile (also when it sees no query, so that
+            // its dK/dV rows are written); it visits the last n query tiles.
+            const int64_t nt = ceil_div(kv_len, kBwdBN);
+            for (int32_t h = 0; h < H; ++h)
+                for (int64_t t = 0; t < nt; ++t) {
+                    const int64_t n = bwd_inner(q_len, kv_len, t, causal);
+                    out->push_back({{b, h, int32_t(t), int32_t(n)}, 5 * n / 2 + 2});
+                }
+        }
+    }
+}
+
+}  // namespace
+
+int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
+                    int32_t causal, int32_t pass) {
+    (void)causal;
+    int64_t n = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        const int64_t len = pass == 0 ? q_off[b + 1] - q_off[b] : kv_off[b + 1] - kv_off[b];
+        n += ceil_div(len, pass == 0 ? kFwdBM : kBwdBN) * H;
+    }
+    return n;
+}
+
+void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
+                    int32_t causal, int32_t pass, int32_t n_ctas, WorkItem* items,
+                    int32_t* cta_off, int64_t* cta_cost) {
+    std::vector<Costed> all;
+    all.reserve(size_t(count_items(q_off, kv_off, B, H, causal, pass)));
+    build_items(q_off, kv_off, B, H, causal, pass, &all);
+
+    // Longest first; equal costs in (sequence, head, tile) order so the plan is
+    // deterministic.
+    std::stable_sort(all.begin(), all.end(),
+                     [](const Costed& a, const Costed& b) { return a.cost > b.cost; });
+
+    // Greedy: each item goes to the currently least-loaded CTA (ties: lowest index).
+    using Slot = std::pair<int64_t, int32_t>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int32_t c = 0; c < n_ctas; ++c) heap.push({0, c});
+    std::vector<int32_t> owner(all.size());
+    std::vector<int64_t> load(size_t(n_ctas), 0);
+    std::vector<int32_t> count(size_t(n_ctas), 0);
+    for (size_t i = 0; i < all.size(); ++i) {
+        Slot s = heap.top();
+        heap.pop();
+        owner[i] = s.second;
+        s.first += all[i].cost;
+        load[size_t(s.second)] = s.first;
+        count[size_t(s.second)]++;
+        heap.push(s);
+    }
+    cta_off[0] = 0;
+    for (int32_t c = 0; c < n_ctas; ++c) cta_off[c + 1] = cta_off[c] + count[size_t(c)];
+    std::vector<int32_t> cursor(cta_off, cta_off + n_ctas);
+    for (size_t i = 0; i < all.size(); ++i) items[cursor[size_t(owner[i])]++] = all[i].w;
+    if (cta_cost)
+        for (int32_t c = 0; c < n_ctas; ++c) cta_cost[c] = load[size_t(c)];
+}
+
+}  // namespace jfa

@@ -1,0 +1,262 @@
+"""Thin Python binding of libjfa (include/jfa.h), same entry-point names.
+
+Argument marshalling only: torch tensors are passed as raw device pointers with
+the current CUDA stream; every step of the computation runs in the library's
+kernels.  The library must have been built (``__graft_entry__.build()`` or
+``python -m jagged_sequence_attention_gb300._build``); if it is missing or fails to
+load, every call raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libjfa.so")
+
+JFA_OK, JFA_ERR_INVALID_ARG, JFA_ERR_UNSUPPORTED, JFA_ERR_CUDA = 0, 1, 2, 3
+JFA_ERR_TIMEOUT, JFA_ERR_DEVICE_BOUNDS, JFA_ERR_PLAN_MISMATCH, JFA_ERR_NO_DEVICE = 4, 5, 6, 7
+JFA_SOFTMAX, JFA_GDPA_GELU_TANH, JFA_GDPA_SILU = 0, 1, 2
+JFA_BF16, JFA_F32 = 0, 1
+JFA_BIAS_NONE, JFA_BIAS_RELPOS32 = 0, 1
+
+MODES = {"softmax": JFA_SOFTMAX, "gelu_tanh": JFA_GDPA_GELU_TANH, "silu": JFA_GDPA_SILU}
+DTYPES = {torch.bfloat16: JFA_BF16, torch.float32: JFA_F32}
+
+EXPORTED = ["jfa_plan_create", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd_workspace_size",
+            "jfa_bwd", "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build",
+            "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times"]
+
+
+class JFAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {jfa_status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib():
+    """Load libjfa.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libjfa.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        P = ctypes.POINTER
+        L.jfa_plan_create.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, P(vp)]
+        L.jfa_plan_destroy.argtypes = [vp]
+        L.jfa_plan_info.argtypes = [vp, P(i64), i32]
+        L.jfa_fwd.argtypes = [vp, i32, vp, vp, vp, i32, vp, f32, vp, i32, vp, vp]
+        L.jfa_bwd_workspace_size.argtypes = [vp, i32]
+        L.jfa_bwd_workspace_size.restype = sz
+        L.jfa_bwd.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
+        L.jfa_plan_device_status.argtypes = [vp, vp]
+        L.jfa_worklist_size.argtypes = [vp, vp, i32, i32, i32, i32, P(i64)]
+        L.jfa_worklist_build.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+        L.jfa_plan_set_timing.argtypes = [vp, i32]
+        L.jfa_plan_kernel_times.argtypes = [vp, vp, vp]
+        L.jfa_status_string.argtypes = [i32]
+        L.jfa_status_string.restype = ctypes.c_char_p
+        for name in ("jfa_plan_create", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
+                     "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build", "jfa_plan_set_timing",
+                     "jfa_plan_kernel_times"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def jfa_status_string(status: int) -> str:
+    return lib().jfa_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != JFA_OK:
+        raise JFAError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+class Plan:
+    """Owns a jfa_plan handle."""
+
+    def __init__(self, handle, B, H, D, mode, causal, Tq, Tkv):
+        self.handle = handle
+        self.B, self.H, self.D, self.mode, self.causal = B, H, D, mode, causal
+        self.Tq, self.Tkv = Tq, Tkv
+
+    def info(self) -> dict:
+        return jfa_plan_info(self)
+
+    def __del__(self):
+        try:
+            if self.handle is not None and _lib is not None:
+                _lib.jfa_plan_destroy(self.handle)
+        finally:
+            self.handle = None
+
+
+def jfa_plan_create(q_offsets, kv_offsets, H: int, D: int, mode="softmax", causal=False, stream=None) -> Plan:
+    """Offsets: host int32 arrays (or CUDA int32 tensors, copied with a sync)."""
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    on_dev = isinstance(q_offsets, torch.Tensor) and q_offsets.is_cuda
+    if on_dev:
+        qo = q_offsets.to(torch.int32).contiguous()
+        ko = kv_offsets.to(torch.int32).contiguous()
+        qp, kp, B = _ptr(qo), _ptr(ko), qo.numel() - 1
+        Tq, Tkv = None, None
+    else:
+        qo = _i32(q_offsets.cpu() if isinstance(q_offsets, torch.Tensor) else q_offsets)
+        ko = _i32(kv_offsets.cpu() if isinstance(kv_offsets, torch.Tensor) else kv_offsets)
+        qp, kp, B = qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p), qo.size - 1
+        Tq, Tkv = int(qo[-1]), int(ko[-1])
+    if (qo.numel() if on_dev else qo.size) != (ko.numel() if on_dev else ko.size):
+        raise JFAError("jfa_plan_create", JFA_ERR_INVALID_ARG)
+    h = ctypes.c_void_p()
+    _check("jfa_plan_create", lib().jfa_plan_create(qp, kp, int(B), int(H), int(D), m, int(bool(causal)),
+                                                     int(on_dev), _stream(stream), ctypes.byref(h)))
+    plan = Plan(h, int(B), int(H), int(D), m, bool(causal), Tq, Tkv)
+    if Tq is None:
+        inf = jfa_plan_info(plan)
+        plan.Tq, plan.Tkv = inf["T_q"], inf["T_kv"]
+    return plan
+
+
+def jfa_plan_destroy(plan: Plan):
+    if plan.handle is not None:
+        _check("jfa_plan_destroy", lib().jfa_plan_destroy(plan.handle))
+        plan.handle = None
+
+
+INFO_KEYS = ["T_q", "T_kv", "B", "H", "D", "mode", "causal", "fwd_items", "fwd_grid", "bwd_items", "bwd_grid",
+             "num_sms"]
+
+
+def jfa_plan_info(plan: Plan) -> dict:
+    buf = (ctypes.c_int64 * len(INFO_KEYS))()
+    _check("jfa_plan_info", lib().jfa_plan_info(plan.handle, buf, len(INFO_KEYS)))
+    return dict(zip(INFO_KEYS, [int(x) for x in buf]))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in DTYPES:
+        raise JFAError("dtype", JFA_ERR_UNSUPPORTED)
+    return DTYPES[t.dtype]
+
+
+def _bias_args(bias):
+    if bias is None:
+        return JFA_BIAS_NONE, None
+    return JFA_BIAS_RELPOS32, _ptr(bias)
+
+
+def jfa_fwd(plan: Plan, Q, K, V, bias=None, scale=None, O=None, lse=None, stream=None, out_dtype=None):
+    """Returns (O, lse); lse is None in GDPA modes.  O is written in out_dtype (default:
+    O's dtype if given, else Q's)."""
+    dt = _dtype_code(Q)
+    scale = 1.0 / float(plan.D) ** 0.5 if scale is None else float(scale)
+    if O is None:
+        O = torch.empty(Q.shape, dtype=out_dtype or Q.dtype, device=Q.device)
+    if lse is None and plan.mode == JFA_SOFTMAX:
+        lse = torch.empty((Q.shape[0], plan.H), dtype=torch.float32, device=Q.device)
+    bk, bp = _bias_args(bias)
+    _check("jfa_fwd", lib().jfa_fwd(plan.handle, dt, _ptr(Q), _ptr(K), _ptr(V), bk, bp, scale, _ptr(O),
+                                    _dtype_code(O), _ptr(lse), _stream(stream)))
+    return O, lse
+
+
+def jfa_bwd_workspace_size(plan: Plan, dtype=torch.bfloat16) -> int:
+    return int(lib().jfa_bwd_workspace_size(plan.handle, DTYPES[dtype]))
+
+
+def jfa_bwd(plan: Plan, Q, K, V, O, dO, lse, bias=None, scale=None, dQ=None, dK=None, dV=None, workspace=None,
+            stream=None):
+    """Returns (dQ, dK, dV)."""
+    dt = _dtype_code(Q)
+    scale = 1.0 / float(plan.D) ** 0.5 if scale is None else float(scale)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    need = jfa_bwd_workspace_size(plan, Q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    bk, bp = _bias_args(bias)
+    _check("jfa_bwd", lib().jfa_bwd(plan.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _dtype_code(O), _ptr(dO),
+                                    _ptr(lse), bk, bp, scale, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dQ, dK, dV
+
+
+def jfa_plan_device_status(plan: Plan, stream=None) -> int:
+    return int(lib().jfa_plan_device_status(plan.handle, _stream(stream)))
+
+
+KERNEL_KINDS = ["fwd", "bwd_pre", "bwd_main", "bwd_post"]
+
+
+def jfa_plan_set_timing(plan: Plan, enable: bool = True):
+    _check("jfa_plan_set_timing", lib().jfa_plan_set_timing(plan.handle, int(bool(enable))))
+
+
+def jfa_plan_kernel_times(plan: Plan) -> dict:
+    """{kind: (total_ms, launches)} since the previous query (synchronises)."""
+    ms = (ctypes.c_double * 4)()
+    n = (ctypes.c_int64 * 4)()
+    _check("jfa_plan_kernel_times", lib().jfa_plan_kernel_times(plan.handle, ms, n))
+    return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def jfa_worklist_size(q_offsets, kv_offsets, H: int, causal: bool, pass_: int) -> int:
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    n = ctypes.c_int64()
+    _check("jfa_worklist_size", lib().jfa_worklist_size(qo.ctypes.data_as(ctypes.c_void_p),
+                                                         ko.ctypes.data_as(ctypes.c_void_p), qo.size - 1, int(H),
+                                                         int(bool(causal)), int(pass_), ctypes.byref(n)))
+    return int(n.value)
+
+
+def jfa_worklist_build(q_offsets, kv_offsets, H: int, causal: bool, pass_: int, n_ctas: int):
+    """Host planner.  Returns (items int32 [n,4] (seq, head, tile, inner), cta_offsets [n_ctas+1],
+    cta_cost [n_ctas])."""
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    n = jfa_worklist_size(qo, ko, H, causal, pass_)
+    items = np.zeros((max(n, 1), 4), dtype=np.int32)
+    offs = np.zeros(n_ctas + 1, dtype=np.int32)
+    cost = np.zeros(n_ctas, dtype=np.int64)
+    _check("jfa_worklist_build", lib().jfa_worklist_build(
+        qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p), qo.size - 1, int(H),
+        int(bool(causal)), int(pass_), int(n_ctas), items.ctypes.data_as(ctypes.c_void_p),
+        offs.ctypes.data_as(ctypes.c_void_p), cost.ctypes.data_as(ctypes.c_void_p)))
+    return items[:n], offs, cost
+
+
+# --------------------------------------------------------------------------- convenience
+
+
+def attention(batch, with_backward=True, stream=None, out_dtype=None):
+    """Run forward (and backward) for a workloads.Batch on the GPU: returns dict of tensors."""
+    plan = jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal, stream)
+    O, lse = jfa_fwd(plan, batch.Q, batch.K, batch.V, batch.bias, batch.scale, stream=stream, out_dtype=out_dtype)
+    out = {"O": O, "lse": lse, "plan": plan}
+    if with_backward:
+        dQ, dK, dV = jfa_bwd(plan, batch.Q, batch.K, batch.V, O, batch.dO, lse, batch.bias, batch.scale,
+                             stream=stream)
+        out.update(dQ=dQ, dK=dK, dV=dV)
+    return out

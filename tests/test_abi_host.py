@@ -1,0 +1,163 @@
+"""Host-side checks of libjfa: it builds, loads without a GPU, exports every entry
+point include/jfa.h declares, and its planner (pure host code) produces correct,
+balanced work lists.  No CUDA call is made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from jagged_sequence_attention_gb300 import _build
+from jagged_sequence_attention_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "jfa.h")
+
+BM_FWD, BN_FWD = 128, 128
+BN_BWD, BM_BWD = 128, 64
+
+
+@pytest.fixture(scope="module")
+def jfa():
+    _build.build()
+    from jagged_sequence_attention_gb300 import jfa as m
+    m.lib()
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(jfa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ("jfa_plan_create", "jfa_plan_destroy", "jfa_fwd", "jfa_bwd", "jfa_bwd_workspace_size",
+              "jfa_plan_device_status", "jfa_status_string", "jfa_worklist_size", "jfa_worklist_build",
+              "jfa_plan_info"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(jfa):
+    lib = jfa.lib()
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", jfa._LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (jfa_[a-z_]+)\b", out))
+    assert set(declared_functions()) <= exported
+    assert set(jfa.EXPORTED) <= exported
+
+
+def test_status_strings(jfa):
+    for s in range(8):
+        assert jfa.jfa_status_string(s) and jfa.jfa_status_string(s) != "unknown status"
+    assert jfa.jfa_status_string(99) == "unknown status"
+
+
+def visited_fwd(q_len, kv_len, t, causal):
+    """Brute force: key tiles that hold at least one allowed (row, key) pair for query
+    tile t (bottom-right causal)."""
+    rows = range(t * BM_FWD, min(q_len, (t + 1) * BM_FWD))
+    n = 0
+    for kt in range((kv_len + BN_FWD - 1) // BN_FWD):
+        cols = range(kt * BN_FWD, min(kv_len, (kt + 1) * BN_FWD))
+        if any((not causal) or c <= r + kv_len - q_len for r in rows for c in (cols[0],)):
+            n = kt + 1
+    return n
+
+
+def visited_bwd(q_len, kv_len, t, causal):
+    """Brute force: query tiles (64 rows) with at least one allowed pair for key tile t."""
+    cols = range(t * BN_BWD, min(kv_len, (t + 1) * BN_BWD))
+    tiles = set()
+    for r in range(q_len):
+        if (not causal) or cols[0] <= r + kv_len - q_len:
+            tiles.add(r // BM_BWD)
+    if not tiles:
+        return 0, None
+    # the kernel visits a contiguous range ending at the last query tile
+    assert max(tiles) == (q_len - 1) // BM_BWD
+    assert tiles == set(range(min(tiles), max(tiles) + 1))
+    return len(tiles), min(tiles)
+
+
+CASES = [
+    ([0, 1, 127, 128, 129, 300, 5], [4, 1, 127, 128, 129, 300, 0]),
+    ([3, 200, 64, 1], [700, 130, 1, 257]),
+    ([1000, 1, 513], [1000, 1, 513]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("pass_", [0, 1])
+@pytest.mark.parametrize("n_ctas", [1, 3, 148])
+def test_worklist_covers_every_tile_once(jfa, case, causal, pass_, n_ctas):
+    q, kv = CASES[case]
+    H = 3
+    qo, ko = wl.offsets(q), wl.offsets(kv)
+    items, offs, cost = jfa.jfa_worklist_build(qo, ko, H, causal, pass_, n_ctas)
+    assert offs[0] == 0 and offs[-1] == len(items) and np.all(np.diff(offs) >= 0)
+    expect = {}
+    for b in range(len(q)):
+        L = q[b] if pass_ == 0 else kv[b]
+        T = BM_FWD if pass_ == 0 else BN_BWD
+        for h in range(H):
+            for t in range((L + T - 1) // T):
+                if pass_ == 0:
+                    expect[(b, h, t)] = visited_fwd(q[b], kv[b], t, causal)
+                else:
+                    n, first = visited_bwd(q[b], kv[b], t, causal)
+                    expect[(b, h, t)] = n
+                    if n:
+                        assert first == (q[b] + BM_BWD - 1) // BM_BWD - n
+    got = {(int(i[0]), int(i[1]), int(i[2])): int(i[3]) for i in items}
+    assert len(got) == len(items), "duplicate work items"
+    assert got == expect
+
+
+def test_worklist_is_lpt_balanced(jfa):
+    w = wl.WORKLOADS["causal_bias"]
+    q, kv = wl.lengths(w)
+    qo, ko = wl.offsets(q), wl.offsets(kv)
+    for pass_ in (0, 1):
+        items, offs, cost = jfa.jfa_worklist_build(qo, ko, 8, True, pass_, 148)
+        c = (2 * items[:, 3] + 1) if pass_ == 0 else (5 * items[:, 3] // 2 + 2)
+        # per-CTA cost matches the items assigned to it, items in non-increasing cost
+        for k in range(148):
+            seg = c[offs[k]:offs[k + 1]]
+            assert seg.sum() == cost[k]
+            assert np.all(np.diff(seg) <= 0)
+        # greedy LPT bound: no CTA exceeds the least loaded one by more than the largest item
+        assert cost.max() - cost.min() <= c.max()
+        assert cost.sum() == c.sum()
+
+
+def test_worklist_rejects_bad_offsets(jfa):
+    with pytest.raises(jfa.JFAError) as e:
+        jfa.jfa_worklist_build([0, 5, 3], [0, 1, 2], 2, False, 0, 4)
+    assert e.value.status == jfa.JFA_ERR_INVALID_ARG
+    with pytest.raises(jfa.JFAError):
+        jfa.jfa_worklist_build([1, 5], [0, 1], 2, False, 0, 4)
+    with pytest.raises(jfa.JFAError):
+        jfa.jfa_worklist_size([0, 5], [0, 1], 0, False, 0)
+
+
+def test_empty_batches(jfa):
+    items, offs, cost = jfa.jfa_worklist_build([0], [0], 4, True, 0, 8)
+    assert len(items) == 0 and np.all(offs == 0) and np.all(cost == 0)
+    items, offs, cost = jfa.jfa_worklist_build([0, 0, 0], [0, 5, 5], 2, True, 1, 8)
+    # the key tile still gets an item (with 0 query tiles) so its gradients are written
+    assert len(items) == 2 and np.all(items[:, 3] == 0)
+
+
+def test_worklist_is_deterministic(jfa):
+    q, kv = wl.lengths(wl.WORKLOADS["cross"])
+    qo, ko = wl.offsets(q), wl.offsets(kv)
+    a = jfa.jfa_worklist_build(qo, ko, 8, False, 0, 148)
+    b = jfa.jfa_worklist_build(qo, ko, 8, False, 0, 148)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)

@@ -1,0 +1,164 @@
+"""Parity of the CUDA path (through the C-ABI) against the CPU oracle.
+
+Small cases are compared element by element over every output; the full-size
+workloads run exactly as the benchmark launches them and are compared on sampled
+outputs that the oracle computes exactly through suffix sub-problems (see
+``parity.suffix_problem``).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from jagged_sequence_attention_gb300 import workloads as wl
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from jagged_sequence_attention_gb300 import _build
+    _build.build()
+
+
+def check_full(batch, with_backward=True, out_dtype=torch.float32):
+    g = parity.run_gpu(batch, with_backward, out_dtype=out_dtype)
+    assert g["status"] == 0, g["status"]
+    r = parity.run_oracle(batch, with_backward)
+    m = parity.compare(g, r, softmax=batch.mode == "softmax", with_backward=with_backward)
+    print(batch.name, m)
+    parity.assert_within(m, softmax=batch.mode == "softmax")
+    return g, r
+
+
+def test_tiny_workload_full():
+    check_full(wl.make("tiny", device="cuda"))
+
+
+def pick_sequences(batch, k_random=4, seed=0):
+    lens = batch.q_lens * batch.kv_lens + batch.q_lens
+    order = np.argsort(lens)
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(order[2:-2], size=min(k_random, max(0, len(order) - 4)), replace=False)
+    return sorted(set(order[:2].tolist() + order[-2:].tolist() + mid.tolist()))
+
+
+@pytest.mark.parametrize("name", ["causal_bias", "cross", "gdpa_gelu", "gdpa_silu"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_workload_slice_full(name, out):
+    full = wl.make(name, device="cuda")
+    check_full(wl.subset(full, pick_sequences(full)), out_dtype=torch.float32 if out == "f32" else torch.bfloat16)
+
+
+def test_long_causal_scaled_down_full():
+    """The long-sequence workload's structure (causal, bias, 8 heads, head_dim 128) at
+    lengths the oracle finishes in seconds, spanning many tiles with ragged tails."""
+    rng = np.random.default_rng(5)
+    lens = rng.integers(200, 1500, size=6)
+    check_full(wl.make_custom(lens, lens, H=8, D=128, causal=True, bias=True, device="cuda", seed=77))
+
+
+@pytest.mark.parametrize("mode", ["softmax", "gelu_tanh", "silu"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("bias", [False, True])
+def test_edge_lengths(mode, causal, bias):
+    # empty sequences, single tokens, tile boundaries +-1, q > kv and q < kv, a kv tail
+    # inside a tile, and the last sequence ending at the end of the buffers
+    q = [0, 1, 127, 128, 129, 3, 0, 5, 1, 200, 64]
+    kv = [4, 1, 127, 128, 129, 0, 0, 300, 257, 130, 1]
+    std = 1.0 if mode == "softmax" else 0.5
+    check_full(wl.make_custom(q, kv, H=2, D=128, mode=mode, causal=causal, bias=bias, value_std=std,
+                              device="cuda", seed=11))
+
+
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 64), (torch.float32, 32), (torch.float32, 64)])
+def test_other_head_dims(dtype, D):
+    check_full(wl.make_custom([7, 130, 64, 1], [200, 5, 64, 129], H=3, D=D, dtype=dtype, causal=True, bias=True,
+                              device="cuda", seed=12))
+
+
+def test_guard_bands_untouched():
+    """Rows past the last offset of every output buffer keep their canary values."""
+    from jagged_sequence_attention_gb300 import jfa
+    b = wl.make_custom([5, 130, 77], [129, 3, 200], H=2, D=128, causal=True, bias=True, device="cuda", seed=13)
+    Tq, Tkv, pad = int(b.q_off[-1]), int(b.kv_off[-1]), 37
+    canary = 1234.5
+
+    def buf(T, like):
+        t = torch.full((T + pad, b.H, b.D), canary, dtype=like.dtype, device="cuda")
+        return t
+
+    O, dQ, dK, dV = buf(Tq, b.Q), buf(Tq, b.Q), buf(Tkv, b.K), buf(Tkv, b.K)
+    O = O.float()
+    lse = torch.full((Tq + pad, b.H), canary, dtype=torch.float32, device="cuda")
+    plan = jfa.jfa_plan_create(b.q_off, b.kv_off, b.H, b.D, b.mode, b.causal)
+    jfa.jfa_fwd(plan, b.Q, b.K, b.V, b.bias, b.scale, O=O, lse=lse)
+    jfa.jfa_bwd(plan, b.Q, b.K, b.V, O, b.dO, lse, b.bias, b.scale, dQ=dQ, dK=dK, dV=dV)
+    torch.cuda.synchronize()
+    assert jfa.jfa_plan_device_status(plan) == 0
+    for t, T in ((O, Tq), (dQ, Tq), (dK, Tkv), (dV, Tkv), (lse, Tq)):
+        assert torch.all(t[T:] == canary)
+        assert not torch.any(t[:T] == canary)
+    r = parity.run_oracle(b)
+    m = parity.compare({"O": O[:Tq], "lse": lse[:Tq], "dQ": dQ[:Tq], "dK": dK[:Tkv], "dV": dV[:Tkv]}, r)
+    parity.assert_within(m)
+
+
+def test_no_key_rows_are_exact_zero():
+    b = wl.make_custom([3, 6], [0, 2], H=2, D=128, causal=True, device="cuda", seed=14)
+    g = parity.run_gpu(b)
+    O = g["O"].float().cpu()
+    assert torch.all(O[0:3] == 0) and torch.all(torch.isneginf(g["lse"][0:3].cpu()))
+    # second sequence: q=6 > kv=2, rows 0..3 see no key
+    assert torch.all(O[3:7] == 0) and torch.all(g["dQ"][3:7].float().cpu() == 0)
+
+
+# ----------------------------------------------------------------------------- full size
+
+SAMPLES = {
+    # (sequence selector, head, rows kept from the end)
+    "causal_bias": [("longest", 0, 300), ("shortest", 3, 10**9), ("median", 7, 10**9)],
+    "cross": [("longest_kv", 1, 10**9), ("shortest", 5, 10**9), ("median", 2, 10**9)],
+    "gdpa_gelu": [("longest_kv", 0, 10**9), ("longest_q", 3, 10**9), ("median", 2, 10**9)],
+    "gdpa_silu": [("longest_kv", 1, 10**9), ("longest_q", 2, 10**9)],
+    "long_causal": [("longest", 0, 128), ("longest", 5, 128), ("shortest", 3, 200), ("median", 6, 160)],
+}
+
+
+def select(batch, how):
+    ql, kl = batch.q_lens, batch.kv_lens
+    if how == "longest":
+        return int(np.argmax(ql))
+    if how == "longest_kv":
+        return int(np.argmax(kl))
+    if how == "longest_q":
+        return int(np.argmax(ql * 100000 + kl))
+    if how == "shortest":
+        return int(np.argmin(ql * 100000 + kl))
+    if how == "median":
+        return int(np.argsort(ql * 100000 + kl)[len(ql) // 2])
+    raise ValueError(how)
+
+
+@pytest.mark.parametrize("name", ["causal_bias", "cross", "gdpa_gelu", "gdpa_silu", "long_causal"])
+def test_full_size_workload_sampled(name):
+    batch = wl.make(name, device="cuda")
+    # the launch configuration the benchmark times: O written in the input type
+    g = parity.run_gpu(batch, out_dtype=torch.bfloat16)
+    assert g["status"] == 0
+    samples = []
+    for how, h, keep in SAMPLES[name]:
+        b = select(batch, how)
+        q_len = int(batch.q_lens[b])
+        samples.append((b, h, max(0, q_len - keep)))
+    m = parity.sampled_parity(batch, g, samples)
+    print(name, samples, m)
+    parity.assert_within(m, softmax=batch.mode == "softmax")
+    # whole-output sanity at full size: finite everywhere
+    for k in ("O", "dQ", "dK", "dV"):
+        assert torch.isfinite(g[k]).all(), k
