@@ -24,6 +24,7 @@
 // dQ^T [448,512).
 #include "jfa_internal.h"
 #include "ptx.cuh"
+#include "tilemath.cuh"
 
 #include <algorithm>
 
@@ -106,31 +107,6 @@ enum {
     C_ACC_EMPTY = 19,
     C_DRAIN = 20,
 };
-
-__device__ __forceinline__ int relpos_bucket_b(int r) {
-    r = r < 0 ? -r : r;
-    if (r >= 46340) return 31;
-    const uint32_t v = uint32_t(r + 1) * uint32_t(r + 1);
-    return 31 - __clz(v);
-}
-
-// GDPA activation and its derivative (tanh-form GELU, SiLU).
-__device__ __forceinline__ void act_and_grad(bool gelu, float x, float& a, float& da) {
-    if (gelu) {
-        const float k0 = 0.7978845608028654f, k1 = 0.035677408136300125f;
-        const float x2 = x * x;
-        const float t = tanh_approx(x * fmaf(k1, x2, k0));
-        const float hx = 0.5f * x;
-        a = fmaf(hx, t, hx);
-        // d/dx: 0.5(1+t) + 0.5 x (1-t^2) (k0 + 3 k1 x^2)
-        da = fmaf(hx * fmaf(-t, t, 1.f), fmaf(3.f * k1, x2, k0), fmaf(0.5f, t, 0.5f));
-    } else {
-        const float hx = 0.5f * x;
-        const float sg = fmaf(0.5f, tanh_approx(hx), 0.5f);  // sigmoid(x)
-        a = x * sg;
-        da = sg * fmaf(x, 1.f - sg, 1.f);
-    }
-}
 
 template <typename T>
 __device__ __forceinline__ void store_vec(T* dst, const float* v, int n, float mul);
@@ -390,64 +366,87 @@ __global__ void __launch_bounds__(320, 1)
             const int first_qt = (q_len + C::BM - 1) / C::BM - n;
             const int j = nt * C::BN + r;  // key row within the sequence
             const bool key_valid = j < kv_len;
-            if (p.bias) {
-                bias_w[lane] = p.bias[h * 32 + lane] * (softmax ? 1.4426950408889634f : 1.0f);
-            }
-            for (int i = 0; i < n; ++i) {
-                const uint32_t g = step_it + i, sb = g & 1, ph = (g >> 1) & 1;
-                const int qrow0 = (first_qt + i) * C::BM;  // first query row of the step
-                // per-warp copies of the step's row terms (guarded at the sequence end)
+            if (p.bias) bias_w[lane] = p.bias[h * 32 + lane] * (softmax ? 1.4426950408889634f : 1.0f);
+            // Row terms (lse in log2 units, Delta) of the step's 64 query rows: each lane
+            // holds two, loaded one step ahead so the load latency hides behind a step.
+            float nl[2] = {0.f, 0.f}, nd[2] = {0.f, 0.f};
+            auto fetch = [&](int qrow0) {
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int c = lane + 32 * k;
-                    const bool v = qrow0 + c < q_len;
-                    const size_t ridx = (size_t(q0) + size_t(qrow0 + c)) * size_t(p.H) + size_t(h);
-                    lse_s[c] = (softmax && v) ? p.lse[ridx] * 1.4426950408889634f : 0.f;
-                    del_s[c] = (softmax && v) ? p.delta[ridx] : 0.f;
+                    const bool v = softmax && qrow0 + c < q_len;
+                    const size_t ridx = (size_t(q0) + size_t(v ? qrow0 + c : 0)) * size_t(p.H) + size_t(h);
+                    nl[k] = v ? p.lse[ridx] * 1.4426950408889634f : 0.f;
+                    nd[k] = v ? p.delta[ridx] : 0.f;
+                }
+            };
+            fetch(first_qt * C::BM);
+            for (int i = 0; i < n; ++i) {
+                const uint32_t g = step_it + i, sb = g & 1, ph = (g >> 1) & 1;
+                const int qrow0 = (first_qt + i) * C::BM;  // first query row of the step
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    lse_s[lane + 32 * k] = nl[k];
+                    del_s[lane + 32 * k] = nd[k];
                 }
                 __syncwarp();
+                if (i + 1 < n) fetch(qrow0 + C::BM);
                 // subtraction scheme: valid query columns are [lo, hi)
                 const int hi = key_valid ? min(C::BM, q_len - qrow0) : 0;
                 const int lo = p.causal ? max(0, j - diag - qrow0) : 0;
+                const bool full = __all_sync(0xffffffffu, lo == 0 && hi == C::BM);
                 const int rbase = qrow0 + diag - j;  // relative position of column 0
+                const float xs = softmax ? p.scale_log2 : p.scale;
+                bool cconst = true;
+                float cbias[C::BM / 32];
+#pragma unroll
+                for (int k = 0; k < C::BM / 32; ++k) {
+                    int bk = 0;
+                    // columns 32k..32k+31 have positions rbase+32k .. rbase+32k+31
+                    if (p.bias) cconst &= chunk_bucket_const(rbase + 32 * k + 31, bk);
+                    cbias[k] = p.bias ? bias_w[bk] : 0.f;
+                }
+                cconst = __all_sync(0xffffffffu, cconst);
 
                 if (!warp_wait(C_S_FULL + sb, ph)) { ok = false; break; }
                 tc_fence_after();
                 float pv[C::BM];
+{
+                    uint32_t rr[C::BM / 32][32];
 #pragma unroll
-                for (int c = 0; c < C::BM / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tmem + lane_base + C::kTmS + sb * 64u + c * 32u, rr);
+                    for (int c = 0; c < C::BM / 32; ++c) tmem_ld32(tmem + lane_base + C::kTmS + sb * 64u + c * 32u, rr[c]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) pv[c * 32 + e] = __uint_as_float(rr[e]);
+                    for (int c = 0; c < C::BM / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) pv[c * 32 + e] = __uint_as_float(rr[c][e]);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C_S_EMPTY + sb));
 
-                // pv: scaled (and biased) scores; then P^T (softmax) -- masked to 0.
+                // pv: scaled (and biased) scores
+                if (cconst) {
 #pragma unroll
-                for (int c = 0; c < C::BM; ++c) {
-                    float x = pv[c] * (softmax ? p.scale_log2 : p.scale);
-                    if (p.bias) x += bias_w[relpos_bucket_b(rbase + c)];
-                    pv[c] = x;
+                    for (int c = 0; c < C::BM; ++c) pv[c] = fmaf(pv[c], xs, cbias[c >> 5]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C::BM; ++c) pv[c] = fmaf(pv[c], xs, bias_w[relpos_bucket(rbase + c)]);
                 }
                 if (!warp_wait(C_PT_EMPTY, (g & 1) ^ 1)) { ok = false; break; }
                 if (softmax) {
 #pragma unroll
                     for (int c = 0; c < C::BM; ++c) {
                         const float e = ex2_approx(pv[c] - lse_s[c]);
-                        pv[c] = (c >= lo && c < hi) ? e : 0.f;
+                        pv[c] = (full || (c >= lo && c < hi)) ? e : 0.f;
                     }
                     write_ptile_row<T>(sPt, r, pv);
                 } else {
                     float pa[C::BM];
 #pragma unroll
                     for (int c = 0; c < C::BM; ++c) {
-                        float a, da;
-                        act_and_grad(gelu, pv[c], a, da);
-                        pa[c] = (c >= lo && c < hi) ? a : 0.f;
+                        const float a = gdpa_act(gelu, pv[c]);
+                        pa[c] = (full || (c >= lo && c < hi)) ? a : 0.f;
                     }
                     write_ptile_row<T>(sPt, r, pa);
                 }
@@ -458,13 +457,15 @@ __global__ void __launch_bounds__(320, 1)
                 if (!warp_wait(C_DP_FULL, g & 1)) { ok = false; break; }
                 tc_fence_after();
                 float dp[C::BM];
+{
+                    uint32_t rr[C::BM / 32][32];
 #pragma unroll
-                for (int c = 0; c < C::BM / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tmem + lane_base + C::kTmDP + c * 32u, rr);
+                    for (int c = 0; c < C::BM / 32; ++c) tmem_ld32(tmem + lane_base + C::kTmDP + c * 32u, rr[c]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) dp[c * 32 + e] = __uint_as_float(rr[e]);
+                    for (int c = 0; c < C::BM / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) dp[c * 32 + e] = __uint_as_float(rr[c][e]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -476,8 +477,8 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                     for (int c = 0; c < C::BM; ++c) {
                         float a, da;
-                        act_and_grad(gelu, pv[c], a, da);
-                        dp[c] = (c >= lo && c < hi) ? da * dp[c] : 0.f;
+                        gdpa_act_grad(gelu, pv[c], a, da);
+                        dp[c] = (full || (c >= lo && c < hi)) ? da * dp[c] : 0.f;
                     }
                 }
                 if (!warp_wait(C_DS_EMPTY, (g & 1) ^ 1)) { ok = false; break; }
@@ -520,13 +521,15 @@ __global__ void __launch_bounds__(320, 1)
                 if (!warp_wait(C_DQ_FULL, g & 1)) { ok = false; break; }
                 tc_fence_after();
                 float acc[C::BM];
+                {
+                    uint32_t rr[C::BM / 32][32];
 #pragma unroll
-                for (int c = 0; c < C::BM / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tmem + lane_base + C::kTmDQ + c * 32u, rr);
+                    for (int c = 0; c < C::BM / 32; ++c) tmem_ld32(tmem + lane_base + C::kTmDQ + c * 32u, rr[c]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) acc[c * 32 + e] = __uint_as_float(rr[e]);
+                    for (int c = 0; c < C::BM / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) acc[c * 32 + e] = __uint_as_float(rr[c][e]);
                 }
                 tc_fence_before();
                 __syncwarp();

@@ -22,6 +22,7 @@
 // MN-major operand.
 #include "jfa_internal.h"
 #include "ptx.cuh"
+#include "tilemath.cuh"
 
 namespace jfa {
 
@@ -59,7 +60,8 @@ struct FwdCfg {
     static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffP = kOffV + kStages * kKVBytes;
-    static constexpr int kOffBar = kOffP + kPBytes;
+    static constexpr int kOffP2 = kOffP + kPBytes;  // GDPA: P - bf16(P), second PV product
+    static constexpr int kOffBar = kOffP2 + kPBytes;
     static constexpr int kNumBars = 20;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kMiscBytes = 16 + 2 * 4 * 32 * 4;  // tmem slot, abort flag, bias tables
@@ -93,29 +95,6 @@ enum {
     B_DRAIN = 17,
 };
 
-__device__ __forceinline__ int relpos_bucket(int r) {
-    // floor(log2((1+r)^2)) capped at 31; (1+r)^2 < 2^31 exactly when r < 46340.
-    r = r < 0 ? -r : r;
-    if (r >= 46340) return 31;
-    const uint32_t v = uint32_t(r + 1) * uint32_t(r + 1);
-    return 31 - __clz(v);
-}
-
-__device__ __forceinline__ float gelu_tanh_f(float x) {
-    // 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
-    const float k0 = 0.7978845608028654f, k1 = 0.035677408136300125f;
-    const float u = x * fmaf(k1, x * x, k0);
-    const float t = tanh_approx(u);
-    const float hx = 0.5f * x;
-    return fmaf(hx, t, hx);
-}
-
-__device__ __forceinline__ float silu_f(float x) {
-    // x * sigmoid(x), sigmoid(x) = (1 + tanh(x/2)) / 2
-    const float hx = 0.5f * x;
-    return fmaf(hx, tanh_approx(hx), hx);
-}
-
 template <typename T>
 __device__ __forceinline__ void store_row(T* dst, const float* v, int n);
 
@@ -148,7 +127,8 @@ __global__ void __launch_bounds__(192, 1)
                                                ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV,
-                   sP = sbase + C::kOffP;
+                   sP = sbase + C::kOffP, sP2 = sbase + C::kOffP2;
+    const bool gdpa = p.mode != JFA_SOFTMAX;
     auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * uint32_t(i); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -266,8 +246,7 @@ __global__ void __launch_bounds__(192, 1)
                             const uint32_t cb = (s * 32) >> 7;     // 128-byte column block
                             const uint64_t a = make_sdesc_sw128(sQ + cb * C::BM * 128 + koff, 16, 1024);
                             const uint64_t bd = make_sdesc_sw128(kbase + cb * C::BN * 128 + koff, 16, 1024);
-                            if constexpr (sizeof(T) == 2) mma_f16_ss(d_tmem, a, bd, C::kIdescQK, s > 0);
-                            else mma_tf32_ss(d_tmem, a, bd, C::kIdescQK, s > 0);
+                            mma_f16_ss(d_tmem, a, bd, C::kIdescQK, s > 0);
                         }
                         tc_commit(bar(B_S_FULL + st));
                         tc_commit(bar(B_K_EMPTY + st));
@@ -287,8 +266,17 @@ __global__ void __launch_bounds__(192, 1)
                             const uint32_t cb = (s * 32) >> 7;
                             const uint64_t a = make_sdesc_sw128(sP + cb * C::BM * 128 + koff, 16, 1024);
                             const uint64_t bd = make_sdesc_sw128(vbase + s * C::kUmmaK * 128, C::BN * 128, 1024);
-                            if constexpr (sizeof(T) == 2) mma_f16_ss(tmem + C::kTmemO, a, bd, C::kIdescPV, (jj > 0 || s > 0));
-                            else mma_tf32_ss(tmem + C::kTmemO, a, bd, C::kIdescPV, (jj > 0 || s > 0));
+                            mma_f16_ss(tmem + C::kTmemO, a, bd, C::kIdescPV, (jj > 0 || s > 0));
+                        }
+                        if (gdpa) {  // O += (P - bf16(P)) V: P to ~16 significant bits
+#pragma unroll
+                            for (int s = 0; s < C::kPVSteps; ++s) {
+                                const uint32_t koff = (s * 32) & 127;
+                                const uint32_t cb = (s * 32) >> 7;
+                                const uint64_t a = make_sdesc_sw128(sP2 + cb * C::BM * 128 + koff, 16, 1024);
+                                const uint64_t bd = make_sdesc_sw128(vbase + s * C::kUmmaK * 128, C::BN * 128, 1024);
+                                mma_f16_ss(tmem + C::kTmemO, a, bd, C::kIdescPV, 1u);
+                            }
                         }
                         tc_commit(bar(B_O_FULL));
                         tc_commit(bar(B_V_EMPTY + st));
@@ -343,13 +331,15 @@ __global__ void __launch_bounds__(192, 1)
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_S_FULL + sb), ph, abort_flag))) { ok = false; break; }
                 tc_fence_after();
                 float x[C::BN];
+                {
+                    uint32_t r[C::BN / 32][32];
 #pragma unroll
-                for (int c = 0; c < C::BN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + sb * 128u + c * 32u, r);
+                    for (int c = 0; c < C::BN / 32; ++c) tmem_ld32(tmem + lane_base + sb * 128u + c * 32u, r[c]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]);
+                    for (int c = 0; c < C::BN / 32; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[c][i]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -359,18 +349,39 @@ __global__ void __launch_bounds__(192, 1)
                 int lim = kv_len - col0;  // subtraction scheme: columns >= lim are masked
                 if (p.causal) lim = min(lim, row + diag + 1 - col0);
                 const int rbase = row + diag - col0;  // relative position of column 0
+                const bool full = __all_sync(0xffffffffu, lim >= C::BN);
+                const float xs = softmax ? p.scale_log2 : p.scale;
+                // x = scale * s + bias: one constant per 32-column chunk when the whole
+                // chunk sits in one bucket (warp-uniform), else per element.
+                bool cconst = true;
+                float cb[C::BN / 32];
+#pragma unroll
+                for (int k = 0; k < C::BN / 32; ++k) {
+                    int bk = 0;
+                    if (p.bias) cconst &= chunk_bucket_const(rbase - 32 * k, bk);
+                    cb[k] = p.bias ? btab[bk] : 0.f;
+                }
+                if (__all_sync(0xffffffffu, cconst)) {
+#pragma unroll
+                    for (int c = 0; c < C::BN; ++c) x[c] = fmaf(x[c], xs, cb[c >> 5]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C::BN; ++c) x[c] = fmaf(x[c], xs, btab[relpos_bucket(rbase - c)]);
+                }
                 bool need_rescale = false;
                 float alpha = 1.f;
                 if (softmax) {
-                    float mx = -INFINITY;
+                    if (!full) {
 #pragma unroll
-                    for (int c = 0; c < C::BN; ++c) {
-                        float v = x[c] * p.scale_log2;
-                        if (p.bias) v += btab[relpos_bucket(rbase - c)];
-                        v = (c < lim) ? v : -INFINITY;
-                        x[c] = v;
-                        mx = fmaxf(mx, v);
+                        for (int c = 0; c < C::BN; ++c) x[c] = (c < lim) ? x[c] : -INFINITY;
                     }
+                    float mx8[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+#pragma unroll
+                    for (int c = 8; c < C::BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+                    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                     // Lazy rescaling: keep the running max unless it grows by more
                     // than 2^8; both O and l use the same stale max, so the final
                     // O / l is unchanged.
@@ -380,21 +391,21 @@ __global__ void __launch_bounds__(192, 1)
                     alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_use);
                     if (m_new != m) need_rescale = (j > 0);
                     m = m_new;
-                    float rs = 0.f;
+                    float rs8[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
 #pragma unroll
                     for (int c = 0; c < C::BN; ++c) {
                         x[c] = ex2_approx(x[c] - m_use);
-                        rs += x[c];
+                        rs8[c & 7] += x[c];
                     }
-                    l = l * alpha + rs;
+                    l = l * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
                 } else {
                     const bool gelu = p.mode == JFA_GDPA_GELU_TANH;
 #pragma unroll
                     for (int c = 0; c < C::BN; ++c) {
-                        float v = x[c] * p.scale;
-                        if (p.bias) v += btab[relpos_bucket(rbase - c)];
-                        const float a = gelu ? gelu_tanh_f(v) : silu_f(v);
-                        x[c] = (c < lim) ? a : 0.f;
+                        const float a = gdpa_act(gelu, x[c]);
+                        x[c] = (full || c < lim) ? a : 0.f;
                     }
                 }
                 // P buffer and O are free once the previous P V product is done.
@@ -416,20 +427,24 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     tmem_st_wait();
                 }
-                // P row -> shared memory, 128-byte swizzled K-major.
-                if constexpr (sizeof(T) == 2) {
+                // P row -> shared memory, 128-byte swizzled K-major (bf16).  GDPA also
+                // writes the rounding remainder P - bf16(P) for a second P V product.
 #pragma unroll
-                    for (int k = 0; k < C::BN / 8; ++k) {
-                        const uint32_t addr = sP + (k >> 3) * (C::BM * 128) + sw128_offset(t, k & 7);
-                        st_shared_v4(addr, pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
-                                     pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
-                    }
-                } else {
+                for (int k = 0; k < C::BN / 8; ++k) {
+                    const uint32_t off = (k >> 3) * (C::BM * 128) + sw128_offset(t, k & 7);
+                    uint32_t u[4];
 #pragma unroll
-                    for (int k = 0; k < C::BN / 4; ++k) {
-                        const uint32_t addr = sP + (k >> 3) * (C::BM * 128) + sw128_offset(t, k & 7);
-                        st_shared_v4(addr, __float_as_uint(x[4 * k]), __float_as_uint(x[4 * k + 1]),
-                                     __float_as_uint(x[4 * k + 2]), __float_as_uint(x[4 * k + 3]));
+                    for (int e = 0; e < 4; ++e) u[e] = pack_bf16x2(x[8 * k + 2 * e], x[8 * k + 2 * e + 1]);
+                    st_shared_v4(sP + off, u[0], u[1], u[2], u[3]);
+                    if (gdpa) {
+                        uint32_t v[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float lo0 = x[8 * k + 2 * e] - __uint_as_float(u[e] << 16);
+                            const float lo1 = x[8 * k + 2 * e + 1] - __uint_as_float(u[e] & 0xffff0000u);
+                            v[e] = pack_bf16x2(lo0, lo1);
+                        }
+                        st_shared_v4(sP2 + off, v[0], v[1], v[2], v[3]);
                     }
                 }
                 fence_proxy_async_smem();

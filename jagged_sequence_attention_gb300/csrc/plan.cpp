@@ -5,9 +5,13 @@
 // become the bottleneck (vibekk.com GEM article, section 第一轮瓶颈迁移: short sequences
 // finish early, long ones keep computing; aihot.vn article, "Jagged Sequence Flash
 // Attention": padding-free kernels otherwise leave SMs idle).  Each (sequence, head,
-// tile) is costed by the score tiles it visits and placed, longest first, on the
-// CTA with the least accumulated cost (Graham's LPT rule), so every CTA of the
-// persistent grid ends within one item of the others.
+// tile) is costed by the score tiles it visits.  Items are listed group by group --
+// a group is one (sequence, head), the largest groups first and, inside a group, the
+// costliest tiles first -- and each item goes to the CTA with the least accumulated
+// cost (greedy list scheduling).  Greedy assignment keeps every CTA within one item
+// of the least loaded one, and because CTAs then run their items in list order, the
+// tiles in flight at any moment belong to a few groups: their K/V (forward) or Q,
+// dO and dQ accumulator rows (backward) stay in L2 instead of being re-read from HBM.
 #include <algorithm>
 #include <cstring>
 #include <numeric>
@@ -104,10 +108,20 @@ void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
     all.reserve(size_t(count_items(q_off, kv_off, B, H, causal, pass)));
     build_items(q_off, kv_off, B, H, causal, pass, &all);
 
-    // Longest first; equal costs in (sequence, head, tile) order so the plan is
-    // deterministic.
-    std::stable_sort(all.begin(), all.end(),
-                     [](const Costed& a, const Costed& b) { return a.cost > b.cost; });
+    // Group-major order: groups by total cost (largest first, ties by sequence and
+    // head), then items by cost inside the group; the sort is stable so equal keys
+    // keep (sequence, head, tile) order and the plan is deterministic.
+    std::vector<int64_t> group_cost(size_t(B) * size_t(H), 0);
+    for (const Costed& c : all) group_cost[size_t(c.w.b) * size_t(H) + size_t(c.w.h)] += c.cost;
+    auto gkey = [&](const Costed& c) { return size_t(c.w.b) * size_t(H) + size_t(c.w.h); };
+    std::stable_sort(all.begin(), all.end(), [&](const Costed& a, const Costed& b) {
+        const size_t ga = gkey(a), gb = gkey(b);
+        if (ga != gb) {
+            if (group_cost[ga] != group_cost[gb]) return group_cost[ga] > group_cost[gb];
+            return ga < gb;
+        }
+        return a.cost > b.cost;
+    });
 
     // Greedy: each item goes to the currently least-loaded CTA (ties: lowest index).
     using Slot = std::pair<int64_t, int32_t>;

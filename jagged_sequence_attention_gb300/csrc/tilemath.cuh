@@ -1,0 +1,69 @@
+// Element-wise pieces shared by the bf16 kernels: the relative-position bucket, the
+// per-chunk constant-bias test, and the GDPA activations with their derivatives.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace jfa {
+
+// bucket(r) = min(31, floor(log2((1+r)^2))) for r >= 0, in integer arithmetic:
+// (1+r)^2 < 2^31 exactly when r < 46340, and then floor(log2(v)) = 31 - clz(v).
+__device__ __forceinline__ int relpos_bucket(int r) {
+    r = abs(r);
+    const int rc = min(r, 46339);
+    const uint32_t v = uint32_t(rc + 1) * uint32_t(rc + 1);
+    const int b = 31 - __clz(v);
+    return r >= 46340 ? 31 : b;
+}
+
+// For 32 consecutive columns whose relative positions run from r_hi down to
+// r_hi - 31: true when all of them are >= 0 and fall in one bucket (the bucket is
+// non-decreasing in r), so the chunk's bias is the single value bucket(r_hi).
+__device__ __forceinline__ bool chunk_bucket_const(int r_hi, int& bucket) {
+    const int r_lo = r_hi - 31;
+    bucket = relpos_bucket(r_hi);
+    return r_lo >= 0 && relpos_bucket(r_lo) == bucket;
+}
+
+// tanh(u) = 1 - 2 / (exp(2u) + 1) from the hardware exp2 and reciprocal (relative
+// error about 2^-22 each); saturates correctly at +-inf.
+__device__ __forceinline__ float tanh_acc(float u) {
+    const float e = ex2_approx(u * 2.8853900817779268f);  // 2 log2(e)
+    return fmaf(-2.f, rcp_approx(e + 1.f), 1.f);
+}
+
+// sigmoid(x) = 1 / (1 + exp(-x))
+__device__ __forceinline__ float sigmoid_acc(float x) {
+    return rcp_approx(1.f + ex2_approx(-1.4426950408889634f * x));
+}
+
+// GDPA activations and derivatives:
+//   gelu(x)  = 0.5 x (1 + tanh(k0 x + k1 x^3)),  k0 = sqrt(2/pi), k1 = 0.044715 k0
+//   gelu'(x) = 0.5 (1 + t) + 0.5 x (1 - t^2) (k0 + 3 k1 x^2)
+//   silu(x)  = x s(x),  silu'(x) = s(x) (1 + x (1 - s(x)))
+__device__ __forceinline__ float gdpa_act(bool gelu, float x) {
+    if (gelu) {
+        const float k0 = 0.7978845608028654f, k1 = 0.035677408136300125f;
+        const float t = tanh_acc(x * fmaf(k1, x * x, k0));
+        const float hx = 0.5f * x;
+        return fmaf(hx, t, hx);
+    }
+    return x * sigmoid_acc(x);
+}
+
+__device__ __forceinline__ void gdpa_act_grad(bool gelu, float x, float& a, float& da) {
+    if (gelu) {
+        const float k0 = 0.7978845608028654f, k1 = 0.035677408136300125f;
+        const float x2 = x * x;
+        const float t = tanh_acc(x * fmaf(k1, x2, k0));
+        const float hx = 0.5f * x;
+        a = fmaf(hx, t, hx);
+        da = fmaf(hx * fmaf(-t, t, 1.f), fmaf(3.f * k1, x2, k0), fmaf(0.5f, t, 0.5f));
+    } else {
+        const float sg = sigmoid_acc(x);
+        a = x * sg;
+        da = sg * fmaf(x, 1.f - sg, 1.f);
+    }
+}
+
+}  // namespace jfa

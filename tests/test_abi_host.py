@@ -119,19 +119,27 @@ def test_worklist_covers_every_tile_once(jfa, case, causal, pass_, n_ctas):
     assert got == expect
 
 
-def test_worklist_is_lpt_balanced(jfa):
-    w = wl.WORKLOADS["causal_bias"]
+@pytest.mark.parametrize("name", ["causal_bias", "long_causal", "cross"])
+def test_worklist_is_balanced_and_group_major(jfa, name):
+    w = wl.WORKLOADS[name]
     q, kv = wl.lengths(w)
     qo, ko = wl.offsets(q), wl.offsets(kv)
     for pass_ in (0, 1):
-        items, offs, cost = jfa.jfa_worklist_build(qo, ko, 8, True, pass_, 148)
-        c = (2 * items[:, 3] + 1) if pass_ == 0 else (5 * items[:, 3] // 2 + 2)
-        # per-CTA cost matches the items assigned to it, items in non-increasing cost
+        items, offs, cost = jfa.jfa_worklist_build(qo, ko, w.H, w.causal, pass_, 148)
+        c = (2 * items[:, 3].astype(np.int64) + 1) if pass_ == 0 else (5 * items[:, 3].astype(np.int64) // 2 + 2)
+        gid = items[:, 0].astype(np.int64) * w.H + items[:, 1]
+        gcost = {}
+        for g, x in zip(gid.tolist(), c.tolist()):
+            gcost[g] = gcost.get(g, 0) + x
         for k in range(148):
-            seg = c[offs[k]:offs[k + 1]]
-            assert seg.sum() == cost[k]
-            assert np.all(np.diff(seg) <= 0)
-        # greedy LPT bound: no CTA exceeds the least loaded one by more than the largest item
+            seg = slice(offs[k], offs[k + 1])
+            # per-CTA cost matches the items assigned to it
+            assert c[seg].sum() == cost[k]
+            # a CTA runs its items group by group, largest groups first
+            gs = [gcost[g] for g in gid[seg].tolist()]
+            assert all(a >= b for a, b in zip(gs, gs[1:]))
+        # greedy list scheduling: no CTA exceeds the least loaded one by more than the
+        # largest item
         assert cost.max() - cost.min() <= c.max()
         assert cost.sum() == c.sum()
 

@@ -87,7 +87,7 @@ def test_guard_bands_untouched():
     from jagged_sequence_attention_gb300 import jfa
     b = wl.make_custom([5, 130, 77], [129, 3, 200], H=2, D=128, causal=True, bias=True, device="cuda", seed=13)
     Tq, Tkv, pad = int(b.q_off[-1]), int(b.kv_off[-1]), 37
-    canary = 1234.5
+    canary = 1536.0  # exactly representable in bf16 and fp32
 
     def buf(T, like):
         t = torch.full((T + pad, b.H, b.D), canary, dtype=like.dtype, device="cuda")
