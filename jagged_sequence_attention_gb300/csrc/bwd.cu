@@ -70,8 +70,15 @@ struct BwdCfg {
     static constexpr int kOffBar = kOffDSt + kPTile;
     static constexpr int kNumBars = 24;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    // tmem slot + abort flag (16 B), per compute warp: lse[64], delta[64], bias[32]
-    static constexpr int kMiscBytes = 16 + 4 * (64 + 64 + 32) * 4;
+    // Warp roles: kCompWarps compute warps (two warpgroups, each owning 32 of the 64
+    // query columns of a step), 4 dQ/epilogue warps, 1 TMA producer, 1 MMA issuer.
+    static constexpr int kCompWarps = 8;
+    static constexpr int kDqWarp0 = kCompWarps;
+    static constexpr int kProdWarp = kCompWarps + 4;
+    static constexpr int kMmaWarp = kCompWarps + 5;
+    static constexpr int kColsPerWarp = BM * 4 / kCompWarps;  // query columns per compute thread
+    // tmem slot + abort flag (16 B), per compute warp: lse, delta (one per column), bias[32]
+    static constexpr int kMiscBytes = 16 + kCompWarps * (2 * kColsPerWarp + 32) * 4;
     static constexpr int kSmemNeed = kOffMisc + kMiscBytes + 1024;
     // At least 120 KB so that exactly one CTA fits on an SM: the CTA allocates all
     // 512 TMEM columns.
@@ -85,7 +92,7 @@ struct BwdCfg {
     static constexpr uint32_t kIdescST = make_idesc(BElem<T>::kFmt, BN, BM, false, false);
     static constexpr uint32_t kIdescAcc = make_idesc(BElem<T>::kFmt, BN, D, false, true);
     static constexpr uint32_t kIdescDQ = make_idesc(BElem<T>::kFmt, 128, BM, true, true);
-    static constexpr int kThreads = 320;
+    static constexpr int kThreads = (kCompWarps + 6) * 32;
 };
 
 enum {
@@ -131,30 +138,21 @@ __device__ __forceinline__ void store_vec<float>(float* dst, const float* v, int
         d4[i] = make_float4(v[4 * i] * mul, v[4 * i + 1] * mul, v[4 * i + 2] * mul, v[4 * i + 3] * mul);
 }
 
-// Write one 64-value row (key row `r`) of P^T or dS^T into the 128-byte swizzled
-// K-major tile at `base`.
+// Write 32 values (query columns [32*half, 32*half+32)) of key row `r` of P^T or
+// dS^T into the 128-byte swizzled K-major bf16 tile at `base` (a row is 64 columns =
+// 128 bytes = 8 chunks of 16 bytes).
 template <typename T>
-__device__ __forceinline__ void write_ptile_row(uint32_t base, int r, const float* v);
-
-template <>
-__device__ __forceinline__ void write_ptile_row<__nv_bfloat16>(uint32_t base, int r, const float* v) {
+__device__ __forceinline__ void write_ptile_half(uint32_t base, int r, int half, const float* v) {
+    static_assert(sizeof(T) == 2, "bf16 tiles only");
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-        st_shared_v4(base + sw128_offset(r, k), pack_bf16x2(v[8 * k], v[8 * k + 1]),
+    for (int k = 0; k < 4; ++k)
+        st_shared_v4(base + sw128_offset(r, half * 4 + k), pack_bf16x2(v[8 * k], v[8 * k + 1]),
                      pack_bf16x2(v[8 * k + 2], v[8 * k + 3]), pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
                      pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
 }
 
-template <>
-__device__ __forceinline__ void write_ptile_row<float>(uint32_t base, int r, const float* v) {
-#pragma unroll
-    for (int k = 0; k < 16; ++k)
-        st_shared_v4(base + (k >> 3) * (kBwdBN * 128) + sw128_offset(r, k & 7), __float_as_uint(v[4 * k]),
-                     __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
-}
-
 template <typename T, int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     jfa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                    const BwdParams p) {
@@ -178,13 +176,13 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(bar(C_Q_FULL + s), 1);
             mbar_init(bar(C_Q_EMPTY + s), 1);
             mbar_init(bar(C_S_FULL + s), 1);
-            mbar_init(bar(C_S_EMPTY + s), 4);
+            mbar_init(bar(C_S_EMPTY + s), C::kCompWarps);
         }
         mbar_init(bar(C_DP_FULL), 1);
-        mbar_init(bar(C_DP_EMPTY), 4);
-        mbar_init(bar(C_PT_FULL), 4);
+        mbar_init(bar(C_DP_EMPTY), C::kCompWarps);
+        mbar_init(bar(C_PT_FULL), C::kCompWarps);
         mbar_init(bar(C_PT_EMPTY), 1);
-        mbar_init(bar(C_DS_FULL), 4);
+        mbar_init(bar(C_DS_FULL), C::kCompWarps);
         mbar_init(bar(C_DS_EMPTY), 1);
         mbar_init(bar(C_DQ_FULL), 1);
         mbar_init(bar(C_DQ_EMPTY), 4);
@@ -194,11 +192,11 @@ __global__ void __launch_bounds__(320, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 9) {
+    if (warp == C::kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == C::kProdWarp && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
@@ -218,7 +216,7 @@ __global__ void __launch_bounds__(320, 1)
         return __all_sync(0xffffffffu, mbar_wait_bounded(bar(b), parity, abort_flag));
     };
 
-    if (warp == 8) {
+    if (warp == C::kProdWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t step_it = 0, item_it = 0;
@@ -260,7 +258,7 @@ __global__ void __launch_bounds__(320, 1)
                     mbar_wait_bounded(bar(C_Q_FULL + s), (last >> 1) & 1, nullptr);
                 }
         }
-    } else if (warp == 9) {
+    } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t step_it = 0, item_it = 0;
@@ -344,13 +342,18 @@ __global__ void __launch_bounds__(320, 1)
             tc_commit(bar(C_DRAIN));
             mbar_wait_bounded(bar(C_DRAIN), 0, nullptr);
         }
-    } else if (warp < 4) {
+    } else if (warp < C::kCompWarps) {
         // ------------------------------------------------------------ P^T and dS^T
-        const int r = threadIdx.x;  // key row in the tile == TMEM lane
-        const uint32_t lane_base = uint32_t(warp * 32) << 16;
-        float* lse_s = misc_f + warp * (64 + 64 + 32);
-        float* del_s = lse_s + 64;
-        float* bias_w = del_s + 64;
+        // Thread = key row r (TMEM lane); warpgroup cw owns query columns
+        // [cw*32, cw*32+32) of each 64-row step.
+        constexpr int NC = C::kColsPerWarp;
+        const int r = (warp & 3) * 32 + lane;
+        const int cw = warp >> 2;
+        const int c0 = cw * NC;
+        const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+        float* lse_s = misc_f + warp * (2 * NC + 32);
+        float* del_s = lse_s + NC;
+        float* bias_w = del_s + NC;
         const bool softmax = p.mode == JFA_SOFTMAX;
         const bool gelu = p.mode == JFA_GDPA_GELU_TANH;
         uint32_t step_it = 0;
@@ -367,59 +370,45 @@ __global__ void __launch_bounds__(320, 1)
             const int j = nt * C::BN + r;  // key row within the sequence
             const bool key_valid = j < kv_len;
             if (p.bias) bias_w[lane] = p.bias[h * 32 + lane] * (softmax ? 1.4426950408889634f : 1.0f);
-            // Row terms (lse in log2 units, Delta) of the step's 64 query rows: each lane
-            // holds two, loaded one step ahead so the load latency hides behind a step.
-            float nl[2] = {0.f, 0.f}, nd[2] = {0.f, 0.f};
+            // Row terms (lse in log2 units, Delta) of this warp's query columns: lane l
+            // holds column c0 + l, fetched one step ahead so the latency hides.
+            float nl = 0.f, nd = 0.f;
             auto fetch = [&](int qrow0) {
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int c = lane + 32 * k;
-                    const bool v = softmax && qrow0 + c < q_len;
-                    const size_t ridx = (size_t(q0) + size_t(v ? qrow0 + c : 0)) * size_t(p.H) + size_t(h);
-                    nl[k] = v ? p.lse[ridx] * 1.4426950408889634f : 0.f;
-                    nd[k] = v ? p.delta[ridx] : 0.f;
-                }
+                const int c = c0 + lane;
+                const bool v = softmax && qrow0 + c < q_len;
+                const size_t ridx = (size_t(q0) + size_t(v ? qrow0 + c : 0)) * size_t(p.H) + size_t(h);
+                nl = v ? p.lse[ridx] * 1.4426950408889634f : 0.f;
+                nd = v ? p.delta[ridx] : 0.f;
             };
             fetch(first_qt * C::BM);
             for (int i = 0; i < n; ++i) {
                 const uint32_t g = step_it + i, sb = g & 1, ph = (g >> 1) & 1;
                 const int qrow0 = (first_qt + i) * C::BM;  // first query row of the step
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    lse_s[lane + 32 * k] = nl[k];
-                    del_s[lane + 32 * k] = nd[k];
-                }
+                lse_s[lane] = nl;
+                del_s[lane] = nd;
                 __syncwarp();
                 if (i + 1 < n) fetch(qrow0 + C::BM);
-                // subtraction scheme: valid query columns are [lo, hi)
-                const int hi = key_valid ? min(C::BM, q_len - qrow0) : 0;
-                const int lo = p.causal ? max(0, j - diag - qrow0) : 0;
-                const bool full = __all_sync(0xffffffffu, lo == 0 && hi == C::BM);
-                const int rbase = qrow0 + diag - j;  // relative position of column 0
+                // subtraction scheme: valid local columns are [lo, hi)
+                const int hi = key_valid ? min(NC, q_len - qrow0 - c0) : 0;
+                const int lo = p.causal ? max(0, j - diag - qrow0 - c0) : 0;
+                const bool full = __all_sync(0xffffffffu, lo == 0 && hi == NC);
+                const int rbase = qrow0 + c0 + diag - j;  // relative position of local column 0
                 const float xs = softmax ? p.scale_log2 : p.scale;
+                int bk = 0;
                 bool cconst = true;
-                float cbias[C::BM / 32];
-#pragma unroll
-                for (int k = 0; k < C::BM / 32; ++k) {
-                    int bk = 0;
-                    // columns 32k..32k+31 have positions rbase+32k .. rbase+32k+31
-                    if (p.bias) cconst &= chunk_bucket_const(rbase + 32 * k + 31, bk);
-                    cbias[k] = p.bias ? bias_w[bk] : 0.f;
-                }
+                if (p.bias) cconst = chunk_bucket_const(rbase + NC - 1, bk);
+                const float cbias = p.bias ? bias_w[bk] : 0.f;
                 cconst = __all_sync(0xffffffffu, cconst);
 
                 if (!warp_wait(C_S_FULL + sb, ph)) { ok = false; break; }
                 tc_fence_after();
-                float pv[C::BM];
-{
-                    uint32_t rr[C::BM / 32][32];
-#pragma unroll
-                    for (int c = 0; c < C::BM / 32; ++c) tmem_ld32(tmem + lane_base + C::kTmS + sb * 64u + c * 32u, rr[c]);
+                float pv[NC];
+                {
+                    uint32_t rr[NC];
+                    tmem_ld32(tmem + lane_base + C::kTmS + sb * 64u + uint32_t(c0), rr);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < C::BM / 32; ++c)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) pv[c * 32 + e] = __uint_as_float(rr[c][e]);
+                    for (int e = 0; e < NC; ++e) pv[e] = __uint_as_float(rr[e]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -428,27 +417,27 @@ __global__ void __launch_bounds__(320, 1)
                 // pv: scaled (and biased) scores
                 if (cconst) {
 #pragma unroll
-                    for (int c = 0; c < C::BM; ++c) pv[c] = fmaf(pv[c], xs, cbias[c >> 5]);
+                    for (int c = 0; c < NC; ++c) pv[c] = fmaf(pv[c], xs, cbias);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < C::BM; ++c) pv[c] = fmaf(pv[c], xs, bias_w[relpos_bucket(rbase + c)]);
+                    for (int c = 0; c < NC; ++c) pv[c] = fmaf(pv[c], xs, bias_w[relpos_bucket(rbase + c)]);
                 }
                 if (!warp_wait(C_PT_EMPTY, (g & 1) ^ 1)) { ok = false; break; }
                 if (softmax) {
 #pragma unroll
-                    for (int c = 0; c < C::BM; ++c) {
+                    for (int c = 0; c < NC; ++c) {
                         const float e = ex2_approx(pv[c] - lse_s[c]);
                         pv[c] = (full || (c >= lo && c < hi)) ? e : 0.f;
                     }
-                    write_ptile_row<T>(sPt, r, pv);
+                    write_ptile_half<T>(sPt, r, cw, pv);
                 } else {
-                    float pa[C::BM];
+                    float pa[NC];
 #pragma unroll
-                    for (int c = 0; c < C::BM; ++c) {
+                    for (int c = 0; c < NC; ++c) {
                         const float a = gdpa_act(gelu, pv[c]);
                         pa[c] = (full || (c >= lo && c < hi)) ? a : 0.f;
                     }
-                    write_ptile_row<T>(sPt, r, pa);
+                    write_ptile_half<T>(sPt, r, cw, pa);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -456,33 +445,30 @@ __global__ void __launch_bounds__(320, 1)
 
                 if (!warp_wait(C_DP_FULL, g & 1)) { ok = false; break; }
                 tc_fence_after();
-                float dp[C::BM];
-{
-                    uint32_t rr[C::BM / 32][32];
-#pragma unroll
-                    for (int c = 0; c < C::BM / 32; ++c) tmem_ld32(tmem + lane_base + C::kTmDP + c * 32u, rr[c]);
+                float dp[NC];
+                {
+                    uint32_t rr[NC];
+                    tmem_ld32(tmem + lane_base + C::kTmDP + uint32_t(c0), rr);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < C::BM / 32; ++c)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) dp[c * 32 + e] = __uint_as_float(rr[c][e]);
+                    for (int e = 0; e < NC; ++e) dp[e] = __uint_as_float(rr[e]);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C_DP_EMPTY));
                 if (softmax) {
 #pragma unroll
-                    for (int c = 0; c < C::BM; ++c) dp[c] = pv[c] * (dp[c] - del_s[c]);
+                    for (int c = 0; c < NC; ++c) dp[c] = pv[c] * (dp[c] - del_s[c]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < C::BM; ++c) {
+                    for (int c = 0; c < NC; ++c) {
                         float a, da;
                         gdpa_act_grad(gelu, pv[c], a, da);
                         dp[c] = (full || (c >= lo && c < hi)) ? da * dp[c] : 0.f;
                     }
                 }
                 if (!warp_wait(C_DS_EMPTY, (g & 1) ^ 1)) { ok = false; break; }
-                write_ptile_row<T>(sDSt, r, dp);
+                write_ptile_half<T>(sDSt, r, cw, dp);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C_DS_FULL));
@@ -492,7 +478,7 @@ __global__ void __launch_bounds__(320, 1)
         if (!ok) fail();
     } else {
         // ------------------------------------------------------------ dQ reduction, dK/dV epilogue
-        const int wq = warp - 4;
+        const int wq = warp - C::kDqWarp0;
         const int r = wq * 32 + lane;  // TMEM lane: head-dim index for dQ^T, key row for dK/dV
         const uint32_t lane_base = uint32_t(wq * 32) << 16;
         uint32_t step_it = 0, item_it = 0;
@@ -578,7 +564,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 9) tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // Delta_i = sum_d dO_id * O_id for each (row, head); one 8-lane group per row.
