@@ -404,33 +404,54 @@ __global__ void __launch_bounds__(448, 1)
                 tc_fence_after();
                 float pv[NC];
                 {
-                    uint32_t rr[NC];
+                    uint32_t (&rr)[NC] = *reinterpret_cast<uint32_t(*)[NC]>(pv);
                     tmem_ld32(tmem + lane_base + C::kTmS + sb * 64u + uint32_t(c0), rr);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < NC; ++e) pv[e] = __uint_as_float(rr[e]);
+                    tmem_ld_wait(rr);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C_S_EMPTY + sb));
 
-                // pv: scaled (and biased) scores
-                if (cconst) {
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) pv[c] = fmaf(pv[c], xs, cbias);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) pv[c] = fmaf(pv[c], xs, bias_w[relpos_bucket(rbase + c)]);
-                }
+                // P^T = exp2(xs * s + bias - lse) (softmax) or act(scale * s + bias):
+                // packed FMA with the per-column addend (bias - lse) precomputed.
                 if (!warp_wait(C_PT_EMPTY, (g & 1) ^ 1)) { ok = false; break; }
                 if (softmax) {
+                    float lv[NC];
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        const float e = ex2_approx(pv[c] - lse_s[c]);
-                        pv[c] = (full || (c >= lo && c < hi)) ? e : 0.f;
+                    for (int c = 0; c < NC; c += 4) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(lse_s + c);
+                        lv[c] = q4.x;
+                        lv[c + 1] = q4.y;
+                        lv[c + 2] = q4.z;
+                        lv[c + 3] = q4.w;
+                    }
+                    const float2 xs2 = make_float2(xs, xs);
+                    if (cconst) {
+#pragma unroll
+                        for (int c = 0; c < NC; c += 2) {
+                            const float2 e = fma2(make_float2(pv[c], pv[c + 1]), xs2,
+                                                  make_float2(cbias - lv[c], cbias - lv[c + 1]));
+                            pv[c] = ex2_approx(e.x);
+                            pv[c + 1] = ex2_approx(e.y);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < NC; ++c)
+                            pv[c] = ex2_approx(fmaf(pv[c], xs, bias_w[relpos_bucket(rbase + c)] - lv[c]));
+                    }
+                    if (!full) {
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) pv[c] = (c >= lo && c < hi) ? pv[c] : 0.f;
                     }
                     write_ptile_half<T>(sPt, r, cw, pv);
                 } else {
+                    if (cconst) {
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) pv[c] = fmaf(pv[c], xs, cbias);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) pv[c] = fmaf(pv[c], xs, bias_w[relpos_bucket(rbase + c)]);
+                    }
                     float pa[NC];
 #pragma unroll
                     for (int c = 0; c < NC; ++c) {
@@ -447,18 +468,27 @@ __global__ void __launch_bounds__(448, 1)
                 tc_fence_after();
                 float dp[NC];
                 {
-                    uint32_t rr[NC];
+                    uint32_t (&rr)[NC] = *reinterpret_cast<uint32_t(*)[NC]>(dp);
                     tmem_ld32(tmem + lane_base + C::kTmDP + uint32_t(c0), rr);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < NC; ++e) dp[e] = __uint_as_float(rr[e]);
+                    tmem_ld_wait(rr);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C_DP_EMPTY));
                 if (softmax) {
+                    // dS^T = P^T (dP^T - Delta), packed
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) dp[c] = pv[c] * (dp[c] - del_s[c]);
+                    for (int c = 0; c < NC; c += 4) {
+                        const float4 d4 = *reinterpret_cast<const float4*>(del_s + c);
+                        const float2 a = mul2(make_float2(pv[c], pv[c + 1]),
+                                              add2(make_float2(dp[c], dp[c + 1]), make_float2(-d4.x, -d4.y)));
+                        const float2 b2 = mul2(make_float2(pv[c + 2], pv[c + 3]),
+                                               add2(make_float2(dp[c + 2], dp[c + 3]), make_float2(-d4.z, -d4.w)));
+                        dp[c] = a.x;
+                        dp[c + 1] = a.y;
+                        dp[c + 2] = b2.x;
+                        dp[c + 3] = b2.y;
+                    }
                 } else {
 #pragma unroll
                     for (int c = 0; c < NC; ++c) {
@@ -511,7 +541,8 @@ __global__ void __launch_bounds__(448, 1)
                     uint32_t rr[C::BM / 32][32];
 #pragma unroll
                     for (int c = 0; c < C::BM / 32; ++c) tmem_ld32(tmem + lane_base + C::kTmDQ + c * 32u, rr[c]);
-                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < C::BM / 32; ++c) tmem_ld_wait(rr[c]);
 #pragma unroll
                     for (int c = 0; c < C::BM / 32; ++c)
 #pragma unroll
@@ -541,12 +572,12 @@ __global__ void __launch_bounds__(448, 1)
                     uint32_t rr[32];
                     float v[32];
                     tmem_ld32(tmem + lane_base + C::kTmDV + c * 32u, rr);
-                    tmem_ld_wait();
+                    tmem_ld_wait(rr);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(rr[e]);
                     if (kv_ok) store_vec<T>(dv_row + c * 32, v, 32, 1.f);
                     tmem_ld32(tmem + lane_base + C::kTmDK + c * 32u, rr);
-                    tmem_ld_wait();
+                    tmem_ld_wait(rr);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(rr[e]);
                     if (kv_ok) store_vec<T>(dk_row + c * 32, v, 32, p.scale);

@@ -43,17 +43,19 @@ __device__ __forceinline__ float act_grad_f32(int mode, float x) {
     return sg * (1.f + x * (1.f - sg));
 }
 
-// One CTA per forward work item (query tile of 128 rows); thread = query row.
+// Two CTAs per forward work item (a pair of 128-row query tiles); thread = query row.
 template <int D>
 __global__ void __launch_bounds__(kF32Rows) jfa_fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                                                                 const float* __restrict__ V, const FwdParams p) {
     __shared__ float sK[kF32Inner][D];
     __shared__ float sV[kF32Inner][D];
     __shared__ float sB[32];
-    const int4 w = p.items[blockIdx.x];
-    const int b = w.x, h = w.y, mt = w.z, n_tiles = w.w;
+    const int4 w = p.items[blockIdx.x >> 1];
+    const int b = w.x, h = w.y, mt = 2 * w.z + int(blockIdx.x & 1);
     const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
     const int k0 = p.kv_off[b], kv_len = p.kv_off[b + 1] - k0;
+    if (mt * kF32Rows >= q_len) return;  // second tile of a short last pair (uniform exit)
+    const int n_tiles = fwd_tiles_of(q_len, kv_len, mt, p.causal);
     const int t = threadIdx.x, row = mt * kF32Rows + t;
     const bool valid = row < q_len;
     const int diag = kv_len - q_len;
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
 cudaError_t launch_fwd_f32(int D, const void* Q, const void* K, const void* V, const FwdParams& p, int64_t n_items,
                            cudaStream_t st) {
     if (n_items <= 0) return cudaSuccess;
-    const unsigned g = unsigned(n_items);
+    const unsigned g = unsigned(2 * n_items);
     if (D == 32)
         jfa_fwd_f32_kernel<32><<<g, kF32Rows, 0, st>>>(static_cast<const float*>(Q), static_cast<const float*>(K),
                                                        static_cast<const float*>(V), p);

@@ -1,83 +1,71 @@
 // Forward kernel: jagged flash attention / GDPA on sm_103a.
 //
-// Computes, per (sequence, head, 128-row query tile) work item, the attention of
-// the GEM articles' "Jagged Sequence Flash Attention" (aihot.vn, that section):
-// directly on packed values plus offsets, never materialising a padded tensor.
-// Masking follows the "subtraction scheme" the kerneldigest.dev summary names
-// (section "Arquitectura del Sistema"): for a key tile starting at column c0 the
-// kernel subtracts c0 from the sequence's key length (and from the row's causal
+// Computes, per (sequence, head, pair of 128-row query tiles) work item, the
+// attention of the GEM articles' "Jagged Sequence Flash Attention" (aihot.vn, that
+// section): directly on packed values plus offsets, never materialising a padded
+// tensor.  Masking follows the "subtraction scheme" the kerneldigest.dev summary
+// names (section "Arquitectura del Sistema"): for a key tile starting at column c0
+// the kernel subtracts c0 from the sequence's key length (and from the row's causal
 // limit) and masks columns at or beyond what remains -- no mask tensor, no padding.
 // The GDPA mode (aihot.vn, "Generalized Dot-Product Attention (GDPA)") swaps the
 // online softmax for an elementwise GELU/SiLU with no normalisation.
 //
-// CTA = 6 warps, persistent, one CTA per SM, work list from the LPT planner:
-//   warps 0-3  softmax/activation + correction + epilogue; thread t owns query row t
-//              of the tile and TMEM lane t;
-//   warp 4     TMA producer (Q once per item; K_j, V_j through 2-stage rings);
-//   warp 5     tcgen05.mma issuer and TMEM owner.
-// TMEM (512 columns): S double buffer at columns [0,128) and [128,256), O at
-// [256, 256+D).  The MMA warp computes S_{j+1} = Q K_{j+1}^T while the softmax
-// warps turn S_j into P_j; P_j goes to shared memory (bf16, or fp32 read as TF32)
-// in the 128-byte-swizzled K-major layout, and O += P_j V_j runs with V as an
-// MN-major operand.
+// CTA = 10 warps, persistent, one CTA per SM, work list from the planner.  Two query
+// tiles (A: rows 256p..256p+127, B: the next 128) share every K/V tile, so each K/V
+// byte loaded feeds two products, and two softmax warpgroups ping-pong around the
+// tensor core:
+//   warps 0-3  tile A softmax/activation, correction, epilogue (thread = row = lane)
+//   warps 4-7  tile B, the same
+//   warp 8     TMA producer: Q_A, Q_B once per item; K_j, V_j through 2-stage rings
+//   warp 9     tcgen05.mma issuer and TMEM owner
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [384,384+D).
+// P is written back over its own S columns as packed bf16 (64 columns; GDPA adds the
+// rounding remainder in the next 64) and read by O += P V straight from TMEM.  The
+// MMA issue order S_A(j) S_B(j) PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ... keeps the
+// tensor core on one tile while the other tile's softmax runs.
 #include "jfa_internal.h"
 #include "ptx.cuh"
 #include "tilemath.cuh"
 
 namespace jfa {
 
-template <typename T>
-struct Elem;
-template <>
-struct Elem<__nv_bfloat16> {
-    static constexpr int kBytes = 2;
-    static constexpr uint32_t kFmt = kFmtBF16;
-    static constexpr int kUmmaK = 16;  // K elements per tcgen05.mma (32 bytes)
-    static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-};
-template <>
-struct Elem<float> {
-    static constexpr int kBytes = 4;
-    static constexpr uint32_t kFmt = kFmtTF32;
-    static constexpr int kUmmaK = 8;
-    static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-};
-
-template <typename T, int D>
+template <int D>
 struct FwdCfg {
     static constexpr int BM = kFwdBM, BN = kFwdBN;
-    static constexpr int E = Elem<T>::kBytes;
-    static constexpr int kRowBytes = D * E;
+    static constexpr int kRowBytes = D * 2;
     static_assert(kRowBytes % 128 == 0 && kRowBytes <= 256, "head row must be 128 or 256 bytes");
     static constexpr int kCB = kRowBytes / 128;  // 128-byte column blocks of a tile
-    static constexpr int kBoxCols = 128 / E;     // elements per 128-byte box row
+    static constexpr int kBoxCols = 64;          // bf16 elements per 128-byte box row
     static constexpr int kQBytes = BM * kRowBytes;
     static constexpr int kKVBytes = BN * kRowBytes;
-    static constexpr int kPRowBytes = BN * E;
-    static constexpr int kPBytes = BM * kPRowBytes;
     static constexpr int kStages = 2;
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQBytes;
+    static constexpr int kOffQ = 0;  // + tile * kQBytes
+    static constexpr int kOffK = kOffQ + 2 * kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
-    static constexpr int kOffP = kOffV + kStages * kKVBytes;
-    static constexpr int kOffP2 = kOffP + kPBytes;  // GDPA: P - bf16(P), second PV product
-    static constexpr int kOffBar = kOffP2 + kPBytes;
-    static constexpr int kNumBars = 20;
+    static constexpr int kOffBar = kOffV + kStages * kKVBytes;
+    static constexpr int kNumBars = 24;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kMiscBytes = 16 + 2 * 4 * 32 * 4;  // tmem slot, abort flag, bias tables
+    static constexpr int kMiscBytes = 16 + 2 * 8 * 32 * 4;  // tmem slot, abort flag, bias tables
     static constexpr int kSmemNeed = kOffMisc + kMiscBytes + 1024;
     // At least 120 KB so that exactly one CTA fits on an SM: the CTA allocates all
     // 512 TMEM columns.
     static constexpr int kSmemBytes = kSmemNeed > 120 * 1024 ? kSmemNeed : 120 * 1024;
-    static constexpr int kUmmaK = Elem<T>::kUmmaK;
+    static constexpr int kUmmaK = 16;
     static constexpr int kQKSteps = D / kUmmaK;
     static constexpr int kPVSteps = BN / kUmmaK;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kTmemO = 256;
-    static constexpr uint32_t kIdescQK = make_idesc(Elem<T>::kFmt, BM, BN, false, false);
-    static constexpr uint32_t kIdescPV = make_idesc(Elem<T>::kFmt, BM, D, false, true);
-    static constexpr int kThreads = 192;
+    static constexpr uint32_t kIdescQK = make_idesc(kFmtBF16, BM, BN, false, false);
+    static constexpr uint32_t kIdescPV = make_idesc(kFmtBF16, BM, D, false, true);
+    static constexpr int kThreads = 320;
+    static constexpr int kProdWarp = 8, kMmaWarp = 9;
+    __host__ __device__ static constexpr uint32_t tmem_s(int x) { return x ? 128u : 0u; }
+    __host__ __device__ static constexpr uint32_t tmem_o(int x) { return x ? 384u : 256u; }
 };
+
+// TMEM column (within a tile's S/P columns) of the 16 P values of PV K-step s: P of
+// S chunk k (32 columns) occupies the chunk's first 16 columns, two bf16 per column,
+// and the GDPA rounding remainder the next 16.
+__device__ __forceinline__ uint32_t p_col(int s) { return uint32_t(32 * (s >> 1) + 8 * (s & 1)); }
 
 // Barrier slots.
 enum {
@@ -87,12 +75,11 @@ enum {
     B_K_EMPTY = 4,  // +stage
     B_V_FULL = 6,
     B_V_EMPTY = 8,
-    B_S_FULL = 10,   // +buffer
-    B_S_EMPTY = 12,  // +buffer
-    B_P_FULL = 14,
-    B_O_FULL = 15,
-    B_O_EMPTY = 16,
-    B_DRAIN = 17,
+    B_S_FULL = 10,   // +tile
+    B_P_FULL = 12,   // +tile
+    B_O_DONE = 14,   // +tile: a P V product of the tile finished
+    B_O_EMPTY = 16,  // +tile: the tile's epilogue has read O
+    B_DRAIN = 18,
 };
 
 template <typename T>
@@ -117,22 +104,21 @@ __device__ __forceinline__ void store_row<float>(float* dst, const float* v, int
     for (int i = 0; i < n / 4; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-template <typename T, int D, typename OT>
-__global__ void __launch_bounds__(192, 1)
+template <int D, typename OT, bool GDPA>
+__global__ void __launch_bounds__(320, 1)
     jfa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using C = FwdCfg<T, D>;
+    using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV,
-                   sP = sbase + C::kOffP, sP2 = sbase + C::kOffP2;
-    const bool gdpa = p.mode != JFA_SOFTMAX;
+    const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV;
     auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * uint32_t(i); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     float* bias_s = reinterpret_cast<float*>(smem + C::kOffMisc + 16);
+    constexpr bool gdpa = GDPA;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -145,20 +131,19 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bar(B_V_FULL + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
             mbar_init(bar(B_S_FULL + s), 1);
-            mbar_init(bar(B_S_EMPTY + s), 4);
+            mbar_init(bar(B_P_FULL + s), 4);
+            mbar_init(bar(B_O_DONE + s), 1);
+            mbar_init(bar(B_O_EMPTY + s), 4);
         }
-        mbar_init(bar(B_P_FULL), 4);
-        mbar_init(bar(B_O_FULL), 1);
-        mbar_init(bar(B_O_EMPTY), 4);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == C::kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == C::kProdWarp && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
@@ -176,7 +161,7 @@ __global__ void __launch_bounds__(192, 1)
         atomicOr(p.status, kStatusTimeout);
     };
 
-    if (warp == 4) {
+    if (warp == C::kProdWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t kv_it = 0, item_it = 0;
@@ -185,14 +170,16 @@ __global__ void __launch_bounds__(192, 1)
                 const int4 w = p.items[it];
                 const int n = w.w;
                 if (n == 0) continue;
-                const int b = w.x, h = w.y, mt = w.z;
-                const int q0 = p.q_off[b], kv0 = p.kv_off[b];
+                const int b = w.x, h = w.y, pr = w.z;
+                const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0, kv0 = p.kv_off[b];
+                const int ntiles = (2 * pr + 1) * C::BM < q_len ? 2 : 1;
                 if (!mbar_wait_bounded(bar(B_Q_EMPTY), (item_it & 1) ^ 1, abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(bar(B_Q_FULL), C::kQBytes);
+                mbar_arrive_expect_tx(bar(B_Q_FULL), C::kQBytes * ntiles);
+                for (int tq = 0; tq < ntiles; ++tq)
 #pragma unroll
-                for (int cb = 0; cb < C::kCB; ++cb)
-                    tma_load_2d(sQ + cb * C::BM * 128, &tmQ, bar(B_Q_FULL), h * D + cb * C::kBoxCols,
-                                q0 + mt * C::BM);
+                    for (int cb = 0; cb < C::kCB; ++cb)
+                        tma_load_2d(sQ + tq * C::kQBytes + cb * C::BM * 128, &tmQ, bar(B_Q_FULL),
+                                    h * D + cb * C::kBoxCols, q0 + (2 * pr + tq) * C::BM);
                 ++item_it;
                 for (int j = 0; j < n; ++j, ++kv_it) {
                     const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
@@ -222,69 +209,91 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t kv_it = 0, item_it = 0, pv_it = 0;
+            uint32_t kv_it = 0, item_it = 0;
+            uint32_t pv_cnt[2] = {0, 0}, items_x[2] = {0, 0};
             bool ok = true;
-            for (int it = it_begin; it < it_end && ok; ++it) {
-                const int n = p.items[it].w;
-                if (n == 0) continue;
-                if (!mbar_wait_bounded(bar(B_Q_FULL), item_it & 1, abort_flag)) { ok = false; break; }
+            // S_x = Q_x K^T into the tile's S columns; first waits for the tile's
+            // previous P V product, which reads P from those columns.
+            auto issue_s = [&](int x, uint32_t st) -> bool {
+                if (pv_cnt[x] > 0 && !mbar_wait_bounded(bar(B_O_DONE + x), (pv_cnt[x] - 1) & 1, abort_flag))
+                    return false;
                 tc_fence_after();
-                for (int j = 0; j <= n && ok; ++j) {
-                    if (j < n) {
-                        const uint32_t g = kv_it + j, st = g & 1, ph = (g >> 1) & 1;
-                        if (!mbar_wait_bounded(bar(B_K_FULL + st), ph, abort_flag) ||
-                            !mbar_wait_bounded(bar(B_S_EMPTY + st), ph ^ 1, abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t d_tmem = tmem + st * 128u;
-                        const uint32_t kbase = sK + st * C::kKVBytes;
+                const uint32_t kbase = sK + st * C::kKVBytes;
+                const uint32_t qbase = sQ + x * C::kQBytes;
 #pragma unroll
-                        for (int s = 0; s < C::kQKSteps; ++s) {
-                            const uint32_t koff = (s * 32) & 127;  // bytes into the 128-byte row
-                            const uint32_t cb = (s * 32) >> 7;     // 128-byte column block
-                            const uint64_t a = make_sdesc_sw128(sQ + cb * C::BM * 128 + koff, 16, 1024);
-                            const uint64_t bd = make_sdesc_sw128(kbase + cb * C::BN * 128 + koff, 16, 1024);
-                            mma_f16_ss(d_tmem, a, bd, C::kIdescQK, s > 0);
-                        }
-                        tc_commit(bar(B_S_FULL + st));
-                        tc_commit(bar(B_K_EMPTY + st));
-                        if (j == n - 1) tc_commit(bar(B_Q_EMPTY));
+                for (int s = 0; s < C::kQKSteps; ++s) {
+                    const uint32_t koff = (s * 32) & 127;  // bytes into the 128-byte row
+                    const uint32_t cb = (s * 32) >> 7;     // 128-byte column block
+                    mma_f16_ss(tmem + C::tmem_s(x), make_sdesc_sw128(qbase + cb * C::BM * 128 + koff, 16, 1024),
+                               make_sdesc_sw128(kbase + cb * C::BN * 128 + koff, 16, 1024), C::kIdescQK, s > 0);
+                }
+                tc_commit(bar(B_S_FULL + x));
+                return true;
+            };
+            // O_x += P_x V with P read from TMEM; GDPA adds the remainder product.
+            auto issue_pv = [&](int x, uint32_t st, bool first) -> bool {
+                if (!mbar_wait_bounded(bar(B_P_FULL + x), pv_cnt[x] & 1, abort_flag)) return false;
+                if (first && !mbar_wait_bounded(bar(B_O_EMPTY + x), (items_x[x] & 1) ^ 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t vbase = sV + st * C::kKVBytes;
+#pragma unroll
+                for (int s = 0; s < C::kPVSteps; ++s) {
+                    const uint64_t bd = make_sdesc_sw128(vbase + s * C::kUmmaK * 128, C::BN * 128, 1024);
+                    mma_f16_ts(tmem + C::tmem_o(x), tmem + C::tmem_s(x) + p_col(s), bd, C::kIdescPV,
+                               (!first || s > 0));
+                }
+                if (gdpa) {
+#pragma unroll
+                    for (int s = 0; s < C::kPVSteps; ++s) {
+                        const uint64_t bd = make_sdesc_sw128(vbase + s * C::kUmmaK * 128, C::BN * 128, 1024);
+                        mma_f16_ts(tmem + C::tmem_o(x), tmem + C::tmem_s(x) + p_col(s) + 16u, bd,
+                                   C::kIdescPV, 1u);
                     }
-                    if (j > 0) {
-                        const int jj = j - 1;
-                        const uint32_t g = kv_it + jj, st = g & 1, ph = (g >> 1) & 1;
-                        if (!mbar_wait_bounded(bar(B_P_FULL), pv_it & 1, abort_flag) ||
-                            !mbar_wait_bounded(bar(B_V_FULL + st), ph, abort_flag)) { ok = false; break; }
-                        if (jj == 0 && !mbar_wait_bounded(bar(B_O_EMPTY), (item_it & 1) ^ 1, abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t vbase = sV + st * C::kKVBytes;
-#pragma unroll
-                        for (int s = 0; s < C::kPVSteps; ++s) {
-                            const uint32_t koff = (s * 32) & 127;
-                            const uint32_t cb = (s * 32) >> 7;
-                            const uint64_t a = make_sdesc_sw128(sP + cb * C::BM * 128 + koff, 16, 1024);
-                            const uint64_t bd = make_sdesc_sw128(vbase + s * C::kUmmaK * 128, C::BN * 128, 1024);
-                            mma_f16_ss(tmem + C::kTmemO, a, bd, C::kIdescPV, (jj > 0 || s > 0));
-                        }
-                        if (gdpa) {  // O += (P - bf16(P)) V: P to ~16 significant bits
-#pragma unroll
-                            for (int s = 0; s < C::kPVSteps; ++s) {
-                                const uint32_t koff = (s * 32) & 127;
-                                const uint32_t cb = (s * 32) >> 7;
-                                const uint64_t a = make_sdesc_sw128(sP2 + cb * C::BM * 128 + koff, 16, 1024);
-                                const uint64_t bd = make_sdesc_sw128(vbase + s * C::kUmmaK * 128, C::BN * 128, 1024);
-                                mma_f16_ss(tmem + C::kTmemO, a, bd, C::kIdescPV, 1u);
-                            }
-                        }
-                        tc_commit(bar(B_O_FULL));
-                        tc_commit(bar(B_V_EMPTY + st));
-                        ++pv_it;
+                }
+                tc_commit(bar(B_O_DONE + x));
+                ++pv_cnt[x];
+                return true;
+            };
+            for (int it = it_begin; it < it_end && ok; ++it) {
+                const int4 w = p.items[it];
+                const int n = w.w;
+                if (n == 0) continue;
+                const int b = w.x, pr = w.z;
+                const int q_len = p.q_off[b + 1] - p.q_off[b], kv_len = p.kv_off[b + 1] - p.kv_off[b];
+                const int nx0 = fwd_tiles_of(q_len, kv_len, 2 * pr, p.causal);
+                const int nx1 = fwd_tiles_of(q_len, kv_len, 2 * pr + 1, p.causal);
+                if (!mbar_wait_bounded(bar(B_Q_FULL), item_it & 1, abort_flag)) { ok = false; break; }
+                // prologue: S of key tile 0
+                {
+                    const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
+                    if (!mbar_wait_bounded(bar(B_K_FULL + st), ph, abort_flag)) { ok = false; break; }
+                    if (nx0 > 0 && !issue_s(0, st)) { ok = false; break; }
+                    if (nx1 > 0 && !issue_s(1, st)) { ok = false; break; }
+                    tc_commit(bar(B_K_EMPTY + st));
+                    if (n == 1) tc_commit(bar(B_Q_EMPTY));
+                }
+                for (int j = 0; j < n && ok; ++j) {
+                    const uint32_t g = kv_it + j, st = g & 1, ph = (g >> 1) & 1;
+                    const uint32_t g1 = g + 1, st1 = g1 & 1, ph1 = (g1 >> 1) & 1;
+                    if (!mbar_wait_bounded(bar(B_V_FULL + st), ph, abort_flag)) { ok = false; break; }
+                    if (j < nx0 && !issue_pv(0, st, j == 0)) { ok = false; break; }
+                    if (j + 1 < n && !mbar_wait_bounded(bar(B_K_FULL + st1), ph1, abort_flag)) { ok = false; break; }
+                    if (j + 1 < nx0 && !issue_s(0, st1)) { ok = false; break; }
+                    if (j < nx1 && !issue_pv(1, st, j == 0)) { ok = false; break; }
+                    tc_commit(bar(B_V_EMPTY + st));
+                    if (j + 1 < nx1 && !issue_s(1, st1)) { ok = false; break; }
+                    if (j + 1 < n) {
+                        tc_commit(bar(B_K_EMPTY + st1));
+                        if (j + 2 == n) tc_commit(bar(B_Q_EMPTY));
                     }
                 }
                 kv_it += n;
                 ++item_it;
+                items_x[0] += nx0 > 0 ? 1 : 0;
+                items_x[1] += nx1 > 0 ? 1 : 0;
             }
             if (!ok) fail();
             // Drain all issued MMAs before TMEM is released.
@@ -293,22 +302,28 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax / epilogue
-        const int t = threadIdx.x;  // query row in the tile == TMEM lane
-        const uint32_t lane_base = uint32_t(warp * 32) << 16;
-        const bool softmax = p.mode == JFA_SOFTMAX;
-        uint32_t kv_it = 0, item_it = 0, pv_wait = 0;
+        const int x = warp >> 2;               // query tile of this warpgroup
+        const int t = (warp & 3) * 32 + lane;  // row in the tile == TMEM lane
+        const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::tmem_s(x);
+        const uint32_t tO = tmem + lane_base + C::tmem_o(x);
+        constexpr bool softmax = !GDPA;
+        uint32_t s_cnt = 0;
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
             const int4 w = p.items[it];
-            const int n = w.w, b = w.x, h = w.y, mt = w.z;
+            const int b = w.x, h = w.y, pr = w.z;
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
             const int kv_len = p.kv_off[b + 1] - p.kv_off[b];
-            const int row = mt * C::BM + t;
+            const int tile = 2 * pr + x;
+            if (tile * C::BM >= q_len) continue;  // tile B of a short last pair
+            const int n = fwd_tiles_of(q_len, kv_len, tile, p.causal);
+            const int row = tile * C::BM + t;
             const bool row_valid = row < q_len;
             const int diag = kv_len - q_len;
             // Each warp keeps its own copy of the head's bias row (log2 units for
             // softmax), double-buffered by item parity, so no cross-warp barrier.
-            float* btab = bias_s + ((item_it & 1) * 4 + warp) * 32;
+            float* btab = bias_s + ((it & 1) * 8 + warp) * 32;
             if (p.bias) {
                 btab[lane] = p.bias[h * 32 + lane] * (softmax ? 1.4426950408889634f : 1.0f);
                 __syncwarp();
@@ -316,43 +331,29 @@ __global__ void __launch_bounds__(192, 1)
             const size_t orow = (size_t(q0) + size_t(row)) * size_t(p.H) + size_t(h);
             if (n == 0) {
                 if (row_valid) {
-                    float z[D];
+                    float z[32];
 #pragma unroll
-                    for (int d = 0; d < D; ++d) z[d] = 0.f;
-                    store_row<OT>(reinterpret_cast<OT*>(p.O) + orow * D, z, D);
+                    for (int d = 0; d < 32; ++d) z[d] = 0.f;
+                    for (int c = 0; c < D / 32; ++c) store_row<OT>(reinterpret_cast<OT*>(p.O) + orow * D + c * 32, z, 32);
                     if (p.lse) p.lse[orow] = -INFINITY;
                 }
-                ++item_it;
                 continue;
             }
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
-                const uint32_t g = kv_it + j, sb = g & 1, ph = (g >> 1) & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_S_FULL + sb), ph, abort_flag))) { ok = false; break; }
-                tc_fence_after();
-                float x[C::BN];
-                {
-                    uint32_t r[C::BN / 32][32];
-#pragma unroll
-                    for (int c = 0; c < C::BN / 32; ++c) tmem_ld32(tmem + lane_base + sb * 128u + c * 32u, r[c]);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < C::BN / 32; ++c)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[c][i]);
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_S_FULL + x), s_cnt & 1, abort_flag))) {
+                    ok = false;
+                    break;
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_S_EMPTY + sb));
-
+                tc_fence_after();
                 const int col0 = j * C::BN;
                 int lim = kv_len - col0;  // subtraction scheme: columns >= lim are masked
                 if (p.causal) lim = min(lim, row + diag + 1 - col0);
                 const int rbase = row + diag - col0;  // relative position of column 0
                 const bool full = __all_sync(0xffffffffu, lim >= C::BN);
                 const float xs = softmax ? p.scale_log2 : p.scale;
-                // x = scale * s + bias: one constant per 32-column chunk when the whole
-                // chunk sits in one bucket (warp-uniform), else per element.
+                // Bias: one constant per 32-column chunk when the whole chunk sits in one
+                // bucket (warp-uniform), else per element.
                 bool cconst = true;
                 float cb[C::BN / 32];
 #pragma unroll
@@ -361,27 +362,68 @@ __global__ void __launch_bounds__(192, 1)
                     if (p.bias) cconst &= chunk_bucket_const(rbase - 32 * k, bk);
                     cb[k] = p.bias ? btab[bk] : 0.f;
                 }
-                if (__all_sync(0xffffffffu, cconst)) {
+                cconst = __all_sync(0xffffffffu, cconst);
+                // Scaled, biased and masked scores of chunk k minus `shift`.
+                auto chunk_x = [&](const uint32_t (&r)[32], int k, float shift, float (&v)[32]) {
+                    if (cconst) {
+                        const float2 sc = make_float2(xs, xs), add = make_float2(cb[k] - shift, cb[k] - shift);
 #pragma unroll
-                    for (int c = 0; c < C::BN; ++c) x[c] = fmaf(x[c], xs, cb[c >> 5]);
-                } else {
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 t2 = fma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sc, add);
+                            v[i] = t2.x;
+                            v[i + 1] = t2.y;
+                        }
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < C::BN; ++c) x[c] = fmaf(x[c], xs, btab[relpos_bucket(rbase - c)]);
-                }
-                bool need_rescale = false;
-                float alpha = 1.f;
-                if (softmax) {
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = fmaf(__uint_as_float(r[i]), xs, btab[relpos_bucket(rbase - 32 * k - i)] - shift);
+                    }
                     if (!full) {
 #pragma unroll
-                        for (int c = 0; c < C::BN; ++c) x[c] = (c < lim) ? x[c] : -INFINITY;
+                        for (int i = 0; i < 32; ++i) v[i] = (32 * k + i < lim) ? v[i] : -INFINITY;
                     }
-                    float mx8[8];
+                };
+                // S streams from TMEM in 32-column chunks; the load of chunk k+1 is in
+                // flight while chunk k is processed.  P of chunk k (and, for GDPA, its
+                // rounding remainder) is written over chunk k's own columns: P at
+                // [32k, 32k+16), remainder at [32k+16, 32k+32), two bf16 per column.
+                uint32_t ra[32], rb[32];
+                bool need_rescale = false;
+                float alpha = 1.f;
+                if constexpr (softmax) {
+                    // pass 1: row max.  With a constant bias per chunk the max of
+                    // xs * s + cb is xs * max(s) + cb (xs > 0): one FMNMX per element.
+                    float mx = -INFINITY;
+                    tmem_ld32(tS, ra);
+                    tmem_ld_wait(ra);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+                    for (int k = 0; k < C::BN / 32; ++k) {
+                        uint32_t (&cur)[32] = (k & 1) ? rb : ra;
+                        uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
+                        if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
+                        float mk;
+                        if (cconst) {
+                            float m4[4];
 #pragma unroll
-                    for (int c = 8; c < C::BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-                    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                            for (int e = 0; e < 4; ++e)
+                                m4[e] = (full || 32 * k + e < lim) ? __uint_as_float(cur[e]) : -INFINITY;
+#pragma unroll
+                            for (int i = 4; i < 32; ++i) {
+                                const float si = (full || 32 * k + i < lim) ? __uint_as_float(cur[i]) : -INFINITY;
+                                m4[i & 3] = fmaxf(m4[i & 3], si);
+                            }
+                            mk = fmaf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), xs, cb[k]);
+                        } else {
+                            float v[32];
+                            chunk_x(cur, k, 0.f, v);
+                            float m4[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+                            for (int i = 4; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
+                            mk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                        }
+                        mx = fmaxf(mx, mk);
+                        if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
+                    }
                     // Lazy rescaling: keep the running max unless it grows by more
                     // than 2^8; both O and l use the same stale max, so the final
                     // O / l is unchanged.
@@ -391,71 +433,81 @@ __global__ void __launch_bounds__(192, 1)
                     alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_use);
                     if (m_new != m) need_rescale = (j > 0);
                     m = m_new;
-                    float rs8[8];
+                    // pass 2: P = exp2(x - m) (packed FMA folds in -m), packed row sum,
+                    // P -> TMEM
+                    float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                    make_float2(0.f, 0.f)};
+                    tmem_ld32(tS, ra);
+                    tmem_ld_wait(ra);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
+                    for (int k = 0; k < C::BN / 32; ++k) {
+                        uint32_t (&cur)[32] = (k & 1) ? rb : ra;
+                        uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
+                        if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
+                        float v[32];
+                        chunk_x(cur, k, m_use, v);
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int c = 0; c < C::BN; ++c) {
-                        x[c] = ex2_approx(x[c] - m_use);
-                        rs8[c & 7] += x[c];
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 e2 = make_float2(ex2_approx(v[i]), ex2_approx(v[i + 1]));
+                            rs[(i >> 1) & 3] = add2(rs[(i >> 1) & 3], e2);
+                            pk[i >> 1] = pack_bf16x2(e2.x, e2.y);
+                        }
+                        tmem_st16(tS + 32u * k, pk);
+                        if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
                     }
-                    l = l * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
+                    const float2 r01 = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
+                    l = l * alpha + (r01.x + r01.y);
                 } else {
+                    // GDPA: P = act(x), one pass; remainder P - bf16(P) beside it.
                     const bool gelu = p.mode == JFA_GDPA_GELU_TANH;
+                    tmem_ld32(tS, ra);
+                    tmem_ld_wait(ra);
 #pragma unroll
-                    for (int c = 0; c < C::BN; ++c) {
-                        const float a = gdpa_act(gelu, x[c]);
-                        x[c] = (full || c < lim) ? a : 0.f;
+                    for (int k = 0; k < C::BN / 32; ++k) {
+                        uint32_t (&cur)[32] = (k & 1) ? rb : ra;
+                        uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
+                        if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
+                        float v[32];
+                        chunk_x(cur, k, 0.f, v);
+                        uint32_t pk[16], pl[16];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float a0 = (full || 32 * k + i < lim) ? gdpa_act(gelu, v[i]) : 0.f;
+                            const float a1 = (full || 32 * k + i + 1 < lim) ? gdpa_act(gelu, v[i + 1]) : 0.f;
+                            const uint32_t u = pack_bf16x2(a0, a1);
+                            pk[i >> 1] = u;
+                            pl[i >> 1] = pack_bf16x2(a0 - __uint_as_float(u << 16), a1 - __uint_as_float(u & 0xffff0000u));
+                        }
+                        tmem_st16(tS + 32u * k, pk);
+                        tmem_st16(tS + 32u * k + 16u, pl);
+                        if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
                     }
                 }
-                // P buffer and O are free once the previous P V product is done.
-                if (j > 0) {
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_O_FULL), pv_wait & 1, abort_flag))) { ok = false; break; }
-                    ++pv_wait;
-                    tc_fence_after();
-                }
+                // O of this tile is stable here: S_x(j) was issued after P_x(j-1) V.
                 if (__any_sync(0xffffffffu, need_rescale)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t r[32];
-                        const uint32_t ta = tmem + lane_base + C::kTmemO + c * 32u;
-                        tmem_ld32(ta, r);
-                        tmem_ld_wait();
+                        tmem_ld32(tO + c * 32u, r);
+                        tmem_ld_wait(r);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(ta, r);
-                    }
-                    tmem_st_wait();
-                }
-                // P row -> shared memory, 128-byte swizzled K-major (bf16).  GDPA also
-                // writes the rounding remainder P - bf16(P) for a second P V product.
-#pragma unroll
-                for (int k = 0; k < C::BN / 8; ++k) {
-                    const uint32_t off = (k >> 3) * (C::BM * 128) + sw128_offset(t, k & 7);
-                    uint32_t u[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) u[e] = pack_bf16x2(x[8 * k + 2 * e], x[8 * k + 2 * e + 1]);
-                    st_shared_v4(sP + off, u[0], u[1], u[2], u[3]);
-                    if (gdpa) {
-                        uint32_t v[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float lo0 = x[8 * k + 2 * e] - __uint_as_float(u[e] << 16);
-                            const float lo1 = x[8 * k + 2 * e + 1] - __uint_as_float(u[e] & 0xffff0000u);
-                            v[e] = pack_bf16x2(lo0, lo1);
-                        }
-                        st_shared_v4(sP2 + off, v[0], v[1], v[2], v[3]);
+                        tmem_st32(tO + c * 32u, r);
                     }
                 }
-                fence_proxy_async_smem();
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_P_FULL));
+                if (lane == 0) mbar_arrive(bar(B_P_FULL + x));
+                ++s_cnt;
             }
             if (!ok) break;
-            // Epilogue: wait for the last P V product, read O, release it.
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_O_FULL), pv_wait & 1, abort_flag))) { ok = false; break; }
-            ++pv_wait;
+            // Epilogue: wait for the tile's last P V product, read O, release it.
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_O_DONE + x), (s_cnt - 1) & 1, abort_flag))) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             {
                 const float inv = (softmax && l > 0.f) ? 1.f / l : (softmax ? 0.f : 1.f);
@@ -464,8 +516,8 @@ __global__ void __launch_bounds__(192, 1)
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
                     float v[32];
-                    tmem_ld32(tmem + lane_base + C::kTmemO + c * 32u, r);
-                    tmem_ld_wait();
+                    tmem_ld32(tO + c * 32u, r);
+                    tmem_ld_wait(r);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * inv;
                     if (row_valid) store_row<OT>(orow_p + c * 32, v, 32);
@@ -473,11 +525,9 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_O_EMPTY));
+            if (lane == 0) mbar_arrive(bar(B_O_EMPTY + x));
             if (row_valid && softmax && p.lse)
                 p.lse[orow] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-            kv_it += n;
-            ++item_it;
         }
         if (!ok) fail();
     }
@@ -485,32 +535,39 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <typename T, int D, typename OT>
-static cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+template <int D, typename OT, bool GDPA>
+static cudaError_t launch_fwd_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const FwdParams& p, int grid, cudaStream_t st) {
-    using C = FwdCfg<T, D>;
+    using C = FwdCfg<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<T, D, OT>,
+        cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, OT, GDPA>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_fwd_kernel<T, D, OT><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, p);
+    jfa_fwd_kernel<D, OT, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
+}
+
+template <int D, typename OT>
+static cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                const FwdParams& p, int grid, cudaStream_t st) {
+    return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false>(tmQ, tmK, tmV, p, grid, st)
+                                 : launch_fwd_m<D, OT, true>(tmQ, tmK, tmV, p, grid, st);
 }
 
 cudaError_t launch_fwd(int dtype, int o_dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const FwdParams& p, int grid, cudaStream_t st) {
     using bf16 = __nv_bfloat16;
     if (dtype != JFA_BF16) return cudaErrorInvalidValue;
-    if (D == 128 && o_dtype == JFA_BF16) return launch_fwd_t<bf16, 128, bf16>(tmQ, tmK, tmV, p, grid, st);
-    if (D == 128 && o_dtype == JFA_F32) return launch_fwd_t<bf16, 128, float>(tmQ, tmK, tmV, p, grid, st);
-    if (D == 64 && o_dtype == JFA_BF16) return launch_fwd_t<bf16, 64, bf16>(tmQ, tmK, tmV, p, grid, st);
-    if (D == 64 && o_dtype == JFA_F32) return launch_fwd_t<bf16, 64, float>(tmQ, tmK, tmV, p, grid, st);
+    if (D == 128 && o_dtype == JFA_BF16) return launch_fwd_t<128, bf16>(tmQ, tmK, tmV, p, grid, st);
+    if (D == 128 && o_dtype == JFA_F32) return launch_fwd_t<128, float>(tmQ, tmK, tmV, p, grid, st);
+    if (D == 64 && o_dtype == JFA_BF16) return launch_fwd_t<64, bf16>(tmQ, tmK, tmV, p, grid, st);
+    if (D == 64 && o_dtype == JFA_F32) return launch_fwd_t<64, float>(tmQ, tmK, tmV, p, grid, st);
     return cudaErrorInvalidValue;
 }
 

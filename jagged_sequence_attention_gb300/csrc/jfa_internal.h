@@ -12,10 +12,12 @@
 
 namespace jfa {
 
-// Forward tiles: 128 query rows x 128 key rows.  Backward tiles: 128 key rows
+// Forward tiles: 128 query rows x 128 key rows, and a forward work item is a pair of
+// query tiles (256 rows) sharing its key/value tiles.  Backward tiles: 128 key rows
 // (resident) x 64 query rows (streamed).
 constexpr int kFwdBM = 128;
 constexpr int kFwdBN = 128;
+constexpr int kFwdPairRows = 2 * kFwdBM;
 constexpr int kBwdBN = 128;
 constexpr int kBwdBM = 64;
 
@@ -25,6 +27,20 @@ struct WorkItem {
     int32_t b, h, tile, n_inner;
 };
 static_assert(sizeof(WorkItem) == 16, "WorkItem must match int4");
+
+// Key tiles a 128-row query tile visits: all of them, or (causal, bottom-right) up
+// to the one holding its last row's diagonal; 0 for a tile past the sequence end.
+__host__ __device__ inline int fwd_tiles_of(int64_t q_len, int64_t kv_len, int64_t tile, int causal) {
+    const int64_t rows0 = tile * kFwdBM;
+    if (rows0 >= q_len) return 0;
+    int64_t n = (kv_len + kFwdBN - 1) / kFwdBN;
+    if (causal) {
+        const int64_t last_row = (q_len < rows0 + kFwdBM ? q_len : rows0 + kFwdBM) - 1;
+        const int64_t max_col = last_row + (kv_len - q_len);
+        n = max_col < 0 ? 0 : (n < max_col / kFwdBN + 1 ? n : max_col / kFwdBN + 1);
+    }
+    return int(n);
+}
 
 // Status bits the kernels OR into the plan's device status word.
 enum : int { kStatusTimeout = 1, kStatusBounds = 2 };

@@ -36,17 +36,6 @@ namespace {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Inner tiles visited by an outer tile; see the comments in build_items.
-inline int64_t fwd_inner(int64_t q_len, int64_t kv_len, int64_t mt, int causal) {
-    int64_t n = ceil_div(kv_len, kFwdBN);
-    if (causal) {
-        const int64_t last_row = std::min(q_len, (mt + 1) * kFwdBM) - 1;
-        const int64_t max_col = last_row + (kv_len - q_len);
-        n = max_col < 0 ? 0 : std::min(n, max_col / kFwdBN + 1);
-    }
-    return n;
-}
-
 inline int64_t bwd_inner(int64_t q_len, int64_t kv_len, int64_t nt, int causal) {
     const int64_t nq = ceil_div(q_len, kBwdBM);
     if (!causal) return nq;
@@ -67,13 +56,15 @@ void build_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t
         const int64_t q_len = q_off[b + 1] - q_off[b];
         const int64_t kv_len = kv_off[b + 1] - kv_off[b];
         if (pass == 0) {
-            // Forward: one item per query tile; it visits key tiles from 0 up to the
-            // causal diagonal of its last row (or all of them).
-            const int64_t nt = ceil_div(q_len, kFwdBM);
+            // Forward: one item per pair of 128-row query tiles; each tile visits key
+            // tiles from 0 up to the causal diagonal of its last row (or all of them),
+            // and the item streams the larger of the two counts.
+            const int64_t np = ceil_div(q_len, kFwdPairRows);
             for (int32_t h = 0; h < H; ++h)
-                for (int64_t t = 0; t < nt; ++t) {
-                    const int64_t n = fwd_inner(q_len, kv_len, t, causal);
-                    out->push_back({{b, h, int32_t(t), int32_t(n)}, 2 * n + 1});
+                for (int64_t t = 0; t < np; ++t) {
+                    const int64_t na = fwd_tiles_of(q_len, kv_len, 2 * t, causal);
+                    const int64_t nb = fwd_tiles_of(q_len, kv_len, 2 * t + 1, causal);
+                    out->push_back({{b, h, int32_t(t), int32_t(na > nb ? na : nb)}, 2 * (na + nb) + 2});
                 }
         } else {
             // Backward: one item per key tile (also when it sees no query, so that
@@ -96,7 +87,7 @@ int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
     int64_t n = 0;
     for (int32_t b = 0; b < B; ++b) {
         const int64_t len = pass == 0 ? q_off[b + 1] - q_off[b] : kv_off[b + 1] - kv_off[b];
-        n += ceil_div(len, pass == 0 ? kFwdBM : kBwdBN) * H;
+        n += ceil_div(len, pass == 0 ? kFwdPairRows : kBwdBN) * H;
     }
     return n;
 }

@@ -75,6 +75,13 @@ WORKLOADS = {
         ("uniform", 4096, 32768), None,
         "64 sequences, lengths U{4096..32768} (~1.2M tokens), causal self-attention, 8 heads, "
         "head_dim 128, bf16, relative-position bias"),
+    # Profiling case: the long-sequence structure at a size one profiler pass covers
+    # quickly, with every input and the dQ accumulator still larger than L2.
+    "long_causal_profile": Workload(
+        "long_causal_profile", 6, 8, 8, 128, torch.bfloat16, "softmax", True, True, 1.0,
+        ("uniform", 6144, 10240), None,
+        "8 sequences, lengths U{6144..10240}, causal self-attention, 8 heads, head_dim 128, bf16, "
+        "relative-position bias (profiling size of the long-sequence workload)"),
 }
 
 

@@ -16,6 +16,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "jfa.h")
 
 BM_FWD, BN_FWD = 128, 128
+PAIR_FWD = 2 * BM_FWD
 BN_BWD, BM_BWD = 128, 64
 
 
@@ -69,6 +70,28 @@ def visited_fwd(q_len, kv_len, t, causal):
     return n
 
 
+def tiles_np(q_len, kv_len, tile, causal):
+    """Vectorised closed form of the forward tile count (checked against the brute
+    force `visited_fwd` in test_tile_count_closed_form)."""
+    q_len, kv_len, tile = (np.asarray(a, dtype=np.int64) for a in (q_len, kv_len, tile))
+    n = (kv_len + BN_FWD - 1) // BN_FWD
+    if causal:
+        last = np.minimum(q_len, (tile + 1) * BM_FWD) - 1
+        max_col = last + kv_len - q_len
+        n = np.where(max_col < 0, 0, np.minimum(n, max_col // BN_FWD + 1))
+    return np.where(tile * BM_FWD < q_len, n, 0)
+
+
+def test_tile_count_closed_form():
+    rng = np.random.default_rng(0)
+    for _ in range(300):
+        q, kv = int(rng.integers(0, 700)), int(rng.integers(0, 700))
+        for t in range(0, 7):
+            for causal in (False, True):
+                want = visited_fwd(q, kv, t, causal) if t * BM_FWD < q else 0
+                assert tiles_np(q, kv, t, causal) == want, (q, kv, t, causal)
+
+
 def visited_bwd(q_len, kv_len, t, causal):
     """Brute force: query tiles (64 rows) with at least one allowed pair for key tile t."""
     cols = range(t * BN_BWD, min(kv_len, (t + 1) * BN_BWD))
@@ -104,11 +127,13 @@ def test_worklist_covers_every_tile_once(jfa, case, causal, pass_, n_ctas):
     expect = {}
     for b in range(len(q)):
         L = q[b] if pass_ == 0 else kv[b]
-        T = BM_FWD if pass_ == 0 else BN_BWD
+        T = PAIR_FWD if pass_ == 0 else BN_BWD
         for h in range(H):
             for t in range((L + T - 1) // T):
                 if pass_ == 0:
-                    expect[(b, h, t)] = visited_fwd(q[b], kv[b], t, causal)
+                    # a pair of query tiles streams the larger of the two tiles' counts
+                    nb = visited_fwd(q[b], kv[b], 2 * t + 1, causal) if (2 * t + 1) * BM_FWD < q[b] else 0
+                    expect[(b, h, t)] = max(visited_fwd(q[b], kv[b], 2 * t, causal), nb)
                 else:
                     n, first = visited_bwd(q[b], kv[b], t, causal)
                     expect[(b, h, t)] = n
@@ -126,7 +151,11 @@ def test_worklist_is_balanced_and_group_major(jfa, name):
     qo, ko = wl.offsets(q), wl.offsets(kv)
     for pass_ in (0, 1):
         items, offs, cost = jfa.jfa_worklist_build(qo, ko, w.H, w.causal, pass_, 148)
-        c = (2 * items[:, 3].astype(np.int64) + 1) if pass_ == 0 else (5 * items[:, 3].astype(np.int64) // 2 + 2)
+        if pass_ == 0:
+            qi, ki, t = q[items[:, 0]], kv[items[:, 0]], items[:, 2].astype(np.int64)
+            c = 2 * (tiles_np(qi, ki, 2 * t, w.causal) + tiles_np(qi, ki, 2 * t + 1, w.causal)) + 2
+        else:
+            c = 5 * items[:, 3].astype(np.int64) // 2 + 2
         gid = items[:, 0].astype(np.int64) * w.H + items[:, 1]
         gcost = {}
         for g, x in zip(gid.tolist(), c.tolist()):

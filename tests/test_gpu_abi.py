@@ -41,7 +41,7 @@ def test_plan_info_and_device_offsets(jfa):
                             4, 128, "softmax", True)
     info = p.info()
     assert info["T_q"] == 303 and info["T_kv"] == 141 and info["B"] == 3 and info["H"] == 4
-    assert info["fwd_items"] == 4 * (1 + 0 + 3) and info["bwd_items"] == 4 * (1 + 1 + 2)
+    assert info["fwd_items"] == 4 * (1 + 0 + 2) and info["bwd_items"] == 4 * (1 + 1 + 2)
     assert 1 <= info["fwd_grid"] <= info["num_sms"]
 
 
