@@ -263,10 +263,15 @@ __global__ void __launch_bounds__(448, 1)
         if (lane == 0) {
             uint32_t step_it = 0, item_it = 0;
             bool ok = true;
-            auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-                if constexpr (sizeof(T) == 2) mma_f16_ss(d, a, b, idesc, acc);
-                else mma_tf32_ss(d, a, b, idesc, acc);
-            };
+            // Descriptors built once; each MMA adds a compile-time byte offset.
+            const SDesc dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
+            const SDesc dQk[2] = {sdesc_sw128(sQ, 16, 1024), sdesc_sw128(sQ + C::kQTile, 16, 1024)};
+            const SDesc dOk[2] = {sdesc_sw128(sDO, 16, 1024), sdesc_sw128(sDO + C::kQTile, 16, 1024)};
+            const SDesc dQm[2] = {sdesc_sw128(sQ, C::BM * 128, 1024), sdesc_sw128(sQ + C::kQTile, C::BM * 128, 1024)};
+            const SDesc dOm[2] = {sdesc_sw128(sDO, C::BM * 128, 1024),
+                                  sdesc_sw128(sDO + C::kQTile, C::BM * 128, 1024)};
+            const SDesc dPt = sdesc_sw128(sPt, 16, 1024), dDSt = sdesc_sw128(sDSt, 16, 1024);
+            const SDesc dKm = sdesc_sw128(sK, C::BN * 128, 1024), dDSm = sdesc_sw128(sDSt, C::BN * 128, 1024);
             for (int it = it_begin; it < it_end && ok; ++it) {
                 const int n = p.items[it].w;
                 if (n == 0) continue;
@@ -278,55 +283,42 @@ __global__ void __launch_bounds__(448, 1)
                         if (!mbar_wait_bounded(bar(C_Q_FULL + st), ph, abort_flag) ||
                             !mbar_wait_bounded(bar(C_S_EMPTY + st), ph ^ 1, abort_flag)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t qb = sQ + st * C::kQTile, dob = sDO + st * C::kQTile;
 #pragma unroll
-                        for (int s = 0; s < C::kDSteps; ++s) {  // S^T = K Q^T
-                            const uint32_t koff = (s * 32) & 127, cb = (s * 32) >> 7;
-                            mma(tmem + C::kTmS + st * 64u, make_sdesc_sw128(sK + cb * C::BN * 128 + koff, 16, 1024),
-                                make_sdesc_sw128(qb + cb * C::BM * 128 + koff, 16, 1024), C::kIdescST, s > 0);
-                        }
+                        for (int s = 0; s < C::kDSteps; ++s)  // S^T = K Q^T
+                            mma_ss(tmem + C::kTmS + st * 64u, dK, ((s * 32) >> 7) * C::BN * 128 + ((s * 32) & 127),
+                                   dQk[st], ((s * 32) >> 7) * C::BM * 128 + ((s * 32) & 127), C::kIdescST, s > 0);
                         tc_commit(bar(C_S_FULL + st));
                         if (!mbar_wait_bounded(bar(C_DP_EMPTY), (g & 1) ^ 1, abort_flag)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
-                        for (int s = 0; s < C::kDSteps; ++s) {  // dP^T = V dO^T
-                            const uint32_t koff = (s * 32) & 127, cb = (s * 32) >> 7;
-                            mma(tmem + C::kTmDP, make_sdesc_sw128(sV + cb * C::BN * 128 + koff, 16, 1024),
-                                make_sdesc_sw128(dob + cb * C::BM * 128 + koff, 16, 1024), C::kIdescST, s > 0);
-                        }
+                        for (int s = 0; s < C::kDSteps; ++s)  // dP^T = V dO^T
+                            mma_ss(tmem + C::kTmDP, dV, ((s * 32) >> 7) * C::BN * 128 + ((s * 32) & 127), dOk[st],
+                                   ((s * 32) >> 7) * C::BM * 128 + ((s * 32) & 127), C::kIdescST, s > 0);
                         tc_commit(bar(C_DP_FULL));
                     }
                     if (i > 0) {
                         const int ii = i - 1;
                         const uint32_t g = step_it + ii, st = g & 1;
-                        const uint32_t qb = sQ + st * C::kQTile, dob = sDO + st * C::kQTile;
                         if (!mbar_wait_bounded(bar(C_PT_FULL), g & 1, abort_flag)) { ok = false; break; }
                         if (ii == 0 && !mbar_wait_bounded(bar(C_ACC_EMPTY), (item_it & 1) ^ 1, abort_flag)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
-                        for (int s = 0; s < C::kQSteps; ++s) {  // dV += P^T dO
-                            const uint32_t koff = (s * 32) & 127, cb = (s * 32) >> 7;
-                            mma(tmem + C::kTmDV, make_sdesc_sw128(sPt + cb * C::BN * 128 + koff, 16, 1024),
-                                make_sdesc_sw128(dob + s * C::kUmmaK * 128, C::BM * 128, 1024), C::kIdescAcc,
-                                (ii > 0 || s > 0));
-                        }
+                        for (int s = 0; s < C::kQSteps; ++s)  // dV += P^T dO
+                            mma_ss(tmem + C::kTmDV, dPt, ((s * 32) >> 7) * C::BN * 128 + ((s * 32) & 127), dOm[st],
+                                   s * C::kUmmaK * 128, C::kIdescAcc, (ii > 0 || s > 0));
                         tc_commit(bar(C_PT_EMPTY));
                         if (!mbar_wait_bounded(bar(C_DS_FULL), g & 1, abort_flag)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
-                        for (int s = 0; s < C::kQSteps; ++s) {  // dK += dS^T Q
-                            const uint32_t koff = (s * 32) & 127, cb = (s * 32) >> 7;
-                            mma(tmem + C::kTmDK, make_sdesc_sw128(sDSt + cb * C::BN * 128 + koff, 16, 1024),
-                                make_sdesc_sw128(qb + s * C::kUmmaK * 128, C::BM * 128, 1024), C::kIdescAcc,
-                                (ii > 0 || s > 0));
-                        }
+                        for (int s = 0; s < C::kQSteps; ++s)  // dK += dS^T Q
+                            mma_ss(tmem + C::kTmDK, dDSt, ((s * 32) >> 7) * C::BN * 128 + ((s * 32) & 127), dQm[st],
+                                   s * C::kUmmaK * 128, C::kIdescAcc, (ii > 0 || s > 0));
                         if (!mbar_wait_bounded(bar(C_DQ_EMPTY), (g & 1) ^ 1, abort_flag)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
-                        for (int s = 0; s < C::kKVSteps; ++s) {  // dQ^T = K^T dS^T
-                            mma(tmem + C::kTmDQ, make_sdesc_sw128(sK + s * C::kUmmaK * 128, C::BN * 128, 1024),
-                                make_sdesc_sw128(sDSt + s * C::kUmmaK * 128, C::BN * 128, 1024), C::kIdescDQ, s > 0);
-                        }
+                        for (int s = 0; s < C::kKVSteps; ++s)  // dQ^T = K^T dS^T
+                            mma_ss(tmem + C::kTmDQ, dKm, s * C::kUmmaK * 128, dDSm, s * C::kUmmaK * 128, C::kIdescDQ,
+                                   s > 0);
                         tc_commit(bar(C_DQ_FULL));
                         tc_commit(bar(C_DS_EMPTY));
                         tc_commit(bar(C_Q_EMPTY + st));

@@ -45,7 +45,10 @@ struct FwdCfg {
     static constexpr int kOffBar = kOffV + kStages * kKVBytes;
     static constexpr int kNumBars = 24;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kMiscBytes = 16 + 2 * 8 * 32 * 4;  // tmem slot, abort flag, bias tables
+    // tmem slot + abort flag; per softmax warp: the head's bias row (32) and a tile's
+    // bias-by-relative-position table (160)
+    static constexpr int kBiasRow = 32, kBiasTab = 160;
+    static constexpr int kMiscBytes = 16 + 8 * (kBiasRow + kBiasTab) * 4;
     static constexpr int kSmemNeed = kOffMisc + kMiscBytes + 1024;
     // At least 120 KB so that exactly one CTA fits on an SM: the CTA allocates all
     // 512 TMEM columns.
@@ -215,20 +218,24 @@ __global__ void __launch_bounds__(320, 1)
             uint32_t kv_it = 0, item_it = 0;
             uint32_t pv_cnt[2] = {0, 0}, items_x[2] = {0, 0};
             bool ok = true;
+            // Descriptors of every operand tile, built once; each MMA below adds a
+            // compile-time byte offset to the low half.
+            const SDesc dQ0 = sdesc_sw128(sQ, 16, 1024), dQ1 = sdesc_sw128(sQ + C::kQBytes, 16, 1024);
+            const SDesc dK0 = sdesc_sw128(sK, 16, 1024), dK1 = sdesc_sw128(sK + C::kKVBytes, 16, 1024);
+            const SDesc dV0 = sdesc_sw128(sV, C::BN * 128, 1024), dV1 = sdesc_sw128(sV + C::kKVBytes, C::BN * 128, 1024);
             // S_x = Q_x K^T into the tile's S columns; first waits for the tile's
             // previous P V product, which reads P from those columns.
             auto issue_s = [&](int x, uint32_t st) -> bool {
                 if (pv_cnt[x] > 0 && !mbar_wait_bounded(bar(B_O_DONE + x), (pv_cnt[x] - 1) & 1, abort_flag))
                     return false;
                 tc_fence_after();
-                const uint32_t kbase = sK + st * C::kKVBytes;
-                const uint32_t qbase = sQ + x * C::kQBytes;
+                const SDesc dq = x ? dQ1 : dQ0, dk = st ? dK1 : dK0;
+                const uint32_t d_tmem = tmem + C::tmem_s(x);
 #pragma unroll
                 for (int s = 0; s < C::kQKSteps; ++s) {
-                    const uint32_t koff = (s * 32) & 127;  // bytes into the 128-byte row
-                    const uint32_t cb = (s * 32) >> 7;     // 128-byte column block
-                    mma_f16_ss(tmem + C::tmem_s(x), make_sdesc_sw128(qbase + cb * C::BM * 128 + koff, 16, 1024),
-                               make_sdesc_sw128(kbase + cb * C::BN * 128 + koff, 16, 1024), C::kIdescQK, s > 0);
+                    // K step s: 128-byte column block (s*32)>>7, (s*32)&127 bytes into the row
+                    mma_ss(d_tmem, dq, ((s * 32) >> 7) * C::BM * 128 + ((s * 32) & 127), dk,
+                           ((s * 32) >> 7) * C::BN * 128 + ((s * 32) & 127), C::kIdescQK, s > 0);
                 }
                 tc_commit(bar(B_S_FULL + x));
                 return true;
@@ -238,20 +245,15 @@ __global__ void __launch_bounds__(320, 1)
                 if (!mbar_wait_bounded(bar(B_P_FULL + x), pv_cnt[x] & 1, abort_flag)) return false;
                 if (first && !mbar_wait_bounded(bar(B_O_EMPTY + x), (items_x[x] & 1) ^ 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t vbase = sV + st * C::kKVBytes;
+                const SDesc dv = st ? dV1 : dV0;
+                const uint32_t d_tmem = tmem + C::tmem_o(x), a_tmem = tmem + C::tmem_s(x);
 #pragma unroll
-                for (int s = 0; s < C::kPVSteps; ++s) {
-                    const uint64_t bd = make_sdesc_sw128(vbase + s * C::kUmmaK * 128, C::BN * 128, 1024);
-                    mma_f16_ts(tmem + C::tmem_o(x), tmem + C::tmem_s(x) + p_col(s), bd, C::kIdescPV,
-                               (!first || s > 0));
-                }
+                for (int s = 0; s < C::kPVSteps; ++s)
+                    mma_ts(d_tmem, a_tmem + p_col(s), dv, s * C::kUmmaK * 128, C::kIdescPV, (!first || s > 0));
                 if (gdpa) {
 #pragma unroll
-                    for (int s = 0; s < C::kPVSteps; ++s) {
-                        const uint64_t bd = make_sdesc_sw128(vbase + s * C::kUmmaK * 128, C::BN * 128, 1024);
-                        mma_f16_ts(tmem + C::tmem_o(x), tmem + C::tmem_s(x) + p_col(s) + 16u, bd,
-                                   C::kIdescPV, 1u);
-                    }
+                    for (int s = 0; s < C::kPVSteps; ++s)
+                        mma_ts(d_tmem, a_tmem + p_col(s) + 16u, dv, s * C::kUmmaK * 128, C::kIdescPV, 1u);
                 }
                 tc_commit(bar(B_O_DONE + x));
                 ++pv_cnt[x];
@@ -323,9 +325,18 @@ __global__ void __launch_bounds__(320, 1)
             const int diag = kv_len - q_len;
             // Each warp keeps its own copy of the head's bias row (log2 units for
             // softmax), double-buffered by item parity, so no cross-warp barrier.
-            float* btab = bias_s + ((it & 1) * 8 + warp) * 32;
+            // Each warp keeps its own copy of the head's bias row (log2 units for
+            // softmax) and its maximum, so no cross-warp barrier is needed.
+            float* btab = bias_s + warp * (C::kBiasRow + C::kBiasTab);
+            float* rtab = btab + C::kBiasRow;
+            float bmax = 0.f;
             if (p.bias) {
-                btab[lane] = p.bias[h * 32 + lane] * (softmax ? 1.4426950408889634f : 1.0f);
+                __syncwarp();
+                const float bv = p.bias[h * 32 + lane] * (softmax ? 1.4426950408889634f : 1.0f);
+                btab[lane] = bv;
+                bmax = bv;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
                 __syncwarp();
             }
             const size_t orow = (size_t(q0) + size_t(row)) * size_t(p.H) + size_t(h);
@@ -352,20 +363,32 @@ __global__ void __launch_bounds__(320, 1)
                 const int rbase = row + diag - col0;  // relative position of column 0
                 const bool full = __all_sync(0xffffffffu, lim >= C::BN);
                 const float xs = softmax ? p.scale_log2 : p.scale;
-                // Bias: one constant per 32-column chunk when the whole chunk sits in one
-                // bucket (warp-uniform), else per element.
-                bool cconst = true;
+                // Bias per 32-column chunk: a constant when every lane's chunk sits in
+                // one bucket (warp-uniform flag per chunk); otherwise read per element
+                // from a table of the bias by relative position built for this tile.
+                uint32_t cmask = 0;  // bit k: chunk k has a constant bias
                 float cb[C::BN / 32];
 #pragma unroll
                 for (int k = 0; k < C::BN / 32; ++k) {
                     int bk = 0;
-                    if (p.bias) cconst &= chunk_bucket_const(rbase - 32 * k, bk);
+                    const bool c = p.bias ? chunk_bucket_const(rbase - 32 * k, bk) : true;
                     cb[k] = p.bias ? btab[bk] : 0.f;
+                    if (__all_sync(0xffffffffu, c)) cmask |= 1u << k;
                 }
-                cconst = __all_sync(0xffffffffu, cconst);
-                // Scaled, biased and masked scores of chunk k minus `shift`.
+                if (cmask != (1u << (C::BN / 32)) - 1) {
+                    // rtab[i] = bias(r) for r = (lane 0's rbase) - 127 + i, i in [0, 160):
+                    // element (lane, c) reads rtab[lane + 127 - c].
+                    const int r0 = __shfl_sync(0xffffffffu, rbase, 0) - (C::BN - 1);
+                    __syncwarp();
+#pragma unroll
+                    for (int m2 = 0; m2 < C::kBiasTab / 32; ++m2)
+                        rtab[lane + 32 * m2] = btab[relpos_bucket(r0 + lane + 32 * m2)];
+                    __syncwarp();
+                }
+                const float* rrow = rtab + lane + (C::BN - 1);  // rrow[-c] = bias of column c
+                // Scaled, biased and masked scores of chunk k, minus `shift`.
                 auto chunk_x = [&](const uint32_t (&r)[32], int k, float shift, float (&v)[32]) {
-                    if (cconst) {
+                    if (cmask & (1u << k)) {
                         const float2 sc = make_float2(xs, xs), add = make_float2(cb[k] - shift, cb[k] - shift);
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
@@ -375,12 +398,12 @@ __global__ void __launch_bounds__(320, 1)
                         }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = fmaf(__uint_as_float(r[i]), xs, btab[relpos_bucket(rbase - 32 * k - i)] - shift);
+                        for (int i = 0; i < 32; ++i) v[i] = fmaf(__uint_as_float(r[i]), xs, rrow[-(32 * k + i)] - shift);
                     }
                     if (!full) {
+                        const int lk = lim - 32 * k;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = (32 * k + i < lim) ? v[i] : -INFINITY;
+                        for (int i = 0; i < 32; ++i) v[i] = (i < lk) ? v[i] : -INFINITY;
                     }
                 };
                 // S streams from TMEM in 32-column chunks; the load of chunk k+1 is in
@@ -391,8 +414,9 @@ __global__ void __launch_bounds__(320, 1)
                 bool need_rescale = false;
                 float alpha = 1.f;
                 if constexpr (softmax) {
-                    // pass 1: row max.  With a constant bias per chunk the max of
-                    // xs * s + cb is xs * max(s) + cb (xs > 0): one FMNMX per element.
+                    // pass 1: an upper bound of the row max from the raw scores (one FMNMX
+                    // per element): xs * max(s) + the chunk's bias (constant, or the
+                    // head's largest).  Any m >= the true max gives the same P / l.
                     float mx = -INFINITY;
                     tmem_ld32(tS, ra);
                     tmem_ld_wait(ra);
@@ -401,27 +425,18 @@ __global__ void __launch_bounds__(320, 1)
                         uint32_t (&cur)[32] = (k & 1) ? rb : ra;
                         uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
                         if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
-                        float mk;
-                        if (cconst) {
-                            float m4[4];
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                        if (full) {
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                m4[e] = (full || 32 * k + e < lim) ? __uint_as_float(cur[e]) : -INFINITY;
-#pragma unroll
-                            for (int i = 4; i < 32; ++i) {
-                                const float si = (full || 32 * k + i < lim) ? __uint_as_float(cur[i]) : -INFINITY;
-                                m4[i & 3] = fmaxf(m4[i & 3], si);
-                            }
-                            mk = fmaf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), xs, cb[k]);
+                            for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(cur[i]));
                         } else {
-                            float v[32];
-                            chunk_x(cur, k, 0.f, v);
-                            float m4[4] = {v[0], v[1], v[2], v[3]};
+                            const int lk = lim - 32 * k;
 #pragma unroll
-                            for (int i = 4; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
-                            mk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                            for (int i = 0; i < 32; ++i)
+                                m4[i & 3] = fmaxf(m4[i & 3], (i < lk) ? __uint_as_float(cur[i]) : -INFINITY);
                         }
-                        mx = fmaxf(mx, mk);
+                        const float mk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                        mx = fmaxf(mx, fmaf(mk, xs, (cmask & (1u << k)) ? cb[k] : bmax));
                         if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
                     }
                     // Lazy rescaling: keep the running max unless it grows by more
@@ -473,8 +488,9 @@ __global__ void __launch_bounds__(320, 1)
                         uint32_t pk[16], pl[16];
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
-                            const float a0 = (full || 32 * k + i < lim) ? gdpa_act(gelu, v[i]) : 0.f;
-                            const float a1 = (full || 32 * k + i + 1 < lim) ? gdpa_act(gelu, v[i + 1]) : 0.f;
+                            // masked entries are -inf here: contribute exactly 0
+                            const float a0 = v[i] == -INFINITY ? 0.f : gdpa_act(gelu, v[i]);
+                            const float a1 = v[i + 1] == -INFINITY ? 0.f : gdpa_act(gelu, v[i + 1]);
                             const uint32_t u = pack_bf16x2(a0, a1);
                             pk[i >> 1] = u;
                             pl[i >> 1] = pack_bf16x2(a0 - __uint_as_float(u << 16), a1 - __uint_as_float(u & 0xffff0000u));

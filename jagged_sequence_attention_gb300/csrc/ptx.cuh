@@ -188,6 +188,40 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
     return d;
 }
 
+// A shared-memory descriptor split into its 32-bit halves.  The start address lives
+// in the low 14 bits (address >> 4), so moving an operand by `bytes` inside shared
+// memory is a single 32-bit add of bytes >> 4 to `lo` (addresses stay below 256 KB,
+// so the field never overflows).
+struct SDesc {
+    uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    const uint64_t d = make_sdesc_sw128(saddr, lbo, sbo);
+    return SDesc{uint32_t(d), uint32_t(d >> 32)};
+}
+
+// MMA issue with descriptors given as (lo + byte offset / 16, hi); the offsets are
+// compile-time constants in the callers' unrolled loops, so each MMA costs an add or
+// two and the instruction itself.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, SDesc a, uint32_t a_off, SDesc b, uint32_t b_off,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a.lo + (a_off >> 4)), "r"(a.hi), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, SDesc b, uint32_t b_off, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc), "r"(accumulate));
+}
+
 // tcgen05.ld 32x32b: thread t of warp w (w = warp index mod 4) reads TMEM lane
 // 32*w + t; .xN reads N consecutive 32-bit columns starting at taddr's column.
 #define JFA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
