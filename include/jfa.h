@@ -53,7 +53,8 @@ typedef enum {
     JFA_ERR_TIMEOUT = 4,        /* a kernel pipeline wait exceeded its limit (device status) */
     JFA_ERR_DEVICE_BOUNDS = 5,  /* a kernel's own bounds check fired (device status) */
     JFA_ERR_PLAN_MISMATCH = 6,  /* the call does not match the plan (mode, head_dim) */
-    JFA_ERR_NO_DEVICE = 7       /* no usable sm_100-family GPU */
+    JFA_ERR_NO_DEVICE = 7,      /* no usable sm_100-family GPU */
+    JFA_ERR_SCRATCH_LIMIT = 8   /* the problem needs more scratch than JFA_STATIC_SCRATCH_BYTES */
 } jfa_status;
 
 typedef enum { JFA_SOFTMAX = 0, JFA_GDPA_GELU_TANH = 1, JFA_GDPA_SILU = 2 } jfa_mode;
@@ -128,6 +129,42 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
                    const void* O, int32_t o_dtype, const void* dO, const float* lse,
                    int32_t bias_kind, const float* bias_table, float scale, void* dQ, void* dK,
                    void* dV, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Size of the library-held scratch array that jfa_bwd_static_scratch uses on each
+ * GPU (64 MiB).  A plan fits when jfa_bwd_workspace_size(plan, dtype) is at most
+ * this: with head_dim 128 that is T_q * H up to about 130,000 (token, head) rows. */
+#define JFA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * jfa_bwd without a caller-supplied workspace, for callers that cannot allocate
+ * device memory at all.  Examples are a host program whose device buffers are all
+ * handed to it by another runtime, or one whose device memory is entirely reserved
+ * by a pool at start-up, where one more cudaMalloc fails or defeats the pool.  The
+ * paper has no counterpart to this call; it exists only for such callers.
+ *   Arguments, layout, results and asynchrony are those of jfa_bwd.  The scratch is
+ *   the library's own JFA_STATIC_SCRATCH_BYTES device array, which every GPU that
+ *   loads the library holds until the process exits.  This call allocates nothing:
+ *   no cudaMalloc, no cudaFree, no allocating library routine.  The plan's timing
+ *   hook, when a caller has switched it on, creates CUDA events as it does for
+ *   jfa_bwd; it is off by default.
+ *   Set-up: the first call on a device, with that device current, looks up the
+ *   array's device address and keeps it for later calls.  That look-up can load
+ *   the library's module on the device, so make the first call before any stream
+ *   capture.
+ *   Every call on a device uses the same array.  Each call clears the dQ
+ *   accumulator on its stream before it adds anything in, so no call depends on
+ *   what an earlier call left there.  Calls that may overlap on the GPU race on the
+ *   array and corrupt each other's dQ: order them on one stream, or by events.
+ *   The current device must be the plan's device.
+ * Errors: SCRATCH_LIMIT when jfa_bwd_workspace_size(plan, dtype) exceeds
+ * JFA_STATIC_SCRATCH_BYTES (checked before anything is launched); PLAN_MISMATCH
+ * when another device is current; CUDA if the address look-up fails; otherwise
+ * those of jfa_bwd.
+ */
+jfa_status jfa_bwd_static_scratch(jfa_plan plan, int32_t dtype, const void* Q, const void* K,
+                                  const void* V, const void* O, int32_t o_dtype, const void* dO,
+                                  const float* lse, int32_t bias_kind, const float* bias_table,
+                                  float scale, void* dQ, void* dK, void* dV, void* stream);
 
 /* Synchronises `stream`, then reads and clears the plan's device status word, which
  * the kernels set when a pipeline wait times out (TIMEOUT) or a bounds check fires

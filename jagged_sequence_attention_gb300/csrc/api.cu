@@ -116,6 +116,7 @@ const char* jfa_status_string(int32_t s) {
         case JFA_ERR_DEVICE_BOUNDS: return "kernel bounds check fired";
         case JFA_ERR_PLAN_MISMATCH: return "call does not match the plan";
         case JFA_ERR_NO_DEVICE: return "no usable sm_100-family GPU";
+        case JFA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the static array holds (JFA_STATIC_SCRATCH_BYTES)";
         default: return "unknown status";
     }
 }

@@ -1,0 +1,66 @@
+// jfa_bwd_static_scratch: the backward pass with its scratch held by the library.
+//
+// jfa_bwd needs scratch: an fp32 dQ accumulator [T_q, H, D], into which every
+// key/value tile adds its share, and the softmax row terms [T_q, H].  Callers of
+// jfa_bwd must pass that scratch in, which some cannot do.  Such callers include
+// host code that owns no device allocator (the memory it works in was handed to it
+// by another runtime), and programs whose device memory is all reserved by a pool
+// set up at start, where a further cudaMalloc fails or breaks the pool's
+// accounting.  For them this entry point keeps the scratch in one fixed-size
+// device array that is part of the library image.  The array is created when the
+// library's module loads on a GPU and stays until the process exits.
+//
+// Set-up: host code cannot use the array's name as a device address, because on the
+// host that name is only a stand-in symbol.  The first call on each device therefore
+// asks the runtime for the array's device address (cudaGetSymbolAddress, with that
+// device current) and remembers it; later calls reuse it.  That first call may load
+// the module on the device, so make it before any stream capture.
+//
+// The launches themselves are those of jfa_bwd, given the array as its workspace:
+// the preprocess clears the dQ accumulator on the stream before anything adds to
+// it, and writes every row term before the main kernel reads one.  So a call never
+// depends on what an earlier call left in the array.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "jfa_internal.h"
+
+// Scratch of every jfa_bwd_static_scratch call on a device (dQ accumulator, then row
+// terms, each starting on a 256-byte boundary as in jfa_bwd's workspace).
+static __device__ __align__(256) unsigned char jfa_static_bwd_scratch[JFA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the array on device `dev` (current); nullptr on failure.
+void* scratch_address(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, jfa_static_bwd_scratch) != cudaSuccess || !ptr) return nullptr;
+        g_scratch_addr[dev] = ptr;
+    }
+    return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" jfa_status jfa_bwd_static_scratch(jfa_plan plan, int32_t dtype, const void* Q, const void* K,
+                                             const void* V, const void* O, int32_t o_dtype, const void* dO,
+                                             const float* lse, int32_t bias_kind, const float* bias_table,
+                                             float scale, void* dQ, void* dK, void* dV, void* stream) {
+    if (!plan || (dtype != JFA_BF16 && dtype != JFA_F32)) return JFA_ERR_INVALID_ARG;
+    if (jfa_bwd_workspace_size(plan, dtype) > JFA_STATIC_SCRATCH_BYTES) return JFA_ERR_SCRATCH_LIMIT;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_NO_DEVICE;
+    if (dev != plan->device) return JFA_ERR_PLAN_MISMATCH;
+    void* scratch = scratch_address(dev);
+    if (!scratch) return JFA_ERR_CUDA;
+    return jfa_bwd(plan, dtype, Q, K, V, O, o_dtype, dO, lse, bias_kind, bias_table, scale, dQ, dK, dV, scratch,
+                   JFA_STATIC_SCRATCH_BYTES, stream);
+}

@@ -19,6 +19,8 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libjfa.so"
 
 JFA_OK, JFA_ERR_INVALID_ARG, JFA_ERR_UNSUPPORTED, JFA_ERR_CUDA = 0, 1, 2, 3
 JFA_ERR_TIMEOUT, JFA_ERR_DEVICE_BOUNDS, JFA_ERR_PLAN_MISMATCH, JFA_ERR_NO_DEVICE = 4, 5, 6, 7
+JFA_ERR_SCRATCH_LIMIT = 8
+JFA_STATIC_SCRATCH_BYTES = 64 << 20
 JFA_SOFTMAX, JFA_GDPA_GELU_TANH, JFA_GDPA_SILU = 0, 1, 2
 JFA_BF16, JFA_F32 = 0, 1
 JFA_BIAS_NONE, JFA_BIAS_RELPOS32 = 0, 1
@@ -28,7 +30,7 @@ DTYPES = {torch.bfloat16: JFA_BF16, torch.float32: JFA_F32}
 
 EXPORTED = ["jfa_plan_create", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd_workspace_size",
             "jfa_bwd", "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build",
-            "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times"]
+            "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times", "jfa_bwd_static_scratch"]
 
 
 class JFAError(RuntimeError):
@@ -56,6 +58,7 @@ def lib():
         L.jfa_bwd_workspace_size.argtypes = [vp, i32]
         L.jfa_bwd_workspace_size.restype = sz
         L.jfa_bwd.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
+        L.jfa_bwd_static_scratch.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp]
         L.jfa_plan_device_status.argtypes = [vp, vp]
         L.jfa_worklist_size.argtypes = [vp, vp, i32, i32, i32, i32, P(i64)]
         L.jfa_worklist_build.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
@@ -65,7 +68,7 @@ def lib():
         L.jfa_status_string.restype = ctypes.c_char_p
         for name in ("jfa_plan_create", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
                      "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build", "jfa_plan_set_timing",
-                     "jfa_plan_kernel_times"):
+                     "jfa_plan_kernel_times", "jfa_bwd_static_scratch"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -201,6 +204,23 @@ def jfa_bwd(plan: Plan, Q, K, V, O, dO, lse, bias=None, scale=None, dQ=None, dK=
     _check("jfa_bwd", lib().jfa_bwd(plan.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _dtype_code(O), _ptr(dO),
                                     _ptr(lse), bk, bp, scale, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dQ, dK, dV
+
+
+def jfa_bwd_static_scratch(plan: Plan, Q, K, V, O, dO, lse, bias=None, scale=None, dQ=None, dK=None, dV=None,
+                           stream=None):
+    """jfa_bwd with the library's static scratch array in place of a workspace, for
+    callers that cannot allocate device memory: pass dQ, dK and dV preallocated and
+    this binding allocates nothing either.  Returns (dQ, dK, dV)."""
+    dt = _dtype_code(Q)
+    scale = 1.0 / float(plan.D) ** 0.5 if scale is None else float(scale)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    bk, bp = _bias_args(bias)
+    _check("jfa_bwd_static_scratch", lib().jfa_bwd_static_scratch(
+        plan.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _dtype_code(O), _ptr(dO), _ptr(lse), bk, bp, scale,
+        _ptr(dQ), _ptr(dK), _ptr(dV), _stream(stream)))
     return dQ, dK, dV
 
 
