@@ -61,10 +61,22 @@ def flops_of(batch):
 
 
 def algorithmic_bytes(batch, elem=2):
+    """Compulsory HBM bytes of one launch of each tensor-core kernel: every input it
+    reads and every output it writes, once."""
     Tq, Tkv, H, D = int(batch.q_off[-1]), int(batch.kv_off[-1]), batch.H, batch.D
-    fwd = elem * H * D * (2 * Tq + 2 * Tkv) + 4 * H * Tq
-    bwd = elem * H * D * (3 * Tq + 4 * Tkv) + 8 * H * Tq
-    return fwd, bwd
+    return {
+        "fwd": elem * H * D * (2 * Tq + 2 * Tkv) + 4 * H * Tq,             # Q,K,V -> O; lse
+        "bwd_main": elem * H * D * (2 * Tq + 4 * Tkv) + 8 * H * Tq,        # Q,dO,K,V -> dK,dV; lse,Delta
+        "bwd_dq": elem * H * D * (3 * Tq + 2 * Tkv) + 8 * H * Tq,          # Q,dO,K,V -> dQ; lse,Delta
+    }
+
+
+def kernel_flops(fwd_flop):
+    """Algorithmic FLOPs per launch of each tensor-core kernel.  The backward's five
+    products (S, dP, dV, dK, dQ; 2.5x the forward's two) split as: dK/dV kernel S, dP,
+    dV, dK (2x), dQ kernel the dQ product (0.5x); its recomputed S and dP are not
+    algorithmic work and are not counted."""
+    return {"fwd": fwd_flop, "bwd_main": 2.0 * fwd_flop, "bwd_dq": 0.5 * fwd_flop}
 
 
 def load_peaks():
@@ -268,7 +280,7 @@ def main():
     seed = wl.seed_of(w) + 7919 * rank
     batch = wl.make(args.workload, device=dev, seed=seed)
     fl_f, fl_b = flops_of(batch)
-    by_f, by_b = algorithmic_bytes(batch)
+    kbytes = algorithmic_bytes(batch)
     cfg.update({"tokens": int(batch.q_off[-1]), "kv_tokens": int(batch.kv_off[-1]),
                 "unpadded_fwd_flop": fl_f, "unpadded_bwd_flop": fl_b})
 
@@ -323,20 +335,22 @@ def main():
     value = world * (fl_f + fl_b) / (ms_step / 1e3) / 1e12
     peaks = load_peaks()
 
-    # dominant kernel: the larger share of device time among the two tensor-core kernels
+    # dominant kernel: the largest share of device time among the tensor-core kernels
     per = {k: (v[0] / v[1] if v[1] else 0.0, v[1], v[0]) for k, v in kt.items()}
-    dom = max(("fwd", "bwd_main"), key=lambda k: per[k][2])
-    dom_flop = fl_f if dom == "fwd" else fl_b
+    kflop = kernel_flops(fl_f)
+    kname_of = {"fwd": "jfa_fwd_kernel", "bwd_main": "jfa_bwd_dkdv_kernel", "bwd_dq": "jfa_bwd_dq_kernel"}
+    dom = max(kname_of, key=lambda k: per[k][2])
     dom_ms = per[dom][0]
-    achieved = dom_flop / (dom_ms / 1e3) / 1e12 if dom_ms > 0 else 0.0
-    kname = {"fwd": "jfa_fwd_kernel", "bwd_main": "jfa_bwd_kernel"}[dom]
+    achieved = kflop[dom] / (dom_ms / 1e3) / 1e12 if dom_ms > 0 else 0.0
+    kname = kname_of[dom]
     roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
                 "peak_kind": f"bf16 dense, sustained, {peaks['source']}", "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops_sustained"],
                 "traffic": measured_traffic(kname, args.workload),
-                "algorithmic_bytes_per_launch": by_f if dom == "fwd" else by_b,
-                "flop_per_launch": dom_flop}
-    kernels = {k: {"ms_per_launch": v[0], "launches": v[1], "share": v[2] / max(1e-9, sum(x[2] for x in per.values()))}
+                "algorithmic_bytes_per_launch": kbytes[dom],
+                "flop_per_launch": kflop[dom]}
+    kernels = {k: {"ms_per_launch": v[0], "launches": v[1], "share": v[2] / max(1e-9, sum(x[2] for x in per.values())),
+                   **({"tflops": kflop[k] / (v[0] / 1e3) / 1e12} if k in kflop and v[0] > 0 else {})}
                for k, v in per.items()}
     launches = int(sum(v[1] for v in per.values()))
 

@@ -65,9 +65,9 @@ typedef struct jfa_plan_t* jfa_plan;
 
 /*
  * Builds the work lists for one batch shape (the planner): validates offsets,
- * splits every (sequence, head) into query tiles (forward) and key/value tiles
- * (backward), costs each tile by the number of score tiles it visits (causal
- * tiles stop at the diagonal), and assigns them longest-first to the least loaded
+ * splits every (sequence, head) into query tiles (forward, backward dQ) and
+ * key/value tiles (backward dK/dV), costs each tile by the tensor-core products it
+ * issues (causal tiles stop at the diagonal), and assigns them longest-first to the least loaded
  * CTA of a persistent grid, so that short sequences never leave SMs idle while a
  * long one finishes (the article's point that padding-free kernels otherwise idle
  * SMs when short sequences end early).
@@ -91,8 +91,8 @@ jfa_status jfa_plan_destroy(jfa_plan plan);
 
 /*
  * Plan facts for callers and tests, written to info[0..n): T_q, T_kv, B, H, D,
- * mode, causal, forward work items, forward grid, backward work items, backward
- * grid, SM count.  n may be smaller than 12.
+ * mode, causal, forward work items, forward grid, backward dK/dV work items, its
+ * grid, SM count, backward dQ work items, its grid.  n may be smaller than 14.
  */
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
 
@@ -111,8 +111,8 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
                    int32_t bias_kind, const float* bias_table, float scale, void* O, int32_t o_dtype,
                    float* lse, void* stream);
 
-/* Bytes of device workspace jfa_bwd needs for this plan and dtype (fp32 dQ
- * accumulator [T_q,H,D] plus fp32 row terms [T_q,H]); 0 on a bad plan. */
+/* Bytes of device workspace jfa_bwd needs for this plan and dtype: fp32 row terms
+ * [T_q,H], and for JFA_F32 also an fp32 dQ accumulator [T_q,H,D]; 0 on a bad plan. */
 size_t jfa_bwd_workspace_size(jfa_plan plan, int32_t dtype);
 
 /*
@@ -132,7 +132,8 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
 
 /* Size of the library-held scratch array that jfa_bwd_static_scratch uses on each
  * GPU (64 MiB).  A plan fits when jfa_bwd_workspace_size(plan, dtype) is at most
- * this: with head_dim 128 that is T_q * H up to about 130,000 (token, head) rows. */
+ * this: T_q * H up to about 16.7 million (token, head) rows for JFA_BF16, and
+ * about 258,000 for JFA_F32 at head_dim 64. */
 #define JFA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 
 /*
@@ -151,10 +152,12 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
  *   array's device address and keeps it for later calls.  That look-up can load
  *   the library's module on the device, so make the first call before any stream
  *   capture.
- *   Every call on a device uses the same array.  Each call clears the dQ
- *   accumulator on its stream before it adds anything in, so no call depends on
+ *   Every call on a device uses the same array.  A call rewrites the row terms
+ *   held there before reading them.  With JFA_F32 it also clears the dQ
+ *   accumulator on its stream before adding anything in.  So no call depends on
  *   what an earlier call left there.  Calls that may overlap on the GPU race on the
- *   array and corrupt each other's dQ: order them on one stream, or by events.
+ *   array and corrupt each other's gradients: order them on one stream, or by
+ *   events.
  *   The current device must be the plan's device.
  * Errors: SCRATCH_LIMIT when jfa_bwd_workspace_size(plan, dtype) exceeds
  * JFA_STATIC_SCRATCH_BYTES (checked before anything is launched); PLAN_MISMATCH
@@ -172,11 +175,12 @@ jfa_status jfa_bwd_static_scratch(jfa_plan plan, int32_t dtype, const void* Q, c
 jfa_status jfa_plan_device_status(jfa_plan plan, void* stream);
 
 /* Host-only planner, usable without a GPU (the same code jfa_plan_create runs).
- * pass 0 = forward (query tiles of 128 rows), 1 = backward (key/value tiles of 128
- * rows).  jfa_worklist_size gives the number of work items; jfa_worklist_build
+ * pass 0 = forward (pairs of 128-row query tiles), 1 = backward dK/dV (key/value
+ * tiles of 128 rows, visiting 128-row query tiles), 2 = backward dQ (128-row query
+ * tiles).  jfa_worklist_size gives the number of work items; jfa_worklist_build
  * writes items as int32 quadruples (sequence, head, tile index, inner tiles
  * visited) grouped by CTA, cta_offsets[n_ctas+1] delimiting each CTA's items, and
- * optionally each CTA's total cost in score-tile units. */
+ * optionally each CTA's total cost in units of tensor-core products. */
 jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
                              int32_t H, int32_t causal, int32_t pass, int64_t* n_items);
 jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
@@ -186,11 +190,11 @@ jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offset
 /* Kernel timing for measurement.  With timing enabled, every kernel launch made for
  * this plan is bracketed by a pair of CUDA events recorded on the launch stream.
  * jfa_plan_kernel_times synchronises those events and returns, per kernel kind
- * (0 forward, 1 backward preprocess, 2 backward main, 3 backward dQ convert), the
- * summed milliseconds and the number of launches since the previous query, then
- * forgets them.  Timing is off by default; enabling it adds one event record before
- * and after each launch.  total_ms and launches point to arrays of 4 (either may be
- * NULL). */
+ * (0 forward, 1 backward preprocess, 2 backward dK/dV (fp32 inputs: backward main),
+ * 3 fp32 dQ conversion, 4 bf16 backward dQ), the summed milliseconds and the number
+ * of launches since the previous query, then forgets them.  Timing is off by
+ * default; enabling it adds one event record before and after each launch.
+ * total_ms and launches point to arrays of 5 (either may be NULL). */
 jfa_status jfa_plan_set_timing(jfa_plan plan, int32_t enable);
 jfa_status jfa_plan_kernel_times(jfa_plan plan, double* total_ms, int64_t* launches);
 

@@ -123,7 +123,7 @@ const char* jfa_status_string(int32_t s) {
 
 jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H,
                              int32_t causal, int32_t pass, int64_t* n_items) {
-    if (!n_items || H < 1 || (pass != 0 && pass != 1)) return JFA_ERR_INVALID_ARG;
+    if (!n_items || H < 1 || pass < kPassFwd || pass > kPassBwdQ) return JFA_ERR_INVALID_ARG;
     jfa_status s = validate_offsets(q_offsets, kv_offsets, B);
     if (s != JFA_OK) return s;
     *n_items = count_items(q_offsets, kv_offsets, B, H, causal, pass);
@@ -133,7 +133,7 @@ jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets
 jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H,
                               int32_t causal, int32_t pass, int32_t n_ctas, int32_t* items,
                               int32_t* cta_offsets, int64_t* cta_cost) {
-    if (H < 1 || n_ctas < 1 || !cta_offsets || (pass != 0 && pass != 1)) return JFA_ERR_INVALID_ARG;
+    if (H < 1 || n_ctas < 1 || !cta_offsets || pass < kPassFwd || pass > kPassBwdQ) return JFA_ERR_INVALID_ARG;
     jfa_status s = validate_offsets(q_offsets, kv_offsets, B);
     if (s != JFA_OK) return s;
     const int64_t n = count_items(q_offsets, kv_offsets, B, H, causal, pass);
@@ -187,15 +187,19 @@ jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, 
     p->kv_off = ko;
     p->timing = false;
 
-    p->n_fwd_items = count_items(qo.data(), ko.data(), B, H, causal, 0);
-    p->n_bwd_items = count_items(qo.data(), ko.data(), B, H, causal, 1);
+    p->n_fwd_items = count_items(qo.data(), ko.data(), B, H, causal, kPassFwd);
+    p->n_bwd_items = count_items(qo.data(), ko.data(), B, H, causal, kPassBwdKV);
+    p->n_dq_items = count_items(qo.data(), ko.data(), B, H, causal, kPassBwdQ);
     p->fwd_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_fwd_items)));
     p->bwd_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_bwd_items)));
+    p->dq_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_dq_items)));
     std::vector<WorkItem> fi(size_t(std::max<int64_t>(1, p->n_fwd_items)));
     std::vector<WorkItem> bi(size_t(std::max<int64_t>(1, p->n_bwd_items)));
-    std::vector<int32_t> fo(size_t(p->fwd_grid) + 1), bo(size_t(p->bwd_grid) + 1);
-    build_worklist(qo.data(), ko.data(), B, H, causal, 0, p->fwd_grid, fi.data(), fo.data(), nullptr);
-    build_worklist(qo.data(), ko.data(), B, H, causal, 1, p->bwd_grid, bi.data(), bo.data(), nullptr);
+    std::vector<WorkItem> qi(size_t(std::max<int64_t>(1, p->n_dq_items)));
+    std::vector<int32_t> fo(size_t(p->fwd_grid) + 1), bo(size_t(p->bwd_grid) + 1), qio(size_t(p->dq_grid) + 1);
+    build_worklist(qo.data(), ko.data(), B, H, causal, kPassFwd, p->fwd_grid, fi.data(), fo.data(), nullptr);
+    build_worklist(qo.data(), ko.data(), B, H, causal, kPassBwdKV, p->bwd_grid, bi.data(), bo.data(), nullptr);
+    build_worklist(qo.data(), ko.data(), B, H, causal, kPassBwdQ, p->dq_grid, qi.data(), qio.data(), nullptr);
 
     // One device block: offsets, status word, work lists (16-byte aligned pieces).
     const size_t off_bytes = round_up((size_t(B) + 1) * 4, 256);
@@ -207,6 +211,8 @@ jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, 
     const size_t o_fo = cur; cur += round_up(fo.size() * 4, 256);
     const size_t o_bi = cur; cur += round_up(bi.size() * 16, 256);
     const size_t o_bo = cur; cur += round_up(bo.size() * 4, 256);
+    const size_t o_qi = cur; cur += round_up(qi.size() * 16, 256);
+    const size_t o_qo = cur; cur += round_up(qio.size() * 4, 256);
     if (cudaMalloc(&p->dev_block, cur) != cudaSuccess) {
         delete p;
         return JFA_ERR_CUDA;
@@ -219,13 +225,17 @@ jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, 
     p->d_fwd_cta_off = reinterpret_cast<int32_t*>(base + o_fo);
     p->d_bwd_items = reinterpret_cast<int4*>(base + o_bi);
     p->d_bwd_cta_off = reinterpret_cast<int32_t*>(base + o_bo);
+    p->d_dq_items = reinterpret_cast<int4*>(base + o_qi);
+    p->d_dq_cta_off = reinterpret_cast<int32_t*>(base + o_qo);
     bool ok = cudaMemcpyAsync(p->d_q_off, qo.data(), qo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
               cudaMemcpyAsync(p->d_kv_off, ko.data(), ko.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
               cudaMemsetAsync(p->d_status, 0, 256, st) == cudaSuccess &&
               cudaMemcpyAsync(p->d_fwd_items, fi.data(), fi.size() * 16, cudaMemcpyHostToDevice, st) == cudaSuccess &&
               cudaMemcpyAsync(p->d_fwd_cta_off, fo.data(), fo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
               cudaMemcpyAsync(p->d_bwd_items, bi.data(), bi.size() * 16, cudaMemcpyHostToDevice, st) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_bwd_cta_off, bo.data(), bo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess;
+              cudaMemcpyAsync(p->d_bwd_cta_off, bo.data(), bo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(p->d_dq_items, qi.data(), qi.size() * 16, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(p->d_dq_cta_off, qio.data(), qio.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess;
     // The host vectors are pageable: the copies above are staged before returning,
     // but keep the stream ordered before the vectors go out of scope.
     if (!ok || cudaStreamSynchronize(st) != cudaSuccess) {
@@ -251,9 +261,10 @@ jfa_status jfa_plan_destroy(jfa_plan plan) {
 
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
     if (!plan || !info || n < 0) return JFA_ERR_INVALID_ARG;
-    const int64_t v[12] = {plan->Tq, plan->Tkv, plan->B, plan->H, plan->D, plan->mode, plan->causal,
-                           plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items, plan->bwd_grid, plan->num_sms};
-    for (int32_t i = 0; i < n && i < 12; ++i) info[i] = v[i];
+    const int64_t v[14] = {plan->Tq,          plan->Tkv,      plan->B,           plan->H,        plan->D,
+                           plan->mode,        plan->causal,   plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items,
+                           plan->bwd_grid,    plan->num_sms,  plan->n_dq_items,  plan->dq_grid};
+    for (int32_t i = 0; i < n && i < 14; ++i) info[i] = v[i];
     return JFA_OK;
 }
 
@@ -265,8 +276,8 @@ jfa_status jfa_plan_set_timing(jfa_plan plan, int32_t enable) {
 
 jfa_status jfa_plan_kernel_times(jfa_plan plan, double* total_ms, int64_t* launches) {
     if (!plan) return JFA_ERR_INVALID_ARG;
-    double t[4] = {0, 0, 0, 0};
-    int64_t n[4] = {0, 0, 0, 0};
+    double t[kNumKernelKinds] = {};
+    int64_t n[kNumKernelKinds] = {};
     jfa_status st = JFA_OK;
     for (auto& pr : plan->ev_pending) {
         float ms = 0.f;
@@ -279,7 +290,7 @@ jfa_status jfa_plan_kernel_times(jfa_plan plan, double* total_ms, int64_t* launc
         plan->ev_pool.push_back(pr.second.second);
     }
     plan->ev_pending.clear();
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kNumKernelKinds; ++i) {
         if (total_ms) total_ms[i] = t[i];
         if (launches) launches[i] = n[i];
     }
@@ -342,7 +353,8 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
 size_t jfa_bwd_workspace_size(jfa_plan plan, int32_t dtype) {
     if (!plan || (dtype != JFA_BF16 && dtype != JFA_F32)) return 0;
     const size_t rows = size_t(plan->Tq) * size_t(plan->H);
-    return round_up(rows * size_t(plan->D) * 4, 256) + round_up(rows * 4, 256);
+    // row terms; fp32 inputs also accumulate dQ in fp32 before converting it
+    return round_up(rows * 4, 256) + (dtype == JFA_F32 ? round_up(rows * size_t(plan->D) * 4, 256) : 0);
 }
 
 jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, const void* V, const void* O,
@@ -365,8 +377,9 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
     if (plan->Tkv == 0 && plan->Tq == 0) return JFA_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t rows = size_t(plan->Tq) * size_t(plan->H);
-    float* dq_acc = static_cast<float*>(workspace);
-    float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * size_t(plan->D) * 4, 256));
+    float* delta = static_cast<float*>(workspace);
+    float* dq_acc = dtype == JFA_F32 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * 4, 256))
+                                     : nullptr;
 
     cudaError_t e = cudaSuccess;
     if (plan->Tq > 0) {
@@ -375,15 +388,15 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
         tm.done();
         if (e != cudaSuccess) return JFA_ERR_CUDA;
     }
-    if (plan->n_bwd_items > 0) {
-        CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo;
+    BwdParams p;
+    if (plan->n_bwd_items > 0 || (dtype == JFA_BF16 && plan->n_dq_items > 0)) {
         if (dtype == JFA_BF16 &&
             ((s = make_map(&mq, dtype, Q, plan->Tq, plan->H, plan->D, plan->dev_block, kBwdBM)) != JFA_OK ||
              (s = make_map(&mk, dtype, K, plan->Tkv, plan->H, plan->D, plan->dev_block, kBwdBN)) != JFA_OK ||
              (s = make_map(&mv, dtype, V, plan->Tkv, plan->H, plan->D, plan->dev_block, kBwdBN)) != JFA_OK ||
              (s = make_map(&mdo, dtype, dO, plan->Tq, plan->H, plan->D, plan->dev_block, kBwdBM)) != JFA_OK))
             return s;
-        BwdParams p;
         p.items = plan->d_bwd_items;
         p.cta_off = plan->d_bwd_cta_off;
         p.q_off = plan->d_q_off;
@@ -397,16 +410,28 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
         p.lse = softmax ? lse : nullptr;
         p.delta = delta;
         p.dq_acc = dq_acc;
+        p.dQ = dQ;
         p.dK = dK;
         p.dV = dV;
         p.status = plan->d_status;
+    }
+    if (plan->n_bwd_items > 0) {
         KernelTimer tm(plan, 2, st);
         e = dtype == JFA_BF16 ? launch_bwd_main(dtype, plan->D, mq, mk, mv, mdo, p, plan->bwd_grid, st)
                               : launch_bwd_f32(plan->D, Q, K, V, dO, p, plan->n_bwd_items, st);
         tm.done();
         if (e != cudaSuccess) return JFA_ERR_CUDA;
     }
-    if (plan->Tq > 0) {
+    if (dtype == JFA_BF16 && plan->n_dq_items > 0) {
+        // dQ per query tile, written directly (also the zero rows of tiles that see no key)
+        p.items = plan->d_dq_items;
+        p.cta_off = plan->d_dq_cta_off;
+        KernelTimer tm(plan, 4, st);
+        e = launch_bwd_dq(dtype, plan->D, mq, mk, mv, mdo, p, plan->dq_grid, st);
+        tm.done();
+        if (e != cudaSuccess) return JFA_ERR_CUDA;
+    }
+    if (dtype == JFA_F32 && plan->Tq > 0) {
         KernelTimer tm(plan, 3, st);
         e = launch_bwd_post(dtype, plan->D, dq_acc, dQ, plan->Tq, plan->H, scale, st);
         tm.done();

@@ -13,13 +13,22 @@
 namespace jfa {
 
 // Forward tiles: 128 query rows x 128 key rows, and a forward work item is a pair of
-// query tiles (256 rows) sharing its key/value tiles.  Backward tiles: 128 key rows
-// (resident) x 64 query rows (streamed).
+// query tiles (256 rows) sharing its key/value tiles.  Backward dK/dV tiles: 128 key
+// rows (resident) x 128 query rows (streamed); backward dQ tiles: 128 query rows
+// (resident) x 128 key rows (streamed), the forward's single-tile geometry.
 constexpr int kFwdBM = 128;
 constexpr int kFwdBN = 128;
 constexpr int kFwdPairRows = 2 * kFwdBM;
 constexpr int kBwdBN = 128;
-constexpr int kBwdBM = 64;
+constexpr int kBwdBM = 128;
+
+// Work-list passes: forward query-tile pairs, backward key tiles (dK/dV), backward
+// query tiles (dQ).
+enum : int { kPassFwd = 0, kPassBwdKV = 1, kPassBwdQ = 2 };
+
+// Kernel kinds of the timing hook: forward, backward preprocess, backward dK/dV (or
+// the fp32 main kernel), fp32 dQ conversion, bf16 dQ.
+constexpr int kNumKernelKinds = 5;
 
 // One unit of persistent-grid work: sequence, head, tile index (query tile for the
 // forward, key/value tile for the backward) and the number of inner tiles visited.
@@ -74,7 +83,8 @@ struct BwdParams {
     const float* bias;
     const float* lse;    // [T_q,H] (softmax)
     const float* delta;  // [T_q,H] rowsum(dO*O) (softmax)
-    float* dq_acc;       // [T_q,H,D] fp32, zeroed by the preprocess kernel
+    float* dq_acc;       // [T_q,H,D] fp32, zeroed by the preprocess kernel (fp32 inputs only)
+    void* dQ;            // [T_q,H,D] (bf16 inputs: written by the dQ kernel)
     void* dK;
     void* dV;
     int* status;
@@ -88,7 +98,7 @@ void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
                     int32_t causal, int32_t pass, int32_t n_ctas, WorkItem* items,
                     int32_t* cta_off, int64_t* cta_cost);
 
-// Kernel launchers (fwd.cu, bwd.cu).  Return cudaSuccess or the launch error.
+// Kernel launchers (fwd.cu, bwd.cu, bwd_dq.cu).  Return cudaSuccess or the launch error.
 cudaError_t launch_fwd(int dtype, int o_dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const FwdParams& p, int grid, cudaStream_t st);
 cudaError_t launch_bwd_pre(int dtype, int o_dtype, int D, const void* O, const void* dO, float* delta,
@@ -96,6 +106,9 @@ cudaError_t launch_bwd_pre(int dtype, int o_dtype, int D, const void* O, const v
 cudaError_t launch_bwd_main(int dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdParams& p,
                             int grid, cudaStream_t st);
+cudaError_t launch_bwd_dq(int dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdParams& p,
+                          int grid, cudaStream_t st);
 cudaError_t launch_bwd_post(int dtype, int D, const float* dq_acc, void* dQ, int64_t Tq, int H,
                             float scale, cudaStream_t st);
 
@@ -123,8 +136,10 @@ struct jfa_plan_t {
     int32_t* d_fwd_cta_off;
     int4* d_bwd_items;
     int32_t* d_bwd_cta_off;
-    int64_t n_fwd_items, n_bwd_items;
-    int fwd_grid, bwd_grid;
+    int4* d_dq_items;
+    int32_t* d_dq_cta_off;
+    int64_t n_fwd_items, n_bwd_items, n_dq_items;
+    int fwd_grid, bwd_grid, dq_grid;
     // optional per-kernel timing (jfa_plan_set_timing)
     bool timing;
     std::vector<cudaEvent_t> ev_pool;                 // reusable events

@@ -5,13 +5,13 @@
 // become the bottleneck (vibekk.com GEM article, section 第一轮瓶颈迁移: short sequences
 // finish early, long ones keep computing; aihot.vn article, "Jagged Sequence Flash
 // Attention": padding-free kernels otherwise leave SMs idle).  Each (sequence, head,
-// tile) is costed by the score tiles it visits.  Items are listed group by group --
+// tile) is costed by the tensor-core products it issues.  Items are listed group by group --
 // a group is one (sequence, head), the largest groups first and, inside a group, the
 // costliest tiles first -- and each item goes to the CTA with the least accumulated
 // cost (greedy list scheduling).  Greedy assignment keeps every CTA within one item
 // of the least loaded one, and because CTAs then run their items in list order, the
-// tiles in flight at any moment belong to a few groups: their K/V (forward) or Q,
-// dO and dQ accumulator rows (backward) stay in L2 instead of being re-read from HBM.
+// tiles in flight at any moment belong to a few groups: their K/V (forward, dQ) or
+// Q and dO rows (dK/dV) stay in L2 instead of being re-read from HBM.
 #include <algorithm>
 #include <cstring>
 #include <numeric>
@@ -66,14 +66,25 @@ void build_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t
                     const int64_t nb = fwd_tiles_of(q_len, kv_len, 2 * t + 1, causal);
                     out->push_back({{b, h, int32_t(t), int32_t(na > nb ? na : nb)}, 2 * (na + nb) + 2});
                 }
-        } else {
-            // Backward: one item per key tile (also when it sees no query, so that
-            // its dK/dV rows are written); it visits the last n query tiles.
+        } else if (pass == kPassBwdKV) {
+            // Backward dK/dV: one item per key tile (also when it sees no query, so
+            // that its dK/dV rows are written); it visits the last n query tiles, four
+            // products each.
             const int64_t nt = ceil_div(kv_len, kBwdBN);
             for (int32_t h = 0; h < H; ++h)
                 for (int64_t t = 0; t < nt; ++t) {
                     const int64_t n = bwd_inner(q_len, kv_len, t, causal);
-                    out->push_back({{b, h, int32_t(t), int32_t(n)}, 5 * n / 2 + 2});
+                    out->push_back({{b, h, int32_t(t), int32_t(n)}, 4 * n + 2});
+                }
+        } else {
+            // Backward dQ: one item per 128-row query tile (also when it sees no key, so
+            // that its dQ rows are written); it visits the forward's key tiles, three
+            // products each.
+            const int64_t nt = ceil_div(q_len, kFwdBM);
+            for (int32_t h = 0; h < H; ++h)
+                for (int64_t t = 0; t < nt; ++t) {
+                    const int64_t n = fwd_tiles_of(q_len, kv_len, t, causal);
+                    out->push_back({{b, h, int32_t(t), int32_t(n)}, 3 * n + 2});
                 }
         }
     }
@@ -86,8 +97,9 @@ int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
     (void)causal;
     int64_t n = 0;
     for (int32_t b = 0; b < B; ++b) {
-        const int64_t len = pass == 0 ? q_off[b + 1] - q_off[b] : kv_off[b + 1] - kv_off[b];
-        n += ceil_div(len, pass == 0 ? kFwdPairRows : kBwdBN) * H;
+        const int64_t len = pass == kPassBwdKV ? kv_off[b + 1] - kv_off[b] : q_off[b + 1] - q_off[b];
+        const int64_t tile = pass == kPassFwd ? kFwdPairRows : pass == kPassBwdKV ? kBwdBN : kFwdBM;
+        n += ceil_div(len, tile) * H;
     }
     return n;
 }

@@ -1,8 +1,8 @@
 // jfa_bwd_static_scratch: the backward pass with its scratch held by the library.
 //
-// jfa_bwd needs scratch: an fp32 dQ accumulator [T_q, H, D], into which every
-// key/value tile adds its share, and the softmax row terms [T_q, H].  Callers of
-// jfa_bwd must pass that scratch in, which some cannot do.  Such callers include
+// jfa_bwd needs scratch: the softmax row terms [T_q, H], and for fp32 inputs an fp32
+// dQ accumulator [T_q, H, D] into which every key/value tile adds its share.
+// Callers of jfa_bwd must pass that scratch in, which some cannot do.  Such callers include
 // host code that owns no device allocator (the memory it works in was handed to it
 // by another runtime), and programs whose device memory is all reserved by a pool
 // set up at start, where a further cudaMalloc fails or breaks the pool's
@@ -17,17 +17,18 @@
 // the module on the device, so make it before any stream capture.
 //
 // The launches themselves are those of jfa_bwd, given the array as its workspace:
-// the preprocess clears the dQ accumulator on the stream before anything adds to
-// it, and writes every row term before the main kernel reads one.  So a call never
-// depends on what an earlier call left in the array.
+// the preprocess writes every row term before a later kernel reads one and, for
+// fp32 inputs, clears the dQ accumulator on the stream before anything adds to it.
+// So a call never depends on what an earlier call left in the array.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "jfa_internal.h"
 
-// Scratch of every jfa_bwd_static_scratch call on a device (dQ accumulator, then row
-// terms, each starting on a 256-byte boundary as in jfa_bwd's workspace).
+// Scratch of every jfa_bwd_static_scratch call on a device (row terms, then for fp32
+// inputs the dQ accumulator, each starting on a 256-byte boundary as in jfa_bwd's
+// workspace).
 static __device__ __align__(256) unsigned char jfa_static_bwd_scratch[JFA_STATIC_SCRATCH_BYTES];
 
 namespace {

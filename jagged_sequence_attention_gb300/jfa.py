@@ -149,7 +149,7 @@ def jfa_plan_destroy(plan: Plan):
 
 
 INFO_KEYS = ["T_q", "T_kv", "B", "H", "D", "mode", "causal", "fwd_items", "fwd_grid", "bwd_items", "bwd_grid",
-             "num_sms"]
+             "num_sms", "dq_items", "dq_grid"]
 
 
 def jfa_plan_info(plan: Plan) -> dict:
@@ -228,7 +228,7 @@ def jfa_plan_device_status(plan: Plan, stream=None) -> int:
     return int(lib().jfa_plan_device_status(plan.handle, _stream(stream)))
 
 
-KERNEL_KINDS = ["fwd", "bwd_pre", "bwd_main", "bwd_post"]
+KERNEL_KINDS = ["fwd", "bwd_pre", "bwd_main", "bwd_post", "bwd_dq"]
 
 
 def jfa_plan_set_timing(plan: Plan, enable: bool = True):
@@ -237,8 +237,8 @@ def jfa_plan_set_timing(plan: Plan, enable: bool = True):
 
 def jfa_plan_kernel_times(plan: Plan) -> dict:
     """{kind: (total_ms, launches)} since the previous query (synchronises)."""
-    ms = (ctypes.c_double * 4)()
-    n = (ctypes.c_int64 * 4)()
+    ms = (ctypes.c_double * len(KERNEL_KINDS))()
+    n = (ctypes.c_int64 * len(KERNEL_KINDS))()
     _check("jfa_plan_kernel_times", lib().jfa_plan_kernel_times(plan.handle, ms, n))
     return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KERNEL_KINDS)}
 

@@ -17,7 +17,7 @@ HEADER = os.path.join(ROOT, "include", "jfa.h")
 
 BM_FWD, BN_FWD = 128, 128
 PAIR_FWD = 2 * BM_FWD
-BN_BWD, BM_BWD = 128, 64
+BN_BWD, BM_BWD = 128, 128
 
 
 @pytest.fixture(scope="module")
@@ -93,7 +93,7 @@ def test_tile_count_closed_form():
 
 
 def visited_bwd(q_len, kv_len, t, causal):
-    """Brute force: query tiles (64 rows) with at least one allowed pair for key tile t."""
+    """Brute force: query tiles (128 rows) with at least one allowed pair for key tile t."""
     cols = range(t * BN_BWD, min(kv_len, (t + 1) * BN_BWD))
     tiles = set()
     for r in range(q_len):
@@ -116,7 +116,7 @@ CASES = [
 
 @pytest.mark.parametrize("case", range(len(CASES)))
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("pass_", [0, 1])
+@pytest.mark.parametrize("pass_", [0, 1, 2])
 @pytest.mark.parametrize("n_ctas", [1, 3, 148])
 def test_worklist_covers_every_tile_once(jfa, case, causal, pass_, n_ctas):
     q, kv = CASES[case]
@@ -126,11 +126,14 @@ def test_worklist_covers_every_tile_once(jfa, case, causal, pass_, n_ctas):
     assert offs[0] == 0 and offs[-1] == len(items) and np.all(np.diff(offs) >= 0)
     expect = {}
     for b in range(len(q)):
-        L = q[b] if pass_ == 0 else kv[b]
-        T = PAIR_FWD if pass_ == 0 else BN_BWD
+        L = kv[b] if pass_ == 1 else q[b]
+        T = {0: PAIR_FWD, 1: BN_BWD, 2: BM_FWD}[pass_]
         for h in range(H):
             for t in range((L + T - 1) // T):
-                if pass_ == 0:
+                if pass_ == 2:
+                    # dQ: one query tile, the forward's key tiles
+                    expect[(b, h, t)] = visited_fwd(q[b], kv[b], t, causal)
+                elif pass_ == 0:
                     # a pair of query tiles streams the larger of the two tiles' counts
                     nb = visited_fwd(q[b], kv[b], 2 * t + 1, causal) if (2 * t + 1) * BM_FWD < q[b] else 0
                     expect[(b, h, t)] = max(visited_fwd(q[b], kv[b], 2 * t, causal), nb)
@@ -149,13 +152,17 @@ def test_worklist_is_balanced_and_group_major(jfa, name):
     w = wl.WORKLOADS[name]
     q, kv = wl.lengths(w)
     qo, ko = wl.offsets(q), wl.offsets(kv)
-    for pass_ in (0, 1):
+    for pass_ in (0, 1, 2):
         items, offs, cost = jfa.jfa_worklist_build(qo, ko, w.H, w.causal, pass_, 148)
         if pass_ == 0:
             qi, ki, t = q[items[:, 0]], kv[items[:, 0]], items[:, 2].astype(np.int64)
             c = 2 * (tiles_np(qi, ki, 2 * t, w.causal) + tiles_np(qi, ki, 2 * t + 1, w.causal)) + 2
+        elif pass_ == 1:
+            c = 4 * items[:, 3].astype(np.int64) + 2
         else:
-            c = 5 * items[:, 3].astype(np.int64) // 2 + 2
+            qi, ki, t = q[items[:, 0]], kv[items[:, 0]], items[:, 2].astype(np.int64)
+            assert np.array_equal(items[:, 3], tiles_np(qi, ki, t, w.causal))
+            c = 3 * items[:, 3].astype(np.int64) + 2
         gid = items[:, 0].astype(np.int64) * w.H + items[:, 1]
         gcost = {}
         for g, x in zip(gid.tolist(), c.tolist()):

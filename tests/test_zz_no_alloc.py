@@ -65,16 +65,22 @@ def test_static_scratch_matches_jfa_bwd_on_consecutive_calls(jfa, mode, causal, 
 
 
 def test_static_scratch_refuses_problems_beyond_its_size(jfa):
-    # T_q * H * D * 4 bytes of dQ accumulator alone exceed the array by a little.
-    D, H = 128, 1
+    # fp32 inputs keep an fp32 dQ accumulator in the scratch: T_q * H * D * 4 bytes of it
+    # alone exceed the array by a little.
+    D, H = 64, 1
     tq = jfa.JFA_STATIC_SCRATCH_BYTES // (4 * D * H) + 64
-    b = wl.make_custom([tq], [tq], H=H, D=D, dtype=torch.bfloat16, device="cuda", seed=5)
+    b = wl.make_custom([tq], [tq], H=H, D=D, dtype=torch.float32, device="cuda", seed=5)
     plan = jfa.jfa_plan_create(b.q_off, b.kv_off, H, D, "softmax", False)
-    assert jfa.jfa_bwd_workspace_size(plan) > jfa.JFA_STATIC_SCRATCH_BYTES
+    assert jfa.jfa_bwd_workspace_size(plan, torch.float32) > jfa.JFA_STATIC_SCRATCH_BYTES
     O = torch.zeros(b.Q.shape, dtype=torch.float32, device="cuda")
     lse = torch.zeros((tq, H), dtype=torch.float32, device="cuda")
     dQ, dK, dV = (torch.zeros_like(t) for t in (b.Q, b.K, b.V))
-    assert _static_call(jfa, plan, b, O, lse, dQ, dK, dV) == jfa.JFA_ERR_SCRATCH_LIMIT
+    L = jfa.lib()
+    st = L.jfa_bwd_static_scratch(plan.handle, jfa.JFA_F32, jfa._ptr(b.Q), jfa._ptr(b.K), jfa._ptr(b.V),
+                                  jfa._ptr(O), jfa.JFA_F32, jfa._ptr(b.dO), jfa._ptr(lse), jfa.JFA_BIAS_NONE,
+                                  None, ctypes.c_float(b.scale), jfa._ptr(dQ), jfa._ptr(dK), jfa._ptr(dV),
+                                  jfa._stream())
+    assert st == jfa.JFA_ERR_SCRATCH_LIMIT
     assert "scratch" in jfa.jfa_status_string(jfa.JFA_ERR_SCRATCH_LIMIT)
     torch.cuda.synchronize()
     assert torch.count_nonzero(dQ) == 0 and torch.count_nonzero(dK) == 0
