@@ -61,8 +61,11 @@ struct KvCfg {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kCompWarps = 8;
     static constexpr int kCols = BM / 2;  // query columns per compute thread
-    // tmem slot + abort flag (16 B); per compute warp: lse and Delta of its columns, bias row
-    static constexpr int kMiscBytes = 16 + kCompWarps * (2 * kCols + 32) * 4;
+    // tmem slot + abort flag (16 B); per compute warp: -lse and -Delta of its columns, the
+    // head's bias row, and a step's bias-by-relative-position table (kCols + 32 entries)
+    static constexpr int kRelTab = kCols + 32;
+    static constexpr int kWarpMisc = 2 * kCols + 32 + kRelTab;
+    static constexpr int kMiscBytes = 16 + kCompWarps * kWarpMisc * 4;
     static constexpr int kSmemNeed = kOffMisc + kMiscBytes + 1024;
     // At least 120 KB so that exactly one CTA fits on an SM: it allocates all 512 TMEM columns.
     static constexpr int kSmemBytes = kSmemNeed > 120 * 1024 ? kSmemNeed : 120 * 1024;
@@ -211,98 +214,116 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t step_it = 0, item_it = 0, dv_cnt = 0, dk_cnt = 0;
-            bool ok = true;
-            const SDesc dKa = sdesc_sw128(sK, 16, 1024), dVa = sdesc_sw128(sV, 16, 1024);
-            const SDesc dQk[2] = {sdesc_sw128(sQ, 16, 1024), sdesc_sw128(sQ + C::kQTile, 16, 1024)};
-            const SDesc dOk[2] = {sdesc_sw128(sDO, 16, 1024), sdesc_sw128(sDO + C::kQTile, 16, 1024)};
-            const SDesc dQm[2] = {sdesc_sw128(sQ, C::BM * 128, 1024), sdesc_sw128(sQ + C::kQTile, C::BM * 128, 1024)};
-            const SDesc dOm[2] = {sdesc_sw128(sDO, C::BM * 128, 1024),
-                                  sdesc_sw128(sDO + C::kQTile, C::BM * 128, 1024)};
-            // K step s of a head_dim contraction: 128-byte column block (s*32)>>7,
-            // (s*32)&127 bytes into the row; both operands have 128 rows.
-            auto koff = [](int s) -> uint32_t { return uint32_t(((s * 32) >> 7) * 128 * 128 + ((s * 32) & 127)); };
-            // S^T(g) = K Q^T into the S^T columns, once dV of the previous step has read P^T there.
-            auto issue_s = [&](uint32_t g) -> bool {
-                const uint32_t st = g & 1, ph = (g >> 1) & 1;
-                if (!mbar_wait_bounded(bar(KV_Q_FULL + st), ph, abort_flag)) return false;
-                if (dv_cnt > 0 && !mbar_wait_bounded(bar(KV_X_FREE), (dv_cnt - 1) & 1, abort_flag)) return false;
-                tc_fence_after();
+        // The whole warp runs the schedule, so descriptors and counters stay
+        // warp-uniform; one elected lane (always lane 0) issues every MMA and commit.
+        uint32_t step_it = 0, item_it = 0, dv_cnt = 0, dk_cnt = 0;
+        bool ok = true;
+        const SDesc dKa = sdesc_sw128(sK, 16, 1024), dVa = sdesc_sw128(sV, 16, 1024);
+        // Descriptors of both ring stages, selected by value (no indexed array, which
+        // would live in local memory).
+        const SDesc dQk0 = sdesc_sw128(sQ, 16, 1024), dQk1 = sdesc_sw128(sQ + C::kQTile, 16, 1024);
+        const SDesc dOk0 = sdesc_sw128(sDO, 16, 1024), dOk1 = sdesc_sw128(sDO + C::kQTile, 16, 1024);
+        const SDesc dQm0 = sdesc_sw128(sQ, C::BM * 128, 1024), dQm1 = sdesc_sw128(sQ + C::kQTile, C::BM * 128, 1024);
+        const SDesc dOm0 = sdesc_sw128(sDO, C::BM * 128, 1024), dOm1 = sdesc_sw128(sDO + C::kQTile, C::BM * 128, 1024);
+        // K step s of a head_dim contraction: 128-byte column block (s*32)>>7,
+        // (s*32)&127 bytes into the row; both operands have 128 rows.
+        auto koff = [](int s) -> uint32_t { return uint32_t(((s * 32) >> 7) * 128 * 128 + ((s * 32) & 127)); };
+        // S^T(g) = K Q^T into the S^T columns, once dV of the previous step has read P^T there.
+        auto issue_s = [&](uint32_t g) -> bool {
+            const uint32_t st = g & 1, ph = (g >> 1) & 1;
+            if (!warp_wait(KV_Q_FULL + st, ph)) return false;
+            if (dv_cnt > 0 && !warp_wait(KV_X_FREE, (dv_cnt - 1) & 1)) return false;
+            tc_fence_after();
+            const SDesc dq = st ? dQk1 : dQk0;
+            if (elect_one()) {
 #pragma unroll
-                for (int s = 0; s < C::kDSteps; ++s)
-                    mma_ss(tmem + C::kTmX, dKa, koff(s), dQk[st], koff(s), C::kIdescS, s > 0);
+                for (int s = 0; s < C::kDSteps; ++s) mma_ss(tmem + C::kTmX, dKa, koff(s), dq, koff(s), C::kIdescS, s > 0);
                 tc_commit(bar(KV_S_FULL));
-                return true;
-            };
-            // dP^T(g) = V dO^T into the dP^T columns, once dK of the previous step has read dS^T there.
-            auto issue_dp = [&](uint32_t g) -> bool {
-                const uint32_t st = g & 1, ph = (g >> 1) & 1;
-                if (!mbar_wait_bounded(bar(KV_DO_FULL + st), ph, abort_flag)) return false;
-                if (dk_cnt > 0 && !mbar_wait_bounded(bar(KV_Y_FREE), (dk_cnt - 1) & 1, abort_flag)) return false;
-                tc_fence_after();
+            }
+            __syncwarp();
+            return true;
+        };
+        // dP^T(g) = V dO^T into the dP^T columns, once dK of the previous step has read dS^T there.
+        auto issue_dp = [&](uint32_t g) -> bool {
+            const uint32_t st = g & 1, ph = (g >> 1) & 1;
+            if (!warp_wait(KV_DO_FULL + st, ph)) return false;
+            if (dk_cnt > 0 && !warp_wait(KV_Y_FREE, (dk_cnt - 1) & 1)) return false;
+            tc_fence_after();
+            const SDesc dO = st ? dOk1 : dOk0;
+            if (elect_one()) {
 #pragma unroll
-                for (int s = 0; s < C::kDSteps; ++s)
-                    mma_ss(tmem + C::kTmY, dVa, koff(s), dOk[st], koff(s), C::kIdescS, s > 0);
+                for (int s = 0; s < C::kDSteps; ++s) mma_ss(tmem + C::kTmY, dVa, koff(s), dO, koff(s), C::kIdescS, s > 0);
                 tc_commit(bar(KV_DP_FULL));
-                return true;
-            };
-            // dV += P^T dO with P^T read from TMEM; the first step of an item waits for
-            // the epilogue of the previous item to have read the accumulators.
-            auto issue_dv = [&](uint32_t g, bool first) -> bool {
-                const uint32_t st = g & 1;
-                if (!mbar_wait_bounded(bar(KV_P_FULL), g & 1, abort_flag)) return false;
-                if (first && !mbar_wait_bounded(bar(KV_ACC_EMPTY), (item_it & 1) ^ 1, abort_flag)) return false;
-                tc_fence_after();
+            }
+            __syncwarp();
+            return true;
+        };
+        // dV += P^T dO with P^T read from TMEM; the first step of an item waits for
+        // the epilogue of the previous item to have read the accumulators.
+        auto issue_dv = [&](uint32_t g, bool first) -> bool {
+            const uint32_t st = g & 1;
+            if (!warp_wait(KV_P_FULL, g & 1)) return false;
+            if (first && !warp_wait(KV_ACC_EMPTY, (item_it & 1) ^ 1)) return false;
+            tc_fence_after();
+            const SDesc dO = st ? dOm1 : dOm0;
+            if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < C::kQSteps; ++s)
-                    mma_ts(tmem + C::kTmDV, tmem + C::kTmX + packed_col(s), dOm[st], s * 16 * 128, C::kIdescAcc,
+                    mma_ts(tmem + C::kTmDV, tmem + C::kTmX + packed_col(s), dO, s * 16 * 128, C::kIdescAcc,
                            (!first || s > 0));
                 tc_commit(bar(KV_X_FREE));
-                ++dv_cnt;
                 tc_commit(bar(KV_DO_EMPTY + st));
-                return true;
-            };
-            // dK += dS^T Q with dS^T read from TMEM.
-            auto issue_dk = [&](uint32_t g, bool first) -> bool {
-                const uint32_t st = g & 1;
-                if (!mbar_wait_bounded(bar(KV_DS_FULL), g & 1, abort_flag)) return false;
-                tc_fence_after();
+            }
+            __syncwarp();
+            ++dv_cnt;
+            return true;
+        };
+        // dK += dS^T Q with dS^T read from TMEM.
+        auto issue_dk = [&](uint32_t g, bool first) -> bool {
+            const uint32_t st = g & 1;
+            if (!warp_wait(KV_DS_FULL, g & 1)) return false;
+            tc_fence_after();
+            const SDesc dq = st ? dQm1 : dQm0;
+            if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < C::kQSteps; ++s)
-                    mma_ts(tmem + C::kTmDK, tmem + C::kTmY + packed_col(s), dQm[st], s * 16 * 128, C::kIdescAcc,
+                    mma_ts(tmem + C::kTmDK, tmem + C::kTmY + packed_col(s), dq, s * 16 * 128, C::kIdescAcc,
                            (!first || s > 0));
                 tc_commit(bar(KV_Y_FREE));
-                ++dk_cnt;
                 tc_commit(bar(KV_Q_EMPTY + st));
-                return true;
-            };
-            for (int it = it_begin; it < it_end && ok; ++it) {
-                const int n = p.items[it].w;
-                if (n == 0) continue;
-                if (!mbar_wait_bounded(bar(KV_K_FULL), item_it & 1, abort_flag) ||
-                    !mbar_wait_bounded(bar(KV_V_FULL), item_it & 1, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t g0 = step_it;
-                if (!issue_s(g0) || !issue_dp(g0) || !issue_dv(g0, true)) { ok = false; break; }
-                for (int i = 0; i < n && ok; ++i) {
-                    const uint32_t g = g0 + uint32_t(i);
-                    if (!issue_dk(g, i == 0)) { ok = false; break; }
-                    if (i + 1 < n && (!issue_s(g + 1) || !issue_dp(g + 1) || !issue_dv(g + 1, false))) {
-                        ok = false;
-                        break;
-                    }
+            }
+            __syncwarp();
+            ++dk_cnt;
+            return true;
+        };
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const int n = p.items[it].w;
+            if (n == 0) continue;
+            if (!warp_wait(KV_K_FULL, item_it & 1) || !warp_wait(KV_V_FULL, item_it & 1)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t g0 = step_it;
+            if (!issue_s(g0) || !issue_dp(g0) || !issue_dv(g0, true)) { ok = false; break; }
+            for (int i = 0; i < n && ok; ++i) {
+                const uint32_t g = g0 + uint32_t(i);
+                if (!issue_dk(g, i == 0)) { ok = false; break; }
+                if (i + 1 < n && (!issue_s(g + 1) || !issue_dp(g + 1) || !issue_dv(g + 1, false))) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
+            }
+            if (!ok) break;
+            if (elect_one()) {
                 tc_commit(bar(KV_ACC_FULL));
                 tc_commit(bar(KV_KV_EMPTY));
-                step_it += uint32_t(n);
-                ++item_it;
             }
-            if (!ok) fail();
-            tc_commit(bar(KV_DRAIN));
-            mbar_wait_bounded(bar(KV_DRAIN), 0, nullptr);
+            __syncwarp();
+            step_it += uint32_t(n);
+            ++item_it;
         }
+        if (!ok) fail();
+        if (elect_one()) tc_commit(bar(KV_DRAIN));
+        __syncwarp();
+        mbar_wait_bounded(bar(KV_DRAIN), 0, nullptr);
     } else {
         // ------------------------------------------------------------ P^T, dS^T, epilogue
         // Thread = key row r (TMEM lane); warpgroup wg owns query columns [c0, c0+64).
@@ -313,9 +334,13 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
         const uint32_t tX = tmem + lane_base + C::kTmX + uint32_t(c0);
         const uint32_t tY = tmem + lane_base + C::kTmY + uint32_t(c0);
-        float* lse_s = misc_f + warp * (2 * NC + 32);
-        float* del_s = lse_s + NC;
-        float* bias_w = del_s + NC;
+        float* lse_s = misc_f + warp * C::kWarpMisc;  // -lse (log2 units) per column
+        float* del_s = lse_s + NC;                      // -Delta per column
+        float* bias_w = del_s + NC;                     // the head's bias row (log2 units for softmax)
+        float* rtab = bias_w + 32;                      // bias by relative position, per step
+        // Element (lane, c) has relative position rbase(lane 0) - lane + c: rtab[k] holds
+        // the bias of rbase(lane 0) - 31 + k, so the lane reads rrow[c], rrow = rtab + 31 - lane.
+        const float* rrow = rtab + 31 - lane;
         const bool softmax = p.mode == JFA_SOFTMAX;
         const bool gelu = p.mode == JFA_GDPA_GELU_TANH;
         uint32_t step_it = 0, item_it = 0;
@@ -353,8 +378,8 @@ __global__ void __launch_bounds__(320, 1)
                     const int c = qrow0 + c0 + 32 * k + lane;
                     const bool v = softmax && c < q_len;
                     const size_t ridx = (size_t(q0) + size_t(v ? c : 0)) * size_t(p.H) + size_t(h);
-                    nl[k] = v ? p.lse[ridx] * 1.4426950408889634f : 0.f;
-                    nd[k] = v ? p.delta[ridx] : 0.f;
+                    nl[k] = v ? -p.lse[ridx] * 1.4426950408889634f : 0.f;
+                    nd[k] = v ? -p.delta[ridx] : 0.f;
                 }
             };
             fetch(first_qt * C::BM);
@@ -375,16 +400,29 @@ __global__ void __launch_bounds__(320, 1)
                 const int rbase = qrow0 + c0 + diag - j;  // relative position of local column 0
                 const float xs = softmax ? p.scale_log2 : p.scale;
                 // Bias per 32-column chunk: one value when every lane's chunk sits in
-                // one bucket, else looked up per element.
-                bool cconst[2];
-                float cbias[2];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
+                // one bucket, else read per element from the relative-position table.
+                // Lane k tests chunk k for the whole warp: over the warp's keys, chunk k
+                // spans relative positions rbase(lane 0) + 32k - 31 .. + 62.
+                bool cconst[2] = {true, true};
+                float cbias[2] = {0.f, 0.f};
+                if (p.bias) {
+                    const int rb0 = __shfl_sync(0xffffffffu, rbase, 0);
                     int bk = 0;
-                    bool c = true;
-                    if (p.bias) c = chunk_bucket_const(rbase + 32 * k + 31, bk);
-                    cbias[k] = p.bias ? bias_w[bk] : 0.f;
-                    cconst[k] = __all_sync(0xffffffffu, c);
+                    const uint32_t cm = warp_const_chunks(lane < 2, rb0 + 32 * lane - 31, bk);
+                    const float bv = bias_w[bk];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        cconst[k] = (cm >> k) & 1u;
+                        cbias[k] = __shfl_sync(0xffffffffu, bv, k);
+                    }
+                }
+                if (!(cconst[0] && cconst[1])) {
+                    const int r0 = __shfl_sync(0xffffffffu, rbase, 0) - 31;
+                    __syncwarp();
+#pragma unroll
+                    for (int m = 0; m < C::kRelTab / 32; ++m)
+                        rtab[lane + 32 * m] = bias_w[relpos_bucket(r0 + lane + 32 * m)];
+                    __syncwarp();
                 }
 
                 if (!warp_wait(KV_S_FULL, g & 1)) { ok = false; break; }
@@ -405,23 +443,20 @@ __global__ void __launch_bounds__(320, 1)
                     const float2 xs2 = make_float2(xs, xs);
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
-                        if (cconst[k]) {
+                        // exponent = xs * s + (bias - lse): the addend is one packed add of
+                        // the staged -lse and the chunk's bias (constant or from the table)
+                        const float2 cb2 = make_float2(cbias[k], cbias[k]);
 #pragma unroll
-                            for (int c = 32 * k; c < 32 * k + 32; c += 4) {
-                                const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c);
-                                const float2 e0 = fma2(make_float2(pv[c], pv[c + 1]), xs2,
-                                                       make_float2(cbias[k] - l4.x, cbias[k] - l4.y));
-                                const float2 e1 = fma2(make_float2(pv[c + 2], pv[c + 3]), xs2,
-                                                       make_float2(cbias[k] - l4.z, cbias[k] - l4.w));
-                                pv[c] = ex2_approx(e0.x);
-                                pv[c + 1] = ex2_approx(e0.y);
-                                pv[c + 2] = ex2_approx(e1.x);
-                                pv[c + 3] = ex2_approx(e1.y);
-                            }
-                        } else {
-#pragma unroll
-                            for (int c = 32 * k; c < 32 * k + 32; ++c)
-                                pv[c] = ex2_approx(fmaf(pv[c], xs, bias_w[relpos_bucket(rbase + c)] - lse_s[c]));
+                        for (int c = 32 * k; c < 32 * k + 32; c += 4) {
+                            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c);
+                            const float2 b0 = cconst[k] ? cb2 : make_float2(rrow[c], rrow[c + 1]);
+                            const float2 b1 = cconst[k] ? cb2 : make_float2(rrow[c + 2], rrow[c + 3]);
+                            const float2 e0 = fma2(make_float2(pv[c], pv[c + 1]), xs2, add2(make_float2(l4.x, l4.y), b0));
+                            const float2 e1 = fma2(make_float2(pv[c + 2], pv[c + 3]), xs2, add2(make_float2(l4.z, l4.w), b1));
+                            pv[c] = ex2_approx(e0.x);
+                            pv[c + 1] = ex2_approx(e0.y);
+                            pv[c + 2] = ex2_approx(e1.x);
+                            pv[c + 3] = ex2_approx(e1.y);
                         }
                     }
                     if (!full) {
@@ -435,7 +470,7 @@ __global__ void __launch_bounds__(320, 1)
                     for (int k = 0; k < 2; ++k) {
 #pragma unroll
                         for (int c = 32 * k; c < 32 * k + 32; ++c)
-                            pv[c] = fmaf(pv[c], xs, cconst[k] ? cbias[k] : bias_w[relpos_bucket(rbase + c)]);
+                            pv[c] = fmaf(pv[c], xs, cconst[k] ? cbias[k] : rrow[c]);
                     }
 #pragma unroll
                     for (int c = 0; c < NC; c += 2) {
@@ -475,9 +510,9 @@ __global__ void __launch_bounds__(320, 1)
                             const float4 d4 = *reinterpret_cast<const float4*>(del_s + 32 * k + c);
                             const float* pp = pv + 32 * k + c;
                             const float2 a = mul2(make_float2(pp[0], pp[1]),
-                                                  add2(make_float2(dp[c], dp[c + 1]), make_float2(-d4.x, -d4.y)));
+                                                  add2(make_float2(dp[c], dp[c + 1]), make_float2(d4.x, d4.y)));
                             const float2 b2 = mul2(make_float2(pp[2], pp[3]),
-                                                   add2(make_float2(dp[c + 2], dp[c + 3]), make_float2(-d4.z, -d4.w)));
+                                                   add2(make_float2(dp[c + 2], dp[c + 3]), make_float2(d4.z, d4.w)));
                             pd[c >> 1] = pack_bf16x2(a.x, a.y);
                             pd[(c >> 1) + 1] = pack_bf16x2(b2.x, b2.y);
                         }

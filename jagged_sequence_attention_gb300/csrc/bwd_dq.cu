@@ -201,81 +201,94 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t kv_it = 0, item_it = 0;
-            bool ok = true;
-            const SDesc dQa = sdesc_sw128(sQ, 16, 1024), dOa = sdesc_sw128(sDO, 16, 1024);
-            const SDesc dKk[3] = {sdesc_sw128(sK, 16, 1024), sdesc_sw128(sK + C::kKVTile, 16, 1024),
-                                  sdesc_sw128(sK + 2 * C::kKVTile, 16, 1024)};
-            const SDesc dVk[2] = {sdesc_sw128(sV, 16, 1024), sdesc_sw128(sV + C::kKVTile, 16, 1024)};
-            const SDesc dKm[3] = {sdesc_sw128(sK, C::BN * 128, 1024), sdesc_sw128(sK + C::kKVTile, C::BN * 128, 1024),
-                                  sdesc_sw128(sK + 2 * C::kKVTile, C::BN * 128, 1024)};
-            auto koff = [](int s) -> uint32_t { return uint32_t(((s * 32) >> 7) * 128 * 128 + ((s * 32) & 127)); };
-            // S(g) = Q K^T into buffer g&1, once the dQ product that read that buffer is done.
-            auto issue_s = [&](uint32_t g) -> bool {
-                const uint32_t sb = g & 1, ph = (g >> 1) & 1, kst = g % 3;
-                if (!mbar_wait_bounded(bar(DQ_K_FULL + kst), (g / 3) & 1, abort_flag) ||
-                    !mbar_wait_bounded(bar(DQ_SB_FREE + sb), ph ^ 1, abort_flag))
-                    return false;
-                tc_fence_after();
+        // The whole warp runs the schedule, so descriptors and counters stay
+        // warp-uniform; one elected lane (always lane 0) issues every MMA and commit.
+        uint32_t kv_it = 0, item_it = 0;
+        bool ok = true;
+        const SDesc dQa = sdesc_sw128(sQ, 16, 1024), dOa = sdesc_sw128(sDO, 16, 1024);
+        // Descriptors of every ring stage, selected by value (no indexed array, which
+        // would live in local memory).
+        const SDesc dKk0 = sdesc_sw128(sK, 16, 1024), dKk1 = sdesc_sw128(sK + C::kKVTile, 16, 1024),
+                    dKk2 = sdesc_sw128(sK + 2 * C::kKVTile, 16, 1024);
+        const SDesc dVk0 = sdesc_sw128(sV, 16, 1024), dVk1 = sdesc_sw128(sV + C::kKVTile, 16, 1024);
+        const SDesc dKm0 = sdesc_sw128(sK, C::BN * 128, 1024), dKm1 = sdesc_sw128(sK + C::kKVTile, C::BN * 128, 1024),
+                    dKm2 = sdesc_sw128(sK + 2 * C::kKVTile, C::BN * 128, 1024);
+        auto koff = [](int s) -> uint32_t { return uint32_t(((s * 32) >> 7) * 128 * 128 + ((s * 32) & 127)); };
+        // S(g) = Q K^T into buffer g&1, once the dQ product that read that buffer is done.
+        auto issue_s = [&](uint32_t g) -> bool {
+            const uint32_t sb = g & 1, ph = (g >> 1) & 1, kst = g % 3;
+            if (!warp_wait(DQ_K_FULL + kst, (g / 3) & 1) || !warp_wait(DQ_SB_FREE + sb, ph ^ 1)) return false;
+            tc_fence_after();
+            const SDesc dk = kst == 0 ? dKk0 : kst == 1 ? dKk1 : dKk2;
+            if (elect_one()) {
 #pragma unroll
-                for (int s = 0; s < C::kDSteps; ++s)
-                    mma_ss(tmem + sb * 128u, dQa, koff(s), dKk[kst], koff(s), C::kIdescS, s > 0);
+                for (int s = 0; s < C::kDSteps; ++s) mma_ss(tmem + sb * 128u, dQa, koff(s), dk, koff(s), C::kIdescS, s > 0);
                 tc_commit(bar(DQ_S_FULL + sb));
-                return true;
-            };
-            // dP(g) = dO V^T; the compute threads read dP(g-1) before signalling dS(g-1),
-            // which the issuer waited for before getting here.
-            auto issue_dp = [&](uint32_t g) -> bool {
-                const uint32_t st = g & 1, ph = (g >> 1) & 1;
-                if (!mbar_wait_bounded(bar(DQ_V_FULL + st), ph, abort_flag)) return false;
-                tc_fence_after();
+            }
+            __syncwarp();
+            return true;
+        };
+        // dP(g) = dO V^T; the compute threads read dP(g-1) before signalling dS(g-1),
+        // which the issuer waited for before getting here.
+        auto issue_dp = [&](uint32_t g) -> bool {
+            const uint32_t st = g & 1, ph = (g >> 1) & 1;
+            if (!warp_wait(DQ_V_FULL + st, ph)) return false;
+            tc_fence_after();
+            const SDesc dv = st ? dVk1 : dVk0;
+            if (elect_one()) {
 #pragma unroll
-                for (int s = 0; s < C::kDSteps; ++s)
-                    mma_ss(tmem + C::kTmDP, dOa, koff(s), dVk[st], koff(s), C::kIdescS, s > 0);
+                for (int s = 0; s < C::kDSteps; ++s) mma_ss(tmem + C::kTmDP, dOa, koff(s), dv, koff(s), C::kIdescS, s > 0);
                 tc_commit(bar(DQ_DP_FULL));
                 tc_commit(bar(DQ_V_EMPTY + st));
-                return true;
-            };
-            // dQ += dS K with dS read from buffer g&1; the first product of an item waits
-            // for the previous item's epilogue to have read the accumulator.
-            auto issue_dq = [&](uint32_t g, bool first) -> bool {
-                const uint32_t sb = g & 1, kst = g % 3;
-                if (!mbar_wait_bounded(bar(DQ_DS_FULL), g & 1, abort_flag)) return false;
-                if (first && !mbar_wait_bounded(bar(DQ_ACC_EMPTY), (item_it & 1) ^ 1, abort_flag)) return false;
-                tc_fence_after();
+            }
+            __syncwarp();
+            return true;
+        };
+        // dQ += dS K with dS read from buffer g&1; the first product of an item waits
+        // for the previous item's epilogue to have read the accumulator.
+        auto issue_dq = [&](uint32_t g, bool first) -> bool {
+            const uint32_t sb = g & 1, kst = g % 3;
+            if (!warp_wait(DQ_DS_FULL, g & 1)) return false;
+            if (first && !warp_wait(DQ_ACC_EMPTY, (item_it & 1) ^ 1)) return false;
+            tc_fence_after();
+            const SDesc dk = kst == 0 ? dKm0 : kst == 1 ? dKm1 : dKm2;
+            if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < C::kKSteps; ++s)
-                    mma_ts(tmem + C::kTmDQ, tmem + sb * 128u + packed_col(s), dKm[kst], s * 16 * 128, C::kIdescDQ,
+                    mma_ts(tmem + C::kTmDQ, tmem + sb * 128u + packed_col(s), dk, s * 16 * 128, C::kIdescDQ,
                            (!first || s > 0));
                 tc_commit(bar(DQ_SB_FREE + sb));
                 tc_commit(bar(DQ_K_EMPTY + kst));
-                return true;
-            };
-            for (int it = it_begin; it < it_end && ok; ++it) {
-                const int n = p.items[it].w;
-                if (n == 0) continue;
-                if (!mbar_wait_bounded(bar(DQ_Q_FULL), item_it & 1, abort_flag) ||
-                    !mbar_wait_bounded(bar(DQ_DO_FULL), item_it & 1, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t g0 = kv_it;
-                if (!issue_s(g0) || !issue_dp(g0)) { ok = false; break; }
-                for (int j = 0; j < n && ok; ++j) {
-                    const uint32_t g = g0 + uint32_t(j);
-                    if (j + 1 < n && !issue_s(g + 1)) { ok = false; break; }
-                    if (!issue_dq(g, j == 0)) { ok = false; break; }
-                    if (j + 1 < n && !issue_dp(g + 1)) { ok = false; break; }
-                }
-                if (!ok) break;
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const int n = p.items[it].w;
+            if (n == 0) continue;
+            if (!warp_wait(DQ_Q_FULL, item_it & 1) || !warp_wait(DQ_DO_FULL, item_it & 1)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t g0 = kv_it;
+            if (!issue_s(g0) || !issue_dp(g0)) { ok = false; break; }
+            for (int j = 0; j < n && ok; ++j) {
+                const uint32_t g = g0 + uint32_t(j);
+                if (j + 1 < n && !issue_s(g + 1)) { ok = false; break; }
+                if (!issue_dq(g, j == 0)) { ok = false; break; }
+                if (j + 1 < n && !issue_dp(g + 1)) { ok = false; break; }
+            }
+            if (!ok) break;
+            if (elect_one()) {
                 tc_commit(bar(DQ_ACC_FULL));
                 tc_commit(bar(DQ_QDO_EMPTY));
-                kv_it += uint32_t(n);
-                ++item_it;
             }
-            if (!ok) fail();
-            tc_commit(bar(DQ_DRAIN));
-            mbar_wait_bounded(bar(DQ_DRAIN), 0, nullptr);
+            __syncwarp();
+            kv_it += uint32_t(n);
+            ++item_it;
         }
+        if (!ok) fail();
+        if (elect_one()) tc_commit(bar(DQ_DRAIN));
+        __syncwarp();
+        mbar_wait_bounded(bar(DQ_DRAIN), 0, nullptr);
     } else {
         // ------------------------------------------------------------ dS, epilogue
         // Thread = query row t of the tile (TMEM lane); warpgroup wg owns key columns
@@ -320,15 +333,20 @@ __global__ void __launch_bounds__(320, 1)
                 if (!row_valid) lim = 0;
                 const bool full = __all_sync(0xffffffffu, lim >= NC);
                 const int rb = row + diag - col0;  // relative position of local column 0
-                bool cconst[2];
-                float cbias[2];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
+                // Lane k tests chunk k for the whole warp: over the warp's rows, chunk k
+                // spans relative positions rb(lane 0) - 32k - 31 .. + 62.
+                bool cconst[2] = {true, true};
+                float cbias[2] = {0.f, 0.f};
+                if (p.bias) {
+                    const int rb0 = __shfl_sync(0xffffffffu, rb, 0);
                     int bk = 0;
-                    bool c = true;
-                    if (p.bias) c = chunk_bucket_const(rb - 32 * k, bk);
-                    cbias[k] = p.bias ? bias_w[bk] : 0.f;
-                    cconst[k] = __all_sync(0xffffffffu, c);
+                    const uint32_t cm = warp_const_chunks(lane < 2, rb0 - 32 * lane - 31, bk);
+                    const float bv = bias_w[bk];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        cconst[k] = (cm >> k) & 1u;
+                        cbias[k] = __shfl_sync(0xffffffffu, bv, k);
+                    }
                 }
                 const uint32_t tS = tmem + lane_base + sb * 128u + uint32_t(c0);
 

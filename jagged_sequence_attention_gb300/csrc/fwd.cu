@@ -214,23 +214,28 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t kv_it = 0, item_it = 0;
-            uint32_t pv_cnt[2] = {0, 0}, items_x[2] = {0, 0};
-            bool ok = true;
-            // Descriptors of every operand tile, built once; each MMA below adds a
-            // compile-time byte offset to the low half.
-            const SDesc dQ0 = sdesc_sw128(sQ, 16, 1024), dQ1 = sdesc_sw128(sQ + C::kQBytes, 16, 1024);
-            const SDesc dK0 = sdesc_sw128(sK, 16, 1024), dK1 = sdesc_sw128(sK + C::kKVBytes, 16, 1024);
-            const SDesc dV0 = sdesc_sw128(sV, C::BN * 128, 1024), dV1 = sdesc_sw128(sV + C::kKVBytes, C::BN * 128, 1024);
-            // S_x = Q_x K^T into the tile's S columns; first waits for the tile's
-            // previous P V product, which reads P from those columns.
-            auto issue_s = [&](int x, uint32_t st) -> bool {
-                if (pv_cnt[x] > 0 && !mbar_wait_bounded(bar(B_O_DONE + x), (pv_cnt[x] - 1) & 1, abort_flag))
-                    return false;
-                tc_fence_after();
-                const SDesc dq = x ? dQ1 : dQ0, dk = st ? dK1 : dK0;
-                const uint32_t d_tmem = tmem + C::tmem_s(x);
+        // The whole warp runs the schedule, so descriptors and counters stay
+        // warp-uniform; one elected lane (always lane 0) issues every MMA and commit.
+        auto wwait = [&](int b, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(b), parity, abort_flag));
+        };
+        uint32_t kv_it = 0, item_it = 0;
+        uint32_t pv_cnt0 = 0, pv_cnt1 = 0, items_x0 = 0, items_x1 = 0;
+        bool ok = true;
+        // Descriptors of every operand tile, built once; each MMA below adds a
+        // compile-time byte offset to the low half.
+        const SDesc dQ0 = sdesc_sw128(sQ, 16, 1024), dQ1 = sdesc_sw128(sQ + C::kQBytes, 16, 1024);
+        const SDesc dK0 = sdesc_sw128(sK, 16, 1024), dK1 = sdesc_sw128(sK + C::kKVBytes, 16, 1024);
+        const SDesc dV0 = sdesc_sw128(sV, C::BN * 128, 1024), dV1 = sdesc_sw128(sV + C::kKVBytes, C::BN * 128, 1024);
+        // S_x = Q_x K^T into the tile's S columns; first waits for the tile's
+        // previous P V product, which reads P from those columns.
+        auto issue_s = [&](int x, uint32_t st) -> bool {
+            const uint32_t pc = x ? pv_cnt1 : pv_cnt0;
+            if (pc > 0 && !wwait(B_O_DONE + x, (pc - 1) & 1)) return false;
+            tc_fence_after();
+            const SDesc dq = x ? dQ1 : dQ0, dk = st ? dK1 : dK0;
+            const uint32_t d_tmem = tmem + C::tmem_s(x);
+            if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < C::kQKSteps; ++s) {
                     // K step s: 128-byte column block (s*32)>>7, (s*32)&127 bytes into the row
@@ -238,15 +243,19 @@ __global__ void __launch_bounds__(320, 1)
                            ((s * 32) >> 7) * C::BN * 128 + ((s * 32) & 127), C::kIdescQK, s > 0);
                 }
                 tc_commit(bar(B_S_FULL + x));
-                return true;
-            };
-            // O_x += P_x V with P read from TMEM; GDPA adds the remainder product.
-            auto issue_pv = [&](int x, uint32_t st, bool first) -> bool {
-                if (!mbar_wait_bounded(bar(B_P_FULL + x), pv_cnt[x] & 1, abort_flag)) return false;
-                if (first && !mbar_wait_bounded(bar(B_O_EMPTY + x), (items_x[x] & 1) ^ 1, abort_flag)) return false;
-                tc_fence_after();
-                const SDesc dv = st ? dV1 : dV0;
-                const uint32_t d_tmem = tmem + C::tmem_o(x), a_tmem = tmem + C::tmem_s(x);
+            }
+            __syncwarp();
+            return true;
+        };
+        // O_x += P_x V with P read from TMEM; GDPA adds the remainder product.
+        auto issue_pv = [&](int x, uint32_t st, bool first) -> bool {
+            const uint32_t pc = x ? pv_cnt1 : pv_cnt0, ix = x ? items_x1 : items_x0;
+            if (!wwait(B_P_FULL + x, pc & 1)) return false;
+            if (first && !wwait(B_O_EMPTY + x, (ix & 1) ^ 1)) return false;
+            tc_fence_after();
+            const SDesc dv = st ? dV1 : dV0;
+            const uint32_t d_tmem = tmem + C::tmem_o(x), a_tmem = tmem + C::tmem_s(x);
+            if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < C::kPVSteps; ++s)
                     mma_ts(d_tmem, a_tmem + p_col(s), dv, s * C::kUmmaK * 128, C::kIdescPV, (!first || s > 0));
@@ -256,52 +265,57 @@ __global__ void __launch_bounds__(320, 1)
                         mma_ts(d_tmem, a_tmem + p_col(s) + 16u, dv, s * C::kUmmaK * 128, C::kIdescPV, 1u);
                 }
                 tc_commit(bar(B_O_DONE + x));
-                ++pv_cnt[x];
-                return true;
-            };
-            for (int it = it_begin; it < it_end && ok; ++it) {
-                const int4 w = p.items[it];
-                const int n = w.w;
-                if (n == 0) continue;
-                const int b = w.x, pr = w.z;
-                const int q_len = p.q_off[b + 1] - p.q_off[b], kv_len = p.kv_off[b + 1] - p.kv_off[b];
-                const int nx0 = fwd_tiles_of(q_len, kv_len, 2 * pr, p.causal);
-                const int nx1 = fwd_tiles_of(q_len, kv_len, 2 * pr + 1, p.causal);
-                if (!mbar_wait_bounded(bar(B_Q_FULL), item_it & 1, abort_flag)) { ok = false; break; }
-                // prologue: S of key tile 0
-                {
-                    const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
-                    if (!mbar_wait_bounded(bar(B_K_FULL + st), ph, abort_flag)) { ok = false; break; }
-                    if (nx0 > 0 && !issue_s(0, st)) { ok = false; break; }
-                    if (nx1 > 0 && !issue_s(1, st)) { ok = false; break; }
-                    tc_commit(bar(B_K_EMPTY + st));
-                    if (n == 1) tc_commit(bar(B_Q_EMPTY));
-                }
-                for (int j = 0; j < n && ok; ++j) {
-                    const uint32_t g = kv_it + j, st = g & 1, ph = (g >> 1) & 1;
-                    const uint32_t g1 = g + 1, st1 = g1 & 1, ph1 = (g1 >> 1) & 1;
-                    if (!mbar_wait_bounded(bar(B_V_FULL + st), ph, abort_flag)) { ok = false; break; }
-                    if (j < nx0 && !issue_pv(0, st, j == 0)) { ok = false; break; }
-                    if (j + 1 < n && !mbar_wait_bounded(bar(B_K_FULL + st1), ph1, abort_flag)) { ok = false; break; }
-                    if (j + 1 < nx0 && !issue_s(0, st1)) { ok = false; break; }
-                    if (j < nx1 && !issue_pv(1, st, j == 0)) { ok = false; break; }
-                    tc_commit(bar(B_V_EMPTY + st));
-                    if (j + 1 < nx1 && !issue_s(1, st1)) { ok = false; break; }
-                    if (j + 1 < n) {
-                        tc_commit(bar(B_K_EMPTY + st1));
-                        if (j + 2 == n) tc_commit(bar(B_Q_EMPTY));
-                    }
-                }
-                kv_it += n;
-                ++item_it;
-                items_x[0] += nx0 > 0 ? 1 : 0;
-                items_x[1] += nx1 > 0 ? 1 : 0;
             }
-            if (!ok) fail();
-            // Drain all issued MMAs before TMEM is released.
-            tc_commit(bar(B_DRAIN));
-            mbar_wait_bounded(bar(B_DRAIN), 0, nullptr);
+            __syncwarp();
+            if (x) ++pv_cnt1; else ++pv_cnt0;
+            return true;
+        };
+        auto commit = [&](int b) {
+            if (elect_one()) tc_commit(bar(b));
+            __syncwarp();
+        };
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const int4 w = p.items[it];
+            const int n = w.w;
+            if (n == 0) continue;
+            const int b = w.x, pr = w.z;
+            const int q_len = p.q_off[b + 1] - p.q_off[b], kv_len = p.kv_off[b + 1] - p.kv_off[b];
+            const int nx0 = fwd_tiles_of(q_len, kv_len, 2 * pr, p.causal);
+            const int nx1 = fwd_tiles_of(q_len, kv_len, 2 * pr + 1, p.causal);
+            if (!wwait(B_Q_FULL, item_it & 1)) { ok = false; break; }
+            // prologue: S of key tile 0
+            {
+                const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
+                if (!wwait(B_K_FULL + st, ph)) { ok = false; break; }
+                if (nx0 > 0 && !issue_s(0, st)) { ok = false; break; }
+                if (nx1 > 0 && !issue_s(1, st)) { ok = false; break; }
+                commit(B_K_EMPTY + st);
+                if (n == 1) commit(B_Q_EMPTY);
+            }
+            for (int j = 0; j < n && ok; ++j) {
+                const uint32_t g = kv_it + j, st = g & 1, ph = (g >> 1) & 1;
+                const uint32_t g1 = g + 1, st1 = g1 & 1, ph1 = (g1 >> 1) & 1;
+                if (!wwait(B_V_FULL + st, ph)) { ok = false; break; }
+                if (j < nx0 && !issue_pv(0, st, j == 0)) { ok = false; break; }
+                if (j + 1 < n && !wwait(B_K_FULL + st1, ph1)) { ok = false; break; }
+                if (j + 1 < nx0 && !issue_s(0, st1)) { ok = false; break; }
+                if (j < nx1 && !issue_pv(1, st, j == 0)) { ok = false; break; }
+                commit(B_V_EMPTY + st);
+                if (j + 1 < nx1 && !issue_s(1, st1)) { ok = false; break; }
+                if (j + 1 < n) {
+                    commit(B_K_EMPTY + st1);
+                    if (j + 2 == n) commit(B_Q_EMPTY);
+                }
+            }
+            kv_it += n;
+            ++item_it;
+            items_x0 += nx0 > 0 ? 1 : 0;
+            items_x1 += nx1 > 0 ? 1 : 0;
         }
+        if (!ok) fail();
+        // Drain all issued MMAs before TMEM is released.
+        commit(B_DRAIN);
+        mbar_wait_bounded(bar(B_DRAIN), 0, nullptr);
     } else {
         // ------------------------------------------------------------ softmax / epilogue
         const int x = warp >> 2;               // query tile of this warpgroup
@@ -366,14 +380,19 @@ __global__ void __launch_bounds__(320, 1)
                 // Bias per 32-column chunk: a constant when every lane's chunk sits in
                 // one bucket (warp-uniform flag per chunk); otherwise read per element
                 // from a table of the bias by relative position built for this tile.
-                uint32_t cmask = 0;  // bit k: chunk k has a constant bias
+                // Lane k tests chunk k for the whole warp: over the warp's rows, chunk k
+                // spans relative positions rbase(lane 0) - 32k - 31 .. + 62.
+                uint32_t cmask = (1u << (C::BN / 32)) - 1;  // bit k: chunk k has a constant bias
                 float cb[C::BN / 32];
 #pragma unroll
-                for (int k = 0; k < C::BN / 32; ++k) {
+                for (int k = 0; k < C::BN / 32; ++k) cb[k] = 0.f;
+                if (p.bias) {
+                    const int rb0 = __shfl_sync(0xffffffffu, rbase, 0);
                     int bk = 0;
-                    const bool c = p.bias ? chunk_bucket_const(rbase - 32 * k, bk) : true;
-                    cb[k] = p.bias ? btab[bk] : 0.f;
-                    if (__all_sync(0xffffffffu, c)) cmask |= 1u << k;
+                    cmask = warp_const_chunks(lane < C::BN / 32, rb0 - 32 * lane - 31, bk) & cmask;
+                    const float bv = btab[bk];
+#pragma unroll
+                    for (int k = 0; k < C::BN / 32; ++k) cb[k] = __shfl_sync(0xffffffffu, bv, k);
                 }
                 if (cmask != (1u << (C::BN / 32)) - 1) {
                     // rtab[i] = bias(r) for r = (lane 0's rbase) - 127 + i, i in [0, 160):

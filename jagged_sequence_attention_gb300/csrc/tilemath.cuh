@@ -25,6 +25,19 @@ __device__ __forceinline__ bool chunk_bucket_const(int r_hi, int& bucket) {
     return r_lo >= 0 && relpos_bucket(r_lo) == bucket;
 }
 
+// Warp-level form of the test above.  In the callers, the 32 lanes' windows for one
+// chunk tile a range of 63 relative positions [lo, lo + 62] (consecutive rows or keys
+// shift the window by one).  A bucket boundary inside that range lies inside some lane's
+// window, so every lane's chunk is constant exactly when the whole range is >= 0 and in
+// one bucket, and then all lanes share that bucket.  Each lane evaluates one chunk (the
+// caller passes lane k the range of chunk k); returns the ballot of constant chunks, and
+// the chunk's bucket in `bucket`.
+__device__ __forceinline__ uint32_t warp_const_chunks(bool active, int lo, int& bucket) {
+    bucket = relpos_bucket(lo + 62);
+    const bool c = active && lo >= 0 && relpos_bucket(lo) == bucket;
+    return __ballot_sync(0xffffffffu, c);
+}
+
 // tanh(u) = 1 - 2 / (exp(2u) + 1) from the hardware exp2 and reciprocal (relative
 // error about 2^-22 each); saturates correctly at +-inf.
 __device__ __forceinline__ float tanh_acc(float u) {
