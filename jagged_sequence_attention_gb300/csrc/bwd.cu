@@ -30,7 +30,8 @@
 // 9 MMA issuer.  TMEM: dV [0,128), dK [128,256), S^T/P^T [256,384), dP^T/dS^T
 // [384,512).  Issue order per step: dK(i), S(i+1), dP(i+1), dV(i+1); each product
 // that must wait for a TMEM region to be consumed finds another product queued
-// ahead of it.
+// ahead of it.  P^T and dS^T are signalled per 32-column chunk, so dV and dK start on
+// the first chunk while the second is being formed.
 #include <algorithm>
 
 #include "bwd_common.cuh"
@@ -87,14 +88,14 @@ enum {
     KV_DO_FULL = 7,   // +stage
     KV_DO_EMPTY = 9,  // +stage
     KV_S_FULL = 11,
-    KV_P_FULL = 12,
-    KV_DP_FULL = 13,
-    KV_DS_FULL = 14,
-    KV_X_FREE = 15,  // dV(i) done: the S^T/P^T columns may be rewritten
-    KV_Y_FREE = 16,  // dK(i) done: the dP^T/dS^T columns may be rewritten
-    KV_ACC_FULL = 17,
-    KV_ACC_EMPTY = 18,
-    KV_DRAIN = 19,
+    KV_P_FULL = 12,   // +chunk: columns [32k, 32k+32) of both warpgroups' P^T are in TMEM
+    KV_DP_FULL = 14,
+    KV_DS_FULL = 15,  // +chunk, as for P^T
+    KV_X_FREE = 17,   // dV(i) done: the S^T/P^T columns may be rewritten
+    KV_Y_FREE = 18,   // dK(i) done: the dP^T/dS^T columns may be rewritten
+    KV_ACC_FULL = 19,
+    KV_ACC_EMPTY = 20,
+    KV_DRAIN = 21,
 };
 
 template <int D>
@@ -126,8 +127,10 @@ __global__ void __launch_bounds__(320, 1)
         }
         mbar_init(bar(KV_S_FULL), 1);
         mbar_init(bar(KV_P_FULL), C::kCompWarps);
+        mbar_init(bar(KV_P_FULL + 1), C::kCompWarps);
         mbar_init(bar(KV_DP_FULL), 1);
         mbar_init(bar(KV_DS_FULL), C::kCompWarps);
+        mbar_init(bar(KV_DS_FULL + 1), C::kCompWarps);
         mbar_init(bar(KV_X_FREE), 1);
         mbar_init(bar(KV_Y_FREE), 1);
         mbar_init(bar(KV_ACC_FULL), 1);
@@ -258,41 +261,59 @@ __global__ void __launch_bounds__(320, 1)
             __syncwarp();
             return true;
         };
-        // dV += P^T dO with P^T read from TMEM; the first step of an item waits for
-        // the epilogue of the previous item to have read the accumulators.
+        // The K-steps (16 query rows each) that read chunk c of the packed operand:
+        // warpgroup w's chunk c covers query rows 64w + 32c .. + 31, K-steps 4w + 2c, +1.
+        auto chunk_step = [](int c, int i) -> int { return 4 * (i >> 1) + 2 * c + (i & 1); };
+        // dV += P^T dO with P^T read from TMEM, chunk by chunk as the compute warps
+        // finish it; the first step of an item waits for the epilogue of the previous
+        // item to have read the accumulators.
         auto issue_dv = [&](uint32_t g, bool first) -> bool {
             const uint32_t st = g & 1;
-            if (!warp_wait(KV_P_FULL, g & 1)) return false;
-            if (first && !warp_wait(KV_ACC_EMPTY, (item_it & 1) ^ 1)) return false;
-            tc_fence_after();
             const SDesc dO = st ? dOm1 : dOm0;
-            if (elect_one()) {
 #pragma unroll
-                for (int s = 0; s < C::kQSteps; ++s)
-                    mma_ts(tmem + C::kTmDV, tmem + C::kTmX + packed_col(s), dO, s * 16 * 128, C::kIdescAcc,
-                           (!first || s > 0));
-                tc_commit(bar(KV_X_FREE));
-                tc_commit(bar(KV_DO_EMPTY + st));
+            for (int c = 0; c < 2; ++c) {
+                if (!warp_wait(KV_P_FULL + c, g & 1)) return false;
+                if (c == 0 && first && !warp_wait(KV_ACC_EMPTY, (item_it & 1) ^ 1)) return false;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int s = chunk_step(c, i);
+                        mma_ts(tmem + C::kTmDV, tmem + C::kTmX + packed_col(s), dO, s * 16 * 128, C::kIdescAcc,
+                               (!first || c > 0 || i > 0));
+                    }
+                    if (c == 1) {
+                        tc_commit(bar(KV_X_FREE));
+                        tc_commit(bar(KV_DO_EMPTY + st));
+                    }
+                }
+                __syncwarp();
             }
-            __syncwarp();
             ++dv_cnt;
             return true;
         };
-        // dK += dS^T Q with dS^T read from TMEM.
+        // dK += dS^T Q with dS^T read from TMEM, chunk by chunk.
         auto issue_dk = [&](uint32_t g, bool first) -> bool {
             const uint32_t st = g & 1;
-            if (!warp_wait(KV_DS_FULL, g & 1)) return false;
-            tc_fence_after();
             const SDesc dq = st ? dQm1 : dQm0;
-            if (elect_one()) {
 #pragma unroll
-                for (int s = 0; s < C::kQSteps; ++s)
-                    mma_ts(tmem + C::kTmDK, tmem + C::kTmY + packed_col(s), dq, s * 16 * 128, C::kIdescAcc,
-                           (!first || s > 0));
-                tc_commit(bar(KV_Y_FREE));
-                tc_commit(bar(KV_Q_EMPTY + st));
+            for (int c = 0; c < 2; ++c) {
+                if (!warp_wait(KV_DS_FULL + c, g & 1)) return false;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int s = chunk_step(c, i);
+                        mma_ts(tmem + C::kTmDK, tmem + C::kTmY + packed_col(s), dq, s * 16 * 128, C::kIdescAcc,
+                               (!first || c > 0 || i > 0));
+                    }
+                    if (c == 1) {
+                        tc_commit(bar(KV_Y_FREE));
+                        tc_commit(bar(KV_Q_EMPTY + st));
+                    }
+                }
+                __syncwarp();
             }
-            __syncwarp();
             ++dk_cnt;
             return true;
         };
@@ -386,12 +407,10 @@ __global__ void __launch_bounds__(320, 1)
             for (int i = 0; i < n; ++i) {
                 const uint32_t g = step_it + uint32_t(i);
                 const int qrow0 = (first_qt + i) * C::BM;  // first query row of the step
+                const float cur_nl0 = nl[0], cur_nl1 = nl[1];
                 __syncwarp();
-                lse_s[lane] = nl[0];
-                lse_s[32 + lane] = nl[1];
                 del_s[lane] = nd[0];
                 del_s[32 + lane] = nd[1];
-                __syncwarp();
                 if (i + 1 < n) fetch(qrow0 + C::BM);
                 // subtraction scheme: valid local columns are [lo, hi)
                 const int hi = key_valid ? min(NC, q_len - qrow0 - c0) : 0;
@@ -416,14 +435,17 @@ __global__ void __launch_bounds__(320, 1)
                         cbias[k] = __shfl_sync(0xffffffffu, bv, k);
                     }
                 }
+                // Staged addend of column c: -lse, plus the chunk's bias when that is
+                // one value for the whole warp (it then is the same for every lane).
+                lse_s[lane] = cur_nl0 + (cconst[0] ? cbias[0] : 0.f);
+                lse_s[32 + lane] = cur_nl1 + (cconst[1] ? cbias[1] : 0.f);
                 if (!(cconst[0] && cconst[1])) {
                     const int r0 = __shfl_sync(0xffffffffu, rbase, 0) - 31;
-                    __syncwarp();
 #pragma unroll
                     for (int m = 0; m < C::kRelTab / 32; ++m)
                         rtab[lane + 32 * m] = bias_w[relpos_bucket(r0 + lane + 32 * m)];
-                    __syncwarp();
                 }
+                __syncwarp();
 
                 if (!warp_wait(KV_S_FULL, g & 1)) { ok = false; break; }
                 tc_fence_after();
@@ -437,59 +459,57 @@ __global__ void __launch_bounds__(320, 1)
                     tmem_ld_wait(rb);
                 }
                 // P^T = exp2(xs * s + bias - lse) (softmax; pv keeps P) or act(scale * s +
-                // bias) (GDPA; pv keeps act' for dS, pa the activation).
-                uint32_t pk[NC / 2];
-                if (softmax) {
-                    const float2 xs2 = make_float2(xs, xs);
+                // bias) (GDPA; pv keeps act' for dS), one 32-column chunk at a time: each
+                // chunk is packed over the warpgroup's own S^T columns (already read) and
+                // signalled at once, so dV can start on it while the next chunk is formed.
+                const float2 xs2 = make_float2(xs, xs);
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        // exponent = xs * s + (bias - lse): the addend is one packed add of
-                        // the staged -lse and the chunk's bias (constant or from the table)
-                        const float2 cb2 = make_float2(cbias[k], cbias[k]);
+                for (int k = 0; k < 2; ++k) {
+                    uint32_t pk[16];
+                    if (softmax) {
+                        // exponent = xs * s + (bias - lse): the staged addend already holds
+                        // the bias of a warp-constant chunk; other chunks add it per element
+                        // from the relative-position table.
 #pragma unroll
                         for (int c = 32 * k; c < 32 * k + 32; c += 4) {
                             const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c);
-                            const float2 b0 = cconst[k] ? cb2 : make_float2(rrow[c], rrow[c + 1]);
-                            const float2 b1 = cconst[k] ? cb2 : make_float2(rrow[c + 2], rrow[c + 3]);
-                            const float2 e0 = fma2(make_float2(pv[c], pv[c + 1]), xs2, add2(make_float2(l4.x, l4.y), b0));
-                            const float2 e1 = fma2(make_float2(pv[c + 2], pv[c + 3]), xs2, add2(make_float2(l4.z, l4.w), b1));
+                            float2 a0 = make_float2(l4.x, l4.y), a1 = make_float2(l4.z, l4.w);
+                            if (!cconst[k]) {
+                                a0 = add2(a0, make_float2(rrow[c], rrow[c + 1]));
+                                a1 = add2(a1, make_float2(rrow[c + 2], rrow[c + 3]));
+                            }
+                            const float2 e0 = fma2(make_float2(pv[c], pv[c + 1]), xs2, a0);
+                            const float2 e1 = fma2(make_float2(pv[c + 2], pv[c + 3]), xs2, a1);
                             pv[c] = ex2_approx(e0.x);
                             pv[c + 1] = ex2_approx(e0.y);
                             pv[c + 2] = ex2_approx(e1.x);
                             pv[c + 3] = ex2_approx(e1.y);
                         }
+                        if (!full) {
+#pragma unroll
+                            for (int c = 32 * k; c < 32 * k + 32; ++c) pv[c] = (c >= lo && c < hi) ? pv[c] : 0.f;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) pk[c >> 1] = pack_bf16x2(pv[32 * k + c], pv[32 * k + c + 1]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const int cc = 32 * k + c;
+                            float a0, a1, d0, d1;
+                            gdpa_act_grad(gelu, fmaf(pv[cc], xs, cconst[k] ? cbias[k] : rrow[cc]), a0, d0);
+                            gdpa_act_grad(gelu, fmaf(pv[cc + 1], xs, cconst[k] ? cbias[k] : rrow[cc + 1]), a1, d1);
+                            const bool v0 = full || (cc >= lo && cc < hi), v1 = full || (cc + 1 >= lo && cc + 1 < hi);
+                            pk[c >> 1] = pack_bf16x2(v0 ? a0 : 0.f, v1 ? a1 : 0.f);
+                            pv[cc] = v0 ? d0 : 0.f;
+                            pv[cc + 1] = v1 ? d1 : 0.f;
+                        }
                     }
-                    if (!full) {
-#pragma unroll
-                        for (int c = 0; c < NC; ++c) pv[c] = (c >= lo && c < hi) ? pv[c] : 0.f;
-                    }
-#pragma unroll
-                    for (int c = 0; c < NC; c += 2) pk[c >> 1] = pack_bf16x2(pv[c], pv[c + 1]);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-#pragma unroll
-                        for (int c = 32 * k; c < 32 * k + 32; ++c)
-                            pv[c] = fmaf(pv[c], xs, cconst[k] ? cbias[k] : rrow[c]);
-                    }
-#pragma unroll
-                    for (int c = 0; c < NC; c += 2) {
-                        float a0, a1, d0, d1;
-                        gdpa_act_grad(gelu, pv[c], a0, d0);
-                        gdpa_act_grad(gelu, pv[c + 1], a1, d1);
-                        const bool v0 = full || (c >= lo && c < hi), v1 = full || (c + 1 >= lo && c + 1 < hi);
-                        pk[c >> 1] = pack_bf16x2(v0 ? a0 : 0.f, v1 ? a1 : 0.f);
-                        pv[c] = v0 ? d0 : 0.f;
-                        pv[c + 1] = v1 ? d1 : 0.f;
-                    }
+                    tmem_st16(tX + 16u * k, pk);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(KV_P_FULL + k));
                 }
-                // P^T over the warpgroup's own S^T columns (already read): 64 values in 32 columns.
-                tmem_st16(tX, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-                tmem_st16(tX + 16u, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(KV_P_FULL));
 
                 if (!warp_wait(KV_DP_FULL, g & 1)) { ok = false; break; }
                 tc_fence_after();
@@ -525,11 +545,11 @@ __global__ void __launch_bounds__(320, 1)
                         }
                     }
                     tmem_st16(tY + 16u * k, pd);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(KV_DS_FULL + k));
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(KV_DS_FULL));
             }
             if (!ok) break;
             // Epilogue: dV and dK (times scale) of this key row, the warpgroup's half of D.

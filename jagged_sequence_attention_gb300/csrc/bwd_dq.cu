@@ -73,10 +73,10 @@ enum {
     DQ_S_FULL = 13,   // +buffer
     DQ_SB_FREE = 15,  // +buffer: the dQ product that read dS from the buffer is done
     DQ_DP_FULL = 17,
-    DQ_DS_FULL = 18,
-    DQ_ACC_FULL = 19,
-    DQ_ACC_EMPTY = 20,
-    DQ_DRAIN = 21,
+    DQ_DS_FULL = 18,  // +chunk: key columns [32k, 32k+32) of both warpgroups' dS are in TMEM
+    DQ_ACC_FULL = 20,
+    DQ_ACC_EMPTY = 21,
+    DQ_DRAIN = 22,
 };
 
 template <int D>
@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         mbar_init(bar(DQ_DP_FULL), 1);
         mbar_init(bar(DQ_DS_FULL), C::kCompWarps);
+        mbar_init(bar(DQ_DS_FULL + 1), C::kCompWarps);
         mbar_init(bar(DQ_ACC_FULL), 1);
         mbar_init(bar(DQ_ACC_EMPTY), C::kCompWarps);
         mbar_init(bar(DQ_DRAIN), 1);
@@ -248,19 +249,27 @@ __global__ void __launch_bounds__(320, 1)
         // for the previous item's epilogue to have read the accumulator.
         auto issue_dq = [&](uint32_t g, bool first) -> bool {
             const uint32_t sb = g & 1, kst = g % 3;
-            if (!warp_wait(DQ_DS_FULL, g & 1)) return false;
-            if (first && !warp_wait(DQ_ACC_EMPTY, (item_it & 1) ^ 1)) return false;
-            tc_fence_after();
             const SDesc dk = kst == 0 ? dKm0 : kst == 1 ? dKm1 : dKm2;
-            if (elect_one()) {
+            // chunk c of warpgroup w covers key rows 64w + 32c .. + 31: K-steps 4w + 2c, +1
 #pragma unroll
-                for (int s = 0; s < C::kKSteps; ++s)
-                    mma_ts(tmem + C::kTmDQ, tmem + sb * 128u + packed_col(s), dk, s * 16 * 128, C::kIdescDQ,
-                           (!first || s > 0));
-                tc_commit(bar(DQ_SB_FREE + sb));
-                tc_commit(bar(DQ_K_EMPTY + kst));
+            for (int c = 0; c < 2; ++c) {
+                if (!warp_wait(DQ_DS_FULL + c, g & 1)) return false;
+                if (c == 0 && first && !warp_wait(DQ_ACC_EMPTY, (item_it & 1) ^ 1)) return false;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int s = 4 * (i >> 1) + 2 * c + (i & 1);
+                        mma_ts(tmem + C::kTmDQ, tmem + sb * 128u + packed_col(s), dk, s * 16 * 128, C::kIdescDQ,
+                               (!first || c > 0 || i > 0));
+                    }
+                    if (c == 1) {
+                        tc_commit(bar(DQ_SB_FREE + sb));
+                        tc_commit(bar(DQ_K_EMPTY + kst));
+                    }
+                }
+                __syncwarp();
             }
-            __syncwarp();
             return true;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
@@ -418,11 +427,11 @@ __global__ void __launch_bounds__(320, 1)
                         pd[c >> 1] = pack_bf16x2(a.x, a.y);
                     }
                     tmem_st16(tS + 16u * k, pd);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(DQ_DS_FULL + k));
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(DQ_DS_FULL));
             }
             if (!ok) break;
             // Epilogue: dQ = scale * accumulator, the warpgroup's half of D.

@@ -447,7 +447,8 @@ __global__ void __launch_bounds__(320, 1)
                         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                         if (full) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(cur[i]));
+                            for (int i = 0; i < 32; i += 2)
+                                m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
                         } else {
                             const int lk = lim - 32 * k;
 #pragma unroll
@@ -467,6 +468,19 @@ __global__ void __launch_bounds__(320, 1)
                     alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_use);
                     if (m_new != m) need_rescale = (j > 0);
                     m = m_new;
+                    // O of this tile is stable here: S_x(j) was issued after P_x(j-1) V
+                    // completed, and P V of step j waits for this tile's P.
+                    if (__any_sync(0xffffffffu, need_rescale)) {
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t r[32];
+                            tmem_ld32(tO + c * 32u, r);
+                            tmem_ld_wait(r);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st32(tO + c * 32u, r);
+                        }
+                    }
                     // pass 2: P = exp2(x - m) (packed FMA folds in -m), packed row sum,
                     // P -> TMEM
                     float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -517,18 +531,6 @@ __global__ void __launch_bounds__(320, 1)
                         tmem_st16(tS + 32u * k, pk);
                         tmem_st16(tS + 32u * k + 16u, pl);
                         if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
-                    }
-                }
-                // O of this tile is stable here: S_x(j) was issued after P_x(j-1) V.
-                if (__any_sync(0xffffffffu, need_rescale)) {
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(tO + c * 32u, r);
-                        tmem_ld_wait(r);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tO + c * 32u, r);
                     }
                 }
                 tmem_st_wait();
