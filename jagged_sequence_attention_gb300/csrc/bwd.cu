@@ -72,6 +72,8 @@ struct KvCfg {
     static constexpr int kSmemBytes = kSmemNeed > 120 * 1024 ? kSmemNeed : 120 * 1024;
     static constexpr int kDSteps = D / 16;   // contraction over head_dim
     static constexpr int kQSteps = BM / 16;  // contraction over query rows
+    // dV/dK issue their K-steps per (warpgroup, 32-column chunk): 2 x 2 x 2 steps
+    static_assert(kQSteps == 8 && kCols == 64, "chunked dV/dK issue assumes 128-row query steps");
     static constexpr uint32_t kTmDV = 0, kTmDK = 128, kTmX = 256, kTmY = 384;
     static constexpr uint32_t kIdescS = make_idesc(kFmtBF16, BN, BM, false, false);
     static constexpr uint32_t kIdescAcc = make_idesc(kFmtBF16, BN, D, false, true);
@@ -98,7 +100,7 @@ enum {
     KV_DRAIN = 21,
 };
 
-template <int D>
+template <int D, bool GDPA>
 __global__ void __launch_bounds__(320, 1)
     jfa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(320, 1)
         // Element (lane, c) has relative position rbase(lane 0) - lane + c: rtab[k] holds
         // the bias of rbase(lane 0) - 31 + k, so the lane reads rrow[c], rrow = rtab + 31 - lane.
         const float* rrow = rtab + 31 - lane;
-        const bool softmax = p.mode == JFA_SOFTMAX;
+        constexpr bool softmax = !GDPA;  // the other mode's code is not compiled in
         const bool gelu = p.mode == JFA_GDPA_GELU_TANH;
         uint32_t step_it = 0, item_it = 0;
         bool ok = true;
@@ -623,19 +625,26 @@ __global__ void jfa_bwd_post_kernel(const float4* __restrict__ acc, T* __restric
     }
 }
 
-template <int D>
-cudaError_t launch_dkdv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+template <int D, bool GDPA>
+cudaError_t launch_dkdv_t_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
     using C = KvCfg<D>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e =
-            cudaFuncSetAttribute(jfa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+            cudaFuncSetAttribute(jfa_bwd_dkdv_kernel<D, GDPA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_dkdv_kernel<D><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
+    jfa_bwd_dkdv_kernel<D, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dkdv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
+    return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                                 : launch_dkdv_t_m<D, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
 }
 
 template <typename TO, typename T, int D>

@@ -55,6 +55,8 @@ struct QCfg {
     static constexpr int kSmemBytes = kSmemNeed > 120 * 1024 ? kSmemNeed : 120 * 1024;
     static constexpr int kDSteps = D / 16;   // contraction over head_dim
     static constexpr int kKSteps = BN / 16;  // contraction over key rows
+    // dQ issues its K-steps per (warpgroup, 32-column chunk): 2 x 2 x 2 steps
+    static_assert(kKSteps == 8 && kCols == 64, "chunked dQ issue assumes 128-key tiles");
     static constexpr uint32_t kTmDP = 256, kTmDQ = 384;
     static constexpr uint32_t kIdescS = make_idesc(kFmtBF16, BM, BN, false, false);
     static constexpr uint32_t kIdescDQ = make_idesc(kFmtBF16, BM, D, false, true);
@@ -79,7 +81,7 @@ enum {
     DQ_DRAIN = 22,
 };
 
-template <int D>
+template <int D, bool GDPA>
 __global__ void __launch_bounds__(320, 1)
     jfa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(320, 1)
         const int c0 = wg * NC;
         const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
         float* bias_w = misc_f + warp * 32;
-        const bool softmax = p.mode == JFA_SOFTMAX;
+        constexpr bool softmax = !GDPA;  // the other mode's code is not compiled in
         const bool gelu = p.mode == JFA_GDPA_GELU_TANH;
         uint32_t kv_it = 0, item_it = 0;
         bool ok = true;
@@ -462,19 +464,26 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == C::kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-template <int D>
-cudaError_t launch_dq_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+template <int D, bool GDPA>
+cudaError_t launch_dq_t_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
     using C = QCfg<D>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e =
-            cudaFuncSetAttribute(jfa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+            cudaFuncSetAttribute(jfa_bwd_dq_kernel<D, GDPA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_dq_kernel<D><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
+    jfa_bwd_dq_kernel<D, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dq_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                        const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
+    return p.mode == JFA_SOFTMAX ? launch_dq_t_m<D, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                                 : launch_dq_t_m<D, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
 }
 
 }  // namespace
