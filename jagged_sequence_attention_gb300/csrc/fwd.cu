@@ -436,9 +436,26 @@ __global__ void __launch_bounds__(320, 1)
                     // pass 1: an upper bound of the row max from the raw scores (one FMNMX
                     // per element): xs * max(s) + the chunk's bias (constant, or the
                     // head's largest).  Any m >= the true max gives the same P / l.
+                    // Fast tiles (no column masked, every chunk's bias one value) take a
+                    // branch-free copy of both passes; the rest take the general one.
+                    const bool fast = full && cmask == (1u << (C::BN / 32)) - 1;
                     float mx = -INFINITY;
                     tmem_ld32(tS, ra);
                     tmem_ld_wait(ra);
+                    if (fast) {
+#pragma unroll
+                        for (int k = 0; k < C::BN / 32; ++k) {
+                            uint32_t (&cur)[32] = (k & 1) ? rb : ra;
+                            uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
+                            if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
+                            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2)
+                                m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
+                            mx = fmaxf(mx, fmaf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), xs, cb[k]));
+                            if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
+                        }
+                    } else {
 #pragma unroll
                     for (int k = 0; k < C::BN / 32; ++k) {
                         uint32_t (&cur)[32] = (k & 1) ? rb : ra;
@@ -458,6 +475,7 @@ __global__ void __launch_bounds__(320, 1)
                         const float mk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                         mx = fmaxf(mx, fmaf(mk, xs, (cmask & (1u << k)) ? cb[k] : bmax));
                         if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
+                    }
                     }
                     // Lazy rescaling: keep the running max unless it grows by more
                     // than 2^8; both O and l use the same stale max, so the final
@@ -487,6 +505,26 @@ __global__ void __launch_bounds__(320, 1)
                                     make_float2(0.f, 0.f)};
                     tmem_ld32(tS, ra);
                     tmem_ld_wait(ra);
+                    if (fast) {
+                        const float2 xs2 = make_float2(xs, xs);
+#pragma unroll
+                        for (int k = 0; k < C::BN / 32; ++k) {
+                            uint32_t (&cur)[32] = (k & 1) ? rb : ra;
+                            uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
+                            if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
+                            const float2 add = make_float2(cb[k] - m_use, cb[k] - m_use);
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                const float2 t2 = fma2(make_float2(__uint_as_float(cur[i]), __uint_as_float(cur[i + 1])), xs2, add);
+                                const float2 e2 = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
+                                rs[(i >> 1) & 3] = add2(rs[(i >> 1) & 3], e2);
+                                pk[i >> 1] = pack_bf16x2(e2.x, e2.y);
+                            }
+                            tmem_st16(tS + 32u * k, pk);
+                            if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
+                        }
+                    } else {
 #pragma unroll
                     for (int k = 0; k < C::BN / 32; ++k) {
                         uint32_t (&cur)[32] = (k & 1) ? rb : ra;
@@ -503,6 +541,7 @@ __global__ void __launch_bounds__(320, 1)
                         }
                         tmem_st16(tS + 32u * k, pk);
                         if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
+                    }
                     }
                     const float2 r01 = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
                     l = l * alpha + (r01.x + r01.y);
