@@ -465,10 +465,26 @@ __global__ void __launch_bounds__(320, 1)
                 // chunk is packed over the warpgroup's own S^T columns (already read) and
                 // signalled at once, so dV can start on it while the next chunk is formed.
                 const float2 xs2 = make_float2(xs, xs);
+                // Fast steps (no column masked, both chunks' bias warp-constant) take a
+                // branch-free copy of the exponent loop.
+                const bool fast = full && cconst[0] && cconst[1];
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     uint32_t pk[16];
-                    if (softmax) {
+                    if (softmax && fast) {
+#pragma unroll
+                        for (int c = 32 * k; c < 32 * k + 32; c += 4) {
+                            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c);
+                            const float2 e0 = fma2(make_float2(pv[c], pv[c + 1]), xs2, make_float2(l4.x, l4.y));
+                            const float2 e1 = fma2(make_float2(pv[c + 2], pv[c + 3]), xs2, make_float2(l4.z, l4.w));
+                            pv[c] = ex2_approx(e0.x);
+                            pv[c + 1] = ex2_approx(e0.y);
+                            pv[c + 2] = ex2_approx(e1.x);
+                            pv[c + 3] = ex2_approx(e1.y);
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) pk[c >> 1] = pack_bf16x2(pv[32 * k + c], pv[32 * k + c + 1]);
+                    } else if (softmax) {
                         // exponent = xs * s + (bias - lse): the staged addend already holds
                         // the bias of a warp-constant chunk; other chunks add it per element
                         // from the relative-position table.
@@ -588,21 +604,40 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == C::kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-// Delta_i = sum_d dO_id * O_id for each (row, head); one 8-lane group per row.
+// Eight consecutive elements of a 16-byte aligned row, as floats (one or two 16-byte
+// read-only loads).
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// Delta_i = sum_d dO_id * O_id for each (row, head): D/8 lanes per row, eight elements
+// (16-byte loads) each, reduced across the lanes.
 template <typename TO, typename T, int D>
 __global__ void jfa_bwd_pre_kernel(const TO* __restrict__ O, const T* __restrict__ dO, float* __restrict__ delta,
                                    int64_t rows) {
-    constexpr int kLanes = 8;
-    constexpr int kPer = D / kLanes;
+    constexpr int kLanes = D / 8;
+    static_assert(kLanes >= 1 && kLanes <= 32 && (32 % kLanes) == 0, "row lanes must tile a warp");
     const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t row = gid / kLanes;
     const int sub = int(gid % kLanes);
     float acc = 0.f;
     if (row < rows) {
-        const TO* o = O + row * D + sub * kPer;
-        const T* g = dO + row * D + sub * kPer;
+        float o[8], g[8];
+        load8(O + row * D + sub * 8, o);
+        load8(dO + row * D + sub * 8, g);
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) acc += float(o[k]) * float(g[k]);
+        for (int k = 0; k < 8; ++k) acc = fmaf(o[k], g[k], acc);
     }
 #pragma unroll
     for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -649,7 +684,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const 
 
 template <typename TO, typename T, int D>
 cudaError_t launch_pre_t(const void* O, const void* dO, float* delta, int64_t rows, cudaStream_t st) {
-    const int64_t threads = rows * 8;
+    const int64_t threads = rows * (D / 8);
     const int block = 256;
     const int64_t grid = (threads + block - 1) / block;
     jfa_bwd_pre_kernel<TO, T, D><<<unsigned(grid), block, 0, st>>>(static_cast<const TO*>(O),

@@ -373,7 +373,21 @@ __global__ void __launch_bounds__(320, 1)
                     tmem_ld_wait(rb2);
                 }
                 // softmax: pv = P = exp2(xs * s + bias - lse); GDPA: pv = act'(scale * s + bias)
-                if (softmax) {
+                const bool fast = full && cconst[0] && cconst[1];
+                if (softmax && fast) {
+                    // branch-free copy for steps with no masked column and warp-constant bias
+                    const float2 xs2 = make_float2(xs, xs);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float2 add = make_float2(cbias[k] - lse_row, cbias[k] - lse_row);
+#pragma unroll
+                        for (int c = 32 * k; c < 32 * k + 32; c += 2) {
+                            const float2 e = fma2(make_float2(pv[c], pv[c + 1]), xs2, add);
+                            pv[c] = ex2_approx(e.x);
+                            pv[c + 1] = ex2_approx(e.y);
+                        }
+                    }
+                } else if (softmax) {
                     const float2 xs2 = make_float2(xs, xs);
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
@@ -403,7 +417,7 @@ __global__ void __launch_bounds__(320, 1)
                         }
                     }
                 }
-                if (!full) {
+                if (!fast && !full) {
 #pragma unroll
                     for (int c = 0; c < NC; ++c) pv[c] = (c < lim) ? pv[c] : 0.f;
                 }
