@@ -225,6 +225,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--partition", action="store_true",
+                    help="strong scaling: one batch, its sequences split across the ranks by the LPT partition "
+                         "(default: weak scaling, each rank its own batch of the workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -243,7 +246,8 @@ def main():
     w = wl.WORKLOADS[args.workload]
     cfg = {"workload": args.workload, "description": w.description, "B": w.B, "H": w.H, "D": w.D,
            "mode": w.mode, "causal": w.causal, "bias": w.bias, "seed": wl.seed_of(w),
-           "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"dp{world} (independent batches)"}
+           "l2": "inputs larger than L2 (no flush needed)",
+           "parallelism": f"dp{world} (" + ("LPT partition of one batch" if args.partition else "independent batches") + ")"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -277,9 +281,13 @@ def main():
     from jagged_sequence_attention_gb300 import jfa
     _build.build()
     dev = torch.device("cuda", torch.cuda.current_device())
-    seed = wl.seed_of(w) + 7919 * rank
-    batch = wl.make(args.workload, device=dev, seed=seed)
+    if args.partition:
+        # every rank draws the same batch and keeps its LPT share of the sequences
+        batch = jfa.shard(wl.make(args.workload, device=dev), rank, world)
+    else:
+        batch = wl.make(args.workload, device=dev, seed=wl.seed_of(w) + 7919 * rank)
     fl_f, fl_b = flops_of(batch)
+    job_flop = fl_f + fl_b  # summed over ranks below: the work all ranks processed
     kbytes = algorithmic_bytes(batch)
     cfg.update({"tokens": int(batch.q_off[-1]), "kv_tokens": int(batch.kv_off[-1]),
                 "unpadded_fwd_flop": fl_f, "unpadded_bwd_flop": fl_b})
@@ -331,8 +339,11 @@ def main():
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
+        jf = torch.tensor([job_flop], dtype=torch.float64, device=dev)
+        dist.all_reduce(jf, op=dist.ReduceOp.SUM)
+        job_flop = float(jf.item())
     ms_step = ms / args.steps
-    value = world * (fl_f + fl_b) / (ms_step / 1e3) / 1e12
+    value = job_flop / (ms_step / 1e3) / 1e12
     peaks = load_peaks()
 
     # dominant kernel: the largest share of device time among the tensor-core kernels
@@ -350,16 +361,21 @@ def main():
                 "algorithmic_bytes_per_launch": kbytes[dom],
                 "flop_per_launch": kflop[dom]}
     kernels = {k: {"ms_per_launch": v[0], "launches": v[1], "share": v[2] / max(1e-9, sum(x[2] for x in per.values())),
-                   **({"tflops": kflop[k] / (v[0] / 1e3) / 1e12} if k in kflop and v[0] > 0 else {})}
+                   **({"tflops": kflop[k] / (v[0] / 1e3) / 1e12,
+                       "gbs": kbytes[k] / (v[0] / 1e3) / 1e9} if k in kflop and v[0] > 0 else {})}
                for k, v in per.items()}
     launches = int(sum(v[1] for v in per.values()))
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "strong" if args.partition else "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "pct_of_bf16_peak_sustained": 100.0 * value / world / peaks["bf16_tflops_sustained"],
             "fwd_tflops": fl_f / (kt["fwd"][0] / max(1, kt["fwd"][1]) / 1e3) / 1e12 if kt["fwd"][1] else None,
+            # backward alone: every backward launch of a step (row terms, dK/dV, dQ, fp32 convert)
+            "bwd_tflops": (fl_b / (sum(per[k][0] for k in ("bwd_pre", "bwd_main", "bwd_dq", "bwd_post")) / 1e3) / 1e12
+                           if per["bwd_main"][1] else None),
             "roofline": roofline, "kernels": kernels, "gpu_launches": launches, "clocks": clocks}
 
     # ---------------------------------------------------------------- end to end through the API
@@ -406,7 +422,7 @@ def main():
             t = torch.tensor([el], dtype=torch.float64, device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             el = float(t.item())
-        line["e2e"] = {"value": world * (fl_f + fl_b) / el / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        line["e2e"] = {"value": job_flop / el / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                        "d2h_bytes_per_step": int(d2h), "ms_per_step": el * 1e3, "steps": args.e2e_steps,
                        "includes": "pinned H2D of Q,K,V,dO,bias,offsets; jfa_plan_create; jfa_fwd; jfa_bwd; "
                                    "D2H of O,lse,dQ,dK,dV"}

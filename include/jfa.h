@@ -187,6 +187,20 @@ jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offset
                               int32_t H, int32_t causal, int32_t pass, int32_t n_ctas,
                               int32_t* items, int32_t* cta_offsets, int64_t* cta_cost);
 
+/* Data-parallel split, host only (no GPU needed).  Sequences are independent, so a
+ * batch shards across GPUs with no exchange (GEM articles: jagged batches with long
+ * and short sequences, where balance decides throughput).  Each sequence is costed by
+ * the tensor-core products its forward and backward issue over all heads, and the
+ * sequences are assigned longest-first to the least loaded of n_parts parts
+ * (deterministic: ties go to the lower part and the lower sequence index).
+ *   part_of_seq[B] receives each sequence's part; part_cost[n_parts] (may be NULL)
+ *   each part's total cost.  The greedy bound holds: the most loaded part exceeds
+ *   the least loaded by at most one sequence's cost.
+ * Errors: INVALID_ARG (bad offsets, H < 1, n_parts < 1, causal not 0/1). */
+jfa_status jfa_partition_sequences(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
+                                   int32_t H, int32_t causal, int32_t n_parts, int32_t* part_of_seq,
+                                   int64_t* part_cost);
+
 /* Kernel timing for measurement.  With timing enabled, every kernel launch made for
  * this plan is bracketed by a pair of CUDA events recorded on the launch stream.
  * jfa_plan_kernel_times synchronises those events and returns, per kernel kind

@@ -143,6 +143,15 @@ jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offset
     return JFA_OK;
 }
 
+jfa_status jfa_partition_sequences(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H,
+                                   int32_t causal, int32_t n_parts, int32_t* part_of_seq, int64_t* part_cost) {
+    if (H < 1 || n_parts < 1 || (causal != 0 && causal != 1) || (B > 0 && !part_of_seq)) return JFA_ERR_INVALID_ARG;
+    jfa_status s = validate_offsets(q_offsets, kv_offsets, B);
+    if (s != JFA_OK) return s;
+    partition_sequences(q_offsets, kv_offsets, B, H, causal, n_parts, part_of_seq, part_cost);
+    return JFA_OK;
+}
+
 jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H, int32_t D,
                            int32_t mode, int32_t causal, int32_t offsets_on_device, void* stream, jfa_plan* out) {
     if (!out) return JFA_ERR_INVALID_ARG;

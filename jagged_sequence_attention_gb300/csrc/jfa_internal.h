@@ -98,6 +98,10 @@ void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
                     int32_t causal, int32_t pass, int32_t n_ctas, WorkItem* items,
                     int32_t* cta_off, int64_t* cta_cost);
 
+int64_t sequence_cost(int64_t q_len, int64_t kv_len, int32_t H, int32_t causal);
+void partition_sequences(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H, int32_t causal,
+                         int32_t n_parts, int32_t* part_of_seq, int64_t* part_cost);
+
 // Kernel launchers (fwd.cu, bwd.cu, bwd_dq.cu).  Return cudaSuccess or the launch error.
 cudaError_t launch_fwd(int dtype, int o_dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const FwdParams& p, int grid, cudaStream_t st);

@@ -150,4 +150,42 @@ void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
         for (int32_t c = 0; c < n_ctas; ++c) cta_cost[c] = load[size_t(c)];
 }
 
+// Data-parallel split of a batch: sequences are independent problems, so a batch
+// shards across GPUs with no exchange.  Each sequence is costed by the tensor-core
+// products its forward and backward issue over all heads (two forward, four dK/dV and
+// three dQ products per visited 128x128 score tile, plus a per-tile constant), and the
+// sequences go longest-first to the least loaded part (greedy LPT, ties to the lower
+// part and the lower sequence index, so the result is deterministic).
+int64_t sequence_cost(int64_t q_len, int64_t kv_len, int32_t H, int32_t causal) {
+    const int64_t nq = ceil_div(q_len, kFwdBM), nk = ceil_div(kv_len, kBwdBN);
+    int64_t tiles = 0;
+    for (int64_t t = 0; t < nq; ++t) tiles += fwd_tiles_of(q_len, kv_len, t, causal);
+    return int64_t(H) * (9 * tiles + 2 * (nq + nk));
+}
+
+void partition_sequences(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H, int32_t causal,
+                         int32_t n_parts, int32_t* part_of_seq, int64_t* part_cost) {
+    std::vector<std::pair<int64_t, int32_t>> order(size_t(B > 0 ? B : 0));
+    for (int32_t b = 0; b < B; ++b)
+        order[size_t(b)] = {sequence_cost(q_off[b + 1] - q_off[b], kv_off[b + 1] - kv_off[b], H, causal), b};
+    std::stable_sort(order.begin(), order.end(),
+                     [](const std::pair<int64_t, int32_t>& a, const std::pair<int64_t, int32_t>& b) {
+                         return a.first > b.first;
+                     });
+    using Slot = std::pair<int64_t, int32_t>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int32_t c = 0; c < n_parts; ++c) heap.push({0, c});
+    std::vector<int64_t> load(size_t(n_parts), 0);
+    for (const auto& o : order) {
+        Slot sl = heap.top();
+        heap.pop();
+        part_of_seq[o.second] = sl.second;
+        sl.first += o.first;
+        load[size_t(sl.second)] = sl.first;
+        heap.push(sl);
+    }
+    if (part_cost)
+        for (int32_t c = 0; c < n_parts; ++c) part_cost[c] = load[size_t(c)];
+}
+
 }  // namespace jfa

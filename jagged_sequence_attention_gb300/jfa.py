@@ -30,7 +30,8 @@ DTYPES = {torch.bfloat16: JFA_BF16, torch.float32: JFA_F32}
 
 EXPORTED = ["jfa_plan_create", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd_workspace_size",
             "jfa_bwd", "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build",
-            "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times", "jfa_bwd_static_scratch"]
+            "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times", "jfa_bwd_static_scratch",
+            "jfa_partition_sequences"]
 
 
 class JFAError(RuntimeError):
@@ -60,6 +61,7 @@ def lib():
         L.jfa_bwd.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
         L.jfa_bwd_static_scratch.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp]
         L.jfa_plan_device_status.argtypes = [vp, vp]
+        L.jfa_partition_sequences.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp]
         L.jfa_worklist_size.argtypes = [vp, vp, i32, i32, i32, i32, P(i64)]
         L.jfa_worklist_build.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
         L.jfa_plan_set_timing.argtypes = [vp, i32]
@@ -68,7 +70,7 @@ def lib():
         L.jfa_status_string.restype = ctypes.c_char_p
         for name in ("jfa_plan_create", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
                      "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build", "jfa_plan_set_timing",
-                     "jfa_plan_kernel_times", "jfa_bwd_static_scratch"):
+                     "jfa_plan_kernel_times", "jfa_bwd_static_scratch", "jfa_partition_sequences"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -241,6 +243,29 @@ def jfa_plan_kernel_times(plan: Plan) -> dict:
     n = (ctypes.c_int64 * len(KERNEL_KINDS))()
     _check("jfa_plan_kernel_times", lib().jfa_plan_kernel_times(plan.handle, ms, n))
     return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def jfa_partition_sequences(q_offsets, kv_offsets, H: int, causal: bool, n_parts: int):
+    """Host LPT split of a batch's sequences over n_parts GPUs.  Returns (part_of_seq int32 [B],
+    part_cost int64 [n_parts])."""
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    B = qo.size - 1
+    part = np.zeros(max(B, 1), dtype=np.int32)
+    cost = np.zeros(int(n_parts), dtype=np.int64)
+    _check("jfa_partition_sequences", lib().jfa_partition_sequences(
+        qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p), int(B), int(H), int(bool(causal)),
+        int(n_parts), part.ctypes.data_as(ctypes.c_void_p), cost.ctypes.data_as(ctypes.c_void_p)))
+    return part[:B], cost
+
+
+def shard(batch, rank: int, world: int):
+    """The sequences of `batch` that rank `rank` of `world` processes (a workloads.Batch
+    subset, repacked), by the LPT split above.  Sequences are independent, so results of
+    the shards are exactly the full batch's results for those sequences."""
+    from . import workloads
+    part, _ = jfa_partition_sequences(batch.q_off, batch.kv_off, batch.H, batch.causal, world)
+    seqs = np.nonzero(part == rank)[0]
+    return workloads.subset(batch, seqs)
 
 
 def jfa_worklist_size(q_offsets, kv_offsets, H: int, causal: bool, pass_: int) -> int:
