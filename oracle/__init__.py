@@ -55,10 +55,10 @@ def _load():
             lib.oracle_act_grad.restype = d
             lib.oracle_max_threads.restype = ctypes.c_int
             common = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(i32), P(i32)]
-            lib.oracle_fwd.argtypes = common + [P(d)] * 3 + [ctypes.c_int, ctypes.c_int, P(d), d,
+            lib.oracle_fwd.argtypes = common + [P(d)] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(d), d,
                                                              P(d), P(d), ctypes.c_int]
             lib.oracle_fwd.restype = ctypes.c_int
-            lib.oracle_bwd.argtypes = common + [P(d)] * 4 + [ctypes.c_int, ctypes.c_int, P(d), d,
+            lib.oracle_bwd.argtypes = common + [P(d)] * 4 + [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(d), d,
                                                              P(d), P(d), P(d), ctypes.c_int]
             lib.oracle_bwd.restype = ctypes.c_int
             _lib = lib
@@ -105,8 +105,9 @@ def max_threads() -> int:
 
 
 def fwd(q_off, kv_off, Q, K, V, *, mode="softmax", causal=False, bias=None, scale=None,
-        nthreads=0):
-    """Returns (O [Tq,H,D] fp64, LSE [Tq,H] fp64)."""
+        nthreads=0, window=None):
+    """Returns (O [Tq,H,D] fp64, LSE [Tq,H] fp64).  window W (None: no window): key j is
+    allowed for query i only if j >= i + (kv_len - q_len) - W."""
     lib = _load()
     q_off, kv_off, Q, K, V = _check(q_off, kv_off, Q, K, V)
     B = q_off.size - 1
@@ -117,6 +118,7 @@ def fwd(q_off, kv_off, Q, K, V, *, mode="softmax", causal=False, bias=None, scal
     LSE = np.zeros((Q.shape[0], H), dtype=np.float64)
     rc = lib.oracle_fwd(B, H, D, _ptr(q_off, ctypes.c_int32), _ptr(kv_off, ctypes.c_int32),
                         _ptr(Q), _ptr(K), _ptr(V), MODES[mode], int(bool(causal)),
+                        -1 if window is None else int(window),
                         None if b is None else _ptr(b), scale, _ptr(O), _ptr(LSE), int(nthreads))
     if rc != 0:
         raise MemoryError("oracle_fwd failed")
@@ -124,7 +126,7 @@ def fwd(q_off, kv_off, Q, K, V, *, mode="softmax", causal=False, bias=None, scal
 
 
 def bwd(q_off, kv_off, Q, K, V, dO, *, mode="softmax", causal=False, bias=None, scale=None,
-        nthreads=0):
+        nthreads=0, window=None):
     """Returns (dQ, dK, dV), fp64, same shapes as Q, K, V."""
     lib = _load()
     q_off, kv_off, Q, K, V = _check(q_off, kv_off, Q, K, V)
@@ -138,6 +140,7 @@ def bwd(q_off, kv_off, Q, K, V, dO, *, mode="softmax", causal=False, bias=None, 
     dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
     rc = lib.oracle_bwd(B, H, D, _ptr(q_off, ctypes.c_int32), _ptr(kv_off, ctypes.c_int32),
                         _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), MODES[mode], int(bool(causal)),
+                        -1 if window is None else int(window),
                         None if b is None else _ptr(b), scale, _ptr(dQ), _ptr(dK), _ptr(dV),
                         int(nthreads))
     if rc != 0:

@@ -24,6 +24,11 @@
  *    j <= i + (kv_len - q_len);
  *  - the bias is a per-head table of 32 relative-position buckets,
  *    r = |i + (kv_len - q_len) - j|, bucket(r) = min(31, floor(log2((1+r)^2)));
+ *  - sliding window (aihot.vn GEM article, section "BlockAttention": each token
+ *    limited to its neighbouring events, O(L * window) work): with window W >= 0,
+ *    key j is allowed for query i only if j >= i + (kv_len - q_len) - W, i.e. the
+ *    aligned position itself and the W keys before it (together with the causal
+ *    bound); W < 0 means no window;
  *  - a query row with no allowed key gives o = 0 and lse = -inf, and all
  *    gradients through it are 0;
  *  - GDPA masked entries contribute exactly 0 (the activation is never evaluated
@@ -110,9 +115,12 @@ static double score(const double *qi, const double *kj, int D, double scale,
     return s;
 }
 
-static int allowed(int causal, int64_t i, int64_t j, int64_t q_len, int64_t kv_len)
+static int allowed(int causal, int window, int64_t i, int64_t j, int64_t q_len, int64_t kv_len)
 {
-    return !causal || j <= i + (kv_len - q_len);
+    const int64_t ip = i + (kv_len - q_len);  /* the query's aligned key position */
+    if (causal && j > ip) return 0;
+    if (window >= 0 && j < ip - window) return 0;
+    return 1;
 }
 
 static void set_threads(int nthreads)
@@ -140,7 +148,7 @@ int oracle_max_threads(void)
  */
 int oracle_fwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                const double *Q, const double *K, const double *V, int mode, int causal,
-               const double *bias, double scale, double *O, double *LSE, int nthreads)
+               int window, const double *bias, double scale, double *O, double *LSE, int nthreads)
 {
     int failed = 0;
     set_threads(nthreads);
@@ -165,7 +173,7 @@ int oracle_fwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                 double m = -INFINITY;
                 int64_t n_allowed = 0;
                 for (int64_t j = 0; j < kv_len; j++) {
-                    if (!allowed(causal, i, j, q_len, kv_len)) continue;
+                    if (!allowed(causal, window, i, j, q_len, kv_len)) continue;
                     s[j] = score(qi, K + ((k0 + j) * H + h) * D, D, scale, bias_h, i, j, q_len, kv_len);
                     if (s[j] > m) m = s[j];
                     n_allowed++;
@@ -177,9 +185,9 @@ int oracle_fwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                     }
                     double l = 0.0;
                     for (int64_t j = 0; j < kv_len; j++)
-                        if (allowed(causal, i, j, q_len, kv_len)) l += exp(s[j] - m);
+                        if (allowed(causal, window, i, j, q_len, kv_len)) l += exp(s[j] - m);
                     for (int64_t j = 0; j < kv_len; j++) {
-                        if (!allowed(causal, i, j, q_len, kv_len)) continue;
+                        if (!allowed(causal, window, i, j, q_len, kv_len)) continue;
                         double p = exp(s[j] - m) / l;
                         const double *vj = V + ((k0 + j) * H + h) * D;
                         for (int d = 0; d < D; d++) oi[d] += p * vj[d];
@@ -187,7 +195,7 @@ int oracle_fwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                     *lse = m + log(l);
                 } else {
                     for (int64_t j = 0; j < kv_len; j++) {
-                        if (!allowed(causal, i, j, q_len, kv_len)) continue;
+                        if (!allowed(causal, window, i, j, q_len, kv_len)) continue;
                         double a = oracle_act(mode, s[j]);
                         const double *vj = V + ((k0 + j) * H + h) * D;
                         for (int d = 0; d < D; d++) oi[d] += a * vj[d];
@@ -212,8 +220,8 @@ int oracle_fwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
  */
 int oracle_bwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                const double *Q, const double *K, const double *V, const double *dO, int mode,
-               int causal, const double *bias, double scale, double *dQ, double *dK, double *dV,
-               int nthreads)
+               int causal, int window, const double *bias, double scale, double *dQ, double *dK,
+               double *dV, int nthreads)
 {
     int failed = 0;
     set_threads(nthreads);
@@ -249,7 +257,7 @@ int oracle_bwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                 double m = -INFINITY;
                 int64_t n_allowed = 0;
                 for (int64_t j = 0; j < kv_len; j++) {
-                    if (!allowed(causal, i, j, q_len, kv_len)) continue;
+                    if (!allowed(causal, window, i, j, q_len, kv_len)) continue;
                     s[j] = score(qi, K + ((k0 + j) * H + h) * D, D, scale, bias_h, i, j, q_len, kv_len);
                     if (s[j] > m) m = s[j];
                     n_allowed++;
@@ -258,16 +266,16 @@ int oracle_bwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                 if (mode == ORACLE_SOFTMAX) {
                     double l = 0.0;
                     for (int64_t j = 0; j < kv_len; j++)
-                        if (allowed(causal, i, j, q_len, kv_len)) l += exp(s[j] - m);
+                        if (allowed(causal, window, i, j, q_len, kv_len)) l += exp(s[j] - m);
                     for (int64_t j = 0; j < kv_len; j++)
-                        p[j] = allowed(causal, i, j, q_len, kv_len) ? exp(s[j] - m) / l : 0.0;
+                        p[j] = allowed(causal, window, i, j, q_len, kv_len) ? exp(s[j] - m) / l : 0.0;
                 } else {
                     for (int64_t j = 0; j < kv_len; j++)
-                        p[j] = allowed(causal, i, j, q_len, kv_len) ? oracle_act(mode, s[j]) : 0.0;
+                        p[j] = allowed(causal, window, i, j, q_len, kv_len) ? oracle_act(mode, s[j]) : 0.0;
                 }
                 double delta = 0.0;
                 for (int64_t j = 0; j < kv_len; j++) {
-                    if (!allowed(causal, i, j, q_len, kv_len)) {
+                    if (!allowed(causal, window, i, j, q_len, kv_len)) {
                         dp[j] = 0.0;
                         continue;
                     }
@@ -278,7 +286,7 @@ int oracle_bwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                     delta += p[j] * dp[j];
                 }
                 for (int64_t j = 0; j < kv_len; j++) {
-                    if (!allowed(causal, i, j, q_len, kv_len)) continue;
+                    if (!allowed(causal, window, i, j, q_len, kv_len)) continue;
                     double ds;
                     if (mode == ORACLE_SOFTMAX)
                         ds = p[j] * (dp[j] - delta);
