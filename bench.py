@@ -41,21 +41,23 @@ UNIT = "TFLOP/s"
 # ----------------------------------------------------------------------------- FLOPs / bytes
 
 
-def allowed_pairs(q_lens, kv_lens, causal):
+def allowed_pairs(q_lens, kv_lens, causal, window=None):
     q = np.asarray(q_lens, dtype=np.int64)
     kv = np.asarray(kv_lens, dtype=np.int64)
     if not causal:
         return int(np.sum(q * kv))
     tot = 0
     for a, b in zip(q.tolist(), kv.tolist()):
-        # rows i = 0..a-1 see min(b, i + 1 + b - a) keys (at least 0)
-        i = np.arange(a, dtype=np.int64)
-        tot += int(np.clip(i + 1 + b - a, 0, b).sum())
+        # row i sees keys [max(0, i' - W), min(b - 1, i')], i' = i + b - a
+        ip = np.arange(a, dtype=np.int64) + (b - a)
+        hi = np.minimum(ip, b - 1)
+        lo = np.zeros_like(ip) if window is None else np.maximum(ip - window, 0)
+        tot += int(np.clip(hi - lo + 1, 0, None).sum())
     return tot
 
 
 def flops_of(batch):
-    pairs = allowed_pairs(batch.q_lens, batch.kv_lens, batch.causal)
+    pairs = allowed_pairs(batch.q_lens, batch.kv_lens, batch.causal, batch.window)
     fwd = 4.0 * batch.D * batch.H * pairs
     return fwd, 2.5 * fwd
 
@@ -183,7 +185,8 @@ def oracle_sample(batch, target_seconds=15.0):
     budget = 2.7e9 * target_seconds
     seqs, tot = [], 0.0
     for b in order:
-        f = 3.5 * 4.0 * batch.D * batch.H * allowed_pairs([batch.q_lens[b]], [batch.kv_lens[b]], batch.causal)
+        f = 3.5 * 4.0 * batch.D * batch.H * allowed_pairs([batch.q_lens[b]], [batch.kv_lens[b]], batch.causal,
+                                                          batch.window)
         if seqs and tot + f > budget:
             break
         seqs.append(int(b))
@@ -200,9 +203,10 @@ def run_oracle_once(cpu_batch):
     b = None if cpu_batch.bias is None else f64(cpu_batch.bias)
     t0 = time.perf_counter()
     oracle.fwd(cpu_batch.q_off, cpu_batch.kv_off, f64(cpu_batch.Q), f64(cpu_batch.K), f64(cpu_batch.V),
-               mode=cpu_batch.mode, causal=cpu_batch.causal, bias=b, scale=cpu_batch.scale)
+               mode=cpu_batch.mode, causal=cpu_batch.causal, bias=b, scale=cpu_batch.scale, window=cpu_batch.window)
     oracle.bwd(cpu_batch.q_off, cpu_batch.kv_off, f64(cpu_batch.Q), f64(cpu_batch.K), f64(cpu_batch.V),
-               f64(cpu_batch.dO), mode=cpu_batch.mode, causal=cpu_batch.causal, bias=b, scale=cpu_batch.scale)
+               f64(cpu_batch.dO), mode=cpu_batch.mode, causal=cpu_batch.causal, bias=b, scale=cpu_batch.scale,
+               window=cpu_batch.window)
     return time.perf_counter() - t0
 
 
@@ -245,7 +249,7 @@ def main():
 
     w = wl.WORKLOADS[args.workload]
     cfg = {"workload": args.workload, "description": w.description, "B": w.B, "H": w.H, "D": w.D,
-           "mode": w.mode, "causal": w.causal, "bias": w.bias, "seed": wl.seed_of(w),
+           "mode": w.mode, "causal": w.causal, "bias": w.bias, "window": w.window, "seed": wl.seed_of(w),
            "l2": "inputs larger than L2 (no flush needed)",
            "parallelism": f"dp{world} (" + ("LPT partition of one batch" if args.partition else "independent batches") + ")"}
 
@@ -293,7 +297,8 @@ def main():
                 "unpadded_fwd_flop": fl_f, "unpadded_bwd_flop": fl_b})
 
     stream = torch.cuda.current_stream()
-    plan = jfa.jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal)
+    plan = jfa.jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal,
+                               window=batch.window)
     O = torch.empty_like(batch.Q)
     lse = torch.empty((batch.Q.shape[0], batch.H), dtype=torch.float32, device=dev)
     dQ, dK, dV = torch.empty_like(batch.Q), torch.empty_like(batch.K), torch.empty_like(batch.V)
@@ -400,7 +405,7 @@ def main():
             dOd.copy_(hdO, non_blocking=True)
             if hbias is not None:
                 bias_d.copy_(hbias, non_blocking=True)
-            p2 = jfa.jfa_plan_create(q_off, kv_off, batch.H, batch.D, batch.mode, batch.causal)
+            p2 = jfa.jfa_plan_create(q_off, kv_off, batch.H, batch.D, batch.mode, batch.causal, window=batch.window)
             jfa.jfa_fwd(p2, dQd, dKd, dVd, bias_d, batch.scale, O=O, lse=lse)
             jfa.jfa_bwd(p2, dQd, dKd, dVd, O, dOd, lse, bias_d, batch.scale, dQ=dQ, dK=dK, dV=dV, workspace=ws)
             hO.copy_(O, non_blocking=True)

@@ -13,7 +13,8 @@
  *
  * For sequence b, head h, query row i (0-based within the sequence), key row j:
  *   s_ij   = scale * <q_i, k_j> + bias[h, bucket(|i + (kv_len - q_len) - j|)]
- *   allowed(i, j) = !causal || j <= i + (kv_len - q_len)        (bottom-right causal)
+ *   allowed(i, j) = (!causal || j <= i') && (W < 0 || j >= i' - W),  i' = i + (kv_len - q_len)
+ *                   (bottom-right causal; optional sliding window of W keys before i')
  *   SOFTMAX: o_i = sum_j softmax_j(s_ij) v_j over allowed j;  lse_i = log sum exp s_ij
  *   GDPA:    o_i = sum_j act(s_ij) v_j over allowed j, act = tanh-GELU or SiLU
  *   bucket(r) = min(31, floor(log2((1 + r)^2)))   (exact integer arithmetic)
@@ -85,6 +86,19 @@ jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, 
                            int32_t H, int32_t D, int32_t mode, int32_t causal,
                            int32_t offsets_on_device, void* stream, jfa_plan* out);
 
+/*
+ * jfa_plan_create with a sliding window (aihot.vn GEM article, section
+ * "BlockAttention": each token limited to its neighbouring events, O(L * window)
+ * work): with window W >= 0, query i attends only to keys i' - W <= j <= i', where
+ * i' = i + (kv_len - q_len) is its aligned causal position; the kernels skip every
+ * tile outside the band.  window = -1 is jfa_plan_create.  A window requires causal
+ * = 1.  Errors: those of jfa_plan_create; INVALID_ARG for window < -1 or a window
+ * without causal.
+ */
+jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
+                              int32_t H, int32_t D, int32_t mode, int32_t causal, int32_t window,
+                              int32_t offsets_on_device, void* stream, jfa_plan* out);
+
 /* Frees a plan and its device memory (cudaFree synchronises the device, so launches
  * still using the plan finish first).  NULL is accepted. */
 jfa_status jfa_plan_destroy(jfa_plan plan);
@@ -92,7 +106,8 @@ jfa_status jfa_plan_destroy(jfa_plan plan);
 /*
  * Plan facts for callers and tests, written to info[0..n): T_q, T_kv, B, H, D,
  * mode, causal, forward work items, forward grid, backward dK/dV work items, its
- * grid, SM count, backward dQ work items, its grid.  n may be smaller than 14.
+ * grid, SM count, backward dQ work items, its grid, window (-1: none).  n may be
+ * smaller than 15.
  */
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
 
@@ -180,11 +195,13 @@ jfa_status jfa_plan_device_status(jfa_plan plan, void* stream);
  * tiles).  jfa_worklist_size gives the number of work items; jfa_worklist_build
  * writes items as int32 quadruples (sequence, head, tile index, inner tiles
  * visited) grouped by CTA, cta_offsets[n_ctas+1] delimiting each CTA's items, and
- * optionally each CTA's total cost in units of tensor-core products. */
+ * optionally each CTA's total cost in units of tensor-core products.  window as in
+ * jfa_plan_create_ex (-1: none).  With a window the inner tiles are a band: a
+ * forward pair streams the union of its two query tiles' key ranges. */
 jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
-                             int32_t H, int32_t causal, int32_t pass, int64_t* n_items);
+                             int32_t H, int32_t causal, int32_t window, int32_t pass, int64_t* n_items);
 jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
-                              int32_t H, int32_t causal, int32_t pass, int32_t n_ctas,
+                              int32_t H, int32_t causal, int32_t window, int32_t pass, int32_t n_ctas,
                               int32_t* items, int32_t* cta_offsets, int64_t* cta_cost);
 
 /* Data-parallel split, host only (no GPU needed).  Sequences are independent, so a
@@ -196,10 +213,12 @@ jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offset
  *   part_of_seq[B] receives each sequence's part; part_cost[n_parts] (may be NULL)
  *   each part's total cost.  The greedy bound holds: the most loaded part exceeds
  *   the least loaded by at most one sequence's cost.
- * Errors: INVALID_ARG (bad offsets, H < 1, n_parts < 1, causal not 0/1). */
+ * window as in jfa_plan_create_ex (-1: none).
+ * Errors: INVALID_ARG (bad offsets, H < 1, n_parts < 1, causal not 0/1, a window
+ * without causal). */
 jfa_status jfa_partition_sequences(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
-                                   int32_t H, int32_t causal, int32_t n_parts, int32_t* part_of_seq,
-                                   int64_t* part_cost);
+                                   int32_t H, int32_t causal, int32_t window, int32_t n_parts,
+                                   int32_t* part_of_seq, int64_t* part_cost);
 
 /* Kernel timing for measurement.  With timing enabled, every kernel launch made for
  * this plan is bracketed by a pair of CUDA events recorded on the launch stream.

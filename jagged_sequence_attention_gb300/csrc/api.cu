@@ -122,8 +122,9 @@ const char* jfa_status_string(int32_t s) {
 }
 
 jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H,
-                             int32_t causal, int32_t pass, int64_t* n_items) {
+                             int32_t causal, int32_t window, int32_t pass, int64_t* n_items) {
     if (!n_items || H < 1 || pass < kPassFwd || pass > kPassBwdQ) return JFA_ERR_INVALID_ARG;
+    if (window < -1 || (window >= 0 && causal != 1)) return JFA_ERR_INVALID_ARG;
     jfa_status s = validate_offsets(q_offsets, kv_offsets, B);
     if (s != JFA_OK) return s;
     *n_items = count_items(q_offsets, kv_offsets, B, H, causal, pass);
@@ -131,34 +132,44 @@ jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets
 }
 
 jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H,
-                              int32_t causal, int32_t pass, int32_t n_ctas, int32_t* items,
+                              int32_t causal, int32_t window, int32_t pass, int32_t n_ctas, int32_t* items,
                               int32_t* cta_offsets, int64_t* cta_cost) {
     if (H < 1 || n_ctas < 1 || !cta_offsets || pass < kPassFwd || pass > kPassBwdQ) return JFA_ERR_INVALID_ARG;
+    if (window < -1 || (window >= 0 && causal != 1)) return JFA_ERR_INVALID_ARG;
     jfa_status s = validate_offsets(q_offsets, kv_offsets, B);
     if (s != JFA_OK) return s;
     const int64_t n = count_items(q_offsets, kv_offsets, B, H, causal, pass);
     if (n > 0 && !items) return JFA_ERR_INVALID_ARG;
-    build_worklist(q_offsets, kv_offsets, B, H, causal, pass, n_ctas, reinterpret_cast<WorkItem*>(items),
+    build_worklist(q_offsets, kv_offsets, B, H, causal, window, pass, n_ctas, reinterpret_cast<WorkItem*>(items),
                    cta_offsets, cta_cost);
     return JFA_OK;
 }
 
 jfa_status jfa_partition_sequences(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H,
-                                   int32_t causal, int32_t n_parts, int32_t* part_of_seq, int64_t* part_cost) {
+                                   int32_t causal, int32_t window, int32_t n_parts, int32_t* part_of_seq,
+                                   int64_t* part_cost) {
     if (H < 1 || n_parts < 1 || (causal != 0 && causal != 1) || (B > 0 && !part_of_seq)) return JFA_ERR_INVALID_ARG;
+    if (window < -1 || (window >= 0 && causal != 1)) return JFA_ERR_INVALID_ARG;
     jfa_status s = validate_offsets(q_offsets, kv_offsets, B);
     if (s != JFA_OK) return s;
-    partition_sequences(q_offsets, kv_offsets, B, H, causal, n_parts, part_of_seq, part_cost);
+    partition_sequences(q_offsets, kv_offsets, B, H, causal, window, n_parts, part_of_seq, part_cost);
     return JFA_OK;
 }
 
 jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H, int32_t D,
                            int32_t mode, int32_t causal, int32_t offsets_on_device, void* stream, jfa_plan* out) {
+    return jfa_plan_create_ex(q_offsets, kv_offsets, B, H, D, mode, causal, -1, offsets_on_device, stream, out);
+}
+
+jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H, int32_t D,
+                              int32_t mode, int32_t causal, int32_t window, int32_t offsets_on_device, void* stream,
+                              jfa_plan* out) {
     if (!out) return JFA_ERR_INVALID_ARG;
     *out = nullptr;
     if (!q_offsets || !kv_offsets || B < 0 || H < 1 || H > 65535) return JFA_ERR_INVALID_ARG;
     if (mode != JFA_SOFTMAX && mode != JFA_GDPA_GELU_TANH && mode != JFA_GDPA_SILU) return JFA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return JFA_ERR_INVALID_ARG;
+    if (window < -1 || (window >= 0 && causal != 1)) return JFA_ERR_INVALID_ARG;
     if (D != 32 && D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -188,6 +199,7 @@ jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, 
     p->D = D;
     p->mode = mode;
     p->causal = causal;
+    p->window = window;
     p->Tq = qo[size_t(B)];
     p->Tkv = ko[size_t(B)];
     p->device = dev;
@@ -206,9 +218,9 @@ jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, 
     std::vector<WorkItem> bi(size_t(std::max<int64_t>(1, p->n_bwd_items)));
     std::vector<WorkItem> qi(size_t(std::max<int64_t>(1, p->n_dq_items)));
     std::vector<int32_t> fo(size_t(p->fwd_grid) + 1), bo(size_t(p->bwd_grid) + 1), qio(size_t(p->dq_grid) + 1);
-    build_worklist(qo.data(), ko.data(), B, H, causal, kPassFwd, p->fwd_grid, fi.data(), fo.data(), nullptr);
-    build_worklist(qo.data(), ko.data(), B, H, causal, kPassBwdKV, p->bwd_grid, bi.data(), bo.data(), nullptr);
-    build_worklist(qo.data(), ko.data(), B, H, causal, kPassBwdQ, p->dq_grid, qi.data(), qio.data(), nullptr);
+    build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassFwd, p->fwd_grid, fi.data(), fo.data(), nullptr);
+    build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassBwdKV, p->bwd_grid, bi.data(), bo.data(), nullptr);
+    build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassBwdQ, p->dq_grid, qi.data(), qio.data(), nullptr);
 
     // One device block: offsets, status word, work lists (16-byte aligned pieces).
     const size_t off_bytes = round_up((size_t(B) + 1) * 4, 256);
@@ -270,10 +282,10 @@ jfa_status jfa_plan_destroy(jfa_plan plan) {
 
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
     if (!plan || !info || n < 0) return JFA_ERR_INVALID_ARG;
-    const int64_t v[14] = {plan->Tq,          plan->Tkv,      plan->B,           plan->H,        plan->D,
+    const int64_t v[15] = {plan->Tq,          plan->Tkv,      plan->B,           plan->H,        plan->D,
                            plan->mode,        plan->causal,   plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items,
-                           plan->bwd_grid,    plan->num_sms,  plan->n_dq_items,  plan->dq_grid};
-    for (int32_t i = 0; i < n && i < 14; ++i) info[i] = v[i];
+                           plan->bwd_grid,    plan->num_sms,  plan->n_dq_items,  plan->dq_grid,  plan->window};
+    for (int32_t i = 0; i < n && i < 15; ++i) info[i] = v[i];
     return JFA_OK;
 }
 
@@ -345,6 +357,7 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
     p.H = plan->H;
     p.mode = plan->mode;
     p.causal = plan->causal;
+    p.window = plan->window;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.bias = bias_kind == JFA_BIAS_RELPOS32 ? bias_table : nullptr;
@@ -413,6 +426,7 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
         p.H = plan->H;
         p.mode = plan->mode;
         p.causal = plan->causal;
+        p.window = plan->window;
         p.scale = scale;
         p.scale_log2 = scale * 1.4426950408889634f;
         p.bias = bias_kind == JFA_BIAS_RELPOS32 ? bias_table : nullptr;

@@ -176,7 +176,8 @@ __global__ void __launch_bounds__(320, 1)
                 if (n == 0) continue;
                 const int b = w.x, h = w.y, nt = w.z;
                 const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0, kv0 = p.kv_off[b];
-                const int first_qt = (q_len + C::BM - 1) / C::BM - n;
+                int first_qt, nq;  // query tiles [first_qt, first_qt + n) see this key tile
+                query_tile_range(q_len, p.kv_off[b + 1] - kv0, nt, p.causal, p.window, first_qt, nq);
                 if (!mbar_wait_bounded(bar(KV_KV_EMPTY), (item_it & 1) ^ 1, abort_flag)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(KV_K_FULL), C::kKVTile);
 #pragma unroll
@@ -374,7 +375,8 @@ __global__ void __launch_bounds__(320, 1)
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
             const int kv0 = p.kv_off[b], kv_len = p.kv_off[b + 1] - kv0;
             const int diag = kv_len - q_len;
-            const int first_qt = (q_len + C::BM - 1) / C::BM - n;
+            int first_qt, nq;  // query tiles [first_qt, first_qt + n) see this key tile
+            query_tile_range(q_len, kv_len, nt, p.causal, p.window, first_qt, nq);
             const int j = nt * C::BN + r;  // key row within the sequence
             const bool key_valid = j < kv_len;
             const size_t krow = (size_t(kv0) + size_t(key_valid ? j : 0)) * size_t(p.H) + size_t(h);
@@ -415,7 +417,9 @@ __global__ void __launch_bounds__(320, 1)
                 del_s[32 + lane] = nd[1];
                 if (i + 1 < n) fetch(qrow0 + C::BM);
                 // subtraction scheme: valid local columns are [lo, hi)
-                const int hi = key_valid ? min(NC, q_len - qrow0 - c0) : 0;
+                int hi = key_valid ? min(NC, q_len - qrow0 - c0) : 0;
+                // sliding window: query i sees key j only while j >= i' - W, i.e. i <= j - diag + W
+                if (p.window >= 0) hi = min(hi, j - diag + p.window + 1 - qrow0 - c0);
                 const int lo = p.causal ? max(0, j - diag - qrow0 - c0) : 0;
                 const bool full = __all_sync(0xffffffffu, lo == 0 && hi == NC);
                 const int rbase = qrow0 + c0 + diag - j;  // relative position of local column 0

@@ -156,6 +156,8 @@ __global__ void __launch_bounds__(320, 1)
                 if (n == 0) continue;
                 const int b = w.x, h = w.y, tq = w.z;
                 const int q0 = p.q_off[b], kv0 = p.kv_off[b];
+                int kf, nk;  // key tiles [kf, kf + n)
+                key_tile_range(p.q_off[b + 1] - q0, p.kv_off[b + 1] - kv0, tq, p.causal, p.window, kf, nk);
                 if (!mbar_wait_bounded(bar(DQ_QDO_EMPTY), (item_it & 1) ^ 1, abort_flag)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(DQ_Q_FULL), C::kQTile);
 #pragma unroll
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(320, 1)
                 for (int j = 0; j < n; ++j, ++kv_it) {
                     const uint32_t kst = kv_it % 3, kph = (kv_it / 3) & 1;
                     const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
-                    const int y = kv0 + j * C::BN;
+                    const int y = kv0 + (kf + j) * C::BN;
                     if (!mbar_wait_bounded(bar(DQ_K_EMPTY + kst), kph ^ 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(bar(DQ_K_FULL + kst), C::kKVTile);
 #pragma unroll
@@ -336,13 +338,17 @@ __global__ void __launch_bounds__(320, 1)
             const float lse_row = (softmax && row_valid) ? p.lse[orow] * 1.4426950408889634f : 0.f;
             const float del_row = (softmax && row_valid) ? p.delta[orow] : 0.f;
             const float xs = softmax ? p.scale_log2 : p.scale;
+            int kf, nk;  // key tiles [kf, kf + n)
+            key_tile_range(q_len, kv_len, tq, p.causal, p.window, kf, nk);
             for (int j = 0; j < n; ++j) {
                 const uint32_t g = kv_it + uint32_t(j), sb = g & 1;
-                const int col0 = j * C::BN + c0;
+                const int col0 = (kf + j) * C::BN + c0;
                 int lim = kv_len - col0;  // subtraction scheme: local columns >= lim are masked
                 if (p.causal) lim = min(lim, row + diag + 1 - col0);
                 if (!row_valid) lim = 0;
-                const bool full = __all_sync(0xffffffffu, lim >= NC);
+                // sliding window: local columns below lo are masked
+                const int lo = p.window >= 0 ? row + diag - p.window - col0 : 0;
+                const bool full = __all_sync(0xffffffffu, lim >= NC && lo <= 0);
                 const int rb = row + diag - col0;  // relative position of local column 0
                 // Lane k tests chunk k for the whole warp: over the warp's rows, chunk k
                 // spans relative positions rb(lane 0) - 32k - 31 .. + 62.
@@ -419,7 +425,7 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 if (!fast && !full) {
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) pv[c] = (c < lim) ? pv[c] : 0.f;
+                    for (int c = 0; c < NC; ++c) pv[c] = (c >= lo && c < lim) ? pv[c] : 0.f;
                 }
 
                 if (!warp_wait(DQ_DP_FULL, g & 1)) { ok = false; break; }

@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(kF32Rows) jfa_fwd_f32_kernel(const float* __re
     const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
     const int k0 = p.kv_off[b], kv_len = p.kv_off[b + 1] - k0;
     if (mt * kF32Rows >= q_len) return;  // second tile of a short last pair (uniform exit)
-    const int n_tiles = fwd_tiles_of(q_len, kv_len, mt, p.causal);
+    int kf, n_tiles;  // key tiles [kf, kf + n_tiles)
+    key_tile_range(q_len, kv_len, mt, p.causal, p.window, kf, n_tiles);
     const int t = threadIdx.x, row = mt * kF32Rows + t;
     const bool valid = row < q_len;
     const int diag = kv_len - q_len;
@@ -69,11 +70,12 @@ __global__ void __launch_bounds__(kF32Rows) jfa_fwd_f32_kernel(const float* __re
         o[d] = 0.f;
     }
     float m = -INFINITY, l = 0.f;
-    // keys up to the causal limit of the tile's last row (the planner's count, in
-    // 128-key units), staged 64 at a time
-    const int kv_end = min(kv_len, n_tiles * kFwdBN);
-    const int lim = p.causal ? min(kv_len, row + diag + 1) : kv_len;  // keys [0, lim) allowed
-    for (int c0 = 0; c0 < kv_end; c0 += kF32Inner) {
+    // keys of the tile's range (causal limit of its last row, window start of its first
+    // row, in 128-key units), staged 64 at a time
+    const int kv_end = min(kv_len, (kf + n_tiles) * kFwdBN);
+    const int lim = p.causal ? min(kv_len, row + diag + 1) : kv_len;  // keys [lo, lim) allowed
+    const int lo = p.window >= 0 ? row + diag - p.window : 0;
+    for (int c0 = kf * kFwdBN; c0 < kv_end; c0 += kF32Inner) {
         __syncthreads();
         for (int e = t; e < kF32Inner * D; e += kF32Rows) {
             const int r = e / D, d = e % D;
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(kF32Rows) jfa_fwd_f32_kernel(const float* __re
             for (int d = 0; d < D; ++d) acc = fmaf(q[d], sK[j][d], acc);
             float x = acc * p.scale;
             if (p.bias) x += sB[bucket_f32(row + diag - (c0 + j))];
-            const bool ok = valid && (c0 + j) < lim;
+            const bool ok = valid && (c0 + j) < lim && (c0 + j) >= lo;
             s[j] = ok ? x : -INFINITY;
             mx = fmaxf(mx, s[j]);
         }
@@ -158,10 +160,12 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
         dk[d] = 0.f;
         dv[d] = 0.f;
     }
-    const int nq = (q_len + kBwdBM - 1) / kBwdBM;
-    const int row_begin = (nq - n) * kBwdBM;
+    int first_qt, nq;  // query tiles [first_qt, first_qt + n) see this key tile
+    query_tile_range(q_len, kv_len, nt, p.causal, p.window, first_qt, nq);
+    const int row_begin = first_qt * kBwdBM;
+    const int row_end = min(q_len, (first_qt + n) * kBwdBM);
     const int n_keys = min(kBwdBN, kv_len - nt * kBwdBN);
-    for (int r0 = row_begin; r0 < q_len; r0 += kF32InnerB) {
+    for (int r0 = row_begin; r0 < row_end; r0 += kF32InnerB) {
         __syncthreads();
         for (int e = t; e < kF32InnerB * D; e += kF32Rows) {
             const int r = e / D, d = e % D;
@@ -179,7 +183,8 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
         __syncthreads();
         for (int i = 0; i < kF32InnerB; ++i) {
             const int row = r0 + i;
-            const bool ok = kvalid && row < q_len && (!p.causal || j <= row + diag);
+            const bool ok = kvalid && row < q_len && (!p.causal || j <= row + diag) &&
+                            (p.window < 0 || j >= row + diag - p.window);
             float ds = 0.f;
             if (ok) {
                 float acc = 0.f, dp = 0.f;

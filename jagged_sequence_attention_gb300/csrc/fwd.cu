@@ -107,7 +107,9 @@ __device__ __forceinline__ void store_row<float>(float* dst, const float* v, int
     for (int i = 0; i < n / 4; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-template <int D, typename OT, bool GDPA>
+// WIN: a sliding window is set (p.window >= 0).  Without it the window arithmetic folds
+// away at compile time, so the plain causal and non-causal paths carry none of it.
+template <int D, typename OT, bool GDPA, bool WIN>
 __global__ void __launch_bounds__(320, 1)
     jfa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -122,6 +124,7 @@ __global__ void __launch_bounds__(320, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     float* bias_s = reinterpret_cast<float*>(smem + C::kOffMisc + 16);
     constexpr bool gdpa = GDPA;
+    const int window = WIN ? p.window : -1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -175,7 +178,10 @@ __global__ void __launch_bounds__(320, 1)
                 if (n == 0) continue;
                 const int b = w.x, h = w.y, pr = w.z;
                 const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0, kv0 = p.kv_off[b];
+                const int kv_len = p.kv_off[b + 1] - kv0;
                 const int ntiles = (2 * pr + 1) * C::BM < q_len ? 2 : 1;
+                int f0, ns, na, nb;  // the pair streams key tiles [f0, f0 + n)
+                pair_stream(q_len, kv_len, pr, p.causal, window, f0, ns, na, nb);
                 if (!mbar_wait_bounded(bar(B_Q_EMPTY), (item_it & 1) ^ 1, abort_flag)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(B_Q_FULL), C::kQBytes * ntiles);
                 for (int tq = 0; tq < ntiles; ++tq)
@@ -186,7 +192,7 @@ __global__ void __launch_bounds__(320, 1)
                 ++item_it;
                 for (int j = 0; j < n; ++j, ++kv_it) {
                     const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
-                    const int y = kv0 + j * C::BN;
+                    const int y = kv0 + (f0 + j) * C::BN;
                     if (!mbar_wait_bounded(bar(B_K_EMPTY + st), ph ^ 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(bar(B_K_FULL + st), C::kKVBytes);
 #pragma unroll
@@ -280,15 +286,22 @@ __global__ void __launch_bounds__(320, 1)
             if (n == 0) continue;
             const int b = w.x, pr = w.z;
             const int q_len = p.q_off[b + 1] - p.q_off[b], kv_len = p.kv_off[b + 1] - p.kv_off[b];
-            const int nx0 = fwd_tiles_of(q_len, kv_len, 2 * pr, p.causal);
-            const int nx1 = fwd_tiles_of(q_len, kv_len, 2 * pr + 1, p.causal);
+            // Each tile's key range inside the pair's stream [f0, f0 + n): tile x is active
+            // for stream steps [off_x, off_x + nx_x).
+            int fa, nx0, fb, nx1, f0, ns, na2, nb2;
+            key_tile_range(q_len, kv_len, 2 * pr, p.causal, window, fa, nx0);
+            key_tile_range(q_len, kv_len, 2 * pr + 1, p.causal, window, fb, nx1);
+            pair_stream(q_len, kv_len, pr, p.causal, window, f0, ns, na2, nb2);
+            const int off0 = fa - f0, off1 = fb - f0;
+            auto act0 = [&](int j) { return j >= off0 && j < off0 + nx0; };
+            auto act1 = [&](int j) { return j >= off1 && j < off1 + nx1; };
             if (!wwait(B_Q_FULL, item_it & 1)) { ok = false; break; }
             // prologue: S of key tile 0
             {
                 const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
                 if (!wwait(B_K_FULL + st, ph)) { ok = false; break; }
-                if (nx0 > 0 && !issue_s(0, st)) { ok = false; break; }
-                if (nx1 > 0 && !issue_s(1, st)) { ok = false; break; }
+                if (act0(0) && !issue_s(0, st)) { ok = false; break; }
+                if (act1(0) && !issue_s(1, st)) { ok = false; break; }
                 commit(B_K_EMPTY + st);
                 if (n == 1) commit(B_Q_EMPTY);
             }
@@ -296,12 +309,12 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t g = kv_it + j, st = g & 1, ph = (g >> 1) & 1;
                 const uint32_t g1 = g + 1, st1 = g1 & 1, ph1 = (g1 >> 1) & 1;
                 if (!wwait(B_V_FULL + st, ph)) { ok = false; break; }
-                if (j < nx0 && !issue_pv(0, st, j == 0)) { ok = false; break; }
+                if (act0(j) && !issue_pv(0, st, j == off0)) { ok = false; break; }
                 if (j + 1 < n && !wwait(B_K_FULL + st1, ph1)) { ok = false; break; }
-                if (j + 1 < nx0 && !issue_s(0, st1)) { ok = false; break; }
-                if (j < nx1 && !issue_pv(1, st, j == 0)) { ok = false; break; }
+                if (act0(j + 1) && !issue_s(0, st1)) { ok = false; break; }
+                if (act1(j) && !issue_pv(1, st, j == off1)) { ok = false; break; }
                 commit(B_V_EMPTY + st);
-                if (j + 1 < nx1 && !issue_s(1, st1)) { ok = false; break; }
+                if (act1(j + 1) && !issue_s(1, st1)) { ok = false; break; }
                 if (j + 1 < n) {
                     commit(B_K_EMPTY + st1);
                     if (j + 2 == n) commit(B_Q_EMPTY);
@@ -333,12 +346,11 @@ __global__ void __launch_bounds__(320, 1)
             const int kv_len = p.kv_off[b + 1] - p.kv_off[b];
             const int tile = 2 * pr + x;
             if (tile * C::BM >= q_len) continue;  // tile B of a short last pair
-            const int n = fwd_tiles_of(q_len, kv_len, tile, p.causal);
+            int kf, n;  // key tiles [kf, kf + n)
+            key_tile_range(q_len, kv_len, tile, p.causal, window, kf, n);
             const int row = tile * C::BM + t;
             const bool row_valid = row < q_len;
             const int diag = kv_len - q_len;
-            // Each warp keeps its own copy of the head's bias row (log2 units for
-            // softmax), double-buffered by item parity, so no cross-warp barrier.
             // Each warp keeps its own copy of the head's bias row (log2 units for
             // softmax) and its maximum, so no cross-warp barrier is needed.
             float* btab = bias_s + warp * (C::kBiasRow + C::kBiasTab);
@@ -371,11 +383,13 @@ __global__ void __launch_bounds__(320, 1)
                     break;
                 }
                 tc_fence_after();
-                const int col0 = j * C::BN;
+                const int col0 = (kf + j) * C::BN;
                 int lim = kv_len - col0;  // subtraction scheme: columns >= lim are masked
                 if (p.causal) lim = min(lim, row + diag + 1 - col0);
+                // sliding window: columns below row + diag - W are masked
+                const int lo = WIN ? row + diag - window - col0 : 0;
                 const int rbase = row + diag - col0;  // relative position of column 0
-                const bool full = __all_sync(0xffffffffu, lim >= C::BN);
+                const bool full = __all_sync(0xffffffffu, lim >= C::BN && lo <= 0);
                 const float xs = softmax ? p.scale_log2 : p.scale;
                 // Bias per 32-column chunk: a constant when every lane's chunk sits in
                 // one bucket (warp-uniform flag per chunk); otherwise read per element
@@ -420,9 +434,9 @@ __global__ void __launch_bounds__(320, 1)
                         for (int i = 0; i < 32; ++i) v[i] = fmaf(__uint_as_float(r[i]), xs, rrow[-(32 * k + i)] - shift);
                     }
                     if (!full) {
-                        const int lk = lim - 32 * k;
+                        const int lk = lim - 32 * k, lok = lo - 32 * k;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = (i < lk) ? v[i] : -INFINITY;
+                        for (int i = 0; i < 32; ++i) v[i] = (i >= lok && i < lk) ? v[i] : -INFINITY;
                     }
                 };
                 // S streams from TMEM in 32-column chunks; the load of chunk k+1 is in
@@ -467,10 +481,10 @@ __global__ void __launch_bounds__(320, 1)
                             for (int i = 0; i < 32; i += 2)
                                 m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
                         } else {
-                            const int lk = lim - 32 * k;
+                            const int lk = lim - 32 * k, lok = lo - 32 * k;
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
-                                m4[i & 3] = fmaxf(m4[i & 3], (i < lk) ? __uint_as_float(cur[i]) : -INFINITY);
+                                m4[i & 3] = fmaxf(m4[i & 3], (i >= lok && i < lk) ? __uint_as_float(cur[i]) : -INFINITY);
                         }
                         const float mk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                         mx = fmaxf(mx, fmaf(mk, xs, (cmask & (1u << k)) ? cb[k] : bmax));
@@ -614,26 +628,29 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int D, typename OT, bool GDPA>
+template <int D, typename OT, bool GDPA, bool WIN>
 static cudaError_t launch_fwd_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const FwdParams& p, int grid, cudaStream_t st) {
     using C = FwdCfg<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, OT, GDPA>,
+        cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, OT, GDPA, WIN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_fwd_kernel<D, OT, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, p);
+    jfa_fwd_kernel<D, OT, GDPA, WIN><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
 }
 
 template <int D, typename OT>
 static cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const FwdParams& p, int grid, cudaStream_t st) {
-    return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false>(tmQ, tmK, tmV, p, grid, st)
-                                 : launch_fwd_m<D, OT, true>(tmQ, tmK, tmV, p, grid, st);
+    if (p.window >= 0)
+        return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false, true>(tmQ, tmK, tmV, p, grid, st)
+                                     : launch_fwd_m<D, OT, true, true>(tmQ, tmK, tmV, p, grid, st);
+    return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false, false>(tmQ, tmK, tmV, p, grid, st)
+                                 : launch_fwd_m<D, OT, true, false>(tmQ, tmK, tmV, p, grid, st);
 }
 
 cudaError_t launch_fwd(int dtype, int o_dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,

@@ -37,18 +37,81 @@ struct WorkItem {
 };
 static_assert(sizeof(WorkItem) == 16, "WorkItem must match int4");
 
-// Key tiles a 128-row query tile visits: all of them, or (causal, bottom-right) up
-// to the one holding its last row's diagonal; 0 for a tile past the sequence end.
-__host__ __device__ inline int fwd_tiles_of(int64_t q_len, int64_t kv_len, int64_t tile, int causal) {
+// Key tiles a 128-row query tile visits: [first, first + count).  All of them, or
+// (causal, bottom-right) up to the one holding its last row's diagonal; with a sliding
+// window W >= 0 (row i sees keys i' - W .. i', i' = i + kv_len - q_len) they start at
+// the tile holding its first row's lowest key.  count is 0 for a tile past the
+// sequence end or one that sees no key.
+__host__ __device__ inline void key_tile_range(int64_t q_len, int64_t kv_len, int64_t tile, int causal,
+                                               int window, int& first, int& count) {
+    first = 0;
+    count = 0;
     const int64_t rows0 = tile * kFwdBM;
-    if (rows0 >= q_len) return 0;
-    int64_t n = (kv_len + kFwdBN - 1) / kFwdBN;
+    if (rows0 >= q_len) return;
+    int64_t end = (kv_len + kFwdBN - 1) / kFwdBN;
+    const int64_t diag = kv_len - q_len;
     if (causal) {
         const int64_t last_row = (q_len < rows0 + kFwdBM ? q_len : rows0 + kFwdBM) - 1;
-        const int64_t max_col = last_row + (kv_len - q_len);
-        n = max_col < 0 ? 0 : (n < max_col / kFwdBN + 1 ? n : max_col / kFwdBN + 1);
+        const int64_t max_col = last_row + diag;
+        end = max_col < 0 ? 0 : (end < max_col / kFwdBN + 1 ? end : max_col / kFwdBN + 1);
     }
-    return int(n);
+    int64_t beg = 0;
+    if (window >= 0) {
+        const int64_t min_col = rows0 + diag - window;
+        beg = min_col > 0 ? min_col / kFwdBN : 0;
+    }
+    if (end > beg) {
+        first = int(beg);
+        count = int(end - beg);
+    }
+}
+
+__host__ __device__ inline int fwd_tiles_of(int64_t q_len, int64_t kv_len, int64_t tile, int causal, int window = -1) {
+    int first, count;
+    key_tile_range(q_len, kv_len, tile, causal, window, first, count);
+    return count;
+}
+
+// Key tiles streamed by a forward pair item (query tiles 2t and 2t+1): the union of the
+// two tiles' ranges, [first, first + count).
+__host__ __device__ inline void pair_stream(int64_t q_len, int64_t kv_len, int64_t t, int causal, int window, int& first, int& count,
+                        int& na, int& nb) {
+    int fa, fb;
+    key_tile_range(q_len, kv_len, 2 * t, causal, window, fa, na);
+    key_tile_range(q_len, kv_len, 2 * t + 1, causal, window, fb, nb);
+    if (na == 0 && nb == 0) {
+        first = 0;
+        count = 0;
+    } else if (na == 0) {
+        first = fb;
+        count = nb;
+    } else if (nb == 0) {
+        first = fa;
+        count = na;
+    } else {
+        first = fa < fb ? fa : fb;
+        const int ea = fa + na, eb = fb + nb;
+        count = (ea > eb ? ea : eb) - first;
+    }
+}
+
+// Query tiles (kBwdBM rows) that see key tile nt (kBwdBN keys): [first, first + count).
+// Row i sees key j when j <= i' (causal) and j >= i' - W (window), i' = i + kv_len - q_len.
+__host__ __device__ inline void query_tile_range(int64_t q_len, int64_t kv_len, int64_t nt, int causal, int window,
+                                                 int& first, int& count) {
+    first = 0;
+    count = 0;
+    const int64_t diag = kv_len - q_len;
+    const int64_t j0 = nt * kBwdBN;
+    const int64_t j1 = (kv_len < j0 + kBwdBN ? kv_len : j0 + kBwdBN) - 1;  // last key of the tile
+    if (j1 < j0 || q_len <= 0) return;
+    int64_t first_row = causal ? j0 - diag : 0;
+    if (first_row < 0) first_row = 0;
+    int64_t last_row = q_len - 1;
+    if (window >= 0 && j1 + window - diag < last_row) last_row = j1 + window - diag;
+    if (first_row > last_row) return;
+    first = int(first_row / kBwdBM);
+    count = int(last_row / kBwdBM - first_row / kBwdBM + 1);
 }
 
 // Status bits the kernels OR into the plan's device status word.
@@ -62,6 +125,7 @@ struct FwdParams {
     int H;
     int mode;       // jfa_mode
     int causal;
+    int window;     // sliding window W (>= 0), or -1
     float scale;        // multiplies <q,k>
     float scale_log2;   // scale * log2(e)
     const float* bias;  // [H,32] fp32 or nullptr
@@ -78,6 +142,7 @@ struct BwdParams {
     int H;
     int mode;
     int causal;
+    int window;  // sliding window W (>= 0), or -1
     float scale;
     float scale_log2;
     const float* bias;
@@ -95,12 +160,12 @@ jfa_status validate_offsets(const int32_t* q_off, const int32_t* kv_off, int32_t
 int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
                     int32_t causal, int32_t pass);
 void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
-                    int32_t causal, int32_t pass, int32_t n_ctas, WorkItem* items,
+                    int32_t causal, int32_t window, int32_t pass, int32_t n_ctas, WorkItem* items,
                     int32_t* cta_off, int64_t* cta_cost);
 
-int64_t sequence_cost(int64_t q_len, int64_t kv_len, int32_t H, int32_t causal);
+int64_t sequence_cost(int64_t q_len, int64_t kv_len, int32_t H, int32_t causal, int32_t window);
 void partition_sequences(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H, int32_t causal,
-                         int32_t n_parts, int32_t* part_of_seq, int64_t* part_cost);
+                         int32_t window, int32_t n_parts, int32_t* part_of_seq, int64_t* part_cost);
 
 // Kernel launchers (fwd.cu, bwd.cu, bwd_dq.cu).  Return cudaSuccess or the launch error.
 cudaError_t launch_fwd(int dtype, int o_dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
@@ -127,7 +192,7 @@ bool supported(int dtype, int D);
 }  // namespace jfa
 
 struct jfa_plan_t {
-    int32_t B, H, D, mode, causal;
+    int32_t B, H, D, mode, causal, window;
     int64_t Tq, Tkv;
     int device, num_sms;
     std::vector<int32_t> q_off, kv_off;   // host copies

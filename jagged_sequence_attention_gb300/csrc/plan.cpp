@@ -36,54 +36,46 @@ namespace {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-inline int64_t bwd_inner(int64_t q_len, int64_t kv_len, int64_t nt, int causal) {
-    const int64_t nq = ceil_div(q_len, kBwdBM);
-    if (!causal) return nq;
-    // Row i sees the tile iff its first column nt*BN <= i + (kv_len - q_len).
-    const int64_t first_row = std::max<int64_t>(0, nt * kBwdBN - (kv_len - q_len));
-    if (first_row >= q_len) return 0;
-    return nq - first_row / kBwdBM;
-}
-
 struct Costed {
     WorkItem w;
     int64_t cost;
 };
 
 void build_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
-                 int32_t causal, int32_t pass, std::vector<Costed>* out) {
+                 int32_t causal, int32_t window, int32_t pass, std::vector<Costed>* out) {
     for (int32_t b = 0; b < B; ++b) {
         const int64_t q_len = q_off[b + 1] - q_off[b];
         const int64_t kv_len = kv_off[b + 1] - kv_off[b];
         if (pass == 0) {
-            // Forward: one item per pair of 128-row query tiles; each tile visits key
-            // tiles from 0 up to the causal diagonal of its last row (or all of them),
-            // and the item streams the larger of the two counts.
+            // Forward: one item per pair of 128-row query tiles; each tile visits its
+            // key-tile range (causal: up to the diagonal of its last row; window: from
+            // its first row's lowest key), and the item streams the union of the two.
             const int64_t np = ceil_div(q_len, kFwdPairRows);
             for (int32_t h = 0; h < H; ++h)
                 for (int64_t t = 0; t < np; ++t) {
-                    const int64_t na = fwd_tiles_of(q_len, kv_len, 2 * t, causal);
-                    const int64_t nb = fwd_tiles_of(q_len, kv_len, 2 * t + 1, causal);
-                    out->push_back({{b, h, int32_t(t), int32_t(na > nb ? na : nb)}, 2 * (na + nb) + 2});
+                    int first, n, na, nb;
+                    pair_stream(q_len, kv_len, t, causal, window, first, n, na, nb);
+                    out->push_back({{b, h, int32_t(t), int32_t(n)}, 2 * (int64_t(na) + nb) + 2});
                 }
         } else if (pass == kPassBwdKV) {
             // Backward dK/dV: one item per key tile (also when it sees no query, so
-            // that its dK/dV rows are written); it visits the last n query tiles, four
+            // that its dK/dV rows are written); it visits its query-tile range, four
             // products each.
             const int64_t nt = ceil_div(kv_len, kBwdBN);
             for (int32_t h = 0; h < H; ++h)
                 for (int64_t t = 0; t < nt; ++t) {
-                    const int64_t n = bwd_inner(q_len, kv_len, t, causal);
-                    out->push_back({{b, h, int32_t(t), int32_t(n)}, 4 * n + 2});
+                    int first, n;
+                    query_tile_range(q_len, kv_len, t, causal, window, first, n);
+                    out->push_back({{b, h, int32_t(t), int32_t(n)}, 4 * int64_t(n) + 2});
                 }
         } else {
             // Backward dQ: one item per 128-row query tile (also when it sees no key, so
-            // that its dQ rows are written); it visits the forward's key tiles, three
+            // that its dQ rows are written); it visits the forward's key-tile range, three
             // products each.
             const int64_t nt = ceil_div(q_len, kFwdBM);
             for (int32_t h = 0; h < H; ++h)
                 for (int64_t t = 0; t < nt; ++t) {
-                    const int64_t n = fwd_tiles_of(q_len, kv_len, t, causal);
+                    const int64_t n = fwd_tiles_of(q_len, kv_len, t, causal, window);
                     out->push_back({{b, h, int32_t(t), int32_t(n)}, 3 * n + 2});
                 }
         }
@@ -105,11 +97,11 @@ int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
 }
 
 void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
-                    int32_t causal, int32_t pass, int32_t n_ctas, WorkItem* items,
+                    int32_t causal, int32_t window, int32_t pass, int32_t n_ctas, WorkItem* items,
                     int32_t* cta_off, int64_t* cta_cost) {
     std::vector<Costed> all;
     all.reserve(size_t(count_items(q_off, kv_off, B, H, causal, pass)));
-    build_items(q_off, kv_off, B, H, causal, pass, &all);
+    build_items(q_off, kv_off, B, H, causal, window, pass, &all);
 
     // Group-major order: groups by total cost (largest first, ties by sequence and
     // head), then items by cost inside the group; the sort is stable so equal keys
@@ -156,18 +148,18 @@ void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
 // three dQ products per visited 128x128 score tile, plus a per-tile constant), and the
 // sequences go longest-first to the least loaded part (greedy LPT, ties to the lower
 // part and the lower sequence index, so the result is deterministic).
-int64_t sequence_cost(int64_t q_len, int64_t kv_len, int32_t H, int32_t causal) {
+int64_t sequence_cost(int64_t q_len, int64_t kv_len, int32_t H, int32_t causal, int32_t window) {
     const int64_t nq = ceil_div(q_len, kFwdBM), nk = ceil_div(kv_len, kBwdBN);
     int64_t tiles = 0;
-    for (int64_t t = 0; t < nq; ++t) tiles += fwd_tiles_of(q_len, kv_len, t, causal);
+    for (int64_t t = 0; t < nq; ++t) tiles += fwd_tiles_of(q_len, kv_len, t, causal, window);
     return int64_t(H) * (9 * tiles + 2 * (nq + nk));
 }
 
 void partition_sequences(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H, int32_t causal,
-                         int32_t n_parts, int32_t* part_of_seq, int64_t* part_cost) {
+                         int32_t window, int32_t n_parts, int32_t* part_of_seq, int64_t* part_cost) {
     std::vector<std::pair<int64_t, int32_t>> order(size_t(B > 0 ? B : 0));
     for (int32_t b = 0; b < B; ++b)
-        order[size_t(b)] = {sequence_cost(q_off[b + 1] - q_off[b], kv_off[b + 1] - kv_off[b], H, causal), b};
+        order[size_t(b)] = {sequence_cost(q_off[b + 1] - q_off[b], kv_off[b + 1] - kv_off[b], H, causal, window), b};
     std::stable_sort(order.begin(), order.end(),
                      [](const std::pair<int64_t, int32_t>& a, const std::pair<int64_t, int32_t>& b) {
                          return a.first > b.first;

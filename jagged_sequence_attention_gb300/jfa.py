@@ -28,7 +28,7 @@ JFA_BIAS_NONE, JFA_BIAS_RELPOS32 = 0, 1
 MODES = {"softmax": JFA_SOFTMAX, "gelu_tanh": JFA_GDPA_GELU_TANH, "silu": JFA_GDPA_SILU}
 DTYPES = {torch.bfloat16: JFA_BF16, torch.float32: JFA_F32}
 
-EXPORTED = ["jfa_plan_create", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd_workspace_size",
+EXPORTED = ["jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd_workspace_size",
             "jfa_bwd", "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build",
             "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times", "jfa_bwd_static_scratch",
             "jfa_partition_sequences"]
@@ -53,6 +53,7 @@ def lib():
         vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
         P = ctypes.POINTER
         L.jfa_plan_create.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, P(vp)]
+        L.jfa_plan_create_ex.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, P(vp)]
         L.jfa_plan_destroy.argtypes = [vp]
         L.jfa_plan_info.argtypes = [vp, P(i64), i32]
         L.jfa_fwd.argtypes = [vp, i32, vp, vp, vp, i32, vp, f32, vp, i32, vp, vp]
@@ -61,14 +62,14 @@ def lib():
         L.jfa_bwd.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
         L.jfa_bwd_static_scratch.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp]
         L.jfa_plan_device_status.argtypes = [vp, vp]
-        L.jfa_partition_sequences.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp]
-        L.jfa_worklist_size.argtypes = [vp, vp, i32, i32, i32, i32, P(i64)]
-        L.jfa_worklist_build.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+        L.jfa_partition_sequences.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp]
+        L.jfa_worklist_size.argtypes = [vp, vp, i32, i32, i32, i32, i32, P(i64)]
+        L.jfa_worklist_build.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
         L.jfa_plan_set_timing.argtypes = [vp, i32]
         L.jfa_plan_kernel_times.argtypes = [vp, vp, vp]
         L.jfa_status_string.argtypes = [i32]
         L.jfa_status_string.restype = ctypes.c_char_p
-        for name in ("jfa_plan_create", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
+        for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
                      "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build", "jfa_plan_set_timing",
                      "jfa_plan_kernel_times", "jfa_bwd_static_scratch", "jfa_partition_sequences"):
             getattr(L, name).restype = i32
@@ -118,8 +119,14 @@ class Plan:
             self.handle = None
 
 
-def jfa_plan_create(q_offsets, kv_offsets, H: int, D: int, mode="softmax", causal=False, stream=None) -> Plan:
-    """Offsets: host int32 arrays (or CUDA int32 tensors, copied with a sync)."""
+def _win(window) -> int:
+    return -1 if window is None else int(window)
+
+
+def jfa_plan_create(q_offsets, kv_offsets, H: int, D: int, mode="softmax", causal=False, stream=None,
+                    window=None) -> Plan:
+    """Offsets: host int32 arrays (or CUDA int32 tensors, copied with a sync).  window: sliding
+    window W (query i sees keys i' - W .. i'; needs causal), None for none."""
     m = MODES[mode] if isinstance(mode, str) else int(mode)
     on_dev = isinstance(q_offsets, torch.Tensor) and q_offsets.is_cuda
     if on_dev:
@@ -135,9 +142,10 @@ def jfa_plan_create(q_offsets, kv_offsets, H: int, D: int, mode="softmax", causa
     if (qo.numel() if on_dev else qo.size) != (ko.numel() if on_dev else ko.size):
         raise JFAError("jfa_plan_create", JFA_ERR_INVALID_ARG)
     h = ctypes.c_void_p()
-    _check("jfa_plan_create", lib().jfa_plan_create(qp, kp, int(B), int(H), int(D), m, int(bool(causal)),
-                                                     int(on_dev), _stream(stream), ctypes.byref(h)))
+    _check("jfa_plan_create", lib().jfa_plan_create_ex(qp, kp, int(B), int(H), int(D), m, int(bool(causal)),
+                                                        _win(window), int(on_dev), _stream(stream), ctypes.byref(h)))
     plan = Plan(h, int(B), int(H), int(D), m, bool(causal), Tq, Tkv)
+    plan.window = window
     if Tq is None:
         inf = jfa_plan_info(plan)
         plan.Tq, plan.Tkv = inf["T_q"], inf["T_kv"]
@@ -151,7 +159,7 @@ def jfa_plan_destroy(plan: Plan):
 
 
 INFO_KEYS = ["T_q", "T_kv", "B", "H", "D", "mode", "causal", "fwd_items", "fwd_grid", "bwd_items", "bwd_grid",
-             "num_sms", "dq_items", "dq_grid"]
+             "num_sms", "dq_items", "dq_grid", "window"]
 
 
 def jfa_plan_info(plan: Plan) -> dict:
@@ -245,7 +253,7 @@ def jfa_plan_kernel_times(plan: Plan) -> dict:
     return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KERNEL_KINDS)}
 
 
-def jfa_partition_sequences(q_offsets, kv_offsets, H: int, causal: bool, n_parts: int):
+def jfa_partition_sequences(q_offsets, kv_offsets, H: int, causal: bool, n_parts: int, window=None):
     """Host LPT split of a batch's sequences over n_parts GPUs.  Returns (part_of_seq int32 [B],
     part_cost int64 [n_parts])."""
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
@@ -254,7 +262,7 @@ def jfa_partition_sequences(q_offsets, kv_offsets, H: int, causal: bool, n_parts
     cost = np.zeros(int(n_parts), dtype=np.int64)
     _check("jfa_partition_sequences", lib().jfa_partition_sequences(
         qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p), int(B), int(H), int(bool(causal)),
-        int(n_parts), part.ctypes.data_as(ctypes.c_void_p), cost.ctypes.data_as(ctypes.c_void_p)))
+        _win(window), int(n_parts), part.ctypes.data_as(ctypes.c_void_p), cost.ctypes.data_as(ctypes.c_void_p)))
     return part[:B], cost
 
 
@@ -263,31 +271,33 @@ def shard(batch, rank: int, world: int):
     subset, repacked), by the LPT split above.  Sequences are independent, so results of
     the shards are exactly the full batch's results for those sequences."""
     from . import workloads
-    part, _ = jfa_partition_sequences(batch.q_off, batch.kv_off, batch.H, batch.causal, world)
+    part, _ = jfa_partition_sequences(batch.q_off, batch.kv_off, batch.H, batch.causal, world,
+                                      window=getattr(batch, "window", None))
     seqs = np.nonzero(part == rank)[0]
     return workloads.subset(batch, seqs)
 
 
-def jfa_worklist_size(q_offsets, kv_offsets, H: int, causal: bool, pass_: int) -> int:
+def jfa_worklist_size(q_offsets, kv_offsets, H: int, causal: bool, pass_: int, window=None) -> int:
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
     n = ctypes.c_int64()
     _check("jfa_worklist_size", lib().jfa_worklist_size(qo.ctypes.data_as(ctypes.c_void_p),
                                                          ko.ctypes.data_as(ctypes.c_void_p), qo.size - 1, int(H),
-                                                         int(bool(causal)), int(pass_), ctypes.byref(n)))
+                                                         int(bool(causal)), _win(window), int(pass_),
+                                                         ctypes.byref(n)))
     return int(n.value)
 
 
-def jfa_worklist_build(q_offsets, kv_offsets, H: int, causal: bool, pass_: int, n_ctas: int):
+def jfa_worklist_build(q_offsets, kv_offsets, H: int, causal: bool, pass_: int, n_ctas: int, window=None):
     """Host planner.  Returns (items int32 [n,4] (seq, head, tile, inner), cta_offsets [n_ctas+1],
     cta_cost [n_ctas])."""
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
-    n = jfa_worklist_size(qo, ko, H, causal, pass_)
+    n = jfa_worklist_size(qo, ko, H, causal, pass_, window)
     items = np.zeros((max(n, 1), 4), dtype=np.int32)
     offs = np.zeros(n_ctas + 1, dtype=np.int32)
     cost = np.zeros(n_ctas, dtype=np.int64)
     _check("jfa_worklist_build", lib().jfa_worklist_build(
         qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p), qo.size - 1, int(H),
-        int(bool(causal)), int(pass_), int(n_ctas), items.ctypes.data_as(ctypes.c_void_p),
+        int(bool(causal)), _win(window), int(pass_), int(n_ctas), items.ctypes.data_as(ctypes.c_void_p),
         offs.ctypes.data_as(ctypes.c_void_p), cost.ctypes.data_as(ctypes.c_void_p)))
     return items[:n], offs, cost
 
@@ -297,7 +307,8 @@ def jfa_worklist_build(q_offsets, kv_offsets, H: int, causal: bool, pass_: int, 
 
 def attention(batch, with_backward=True, stream=None, out_dtype=None):
     """Run forward (and backward) for a workloads.Batch on the GPU: returns dict of tensors."""
-    plan = jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal, stream)
+    plan = jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal, stream,
+                           window=getattr(batch, "window", None))
     O, lse = jfa_fwd(plan, batch.Q, batch.K, batch.V, batch.bias, batch.scale, stream=stream, out_dtype=out_dtype)
     out = {"O": O, "lse": lse, "plan": plan}
     if with_backward:

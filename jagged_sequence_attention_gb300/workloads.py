@@ -44,6 +44,7 @@ class Workload:
     q_len: tuple              # ("fixed", [..]) | ("uniform", lo, hi) | ("lognormal", median, lo, hi)
     kv_len: Optional[tuple]   # None: self-attention (kv lengths = q lengths)
     description: str = ""
+    window: Optional[int] = None  # sliding window W (query i sees keys i' - W .. i'), or None
 
 
 WORKLOADS = {
@@ -82,6 +83,13 @@ WORKLOADS = {
         ("uniform", 6144, 10240), None,
         "8 sequences, lengths U{6144..10240}, causal self-attention, 8 heads, head_dim 128, bf16, "
         "relative-position bias (profiling size of the long-sequence workload)"),
+    # Sliding-window form of the long-sequence workload (the GEM articles' move from full to
+    # sliding-window self-attention for long user sequences; window size not published).
+    "long_window": Workload(
+        "long_window", 7, 64, 8, 128, torch.bfloat16, "softmax", True, True, 1.0,
+        ("uniform", 4096, 32768), None,
+        "64 sequences, lengths U{4096..32768} (~1.2M tokens), causal sliding window of 2048 keys, 8 heads, "
+        "head_dim 128, bf16, relative-position bias", window=2048),
 }
 
 
@@ -138,6 +146,7 @@ class Batch:
     H: int
     D: int
     extra: dict = field(default_factory=dict)
+    window: Optional[int] = None   # sliding window W (query i sees keys i' - W .. i'), or None
 
     @property
     def B(self) -> int:
@@ -161,7 +170,7 @@ def _values(shape, std, dtype, gen, device):
 
 def make_custom(q_lens, kv_lens, *, H, D, dtype=torch.bfloat16, mode="softmax", causal=False,
                 bias=False, value_std=1.0, seed=BASE_SEED, device="cpu", with_grad=True,
-                name="custom", pad_rows=0) -> Batch:
+                name="custom", pad_rows=0, window=None) -> Batch:
     """A batch with the given lengths.  ``pad_rows`` extra rows are appended to every
     value tensor (beyond the last offset) so tests can check that nothing there is read
     into a result or written."""
@@ -175,7 +184,7 @@ def make_custom(q_lens, kv_lens, *, H, D, dtype=torch.bfloat16, mode="softmax", 
     b = None
     if bias:
         b = (torch.randn((H, 32), generator=gen, device=device, dtype=torch.float32) * 0.1)
-    return Batch(name, q_off, kv_off, Q, K, V, dO, b, 1.0 / math.sqrt(D), mode, causal, H, D)
+    return Batch(name, q_off, kv_off, Q, K, V, dO, b, 1.0 / math.sqrt(D), mode, causal, H, D, window=window)
 
 
 def make(name: str, device="cpu", with_grad=True, seed: Optional[int] = None) -> Batch:
@@ -185,7 +194,7 @@ def make(name: str, device="cpu", with_grad=True, seed: Optional[int] = None) ->
     q, kv = lengths(w, s)
     return make_custom(q, kv, H=w.H, D=w.D, dtype=w.dtype, mode=w.mode, causal=w.causal,
                        bias=w.bias, value_std=w.value_std, seed=s, device=device,
-                       with_grad=with_grad, name=name)
+                       with_grad=with_grad, name=name, window=w.window)
 
 
 def subset(batch: Batch, seqs, heads=None) -> Batch:
@@ -208,6 +217,6 @@ def subset(batch: Batch, seqs, heads=None) -> Batch:
     sub = Batch(batch.name + "/subset", offsets(batch.q_lens[seqs]), offsets(batch.kv_lens[seqs]),
                 take(batch.Q, qi), take(batch.K, ki), take(batch.V, ki), take(batch.dO, qi),
                 None if batch.bias is None else batch.bias[hs.to(batch.bias.device)].contiguous(),
-                batch.scale, batch.mode, batch.causal, len(heads), batch.D)
+                batch.scale, batch.mode, batch.causal, len(heads), batch.D, window=batch.window)
     sub.extra.update(seqs=seqs, heads=heads, q_index=qi, kv_index=ki)
     return sub

@@ -56,12 +56,12 @@ def run_oracle(batch, with_backward=True):
     Tq, Tkv = int(batch.q_off[-1]), int(batch.kv_off[-1])
     Q, K, V = Q[:Tq], K[:Tkv], V[:Tkv]
     O, LSE = oracle.fwd(batch.q_off, batch.kv_off, Q, K, V, mode=batch.mode, causal=batch.causal,
-                        bias=b, scale=batch.scale)
+                        bias=b, scale=batch.scale, window=batch.window)
     res = {"O": O, "lse": LSE}
     if with_backward:
         dO = np64(batch.dO)[:Tq]
         dQ, dK, dV = oracle.bwd(batch.q_off, batch.kv_off, Q, K, V, dO, mode=batch.mode,
-                                causal=batch.causal, bias=b, scale=batch.scale)
+                                causal=batch.causal, bias=b, scale=batch.scale, window=batch.window)
         res.update(dQ=dQ, dK=dK, dV=dV)
     return res
 
@@ -114,8 +114,9 @@ def assert_within(m, softmax=True):
 
 def suffix_problem(batch, b, h, i0):
     """Exact sub-problem for query rows [i0, q_len) of sequence b, head h, over all of
-    its keys.  With bottom-right causal alignment and |i + kv_len - q_len - j| bias
-    positions, these rows' outputs and dQ are unchanged; for causal attention the keys
+    its keys.  With bottom-right causal alignment (and a sliding window, which is relative
+    to the same aligned position) and |i + kv_len - q_len - j| bias positions, these rows'
+    outputs and dQ are unchanged; for causal attention the keys
     j >= i0 + (kv_len - q_len) also keep their exact dK, dV (no earlier row sees them),
     and for non-causal attention that holds when i0 == 0.
     Returns (sub_batch, q_rows, kv_rows): GPU row indices ([T,...] first axis, head h)
@@ -130,7 +131,7 @@ def suffix_problem(batch, b, h, i0):
     sub = wl.Batch(batch.name + f"/seq{b}/h{h}/rows{i0}:", wl.offsets([q_len - i0]), wl.offsets([kv_len]),
                    take(batch.Q, qs), take(batch.K, ks), take(batch.V, ks), take(batch.dO, qs),
                    None if batch.bias is None else batch.bias[h:h + 1].cpu(), batch.scale, batch.mode,
-                   batch.causal, 1, batch.D)
+                   batch.causal, 1, batch.D, window=batch.window)
     if batch.causal:
         j0 = max(0, i0 + (kv_len - q_len))
     else:
@@ -149,7 +150,7 @@ def _concat_batches(subs):
     s0 = subs[0]
     return wl.Batch(s0.name, wl.offsets(q_l), wl.offsets(k_l), cat([s.Q for s in subs]), cat([s.K for s in subs]),
                     cat([s.V for s in subs]), cat([s.dO for s in subs]), s0.bias, s0.scale, s0.mode, s0.causal, 1,
-                    s0.D)
+                    s0.D, window=s0.window)
 
 
 def sampled_parity(batch, gpu, samples, with_backward=True):
