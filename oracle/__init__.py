@@ -5,7 +5,9 @@ CPU-baseline / reference leg of ``bench.py`` may import this package.  The CUDA
 library never loads it and shares no code with it.
 
 Inputs are numpy arrays: values ``[T, H, D]`` (any float dtype; widened to fp64
-exactly), offsets ``int32[B+1]``, bias table ``[H, 32]`` or ``None``.
+exactly), offsets ``int32[B+1]``, bias table ``[H, 32]`` or ``None``, dense per-pair
+bias ``[H, P]`` (``P = num_pairs(q_off, kv_off)``, sequence b's block row-major
+``[q_len, kv_len]`` at ``pair_offsets(...)[b]``) or ``None``.
 """
 from __future__ import annotations
 
@@ -54,12 +56,14 @@ def _load():
             lib.oracle_act_grad.argtypes = [ctypes.c_int, d]
             lib.oracle_act_grad.restype = d
             lib.oracle_max_threads.restype = ctypes.c_int
+            lib.oracle_num_pairs.argtypes = [ctypes.c_int, P(i32), P(i32)]
+            lib.oracle_num_pairs.restype = ctypes.c_int64
             common = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(i32), P(i32)]
-            lib.oracle_fwd.argtypes = common + [P(d)] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(d), d,
+            lib.oracle_fwd.argtypes = common + [P(d)] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(d), P(d), d,
                                                              P(d), P(d), ctypes.c_int]
             lib.oracle_fwd.restype = ctypes.c_int
-            lib.oracle_bwd.argtypes = common + [P(d)] * 4 + [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(d), d,
-                                                             P(d), P(d), P(d), ctypes.c_int]
+            lib.oracle_bwd.argtypes = common + [P(d)] * 4 + [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(d), P(d), d,
+                                                             P(d), P(d), P(d), P(d), P(d), ctypes.c_int]
             lib.oracle_bwd.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -104,30 +108,60 @@ def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
 
+def pair_offsets(q_off, kv_off):
+    """int64[B+1]: where each sequence's block of a dense per-pair array starts."""
+    q_off = np.asarray(q_off, dtype=np.int64)
+    kv_off = np.asarray(kv_off, dtype=np.int64)
+    out = np.zeros(q_off.size, dtype=np.int64)
+    for b in range(q_off.size - 1):
+        out[b + 1] = out[b] + (q_off[b + 1] - q_off[b]) * (kv_off[b + 1] - kv_off[b])
+    return out
+
+
+def num_pairs(q_off, kv_off) -> int:
+    q_off = np.ascontiguousarray(np.asarray(q_off, dtype=np.int32))
+    kv_off = np.ascontiguousarray(np.asarray(kv_off, dtype=np.int32))
+    return int(_load().oracle_num_pairs(q_off.size - 1, _ptr(q_off, ctypes.c_int32), _ptr(kv_off, ctypes.c_int32)))
+
+
+def _dense(dense, H, q_off, kv_off):
+    if dense is None:
+        return None
+    d = _f64(dense)
+    if d.shape != (H, num_pairs(q_off, kv_off)):
+        raise ValueError("dense bias must be [H, P]")
+    return d
+
+
 def fwd(q_off, kv_off, Q, K, V, *, mode="softmax", causal=False, bias=None, scale=None,
-        nthreads=0, window=None):
+        nthreads=0, window=None, dense_bias=None):
     """Returns (O [Tq,H,D] fp64, LSE [Tq,H] fp64).  window W (None: no window): key j is
-    allowed for query i only if j >= i + (kv_len - q_len) - W."""
+    allowed for query i only if j >= i + (kv_len - q_len) - W.  dense_bias [H, P]: a
+    per-pair additive bias (None: none)."""
     lib = _load()
     q_off, kv_off, Q, K, V = _check(q_off, kv_off, Q, K, V)
     B = q_off.size - 1
     _, H, D = Q.shape
     scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
     b = None if bias is None else _f64(bias).reshape(H, 32)
+    dn = _dense(dense_bias, H, q_off, kv_off)
     O = np.zeros_like(Q)
     LSE = np.zeros((Q.shape[0], H), dtype=np.float64)
     rc = lib.oracle_fwd(B, H, D, _ptr(q_off, ctypes.c_int32), _ptr(kv_off, ctypes.c_int32),
                         _ptr(Q), _ptr(K), _ptr(V), MODES[mode], int(bool(causal)),
                         -1 if window is None else int(window),
-                        None if b is None else _ptr(b), scale, _ptr(O), _ptr(LSE), int(nthreads))
+                        None if b is None else _ptr(b), None if dn is None else _ptr(dn), scale, _ptr(O),
+                        _ptr(LSE), int(nthreads))
     if rc != 0:
         raise MemoryError("oracle_fwd failed")
     return O, LSE
 
 
 def bwd(q_off, kv_off, Q, K, V, dO, *, mode="softmax", causal=False, bias=None, scale=None,
-        nthreads=0, window=None):
-    """Returns (dQ, dK, dV), fp64, same shapes as Q, K, V."""
+        nthreads=0, window=None, dense_bias=None, bias_grads=False):
+    """Returns (dQ, dK, dV), fp64, same shapes as Q, K, V; with bias_grads also the
+    gradient of the bucket table [H, 32] and of a dense per-pair bias [H, P] (both are
+    defined whether or not that bias was given: the gradient of the score)."""
     lib = _load()
     q_off, kv_off, Q, K, V = _check(q_off, kv_off, Q, K, V)
     dO = _f64(dO)
@@ -137,12 +171,18 @@ def bwd(q_off, kv_off, Q, K, V, dO, *, mode="softmax", causal=False, bias=None, 
     _, H, D = Q.shape
     scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
     b = None if bias is None else _f64(bias).reshape(H, 32)
+    dn = _dense(dense_bias, H, q_off, kv_off)
     dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    dbias = np.zeros((H, 32)) if bias_grads else None
+    d_dense = np.zeros((H, num_pairs(q_off, kv_off))) if bias_grads else None
     rc = lib.oracle_bwd(B, H, D, _ptr(q_off, ctypes.c_int32), _ptr(kv_off, ctypes.c_int32),
                         _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), MODES[mode], int(bool(causal)),
                         -1 if window is None else int(window),
-                        None if b is None else _ptr(b), scale, _ptr(dQ), _ptr(dK), _ptr(dV),
-                        int(nthreads))
+                        None if b is None else _ptr(b), None if dn is None else _ptr(dn), scale, _ptr(dQ),
+                        _ptr(dK), _ptr(dV), None if dbias is None else _ptr(dbias),
+                        None if d_dense is None else _ptr(d_dense), int(nthreads))
     if rc != 0:
         raise MemoryError("oracle_bwd failed")
+    if bias_grads:
+        return dQ, dK, dV, dbias, d_dense
     return dQ, dK, dV

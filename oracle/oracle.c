@@ -31,6 +31,16 @@
  *    bound); W < 0 means no window;
  *  - a query row with no allowed key gives o = 0 and lse = -inf, and all
  *    gradients through it are 0;
+ *  - besides the bucket table, a dense per-pair bias may be given (the "custom
+ *    attention bias" of the aihot.vn GEM article, section "Jagged Sequence Flash
+ *    Attention", in its most general form): one value per (head, sequence, query
+ *    row, key row), stored head-major as [H, P] with P = sum_b q_len_b * kv_len_b,
+ *    sequence b's block starting at pair_off[b] = sum_{b' < b} q_len_b' * kv_len_b'
+ *    and laid out row-major [q_len_b, kv_len_b] inside it.  Both biases add to the
+ *    score; the dense value of a masked pair is never read;
+ *  - the gradient of a bias is that of the score it adds to: d bias_dense[h, (i, j)]
+ *    = ds_ij at allowed pairs (0 at masked ones), and d table[h, k] = sum of ds_ij
+ *    over the allowed pairs whose relative position falls in bucket k;
  *  - GDPA masked entries contribute exactly 0 (the activation is never evaluated
  *    on them); GELU is the tanh form of Hendrycks and Gimpel (2016), SiLU is
  *    x * sigmoid(x).
@@ -104,15 +114,33 @@ double oracle_act_grad(int mode, double x)
     return NAN;
 }
 
-/* Score s_ij = scale * <q_i, k_j> + bias[h, bucket(|i + kv_len - q_len - j|)]. */
+/* Score s_ij = scale * <q_i, k_j> + bias[h, bucket(|i + kv_len - q_len - j|)]
+ *              + dense_h_b[i * kv_len + j]. */
 static double score(const double *qi, const double *kj, int D, double scale,
-                    const double *bias_h, int64_t i, int64_t j, int64_t q_len, int64_t kv_len)
+                    const double *bias_h, const double *dense_hb, int64_t i, int64_t j,
+                    int64_t q_len, int64_t kv_len)
 {
     double dot = 0.0;
     for (int d = 0; d < D; d++) dot += qi[d] * kj[d];
     double s = scale * dot;
     if (bias_h) s += bias_h[oracle_relpos_bucket(i + (kv_len - q_len) - j)];
+    if (dense_hb) s += dense_hb[i * kv_len + j];
     return s;
+}
+
+/* First pair of sequence b in a dense per-pair array: sum of q_len * kv_len before b. */
+static int64_t pair_offset(const int32_t *q_off, const int32_t *kv_off, int b)
+{
+    int64_t acc = 0;
+    for (int c = 0; c < b; c++)
+        acc += ((int64_t)q_off[c + 1] - q_off[c]) * ((int64_t)kv_off[c + 1] - kv_off[c]);
+    return acc;
+}
+
+/* P = sum_b q_len_b * kv_len_b: the number of (query, key) pairs of the batch. */
+int64_t oracle_num_pairs(int B, const int32_t *q_off, const int32_t *kv_off)
+{
+    return pair_offset(q_off, kv_off, B);
 }
 
 static int allowed(int causal, int window, int64_t i, int64_t j, int64_t q_len, int64_t kv_len)
@@ -144,13 +172,16 @@ int oracle_max_threads(void)
 /*
  * Forward.  O[T_q, H, D]; LSE[T_q, H] (softmax: log of the row's partition
  * function, -inf for a row with no allowed key; GDPA: 0).
- * bias: [H, 32] or NULL.  Returns 0, or -1 on an allocation failure.
+ * bias: [H, 32] or NULL; dense: [H, P] per-pair bias or NULL.
+ * Returns 0, or -1 on an allocation failure.
  */
 int oracle_fwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                const double *Q, const double *K, const double *V, int mode, int causal,
-               int window, const double *bias, double scale, double *O, double *LSE, int nthreads)
+               int window, const double *bias, const double *dense, double scale, double *O,
+               double *LSE, int nthreads)
 {
     int failed = 0;
+    const int64_t P = oracle_num_pairs(B, q_off, kv_off);
     set_threads(nthreads);
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
     for (int b = 0; b < B; b++) {
@@ -158,6 +189,7 @@ int oracle_fwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
             const int64_t q0 = q_off[b], q_len = (int64_t)q_off[b + 1] - q_off[b];
             const int64_t k0 = kv_off[b], kv_len = (int64_t)kv_off[b + 1] - kv_off[b];
             const double *bias_h = bias ? bias + (int64_t)h * 32 : NULL;
+            const double *dense_hb = dense ? dense + (int64_t)h * P + pair_offset(q_off, kv_off, b) : NULL;
             double *s = (double *)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
             if (!s) {
 #pragma omp atomic write
@@ -174,7 +206,7 @@ int oracle_fwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                 int64_t n_allowed = 0;
                 for (int64_t j = 0; j < kv_len; j++) {
                     if (!allowed(causal, window, i, j, q_len, kv_len)) continue;
-                    s[j] = score(qi, K + ((k0 + j) * H + h) * D, D, scale, bias_h, i, j, q_len, kv_len);
+                    s[j] = score(qi, K + ((k0 + j) * H + h) * D, D, scale, bias_h, dense_hb, i, j, q_len, kv_len);
                     if (s[j] > m) m = s[j];
                     n_allowed++;
                 }
@@ -216,14 +248,24 @@ int oracle_fwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
  *   ds_ij = p_ij (dp_ij - sum_k p_ik dp_ik)   (softmax)
  *   ds_ij = act'(s_ij) dp_ij                  (GDPA, p_ij = act(s_ij))
  *   dq_i  = scale sum_j ds_ij k_j,   dk_j = scale sum_i ds_ij q_i
- * Each (sequence, head) pair owns its rows of dQ, dK and dV.
+ *   d_dense[h, (i, j)] = ds_ij,       dbias[h, k] = sum of ds_ij with bucket(r_ij) = k
+ * Each (sequence, head) pair owns its rows of dQ, dK and dV and its block of d_dense.
+ * dbias [H, 32] and d_dense [H, P] are optional outputs (NULL: not computed); the
+ * table's gradient is summed over sequences in sequence order after the parallel
+ * loop, from one partial table per (sequence, head).
  */
 int oracle_bwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                const double *Q, const double *K, const double *V, const double *dO, int mode,
-               int causal, int window, const double *bias, double scale, double *dQ, double *dK,
-               double *dV, int nthreads)
+               int causal, int window, const double *bias, const double *dense, double scale,
+               double *dQ, double *dK, double *dV, double *dbias, double *d_dense, int nthreads)
 {
     int failed = 0;
+    const int64_t P = oracle_num_pairs(B, q_off, kv_off);
+    double *dbias_part = NULL;
+    if (dbias) {
+        dbias_part = (double *)calloc((size_t)(B > 0 ? B : 1) * (size_t)H * 32, sizeof(double));
+        if (!dbias_part) return -1;
+    }
     set_threads(nthreads);
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
     for (int b = 0; b < B; b++) {
@@ -231,6 +273,12 @@ int oracle_bwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
             const int64_t q0 = q_off[b], q_len = (int64_t)q_off[b + 1] - q_off[b];
             const int64_t k0 = kv_off[b], kv_len = (int64_t)kv_off[b + 1] - kv_off[b];
             const double *bias_h = bias ? bias + (int64_t)h * 32 : NULL;
+            const int64_t pb = pair_offset(q_off, kv_off, b);
+            const double *dense_hb = dense ? dense + (int64_t)h * P + pb : NULL;
+            double *d_dense_hb = d_dense ? d_dense + (int64_t)h * P + pb : NULL;
+            double *dbias_bh = dbias_part ? dbias_part + ((int64_t)b * H + h) * 32 : NULL;
+            if (d_dense_hb)
+                for (int64_t e = 0; e < q_len * kv_len; e++) d_dense_hb[e] = 0.0;
             size_t n = (size_t)(kv_len > 0 ? kv_len : 1);
             double *s = (double *)malloc(sizeof(double) * n);
             double *p = (double *)malloc(sizeof(double) * n);
@@ -258,7 +306,7 @@ int oracle_bwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                 int64_t n_allowed = 0;
                 for (int64_t j = 0; j < kv_len; j++) {
                     if (!allowed(causal, window, i, j, q_len, kv_len)) continue;
-                    s[j] = score(qi, K + ((k0 + j) * H + h) * D, D, scale, bias_h, i, j, q_len, kv_len);
+                    s[j] = score(qi, K + ((k0 + j) * H + h) * D, D, scale, bias_h, dense_hb, i, j, q_len, kv_len);
                     if (s[j] > m) m = s[j];
                     n_allowed++;
                 }
@@ -292,6 +340,8 @@ int oracle_bwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
                         ds = p[j] * (dp[j] - delta);
                     else
                         ds = oracle_act_grad(mode, s[j]) * dp[j];
+                    if (d_dense_hb) d_dense_hb[i * kv_len + j] = ds;
+                    if (dbias_bh) dbias_bh[oracle_relpos_bucket(i + (kv_len - q_len) - j)] += ds;
                     const double *kj = K + ((k0 + j) * H + h) * D;
                     double *dkj = dK + ((k0 + j) * H + h) * D;
                     double *dvj = dV + ((k0 + j) * H + h) * D;
@@ -306,6 +356,12 @@ int oracle_bwd(int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
             free(p);
             free(dp);
         }
+    }
+    if (dbias) {
+        for (int64_t e = 0; e < (int64_t)H * 32; e++) dbias[e] = 0.0;
+        for (int b = 0; b < B; b++)
+            for (int64_t e = 0; e < (int64_t)H * 32; e++) dbias[e] += dbias_part[(int64_t)b * H * 32 + e];
+        free(dbias_part);
     }
     return failed ? -1 : 0;
 }
