@@ -145,6 +145,30 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
                    int32_t bias_kind, const float* bias_table, float scale, void* dQ, void* dK,
                    void* dV, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * jfa_bwd that also returns the gradient of the bias (the article's "custom attention
+ * bias", aihot.vn GEM article, section "Jagged Sequence Flash Attention", made
+ * trainable): a bias adds to the score, so its gradient is dS.  For the table of
+ * JFA_BIAS_RELPOS32, entry (h, k) receives the sum of ds_ij over the allowed pairs
+ * (i, j) of head h, in every sequence, whose relative position falls in bucket k:
+ *   dbias[h, k] = sum_{b, i, j allowed, bucket(|i + kv_len - q_len - j|) = k} ds_ij,
+ *   ds_ij = p_ij (dp_ij - sum_l p_il dp_il) (softmax) or act'(s_ij) dp_ij (GDPA).
+ *   dbias: fp32 [H, 32] device pointer, 4-byte aligned, caller-owned; overwritten
+ *     (not accumulated into).  NULL makes the call exactly jfa_bwd.  Requires
+ *     bias_kind JFA_BIAS_RELPOS32 (the gradient is taken at the given table).
+ *   workspace: at least jfa_bwd_ex_workspace_size(plan, dtype, bias_kind) bytes when
+ *     dbias is set (jfa_bwd_workspace_size otherwise), 256-byte aligned.
+ *   The result is the same on every run: each CTA and warp sums its part in a fixed
+ *   order, and a last kernel adds the parts in a fixed order.
+ * Errors: those of jfa_bwd; INVALID_ARG for a dbias without JFA_BIAS_RELPOS32, a
+ * misaligned dbias or too small a workspace.
+ */
+size_t jfa_bwd_ex_workspace_size(jfa_plan plan, int32_t dtype, int32_t bias_kind);
+jfa_status jfa_bwd_ex(jfa_plan plan, int32_t dtype, const void* Q, const void* K, const void* V,
+                      const void* O, int32_t o_dtype, const void* dO, const float* lse,
+                      int32_t bias_kind, const float* bias_table, float scale, void* dQ, void* dK,
+                      void* dV, float* dbias, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the library-held scratch array that jfa_bwd_static_scratch uses on each
  * GPU (64 MiB).  A plan fits when jfa_bwd_workspace_size(plan, dtype) is at most
  * this: T_q * H up to about 16.7 million (token, head) rows for JFA_BF16, and

@@ -379,10 +379,47 @@ size_t jfa_bwd_workspace_size(jfa_plan plan, int32_t dtype) {
     return round_up(rows * 4, 256) + (dtype == JFA_F32 ? round_up(rows * size_t(plan->D) * 4, 256) : 0);
 }
 
+// Bytes of the partial table gradients: one [H][32] table per (CTA, compute warp) of
+// the dK/dV grid (bf16), or one [32] row per work item (fp32).
+static size_t dbias_part_bytes(jfa_plan plan, int32_t dtype) {
+    const size_t n = dtype == JFA_BF16 ? size_t(plan->bwd_grid) * kDkdvCompWarps * size_t(plan->H) * 32
+                                       : size_t(plan->n_bwd_items) * 32;
+    return round_up(n * 4, 256);
+}
+
+size_t jfa_bwd_ex_workspace_size(jfa_plan plan, int32_t dtype, int32_t bias_kind) {
+    const size_t base = jfa_bwd_workspace_size(plan, dtype);
+    if (base == 0 && !plan) return 0;
+    return base + (bias_kind == JFA_BIAS_RELPOS32 ? dbias_part_bytes(plan, dtype) : 0);
+}
+
+static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const void* K, const void* V, const void* O,
+                           int32_t o_dtype, const void* dO, const float* lse, int32_t bias_kind,
+                           const float* bias_table, float scale, void* dQ, void* dK, void* dV, float* dbias,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
 jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, const void* V, const void* O,
                    int32_t o_dtype, const void* dO, const float* lse, int32_t bias_kind, const float* bias_table,
                    float scale, void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
                    void* stream) {
+    return bwd_impl(plan, dtype, Q, K, V, O, o_dtype, dO, lse, bias_kind, bias_table, scale, dQ, dK, dV, nullptr,
+                    workspace, workspace_bytes, stream);
+}
+
+jfa_status jfa_bwd_ex(jfa_plan plan, int32_t dtype, const void* Q, const void* K, const void* V, const void* O,
+                      int32_t o_dtype, const void* dO, const float* lse, int32_t bias_kind, const float* bias_table,
+                      float scale, void* dQ, void* dK, void* dV, float* dbias, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    if (dbias && (bias_kind != JFA_BIAS_RELPOS32 || (reinterpret_cast<uintptr_t>(dbias) & 3u)))
+        return JFA_ERR_INVALID_ARG;
+    return bwd_impl(plan, dtype, Q, K, V, O, o_dtype, dO, lse, bias_kind, bias_table, scale, dQ, dK, dV, dbias,
+                    workspace, workspace_bytes, stream);
+}
+
+static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const void* K, const void* V, const void* O,
+                           int32_t o_dtype, const void* dO, const float* lse, int32_t bias_kind,
+                           const float* bias_table, float scale, void* dQ, void* dK, void* dV, float* dbias,
+                           void* workspace, size_t workspace_bytes, void* stream) {
     jfa_status s = check_plan_call(plan, dtype, bias_kind, bias_table);
     if (s != JFA_OK) return s;
     if (o_dtype != JFA_BF16 && o_dtype != JFA_F32) return JFA_ERR_INVALID_ARG;
@@ -394,14 +431,21 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
         !aligned16(dK) || !aligned16(dV) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
         (reinterpret_cast<uintptr_t>(bias_table) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return JFA_ERR_INVALID_ARG;
-    const size_t need = jfa_bwd_workspace_size(plan, dtype);
+    const size_t base = jfa_bwd_workspace_size(plan, dtype);
+    const size_t need = dbias ? jfa_bwd_ex_workspace_size(plan, dtype, bias_kind) : base;
     if (workspace_bytes < need || (need > 0 && !workspace)) return JFA_ERR_INVALID_ARG;
-    if (plan->Tkv == 0 && plan->Tq == 0) return JFA_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dbias && plan->n_bwd_items == 0) {
+        // no key tile sees a query: the table gradient is zero
+        if (cudaMemsetAsync(dbias, 0, size_t(plan->H) * 32 * 4, st) != cudaSuccess) return JFA_ERR_CUDA;
+        dbias = nullptr;
+    }
+    if (plan->Tkv == 0 && plan->Tq == 0) return JFA_OK;
     const size_t rows = size_t(plan->Tq) * size_t(plan->H);
     float* delta = static_cast<float*>(workspace);
     float* dq_acc = dtype == JFA_F32 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * 4, 256))
                                      : nullptr;
+    float* dbias_part = dbias ? reinterpret_cast<float*>(static_cast<char*>(workspace) + base) : nullptr;
 
     cudaError_t e = cudaSuccess;
     if (plan->Tq > 0) {
@@ -437,6 +481,7 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
         p.dK = dK;
         p.dV = dV;
         p.status = plan->d_status;
+        p.dbias_part = dbias_part;
     }
     if (plan->n_bwd_items > 0) {
         KernelTimer tm(plan, 2, st);
@@ -444,6 +489,13 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
                               : launch_bwd_f32(plan->D, Q, K, V, dO, p, plan->n_bwd_items, st);
         tm.done();
         if (e != cudaSuccess) return JFA_ERR_CUDA;
+        if (dbias) {
+            e = dtype == JFA_BF16
+                    ? launch_dbias_reduce(dbias_part, int64_t(plan->bwd_grid) * kDkdvCompWarps, plan->H, dbias, st)
+                    : launch_dbias_reduce_items(dbias_part, plan->d_bwd_items, plan->n_bwd_items, plan->H, dbias, st);
+            if (e != cudaSuccess) return JFA_ERR_CUDA;
+        }
+        p.dbias_part = nullptr;  // the dQ pass does not take part
     }
     if (dtype == JFA_BF16 && plan->n_dq_items > 0) {
         // dQ per query tile, written directly (also the zero rows of tiles that see no key)

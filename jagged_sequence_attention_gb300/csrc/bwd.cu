@@ -60,12 +60,13 @@ struct KvCfg {
     static constexpr int kOffBar = kOffDO + 2 * kQTile;
     static constexpr int kNumBars = 24;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kCompWarps = 8;
+    static constexpr int kCompWarps = kDkdvCompWarps;
     static constexpr int kCols = BM / 2;  // query columns per compute thread
     // tmem slot + abort flag (16 B); per compute warp: -lse and -Delta of its columns, the
-    // head's bias row, and a step's bias-by-relative-position table (kCols + 32 entries)
+    // head's bias row, a step's bias-by-relative-position table (kCols + 32 entries) and
+    // the item's bias-table gradient by bucket (32 entries)
     static constexpr int kRelTab = kCols + 32;
-    static constexpr int kWarpMisc = 2 * kCols + 32 + kRelTab;
+    static constexpr int kWarpMisc = 2 * kCols + 32 + kRelTab + 32;
     static constexpr int kMiscBytes = 16 + kCompWarps * kWarpMisc * 4;
     static constexpr int kSmemNeed = kOffMisc + kMiscBytes + 1024;
     // At least 120 KB so that exactly one CTA fits on an SM: it allocates all 512 TMEM columns.
@@ -100,7 +101,17 @@ enum {
     KV_DRAIN = 21,
 };
 
-template <int D, bool GDPA>
+// Warp sum by xor-shuffles: every lane receives the total, in the same order each run.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// DBIAS: also accumulate the gradient of the relative-position bias table, the sum of
+// dS over the allowed pairs of each bucket, into per-(CTA, warp) partial tables that a
+// second kernel sums in a fixed order (so the result is the same on every run).
+template <int D, bool GDPA, bool DBIAS>
 __global__ void __launch_bounds__(320, 1)
     jfa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -362,6 +373,26 @@ __global__ void __launch_bounds__(320, 1)
         float* del_s = lse_s + NC;                      // -Delta per column
         float* bias_w = del_s + NC;                     // the head's bias row (log2 units for softmax)
         float* rtab = bias_w + 32;                      // bias by relative position, per step
+        float* dacc_w = rtab + C::kRelTab;              // the item's table gradient by bucket
+        // This warp's partial table gradient [H][32], owned by this warp alone.
+        float* dpart = DBIAS ? p.dbias_part + (size_t(blockIdx.x) * C::kCompWarps + size_t(warp)) * size_t(p.H) * 32
+                             : nullptr;
+        // Gradient of warp-constant chunks: a per-thread sum for each chunk slot, tagged
+        // with the (warp-uniform) bucket it belongs to, flushed when the bucket changes.
+        float dacc[2] = {0.f, 0.f};
+        int dtag[2] = {-1, -1};
+        auto dflush = [&](int k) {
+            if (dtag[k] >= 0) {
+                const float v = warp_sum(dacc[k]);
+                if (lane == 0) dacc_w[dtag[k]] += v;
+            }
+            dacc[k] = 0.f;
+        };
+        if constexpr (DBIAS) {
+            dacc_w[lane] = 0.f;
+            for (int e = lane; e < p.H * 32; e += 32) dpart[e] = 0.f;
+            __syncwarp();
+        }
         // Element (lane, c) has relative position rbase(lane 0) - lane + c: rtab[k] holds
         // the bias of rbase(lane 0) - 31 + k, so the lane reads rrow[c], rrow = rtab + 31 - lane.
         const float* rrow = rtab + 31 - lane;
@@ -430,6 +461,7 @@ __global__ void __launch_bounds__(320, 1)
                 // spans relative positions rbase(lane 0) + 32k - 31 .. + 62.
                 bool cconst[2] = {true, true};
                 float cbias[2] = {0.f, 0.f};
+                int cbk[2] = {0, 0};  // the bucket of a warp-constant chunk (DBIAS)
                 if (p.bias) {
                     const int rb0 = __shfl_sync(0xffffffffu, rbase, 0);
                     int bk = 0;
@@ -439,6 +471,7 @@ __global__ void __launch_bounds__(320, 1)
                     for (int k = 0; k < 2; ++k) {
                         cconst[k] = (cm >> k) & 1u;
                         cbias[k] = __shfl_sync(0xffffffffu, bv, k);
+                        if constexpr (DBIAS) cbk[k] = __shfl_sync(0xffffffffu, bk, k);
                     }
                 }
                 // Staged addend of column c: -lse, plus the chunk's bias when that is
@@ -557,6 +590,12 @@ __global__ void __launch_bounds__(320, 1)
                                                    add2(make_float2(dp[c + 2], dp[c + 3]), make_float2(d4.z, d4.w)));
                             pd[c >> 1] = pack_bf16x2(a.x, a.y);
                             pd[(c >> 1) + 1] = pack_bf16x2(b2.x, b2.y);
+                            if constexpr (DBIAS) {  // keep dS (fp32) for the table gradient
+                                dp[c] = a.x;
+                                dp[c + 1] = a.y;
+                                dp[c + 2] = b2.x;
+                                dp[c + 3] = b2.y;
+                            }
                         }
                     } else {
 #pragma unroll
@@ -564,6 +603,10 @@ __global__ void __launch_bounds__(320, 1)
                             const float2 a = mul2(make_float2(pv[32 * k + c], pv[32 * k + c + 1]),
                                                   make_float2(dp[c], dp[c + 1]));
                             pd[c >> 1] = pack_bf16x2(a.x, a.y);
+                            if constexpr (DBIAS) {
+                                dp[c] = a.x;
+                                dp[c + 1] = a.y;
+                            }
                         }
                     }
                     tmem_st16(tY + 16u * k, pd);
@@ -571,9 +614,50 @@ __global__ void __launch_bounds__(320, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(KV_DS_FULL + k));
+                    if constexpr (DBIAS) {
+                        // Table gradient of this chunk (dS is exactly 0 at masked pairs).
+                        if (cconst[k]) {
+                            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) s4[c & 3] += dp[c];
+                            if (cbk[k] != dtag[k]) {
+                                dflush(k);
+                                dtag[k] = cbk[k];
+                            }
+                            dacc[k] += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                        } else {
+                            // Element (lane l, column c) lies on diagonal d = c - l + 31 of the
+                            // chunk, relative position rlo + d.  Lane m gathers diagonals m and
+                            // m + 32: from column c it takes lane (c + 31 - m) mod 32's element.
+                            const int rlo = __shfl_sync(0xffffffffu, rbase, 0) + 32 * k - 31;
+                            float g0 = 0.f, g1 = 0.f;
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                const float v = __shfl_sync(0xffffffffu, dp[c], (c + 31 - lane) & 31);
+                                if (lane >= c) g0 += v; else g1 += v;
+                            }
+                            const int b0 = relpos_bucket(rlo + lane), b1 = relpos_bucket(rlo + lane + 32);
+                            const int bmin = __reduce_min_sync(0xffffffffu, min(b0, b1));
+                            const int bmax = __reduce_max_sync(0xffffffffu, max(b0, b1));
+                            for (int kb = bmin; kb <= bmax; ++kb) {
+                                const float v = warp_sum((b0 == kb ? g0 : 0.f) + (b1 == kb ? g1 : 0.f));
+                                if (lane == 0) dacc_w[kb] += v;
+                            }
+                        }
+                    }
                 }
             }
             if (!ok) break;
+            if constexpr (DBIAS) {
+                // the item's table gradient into this warp's partial table of head h
+                dflush(0);
+                dflush(1);
+                dtag[0] = dtag[1] = -1;
+                __syncwarp();
+                dpart[h * 32 + lane] += dacc_w[lane];
+                dacc_w[lane] = 0.f;
+                __syncwarp();
+            }
             // Epilogue: dV and dK (times scale) of this key row, the warpgroup's half of D.
             if (!warp_wait(KV_ACC_FULL, item_it & 1)) { ok = false; break; }
             tc_fence_after();
@@ -664,26 +748,50 @@ __global__ void jfa_bwd_post_kernel(const float4* __restrict__ acc, T* __restric
     }
 }
 
-template <int D, bool GDPA>
+// One thread per (head, bucket): the sum over the partial tables, slot by slot.
+__global__ void jfa_dbias_reduce_kernel(const float* __restrict__ part, int64_t n_slots, int H, float* dbias) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= H * 32) return;
+    float acc = 0.f;
+    for (int64_t s = 0; s < n_slots; ++s) acc += part[s * H * 32 + e];
+    dbias[e] = acc;
+}
+
+// fp32 path: one partial per work item; the item's head selects the row it adds to.
+__global__ void jfa_dbias_reduce_items_kernel(const float* __restrict__ part, const int4* __restrict__ items,
+                                              int64_t n_items, int H, float* dbias) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= H * 32) return;
+    const int h = e >> 5, k = e & 31;
+    float acc = 0.f;
+    for (int64_t it = 0; it < n_items; ++it)
+        if (items[it].y == h) acc += part[it * 32 + k];
+    dbias[e] = acc;
+}
+
+template <int D, bool GDPA, bool DBIAS>
 cudaError_t launch_dkdv_t_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
     using C = KvCfg<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(jfa_bwd_dkdv_kernel<D, GDPA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(jfa_bwd_dkdv_kernel<D, GDPA, DBIAS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_dkdv_kernel<D, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
+    jfa_bwd_dkdv_kernel<D, GDPA, DBIAS><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_dkdv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
-    return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                                 : launch_dkdv_t_m<D, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    if (p.dbias_part)
+        return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false, true>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                                     : launch_dkdv_t_m<D, true, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                                 : launch_dkdv_t_m<D, true, false>(tmQ, tmK, tmV, tmdO, p, grid, st);
 }
 
 template <typename TO, typename T, int D>
@@ -724,6 +832,19 @@ cudaError_t launch_bwd_main(int dtype, int D, const CUtensorMap& tmQ, const CUte
     if (dtype == JFA_BF16 && D == 128) return launch_dkdv_t<128>(tmQ, tmK, tmV, tmdO, p, grid, st);
     if (dtype == JFA_BF16 && D == 64) return launch_dkdv_t<64>(tmQ, tmK, tmV, tmdO, p, grid, st);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dbias_reduce(const float* part, int64_t n_slots, int H, float* dbias, cudaStream_t st) {
+    const int n = H * 32;
+    jfa_dbias_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(part, n_slots, H, dbias);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dbias_reduce_items(const float* part, const int4* items, int64_t n_items, int H, float* dbias,
+                                      cudaStream_t st) {
+    const int n = H * 32;
+    jfa_dbias_reduce_items_kernel<<<(n + 255) / 256, 256, 0, st>>>(part, items, n_items, H, dbias);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_post(int dtype, int D, const float* dq_acc, void* dQ, int64_t Tq, int H, float scale,

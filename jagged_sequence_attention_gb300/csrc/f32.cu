@@ -130,9 +130,11 @@ __global__ void __launch_bounds__(kF32Rows) jfa_fwd_f32_kernel(const float* __re
 }
 
 // One CTA per backward work item (key tile of 128 rows); thread = key row.  Query
-// rows stream through shared memory 64 at a time; dS for the chunk is kept in
+// rows stream through shared memory kF32InnerB at a time; dS for the chunk is kept in
 // shared memory so that dQ is reduced over the CTA's keys before one atomic add per
-// (query row, d).
+// (query row, d).  With p.dbias_part set, the chunk's dS is also summed along its
+// diagonals (one relative position each) and the diagonals by bucket, in a fixed
+// order, into the item's partial table gradient p.dbias_part[item][32].
 template <int D>
 __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                                                                 const float* __restrict__ V, const float* __restrict__ dO,
@@ -142,6 +144,9 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
     __shared__ float sDS[kF32InnerB][kF32Rows + 1];
     __shared__ float sL[kF32InnerB], sDel[kF32InnerB];
     __shared__ float sB[32];
+    constexpr int kDiags = kF32InnerB + kF32Rows - 1;  // diagonals i - t of a chunk
+    __shared__ float sDiag[kDiags];
+    __shared__ float sDB[32];  // the item's table gradient, bucket t owned by thread t
     const int4 w = p.items[blockIdx.x];
     const int b = w.x, h = w.y, nt = w.z, n = w.w;
     const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
@@ -151,6 +156,7 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
     const int diag = kv_len - q_len;
     const bool softmax = p.mode == JFA_SOFTMAX;
     if (t < 32) sB[t] = p.bias ? p.bias[h * 32 + t] : 0.f;
+    if (t < 32) sDB[t] = 0.f;
     const size_t rk = (size_t(k0) + size_t(kvalid ? j : 0)) * p.H + h;
     float k[D], v[D], dk[D], dv[D];
 #pragma unroll
@@ -223,7 +229,27 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
             const size_t rq = (size_t(q0) + size_t(r0 + i)) * p.H + h;
             atomicAdd(p.dq_acc + rq * D + d, acc);
         }
+        if (p.dbias_part) {
+            // diagonal dd holds the elements with i - t = dd - (kF32Rows - 1), i ascending
+            for (int dd = t; dd < kDiags; dd += kF32Rows) {
+                const int off = dd - (kF32Rows - 1);
+                const int i0 = max(0, off), i1 = min(kF32InnerB - 1, kF32Rows - 1 + off);
+                float acc = 0.f;
+                for (int i = i0; i <= i1; ++i) acc += sDS[i][i - off];
+                sDiag[dd] = acc;
+            }
+            __syncthreads();
+            if (t < 32) {
+                // element (i, t') has relative position r0 + i + diag - (nt * 128 + t')
+                const int rel0 = r0 + diag - nt * kBwdBN - (kF32Rows - 1);
+                float acc = 0.f;
+                for (int dd = 0; dd < kDiags; ++dd)
+                    if (bucket_f32(rel0 + dd) == t) acc += sDiag[dd];
+                sDB[t] += acc;
+            }
+        }
     }
+    if (p.dbias_part && t < 32) p.dbias_part[size_t(blockIdx.x) * 32 + t] = sDB[t];
     if (!kvalid) return;
     float* dK = static_cast<float*>(p.dK) + rk * D;
     float* dV = static_cast<float*>(p.dV) + rk * D;

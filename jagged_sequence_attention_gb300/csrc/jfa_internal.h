@@ -29,6 +29,8 @@ enum : int { kPassFwd = 0, kPassBwdKV = 1, kPassBwdQ = 2 };
 // Kernel kinds of the timing hook: forward, backward preprocess, backward dK/dV (or
 // the fp32 main kernel), fp32 dQ conversion, bf16 dQ.
 constexpr int kNumKernelKinds = 5;
+// Compute warps of the bf16 dK/dV kernel (each keeps its own partial table gradient).
+constexpr int kDkdvCompWarps = 8;
 
 // One unit of persistent-grid work: sequence, head, tile index (query tile for the
 // forward, key/value tile for the backward) and the number of inner tiles visited.
@@ -153,6 +155,9 @@ struct BwdParams {
     void* dK;
     void* dV;
     int* status;
+    // Partial gradients of the relative-position bias table, or nullptr: bf16 inputs
+    // [grid][compute warps][H][32], fp32 inputs [work item][32].
+    float* dbias_part = nullptr;
 };
 
 // Host planner (plan.cpp).  Returns JFA_OK or an error for bad offsets.
@@ -184,6 +189,11 @@ cudaError_t launch_bwd_post(int dtype, int D, const float* dq_acc, void* dQ, int
 // fp32 element type: CUDA-core kernels, one CTA per work item (f32.cu).
 cudaError_t launch_fwd_f32(int D, const void* Q, const void* K, const void* V, const FwdParams& p, int64_t n_items,
                            cudaStream_t st);
+// Sums the partial table gradients in a fixed order into dbias [H][32]: slots of
+// [n_slots][H][32] (bf16 path), or items' [n_items][32] partials by their head (fp32).
+cudaError_t launch_dbias_reduce(const float* part, int64_t n_slots, int H, float* dbias, cudaStream_t st);
+cudaError_t launch_dbias_reduce_items(const float* part, const int4* items, int64_t n_items, int H, float* dbias,
+                                      cudaStream_t st);
 cudaError_t launch_bwd_f32(int D, const void* Q, const void* K, const void* V, const void* dO, const BwdParams& p,
                            int64_t n_items, cudaStream_t st);
 

@@ -27,14 +27,14 @@ __device__ __forceinline__ bool chunk_bucket_const(int r_hi, int& bucket) {
 
 // Warp-level form of the test above.  In the callers, the 32 lanes' windows for one
 // chunk tile a range of 63 relative positions [lo, lo + 62] (consecutive rows or keys
-// shift the window by one).  A bucket boundary inside that range lies inside some lane's
-// window, so every lane's chunk is constant exactly when the whole range is >= 0 and in
-// one bucket, and then all lanes share that bucket.  Each lane evaluates one chunk (the
-// caller passes lane k the range of chunk k); returns the ballot of constant chunks, and
-// the chunk's bucket in `bucket`.
+// shift the window by one).  The bucket of |r| is monotone on a range that does not
+// cross 0, so every lane's chunk is constant exactly when the whole range lies on one
+// side of 0 and its two ends share a bucket; then all lanes share that bucket.  Each
+// lane evaluates one chunk (the caller passes lane k the range of chunk k); returns the
+// ballot of constant chunks, and the chunk's bucket in `bucket`.
 __device__ __forceinline__ uint32_t warp_const_chunks(bool active, int lo, int& bucket) {
     bucket = relpos_bucket(lo + 62);
-    const bool c = active && lo >= 0 && relpos_bucket(lo) == bucket;
+    const bool c = active && (lo >= 0 || lo + 62 <= 0) && relpos_bucket(lo) == bucket;
     return __ballot_sync(0xffffffffu, c);
 }
 

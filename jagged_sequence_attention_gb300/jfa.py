@@ -60,6 +60,9 @@ def lib():
         L.jfa_bwd_workspace_size.argtypes = [vp, i32]
         L.jfa_bwd_workspace_size.restype = sz
         L.jfa_bwd.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
+        L.jfa_bwd_ex_workspace_size.argtypes = [vp, i32, i32]
+        L.jfa_bwd_ex_workspace_size.restype = sz
+        L.jfa_bwd_ex.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, vp, sz, vp]
         L.jfa_bwd_static_scratch.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp]
         L.jfa_plan_device_status.argtypes = [vp, vp]
         L.jfa_partition_sequences.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp]
@@ -217,6 +220,33 @@ def jfa_bwd(plan: Plan, Q, K, V, O, dO, lse, bias=None, scale=None, dQ=None, dK=
     return dQ, dK, dV
 
 
+def jfa_bwd_ex_workspace_size(plan: Plan, dtype=torch.bfloat16, bias_grad=True) -> int:
+    return int(lib().jfa_bwd_ex_workspace_size(plan.handle, DTYPES[dtype],
+                                               JFA_BIAS_RELPOS32 if bias_grad else JFA_BIAS_NONE))
+
+
+def jfa_bwd_ex(plan: Plan, Q, K, V, O, dO, lse, bias, scale=None, dQ=None, dK=None, dV=None, dbias=None,
+               workspace=None, stream=None):
+    """jfa_bwd plus the gradient of the relative-position bias table [H, 32] (fp32).
+    Returns (dQ, dK, dV, dbias)."""
+    dt = _dtype_code(Q)
+    scale = 1.0 / float(plan.D) ** 0.5 if scale is None else float(scale)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    if dbias is None:
+        dbias = torch.empty((plan.H, 32), dtype=torch.float32, device=Q.device)
+    need = jfa_bwd_ex_workspace_size(plan, Q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    bk, bp = _bias_args(bias)
+    _check("jfa_bwd_ex", lib().jfa_bwd_ex(plan.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _dtype_code(O),
+                                          _ptr(dO), _ptr(lse), bk, bp, scale, _ptr(dQ), _ptr(dK), _ptr(dV),
+                                          _ptr(dbias), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream)))
+    return dQ, dK, dV, dbias
+
+
 def jfa_bwd_static_scratch(plan: Plan, Q, K, V, O, dO, lse, bias=None, scale=None, dQ=None, dK=None, dV=None,
                            stream=None):
     """jfa_bwd with the library's static scratch array in place of a workspace, for
@@ -305,13 +335,18 @@ def jfa_worklist_build(q_offsets, kv_offsets, H: int, causal: bool, pass_: int, 
 # --------------------------------------------------------------------------- convenience
 
 
-def attention(batch, with_backward=True, stream=None, out_dtype=None):
-    """Run forward (and backward) for a workloads.Batch on the GPU: returns dict of tensors."""
+def attention(batch, with_backward=True, stream=None, out_dtype=None, bias_grad=False):
+    """Run forward (and backward) for a workloads.Batch on the GPU: returns dict of tensors
+    (with bias_grad, also "dbias", the gradient of the batch's bias table)."""
     plan = jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal, stream,
                            window=getattr(batch, "window", None))
     O, lse = jfa_fwd(plan, batch.Q, batch.K, batch.V, batch.bias, batch.scale, stream=stream, out_dtype=out_dtype)
     out = {"O": O, "lse": lse, "plan": plan}
-    if with_backward:
+    if with_backward and bias_grad:
+        dQ, dK, dV, dbias = jfa_bwd_ex(plan, batch.Q, batch.K, batch.V, O, batch.dO, lse, batch.bias, batch.scale,
+                                       stream=stream)
+        out.update(dQ=dQ, dK=dK, dV=dV, dbias=dbias)
+    elif with_backward:
         dQ, dK, dV = jfa_bwd(plan, batch.Q, batch.K, batch.V, O, batch.dO, lse, batch.bias, batch.scale,
                              stream=stream)
         out.update(dQ=dQ, dK=dK, dV=dV)

@@ -158,10 +158,11 @@ def fwd(q_off, kv_off, Q, K, V, *, mode="softmax", causal=False, bias=None, scal
 
 
 def bwd(q_off, kv_off, Q, K, V, dO, *, mode="softmax", causal=False, bias=None, scale=None,
-        nthreads=0, window=None, dense_bias=None, bias_grads=False):
+        nthreads=0, window=None, dense_bias=None, bias_grads=False, dense_grad=True):
     """Returns (dQ, dK, dV), fp64, same shapes as Q, K, V; with bias_grads also the
     gradient of the bucket table [H, 32] and of a dense per-pair bias [H, P] (both are
-    defined whether or not that bias was given: the gradient of the score)."""
+    defined whether or not that bias was given: the gradient of the score).  With
+    dense_grad=False the dense gradient is not formed (returned as None)."""
     lib = _load()
     q_off, kv_off, Q, K, V = _check(q_off, kv_off, Q, K, V)
     dO = _f64(dO)
@@ -174,7 +175,7 @@ def bwd(q_off, kv_off, Q, K, V, dO, *, mode="softmax", causal=False, bias=None, 
     dn = _dense(dense_bias, H, q_off, kv_off)
     dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
     dbias = np.zeros((H, 32)) if bias_grads else None
-    d_dense = np.zeros((H, num_pairs(q_off, kv_off))) if bias_grads else None
+    d_dense = np.zeros((H, num_pairs(q_off, kv_off))) if bias_grads and dense_grad else None
     rc = lib.oracle_bwd(B, H, D, _ptr(q_off, ctypes.c_int32), _ptr(kv_off, ctypes.c_int32),
                         _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), MODES[mode], int(bool(causal)),
                         -1 if window is None else int(window),

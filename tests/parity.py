@@ -49,8 +49,9 @@ def run_gpu(batch, with_backward=True, out_dtype=torch.float32):
     return out
 
 
-def run_oracle(batch, with_backward=True):
-    """Oracle on a (CPU-copied) batch: dict of fp64 numpy arrays."""
+def run_oracle(batch, with_backward=True, bias_grads=False):
+    """Oracle on a (CPU-copied) batch: dict of fp64 numpy arrays (with bias_grads also
+    "dbias", the gradient of the bias table)."""
     b = None if batch.bias is None else np64(batch.bias)
     Q, K, V = np64(batch.Q), np64(batch.K), np64(batch.V)
     Tq, Tkv = int(batch.q_off[-1]), int(batch.kv_off[-1])
@@ -60,9 +61,11 @@ def run_oracle(batch, with_backward=True):
     res = {"O": O, "lse": LSE}
     if with_backward:
         dO = np64(batch.dO)[:Tq]
-        dQ, dK, dV = oracle.bwd(batch.q_off, batch.kv_off, Q, K, V, dO, mode=batch.mode,
-                                causal=batch.causal, bias=b, scale=batch.scale, window=batch.window)
-        res.update(dQ=dQ, dK=dK, dV=dV)
+        g = oracle.bwd(batch.q_off, batch.kv_off, Q, K, V, dO, mode=batch.mode, causal=batch.causal, bias=b,
+                       scale=batch.scale, window=batch.window, bias_grads=bias_grads, dense_grad=False)
+        res.update(dQ=g[0], dK=g[1], dV=g[2])
+        if bias_grads:
+            res["dbias"] = g[3]
     return res
 
 
