@@ -60,7 +60,15 @@ typedef enum {
 
 typedef enum { JFA_SOFTMAX = 0, JFA_GDPA_GELU_TANH = 1, JFA_GDPA_SILU = 2 } jfa_mode;
 typedef enum { JFA_BF16 = 0, JFA_F32 = 1 } jfa_dtype;
-typedef enum { JFA_BIAS_NONE = 0, JFA_BIAS_RELPOS32 = 1 } jfa_bias_kind;
+/* JFA_BIAS_RELPOS32: a per-head table [H, 32] indexed by bucket(relative position).
+ * JFA_BIAS_DENSE: one fp32 value per (head, sequence, query row, key row), the most
+ *   general form of the article's "custom attention bias": [H, P] head-major, with
+ *   P = sum_b q_len_b * kv_len_b (jfa_plan_info fact 15).  Sequence b's block starts at
+ *   pair_off[b] = sum_{b' < b} q_len_b' * kv_len_b' within each head's row and is
+ *   row-major [q_len_b, kv_len_b]: the pair (i, j) is at h * P + pair_off[b] + i * kv_len_b
+ *   + j.  Values of masked pairs are never read.  Meant for short sequences: it moves
+ *   4 bytes per pair (and 4 more for its gradient), where the table moves none. */
+typedef enum { JFA_BIAS_NONE = 0, JFA_BIAS_RELPOS32 = 1, JFA_BIAS_DENSE = 2 } jfa_bias_kind;
 
 typedef struct jfa_plan_t* jfa_plan;
 
@@ -106,15 +114,16 @@ jfa_status jfa_plan_destroy(jfa_plan plan);
 /*
  * Plan facts for callers and tests, written to info[0..n): T_q, T_kv, B, H, D,
  * mode, causal, forward work items, forward grid, backward dK/dV work items, its
- * grid, SM count, backward dQ work items, its grid, window (-1: none).  n may be
- * smaller than 15.
+ * grid, SM count, backward dQ work items, its grid, window (-1: none), and P, the
+ * number of (query, key) pairs sum_b q_len_b * kv_len_b.  n may be smaller than 16.
  */
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
 
 /*
  * Forward pass.
  *   Q [T_q,H,D], K, V [T_kv,H,D] (dtype); bias_table fp32 [H,32] when bias_kind is
- *   JFA_BIAS_RELPOS32, else ignored; scale multiplies <q,k> (typically 1/sqrt(D)).
+ *   JFA_BIAS_RELPOS32, the dense bias fp32 [H,P] when it is JFA_BIAS_DENSE (see
+ *   jfa_bias_kind), else ignored; scale multiplies <q,k> (typically 1/sqrt(D)).
  *   O [T_q,H,D] is written for every row covered by the offsets, in o_dtype:
  *   JFA_F32 (the fp32 accumulator, no output rounding) or JFA_BF16 (rounded to
  *   nearest even); with dtype JFA_F32, o_dtype must be JFA_F32.
@@ -148,14 +157,18 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
 /*
  * jfa_bwd that also returns the gradient of the bias (the article's "custom attention
  * bias", aihot.vn GEM article, section "Jagged Sequence Flash Attention", made
- * trainable): a bias adds to the score, so its gradient is dS.  For the table of
- * JFA_BIAS_RELPOS32, entry (h, k) receives the sum of ds_ij over the allowed pairs
- * (i, j) of head h, in every sequence, whose relative position falls in bucket k:
- *   dbias[h, k] = sum_{b, i, j allowed, bucket(|i + kv_len - q_len - j|) = k} ds_ij,
+ * trainable): a bias adds to the score, so its gradient is dS,
  *   ds_ij = p_ij (dp_ij - sum_l p_il dp_il) (softmax) or act'(s_ij) dp_ij (GDPA).
- *   dbias: fp32 [H, 32] device pointer, 4-byte aligned, caller-owned; overwritten
- *     (not accumulated into).  NULL makes the call exactly jfa_bwd.  Requires
- *     bias_kind JFA_BIAS_RELPOS32 (the gradient is taken at the given table).
+ * For the table of JFA_BIAS_RELPOS32, entry (h, k) receives the sum of ds_ij over the
+ * allowed pairs (i, j) of head h, in every sequence, whose relative position falls in
+ * bucket k:
+ *   dbias[h, k] = sum_{b, i, j allowed, bucket(|i + kv_len - q_len - j|) = k} ds_ij.
+ * For JFA_BIAS_DENSE, dbias has the dense bias's layout [H, P] and receives ds_ij at
+ * every allowed pair and 0 at every masked one.
+ *   dbias: fp32 device pointer, [H, 32] or [H, P] by bias_kind, 4-byte aligned,
+ *     caller-owned; overwritten (not accumulated into).  NULL makes the call exactly
+ *     jfa_bwd.  Requires bias_kind JFA_BIAS_RELPOS32 or JFA_BIAS_DENSE (the gradient
+ *     is taken at the given bias).
  *   workspace: at least jfa_bwd_ex_workspace_size(plan, dtype, bias_kind) bytes when
  *     dbias is set (jfa_bwd_workspace_size otherwise), 256-byte aligned.
  *   The result is the same on every run: each CTA and warp sums its part in a fixed

@@ -97,8 +97,10 @@ jfa_status check_plan_call(jfa_plan plan, int dtype, int bias_kind, const float*
     if (!plan) return JFA_ERR_INVALID_ARG;
     if (dtype != JFA_BF16 && dtype != JFA_F32) return JFA_ERR_INVALID_ARG;
     if (!supported(dtype, plan->D)) return JFA_ERR_UNSUPPORTED;
-    if (bias_kind != JFA_BIAS_NONE && bias_kind != JFA_BIAS_RELPOS32) return JFA_ERR_INVALID_ARG;
+    if (bias_kind != JFA_BIAS_NONE && bias_kind != JFA_BIAS_RELPOS32 && bias_kind != JFA_BIAS_DENSE)
+        return JFA_ERR_INVALID_ARG;
     if (bias_kind == JFA_BIAS_RELPOS32 && !bias_table) return JFA_ERR_INVALID_ARG;
+    if (bias_kind == JFA_BIAS_DENSE && !bias_table && plan->n_pairs > 0) return JFA_ERR_INVALID_ARG;
     return JFA_OK;
 }
 
@@ -221,6 +223,10 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
     build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassFwd, p->fwd_grid, fi.data(), fo.data(), nullptr);
     build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassBwdKV, p->bwd_grid, bi.data(), bo.data(), nullptr);
     build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassBwdQ, p->dq_grid, qi.data(), qio.data(), nullptr);
+    std::vector<int64_t> po(size_t(B) + 1, 0);  // pair offsets of a dense bias
+    for (int32_t b = 0; b < B; ++b)
+        po[size_t(b) + 1] = po[size_t(b)] + int64_t(qo[size_t(b) + 1] - qo[size_t(b)]) * int64_t(ko[size_t(b) + 1] - ko[size_t(b)]);
+    p->n_pairs = po[size_t(B)];
 
     // One device block: offsets, status word, work lists (16-byte aligned pieces).
     const size_t off_bytes = round_up((size_t(B) + 1) * 4, 256);
@@ -234,6 +240,7 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
     const size_t o_bo = cur; cur += round_up(bo.size() * 4, 256);
     const size_t o_qi = cur; cur += round_up(qi.size() * 16, 256);
     const size_t o_qo = cur; cur += round_up(qio.size() * 4, 256);
+    const size_t o_po = cur; cur += round_up(po.size() * 8, 256);
     if (cudaMalloc(&p->dev_block, cur) != cudaSuccess) {
         delete p;
         return JFA_ERR_CUDA;
@@ -248,6 +255,7 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
     p->d_bwd_cta_off = reinterpret_cast<int32_t*>(base + o_bo);
     p->d_dq_items = reinterpret_cast<int4*>(base + o_qi);
     p->d_dq_cta_off = reinterpret_cast<int32_t*>(base + o_qo);
+    p->d_pair_off = reinterpret_cast<int64_t*>(base + o_po);
     bool ok = cudaMemcpyAsync(p->d_q_off, qo.data(), qo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
               cudaMemcpyAsync(p->d_kv_off, ko.data(), ko.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
               cudaMemsetAsync(p->d_status, 0, 256, st) == cudaSuccess &&
@@ -256,7 +264,8 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
               cudaMemcpyAsync(p->d_bwd_items, bi.data(), bi.size() * 16, cudaMemcpyHostToDevice, st) == cudaSuccess &&
               cudaMemcpyAsync(p->d_bwd_cta_off, bo.data(), bo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
               cudaMemcpyAsync(p->d_dq_items, qi.data(), qi.size() * 16, cudaMemcpyHostToDevice, st) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_dq_cta_off, qio.data(), qio.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess;
+              cudaMemcpyAsync(p->d_dq_cta_off, qio.data(), qio.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(p->d_pair_off, po.data(), po.size() * 8, cudaMemcpyHostToDevice, st) == cudaSuccess;
     // The host vectors are pageable: the copies above are staged before returning,
     // but keep the stream ordered before the vectors go out of scope.
     if (!ok || cudaStreamSynchronize(st) != cudaSuccess) {
@@ -282,10 +291,11 @@ jfa_status jfa_plan_destroy(jfa_plan plan) {
 
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
     if (!plan || !info || n < 0) return JFA_ERR_INVALID_ARG;
-    const int64_t v[15] = {plan->Tq,          plan->Tkv,      plan->B,           plan->H,        plan->D,
-                           plan->mode,        plan->causal,   plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items,
-                           plan->bwd_grid,    plan->num_sms,  plan->n_dq_items,  plan->dq_grid,  plan->window};
-    for (int32_t i = 0; i < n && i < 15; ++i) info[i] = v[i];
+    const int64_t v[16] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
+                           plan->mode,     plan->causal,  plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items,
+                           plan->bwd_grid, plan->num_sms, plan->n_dq_items,  plan->dq_grid,  plan->window,
+                           plan->n_pairs};
+    for (int32_t i = 0; i < n && i < 16; ++i) info[i] = v[i];
     return JFA_OK;
 }
 
@@ -364,6 +374,11 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
     p.O = O;
     p.lse = softmax ? lse : nullptr;
     p.status = plan->d_status;
+    if (bias_kind == JFA_BIAS_DENSE) {
+        p.dense = bias_table;
+        p.pair_off = plan->d_pair_off;
+        p.n_pairs = plan->n_pairs;
+    }
     KernelTimer tm(plan, 0, static_cast<cudaStream_t>(stream));
     cudaError_t e = dtype == JFA_BF16
                         ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, plan->fwd_grid, static_cast<cudaStream_t>(stream))
@@ -410,7 +425,8 @@ jfa_status jfa_bwd_ex(jfa_plan plan, int32_t dtype, const void* Q, const void* K
                       int32_t o_dtype, const void* dO, const float* lse, int32_t bias_kind, const float* bias_table,
                       float scale, void* dQ, void* dK, void* dV, float* dbias, void* workspace,
                       size_t workspace_bytes, void* stream) {
-    if (dbias && (bias_kind != JFA_BIAS_RELPOS32 || (reinterpret_cast<uintptr_t>(dbias) & 3u)))
+    if (dbias && ((bias_kind != JFA_BIAS_RELPOS32 && bias_kind != JFA_BIAS_DENSE) ||
+                  (reinterpret_cast<uintptr_t>(dbias) & 3u)))
         return JFA_ERR_INVALID_ARG;
     return bwd_impl(plan, dtype, Q, K, V, O, o_dtype, dO, lse, bias_kind, bias_table, scale, dQ, dK, dV, dbias,
                     workspace, workspace_bytes, stream);
@@ -435,17 +451,20 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
     const size_t need = dbias ? jfa_bwd_ex_workspace_size(plan, dtype, bias_kind) : base;
     if (workspace_bytes < need || (need > 0 && !workspace)) return JFA_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (dbias && plan->n_bwd_items == 0) {
-        // no key tile sees a query: the table gradient is zero
-        if (cudaMemsetAsync(dbias, 0, size_t(plan->H) * 32 * 4, st) != cudaSuccess) return JFA_ERR_CUDA;
-        dbias = nullptr;
+    const bool dense = bias_kind == JFA_BIAS_DENSE;
+    if (dbias && (plan->n_bwd_items == 0 || (dense && (plan->causal || plan->window >= 0)))) {
+        // The kernels write the gradient of allowed pairs only: zero it first where some
+        // pair is masked (dense), or everywhere when no key tile sees a query.
+        const size_t n = dense ? size_t(plan->H) * size_t(plan->n_pairs) : size_t(plan->H) * 32;
+        if (n > 0 && cudaMemsetAsync(dbias, 0, n * 4, st) != cudaSuccess) return JFA_ERR_CUDA;
+        if (plan->n_bwd_items == 0) dbias = nullptr;
     }
     if (plan->Tkv == 0 && plan->Tq == 0) return JFA_OK;
     const size_t rows = size_t(plan->Tq) * size_t(plan->H);
     float* delta = static_cast<float*>(workspace);
     float* dq_acc = dtype == JFA_F32 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * 4, 256))
                                      : nullptr;
-    float* dbias_part = dbias ? reinterpret_cast<float*>(static_cast<char*>(workspace) + base) : nullptr;
+    float* dbias_part = (dbias && !dense) ? reinterpret_cast<float*>(static_cast<char*>(workspace) + base) : nullptr;
 
     cudaError_t e = cudaSuccess;
     if (plan->Tq > 0) {
@@ -482,6 +501,13 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
         p.dV = dV;
         p.status = plan->d_status;
         p.dbias_part = dbias_part;
+        if (dense) {
+            p.bias = nullptr;
+            p.dense = bias_table;
+            p.ddense = dbias;
+            p.pair_off = plan->d_pair_off;
+            p.n_pairs = plan->n_pairs;
+        }
     }
     if (plan->n_bwd_items > 0) {
         KernelTimer tm(plan, 2, st);
@@ -489,7 +515,7 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
                               : launch_bwd_f32(plan->D, Q, K, V, dO, p, plan->n_bwd_items, st);
         tm.done();
         if (e != cudaSuccess) return JFA_ERR_CUDA;
-        if (dbias) {
+        if (dbias_part) {
             e = dtype == JFA_BF16
                     ? launch_dbias_reduce(dbias_part, int64_t(plan->bwd_grid) * kDkdvCompWarps, plan->H, dbias, st)
                     : launch_dbias_reduce_items(dbias_part, plan->d_bwd_items, plan->n_bwd_items, plan->H, dbias, st);

@@ -111,7 +111,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 // DBIAS: also accumulate the gradient of the relative-position bias table, the sum of
 // dS over the allowed pairs of each bucket, into per-(CTA, warp) partial tables that a
 // second kernel sums in a fixed order (so the result is the same on every run).
-template <int D, bool GDPA, bool DBIAS>
+// DENSE: the bias is the dense per-pair array p.dense, read per element; with p.ddense
+// set, dS of every allowed pair is also stored there (its gradient).
+template <int D, bool GDPA, bool DBIAS, bool DENSE>
 __global__ void __launch_bounds__(320, 1)
     jfa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -410,6 +412,9 @@ __global__ void __launch_bounds__(320, 1)
             query_tile_range(q_len, kv_len, nt, p.causal, p.window, first_qt, nq);
             const int j = nt * C::BN + r;  // key row within the sequence
             const bool key_valid = j < kv_len;
+            // dense bias / gradient of key j: element (query row i) at [i * kv_len]
+            const size_t dbase = DENSE ? size_t(h) * size_t(p.n_pairs) + size_t(p.pair_off[b]) + size_t(key_valid ? j : 0)
+                                       : 0;
             const size_t krow = (size_t(kv0) + size_t(key_valid ? j : 0)) * size_t(p.H) + size_t(h);
             __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dV) + krow * D + wg * C::kEpiCols;
             __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dK) + krow * D + wg * C::kEpiCols;
@@ -455,6 +460,8 @@ __global__ void __launch_bounds__(320, 1)
                 const bool full = __all_sync(0xffffffffu, lo == 0 && hi == NC);
                 const int rbase = qrow0 + c0 + diag - j;  // relative position of local column 0
                 const float xs = softmax ? p.scale_log2 : p.scale;
+                // dense bias of local column c: dsrc[c * kv_len] (read only for c in [lo, hi))
+                const float* dsrc = DENSE ? p.dense + dbase + size_t(qrow0 + c0) * size_t(kv_len) : nullptr;
                 // Bias per 32-column chunk: one value when every lane's chunk sits in
                 // one bucket, else read per element from the relative-position table.
                 // Lane k tests chunk k for the whole warp: over the warp's keys, chunk k
@@ -504,7 +511,7 @@ __global__ void __launch_bounds__(320, 1)
                 const float2 xs2 = make_float2(xs, xs);
                 // Fast steps (no column masked, both chunks' bias warp-constant) take a
                 // branch-free copy of the exponent loop.
-                const bool fast = full && cconst[0] && cconst[1];
+                const bool fast = !DENSE && full && cconst[0] && cconst[1];
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     uint32_t pk[16];
@@ -529,7 +536,15 @@ __global__ void __launch_bounds__(320, 1)
                         for (int c = 32 * k; c < 32 * k + 32; c += 4) {
                             const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c);
                             float2 a0 = make_float2(l4.x, l4.y), a1 = make_float2(l4.z, l4.w);
-                            if (!cconst[k]) {
+                            if constexpr (DENSE) {
+                                float bv[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    bv[e] = (c + e >= lo && c + e < hi) ? __ldg(dsrc + size_t(c + e) * size_t(kv_len)) : 0.f;
+                                const float2 l2e = make_float2(1.4426950408889634f, 1.4426950408889634f);
+                                a0 = fma2(make_float2(bv[0], bv[1]), l2e, a0);
+                                a1 = fma2(make_float2(bv[2], bv[3]), l2e, a1);
+                            } else if (!cconst[k]) {
                                 a0 = add2(a0, make_float2(rrow[c], rrow[c + 1]));
                                 a1 = add2(a1, make_float2(rrow[c + 2], rrow[c + 3]));
                             }
@@ -551,9 +566,17 @@ __global__ void __launch_bounds__(320, 1)
                         for (int c = 0; c < 32; c += 2) {
                             const int cc = 32 * k + c;
                             float a0, a1, d0, d1;
-                            gdpa_act_grad(gelu, fmaf(pv[cc], xs, cconst[k] ? cbias[k] : rrow[cc]), a0, d0);
-                            gdpa_act_grad(gelu, fmaf(pv[cc + 1], xs, cconst[k] ? cbias[k] : rrow[cc + 1]), a1, d1);
                             const bool v0 = full || (cc >= lo && cc < hi), v1 = full || (cc + 1 >= lo && cc + 1 < hi);
+                            float b0, b1;
+                            if constexpr (DENSE) {
+                                b0 = v0 ? __ldg(dsrc + size_t(cc) * size_t(kv_len)) : 0.f;
+                                b1 = v1 ? __ldg(dsrc + size_t(cc + 1) * size_t(kv_len)) : 0.f;
+                            } else {
+                                b0 = cconst[k] ? cbias[k] : rrow[cc];
+                                b1 = cconst[k] ? cbias[k] : rrow[cc + 1];
+                            }
+                            gdpa_act_grad(gelu, fmaf(pv[cc], xs, b0), a0, d0);
+                            gdpa_act_grad(gelu, fmaf(pv[cc + 1], xs, b1), a1, d1);
                             pk[c >> 1] = pack_bf16x2(v0 ? a0 : 0.f, v1 ? a1 : 0.f);
                             pv[cc] = v0 ? d0 : 0.f;
                             pv[cc + 1] = v1 ? d1 : 0.f;
@@ -590,7 +613,7 @@ __global__ void __launch_bounds__(320, 1)
                                                    add2(make_float2(dp[c + 2], dp[c + 3]), make_float2(d4.z, d4.w)));
                             pd[c >> 1] = pack_bf16x2(a.x, a.y);
                             pd[(c >> 1) + 1] = pack_bf16x2(b2.x, b2.y);
-                            if constexpr (DBIAS) {  // keep dS (fp32) for the table gradient
+                            if constexpr (DBIAS || DENSE) {  // keep dS (fp32) for a bias gradient
                                 dp[c] = a.x;
                                 dp[c + 1] = a.y;
                                 dp[c + 2] = b2.x;
@@ -603,7 +626,7 @@ __global__ void __launch_bounds__(320, 1)
                             const float2 a = mul2(make_float2(pv[32 * k + c], pv[32 * k + c + 1]),
                                                   make_float2(dp[c], dp[c + 1]));
                             pd[c >> 1] = pack_bf16x2(a.x, a.y);
-                            if constexpr (DBIAS) {
+                            if constexpr (DBIAS || DENSE) {
                                 dp[c] = a.x;
                                 dp[c + 1] = a.y;
                             }
@@ -614,6 +637,16 @@ __global__ void __launch_bounds__(320, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(KV_DS_FULL + k));
+                    if constexpr (DENSE) {
+                        // gradient of the dense bias: dS of the allowed pairs (lanes hold
+                        // consecutive keys, so each column's store is one 128-byte line)
+                        if (p.ddense) {
+                            float* gdst = p.ddense + dbase + size_t(qrow0 + c0 + 32 * k) * size_t(kv_len);
+#pragma unroll
+                            for (int c = 0; c < 32; ++c)
+                                if (32 * k + c >= lo && 32 * k + c < hi) gdst[size_t(c) * size_t(kv_len)] = dp[c];
+                        }
+                    }
                     if constexpr (DBIAS) {
                         // Table gradient of this chunk (dS is exactly 0 at masked pairs).
                         if (cconst[k]) {
@@ -769,29 +802,32 @@ __global__ void jfa_dbias_reduce_items_kernel(const float* __restrict__ part, co
     dbias[e] = acc;
 }
 
-template <int D, bool GDPA, bool DBIAS>
+template <int D, bool GDPA, bool DBIAS, bool DENSE>
 cudaError_t launch_dkdv_t_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
     using C = KvCfg<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(jfa_bwd_dkdv_kernel<D, GDPA, DBIAS>,
+        cudaError_t e = cudaFuncSetAttribute(jfa_bwd_dkdv_kernel<D, GDPA, DBIAS, DENSE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_dkdv_kernel<D, GDPA, DBIAS><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
+    jfa_bwd_dkdv_kernel<D, GDPA, DBIAS, DENSE><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_dkdv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
+    if (p.dense)
+        return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false, false, true>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                                     : launch_dkdv_t_m<D, true, false, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
     if (p.dbias_part)
-        return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false, true>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                                     : launch_dkdv_t_m<D, true, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
-    return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                                 : launch_dkdv_t_m<D, true, false>(tmQ, tmK, tmV, tmdO, p, grid, st);
+        return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false, true, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                                     : launch_dkdv_t_m<D, true, true, false>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false, false, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                                 : launch_dkdv_t_m<D, true, false, false>(tmQ, tmK, tmV, tmdO, p, grid, st);
 }
 
 template <typename TO, typename T, int D>

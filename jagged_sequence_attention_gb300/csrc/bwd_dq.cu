@@ -81,7 +81,8 @@ enum {
     DQ_DRAIN = 22,
 };
 
-template <int D, bool GDPA>
+// DENSE: the bias is the dense per-pair array p.dense, read per element.
+template <int D, bool GDPA, bool DENSE>
 __global__ void __launch_bounds__(320, 1)
     jfa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -336,6 +337,10 @@ __global__ void __launch_bounds__(320, 1)
                 __syncwarp();
             }
             const float lse_row = (softmax && row_valid) ? p.lse[orow] * 1.4426950408889634f : 0.f;
+            // dense bias of this row (read only inside its allowed columns)
+            const float* drow = DENSE ? p.dense + size_t(h) * size_t(p.n_pairs) + size_t(p.pair_off[b]) +
+                                            size_t(row_valid ? row : 0) * size_t(kv_len)
+                                      : nullptr;
             const float del_row = (softmax && row_valid) ? p.delta[orow] : 0.f;
             const float xs = softmax ? p.scale_log2 : p.scale;
             int kf, nk;  // key tiles [kf, kf + n)
@@ -379,8 +384,14 @@ __global__ void __launch_bounds__(320, 1)
                     tmem_ld_wait(rb2);
                 }
                 // softmax: pv = P = exp2(xs * s + bias - lse); GDPA: pv = act'(scale * s + bias)
-                const bool fast = full && cconst[0] && cconst[1];
-                if (softmax && fast) {
+                const bool fast = !DENSE && full && cconst[0] && cconst[1];
+                if (softmax && DENSE) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        const float bv = (c >= lo && c < lim) ? __ldg(drow + col0 + c) : 0.f;
+                        pv[c] = ex2_approx(fmaf(pv[c], xs, fmaf(bv, 1.4426950408889634f, -lse_row)));
+                    }
+                } else if (softmax && fast) {
                     // branch-free copy for steps with no masked column and warp-constant bias
                     const float2 xs2 = make_float2(xs, xs);
 #pragma unroll
@@ -417,8 +428,12 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                         for (int c = 32 * k; c < 32 * k + 32; ++c) {
                             float a, da;
-                            gdpa_act_grad(gelu, fmaf(pv[c], xs, cconst[k] ? cbias[k] : bias_w[relpos_bucket(rb - c)]),
-                                          a, da);
+                            float bv;
+                            if constexpr (DENSE)
+                                bv = (c >= lo && c < lim) ? __ldg(drow + col0 + c) : 0.f;
+                            else
+                                bv = cconst[k] ? cbias[k] : bias_w[relpos_bucket(rb - c)];
+                            gdpa_act_grad(gelu, fmaf(pv[c], xs, bv), a, da);
                             pv[c] = da;
                         }
                     }
@@ -484,26 +499,30 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == C::kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-template <int D, bool GDPA>
+template <int D, bool GDPA, bool DENSE>
 cudaError_t launch_dq_t_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
     using C = QCfg<D>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e =
-            cudaFuncSetAttribute(jfa_bwd_dq_kernel<D, GDPA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+            cudaFuncSetAttribute(jfa_bwd_dq_kernel<D, GDPA, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_dq_kernel<D, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
+    jfa_bwd_dq_kernel<D, GDPA, DENSE><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_dq_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
-    return p.mode == JFA_SOFTMAX ? launch_dq_t_m<D, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                                 : launch_dq_t_m<D, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    if (p.dense)
+        return p.mode == JFA_SOFTMAX ? launch_dq_t_m<D, false, true>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                                     : launch_dq_t_m<D, true, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    return p.mode == JFA_SOFTMAX ? launch_dq_t_m<D, false, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                                 : launch_dq_t_m<D, true, false>(tmQ, tmK, tmV, tmdO, p, grid, st);
 }
 
 }  // namespace

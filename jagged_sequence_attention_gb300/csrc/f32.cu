@@ -75,6 +75,10 @@ __global__ void __launch_bounds__(kF32Rows) jfa_fwd_f32_kernel(const float* __re
     const int kv_end = min(kv_len, (kf + n_tiles) * kFwdBN);
     const int lim = p.causal ? min(kv_len, row + diag + 1) : kv_len;  // keys [lo, lim) allowed
     const int lo = p.window >= 0 ? row + diag - p.window : 0;
+    // dense per-pair bias of this row (read only at allowed keys)
+    const float* drow = p.dense ? p.dense + size_t(h) * size_t(p.n_pairs) + size_t(p.pair_off[b]) +
+                                      size_t(valid ? row : 0) * size_t(kv_len)
+                                : nullptr;
     for (int c0 = kf * kFwdBN; c0 < kv_end; c0 += kF32Inner) {
         __syncthreads();
         for (int e = t; e < kF32Inner * D; e += kF32Rows) {
@@ -95,6 +99,7 @@ __global__ void __launch_bounds__(kF32Rows) jfa_fwd_f32_kernel(const float* __re
             float x = acc * p.scale;
             if (p.bias) x += sB[bucket_f32(row + diag - (c0 + j))];
             const bool ok = valid && (c0 + j) < lim && (c0 + j) >= lo;
+            if (drow && ok) x += __ldg(drow + c0 + j);
             s[j] = ok ? x : -INFINITY;
             mx = fmaxf(mx, s[j]);
         }
@@ -168,6 +173,8 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
     }
     int first_qt, nq;  // query tiles [first_qt, first_qt + n) see this key tile
     query_tile_range(q_len, kv_len, nt, p.causal, p.window, first_qt, nq);
+    // dense per-pair bias and its gradient of key j: element (query row i) at [i * kv_len]
+    const size_t dcol = size_t(h) * size_t(p.n_pairs) + size_t(p.pair_off ? p.pair_off[b] : 0) + size_t(kvalid ? j : 0);
     const int row_begin = first_qt * kBwdBM;
     const int row_end = min(q_len, (first_qt + n) * kBwdBM);
     const int n_keys = min(kBwdBN, kv_len - nt * kBwdBN);
@@ -201,6 +208,7 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
                 }
                 float x = acc * p.scale;
                 if (p.bias) x += sB[bucket_f32(row + diag - j)];
+                if (p.dense) x += __ldg(p.dense + dcol + size_t(row) * size_t(kv_len));
                 float pij;
                 if (softmax) {
                     pij = expf(x - sL[i]);
@@ -209,6 +217,7 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
                     pij = act_f32(p.mode, x);
                     ds = act_grad_f32(p.mode, x) * dp;
                 }
+                if (p.ddense) p.ddense[dcol + size_t(row) * size_t(kv_len)] = ds;
 #pragma unroll
                 for (int d = 0; d < D; ++d) {
                     dv[d] = fmaf(pij, sdO[i][d], dv[d]);

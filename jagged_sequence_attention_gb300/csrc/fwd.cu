@@ -107,9 +107,10 @@ __device__ __forceinline__ void store_row<float>(float* dst, const float* v, int
     for (int i = 0; i < n / 4; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-// WIN: a sliding window is set (p.window >= 0).  Without it the window arithmetic folds
-// away at compile time, so the plain causal and non-causal paths carry none of it.
-template <int D, typename OT, bool GDPA, bool WIN>
+// WIN: a sliding window may be set (p.window >= 0).  Without it the window arithmetic
+// folds away at compile time, so the plain causal and non-causal paths carry none of it.
+// DENSE: the bias is the dense per-pair array p.dense (read per element, both passes).
+template <int D, typename OT, bool GDPA, bool WIN, bool DENSE>
 __global__ void __launch_bounds__(320, 1)
     jfa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -351,6 +352,11 @@ __global__ void __launch_bounds__(320, 1)
             const int row = tile * C::BM + t;
             const bool row_valid = row < q_len;
             const int diag = kv_len - q_len;
+            // dense bias of this row (row-major [q_len, kv_len] block of head h, sequence b)
+            const float* drow = nullptr;
+            if constexpr (DENSE)
+                drow = p.dense + size_t(h) * size_t(p.n_pairs) + size_t(p.pair_off[b]) +
+                       size_t(row_valid ? row : 0) * size_t(kv_len);
             // Each warp keeps its own copy of the head's bias row (log2 units for
             // softmax) and its maximum, so no cross-warp barrier is needed.
             float* btab = bias_s + warp * (C::kBiasRow + C::kBiasTab);
@@ -386,8 +392,9 @@ __global__ void __launch_bounds__(320, 1)
                 const int col0 = (kf + j) * C::BN;
                 int lim = kv_len - col0;  // subtraction scheme: columns >= lim are masked
                 if (p.causal) lim = min(lim, row + diag + 1 - col0);
+                if (DENSE && !row_valid) lim = 0;  // never read a dense bias past the sequence
                 // sliding window: columns below row + diag - W are masked
-                const int lo = WIN ? row + diag - window - col0 : 0;
+                const int lo = (WIN && (!DENSE || window >= 0)) ? row + diag - window - col0 : 0;
                 const int rbase = row + diag - col0;  // relative position of column 0
                 const bool full = __all_sync(0xffffffffu, lim >= C::BN && lo <= 0);
                 const float xs = softmax ? p.scale_log2 : p.scale;
@@ -421,6 +428,19 @@ __global__ void __launch_bounds__(320, 1)
                 const float* rrow = rtab + lane + (C::BN - 1);  // rrow[-c] = bias of column c
                 // Scaled, biased and masked scores of chunk k, minus `shift`.
                 auto chunk_x = [&](const uint32_t (&r)[32], int k, float shift, float (&v)[32]) {
+                    if constexpr (DENSE) {
+                        // per-element bias, read only inside the row's allowed columns
+                        const float bs = softmax ? 1.4426950408889634f : 1.0f;
+                        const int lk = lim - 32 * k, lok = lo - 32 * k;
+                        const float* src = drow + col0 + 32 * k;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const bool in = i >= lok && i < lk;
+                            const float bv = in ? __ldg(src + i) : 0.f;
+                            v[i] = in ? fmaf(__uint_as_float(r[i]), xs, fmaf(bv, bs, -shift)) : -INFINITY;
+                        }
+                        return;
+                    }
                     if (cmask & (1u << k)) {
                         const float2 sc = make_float2(xs, xs), add = make_float2(cb[k] - shift, cb[k] - shift);
 #pragma unroll
@@ -452,7 +472,7 @@ __global__ void __launch_bounds__(320, 1)
                     // head's largest).  Any m >= the true max gives the same P / l.
                     // Fast tiles (no column masked, every chunk's bias one value) take a
                     // branch-free copy of both passes; the rest take the general one.
-                    const bool fast = full && cmask == (1u << (C::BN / 32)) - 1;
+                    const bool fast = !DENSE && full && cmask == (1u << (C::BN / 32)) - 1;
                     float mx = -INFINITY;
                     tmem_ld32(tS, ra);
                     tmem_ld_wait(ra);
@@ -476,7 +496,14 @@ __global__ void __launch_bounds__(320, 1)
                         uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
                         if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
                         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                        if (full) {
+                        if (DENSE) {
+                            // no cheap bound on a dense bias: the exact max of x
+                            float v[32];
+                            chunk_x(cur, k, 0.f, v);
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], v[i], v[i + 1]);
+                            mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                        } else if (full) {
 #pragma unroll
                             for (int i = 0; i < 32; i += 2)
                                 m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
@@ -486,8 +513,10 @@ __global__ void __launch_bounds__(320, 1)
                             for (int i = 0; i < 32; ++i)
                                 m4[i & 3] = fmaxf(m4[i & 3], (i >= lok && i < lk) ? __uint_as_float(cur[i]) : -INFINITY);
                         }
-                        const float mk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                        mx = fmaxf(mx, fmaf(mk, xs, (cmask & (1u << k)) ? cb[k] : bmax));
+                        if (!DENSE) {
+                            const float mk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                            mx = fmaxf(mx, fmaf(mk, xs, (cmask & (1u << k)) ? cb[k] : bmax));
+                        }
                         if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
                     }
                     }
@@ -628,29 +657,32 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int D, typename OT, bool GDPA, bool WIN>
+template <int D, typename OT, bool GDPA, bool WIN, bool DENSE>
 static cudaError_t launch_fwd_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const FwdParams& p, int grid, cudaStream_t st) {
     using C = FwdCfg<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, OT, GDPA, WIN>,
+        cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, OT, GDPA, WIN, DENSE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_fwd_kernel<D, OT, GDPA, WIN><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, p);
+    jfa_fwd_kernel<D, OT, GDPA, WIN, DENSE><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
 }
 
 template <int D, typename OT>
 static cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const FwdParams& p, int grid, cudaStream_t st) {
+    if (p.dense)  // dense bias: the window, if any, is taken at run time
+        return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false, true, true>(tmQ, tmK, tmV, p, grid, st)
+                                     : launch_fwd_m<D, OT, true, true, true>(tmQ, tmK, tmV, p, grid, st);
     if (p.window >= 0)
-        return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false, true>(tmQ, tmK, tmV, p, grid, st)
-                                     : launch_fwd_m<D, OT, true, true>(tmQ, tmK, tmV, p, grid, st);
-    return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false, false>(tmQ, tmK, tmV, p, grid, st)
-                                 : launch_fwd_m<D, OT, true, false>(tmQ, tmK, tmV, p, grid, st);
+        return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false, true, false>(tmQ, tmK, tmV, p, grid, st)
+                                     : launch_fwd_m<D, OT, true, true, false>(tmQ, tmK, tmV, p, grid, st);
+    return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false, false, false>(tmQ, tmK, tmV, p, grid, st)
+                                 : launch_fwd_m<D, OT, true, false, false>(tmQ, tmK, tmV, p, grid, st);
 }
 
 cudaError_t launch_fwd(int dtype, int o_dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,

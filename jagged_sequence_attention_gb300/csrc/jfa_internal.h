@@ -134,6 +134,11 @@ struct FwdParams {
     void* O;
     float* lse;         // [T_q,H] or nullptr (GDPA)
     int* status;
+    // Dense per-pair bias [H, n_pairs] (sequence b's block row-major [q_len, kv_len] from
+    // pair_off[b]), or nullptr.
+    const float* dense = nullptr;
+    const int64_t* pair_off = nullptr;
+    int64_t n_pairs = 0;
 };
 
 struct BwdParams {
@@ -158,6 +163,12 @@ struct BwdParams {
     // Partial gradients of the relative-position bias table, or nullptr: bf16 inputs
     // [grid][compute warps][H][32], fp32 inputs [work item][32].
     float* dbias_part = nullptr;
+    // Dense per-pair bias and its gradient [H, n_pairs] (either may be nullptr), as in
+    // FwdParams.
+    const float* dense = nullptr;
+    float* ddense = nullptr;
+    const int64_t* pair_off = nullptr;
+    int64_t n_pairs = 0;
 };
 
 // Host planner (plan.cpp).  Returns JFA_OK or an error for bad offsets.
@@ -217,6 +228,8 @@ struct jfa_plan_t {
     int32_t* d_bwd_cta_off;
     int4* d_dq_items;
     int32_t* d_dq_cta_off;
+    int64_t* d_pair_off;  // [B+1] first (query, key) pair of each sequence, for a dense bias
+    int64_t n_pairs;      // sum over sequences of q_len * kv_len
     int64_t n_fwd_items, n_bwd_items, n_dq_items;
     int fwd_grid, bwd_grid, dq_grid;
     // optional per-kernel timing (jfa_plan_set_timing)

@@ -23,7 +23,7 @@ JFA_ERR_SCRATCH_LIMIT = 8
 JFA_STATIC_SCRATCH_BYTES = 64 << 20
 JFA_SOFTMAX, JFA_GDPA_GELU_TANH, JFA_GDPA_SILU = 0, 1, 2
 JFA_BF16, JFA_F32 = 0, 1
-JFA_BIAS_NONE, JFA_BIAS_RELPOS32 = 0, 1
+JFA_BIAS_NONE, JFA_BIAS_RELPOS32, JFA_BIAS_DENSE = 0, 1, 2
 
 MODES = {"softmax": JFA_SOFTMAX, "gelu_tanh": JFA_GDPA_GELU_TANH, "silu": JFA_GDPA_SILU}
 DTYPES = {torch.bfloat16: JFA_BF16, torch.float32: JFA_F32}
@@ -31,7 +31,7 @@ DTYPES = {torch.bfloat16: JFA_BF16, torch.float32: JFA_F32}
 EXPORTED = ["jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd_workspace_size",
             "jfa_bwd", "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build",
             "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times", "jfa_bwd_static_scratch",
-            "jfa_partition_sequences"]
+            "jfa_partition_sequences", "jfa_bwd_ex_workspace_size", "jfa_bwd_ex"]
 
 
 class JFAError(RuntimeError):
@@ -74,7 +74,7 @@ def lib():
         L.jfa_status_string.restype = ctypes.c_char_p
         for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
                      "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build", "jfa_plan_set_timing",
-                     "jfa_plan_kernel_times", "jfa_bwd_static_scratch", "jfa_partition_sequences"):
+                     "jfa_plan_kernel_times", "jfa_bwd_static_scratch", "jfa_partition_sequences", "jfa_bwd_ex"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -90,7 +90,13 @@ def _check(fn: str, status: int):
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """The tensor's data pointer.  The library reads and writes dense row-major arrays,
+    so a tensor with any other strides is refused rather than misread."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise JFAError("tensor layout (must be contiguous)", JFA_ERR_INVALID_ARG)
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream=None):
@@ -162,7 +168,7 @@ def jfa_plan_destroy(plan: Plan):
 
 
 INFO_KEYS = ["T_q", "T_kv", "B", "H", "D", "mode", "causal", "fwd_items", "fwd_grid", "bwd_items", "bwd_grid",
-             "num_sms", "dq_items", "dq_grid", "window"]
+             "num_sms", "dq_items", "dq_grid", "window", "pairs"]
 
 
 def jfa_plan_info(plan: Plan) -> dict:
@@ -177,22 +183,29 @@ def _dtype_code(t: torch.Tensor) -> int:
     return DTYPES[t.dtype]
 
 
-def _bias_args(bias):
+def _bias_args(bias, dense=None):
+    """(kind, pointer): the bucket table [H, 32], or a dense per-pair bias [H, P]."""
+    if dense is not None:
+        if bias is not None:
+            raise JFAError("bias", JFA_ERR_INVALID_ARG)
+        return JFA_BIAS_DENSE, _ptr(dense)
     if bias is None:
         return JFA_BIAS_NONE, None
     return JFA_BIAS_RELPOS32, _ptr(bias)
 
 
-def jfa_fwd(plan: Plan, Q, K, V, bias=None, scale=None, O=None, lse=None, stream=None, out_dtype=None):
+def jfa_fwd(plan: Plan, Q, K, V, bias=None, scale=None, O=None, lse=None, stream=None, out_dtype=None,
+            dense_bias=None):
     """Returns (O, lse); lse is None in GDPA modes.  O is written in out_dtype (default:
-    O's dtype if given, else Q's)."""
+    O's dtype if given, else Q's).  bias: the bucket table [H, 32]; dense_bias: a dense
+    per-pair bias [H, P] instead."""
     dt = _dtype_code(Q)
     scale = 1.0 / float(plan.D) ** 0.5 if scale is None else float(scale)
     if O is None:
         O = torch.empty(Q.shape, dtype=out_dtype or Q.dtype, device=Q.device)
     if lse is None and plan.mode == JFA_SOFTMAX:
         lse = torch.empty((Q.shape[0], plan.H), dtype=torch.float32, device=Q.device)
-    bk, bp = _bias_args(bias)
+    bk, bp = _bias_args(bias, dense_bias)
     _check("jfa_fwd", lib().jfa_fwd(plan.handle, dt, _ptr(Q), _ptr(K), _ptr(V), bk, bp, scale, _ptr(O),
                                     _dtype_code(O), _ptr(lse), _stream(stream)))
     return O, lse
@@ -203,7 +216,7 @@ def jfa_bwd_workspace_size(plan: Plan, dtype=torch.bfloat16) -> int:
 
 
 def jfa_bwd(plan: Plan, Q, K, V, O, dO, lse, bias=None, scale=None, dQ=None, dK=None, dV=None, workspace=None,
-            stream=None):
+            stream=None, dense_bias=None):
     """Returns (dQ, dK, dV)."""
     dt = _dtype_code(Q)
     scale = 1.0 / float(plan.D) ** 0.5 if scale is None else float(scale)
@@ -213,33 +226,34 @@ def jfa_bwd(plan: Plan, Q, K, V, O, dO, lse, bias=None, scale=None, dQ=None, dK=
     need = jfa_bwd_workspace_size(plan, Q.dtype)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
-    bk, bp = _bias_args(bias)
+    bk, bp = _bias_args(bias, dense_bias)
     _check("jfa_bwd", lib().jfa_bwd(plan.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _dtype_code(O), _ptr(dO),
                                     _ptr(lse), bk, bp, scale, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)))
     return dQ, dK, dV
 
 
-def jfa_bwd_ex_workspace_size(plan: Plan, dtype=torch.bfloat16, bias_grad=True) -> int:
-    return int(lib().jfa_bwd_ex_workspace_size(plan.handle, DTYPES[dtype],
-                                               JFA_BIAS_RELPOS32 if bias_grad else JFA_BIAS_NONE))
+def jfa_bwd_ex_workspace_size(plan: Plan, dtype=torch.bfloat16, bias_grad=True, dense=False) -> int:
+    kind = (JFA_BIAS_DENSE if dense else JFA_BIAS_RELPOS32) if bias_grad else JFA_BIAS_NONE
+    return int(lib().jfa_bwd_ex_workspace_size(plan.handle, DTYPES[dtype], kind))
 
 
 def jfa_bwd_ex(plan: Plan, Q, K, V, O, dO, lse, bias, scale=None, dQ=None, dK=None, dV=None, dbias=None,
-               workspace=None, stream=None):
-    """jfa_bwd plus the gradient of the relative-position bias table [H, 32] (fp32).
-    Returns (dQ, dK, dV, dbias)."""
+               workspace=None, stream=None, dense_bias=None):
+    """jfa_bwd plus the gradient of the bias: of the bucket table [H, 32], or with
+    dense_bias of the dense per-pair bias [H, P] (fp32).  Returns (dQ, dK, dV, dbias)."""
     dt = _dtype_code(Q)
     scale = 1.0 / float(plan.D) ** 0.5 if scale is None else float(scale)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
     if dbias is None:
-        dbias = torch.empty((plan.H, 32), dtype=torch.float32, device=Q.device)
-    need = jfa_bwd_ex_workspace_size(plan, Q.dtype)
+        shape = (plan.H, 32) if dense_bias is None else tuple(dense_bias.shape)
+        dbias = torch.empty(shape, dtype=torch.float32, device=Q.device)
+    need = jfa_bwd_ex_workspace_size(plan, Q.dtype, dense=dense_bias is not None)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
-    bk, bp = _bias_args(bias)
+    bk, bp = _bias_args(bias, dense_bias)
     _check("jfa_bwd_ex", lib().jfa_bwd_ex(plan.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _dtype_code(O),
                                           _ptr(dO), _ptr(lse), bk, bp, scale, _ptr(dQ), _ptr(dK), _ptr(dV),
                                           _ptr(dbias), _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -340,14 +354,16 @@ def attention(batch, with_backward=True, stream=None, out_dtype=None, bias_grad=
     (with bias_grad, also "dbias", the gradient of the batch's bias table)."""
     plan = jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal, stream,
                            window=getattr(batch, "window", None))
-    O, lse = jfa_fwd(plan, batch.Q, batch.K, batch.V, batch.bias, batch.scale, stream=stream, out_dtype=out_dtype)
+    dense = getattr(batch, "dense", None)
+    O, lse = jfa_fwd(plan, batch.Q, batch.K, batch.V, batch.bias, batch.scale, stream=stream, out_dtype=out_dtype,
+                     dense_bias=dense)
     out = {"O": O, "lse": lse, "plan": plan}
     if with_backward and bias_grad:
         dQ, dK, dV, dbias = jfa_bwd_ex(plan, batch.Q, batch.K, batch.V, O, batch.dO, lse, batch.bias, batch.scale,
-                                       stream=stream)
+                                       stream=stream, dense_bias=dense)
         out.update(dQ=dQ, dK=dK, dV=dV, dbias=dbias)
     elif with_backward:
         dQ, dK, dV = jfa_bwd(plan, batch.Q, batch.K, batch.V, O, batch.dO, lse, batch.bias, batch.scale,
-                             stream=stream)
+                             stream=stream, dense_bias=dense)
         out.update(dQ=dQ, dK=dK, dV=dV)
     return out

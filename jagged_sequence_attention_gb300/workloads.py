@@ -147,6 +147,9 @@ class Batch:
     D: int
     extra: dict = field(default_factory=dict)
     window: Optional[int] = None   # sliding window W (query i sees keys i' - W .. i'), or None
+    # dense per-pair bias fp32 [H, P], P = sum q_len * kv_len, sequence b's block row-major
+    # [q_len, kv_len] from pair_offsets()[b] (used instead of the bucket table), or None
+    dense: Optional[torch.Tensor] = None
 
     @property
     def B(self) -> int:
@@ -168,9 +171,16 @@ def _values(shape, std, dtype, gen, device):
     return x.to(dtype)
 
 
+def pair_offsets(q_off, kv_off) -> np.ndarray:
+    """int64 [B+1]: where each sequence's block of a dense per-pair array starts."""
+    q = np.diff(np.asarray(q_off, dtype=np.int64))
+    kv = np.diff(np.asarray(kv_off, dtype=np.int64))
+    return np.concatenate([[0], np.cumsum(q * kv)]).astype(np.int64)
+
+
 def make_custom(q_lens, kv_lens, *, H, D, dtype=torch.bfloat16, mode="softmax", causal=False,
                 bias=False, value_std=1.0, seed=BASE_SEED, device="cpu", with_grad=True,
-                name="custom", pad_rows=0, window=None) -> Batch:
+                name="custom", pad_rows=0, window=None, dense_bias=False) -> Batch:
     """A batch with the given lengths.  ``pad_rows`` extra rows are appended to every
     value tensor (beyond the last offset) so tests can check that nothing there is read
     into a result or written."""
@@ -184,7 +194,12 @@ def make_custom(q_lens, kv_lens, *, H, D, dtype=torch.bfloat16, mode="softmax", 
     b = None
     if bias:
         b = (torch.randn((H, 32), generator=gen, device=device, dtype=torch.float32) * 0.1)
-    return Batch(name, q_off, kv_off, Q, K, V, dO, b, 1.0 / math.sqrt(D), mode, causal, H, D, window=window)
+    dn = None
+    if dense_bias:  # N(0, 0.5) per pair
+        P = int(pair_offsets(q_off, kv_off)[-1])
+        dn = torch.randn((H, P), generator=gen, device=device, dtype=torch.float32) * 0.5
+    return Batch(name, q_off, kv_off, Q, K, V, dO, b, 1.0 / math.sqrt(D), mode, causal, H, D, window=window,
+                 dense=dn)
 
 
 def make(name: str, device="cpu", with_grad=True, seed: Optional[int] = None) -> Batch:
@@ -214,9 +229,15 @@ def subset(batch: Batch, seqs, heads=None) -> Batch:
         idx = idx.to(t.device)
         return t.index_select(0, idx).index_select(1, hs.to(t.device)).contiguous()
 
+    dn = None
+    if batch.dense is not None:
+        po = pair_offsets(batch.q_off, batch.kv_off)
+        blocks = [batch.dense[:, int(po[s]):int(po[s + 1])] for s in seqs]
+        dn = torch.cat(blocks, dim=1) if blocks else batch.dense[:, :0]
+        dn = dn[hs.to(dn.device)].contiguous()
     sub = Batch(batch.name + "/subset", offsets(batch.q_lens[seqs]), offsets(batch.kv_lens[seqs]),
                 take(batch.Q, qi), take(batch.K, ki), take(batch.V, ki), take(batch.dO, qi),
                 None if batch.bias is None else batch.bias[hs.to(batch.bias.device)].contiguous(),
-                batch.scale, batch.mode, batch.causal, len(heads), batch.D, window=batch.window)
+                batch.scale, batch.mode, batch.causal, len(heads), batch.D, window=batch.window, dense=dn)
     sub.extra.update(seqs=seqs, heads=heads, q_index=qi, kv_index=ki)
     return sub

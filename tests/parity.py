@@ -56,16 +56,18 @@ def run_oracle(batch, with_backward=True, bias_grads=False):
     Q, K, V = np64(batch.Q), np64(batch.K), np64(batch.V)
     Tq, Tkv = int(batch.q_off[-1]), int(batch.kv_off[-1])
     Q, K, V = Q[:Tq], K[:Tkv], V[:Tkv]
+    dn = None if getattr(batch, "dense", None) is None else np64(batch.dense)
     O, LSE = oracle.fwd(batch.q_off, batch.kv_off, Q, K, V, mode=batch.mode, causal=batch.causal,
-                        bias=b, scale=batch.scale, window=batch.window)
+                        bias=b, scale=batch.scale, window=batch.window, dense_bias=dn)
     res = {"O": O, "lse": LSE}
     if with_backward:
         dO = np64(batch.dO)[:Tq]
         g = oracle.bwd(batch.q_off, batch.kv_off, Q, K, V, dO, mode=batch.mode, causal=batch.causal, bias=b,
-                       scale=batch.scale, window=batch.window, bias_grads=bias_grads, dense_grad=False)
+                       scale=batch.scale, window=batch.window, bias_grads=bias_grads, dense_grad=dn is not None,
+                       dense_bias=dn)
         res.update(dQ=g[0], dK=g[1], dV=g[2])
         if bias_grads:
-            res["dbias"] = g[3]
+            res["dbias"] = g[3] if dn is None else g[4]
     return res
 
 

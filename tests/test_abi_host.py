@@ -205,3 +205,15 @@ def test_worklist_is_deterministic(jfa):
     b = jfa.jfa_worklist_build(qo, ko, 8, False, 0, 148)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def test_binding_refuses_non_contiguous_tensors():
+    # the library takes dense row-major arrays; a strided view would be misread
+    import torch
+    from jagged_sequence_attention_gb300 import jfa
+    t = torch.zeros(4, 6)
+    assert jfa._ptr(t) is not None
+    with pytest.raises(jfa.JFAError) as e:
+        jfa._ptr(t.t())
+    assert e.value.status == jfa.JFA_ERR_INVALID_ARG
+    assert jfa._ptr(None) is None
