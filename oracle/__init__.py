@@ -187,3 +187,47 @@ def bwd(q_off, kv_off, Q, K, V, dO, *, mode="softmax", causal=False, bias=None, 
     if bias_grads:
         return dQ, dK, dV, dbias, d_dense
     return dQ, dK, dV
+
+
+# --------------------------------------------------------------------------- shared key/value
+# In-kernel broadcast (IKBO, PyTorch blog "In-Kernel Broadcast Optimization: Co-Designing
+# Kernels for RecSys Inference", section 3 "IKBO Flash Attention" and figure 1): many
+# candidate query sets of one request attend to the same user's key/value history.  The
+# operation is exactly attention over the broadcast (copied) history; the kernel only avoids
+# materialising the copies.  So the oracle is that definition: gather each query set's user
+# rows, attend as above, and (backward of a broadcast) sum the key/value gradients of all
+# query sets that share a user.
+
+
+def _broadcast(kv_off_users, kv_index, K, V):
+    """Per query set b, the rows of user kv_index[b]: (kv_off of the copies, row index)."""
+    kv_off_users = np.asarray(kv_off_users, dtype=np.int64)
+    kv_index = np.asarray(kv_index, dtype=np.int64)
+    lens = kv_off_users[kv_index + 1] - kv_off_users[kv_index]
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    rows = np.concatenate([np.arange(kv_off_users[u], kv_off_users[u + 1]) for u in kv_index]
+                          + [np.zeros(0, dtype=np.int64)]).astype(np.int64)
+    return off, rows
+
+
+def shared_kv_fwd(q_off, kv_off_users, kv_index, Q, K, V, **kw):
+    """Forward with query set b attending to user kv_index[b]'s rows kv_off_users[u] ..
+    kv_off_users[u+1] of K and V.  Same keywords and results as fwd (the dense bias, if
+    any, is laid out over the pairs of the query sets with their users' lengths)."""
+    off, rows = _broadcast(kv_off_users, kv_index, K, V)
+    K, V = _f64(K), _f64(V)
+    return fwd(q_off, off, Q, K[rows], V[rows], **kw)
+
+
+def shared_kv_bwd(q_off, kv_off_users, kv_index, Q, K, V, dO, **kw):
+    """Backward of shared_kv_fwd: (dQ, dK, dV[, bias gradients]) with dK, dV over the
+    users' rows, each the sum over the query sets that share the user."""
+    off, rows = _broadcast(kv_off_users, kv_index, K, V)
+    K, V = _f64(K), _f64(V)
+    res = bwd(q_off, off, Q, K[rows], V[rows], dO, **kw)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    np.add.at(dK, rows, res[1])
+    np.add.at(dV, rows, res[2])
+    return (res[0], dK, dV) + tuple(res[3:])
+
