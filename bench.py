@@ -229,6 +229,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--broadcast", action="store_true",
+                    help="shared key/value workloads: run the plain path on an explicit broadcast copy of each "
+                         "query set's user rows (the copies the in-kernel broadcast avoids; copy not timed)")
     ap.add_argument("--partition", action="store_true",
                     help="strong scaling: one batch, its sequences split across the ranks by the LPT partition "
                          "(default: weak scaling, each rank its own batch of the workload)")
@@ -250,6 +253,7 @@ def main():
     w = wl.WORKLOADS[args.workload]
     cfg = {"workload": args.workload, "description": w.description, "B": w.B, "H": w.H, "D": w.D,
            "mode": w.mode, "causal": w.causal, "bias": w.bias, "window": w.window, "seed": wl.seed_of(w),
+           "users": w.users, "broadcast": bool(args.broadcast and w.users),
            "l2": "inputs larger than L2 (no flush needed)",
            "parallelism": f"dp{world} (" + ("LPT partition of one batch" if args.partition else "independent batches") + ")"}
 
@@ -258,7 +262,7 @@ def main():
             if dist:
                 dist.barrier()
             return
-        batch = wl.make(args.workload, device="cpu")
+        batch = wl.broadcast(wl.make(args.workload, device="cpu"))
         cpu, seqs = oracle_sample(batch, args.cpu_seconds)
         fl_f, fl_b = flops_of(cpu)
         for _ in range(args.warmup if args.steps > 1 else 0):
@@ -290,6 +294,8 @@ def main():
         batch = jfa.shard(wl.make(args.workload, device=dev), rank, world)
     else:
         batch = wl.make(args.workload, device=dev, seed=wl.seed_of(w) + 7919 * rank)
+    if args.broadcast:
+        batch = wl.broadcast(batch)
     fl_f, fl_b = flops_of(batch)
     job_flop = fl_f + fl_b  # summed over ranks below: the work all ranks processed
     kbytes = algorithmic_bytes(batch)
@@ -297,8 +303,7 @@ def main():
                 "unpadded_fwd_flop": fl_f, "unpadded_bwd_flop": fl_b})
 
     stream = torch.cuda.current_stream()
-    plan = jfa.jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal,
-                               window=batch.window)
+    plan = jfa.plan_for(batch)
     O = torch.empty_like(batch.Q)
     lse = torch.empty((batch.Q.shape[0], batch.H), dtype=torch.float32, device=dev)
     dQ, dK, dV = torch.empty_like(batch.Q), torch.empty_like(batch.K), torch.empty_like(batch.V)
@@ -405,7 +410,8 @@ def main():
             dOd.copy_(hdO, non_blocking=True)
             if hbias is not None:
                 bias_d.copy_(hbias, non_blocking=True)
-            p2 = jfa.jfa_plan_create(q_off, kv_off, batch.H, batch.D, batch.mode, batch.causal, window=batch.window)
+            p2 = jfa.plan_for(wl.Batch(batch.name, q_off, kv_off, dQd, dKd, dVd, dOd, bias_d, batch.scale, batch.mode,
+                                       batch.causal, batch.H, batch.D, window=batch.window, kv_map=batch.kv_map))
             jfa.jfa_fwd(p2, dQd, dKd, dVd, bias_d, batch.scale, O=O, lse=lse)
             jfa.jfa_bwd(p2, dQd, dKd, dVd, O, dOd, lse, bias_d, batch.scale, dQ=dQ, dK=dK, dV=dV, workspace=ws)
             hO.copy_(O, non_blocking=True)
@@ -434,7 +440,7 @@ def main():
 
     # ---------------------------------------------------------------- CPU baseline (oracle)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu, seqs = oracle_sample(batch, args.cpu_seconds)
+        cpu, seqs = oracle_sample(wl.broadcast(batch), args.cpu_seconds)
         cf, cb = flops_of(cpu)
         run_oracle_once(wl.subset(cpu, [0], [0]))
         t = run_oracle_once(cpu)

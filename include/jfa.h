@@ -107,6 +107,37 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
                               int32_t H, int32_t D, int32_t mode, int32_t causal, int32_t window,
                               int32_t offsets_on_device, void* stream, jfa_plan* out);
 
+/*
+ * Shared key/value attention: the in-kernel broadcast (IKBO) of the PyTorch blog
+ * "In-Kernel Broadcast Optimization: Co-Designing Kernels for RecSys Inference",
+ * section 3 "IKBO Flash Attention" and figure 1.  Many candidate query sets of a
+ * request attend to the same user history, and the kernels read each user's keys and
+ * values once per use instead of from a copy made per query set.
+ *   Query set b (rows q_offsets[b] .. q_offsets[b+1] of Q, O, dO, dQ) attends to the
+ *   rows of user u = kv_index[b], kv_offsets[u] .. kv_offsets[u+1] of K and V.  The
+ *   results are those of jfa_fwd / jfa_bwd on the broadcast batch, with each query set
+ *   holding its own copy of its user's rows.  dK and dV of a user's rows sum over all
+ *   of its query sets, and are zero for a user that no query set uses.
+ *   kv_offsets: int32[U+1] over the users (T_kv = kv_offsets[U]); kv_index: int32[B],
+ *   each in [0, U).  Host arrays, or device arrays with offsets_on_device (copied to the
+ *   host on `stream`, which this call synchronises).
+ *   Causal alignment, the sliding window and the bias use each query set's q_len and
+ *   its user's kv_len, as in jfa_plan_create_ex.  A dense bias (JFA_BIAS_DENSE) has one
+ *   block per query set, q_len_b x kv_len_{kv_index[b]}.
+ *   Planning: the forward and dQ passes work per query set, reading its user's rows.
+ *   The dK/dV pass works per user key tile over the query tiles of all of that user's
+ *   query sets, so dK and dV accumulate on chip and each user row is written once.
+ *   jfa_plan_info fact 16 is U.
+ *   The other calls take the plan as usual.  jfa_worklist_* and
+ *   jfa_partition_sequences describe plain batches only.
+ * Errors: INVALID_ARG for bad offsets or an index outside [0, U); otherwise those of
+ * jfa_plan_create_ex.
+ */
+jfa_status jfa_plan_create_shared_kv(const int32_t* q_offsets, int32_t B, const int32_t* kv_offsets,
+                                     int32_t U, const int32_t* kv_index, int32_t H, int32_t D,
+                                     int32_t mode, int32_t causal, int32_t window,
+                                     int32_t offsets_on_device, void* stream, jfa_plan* out);
+
 /* Frees a plan and its device memory (cudaFree synchronises the device, so launches
  * still using the plan finish first).  NULL is accepted. */
 jfa_status jfa_plan_destroy(jfa_plan plan);
@@ -114,8 +145,9 @@ jfa_status jfa_plan_destroy(jfa_plan plan);
 /*
  * Plan facts for callers and tests, written to info[0..n): T_q, T_kv, B, H, D,
  * mode, causal, forward work items, forward grid, backward dK/dV work items, its
- * grid, SM count, backward dQ work items, its grid, window (-1: none), and P, the
- * number of (query, key) pairs sum_b q_len_b * kv_len_b.  n may be smaller than 16.
+ * grid, SM count, backward dQ work items, its grid, window (-1: none), P, the number
+ * of (query, key) pairs sum_b q_len_b * kv_len_b, and the number of users U of a
+ * shared key/value plan (-1 for other plans).  n may be smaller than 17.
  */
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
 

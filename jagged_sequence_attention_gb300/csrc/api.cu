@@ -163,56 +163,50 @@ jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, 
     return jfa_plan_create_ex(q_offsets, kv_offsets, B, H, D, mode, causal, -1, offsets_on_device, stream, out);
 }
 
-jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H, int32_t D,
-                              int32_t mode, int32_t causal, int32_t window, int32_t offsets_on_device, void* stream,
-                              jfa_plan* out) {
-    if (!out) return JFA_ERR_INVALID_ARG;
-    *out = nullptr;
-    if (!q_offsets || !kv_offsets || B < 0 || H < 1 || H > 65535) return JFA_ERR_INVALID_ARG;
-    if (mode != JFA_SOFTMAX && mode != JFA_GDPA_GELU_TANH && mode != JFA_GDPA_SILU) return JFA_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return JFA_ERR_INVALID_ARG;
-    if (window < -1 || (window >= 0 && causal != 1)) return JFA_ERR_INVALID_ARG;
-    if (D != 32 && D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-
+// Builds a plan from host offsets.  kv_map (length B) is the query-set-to-user map of
+// shared key/value attention, with U users in kv_off; without it U == B and sequence b
+// attends to its own rows.
+static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::vector<int32_t>& ko,
+                                   const std::vector<int32_t>* kv_map, int32_t B, int32_t U, int32_t H, int32_t D,
+                                   int32_t mode, int32_t causal, int32_t window, cudaStream_t st, jfa_plan* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_NO_DEVICE;
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return JFA_ERR_NO_DEVICE;
     if (prop.major != 10) return JFA_ERR_NO_DEVICE;
 
-    std::vector<int32_t> qo(size_t(B) + 1), ko(size_t(B) + 1);
-    if (offsets_on_device) {
-        if (cudaMemcpyAsync(qo.data(), q_offsets, qo.size() * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-            cudaMemcpyAsync(ko.data(), kv_offsets, ko.size() * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-            cudaStreamSynchronize(st) != cudaSuccess)
-            return JFA_ERR_CUDA;
-    } else {
-        std::memcpy(qo.data(), q_offsets, qo.size() * 4);
-        std::memcpy(ko.data(), kv_offsets, ko.size() * 4);
+    // Per query set, the offsets of its key/value rows as if each had its own copy: the
+    // forward and dQ passes (and a dense bias's pair offsets) only need the lengths.
+    std::vector<int32_t> kvv(size_t(B) + 1, 0);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t u = kv_map ? (*kv_map)[size_t(b)] : b;
+        kvv[size_t(b) + 1] = kvv[size_t(b)] + (ko[size_t(u) + 1] - ko[size_t(u)]);
     }
-    jfa_status s = validate_offsets(qo.data(), ko.data(), B);
-    if (s != JFA_OK) return s;
 
     jfa_plan_t* p = new (std::nothrow) jfa_plan_t();
     if (!p) return JFA_ERR_CUDA;
     p->B = B;
+    p->U = U;
+    p->shared_kv = kv_map != nullptr;
     p->H = H;
     p->D = D;
     p->mode = mode;
     p->causal = causal;
     p->window = window;
     p->Tq = qo[size_t(B)];
-    p->Tkv = ko[size_t(B)];
+    p->Tkv = ko[size_t(U)];
     p->device = dev;
     p->num_sms = prop.multiProcessorCount;
     p->q_off = qo;
     p->kv_off = ko;
     p->timing = false;
 
-    p->n_fwd_items = count_items(qo.data(), ko.data(), B, H, causal, kPassFwd);
-    p->n_bwd_items = count_items(qo.data(), ko.data(), B, H, causal, kPassBwdKV);
-    p->n_dq_items = count_items(qo.data(), ko.data(), B, H, causal, kPassBwdQ);
+    std::vector<int2> steps;
+    std::vector<int32_t> step_off, ktile_off;
+    p->n_fwd_items = count_items(qo.data(), kvv.data(), B, H, causal, kPassFwd);
+    p->n_bwd_items = kv_map ? count_shared_kv_dkdv_items(ko.data(), U, H)
+                            : count_items(qo.data(), ko.data(), B, H, causal, kPassBwdKV);
+    p->n_dq_items = count_items(qo.data(), kvv.data(), B, H, causal, kPassBwdQ);
     p->fwd_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_fwd_items)));
     p->bwd_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_bwd_items)));
     p->dq_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_dq_items)));
@@ -220,19 +214,28 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
     std::vector<WorkItem> bi(size_t(std::max<int64_t>(1, p->n_bwd_items)));
     std::vector<WorkItem> qi(size_t(std::max<int64_t>(1, p->n_dq_items)));
     std::vector<int32_t> fo(size_t(p->fwd_grid) + 1), bo(size_t(p->bwd_grid) + 1), qio(size_t(p->dq_grid) + 1);
-    build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassFwd, p->fwd_grid, fi.data(), fo.data(), nullptr);
-    build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassBwdKV, p->bwd_grid, bi.data(), bo.data(), nullptr);
-    build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassBwdQ, p->dq_grid, qi.data(), qio.data(), nullptr);
+    build_worklist(qo.data(), kvv.data(), B, H, causal, window, kPassFwd, p->fwd_grid, fi.data(), fo.data(), nullptr);
+    if (kv_map)
+        build_shared_kv_dkdv(qo.data(), ko.data(), kv_map->data(), B, U, H, causal, window, p->bwd_grid, bi.data(),
+                             bo.data(), &steps, &step_off, &ktile_off);
+    else
+        build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassBwdKV, p->bwd_grid, bi.data(), bo.data(),
+                       nullptr);
+    build_worklist(qo.data(), kvv.data(), B, H, causal, window, kPassBwdQ, p->dq_grid, qi.data(), qio.data(), nullptr);
     std::vector<int64_t> po(size_t(B) + 1, 0);  // pair offsets of a dense bias
     for (int32_t b = 0; b < B; ++b)
-        po[size_t(b) + 1] = po[size_t(b)] + int64_t(qo[size_t(b) + 1] - qo[size_t(b)]) * int64_t(ko[size_t(b) + 1] - ko[size_t(b)]);
+        po[size_t(b) + 1] = po[size_t(b)] + int64_t(qo[size_t(b) + 1] - qo[size_t(b)]) * int64_t(kvv[size_t(b) + 1] - kvv[size_t(b)]);
     p->n_pairs = po[size_t(B)];
+    p->n_steps = int64_t(steps.size());
+    if (steps.empty()) steps.push_back(make_int2(0, 0));
+    if (step_off.empty()) step_off.push_back(0);
+    if (ktile_off.empty()) ktile_off.push_back(0);
+    std::vector<int32_t> map_h = kv_map ? *kv_map : std::vector<int32_t>(1, 0);
 
     // One device block: offsets, status word, work lists (16-byte aligned pieces).
-    const size_t off_bytes = round_up((size_t(B) + 1) * 4, 256);
     size_t cur = 0;
-    const size_t o_q = cur; cur += off_bytes;
-    const size_t o_kv = cur; cur += off_bytes;
+    const size_t o_q = cur; cur += round_up((size_t(B) + 1) * 4, 256);
+    const size_t o_kv = cur; cur += round_up((size_t(U) + 1) * 4, 256);
     const size_t o_st = cur; cur += 256;
     const size_t o_fi = cur; cur += round_up(fi.size() * 16, 256);
     const size_t o_fo = cur; cur += round_up(fo.size() * 4, 256);
@@ -241,6 +244,10 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
     const size_t o_qi = cur; cur += round_up(qi.size() * 16, 256);
     const size_t o_qo = cur; cur += round_up(qio.size() * 4, 256);
     const size_t o_po = cur; cur += round_up(po.size() * 8, 256);
+    const size_t o_map = cur; cur += round_up(map_h.size() * 4, 256);
+    const size_t o_sp = cur; cur += round_up(steps.size() * 8, 256);
+    const size_t o_so = cur; cur += round_up(step_off.size() * 4, 256);
+    const size_t o_ko = cur; cur += round_up(ktile_off.size() * 4, 256);
     if (cudaMalloc(&p->dev_block, cur) != cudaSuccess) {
         delete p;
         return JFA_ERR_CUDA;
@@ -256,16 +263,21 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
     p->d_dq_items = reinterpret_cast<int4*>(base + o_qi);
     p->d_dq_cta_off = reinterpret_cast<int32_t*>(base + o_qo);
     p->d_pair_off = reinterpret_cast<int64_t*>(base + o_po);
-    bool ok = cudaMemcpyAsync(p->d_q_off, qo.data(), qo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_kv_off, ko.data(), ko.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+    p->d_kv_map = kv_map ? reinterpret_cast<int32_t*>(base + o_map) : nullptr;
+    p->d_steps = kv_map ? reinterpret_cast<int2*>(base + o_sp) : nullptr;
+    p->d_step_off = kv_map ? reinterpret_cast<int32_t*>(base + o_so) : nullptr;
+    p->d_ktile_off = kv_map ? reinterpret_cast<int32_t*>(base + o_ko) : nullptr;
+    auto up = [&](void* dst, const void* src, size_t bytes) {
+        return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    };
+    bool ok = up(p->d_q_off, qo.data(), qo.size() * 4) && up(p->d_kv_off, ko.data(), ko.size() * 4) &&
               cudaMemsetAsync(p->d_status, 0, 256, st) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_fwd_items, fi.data(), fi.size() * 16, cudaMemcpyHostToDevice, st) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_fwd_cta_off, fo.data(), fo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_bwd_items, bi.data(), bi.size() * 16, cudaMemcpyHostToDevice, st) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_bwd_cta_off, bo.data(), bo.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_dq_items, qi.data(), qi.size() * 16, cudaMemcpyHostToDevice, st) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_dq_cta_off, qio.data(), qio.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_pair_off, po.data(), po.size() * 8, cudaMemcpyHostToDevice, st) == cudaSuccess;
+              up(p->d_fwd_items, fi.data(), fi.size() * 16) && up(p->d_fwd_cta_off, fo.data(), fo.size() * 4) &&
+              up(p->d_bwd_items, bi.data(), bi.size() * 16) && up(p->d_bwd_cta_off, bo.data(), bo.size() * 4) &&
+              up(p->d_dq_items, qi.data(), qi.size() * 16) && up(p->d_dq_cta_off, qio.data(), qio.size() * 4) &&
+              up(p->d_pair_off, po.data(), po.size() * 8) && up(base + o_map, map_h.data(), map_h.size() * 4) &&
+              up(base + o_sp, steps.data(), steps.size() * 8) && up(base + o_so, step_off.data(), step_off.size() * 4) &&
+              up(base + o_ko, ktile_off.data(), ktile_off.size() * 4);
     // The host vectors are pageable: the copies above are staged before returning,
     // but keep the stream ordered before the vectors go out of scope.
     if (!ok || cudaStreamSynchronize(st) != cudaSuccess) {
@@ -275,6 +287,63 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
     }
     *out = p;
     return JFA_OK;
+}
+
+// Host copies of offsets (or of a map) given on the host or, with on_device, on the
+// device (copied on `st`, which this synchronises).
+static bool host_copy(const int32_t* src, size_t n, int32_t on_device, cudaStream_t st, std::vector<int32_t>* dst) {
+    dst->resize(n);
+    if (n == 0) return true;
+    if (on_device)
+        return cudaMemcpyAsync(dst->data(), src, n * 4, cudaMemcpyDeviceToHost, st) == cudaSuccess &&
+               cudaStreamSynchronize(st) == cudaSuccess;
+    std::memcpy(dst->data(), src, n * 4);
+    return true;
+}
+
+jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H, int32_t D,
+                              int32_t mode, int32_t causal, int32_t window, int32_t offsets_on_device, void* stream,
+                              jfa_plan* out) {
+    if (!out) return JFA_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!q_offsets || !kv_offsets || B < 0 || H < 1 || H > 65535) return JFA_ERR_INVALID_ARG;
+    if (mode != JFA_SOFTMAX && mode != JFA_GDPA_GELU_TANH && mode != JFA_GDPA_SILU) return JFA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return JFA_ERR_INVALID_ARG;
+    if (window < -1 || (window >= 0 && causal != 1)) return JFA_ERR_INVALID_ARG;
+    if (D != 32 && D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::vector<int32_t> qo, ko;
+    if (!host_copy(q_offsets, size_t(B) + 1, offsets_on_device, st, &qo) ||
+        !host_copy(kv_offsets, size_t(B) + 1, offsets_on_device, st, &ko))
+        return JFA_ERR_CUDA;
+    jfa_status s = validate_offsets(qo.data(), ko.data(), B);
+    if (s != JFA_OK) return s;
+    return plan_create_impl(qo, ko, nullptr, B, B, H, D, mode, causal, window, st, out);
+}
+
+jfa_status jfa_plan_create_shared_kv(const int32_t* q_offsets, int32_t B, const int32_t* kv_offsets, int32_t U,
+                                     const int32_t* kv_index, int32_t H, int32_t D, int32_t mode, int32_t causal,
+                                     int32_t window, int32_t offsets_on_device, void* stream, jfa_plan* out) {
+    if (!out) return JFA_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!q_offsets || !kv_offsets || (B > 0 && !kv_index) || B < 0 || U < 0 || H < 1 || H > 65535)
+        return JFA_ERR_INVALID_ARG;
+    if (mode != JFA_SOFTMAX && mode != JFA_GDPA_GELU_TANH && mode != JFA_GDPA_SILU) return JFA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return JFA_ERR_INVALID_ARG;
+    if (window < -1 || (window >= 0 && causal != 1)) return JFA_ERR_INVALID_ARG;
+    if (D != 32 && D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::vector<int32_t> qo, ko, map;
+    if (!host_copy(q_offsets, size_t(B) + 1, offsets_on_device, st, &qo) ||
+        !host_copy(kv_offsets, size_t(U) + 1, offsets_on_device, st, &ko) ||
+        !host_copy(kv_index, size_t(B), offsets_on_device, st, &map))
+        return JFA_ERR_CUDA;
+    if (qo[0] != 0 || ko[0] != 0) return JFA_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < B; ++b)
+        if (qo[size_t(b) + 1] < qo[size_t(b)] || map[size_t(b)] < 0 || map[size_t(b)] >= U) return JFA_ERR_INVALID_ARG;
+    for (int32_t u = 0; u < U; ++u)
+        if (ko[size_t(u) + 1] < ko[size_t(u)]) return JFA_ERR_INVALID_ARG;
+    return plan_create_impl(qo, ko, &map, B, U, H, D, mode, causal, window, st, out);
 }
 
 jfa_status jfa_plan_destroy(jfa_plan plan) {
@@ -291,11 +360,11 @@ jfa_status jfa_plan_destroy(jfa_plan plan) {
 
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
     if (!plan || !info || n < 0) return JFA_ERR_INVALID_ARG;
-    const int64_t v[16] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
+    const int64_t v[17] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
                            plan->mode,     plan->causal,  plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items,
                            plan->bwd_grid, plan->num_sms, plan->n_dq_items,  plan->dq_grid,  plan->window,
-                           plan->n_pairs};
-    for (int32_t i = 0; i < n && i < 16; ++i) info[i] = v[i];
+                           plan->n_pairs,  plan->shared_kv ? plan->U : -1};
+    for (int32_t i = 0; i < n && i < 17; ++i) info[i] = v[i];
     return JFA_OK;
 }
 
@@ -379,6 +448,7 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
         p.pair_off = plan->d_pair_off;
         p.n_pairs = plan->n_pairs;
     }
+    p.kv_map = plan->d_kv_map;
     KernelTimer tm(plan, 0, static_cast<cudaStream_t>(stream));
     cudaError_t e = dtype == JFA_BF16
                         ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, plan->fwd_grid, static_cast<cudaStream_t>(stream))
@@ -508,6 +578,10 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
             p.pair_off = plan->d_pair_off;
             p.n_pairs = plan->n_pairs;
         }
+        // shared key/value: the dK/dV pass walks the user's step lists, the dQ pass maps
+        p.steps = plan->d_steps;
+        p.step_off = plan->d_step_off;
+        p.ktile_off = plan->d_ktile_off;
     }
     if (plan->n_bwd_items > 0) {
         KernelTimer tm(plan, 2, st);
@@ -527,6 +601,8 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
         // dQ per query tile, written directly (also the zero rows of tiles that see no key)
         p.items = plan->d_dq_items;
         p.cta_off = plan->d_dq_cta_off;
+        p.kv_map = plan->d_kv_map;
+        p.steps = nullptr;
         KernelTimer tm(plan, 4, st);
         e = launch_bwd_dq(dtype, plan->D, mq, mk, mv, mdo, p, plan->dq_grid, st);
         tm.done();

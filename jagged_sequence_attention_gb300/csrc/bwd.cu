@@ -113,7 +113,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 // second kernel sums in a fixed order (so the result is the same on every run).
 // DENSE: the bias is the dense per-pair array p.dense, read per element; with p.ddense
 // set, dS of every allowed pair is also stored there (its gradient).
-template <int D, bool GDPA, bool DBIAS, bool DENSE>
+// SHARED: shared key/value; an item is a user's key tile and its steps, read from
+// p.steps, are the (query set, query tile) pairs of all the user's query sets, so that
+// dK and dV accumulate the broadcast's gradient in TMEM and are written once.
+template <int D, bool GDPA, bool DBIAS, bool DENSE, bool SHARED>
 __global__ void __launch_bounds__(320, 1)
     jfa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -187,10 +190,11 @@ __global__ void __launch_bounds__(320, 1)
                 const int4 w = p.items[it];
                 const int n = w.w;
                 if (n == 0) continue;
-                const int b = w.x, h = w.y, nt = w.z;
-                const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0, kv0 = p.kv_off[b];
-                int first_qt, nq;  // query tiles [first_qt, first_qt + n) see this key tile
-                query_tile_range(q_len, p.kv_off[b + 1] - kv0, nt, p.causal, p.window, first_qt, nq);
+                const int b = w.x, h = w.y, nt = w.z;  // b: key/value sequence (shared: the user)
+                const int q0 = SHARED ? 0 : p.q_off[b], kv0 = p.kv_off[b];
+                int first_qt = 0, nq;  // query tiles [first_qt, first_qt + n) see this key tile
+                if (!SHARED) query_tile_range(p.q_off[b + 1] - q0, p.kv_off[b + 1] - kv0, nt, p.causal, p.window, first_qt, nq);
+                const int s0 = SHARED ? p.step_off[p.ktile_off[b] + nt] : 0;
                 if (!mbar_wait_bounded(bar(KV_KV_EMPTY), (item_it & 1) ^ 1, abort_flag)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(KV_K_FULL), C::kKVTile);
 #pragma unroll
@@ -203,7 +207,13 @@ __global__ void __launch_bounds__(320, 1)
                 ++item_it;
                 for (int i = 0; i < n; ++i, ++step_it) {
                     const uint32_t st = step_it & 1, ph = (step_it >> 1) & 1;
-                    const int y = q0 + (first_qt + i) * C::BM;
+                    int y;
+                    if constexpr (SHARED) {
+                        const int2 stp = p.steps[s0 + i];
+                        y = p.q_off[stp.x] + stp.y * C::BM;
+                    } else {
+                        y = q0 + (first_qt + i) * C::BM;
+                    }
                     if (!mbar_wait_bounded(bar(KV_Q_EMPTY + st), ph ^ 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(bar(KV_Q_FULL + st), C::kQTile);
 #pragma unroll
@@ -404,17 +414,30 @@ __global__ void __launch_bounds__(320, 1)
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
             const int4 w = p.items[it];
-            const int n = w.w, b = w.x, h = w.y, nt = w.z;
-            const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
+            const int n = w.w, b = w.x, h = w.y, nt = w.z;  // b: key/value sequence (shared: the user)
             const int kv0 = p.kv_off[b], kv_len = p.kv_off[b + 1] - kv0;
-            const int diag = kv_len - q_len;
-            int first_qt, nq;  // query tiles [first_qt, first_qt + n) see this key tile
-            query_tile_range(q_len, kv_len, nt, p.causal, p.window, first_qt, nq);
+            // The query sequence of the item (not shared), or of each step (shared).
+            const int q0 = SHARED ? 0 : p.q_off[b], q_len = SHARED ? 0 : p.q_off[b + 1] - q0;
+            int first_qt = 0, nq;  // query tiles [first_qt, first_qt + n) see this key tile
+            if (!SHARED) query_tile_range(q_len, kv_len, nt, p.causal, p.window, first_qt, nq);
+            const int s0 = SHARED ? p.step_off[p.ktile_off[b] + nt] : 0;
             const int j = nt * C::BN + r;  // key row within the sequence
             const bool key_valid = j < kv_len;
-            // dense bias / gradient of key j: element (query row i) at [i * kv_len]
-            const size_t dbase = DENSE ? size_t(h) * size_t(p.n_pairs) + size_t(p.pair_off[b]) + size_t(key_valid ? j : 0)
-                                       : 0;
+            // Step i: query sequence sb (rows from sq0, sq_len of them), first row sqrow0.
+            auto step_q = [&](int i, int& sb, int& sq0, int& sq_len, int& sqrow0) {
+                if constexpr (SHARED) {
+                    const int2 stp = p.steps[s0 + i];
+                    sb = stp.x;
+                    sq0 = p.q_off[sb];
+                    sq_len = p.q_off[sb + 1] - sq0;
+                    sqrow0 = stp.y * C::BM;
+                } else {
+                    sb = b;
+                    sq0 = q0;
+                    sq_len = q_len;
+                    sqrow0 = (first_qt + i) * C::BM;
+                }
+            };
             const size_t krow = (size_t(kv0) + size_t(key_valid ? j : 0)) * size_t(p.H) + size_t(h);
             __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dV) + krow * D + wg * C::kEpiCols;
             __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dK) + krow * D + wg * C::kEpiCols;
@@ -433,27 +456,41 @@ __global__ void __launch_bounds__(320, 1)
             // Row terms (lse in log2 units, Delta) of this warpgroup's query columns:
             // lane l holds columns c0 + l and c0 + 32 + l, fetched one step ahead.
             float nl[2] = {0.f, 0.f}, nd[2] = {0.f, 0.f};
-            auto fetch = [&](int qrow0) {
+            auto fetch = [&](int fq0, int fq_len, int qrow0) {
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int c = qrow0 + c0 + 32 * k + lane;
-                    const bool v = softmax && c < q_len;
-                    const size_t ridx = (size_t(q0) + size_t(v ? c : 0)) * size_t(p.H) + size_t(h);
+                    const bool v = softmax && c < fq_len;
+                    const size_t ridx = (size_t(fq0) + size_t(v ? c : 0)) * size_t(p.H) + size_t(h);
                     nl[k] = v ? -p.lse[ridx] * 1.4426950408889634f : 0.f;
                     nd[k] = v ? -p.delta[ridx] : 0.f;
                 }
             };
-            fetch(first_qt * C::BM);
+            {
+                int fb, fq0, fql, fr0;
+                step_q(0, fb, fq0, fql, fr0);
+                fetch(fq0, fql, fr0);
+            }
             for (int i = 0; i < n; ++i) {
                 const uint32_t g = step_it + uint32_t(i);
-                const int qrow0 = (first_qt + i) * C::BM;  // first query row of the step
+                int sb, sq0, sq_len, qrow0;  // the step's query sequence and first query row
+                step_q(i, sb, sq0, sq_len, qrow0);
+                const int diag = kv_len - sq_len;
                 const float cur_nl0 = nl[0], cur_nl1 = nl[1];
                 __syncwarp();
                 del_s[lane] = nd[0];
                 del_s[32 + lane] = nd[1];
-                if (i + 1 < n) fetch(qrow0 + C::BM);
+                if (i + 1 < n) {
+                    int fb, fq0, fql, fr0;
+                    step_q(i + 1, fb, fq0, fql, fr0);
+                    fetch(fq0, fql, fr0);
+                }
+                // dense bias / gradient of key j: element (query row i) at [i * kv_len]
+                const size_t dbase = DENSE ? size_t(h) * size_t(p.n_pairs) + size_t(p.pair_off[sb]) +
+                                                 size_t(key_valid ? j : 0)
+                                           : 0;
                 // subtraction scheme: valid local columns are [lo, hi)
-                int hi = key_valid ? min(NC, q_len - qrow0 - c0) : 0;
+                int hi = key_valid ? min(NC, sq_len - qrow0 - c0) : 0;
                 // sliding window: query i sees key j only while j >= i' - W, i.e. i <= j - diag + W
                 if (p.window >= 0) hi = min(hi, j - diag + p.window + 1 - qrow0 - c0);
                 const int lo = p.causal ? max(0, j - diag - qrow0 - c0) : 0;
@@ -802,32 +839,40 @@ __global__ void jfa_dbias_reduce_items_kernel(const float* __restrict__ part, co
     dbias[e] = acc;
 }
 
-template <int D, bool GDPA, bool DBIAS, bool DENSE>
+template <int D, bool GDPA, bool DBIAS, bool DENSE, bool SHARED>
 cudaError_t launch_dkdv_t_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
     using C = KvCfg<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(jfa_bwd_dkdv_kernel<D, GDPA, DBIAS, DENSE>,
+        cudaError_t e = cudaFuncSetAttribute(jfa_bwd_dkdv_kernel<D, GDPA, DBIAS, DENSE, SHARED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_dkdv_kernel<D, GDPA, DBIAS, DENSE><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
+    jfa_bwd_dkdv_kernel<D, GDPA, DBIAS, DENSE, SHARED><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
     return cudaGetLastError();
+}
+
+template <int D, bool SHARED>
+cudaError_t launch_dkdv_t_s(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                            const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
+    const bool sm = p.mode == JFA_SOFTMAX;
+    if (p.dense)
+        return sm ? launch_dkdv_t_m<D, false, false, true, SHARED>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                  : launch_dkdv_t_m<D, true, false, true, SHARED>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    if (p.dbias_part)
+        return sm ? launch_dkdv_t_m<D, false, true, false, SHARED>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                  : launch_dkdv_t_m<D, true, true, false, SHARED>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    return sm ? launch_dkdv_t_m<D, false, false, false, SHARED>(tmQ, tmK, tmV, tmdO, p, grid, st)
+              : launch_dkdv_t_m<D, true, false, false, SHARED>(tmQ, tmK, tmV, tmdO, p, grid, st);
 }
 
 template <int D>
 cudaError_t launch_dkdv_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
-    if (p.dense)
-        return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false, false, true>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                                     : launch_dkdv_t_m<D, true, false, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
-    if (p.dbias_part)
-        return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false, true, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                                     : launch_dkdv_t_m<D, true, true, false>(tmQ, tmK, tmV, tmdO, p, grid, st);
-    return p.mode == JFA_SOFTMAX ? launch_dkdv_t_m<D, false, false, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                                 : launch_dkdv_t_m<D, true, false, false>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    return p.steps ? launch_dkdv_t_s<D, true>(tmQ, tmK, tmV, tmdO, p, grid, st)
+                   : launch_dkdv_t_s<D, false>(tmQ, tmK, tmV, tmdO, p, grid, st);
 }
 
 template <typename TO, typename T, int D>

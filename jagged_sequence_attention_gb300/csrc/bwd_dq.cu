@@ -156,9 +156,10 @@ __global__ void __launch_bounds__(320, 1)
                 const int n = w.w;
                 if (n == 0) continue;
                 const int b = w.x, h = w.y, tq = w.z;
-                const int q0 = p.q_off[b], kv0 = p.kv_off[b];
+                const int kb = p.kv_map ? p.kv_map[b] : b;  // key/value sequence (shared: the user)
+                const int q0 = p.q_off[b], kv0 = p.kv_off[kb];
                 int kf, nk;  // key tiles [kf, kf + n)
-                key_tile_range(p.q_off[b + 1] - q0, p.kv_off[b + 1] - kv0, tq, p.causal, p.window, kf, nk);
+                key_tile_range(p.q_off[b + 1] - q0, p.kv_off[kb + 1] - kv0, tq, p.causal, p.window, kf, nk);
                 if (!mbar_wait_bounded(bar(DQ_QDO_EMPTY), (item_it & 1) ^ 1, abort_flag)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(DQ_Q_FULL), C::kQTile);
 #pragma unroll
@@ -321,7 +322,8 @@ __global__ void __launch_bounds__(320, 1)
             const int4 w = p.items[it];
             const int n = w.w, b = w.x, h = w.y, tq = w.z;
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
-            const int kv_len = p.kv_off[b + 1] - p.kv_off[b];
+            const int kb = p.kv_map ? p.kv_map[b] : b;
+            const int kv_len = p.kv_off[kb + 1] - p.kv_off[kb];
             const int diag = kv_len - q_len;
             const int row = tq * C::BM + t;
             const bool row_valid = row < q_len;

@@ -53,7 +53,8 @@ __global__ void __launch_bounds__(kF32Rows) jfa_fwd_f32_kernel(const float* __re
     const int4 w = p.items[blockIdx.x >> 1];
     const int b = w.x, h = w.y, mt = 2 * w.z + int(blockIdx.x & 1);
     const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
-    const int k0 = p.kv_off[b], kv_len = p.kv_off[b + 1] - k0;
+    const int kb = p.kv_map ? p.kv_map[b] : b;  // key/value sequence (shared: the user)
+    const int k0 = p.kv_off[kb], kv_len = p.kv_off[kb + 1] - k0;
     if (mt * kF32Rows >= q_len) return;  // second tile of a short last pair (uniform exit)
     int kf, n_tiles;  // key tiles [kf, kf + n_tiles)
     key_tile_range(q_len, kv_len, mt, p.causal, p.window, kf, n_tiles);
@@ -153,12 +154,11 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
     __shared__ float sDiag[kDiags];
     __shared__ float sDB[32];  // the item's table gradient, bucket t owned by thread t
     const int4 w = p.items[blockIdx.x];
+    // b: the key/value sequence of the item (shared key/value: the user)
     const int b = w.x, h = w.y, nt = w.z, n = w.w;
-    const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
     const int k0 = p.kv_off[b], kv_len = p.kv_off[b + 1] - k0;
     const int t = threadIdx.x, j = nt * kBwdBN + t;
     const bool kvalid = j < kv_len;
-    const int diag = kv_len - q_len;
     const bool softmax = p.mode == JFA_SOFTMAX;
     if (t < 32) sB[t] = p.bias ? p.bias[h * 32 + t] : 0.f;
     if (t < 32) sDB[t] = 0.f;
@@ -171,90 +171,108 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
         dk[d] = 0.f;
         dv[d] = 0.f;
     }
-    int first_qt, nq;  // query tiles [first_qt, first_qt + n) see this key tile
-    query_tile_range(q_len, kv_len, nt, p.causal, p.window, first_qt, nq);
-    // dense per-pair bias and its gradient of key j: element (query row i) at [i * kv_len]
-    const size_t dcol = size_t(h) * size_t(p.n_pairs) + size_t(p.pair_off ? p.pair_off[b] : 0) + size_t(kvalid ? j : 0);
-    const int row_begin = first_qt * kBwdBM;
-    const int row_end = min(q_len, (first_qt + n) * kBwdBM);
     const int n_keys = min(kBwdBN, kv_len - nt * kBwdBN);
-    for (int r0 = row_begin; r0 < row_end; r0 += kF32InnerB) {
-        __syncthreads();
-        for (int e = t; e < kF32InnerB * D; e += kF32Rows) {
-            const int r = e / D, d = e % D;
-            const bool in = r0 + r < q_len;
-            const size_t rq = (size_t(q0) + size_t(in ? r0 + r : 0)) * p.H + h;
-            sQ[r][d] = in ? Q[rq * D + d] : 0.f;
-            sdO[r][d] = in ? dO[rq * D + d] : 0.f;
+    // Query rows that see this key tile, as segments of one query sequence each: the
+    // sequence's own tile range, or (shared key/value) one 128-row query tile per step
+    // of every query set of the user.
+    const int n_seg = p.steps ? n : 1;
+    const int s0 = p.steps ? p.step_off[p.ktile_off[b] + nt] : 0;
+    for (int sg = 0; sg < n_seg; ++sg) {
+        int qb, row_begin, row_end;
+        if (p.steps) {
+            const int2 st = p.steps[s0 + sg];
+            qb = st.x;
+            row_begin = st.y * kBwdBM;
+            row_end = min(p.q_off[qb + 1] - p.q_off[qb], row_begin + kBwdBM);
+        } else {
+            int first_qt, nq;  // query tiles [first_qt, first_qt + n) see this key tile
+            qb = b;
+            query_tile_range(p.q_off[b + 1] - p.q_off[b], kv_len, nt, p.causal, p.window, first_qt, nq);
+            row_begin = first_qt * kBwdBM;
+            row_end = min(p.q_off[b + 1] - p.q_off[b], (first_qt + n) * kBwdBM);
         }
-        if (t < kF32InnerB) {
-            const bool in = r0 + t < q_len;
-            const size_t rq = (size_t(q0) + size_t(in ? r0 + t : 0)) * p.H + h;
-            sL[t] = (in && softmax) ? p.lse[rq] : 0.f;
-            sDel[t] = (in && softmax) ? p.delta[rq] : 0.f;
-        }
-        __syncthreads();
-        for (int i = 0; i < kF32InnerB; ++i) {
-            const int row = r0 + i;
-            const bool ok = kvalid && row < q_len && (!p.causal || j <= row + diag) &&
-                            (p.window < 0 || j >= row + diag - p.window);
-            float ds = 0.f;
-            if (ok) {
-                float acc = 0.f, dp = 0.f;
-#pragma unroll
-                for (int d = 0; d < D; ++d) {
-                    acc = fmaf(sQ[i][d], k[d], acc);
-                    dp = fmaf(sdO[i][d], v[d], dp);
-                }
-                float x = acc * p.scale;
-                if (p.bias) x += sB[bucket_f32(row + diag - j)];
-                if (p.dense) x += __ldg(p.dense + dcol + size_t(row) * size_t(kv_len));
-                float pij;
-                if (softmax) {
-                    pij = expf(x - sL[i]);
-                    ds = pij * (dp - sDel[i]);
-                } else {
-                    pij = act_f32(p.mode, x);
-                    ds = act_grad_f32(p.mode, x) * dp;
-                }
-                if (p.ddense) p.ddense[dcol + size_t(row) * size_t(kv_len)] = ds;
-#pragma unroll
-                for (int d = 0; d < D; ++d) {
-                    dv[d] = fmaf(pij, sdO[i][d], dv[d]);
-                    dk[d] = fmaf(ds, sQ[i][d], dk[d]);
-                }
+        const int q0 = p.q_off[qb], q_len = p.q_off[qb + 1] - q0;
+        const int diag = kv_len - q_len;
+        // dense per-pair bias and its gradient of key j: element (query row i) at [i * kv_len]
+        const size_t dcol = size_t(h) * size_t(p.n_pairs) + size_t(p.pair_off ? p.pair_off[qb] : 0) + size_t(kvalid ? j : 0);
+        for (int r0 = row_begin; r0 < row_end; r0 += kF32InnerB) {
+            __syncthreads();
+            for (int e = t; e < kF32InnerB * D; e += kF32Rows) {
+                const int r = e / D, d = e % D;
+                const bool in = r0 + r < q_len;
+                const size_t rq = (size_t(q0) + size_t(in ? r0 + r : 0)) * p.H + h;
+                sQ[r][d] = in ? Q[rq * D + d] : 0.f;
+                sdO[r][d] = in ? dO[rq * D + d] : 0.f;
             }
-            sDS[i][t] = ds;
-        }
-        __syncthreads();
-        // dQ rows of this chunk: sum over the CTA's keys (K rows re-read through the
-        // cache), then one atomic per element
-        for (int e = t; e < kF32InnerB * D; e += kF32Rows) {
-            const int i = e / D, d = e % D;
-            if (r0 + i >= q_len) continue;
-            float acc = 0.f;
-            for (int jj = 0; jj < n_keys; ++jj)
-                acc = fmaf(sDS[i][jj], __ldg(K + ((size_t(k0) + size_t(nt * kBwdBN + jj)) * p.H + h) * D + d), acc);
-            const size_t rq = (size_t(q0) + size_t(r0 + i)) * p.H + h;
-            atomicAdd(p.dq_acc + rq * D + d, acc);
-        }
-        if (p.dbias_part) {
-            // diagonal dd holds the elements with i - t = dd - (kF32Rows - 1), i ascending
-            for (int dd = t; dd < kDiags; dd += kF32Rows) {
-                const int off = dd - (kF32Rows - 1);
-                const int i0 = max(0, off), i1 = min(kF32InnerB - 1, kF32Rows - 1 + off);
-                float acc = 0.f;
-                for (int i = i0; i <= i1; ++i) acc += sDS[i][i - off];
-                sDiag[dd] = acc;
+            if (t < kF32InnerB) {
+                const bool in = r0 + t < q_len;
+                const size_t rq = (size_t(q0) + size_t(in ? r0 + t : 0)) * p.H + h;
+                sL[t] = (in && softmax) ? p.lse[rq] : 0.f;
+                sDel[t] = (in && softmax) ? p.delta[rq] : 0.f;
             }
             __syncthreads();
-            if (t < 32) {
-                // element (i, t') has relative position r0 + i + diag - (nt * 128 + t')
-                const int rel0 = r0 + diag - nt * kBwdBN - (kF32Rows - 1);
+            for (int i = 0; i < kF32InnerB; ++i) {
+                const int row = r0 + i;
+                const bool ok = kvalid && row < q_len && (!p.causal || j <= row + diag) &&
+                                (p.window < 0 || j >= row + diag - p.window);
+                float ds = 0.f;
+                if (ok) {
+                    float acc = 0.f, dp = 0.f;
+    #pragma unroll
+                    for (int d = 0; d < D; ++d) {
+                        acc = fmaf(sQ[i][d], k[d], acc);
+                        dp = fmaf(sdO[i][d], v[d], dp);
+                    }
+                    float x = acc * p.scale;
+                    if (p.bias) x += sB[bucket_f32(row + diag - j)];
+                    if (p.dense) x += __ldg(p.dense + dcol + size_t(row) * size_t(kv_len));
+                    float pij;
+                    if (softmax) {
+                        pij = expf(x - sL[i]);
+                        ds = pij * (dp - sDel[i]);
+                    } else {
+                        pij = act_f32(p.mode, x);
+                        ds = act_grad_f32(p.mode, x) * dp;
+                    }
+                    if (p.ddense) p.ddense[dcol + size_t(row) * size_t(kv_len)] = ds;
+    #pragma unroll
+                    for (int d = 0; d < D; ++d) {
+                        dv[d] = fmaf(pij, sdO[i][d], dv[d]);
+                        dk[d] = fmaf(ds, sQ[i][d], dk[d]);
+                    }
+                }
+                sDS[i][t] = ds;
+            }
+            __syncthreads();
+            // dQ rows of this chunk: sum over the CTA's keys (K rows re-read through the
+            // cache), then one atomic per element
+            for (int e = t; e < kF32InnerB * D; e += kF32Rows) {
+                const int i = e / D, d = e % D;
+                if (r0 + i >= q_len) continue;
                 float acc = 0.f;
-                for (int dd = 0; dd < kDiags; ++dd)
-                    if (bucket_f32(rel0 + dd) == t) acc += sDiag[dd];
-                sDB[t] += acc;
+                for (int jj = 0; jj < n_keys; ++jj)
+                    acc = fmaf(sDS[i][jj], __ldg(K + ((size_t(k0) + size_t(nt * kBwdBN + jj)) * p.H + h) * D + d), acc);
+                const size_t rq = (size_t(q0) + size_t(r0 + i)) * p.H + h;
+                atomicAdd(p.dq_acc + rq * D + d, acc);
+            }
+            if (p.dbias_part) {
+                // diagonal dd holds the elements with i - t = dd - (kF32Rows - 1), i ascending
+                for (int dd = t; dd < kDiags; dd += kF32Rows) {
+                    const int off = dd - (kF32Rows - 1);
+                    const int i0 = max(0, off), i1 = min(kF32InnerB - 1, kF32Rows - 1 + off);
+                    float acc = 0.f;
+                    for (int i = i0; i <= i1; ++i) acc += sDS[i][i - off];
+                    sDiag[dd] = acc;
+                }
+                __syncthreads();
+                if (t < 32) {
+                    // element (i, t') has relative position r0 + i + diag - (nt * 128 + t')
+                    const int rel0 = r0 + diag - nt * kBwdBN - (kF32Rows - 1);
+                    float acc = 0.f;
+                    for (int dd = 0; dd < kDiags; ++dd)
+                        if (bucket_f32(rel0 + dd) == t) acc += sDiag[dd];
+                    sDB[t] += acc;
+                }
             }
         }
     }

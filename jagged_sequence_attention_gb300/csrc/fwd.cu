@@ -178,8 +178,9 @@ __global__ void __launch_bounds__(320, 1)
                 const int n = w.w;
                 if (n == 0) continue;
                 const int b = w.x, h = w.y, pr = w.z;
-                const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0, kv0 = p.kv_off[b];
-                const int kv_len = p.kv_off[b + 1] - kv0;
+                const int kb = p.kv_map ? p.kv_map[b] : b;  // key/value sequence (shared: the user)
+                const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0, kv0 = p.kv_off[kb];
+                const int kv_len = p.kv_off[kb + 1] - kv0;
                 const int ntiles = (2 * pr + 1) * C::BM < q_len ? 2 : 1;
                 int f0, ns, na, nb;  // the pair streams key tiles [f0, f0 + n)
                 pair_stream(q_len, kv_len, pr, p.causal, window, f0, ns, na, nb);
@@ -286,7 +287,8 @@ __global__ void __launch_bounds__(320, 1)
             const int n = w.w;
             if (n == 0) continue;
             const int b = w.x, pr = w.z;
-            const int q_len = p.q_off[b + 1] - p.q_off[b], kv_len = p.kv_off[b + 1] - p.kv_off[b];
+            const int kb = p.kv_map ? p.kv_map[b] : b;
+            const int q_len = p.q_off[b + 1] - p.q_off[b], kv_len = p.kv_off[kb + 1] - p.kv_off[kb];
             // Each tile's key range inside the pair's stream [f0, f0 + n): tile x is active
             // for stream steps [off_x, off_x + nx_x).
             int fa, nx0, fb, nx1, f0, ns, na2, nb2;
@@ -344,7 +346,8 @@ __global__ void __launch_bounds__(320, 1)
             const int4 w = p.items[it];
             const int b = w.x, h = w.y, pr = w.z;
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
-            const int kv_len = p.kv_off[b + 1] - p.kv_off[b];
+            const int kb = p.kv_map ? p.kv_map[b] : b;
+            const int kv_len = p.kv_off[kb + 1] - p.kv_off[kb];
             const int tile = 2 * pr + x;
             if (tile * C::BM >= q_len) continue;  // tile B of a short last pair
             int kf, n;  // key tiles [kf, kf + n)

@@ -139,6 +139,9 @@ struct FwdParams {
     const float* dense = nullptr;
     const int64_t* pair_off = nullptr;
     int64_t n_pairs = 0;
+    // Shared key/value: kv_map[b] is query set b's key/value sequence (its user), whose
+    // rows are kv_off[u] .. kv_off[u+1]; nullptr: sequence b's own.
+    const int32_t* kv_map = nullptr;
 };
 
 struct BwdParams {
@@ -169,6 +172,13 @@ struct BwdParams {
     float* ddense = nullptr;
     const int64_t* pair_off = nullptr;
     int64_t n_pairs = 0;
+    // Shared key/value, as in FwdParams.  The dK/dV pass then works per user key tile:
+    // item (u, h, tile, n) visits steps[step_off[g] .. + n), g = ktile_off[u] + tile, each
+    // a (query set, query tile) pair.
+    const int32_t* kv_map = nullptr;
+    const int2* steps = nullptr;
+    const int32_t* step_off = nullptr;
+    const int32_t* ktile_off = nullptr;
 };
 
 // Host planner (plan.cpp).  Returns JFA_OK or an error for bad offsets.
@@ -178,6 +188,12 @@ int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
 void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
                     int32_t causal, int32_t window, int32_t pass, int32_t n_ctas, WorkItem* items,
                     int32_t* cta_off, int64_t* cta_cost);
+
+void build_shared_kv_dkdv(const int32_t* q_off, const int32_t* u_off, const int32_t* kv_index, int32_t B,
+                          int32_t U, int32_t H, int32_t causal, int32_t window, int32_t n_ctas, WorkItem* items,
+                          int32_t* cta_off, std::vector<int2>* steps, std::vector<int32_t>* step_off,
+                          std::vector<int32_t>* ktile_off);
+int64_t count_shared_kv_dkdv_items(const int32_t* u_off, int32_t U, int32_t H);
 
 int64_t sequence_cost(int64_t q_len, int64_t kv_len, int32_t H, int32_t causal, int32_t window);
 void partition_sequences(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H, int32_t causal,
@@ -214,6 +230,8 @@ bool supported(int dtype, int D);
 
 struct jfa_plan_t {
     int32_t B, H, D, mode, causal, window;
+    int32_t U;        // key/value sequences (users with shared key/value; else B)
+    bool shared_kv;   // query set b attends to user d_kv_map[b]
     int64_t Tq, Tkv;
     int device, num_sms;
     std::vector<int32_t> q_off, kv_off;   // host copies
@@ -230,6 +248,12 @@ struct jfa_plan_t {
     int32_t* d_dq_cta_off;
     int64_t* d_pair_off;  // [B+1] first (query, key) pair of each sequence, for a dense bias
     int64_t n_pairs;      // sum over sequences of q_len * kv_len
+    // shared key/value (nullptr otherwise): map [B], dK/dV steps and their offsets
+    int32_t* d_kv_map;
+    int2* d_steps;
+    int32_t* d_step_off;
+    int32_t* d_ktile_off;
+    int64_t n_steps;
     int64_t n_fwd_items, n_bwd_items, n_dq_items;
     int fwd_grid, bwd_grid, dq_grid;
     // optional per-kernel timing (jfa_plan_set_timing)

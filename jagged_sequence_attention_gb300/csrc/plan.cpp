@@ -96,13 +96,13 @@ int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
     return n;
 }
 
-void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
-                    int32_t causal, int32_t window, int32_t pass, int32_t n_ctas, WorkItem* items,
-                    int32_t* cta_off, int64_t* cta_cost) {
-    std::vector<Costed> all;
-    all.reserve(size_t(count_items(q_off, kv_off, B, H, causal, pass)));
-    build_items(q_off, kv_off, B, H, causal, window, pass, &all);
+namespace {
 
+// Group-major LPT assignment of costed items (groups: (item.b, item.h), n_groups_b
+// values of item.b) to n_ctas CTAs; writes the items in CTA order.
+void assign_lpt(std::vector<Costed>& all, int32_t n_groups_b, int32_t H, int32_t n_ctas, WorkItem* items,
+                int32_t* cta_off, int64_t* cta_cost) {
+    const int32_t B = n_groups_b;
     // Group-major order: groups by total cost (largest first, ties by sequence and
     // head), then items by cost inside the group; the sort is stable so equal keys
     // keep (sequence, head, tile) order and the plan is deterministic.
@@ -140,6 +140,58 @@ void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
     for (size_t i = 0; i < all.size(); ++i) items[cursor[size_t(owner[i])]++] = all[i].w;
     if (cta_cost)
         for (int32_t c = 0; c < n_ctas; ++c) cta_cost[c] = load[size_t(c)];
+}
+
+}  // namespace
+
+void build_worklist(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
+                    int32_t causal, int32_t window, int32_t pass, int32_t n_ctas, WorkItem* items,
+                    int32_t* cta_off, int64_t* cta_cost) {
+    std::vector<Costed> all;
+    all.reserve(size_t(count_items(q_off, kv_off, B, H, causal, pass)));
+    build_items(q_off, kv_off, B, H, causal, window, pass, &all);
+    assign_lpt(all, B, H, n_ctas, items, cta_off, cta_cost);
+}
+
+// Shared key/value (in-kernel broadcast): query set b attends to user kv_index[b]'s
+// rows.  The dK/dV pass works per user key tile; its steps are the (query set, query
+// tile) pairs of all the user's query sets that see the tile, listed per (user, key
+// tile) in steps[step_off[g]..step_off[g+1]), g = ktile_off[u] + tile (shared by the
+// heads).  Items are (u, h, tile, step count), costed and assigned as above.
+void build_shared_kv_dkdv(const int32_t* q_off, const int32_t* u_off, const int32_t* kv_index, int32_t B,
+                          int32_t U, int32_t H, int32_t causal, int32_t window, int32_t n_ctas, WorkItem* items,
+                          int32_t* cta_off, std::vector<int2>* steps, std::vector<int32_t>* step_off,
+                          std::vector<int32_t>* ktile_off) {
+    std::vector<std::vector<int32_t>> cands(size_t(U > 0 ? U : 0));
+    for (int32_t b = 0; b < B; ++b) cands[size_t(kv_index[b])].push_back(b);
+    ktile_off->assign(size_t(U) + 1, 0);
+    for (int32_t u = 0; u < U; ++u)
+        (*ktile_off)[size_t(u) + 1] = (*ktile_off)[size_t(u)] + int32_t(ceil_div(u_off[u + 1] - u_off[u], kBwdBN));
+    step_off->assign(size_t((*ktile_off)[size_t(U)]) + 1, 0);
+    steps->clear();
+    std::vector<Costed> all;
+    for (int32_t u = 0; u < U; ++u) {
+        const int64_t kv_len = u_off[u + 1] - u_off[u];
+        const int64_t nt = ceil_div(kv_len, kBwdBN);
+        for (int64_t t = 0; t < nt; ++t) {
+            const size_t g = size_t((*ktile_off)[size_t(u)] + t);
+            for (int32_t b : cands[size_t(u)]) {
+                int first, n;
+                query_tile_range(q_off[b + 1] - q_off[b], kv_len, t, causal, window, first, n);
+                for (int k = 0; k < n; ++k) steps->push_back(make_int2(b, first + k));
+            }
+            (*step_off)[g + 1] = int32_t(steps->size());
+            const int32_t n = (*step_off)[g + 1] - (*step_off)[g];
+            for (int32_t h = 0; h < H; ++h) all.push_back({{u, h, int32_t(t), n}, 4 * int64_t(n) + 2});
+        }
+    }
+    assign_lpt(all, U, H, n_ctas, items, cta_off, nullptr);
+}
+
+int64_t count_shared_kv_dkdv_items(const int32_t* u_off, int32_t U, int32_t H) {
+    int64_t n = 0;
+    for (int32_t u = 0; u < U; ++u) n += ceil_div(u_off[u + 1] - u_off[u], kBwdBN) * H;
+    return n;
 }
 
 // Data-parallel split of a batch: sequences are independent problems, so a batch

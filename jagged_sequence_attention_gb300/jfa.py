@@ -31,7 +31,7 @@ DTYPES = {torch.bfloat16: JFA_BF16, torch.float32: JFA_F32}
 EXPORTED = ["jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd_workspace_size",
             "jfa_bwd", "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build",
             "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times", "jfa_bwd_static_scratch",
-            "jfa_partition_sequences", "jfa_bwd_ex_workspace_size", "jfa_bwd_ex"]
+            "jfa_partition_sequences", "jfa_bwd_ex_workspace_size", "jfa_bwd_ex", "jfa_plan_create_shared_kv"]
 
 
 class JFAError(RuntimeError):
@@ -54,6 +54,7 @@ def lib():
         P = ctypes.POINTER
         L.jfa_plan_create.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, P(vp)]
         L.jfa_plan_create_ex.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, P(vp)]
+        L.jfa_plan_create_shared_kv.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, P(vp)]
         L.jfa_plan_destroy.argtypes = [vp]
         L.jfa_plan_info.argtypes = [vp, P(i64), i32]
         L.jfa_fwd.argtypes = [vp, i32, vp, vp, vp, i32, vp, f32, vp, i32, vp, vp]
@@ -74,7 +75,8 @@ def lib():
         L.jfa_status_string.restype = ctypes.c_char_p
         for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
                      "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build", "jfa_plan_set_timing",
-                     "jfa_plan_kernel_times", "jfa_bwd_static_scratch", "jfa_partition_sequences", "jfa_bwd_ex"):
+                     "jfa_plan_kernel_times", "jfa_bwd_static_scratch", "jfa_partition_sequences", "jfa_bwd_ex",
+                     "jfa_plan_create_shared_kv"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -161,6 +163,25 @@ def jfa_plan_create(q_offsets, kv_offsets, H: int, D: int, mode="softmax", causa
     return plan
 
 
+def jfa_plan_create_shared_kv(q_offsets, kv_offsets, kv_index, H: int, D: int, mode="softmax", causal=False,
+                              stream=None, window=None) -> Plan:
+    """Shared key/value plan: query set b attends to the rows of user kv_index[b]
+    (kv_offsets over the users).  Host arrays."""
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    qo, ko, ki = _i32(q_offsets), _i32(kv_offsets), _i32(kv_index)
+    B, U = qo.size - 1, ko.size - 1
+    if ki.size != B:
+        raise JFAError("jfa_plan_create_shared_kv", JFA_ERR_INVALID_ARG)
+    h = ctypes.c_void_p()
+    vp = ctypes.c_void_p
+    _check("jfa_plan_create_shared_kv", lib().jfa_plan_create_shared_kv(
+        qo.ctypes.data_as(vp), int(B), ko.ctypes.data_as(vp), int(U), ki.ctypes.data_as(vp), int(H), int(D), m,
+        int(bool(causal)), _win(window), 0, _stream(stream), ctypes.byref(h)))
+    plan = Plan(h, int(B), int(H), int(D), m, bool(causal), int(qo[-1]), int(ko[-1]))
+    plan.window = window
+    return plan
+
+
 def jfa_plan_destroy(plan: Plan):
     if plan.handle is not None:
         _check("jfa_plan_destroy", lib().jfa_plan_destroy(plan.handle))
@@ -168,7 +189,7 @@ def jfa_plan_destroy(plan: Plan):
 
 
 INFO_KEYS = ["T_q", "T_kv", "B", "H", "D", "mode", "causal", "fwd_items", "fwd_grid", "bwd_items", "bwd_grid",
-             "num_sms", "dq_items", "dq_grid", "window", "pairs"]
+             "num_sms", "dq_items", "dq_grid", "window", "pairs", "users"]
 
 
 def jfa_plan_info(plan: Plan) -> dict:
@@ -315,6 +336,8 @@ def shard(batch, rank: int, world: int):
     subset, repacked), by the LPT split above.  Sequences are independent, so results of
     the shards are exactly the full batch's results for those sequences."""
     from . import workloads
+    if getattr(batch, "kv_map", None) is not None:
+        raise JFAError("shard (shared key/value batches are split by user, not built)", JFA_ERR_UNSUPPORTED)
     part, _ = jfa_partition_sequences(batch.q_off, batch.kv_off, batch.H, batch.causal, world,
                                       window=getattr(batch, "window", None))
     seqs = np.nonzero(part == rank)[0]
@@ -349,11 +372,19 @@ def jfa_worklist_build(q_offsets, kv_offsets, H: int, causal: bool, pass_: int, 
 # --------------------------------------------------------------------------- convenience
 
 
+def plan_for(batch, stream=None) -> Plan:
+    """The plan of a workloads.Batch: shared key/value when it has a query-set-to-user map."""
+    if getattr(batch, "kv_map", None) is not None:
+        return jfa_plan_create_shared_kv(batch.q_off, batch.kv_off, batch.kv_map, batch.H, batch.D, batch.mode,
+                                         batch.causal, stream, window=getattr(batch, "window", None))
+    return jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal, stream,
+                           window=getattr(batch, "window", None))
+
+
 def attention(batch, with_backward=True, stream=None, out_dtype=None, bias_grad=False):
     """Run forward (and backward) for a workloads.Batch on the GPU: returns dict of tensors
     (with bias_grad, also "dbias", the gradient of the batch's bias table)."""
-    plan = jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal, stream,
-                           window=getattr(batch, "window", None))
+    plan = plan_for(batch, stream)
     dense = getattr(batch, "dense", None)
     O, lse = jfa_fwd(plan, batch.Q, batch.K, batch.V, batch.bias, batch.scale, stream=stream, out_dtype=out_dtype,
                      dense_bias=dense)

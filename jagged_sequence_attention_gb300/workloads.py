@@ -45,6 +45,9 @@ class Workload:
     kv_len: Optional[tuple]   # None: self-attention (kv lengths = q lengths)
     description: str = ""
     window: Optional[int] = None  # sliding window W (query i sees keys i' - W .. i'), or None
+    # shared key/value: B query sets over `users` users (kv_len draws the users' lengths),
+    # B // users consecutive query sets per user, or None
+    users: Optional[int] = None
 
 
 WORKLOADS = {
@@ -90,6 +93,15 @@ WORKLOADS = {
         ("uniform", 4096, 32768), None,
         "64 sequences, lengths U{4096..32768} (~1.2M tokens), causal sliding window of 2048 keys, 8 heads, "
         "head_dim 128, bf16, relative-position bias", window=2048),
+    # Shared key/value (in-kernel broadcast): candidate query sets of a request attending to
+    # the request's user history, the shape of the cross-attention workload with 64 query sets
+    # per user (the IKBO article's candidate-to-user ratio is about 70).
+    "ikbo_cross": Workload(
+        "ikbo_cross", 8, 1024, 8, 64, torch.bfloat16, "softmax", False, False, 1.0,
+        ("uniform", 1, 64), ("lognormal", 1000, 100, 16384),
+        "1024 candidate query sets, q lengths U{1..64}, 64 per user over 16 users whose histories are "
+        "log-normal in [100,16384] (median 1000), keys/values shared per user, 8 heads, head_dim 64, bf16, "
+        "softmax, non-causal", users=16),
 }
 
 
@@ -115,11 +127,17 @@ def _draw(spec, n, gen) -> np.ndarray:
 
 
 def lengths(w: Workload, seed: Optional[int] = None):
-    """(q_lens, kv_lens) as int64 numpy arrays of size B."""
+    """(q_lens, kv_lens) as int64 numpy arrays: B of each, or with shared key/value B
+    query lengths and `users` user history lengths."""
     gen = torch.Generator().manual_seed(seed_of(w) if seed is None else seed)
     q = _draw(w.q_len, w.B, gen)
-    kv = q.copy() if w.kv_len is None else _draw(w.kv_len, w.B, gen)
+    kv = q.copy() if w.kv_len is None else _draw(w.kv_len, w.B if w.users is None else w.users, gen)
     return q, kv
+
+
+def kv_map_of(w: Workload) -> np.ndarray:
+    """Shared key/value: consecutive blocks of B // users query sets per user."""
+    return (np.arange(w.B) // (w.B // w.users)).astype(np.int32)
 
 
 def offsets(lens) -> np.ndarray:
@@ -150,6 +168,9 @@ class Batch:
     # dense per-pair bias fp32 [H, P], P = sum q_len * kv_len, sequence b's block row-major
     # [q_len, kv_len] from pair_offsets()[b] (used instead of the bucket table), or None
     dense: Optional[torch.Tensor] = None
+    # shared key/value: query set b attends to the rows of user kv_map[b] (kv_off then
+    # runs over the users), or None
+    kv_map: Optional[np.ndarray] = None
 
     @property
     def B(self) -> int:
@@ -161,7 +182,9 @@ class Batch:
 
     @property
     def kv_lens(self) -> np.ndarray:
-        return np.diff(self.kv_off.astype(np.int64))
+        """Key/value length of each sequence (shared key/value: of each query set's user)."""
+        lens = np.diff(self.kv_off.astype(np.int64))
+        return lens if self.kv_map is None else lens[self.kv_map]
 
 
 def _values(shape, std, dtype, gen, device):
@@ -202,14 +225,56 @@ def make_custom(q_lens, kv_lens, *, H, D, dtype=torch.bfloat16, mode="softmax", 
                  dense=dn)
 
 
+def make_shared_kv(q_lens, user_lens, kv_map, *, H, D, dtype=torch.bfloat16, mode="softmax", causal=False,
+                   bias=False, value_std=1.0, seed=BASE_SEED, device="cpu", with_grad=True, name="shared_kv",
+                   window=None, dense_bias=False) -> Batch:
+    """Query sets (q_lens) attending to users' histories (user_lens) through kv_map: the
+    keys and values exist once per user."""
+    q_off, u_off = offsets(q_lens), offsets(user_lens)
+    kv_map = np.ascontiguousarray(np.asarray(kv_map, dtype=np.int32))
+    gen = torch.Generator(device=device).manual_seed(seed + 2000)
+    Q = _values((int(q_off[-1]), H, D), value_std, dtype, gen, device)
+    K = _values((int(u_off[-1]), H, D), value_std, dtype, gen, device)
+    V = _values((int(u_off[-1]), H, D), value_std, dtype, gen, device)
+    dO = _values((int(q_off[-1]), H, D), 1.0, dtype, gen, device) if with_grad else None
+    b = None
+    if bias:
+        b = (torch.randn((H, 32), generator=gen, device=device, dtype=torch.float32) * 0.1)
+    dn = None
+    if dense_bias:  # one block per query set, q_len x its user's kv_len
+        ul = np.diff(u_off.astype(np.int64))
+        P = int(np.sum(np.diff(q_off.astype(np.int64)) * ul[kv_map])) if kv_map.size else 0
+        dn = torch.randn((H, P), generator=gen, device=device, dtype=torch.float32) * 0.5
+    return Batch(name, q_off, u_off, Q, K, V, dO, b, 1.0 / math.sqrt(D), mode, causal, H, D, window=window,
+                 dense=dn, kv_map=kv_map)
+
+
 def make(name: str, device="cpu", with_grad=True, seed: Optional[int] = None) -> Batch:
     """The named workload, seeded."""
     w = WORKLOADS[name]
     s = seed_of(w) if seed is None else seed
     q, kv = lengths(w, s)
+    if w.users is not None:
+        return make_shared_kv(q, kv, kv_map_of(w), H=w.H, D=w.D, dtype=w.dtype, mode=w.mode, causal=w.causal,
+                              bias=w.bias, value_std=w.value_std, seed=s, device=device, with_grad=with_grad,
+                              name=name, window=w.window)
     return make_custom(q, kv, H=w.H, D=w.D, dtype=w.dtype, mode=w.mode, causal=w.causal,
                        bias=w.bias, value_std=w.value_std, seed=s, device=device,
                        with_grad=with_grad, name=name, window=w.window)
+
+
+def broadcast(batch: Batch) -> Batch:
+    """A shared key/value batch with its broadcast made explicit: each query set gets its
+    own copy of its user's key/value rows (the copies the in-kernel broadcast avoids)."""
+    if batch.kv_map is None:
+        return batch
+    rows = [np.arange(batch.kv_off[u], batch.kv_off[u + 1]) for u in batch.kv_map]
+    rows = np.concatenate(rows).astype(np.int64) if rows else np.zeros(0, dtype=np.int64)
+    idx = torch.from_numpy(rows).to(batch.K.device)
+    return Batch(batch.name + "/broadcast", batch.q_off, offsets(batch.kv_lens), batch.Q,
+                 batch.K.index_select(0, idx).contiguous(), batch.V.index_select(0, idx).contiguous(), batch.dO,
+                 batch.bias, batch.scale, batch.mode, batch.causal, batch.H, batch.D, window=batch.window,
+                 dense=batch.dense)
 
 
 def subset(batch: Batch, seqs, heads=None) -> Batch:

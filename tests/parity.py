@@ -57,14 +57,23 @@ def run_oracle(batch, with_backward=True, bias_grads=False):
     Tq, Tkv = int(batch.q_off[-1]), int(batch.kv_off[-1])
     Q, K, V = Q[:Tq], K[:Tkv], V[:Tkv]
     dn = None if getattr(batch, "dense", None) is None else np64(batch.dense)
-    O, LSE = oracle.fwd(batch.q_off, batch.kv_off, Q, K, V, mode=batch.mode, causal=batch.causal,
-                        bias=b, scale=batch.scale, window=batch.window, dense_bias=dn)
+    kv_map = getattr(batch, "kv_map", None)
+    if kv_map is None:
+        fwd, bwd = oracle.fwd, oracle.bwd
+    else:  # shared key/value: the broadcast definition
+        def fwd(q_off, kv_off, *a, **k):
+            return oracle.shared_kv_fwd(q_off, kv_off, kv_map, *a, **k)
+
+        def bwd(q_off, kv_off, *a, **k):
+            return oracle.shared_kv_bwd(q_off, kv_off, kv_map, *a, **k)
+    O, LSE = fwd(batch.q_off, batch.kv_off, Q, K, V, mode=batch.mode, causal=batch.causal,
+                 bias=b, scale=batch.scale, window=batch.window, dense_bias=dn)
     res = {"O": O, "lse": LSE}
     if with_backward:
         dO = np64(batch.dO)[:Tq]
-        g = oracle.bwd(batch.q_off, batch.kv_off, Q, K, V, dO, mode=batch.mode, causal=batch.causal, bias=b,
-                       scale=batch.scale, window=batch.window, bias_grads=bias_grads, dense_grad=dn is not None,
-                       dense_bias=dn)
+        g = bwd(batch.q_off, batch.kv_off, Q, K, V, dO, mode=batch.mode, causal=batch.causal, bias=b,
+                scale=batch.scale, window=batch.window, bias_grads=bias_grads, dense_grad=dn is not None,
+                dense_bias=dn)
         res.update(dQ=g[0], dK=g[1], dV=g[2])
         if bias_grads:
             res["dbias"] = g[3] if dn is None else g[4]
