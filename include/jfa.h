@@ -127,6 +127,12 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
  *   Planning: the forward and dQ passes work per query set, reading its user's rows.
  *   The dK/dV pass works per user key tile over the query tiles of all of that user's
  *   query sets, so dK and dV accumulate on chip and each user row is written once.
+ *   Without causal masking or a window, a row's result does not depend on which query
+ *   set it belongs to, except through the relative-position table.  The plan then
+ *   also holds a merged view: each run of consecutive query sets of one user is one
+ *   query sequence, so short query sets fill whole 128-row tiles.  Calls use it unless
+ *   they pass JFA_BIAS_RELPOS32.  Query sets of a user placed next to each other in Q
+ *   thus share tiles.
  *   jfa_plan_info fact 16 is U.
  *   The other calls take the plan as usual.  jfa_worklist_* and
  *   jfa_partition_sequences describe plain batches only.
@@ -146,8 +152,10 @@ jfa_status jfa_plan_destroy(jfa_plan plan);
  * Plan facts for callers and tests, written to info[0..n): T_q, T_kv, B, H, D,
  * mode, causal, forward work items, forward grid, backward dK/dV work items, its
  * grid, SM count, backward dQ work items, its grid, window (-1: none), P, the number
- * of (query, key) pairs sum_b q_len_b * kv_len_b, and the number of users U of a
- * shared key/value plan (-1 for other plans).  n may be smaller than 17.
+ * of (query, key) pairs sum_b q_len_b * kv_len_b, the number of users U of a
+ * shared key/value plan (-1 for other plans), and the number of merged query sequences
+ * of a shared key/value plan's merged view (-1 when it has none; see
+ * jfa_plan_create_shared_kv).  n may be smaller than 18.
  */
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
 

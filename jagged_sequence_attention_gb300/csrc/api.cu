@@ -104,6 +104,17 @@ jfa_status check_plan_call(jfa_plan plan, int dtype, int bias_kind, const float*
     return JFA_OK;
 }
 
+// The work lists a call runs on.  A shared key/value plan without causal masking or
+// a window also holds a merged view: consecutive query sets of one user form one query
+// sequence, so their rows fill whole 128-row tiles.  A row's result does not depend on
+// which query set it belongs to unless the relative-position table is used (its
+// positions are per query set), so every call but those with JFA_BIAS_RELPOS32 runs on
+// the merged view.  A dense bias keeps its layout: the query sets' consecutive
+// [q_len, kv_len] blocks are the merged sequence's block.
+const jfa_plan_t* work_view(const jfa_plan_t* plan, int32_t bias_kind) {
+    return (plan->merged && bias_kind != JFA_BIAS_RELPOS32) ? plan->merged : plan;
+}
+
 }  // namespace
 
 extern "C" {
@@ -168,7 +179,8 @@ jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, 
 // attends to its own rows.
 static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::vector<int32_t>& ko,
                                    const std::vector<int32_t>* kv_map, int32_t B, int32_t U, int32_t H, int32_t D,
-                                   int32_t mode, int32_t causal, int32_t window, cudaStream_t st, jfa_plan* out) {
+                                   int32_t mode, int32_t causal, int32_t window, cudaStream_t st, jfa_plan* out,
+                                   bool allow_merge = true) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_NO_DEVICE;
     cudaDeviceProp prop;
@@ -285,6 +297,31 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
         delete p;
         return JFA_ERR_CUDA;
     }
+    // Shared key/value without causal masking or a window: also plan the merged view,
+    // runs of consecutive query sets of one user as one query sequence (see work_view).
+    if (allow_merge && kv_map && !causal && window < 0) {
+        std::vector<int32_t> mqo(1, 0), mmap;
+        for (int32_t b = 0; b < B; ++b) {
+            const int32_t u = (*kv_map)[size_t(b)];
+            if (mmap.empty() || mmap.back() != u) {
+                mmap.push_back(u);
+                mqo.push_back(qo[size_t(b) + 1]);
+            } else {
+                mqo.back() = qo[size_t(b) + 1];
+            }
+        }
+        const int32_t M = int32_t(mmap.size());
+        if (M < B) {
+            jfa_plan child = nullptr;
+            const jfa_status s = plan_create_impl(mqo, ko, &mmap, M, U, H, D, mode, causal, window, st, &child, false);
+            if (s != JFA_OK) {
+                cudaFree(p->dev_block);
+                delete p;
+                return s;
+            }
+            p->merged = child;
+        }
+    }
     *out = p;
     return JFA_OK;
 }
@@ -348,6 +385,7 @@ jfa_status jfa_plan_create_shared_kv(const int32_t* q_offsets, int32_t B, const 
 
 jfa_status jfa_plan_destroy(jfa_plan plan) {
     if (!plan) return JFA_OK;
+    if (plan->merged) jfa_plan_destroy(plan->merged);
     for (auto& pr : plan->ev_pending) {
         cudaEventDestroy(pr.second.first);
         cudaEventDestroy(pr.second.second);
@@ -360,11 +398,12 @@ jfa_status jfa_plan_destroy(jfa_plan plan) {
 
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
     if (!plan || !info || n < 0) return JFA_ERR_INVALID_ARG;
-    const int64_t v[17] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
+    const int64_t v[18] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
                            plan->mode,     plan->causal,  plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items,
                            plan->bwd_grid, plan->num_sms, plan->n_dq_items,  plan->dq_grid,  plan->window,
-                           plan->n_pairs,  plan->shared_kv ? plan->U : -1};
-    for (int32_t i = 0; i < n && i < 17; ++i) info[i] = v[i];
+                           plan->n_pairs,  plan->shared_kv ? plan->U : -1,
+                           plan->merged ? int64_t(plan->merged->B) : -1};
+    for (int32_t i = 0; i < n && i < 18; ++i) info[i] = v[i];
     return JFA_OK;
 }
 
@@ -413,6 +452,7 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
                    const float* bias_table, float scale, void* O, int32_t o_dtype, float* lse, void* stream) {
     jfa_status s = check_plan_call(plan, dtype, bias_kind, bias_table);
     if (s != JFA_OK) return s;
+    const jfa_plan_t* v = work_view(plan, bias_kind);  // work lists and offsets
     if (o_dtype != JFA_BF16 && o_dtype != JFA_F32) return JFA_ERR_INVALID_ARG;
     if (dtype == JFA_F32 && o_dtype != JFA_F32) return JFA_ERR_UNSUPPORTED;
     const bool softmax = plan->mode == JFA_SOFTMAX;
@@ -421,7 +461,7 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(bias_table) & 3u))
         return JFA_ERR_INVALID_ARG;
-    if (plan->Tq == 0 || plan->n_fwd_items == 0) return JFA_OK;
+    if (plan->Tq == 0 || v->n_fwd_items == 0) return JFA_OK;
     CUtensorMap mq, mk, mv;
     if (dtype == JFA_BF16 &&
         ((s = make_map(&mq, dtype, Q, plan->Tq, plan->H, plan->D, plan->dev_block)) != JFA_OK ||
@@ -429,10 +469,10 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
          (s = make_map(&mv, dtype, V, plan->Tkv, plan->H, plan->D, plan->dev_block)) != JFA_OK))
         return s;
     FwdParams p;
-    p.items = plan->d_fwd_items;
-    p.cta_off = plan->d_fwd_cta_off;
-    p.q_off = plan->d_q_off;
-    p.kv_off = plan->d_kv_off;
+    p.items = v->d_fwd_items;
+    p.cta_off = v->d_fwd_cta_off;
+    p.q_off = v->d_q_off;
+    p.kv_off = v->d_kv_off;
     p.H = plan->H;
     p.mode = plan->mode;
     p.causal = plan->causal;
@@ -445,14 +485,14 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
     p.status = plan->d_status;
     if (bias_kind == JFA_BIAS_DENSE) {
         p.dense = bias_table;
-        p.pair_off = plan->d_pair_off;
+        p.pair_off = v->d_pair_off;
         p.n_pairs = plan->n_pairs;
     }
-    p.kv_map = plan->d_kv_map;
+    p.kv_map = v->d_kv_map;
     KernelTimer tm(plan, 0, static_cast<cudaStream_t>(stream));
     cudaError_t e = dtype == JFA_BF16
-                        ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, plan->fwd_grid, static_cast<cudaStream_t>(stream))
-                        : launch_fwd_f32(plan->D, Q, K, V, p, plan->n_fwd_items, static_cast<cudaStream_t>(stream));
+                        ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, v->fwd_grid, static_cast<cudaStream_t>(stream))
+                        : launch_fwd_f32(plan->D, Q, K, V, p, v->n_fwd_items, static_cast<cudaStream_t>(stream));
     tm.done();
     return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
@@ -508,6 +548,7 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
                            void* workspace, size_t workspace_bytes, void* stream) {
     jfa_status s = check_plan_call(plan, dtype, bias_kind, bias_table);
     if (s != JFA_OK) return s;
+    const jfa_plan_t* v = work_view(plan, bias_kind);  // work lists and offsets
     if (o_dtype != JFA_BF16 && o_dtype != JFA_F32) return JFA_ERR_INVALID_ARG;
     if (dtype == JFA_F32 && o_dtype != JFA_F32) return JFA_ERR_UNSUPPORTED;
     const bool softmax = plan->mode == JFA_SOFTMAX;
@@ -522,12 +563,12 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
     if (workspace_bytes < need || (need > 0 && !workspace)) return JFA_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool dense = bias_kind == JFA_BIAS_DENSE;
-    if (dbias && (plan->n_bwd_items == 0 || (dense && (plan->causal || plan->window >= 0)))) {
+    if (dbias && (v->n_bwd_items == 0 || (dense && (plan->causal || plan->window >= 0)))) {
         // The kernels write the gradient of allowed pairs only: zero it first where some
         // pair is masked (dense), or everywhere when no key tile sees a query.
         const size_t n = dense ? size_t(plan->H) * size_t(plan->n_pairs) : size_t(plan->H) * 32;
         if (n > 0 && cudaMemsetAsync(dbias, 0, n * 4, st) != cudaSuccess) return JFA_ERR_CUDA;
-        if (plan->n_bwd_items == 0) dbias = nullptr;
+        if (v->n_bwd_items == 0) dbias = nullptr;
     }
     if (plan->Tkv == 0 && plan->Tq == 0) return JFA_OK;
     const size_t rows = size_t(plan->Tq) * size_t(plan->H);
@@ -545,17 +586,17 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
     }
     CUtensorMap mq, mk, mv, mdo;
     BwdParams p;
-    if (plan->n_bwd_items > 0 || (dtype == JFA_BF16 && plan->n_dq_items > 0)) {
+    if (v->n_bwd_items > 0 || (dtype == JFA_BF16 && v->n_dq_items > 0)) {
         if (dtype == JFA_BF16 &&
             ((s = make_map(&mq, dtype, Q, plan->Tq, plan->H, plan->D, plan->dev_block, kBwdBM)) != JFA_OK ||
              (s = make_map(&mk, dtype, K, plan->Tkv, plan->H, plan->D, plan->dev_block, kBwdBN)) != JFA_OK ||
              (s = make_map(&mv, dtype, V, plan->Tkv, plan->H, plan->D, plan->dev_block, kBwdBN)) != JFA_OK ||
              (s = make_map(&mdo, dtype, dO, plan->Tq, plan->H, plan->D, plan->dev_block, kBwdBM)) != JFA_OK))
             return s;
-        p.items = plan->d_bwd_items;
-        p.cta_off = plan->d_bwd_cta_off;
-        p.q_off = plan->d_q_off;
-        p.kv_off = plan->d_kv_off;
+        p.items = v->d_bwd_items;
+        p.cta_off = v->d_bwd_cta_off;
+        p.q_off = v->d_q_off;
+        p.kv_off = v->d_kv_off;
         p.H = plan->H;
         p.mode = plan->mode;
         p.causal = plan->causal;
@@ -575,36 +616,36 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
             p.bias = nullptr;
             p.dense = bias_table;
             p.ddense = dbias;
-            p.pair_off = plan->d_pair_off;
+            p.pair_off = v->d_pair_off;
             p.n_pairs = plan->n_pairs;
         }
         // shared key/value: the dK/dV pass walks the user's step lists, the dQ pass maps
-        p.steps = plan->d_steps;
-        p.step_off = plan->d_step_off;
-        p.ktile_off = plan->d_ktile_off;
+        p.steps = v->d_steps;
+        p.step_off = v->d_step_off;
+        p.ktile_off = v->d_ktile_off;
     }
-    if (plan->n_bwd_items > 0) {
+    if (v->n_bwd_items > 0) {
         KernelTimer tm(plan, 2, st);
-        e = dtype == JFA_BF16 ? launch_bwd_main(dtype, plan->D, mq, mk, mv, mdo, p, plan->bwd_grid, st)
-                              : launch_bwd_f32(plan->D, Q, K, V, dO, p, plan->n_bwd_items, st);
+        e = dtype == JFA_BF16 ? launch_bwd_main(dtype, plan->D, mq, mk, mv, mdo, p, v->bwd_grid, st)
+                              : launch_bwd_f32(plan->D, Q, K, V, dO, p, v->n_bwd_items, st);
         tm.done();
         if (e != cudaSuccess) return JFA_ERR_CUDA;
         if (dbias_part) {
             e = dtype == JFA_BF16
-                    ? launch_dbias_reduce(dbias_part, int64_t(plan->bwd_grid) * kDkdvCompWarps, plan->H, dbias, st)
-                    : launch_dbias_reduce_items(dbias_part, plan->d_bwd_items, plan->n_bwd_items, plan->H, dbias, st);
+                    ? launch_dbias_reduce(dbias_part, int64_t(v->bwd_grid) * kDkdvCompWarps, plan->H, dbias, st)
+                    : launch_dbias_reduce_items(dbias_part, v->d_bwd_items, v->n_bwd_items, plan->H, dbias, st);
             if (e != cudaSuccess) return JFA_ERR_CUDA;
         }
         p.dbias_part = nullptr;  // the dQ pass does not take part
     }
-    if (dtype == JFA_BF16 && plan->n_dq_items > 0) {
+    if (dtype == JFA_BF16 && v->n_dq_items > 0) {
         // dQ per query tile, written directly (also the zero rows of tiles that see no key)
-        p.items = plan->d_dq_items;
-        p.cta_off = plan->d_dq_cta_off;
-        p.kv_map = plan->d_kv_map;
+        p.items = v->d_dq_items;
+        p.cta_off = v->d_dq_cta_off;
+        p.kv_map = v->d_kv_map;
         p.steps = nullptr;
         KernelTimer tm(plan, 4, st);
-        e = launch_bwd_dq(dtype, plan->D, mq, mk, mv, mdo, p, plan->dq_grid, st);
+        e = launch_bwd_dq(dtype, plan->D, mq, mk, mv, mdo, p, v->dq_grid, st);
         tm.done();
         if (e != cudaSuccess) return JFA_ERR_CUDA;
     }

@@ -254,6 +254,9 @@ struct jfa_plan_t {
     int32_t* d_step_off;
     int32_t* d_ktile_off;
     int64_t n_steps;
+    // shared key/value without causal masking or a window: the merged view (runs of
+    // consecutive query sets of one user as one query sequence), owned by this plan
+    jfa_plan_t* merged = nullptr;
     int64_t n_fwd_items, n_bwd_items, n_dq_items;
     int fwd_grid, bwd_grid, dq_grid;
     // optional per-kernel timing (jfa_plan_set_timing)

@@ -133,3 +133,44 @@ def test_argument_errors():
     with pytest.raises(jfa.JFAError) as e:   # a window without causal
         jfa.jfa_plan_create_shared_kv([0, 5], [0, 10], [0], 2, 128, window=3)
     assert e.value.status == jfa.JFA_ERR_INVALID_ARG
+
+
+def request_batch(seed, n_users=5, per_user=12, **kw):
+    """Query sets of a user next to each other in Q (a request's candidates), so that
+    the merged view packs them into shared tiles."""
+    g = np.random.default_rng(seed)
+    users = g.integers(100, 1500, size=n_users).tolist()
+    kv_map = np.repeat(np.arange(n_users), per_user)
+    q = g.integers(1, 65, size=kv_map.size).tolist()
+    return wl.make_shared_kv(q, users, kv_map, seed=seed, device="cuda", **kw)
+
+
+@pytest.mark.parametrize("mode", ["softmax", "silu"])
+def test_merged_view(mode):
+    from jagged_sequence_attention_gb300 import jfa
+    b = request_batch(90, H=2, D=128, mode=mode, value_std=1.0 if mode == "softmax" else 0.5)
+    out, _ = check(b)
+    info = jfa.jfa_plan_info(out["plan"])
+    assert info["merged"] == 5            # one query sequence per user
+
+
+def test_merged_view_with_dense_bias():
+    check(request_batch(91, H=2, D=64, dense_bias=True), bias_grad=True)
+
+
+def test_merged_and_per_set_views_agree():
+    # a zero relative-position table changes nothing but forces the per-set view
+    from jagged_sequence_attention_gb300 import jfa
+    b = request_batch(92, H=2, D=128)
+    plan = jfa.plan_for(b)
+    zero = torch.zeros((b.H, 32), dtype=torch.float32, device="cuda")
+    O1, lse1 = jfa.jfa_fwd(plan, b.Q, b.K, b.V, None, b.scale, out_dtype=torch.float32)
+    O2, lse2 = jfa.jfa_fwd(plan, b.Q, b.K, b.V, zero, b.scale, out_dtype=torch.float32)
+    g1 = jfa.jfa_bwd(plan, b.Q, b.K, b.V, O1, b.dO, lse1, None, b.scale)
+    g2 = jfa.jfa_bwd(plan, b.Q, b.K, b.V, O2, b.dO, lse2, zero, b.scale)
+    torch.cuda.synchronize()
+    assert jfa.jfa_plan_device_status(plan) == 0
+    assert float((O1 - O2).abs().max()) <= 2 * parity.FWD_MAX_ABS
+    assert float((lse1 - lse2).abs().max()) <= 2 * parity.LSE_MAX_ABS
+    for x, y in zip(g1, g2):
+        assert float((x.float() - y.float()).norm() / y.float().norm()) <= 2 * parity.BWD_REL_FROB
