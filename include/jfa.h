@@ -135,7 +135,8 @@ jfa_status jfa_plan_create_ex(const int32_t* q_offsets, const int32_t* kv_offset
  *   thus share tiles.
  *   jfa_plan_info fact 16 is U.
  *   The other calls take the plan as usual.  jfa_worklist_* and
- *   jfa_partition_sequences describe plain batches only.
+ *   jfa_partition_sequences describe plain batches only; jfa_partition_users splits a
+ *   shared key/value batch.
  * Errors: INVALID_ARG for bad offsets or an index outside [0, U); otherwise those of
  * jfa_plan_create_ex.
  */
@@ -296,6 +297,21 @@ jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offset
 jfa_status jfa_partition_sequences(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
                                    int32_t H, int32_t causal, int32_t window, int32_t n_parts,
                                    int32_t* part_of_seq, int64_t* part_cost);
+
+/*
+ * jfa_partition_sequences for a shared key/value batch (jfa_plan_create_shared_kv):
+ * users, each with all of its query sets, split over n_parts GPUs by greedy LPT on
+ * their cost, the cost of their query sets plus their key tiles.  A user's dK and dV sum
+ * over its query sets, so keeping them together means no GPU exchanges anything.
+ *   Host arrays: q_offsets int32[B+1], kv_offsets int32[U+1], kv_index int32[B].
+ *   part_of_user: int32[U] out, each in [0, n_parts); part_cost: int64[n_parts] out
+ *   (may be NULL).  Deterministic.
+ * Errors: INVALID_ARG for bad offsets or sizes, or an index outside [0, U).
+ */
+jfa_status jfa_partition_users(const int32_t* q_offsets, int32_t B, const int32_t* kv_offsets,
+                               int32_t U, const int32_t* kv_index, int32_t H, int32_t causal,
+                               int32_t window, int32_t n_parts, int32_t* part_of_user,
+                               int64_t* part_cost);
 
 /* Kernel timing for measurement.  With timing enabled, every kernel launch made for
  * this plan is bracketed by a pair of CUDA events recorded on the launch stream.

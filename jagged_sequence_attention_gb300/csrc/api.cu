@@ -169,6 +169,22 @@ jfa_status jfa_partition_sequences(const int32_t* q_offsets, const int32_t* kv_o
     return JFA_OK;
 }
 
+jfa_status jfa_partition_users(const int32_t* q_offsets, int32_t B, const int32_t* kv_offsets, int32_t U,
+                               const int32_t* kv_index, int32_t H, int32_t causal, int32_t window, int32_t n_parts,
+                               int32_t* part_of_user, int64_t* part_cost) {
+    if (!q_offsets || !kv_offsets || (B > 0 && !kv_index) || B < 0 || U < 0 || H < 1 || n_parts < 1 ||
+        (causal != 0 && causal != 1) || (U > 0 && !part_of_user))
+        return JFA_ERR_INVALID_ARG;
+    if (window < -1 || (window >= 0 && causal != 1)) return JFA_ERR_INVALID_ARG;
+    if (q_offsets[0] != 0 || kv_offsets[0] != 0) return JFA_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < B; ++b)
+        if (q_offsets[b + 1] < q_offsets[b] || kv_index[b] < 0 || kv_index[b] >= U) return JFA_ERR_INVALID_ARG;
+    for (int32_t u = 0; u < U; ++u)
+        if (kv_offsets[u + 1] < kv_offsets[u]) return JFA_ERR_INVALID_ARG;
+    partition_users(q_offsets, kv_offsets, kv_index, B, U, H, causal, window, n_parts, part_of_user, part_cost);
+    return JFA_OK;
+}
+
 jfa_status jfa_plan_create(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H, int32_t D,
                            int32_t mode, int32_t causal, int32_t offsets_on_device, void* stream, jfa_plan* out) {
     return jfa_plan_create_ex(q_offsets, kv_offsets, B, H, D, mode, causal, -1, offsets_on_device, stream, out);

@@ -196,6 +196,9 @@ void build_shared_kv_dkdv(const int32_t* q_off, const int32_t* u_off, const int3
 int64_t count_shared_kv_dkdv_items(const int32_t* u_off, int32_t U, int32_t H);
 
 int64_t sequence_cost(int64_t q_len, int64_t kv_len, int32_t H, int32_t causal, int32_t window);
+void partition_users(const int32_t* q_off, const int32_t* u_off, const int32_t* kv_index, int32_t B, int32_t U,
+                     int32_t H, int32_t causal, int32_t window, int32_t n_parts, int32_t* part_of_user,
+                     int64_t* part_cost);
 void partition_sequences(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H, int32_t causal,
                          int32_t window, int32_t n_parts, int32_t* part_of_seq, int64_t* part_cost);
 

@@ -232,4 +232,43 @@ void partition_sequences(const int32_t* q_off, const int32_t* kv_off, int32_t B,
         for (int32_t c = 0; c < n_parts; ++c) part_cost[c] = load[size_t(c)];
 }
 
+// Shared key/value batches split by user: a user's query sets all go with it, so each
+// user's dK and dV are summed on one GPU and no exchange is needed.  A user's cost is
+// that of its query sets (as above, with the user's key/value length) plus the zero
+// rows of its key tiles; greedy LPT as above.
+void partition_users(const int32_t* q_off, const int32_t* u_off, const int32_t* kv_index, int32_t B, int32_t U,
+                     int32_t H, int32_t causal, int32_t window, int32_t n_parts, int32_t* part_of_user,
+                     int64_t* part_cost) {
+    std::vector<int64_t> cost(size_t(U > 0 ? U : 0), 0);
+    for (int32_t u = 0; u < U; ++u) cost[size_t(u)] = int64_t(H) * 2 * ceil_div(u_off[u + 1] - u_off[u], kBwdBN);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t u = kv_index[b];
+        const int64_t q_len = q_off[b + 1] - q_off[b], kv_len = u_off[u + 1] - u_off[u];
+        const int64_t nq = ceil_div(q_len, kFwdBM);
+        int64_t tiles = 0;
+        for (int64_t t = 0; t < nq; ++t) tiles += fwd_tiles_of(q_len, kv_len, t, causal, window);
+        cost[size_t(u)] += int64_t(H) * (9 * tiles + 2 * nq);
+    }
+    std::vector<std::pair<int64_t, int32_t>> order(size_t(U > 0 ? U : 0));
+    for (int32_t u = 0; u < U; ++u) order[size_t(u)] = {cost[size_t(u)], u};
+    std::stable_sort(order.begin(), order.end(),
+                     [](const std::pair<int64_t, int32_t>& a, const std::pair<int64_t, int32_t>& b) {
+                         return a.first > b.first;
+                     });
+    using Slot = std::pair<int64_t, int32_t>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int32_t c = 0; c < n_parts; ++c) heap.push({0, c});
+    std::vector<int64_t> load(size_t(n_parts), 0);
+    for (const auto& o : order) {
+        Slot sl = heap.top();
+        heap.pop();
+        part_of_user[o.second] = sl.second;
+        sl.first += o.first;
+        load[size_t(sl.second)] = sl.first;
+        heap.push(sl);
+    }
+    if (part_cost)
+        for (int32_t c = 0; c < n_parts; ++c) part_cost[c] = load[size_t(c)];
+}
+
 }  // namespace jfa

@@ -31,7 +31,8 @@ DTYPES = {torch.bfloat16: JFA_BF16, torch.float32: JFA_F32}
 EXPORTED = ["jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd_workspace_size",
             "jfa_bwd", "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build",
             "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times", "jfa_bwd_static_scratch",
-            "jfa_partition_sequences", "jfa_bwd_ex_workspace_size", "jfa_bwd_ex", "jfa_plan_create_shared_kv"]
+            "jfa_partition_sequences", "jfa_bwd_ex_workspace_size", "jfa_bwd_ex", "jfa_plan_create_shared_kv",
+            "jfa_partition_users"]
 
 
 class JFAError(RuntimeError):
@@ -67,6 +68,7 @@ def lib():
         L.jfa_bwd_static_scratch.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp]
         L.jfa_plan_device_status.argtypes = [vp, vp]
         L.jfa_partition_sequences.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp]
+        L.jfa_partition_users.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp]
         L.jfa_worklist_size.argtypes = [vp, vp, i32, i32, i32, i32, i32, P(i64)]
         L.jfa_worklist_build.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
         L.jfa_plan_set_timing.argtypes = [vp, i32]
@@ -76,7 +78,7 @@ def lib():
         for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
                      "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build", "jfa_plan_set_timing",
                      "jfa_plan_kernel_times", "jfa_bwd_static_scratch", "jfa_partition_sequences", "jfa_bwd_ex",
-                     "jfa_plan_create_shared_kv"):
+                     "jfa_plan_create_shared_kv", "jfa_partition_users"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -331,13 +333,30 @@ def jfa_partition_sequences(q_offsets, kv_offsets, H: int, causal: bool, n_parts
     return part[:B], cost
 
 
+def jfa_partition_users(q_offsets, kv_offsets, kv_index, H: int, causal: bool, n_parts: int, window=None):
+    """Host LPT split of a shared key/value batch's users (with all their query sets) over
+    n_parts GPUs.  Returns (part_of_user int32 [U], part_cost int64 [n_parts])."""
+    qo, ko, ki = _i32(q_offsets), _i32(kv_offsets), _i32(kv_index)
+    B, U = qo.size - 1, ko.size - 1
+    part = np.zeros(max(U, 1), dtype=np.int32)
+    cost = np.zeros(int(n_parts), dtype=np.int64)
+    vp = ctypes.c_void_p
+    _check("jfa_partition_users", lib().jfa_partition_users(
+        qo.ctypes.data_as(vp), int(B), ko.ctypes.data_as(vp), int(U), ki.ctypes.data_as(vp), int(H),
+        int(bool(causal)), _win(window), int(n_parts), part.ctypes.data_as(vp), cost.ctypes.data_as(vp)))
+    return part[:U], cost
+
+
 def shard(batch, rank: int, world: int):
-    """The sequences of `batch` that rank `rank` of `world` processes (a workloads.Batch
-    subset, repacked), by the LPT split above.  Sequences are independent, so results of
-    the shards are exactly the full batch's results for those sequences."""
+    """The part of `batch` that rank `rank` of `world` processes (a workloads.Batch,
+    repacked), by the LPT splits above: sequences, or for a shared key/value batch users
+    with all their query sets.  The parts are independent, so their results are exactly
+    the full batch's results for those sequences (users)."""
     from . import workloads
     if getattr(batch, "kv_map", None) is not None:
-        raise JFAError("shard (shared key/value batches are split by user, not built)", JFA_ERR_UNSUPPORTED)
+        part, _ = jfa_partition_users(batch.q_off, batch.kv_off, batch.kv_map, batch.H, batch.causal, world,
+                                      window=getattr(batch, "window", None))
+        return workloads.subset_users(batch, np.nonzero(part == rank)[0])
     part, _ = jfa_partition_sequences(batch.q_off, batch.kv_off, batch.H, batch.causal, world,
                                       window=getattr(batch, "window", None))
     seqs = np.nonzero(part == rank)[0]

@@ -277,6 +277,36 @@ def broadcast(batch: Batch) -> Batch:
                  dense=batch.dense)
 
 
+def subset_users(batch: Batch, users) -> Batch:
+    """Users of a shared key/value batch with all their query sets, repacked: users
+    renumbered in the given order, query sets kept in batch order.  extra records the
+    original users ("users") and query sets ("seqs")."""
+    users = [int(u) for u in users]
+    new_id = {u: i for i, u in enumerate(users)}
+    seqs = [b for b in range(batch.B) if int(batch.kv_map[b]) in new_id]
+    qi = [torch.arange(int(batch.q_off[s]), int(batch.q_off[s + 1])) for s in seqs]
+    ki = [torch.arange(int(batch.kv_off[u]), int(batch.kv_off[u + 1])) for u in users]
+    qi = torch.cat(qi) if qi else torch.zeros(0, dtype=torch.long)
+    ki = torch.cat(ki) if ki else torch.zeros(0, dtype=torch.long)
+
+    def take(t, idx):
+        return None if t is None else t.index_select(0, idx.to(t.device)).contiguous()
+
+    dn = None
+    if batch.dense is not None:
+        lens = np.diff(batch.q_off.astype(np.int64)) * batch.kv_lens
+        po = np.concatenate([[0], np.cumsum(lens)])
+        blocks = [batch.dense[:, int(po[s]):int(po[s + 1])] for s in seqs]
+        dn = torch.cat(blocks, dim=1).contiguous() if blocks else batch.dense[:, :0].contiguous()
+    ulens = np.diff(batch.kv_off.astype(np.int64))[users] if users else np.zeros(0, dtype=np.int64)
+    sub = Batch(batch.name + "/users", offsets(batch.q_lens[seqs]), offsets(ulens), take(batch.Q, qi),
+                take(batch.K, ki), take(batch.V, ki), take(batch.dO, qi), batch.bias, batch.scale, batch.mode,
+                batch.causal, batch.H, batch.D, window=batch.window, dense=dn,
+                kv_map=np.asarray([new_id[int(batch.kv_map[s])] for s in seqs], dtype=np.int32))
+    sub.extra.update(users=users, seqs=seqs, q_index=qi, kv_index=ki)
+    return sub
+
+
 def subset(batch: Batch, seqs, heads=None) -> Batch:
     """Independent sequences (and optionally heads) of a batch, repacked; a sequence's
     result does not depend on the others, so the oracle can check a sample this way."""

@@ -156,3 +156,93 @@ def test_two_ranks_over_gloo_reproduce_the_full_batch(jfa, tmp_path):
     oracle.build()
     mp.spawn(_rank_main, args=(2, _free_port(), str(tmp_path)), nprocs=2, join=True)
     assert (tmp_path / "ok").exists()
+
+
+# ------------------------------------------------------------ shared key/value: split by user
+
+
+def shared_case(seed=5):
+    g = np.random.default_rng(seed)
+    users = g.integers(50, 700, size=7).tolist()
+    kv_map = g.integers(0, 6, size=30)            # user 6 has no query set
+    q = g.integers(0, 200, size=30).tolist()
+    return q, users, kv_map
+
+
+@pytest.mark.parametrize("n_parts", [1, 2, 3])
+def test_partition_users_covers_and_balances(jfa, n_parts):
+    q, users, kv_map = shared_case()
+    H = 2
+    part, cost = jfa.jfa_partition_users(wl.offsets(q), wl.offsets(users), kv_map, H, False, n_parts)
+    assert part.shape == (len(users),) and np.all((part >= 0) & (part < n_parts))
+    ucost = np.array([H * 2 * ((L + BN - 1) // BN) for L in users], dtype=np.int64)
+    for b, u in enumerate(kv_map):
+        nq = (q[b] + BM - 1) // BM
+        ucost[u] += H * (9 * tiles_visited(q[b], users[u], False) + 2 * nq)
+    for c in range(n_parts):
+        assert cost[c] == ucost[part == c].sum()
+    assert cost.max() - cost.min() <= ucost.max()
+
+
+def test_shard_of_a_shared_batch_keeps_users_whole(jfa):
+    q, users, kv_map = shared_case()
+    b = wl.make_shared_kv(q, users, kv_map, H=2, D=32, dtype=torch.float32)
+    seen_users, seen_seqs = [], []
+    for r in range(3):
+        sub = jfa.shard(b, r, 3)
+        seen_users += sub.extra["users"]
+        seen_seqs += sub.extra["seqs"]
+        # every query set of a kept user is kept, mapped to its renumbered user
+        for i, s in enumerate(sub.extra["seqs"]):
+            assert sub.extra["users"][sub.kv_map[i]] == kv_map[s]
+    assert sorted(seen_users) == list(range(len(users)))
+    assert sorted(seen_seqs) == list(range(len(q)))
+
+
+def _rank_main_shared(rank, world, port, out_dir):
+    # Each rank: its users (with all their query sets) of one seeded shared key/value
+    # batch, forward + backward with the CPU oracle standing in for its GPU; rank 0
+    # checks every query set's O, dQ and every user's dK, dV against the full batch.
+    import oracle
+    from jagged_sequence_attention_gb300 import jfa
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        q, users, kv_map = shared_case(6)
+        b = wl.make_shared_kv(q, users, kv_map, H=2, D=16, dtype=torch.float32, bias=True, seed=77)
+        sub = jfa.shard(b, rank, world)
+
+        def run(batch):
+            Q, K, V, dO = (t.double().numpy() for t in (batch.Q, batch.K, batch.V, batch.dO))
+            kw = dict(bias=batch.bias.double().numpy(), scale=batch.scale)
+            O, _ = oracle.shared_kv_fwd(batch.q_off, batch.kv_off, batch.kv_map, Q, K, V, **kw)
+            dQ, dK, dV = oracle.shared_kv_bwd(batch.q_off, batch.kv_off, batch.kv_map, Q, K, V, dO, **kw)
+            return O, dQ, dK, dV
+
+        mine = run(sub)
+        gathered = [None] * world
+        dist.all_gather_object(gathered, {"users": list(sub.extra["users"]), "seqs": list(sub.extra["seqs"]),
+                                          "q_off": sub.q_off.tolist(), "kv_off": sub.kv_off.tolist(),
+                                          "out": [a.tolist() for a in mine]})
+        if rank == 0:
+            full = run(b)
+            for g in gathered:
+                O, dQ, dK, dV = (np.asarray(a) for a in g["out"])
+                for k, s in enumerate(g["seqs"]):
+                    lo, hi = int(b.q_off[s]), int(b.q_off[s + 1])
+                    assert np.array_equal(O[g["q_off"][k]:g["q_off"][k + 1]], full[0][lo:hi])
+                    assert np.array_equal(dQ[g["q_off"][k]:g["q_off"][k + 1]], full[1][lo:hi])
+                for k, u in enumerate(g["users"]):
+                    lo, hi = int(b.kv_off[u]), int(b.kv_off[u + 1])
+                    assert np.array_equal(dK[g["kv_off"][k]:g["kv_off"][k + 1]], full[2][lo:hi])
+                    assert np.array_equal(dV[g["kv_off"][k]:g["kv_off"][k + 1]], full[3][lo:hi])
+            open(os.path.join(out_dir, "ok"), "w").write("ok")
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_over_gloo_reproduce_a_shared_batch(jfa, tmp_path):
+    import oracle
+    oracle.build()
+    mp.spawn(_rank_main_shared, args=(2, _free_port(), str(tmp_path)), nprocs=2, join=True)
+    assert (tmp_path / "ok").exists()
