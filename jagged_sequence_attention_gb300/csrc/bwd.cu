@@ -639,6 +639,7 @@ __global__ void __launch_bounds__(320, 1)
                         tmem_ld_wait(ra);
                     }
                     uint32_t pd[16];
+                    float2 cs = make_float2(0.f, 0.f);  // the chunk's dS sum (DBIAS)
                     if (softmax) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 4) {
@@ -656,6 +657,7 @@ __global__ void __launch_bounds__(320, 1)
                                 dp[c + 2] = b2.x;
                                 dp[c + 3] = b2.y;
                             }
+                            if constexpr (DBIAS) cs = add2(cs, add2(a, b2));
                         }
                     } else {
 #pragma unroll
@@ -667,6 +669,7 @@ __global__ void __launch_bounds__(320, 1)
                                 dp[c] = a.x;
                                 dp[c + 1] = a.y;
                             }
+                            if constexpr (DBIAS) cs = add2(cs, a);
                         }
                     }
                     tmem_st16(tY + 16u * k, pd);
@@ -687,14 +690,11 @@ __global__ void __launch_bounds__(320, 1)
                     if constexpr (DBIAS) {
                         // Table gradient of this chunk (dS is exactly 0 at masked pairs).
                         if (cconst[k]) {
-                            float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                            for (int c = 0; c < 32; ++c) s4[c & 3] += dp[c];
                             if (cbk[k] != dtag[k]) {
                                 dflush(k);
                                 dtag[k] = cbk[k];
                             }
-                            dacc[k] += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                            dacc[k] += cs.x + cs.y;
                         } else {
                             // Element (lane l, column c) lies on diagonal d = c - l + 31 of the
                             // chunk, relative position rlo + d.  Lane m gathers diagonals m and
