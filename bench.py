@@ -225,7 +225,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_causal", choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -390,6 +390,12 @@ def main():
 
     # ---------------------------------------------------------------- end to end through the API
     if not args.no_e2e:
+        # Every step: pinned host -> device copies of its inputs (Q, K, V, dO, bias), a new plan
+        # from the host offsets, jfa_fwd, jfa_bwd, and device -> host copies of all its results
+        # (O, lse, dQ, dK, dV).  Steps are pipelined as a training loop prefetches its next
+        # batch: two device buffer sets, inputs copied in on one stream and results copied out
+        # on another while the kernels of the neighbouring step run.  All copies are inside the
+        # timed region.  The same loop run serially (one step at a time) is reported beside it.
         pin = lambda t: t.cpu().pin_memory()  # noqa: E731
         hQ, hK, hV, hdO = pin(batch.Q), pin(batch.K), pin(batch.V), pin(batch.dO)
         hbias = None if batch.bias is None else pin(batch.bias)
@@ -397,46 +403,90 @@ def main():
         hdK, hdV = torch.empty_like(hK).pin_memory(), torch.empty_like(hV).pin_memory()
         hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
         q_off, kv_off = batch.q_off.copy(), batch.kv_off.copy()
-        dQd, dKd, dVd, dOd = batch.Q, batch.K, batch.V, batch.dO
-        bias_d = batch.bias
+        sets = []
+        for k in range(2):
+            sets.append({
+                "Q": batch.Q if k == 0 else torch.empty_like(batch.Q),
+                "K": batch.K if k == 0 else torch.empty_like(batch.K),
+                "V": batch.V if k == 0 else torch.empty_like(batch.V),
+                "dO": batch.dO if k == 0 else torch.empty_like(batch.dO),
+                "bias": None if batch.bias is None else (batch.bias if k == 0 else torch.empty_like(batch.bias)),
+                "O": O if k == 0 else torch.empty_like(O), "lse": lse if k == 0 else torch.empty_like(lse),
+                "dQ": dQ if k == 0 else torch.empty_like(dQ), "dK": dK if k == 0 else torch.empty_like(dK),
+                "dV": dV if k == 0 else torch.empty_like(dV), "ws": ws if k == 0 else torch.empty_like(ws),
+                "freed": torch.cuda.Event()})
+            sets[k]["freed"].record(stream)
+        # plan creation synchronises the stream it is given (the work-list upload): its own
+        s_in, s_out, s_plan = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
         h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hdO)) + (
             0 if hbias is None else hbias.numel() * 4) + q_off.nbytes + kv_off.nbytes
         d2h = sum(t.numel() * t.element_size() for t in (hO, hdQ, hdK, hdV, hlse))
 
-        def e2e_step():
-            dQd.copy_(hQ, non_blocking=True)
-            dKd.copy_(hK, non_blocking=True)
-            dVd.copy_(hV, non_blocking=True)
-            dOd.copy_(hdO, non_blocking=True)
-            if hbias is not None:
-                bias_d.copy_(hbias, non_blocking=True)
-            p2 = jfa.plan_for(wl.Batch(batch.name, q_off, kv_off, dQd, dKd, dVd, dOd, bias_d, batch.scale, batch.mode,
-                                       batch.causal, batch.H, batch.D, window=batch.window, kv_map=batch.kv_map))
-            jfa.jfa_fwd(p2, dQd, dKd, dVd, bias_d, batch.scale, O=O, lse=lse)
-            jfa.jfa_bwd(p2, dQd, dKd, dVd, O, dOd, lse, bias_d, batch.scale, dQ=dQ, dK=dK, dV=dV, workspace=ws)
-            hO.copy_(O, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
-            hdQ.copy_(dQ, non_blocking=True)
-            hdK.copy_(dK, non_blocking=True)
-            hdV.copy_(dV, non_blocking=True)
-            torch.cuda.synchronize()
-            jfa.jfa_plan_destroy(p2)
+        def e2e_step(i, plans):
+            b = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(b["freed"])  # the set's previous step has copied its results out
+                for name, h in (("Q", hQ), ("K", hK), ("V", hV), ("bias", hbias)):
+                    if h is not None:
+                        b[name].copy_(h, non_blocking=True)
+                ev_qkv = torch.cuda.Event()
+                ev_qkv.record(s_in)
+                b["dO"].copy_(hdO, non_blocking=True)
+                ev_do = torch.cuda.Event()
+                ev_do.record(s_in)
+            p2 = jfa.plan_for(wl.Batch(batch.name, q_off, kv_off, b["Q"], b["K"], b["V"], b["dO"], b["bias"],
+                                       batch.scale, batch.mode, batch.causal, batch.H, batch.D,
+                                       window=batch.window, kv_map=batch.kv_map), stream=s_plan)
+            plans.append(p2)
+            stream.wait_event(ev_qkv)
+            jfa.jfa_fwd(p2, b["Q"], b["K"], b["V"], b["bias"], batch.scale, O=b["O"], lse=b["lse"], stream=stream)
+            ev_fwd = torch.cuda.Event()
+            ev_fwd.record(stream)
+            stream.wait_event(ev_do)
+            jfa.jfa_bwd(p2, b["Q"], b["K"], b["V"], b["O"], b["dO"], b["lse"], b["bias"], batch.scale, dQ=b["dQ"],
+                        dK=b["dK"], dV=b["dV"], workspace=b["ws"], stream=stream)
+            ev_bwd = torch.cuda.Event()
+            ev_bwd.record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_fwd)
+                hO.copy_(b["O"], non_blocking=True)
+                hlse.copy_(b["lse"], non_blocking=True)
+                s_out.wait_event(ev_bwd)
+                hdQ.copy_(b["dQ"], non_blocking=True)
+                hdK.copy_(b["dK"], non_blocking=True)
+                hdV.copy_(b["dV"], non_blocking=True)
+                b["freed"].record(s_out)
 
-        e2e_step()
-        if dist:
-            dist.barrier()
-        t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        el = (time.perf_counter() - t0) / args.e2e_steps
-        if dist:
-            t = torch.tensor([el], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            el = float(t.item())
+        def timed(n_steps, serial):
+            plans = []
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            t0 = time.perf_counter()
+            for i in range(n_steps):
+                e2e_step(i, plans)
+                if serial:
+                    torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            el = (time.perf_counter() - t0) / n_steps
+            for p2 in plans:  # freeing device memory synchronises the device: after the timed loop
+                jfa.jfa_plan_destroy(p2)
+            if dist:
+                t = torch.tensor([el], dtype=torch.float64, device=dev)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                el = float(t.item())
+            return el
+
+        timed(2, False)  # warm-up of both buffer sets and streams
+        el = timed(args.e2e_steps, False)
+        el_serial = timed(max(1, args.e2e_steps // 2), True)
         line["e2e"] = {"value": job_flop / el / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                        "d2h_bytes_per_step": int(d2h), "ms_per_step": el * 1e3, "steps": args.e2e_steps,
-                       "includes": "pinned H2D of Q,K,V,dO,bias,offsets; jfa_plan_create; jfa_fwd; jfa_bwd; "
-                                   "D2H of O,lse,dQ,dK,dV"}
+                       "serial_value": job_flop / el_serial / 1e12, "serial_ms_per_step": el_serial * 1e3,
+                       "includes": "every step: pinned H2D of Q,K,V,dO,bias; jfa_plan_create from host offsets; "
+                                   "jfa_fwd; jfa_bwd; D2H of O,lse,dQ,dK,dV. Steps pipelined on two device buffer "
+                                   "sets (copies of one step overlap the kernels of its neighbours); "
+                                   "serial_*: the same steps one at a time"}
 
     # ---------------------------------------------------------------- CPU baseline (oracle)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
