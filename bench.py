@@ -379,7 +379,8 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "strong" if args.partition else "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "vs_baseline": None, "dtype": "f32" if batch.Q.dtype == torch.float32 else "bf16", "data": "synthetic",
+            "config": cfg,
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "pct_of_bf16_peak_sustained": 100.0 * value / world / peaks["bf16_tflops_sustained"],
             "fwd_tflops": fl_f / (kt["fwd"][0] / max(1, kt["fwd"][1]) / 1e3) / 1e12 if kt["fwd"][1] else None,

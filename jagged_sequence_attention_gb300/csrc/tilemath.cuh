@@ -38,29 +38,26 @@ __device__ __forceinline__ uint32_t warp_const_chunks(bool active, int lo, int& 
     return __ballot_sync(0xffffffffu, c);
 }
 
-// tanh(u) = 1 - 2 / (exp(2u) + 1) from the hardware exp2 and reciprocal (relative
-// error about 2^-22 each); saturates correctly at +-inf.
-__device__ __forceinline__ float tanh_acc(float u) {
-    const float e = ex2_approx(u * 2.8853900817779268f);  // 2 log2(e)
-    return fmaf(-2.f, rcp_approx(e + 1.f), 1.f);
-}
-
 // sigmoid(x) = 1 / (1 + exp(-x))
 __device__ __forceinline__ float sigmoid_acc(float x) {
     return rcp_approx(1.f + ex2_approx(-1.4426950408889634f * x));
 }
 
 // GDPA activations and derivatives:
-//   gelu(x)  = 0.5 x (1 + tanh(k0 x + k1 x^3)),  k0 = sqrt(2/pi), k1 = 0.044715 k0
-//   gelu'(x) = 0.5 (1 + t) + 0.5 x (1 - t^2) (k0 + 3 k1 x^2)
+//   gelu(x)  = 0.5 x (1 + tanh(u)),  u = k0 x + k1 x^3,  k0 = sqrt(2/pi), k1 = 0.044715 k0
+//            = x s,  s = sigmoid(2u) = 1 / (1 + 2^z),  z = -2 log2(e) u   (since 0.5 (1 + tanh u)
+//              = sigmoid(2u)); the sigmoid form saturates to 0 and 1 without the cancellation
+//              of 1 + tanh(u) for large negative x, in two fewer operations
+//   gelu'(x) = s + 2 x s (1 - s) (k0 + 3 k1 x^2)
 //   silu(x)  = x s(x),  silu'(x) = s(x) (1 + x (1 - s(x)))
+__device__ __forceinline__ float gelu_sigmoid_arg(float x, float x2) {
+    // z = -2 log2(e) (k0 x + k1 x^3)
+    const float c0 = -2.3022082f, c1 = -0.10294324f;  // -2 log2(e) k0, -2 log2(e) k1
+    return x * fmaf(c1, x2, c0);
+}
+
 __device__ __forceinline__ float gdpa_act(bool gelu, float x) {
-    if (gelu) {
-        const float k0 = 0.7978845608028654f, k1 = 0.035677408136300125f;
-        const float t = tanh_acc(x * fmaf(k1, x * x, k0));
-        const float hx = 0.5f * x;
-        return fmaf(hx, t, hx);
-    }
+    if (gelu) return x * rcp_approx(1.f + ex2_approx(gelu_sigmoid_arg(x, x * x)));
     return x * sigmoid_acc(x);
 }
 
@@ -68,10 +65,9 @@ __device__ __forceinline__ void gdpa_act_grad(bool gelu, float x, float& a, floa
     if (gelu) {
         const float k0 = 0.7978845608028654f, k1 = 0.035677408136300125f;
         const float x2 = x * x;
-        const float t = tanh_acc(x * fmaf(k1, x2, k0));
-        const float hx = 0.5f * x;
-        a = fmaf(hx, t, hx);
-        da = fmaf(hx * fmaf(-t, t, 1.f), fmaf(3.f * k1, x2, k0), fmaf(0.5f, t, 0.5f));
+        const float s = rcp_approx(1.f + ex2_approx(gelu_sigmoid_arg(x, x2)));
+        a = x * s;
+        da = fmaf(2.f * a * (1.f - s), fmaf(3.f * k1, x2, k0), s);
     } else {
         const float sg = sigmoid_acc(x);
         a = x * sg;
