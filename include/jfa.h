@@ -156,7 +156,10 @@ jfa_status jfa_plan_destroy(jfa_plan plan);
  * of (query, key) pairs sum_b q_len_b * kv_len_b, the number of users U of a
  * shared key/value plan (-1 for other plans), and the number of merged query sequences
  * of a shared key/value plan's merged view (-1 when it has none; see
- * jfa_plan_create_shared_kv).  n may be smaller than 18.
+ * jfa_plan_create_shared_kv), and 1 when the forward runs the kernel with split items
+ * (sequences of one query tile whose key range is split in two halves that are merged
+ * at the end; chosen when such items carry at least half the forward's tensor-core
+ * products and the plan has no window), else 0.  n may be smaller than 19.
  */
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
 

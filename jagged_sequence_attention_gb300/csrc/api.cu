@@ -236,6 +236,7 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
                             : count_items(qo.data(), ko.data(), B, H, causal, kPassBwdKV);
     p->n_dq_items = count_items(qo.data(), kvv.data(), B, H, causal, kPassBwdQ);
     p->fwd_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_fwd_items)));
+    p->fwd_split = prefer_split_forward(qo.data(), kvv.data(), B, causal, window);
     p->bwd_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_bwd_items)));
     p->dq_grid = int(std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_dq_items)));
     std::vector<WorkItem> fi(size_t(std::max<int64_t>(1, p->n_fwd_items)));
@@ -414,12 +415,13 @@ jfa_status jfa_plan_destroy(jfa_plan plan) {
 
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
     if (!plan || !info || n < 0) return JFA_ERR_INVALID_ARG;
-    const int64_t v[18] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
+    const int64_t v[19] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
                            plan->mode,     plan->causal,  plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items,
                            plan->bwd_grid, plan->num_sms, plan->n_dq_items,  plan->dq_grid,  plan->window,
                            plan->n_pairs,  plan->shared_kv ? plan->U : -1,
-                           plan->merged ? int64_t(plan->merged->B) : -1};
-    for (int32_t i = 0; i < n && i < 18; ++i) info[i] = v[i];
+                           plan->merged ? int64_t(plan->merged->B) : -1,
+                           plan->fwd_split ? 1 : 0};
+    for (int32_t i = 0; i < n && i < 19; ++i) info[i] = v[i];
     return JFA_OK;
 }
 
@@ -507,7 +509,7 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
     p.kv_map = v->d_kv_map;
     KernelTimer tm(plan, 0, static_cast<cudaStream_t>(stream));
     cudaError_t e = dtype == JFA_BF16
-                        ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, v->fwd_grid, static_cast<cudaStream_t>(stream))
+                        ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, v->fwd_grid, v->fwd_split, static_cast<cudaStream_t>(stream))
                         : launch_fwd_f32(plan->D, Q, K, V, p, v->n_fwd_items, static_cast<cudaStream_t>(stream));
     tm.done();
     return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;

@@ -48,7 +48,8 @@ struct FwdCfg {
     // tmem slot + abort flag; per softmax warp: the head's bias row (32) and a tile's
     // bias-by-relative-position table (160)
     static constexpr int kBiasRow = 32, kBiasTab = 160;
-    static constexpr int kMiscBytes = 16 + 8 * (kBiasRow + kBiasTab) * 4;
+    // ... and, for split items, warpgroup 1's row max and sum (two buffers of 2 x BM floats)
+    static constexpr int kMiscBytes = 16 + 8 * (kBiasRow + kBiasTab) * 4 + 2 * 2 * BM * 4;
     static constexpr int kSmemNeed = kOffMisc + kMiscBytes + 1024;
     // At least 120 KB so that exactly one CTA fits on an SM: the CTA allocates all
     // 512 TMEM columns.
@@ -83,6 +84,7 @@ enum {
     B_O_DONE = 14,   // +tile: a P V product of the tile finished
     B_O_EMPTY = 16,  // +tile: the tile's epilogue has read O
     B_DRAIN = 18,
+    B_COMBINE = 19,  // split item: warpgroup 1's last P V done and its row max/sum written
 };
 
 template <typename T>
@@ -110,7 +112,9 @@ __device__ __forceinline__ void store_row<float>(float* dst, const float* v, int
 // WIN: a sliding window may be set (p.window >= 0).  Without it the window arithmetic
 // folds away at compile time, so the plain causal and non-causal paths carry none of it.
 // DENSE: the bias is the dense per-pair array p.dense (read per element, both passes).
-template <int D, typename OT, bool GDPA, bool WIN, bool DENSE>
+// SPLIT: the work list holds split items (one-tile sequences, see below); without it the
+// split code compiles away and the kernel is the plain two-tile pipeline.
+template <int D, typename OT, bool GDPA, bool WIN, bool DENSE, bool SPLIT>
 __global__ void __launch_bounds__(320, 1)
     jfa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -143,6 +147,7 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(bar(B_O_EMPTY + s), 4);
         }
         mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_COMBINE), 4);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -192,9 +197,14 @@ __global__ void __launch_bounds__(320, 1)
                         tma_load_2d(sQ + tq * C::kQBytes + cb * C::BM * 128, &tmQ, bar(B_Q_FULL),
                                     h * D + cb * C::kBoxCols, q0 + (2 * pr + tq) * C::BM);
                 ++item_it;
+                // A split item (a one-tile sequence with two or more key tiles) streams the two
+                // halves of its key range interleaved: tile 0's half at even steps, tile 1's at odd.
+                const bool split = SPLIT && q_len <= C::BM && na >= 2;
+                const int half0 = (na + 1) / 2;
                 for (int j = 0; j < n; ++j, ++kv_it) {
                     const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
-                    const int y = kv0 + (f0 + j) * C::BN;
+                    const int kt = split ? ((j & 1) ? half0 + (j >> 1) : (j >> 1)) : j;
+                    const int y = kv0 + (f0 + kt) * C::BN;
                     if (!mbar_wait_bounded(bar(B_K_EMPTY + st), ph ^ 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(bar(B_K_FULL + st), C::kKVBytes);
 #pragma unroll
@@ -237,11 +247,12 @@ __global__ void __launch_bounds__(320, 1)
         const SDesc dV0 = sdesc_sw128(sV, C::BN * 128, 1024), dV1 = sdesc_sw128(sV + C::kKVBytes, C::BN * 128, 1024);
         // S_x = Q_x K^T into the tile's S columns; first waits for the tile's
         // previous P V product, which reads P from those columns.
-        auto issue_s = [&](int x, uint32_t st) -> bool {
+        // qx: the query tile the product reads (tile x's own, or tile 0 in a split item)
+        auto issue_s = [&](int x, uint32_t st, int qx) -> bool {
             const uint32_t pc = x ? pv_cnt1 : pv_cnt0;
             if (pc > 0 && !wwait(B_O_DONE + x, (pc - 1) & 1)) return false;
             tc_fence_after();
-            const SDesc dq = x ? dQ1 : dQ0, dk = st ? dK1 : dK0;
+            const SDesc dq = qx ? dQ1 : dQ0, dk = st ? dK1 : dK0;
             const uint32_t d_tmem = tmem + C::tmem_s(x);
             if (elect_one()) {
 #pragma unroll
@@ -296,37 +307,73 @@ __global__ void __launch_bounds__(320, 1)
             key_tile_range(q_len, kv_len, 2 * pr + 1, p.causal, window, fb, nx1);
             pair_stream(q_len, kv_len, pr, p.causal, window, f0, ns, na2, nb2);
             const int off0 = fa - f0, off1 = fb - f0;
-            auto act0 = [&](int j) { return j >= off0 && j < off0 + nx0; };
-            auto act1 = [&](int j) { return j >= off1 && j < off1 + nx1; };
+            // A split item (a one-tile sequence, q_len <= 128, with two or more key tiles): both
+            // tiles' products read query tile 0; tile 0 takes the even stream steps, tile 1 the
+            // odd.  (Short-query batches consist of such items; a long sequence's odd last tile is
+            // not split, which measured faster.)
+            const bool split = SPLIT && q_len <= C::BM && nx0 >= 2;
             if (!wwait(B_Q_FULL, item_it & 1)) { ok = false; break; }
-            // prologue: S of key tile 0
-            {
-                const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
-                if (!wwait(B_K_FULL + st, ph)) { ok = false; break; }
-                if (act0(0) && !issue_s(0, st)) { ok = false; break; }
-                if (act1(0) && !issue_s(1, st)) { ok = false; break; }
-                commit(B_K_EMPTY + st);
-                if (n == 1) commit(B_Q_EMPTY);
-            }
-            for (int j = 0; j < n && ok; ++j) {
-                const uint32_t g = kv_it + j, st = g & 1, ph = (g >> 1) & 1;
-                const uint32_t g1 = g + 1, st1 = g1 & 1, ph1 = (g1 >> 1) & 1;
-                if (!wwait(B_V_FULL + st, ph)) { ok = false; break; }
-                if (act0(j) && !issue_pv(0, st, j == off0)) { ok = false; break; }
-                if (j + 1 < n && !wwait(B_K_FULL + st1, ph1)) { ok = false; break; }
-                if (act0(j + 1) && !issue_s(0, st1)) { ok = false; break; }
-                if (act1(j) && !issue_pv(1, st, j == off1)) { ok = false; break; }
-                commit(B_V_EMPTY + st);
-                if (act1(j + 1) && !issue_s(1, st1)) { ok = false; break; }
-                if (j + 1 < n) {
+            if (!split) {
+                auto act0 = [&](int j) { return j >= off0 && j < off0 + nx0; };
+                auto act1 = [&](int j) { return j >= off1 && j < off1 + nx1; };
+                // prologue: S of key tile 0
+                {
+                    const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
+                    if (!wwait(B_K_FULL + st, ph)) { ok = false; break; }
+                    if (act0(0) && !issue_s(0, st, 0)) { ok = false; break; }
+                    if (act1(0) && !issue_s(1, st, 1)) { ok = false; break; }
+                    commit(B_K_EMPTY + st);
+                    if (n == 1) commit(B_Q_EMPTY);
+                }
+                for (int j = 0; j < n && ok; ++j) {
+                    const uint32_t g = kv_it + j, st = g & 1, ph = (g >> 1) & 1;
+                    const uint32_t g1 = g + 1, st1 = g1 & 1, ph1 = (g1 >> 1) & 1;
+                    if (!wwait(B_V_FULL + st, ph)) { ok = false; break; }
+                    if (act0(j) && !issue_pv(0, st, j == off0)) { ok = false; break; }
+                    if (j + 1 < n && !wwait(B_K_FULL + st1, ph1)) { ok = false; break; }
+                    if (act0(j + 1) && !issue_s(0, st1, 0)) { ok = false; break; }
+                    if (act1(j) && !issue_pv(1, st, j == off1)) { ok = false; break; }
+                    commit(B_V_EMPTY + st);
+                    if (act1(j + 1) && !issue_s(1, st1, 1)) { ok = false; break; }
+                    if (j + 1 < n) {
+                        commit(B_K_EMPTY + st1);
+                        if (j + 2 == n) commit(B_Q_EMPTY);
+                    }
+                }
+            } else {
+                // step j: tile x = j & 1 computes P V of stream step j, then S of step j + 2
+                // (S of steps 0 and 1 in the prologue); every S reads query tile 0.  The
+                // producer streams tile 0's half of the key range at even steps, tile 1's at odd.
+                {
+                    const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
+                    if (!wwait(B_K_FULL + st, ph)) { ok = false; break; }
+                    if (!issue_s(0, st, 0)) { ok = false; break; }
+                    commit(B_K_EMPTY + st);
+                    const uint32_t g1 = kv_it + 1, st1 = g1 & 1, ph1 = (g1 >> 1) & 1;
+                    if (!wwait(B_K_FULL + st1, ph1)) { ok = false; break; }
+                    if (!issue_s(1, st1, 0)) { ok = false; break; }
                     commit(B_K_EMPTY + st1);
-                    if (j + 2 == n) commit(B_Q_EMPTY);
+                    if (n == 2) commit(B_Q_EMPTY);
+                }
+                for (int j = 0; j < n && ok; ++j) {
+                    const int x = j & 1;
+                    const uint32_t g = kv_it + j, st = g & 1, ph = (g >> 1) & 1;
+                    const uint32_t g2 = g + 2, st2 = g2 & 1, ph2 = (g2 >> 1) & 1;
+                    if (!wwait(B_V_FULL + st, ph)) { ok = false; break; }
+                    if (!issue_pv(x, st, j < 2)) { ok = false; break; }
+                    commit(B_V_EMPTY + st);
+                    if (j + 2 < n) {
+                        if (!wwait(B_K_FULL + st2, ph2)) { ok = false; break; }
+                        if (!issue_s(x, st2, 0)) { ok = false; break; }
+                        commit(B_K_EMPTY + st2);
+                        if (j + 3 == n) commit(B_Q_EMPTY);
+                    }
                 }
             }
             kv_it += n;
             ++item_it;
             items_x0 += nx0 > 0 ? 1 : 0;
-            items_x1 += nx1 > 0 ? 1 : 0;
+            items_x1 += (nx1 > 0 || split) ? 1 : 0;
         }
         if (!ok) fail();
         // Drain all issued MMAs before TMEM is released.
@@ -341,6 +388,8 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t tO = tmem + lane_base + C::tmem_o(x);
         constexpr bool softmax = !GDPA;
         uint32_t s_cnt = 0;
+        uint32_t split_cnt = 0;  // split items seen (phase of B_COMBINE, exchange buffer)
+        float* comb_s = bias_s + 8 * (C::kBiasRow + C::kBiasTab);  // [2][max(BM), sum(BM)]
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
             const int4 w = p.items[it];
@@ -348,10 +397,22 @@ __global__ void __launch_bounds__(320, 1)
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
             const int kb = p.kv_map ? p.kv_map[b] : b;
             const int kv_len = p.kv_off[kb + 1] - p.kv_off[kb];
-            const int tile = 2 * pr + x;
+            // Split item (a one-tile sequence with two or more key tiles): both
+            // warpgroups take tile 0's rows, warpgroup x one half of its key range (the first
+            // (na + 1) / 2 key tiles, or the rest) with its own max, sum and O; warpgroup 0
+            // combines the two at the end.  The tile loop is the same in both cases.
+            int kfa, na;
+            key_tile_range(q_len, kv_len, 2 * pr, p.causal, window, kfa, na);
+            const bool split = SPLIT && q_len <= C::BM && na >= 2;
+            const int tile = split ? 2 * pr : 2 * pr + x;
             if (tile * C::BM >= q_len) continue;  // tile B of a short last pair
-            int kf, n;  // key tiles [kf, kf + n)
-            key_tile_range(q_len, kv_len, tile, p.causal, window, kf, n);
+            int kf, n;  // this warpgroup's key tiles [kf, kf + n)
+            if (split) {
+                kf = kfa + (x ? (na + 1) / 2 : 0);
+                n = x ? na / 2 : (na + 1) / 2;
+            } else {
+                key_tile_range(q_len, kv_len, tile, p.causal, window, kf, n);
+            }
             const int row = tile * C::BM + t;
             const bool row_valid = row < q_len;
             const int diag = kv_len - q_len;
@@ -631,6 +692,59 @@ __global__ void __launch_bounds__(320, 1)
                 break;
             }
             tc_fence_after();
+            if (split) {
+                // Warpgroup 1 hands over its row max and sum; warpgroup 0 combines both halves:
+                // O = (O0 2^(m0-m) + O1 2^(m1-m)) / (l0 2^(m0-m) + l1 2^(m1-m)), m = max(m0, m1)
+                // (GDPA: O = O0 + O1), then releases both O accumulators.
+                float* comb = comb_s + (split_cnt & 1) * 2 * C::BM;
+                ++split_cnt;
+                if (x == 1) {
+                    comb[t] = m;
+                    comb[C::BM + t] = l;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_COMBINE));
+                    continue;
+                }
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_COMBINE), (split_cnt - 1) & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float c0 = 1.f, c1 = 1.f, mm = m, ll = l;
+                if constexpr (softmax) {
+                    const float m1 = comb[t], l1 = comb[C::BM + t];
+                    mm = fmaxf(m, m1);
+                    const float a0 = m == -INFINITY ? 0.f : ex2_approx(m - mm);
+                    const float a1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
+                    ll = fmaf(l, a0, l1 * a1);
+                    const float inv = ll > 0.f ? 1.f / ll : 0.f;
+                    c0 = a0 * inv;
+                    c1 = a1 * inv;
+                }
+                const uint32_t tO1 = tmem + lane_base + C::tmem_o(1);
+                OT* orow_p = reinterpret_cast<OT*>(p.O) + orow * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r0[32], r1[32];
+                    float v[32];
+                    tmem_ld32(tO + c * 32u, r0);
+                    tmem_ld32(tO1 + c * 32u, r1);
+                    tmem_ld_wait(r0);
+                    tmem_ld_wait(r1);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = fmaf(__uint_as_float(r0[i]), c0, __uint_as_float(r1[i]) * c1);
+                    if (row_valid) store_row<OT>(orow_p + c * 32, v, 32);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(B_O_EMPTY + 0));
+                    mbar_arrive(bar(B_O_EMPTY + 1));
+                }
+                if (row_valid && softmax && p.lse)
+                    p.lse[orow] = ll > 0.f ? (mm + __log2f(ll)) * 0.6931471805599453f : -INFINITY;
+                continue;
+            }
             {
                 const float inv = (softmax && l > 0.f) ? 1.f / l : (softmax ? 0.f : 1.f);
                 OT* orow_p = reinterpret_cast<OT*>(p.O) + orow * D;
@@ -660,42 +774,46 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int D, typename OT, bool GDPA, bool WIN, bool DENSE>
+template <int D, typename OT, bool GDPA, bool WIN, bool DENSE, bool SPLIT>
 static cudaError_t launch_fwd_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const FwdParams& p, int grid, cudaStream_t st) {
     using C = FwdCfg<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, OT, GDPA, WIN, DENSE>,
+        cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, OT, GDPA, WIN, DENSE, SPLIT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_fwd_kernel<D, OT, GDPA, WIN, DENSE><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, p);
+    jfa_fwd_kernel<D, OT, GDPA, WIN, DENSE, SPLIT><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
 }
 
 template <int D, typename OT>
 static cudaError_t launch_fwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                const FwdParams& p, int grid, cudaStream_t st) {
+                                const FwdParams& p, int grid, bool split_list, cudaStream_t st) {
+    const bool sm = p.mode == JFA_SOFTMAX;
     if (p.dense)  // dense bias: the window, if any, is taken at run time
-        return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false, true, true>(tmQ, tmK, tmV, p, grid, st)
-                                     : launch_fwd_m<D, OT, true, true, true>(tmQ, tmK, tmV, p, grid, st);
+        return sm ? launch_fwd_m<D, OT, false, true, true, false>(tmQ, tmK, tmV, p, grid, st)
+                  : launch_fwd_m<D, OT, true, true, true, false>(tmQ, tmK, tmV, p, grid, st);
     if (p.window >= 0)
-        return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false, true, false>(tmQ, tmK, tmV, p, grid, st)
-                                     : launch_fwd_m<D, OT, true, true, false>(tmQ, tmK, tmV, p, grid, st);
-    return p.mode == JFA_SOFTMAX ? launch_fwd_m<D, OT, false, false, false>(tmQ, tmK, tmV, p, grid, st)
-                                 : launch_fwd_m<D, OT, true, false, false>(tmQ, tmK, tmV, p, grid, st);
+        return sm ? launch_fwd_m<D, OT, false, true, false, false>(tmQ, tmK, tmV, p, grid, st)
+                  : launch_fwd_m<D, OT, true, true, false, false>(tmQ, tmK, tmV, p, grid, st);
+    if (split_list)
+        return sm ? launch_fwd_m<D, OT, false, false, false, true>(tmQ, tmK, tmV, p, grid, st)
+                  : launch_fwd_m<D, OT, true, false, false, true>(tmQ, tmK, tmV, p, grid, st);
+    return sm ? launch_fwd_m<D, OT, false, false, false, false>(tmQ, tmK, tmV, p, grid, st)
+              : launch_fwd_m<D, OT, true, false, false, false>(tmQ, tmK, tmV, p, grid, st);
 }
 
 cudaError_t launch_fwd(int dtype, int o_dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                       const CUtensorMap& tmV, const FwdParams& p, int grid, cudaStream_t st) {
+                       const CUtensorMap& tmV, const FwdParams& p, int grid, bool split_list, cudaStream_t st) {
     using bf16 = __nv_bfloat16;
     if (dtype != JFA_BF16) return cudaErrorInvalidValue;
-    if (D == 128 && o_dtype == JFA_BF16) return launch_fwd_t<128, bf16>(tmQ, tmK, tmV, p, grid, st);
-    if (D == 128 && o_dtype == JFA_F32) return launch_fwd_t<128, float>(tmQ, tmK, tmV, p, grid, st);
-    if (D == 64 && o_dtype == JFA_BF16) return launch_fwd_t<64, bf16>(tmQ, tmK, tmV, p, grid, st);
-    if (D == 64 && o_dtype == JFA_F32) return launch_fwd_t<64, float>(tmQ, tmK, tmV, p, grid, st);
+    if (D == 128 && o_dtype == JFA_BF16) return launch_fwd_t<128, bf16>(tmQ, tmK, tmV, p, grid, split_list, st);
+    if (D == 128 && o_dtype == JFA_F32) return launch_fwd_t<128, float>(tmQ, tmK, tmV, p, grid, split_list, st);
+    if (D == 64 && o_dtype == JFA_BF16) return launch_fwd_t<64, bf16>(tmQ, tmK, tmV, p, grid, split_list, st);
+    if (D == 64 && o_dtype == JFA_F32) return launch_fwd_t<64, float>(tmQ, tmK, tmV, p, grid, split_list, st);
     return cudaErrorInvalidValue;
 }
 

@@ -194,6 +194,7 @@ void build_shared_kv_dkdv(const int32_t* q_off, const int32_t* u_off, const int3
                           int32_t* cta_off, std::vector<int2>* steps, std::vector<int32_t>* step_off,
                           std::vector<int32_t>* ktile_off);
 int64_t count_shared_kv_dkdv_items(const int32_t* u_off, int32_t U, int32_t H);
+bool prefer_split_forward(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t causal, int32_t window);
 
 int64_t sequence_cost(int64_t q_len, int64_t kv_len, int32_t H, int32_t causal, int32_t window);
 void partition_users(const int32_t* q_off, const int32_t* u_off, const int32_t* kv_index, int32_t B, int32_t U,
@@ -204,7 +205,7 @@ void partition_sequences(const int32_t* q_off, const int32_t* kv_off, int32_t B,
 
 // Kernel launchers (fwd.cu, bwd.cu, bwd_dq.cu).  Return cudaSuccess or the launch error.
 cudaError_t launch_fwd(int dtype, int o_dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                       const CUtensorMap& tmV, const FwdParams& p, int grid, cudaStream_t st);
+                       const CUtensorMap& tmV, const FwdParams& p, int grid, bool split_list, cudaStream_t st);
 cudaError_t launch_bwd_pre(int dtype, int o_dtype, int D, const void* O, const void* dO, float* delta,
                            float* dq_acc, int64_t Tq, int H, int mode, cudaStream_t st);
 cudaError_t launch_bwd_main(int dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
@@ -262,6 +263,7 @@ struct jfa_plan_t {
     jfa_plan_t* merged = nullptr;
     int64_t n_fwd_items, n_bwd_items, n_dq_items;
     int fwd_grid, bwd_grid, dq_grid;
+    bool fwd_split;  // forward kernel with split items (prefer_split_forward)
     // optional per-kernel timing (jfa_plan_set_timing)
     bool timing;
     std::vector<cudaEvent_t> ev_pool;                 // reusable events

@@ -188,6 +188,31 @@ void build_shared_kv_dkdv(const int32_t* q_off, const int32_t* u_off, const int3
     assign_lpt(all, U, H, n_ctas, items, cta_off, nullptr);
 }
 
+// The forward's split items: a sequence with a single query tile (q_len <= 128) that
+// visits two key tiles or more has no second tile to overlap its softmax with, so the
+// kernel splits its key range into two halves run as if they were the two tiles of a
+// pair and merges the halves' (max, sum, O) at the end.  Code for that costs the plain
+// two-tile pipeline some speed even where no item splits, so the plan picks the kernel
+// with split items only when they carry at least half the forward's products.  The
+// sliding-window forward has no split form.
+bool prefer_split_forward(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t causal, int32_t window) {
+    if (window >= 0) return false;
+    int64_t split = 0, total = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        const int64_t q_len = q_off[b + 1] - q_off[b];
+        const int64_t kv_len = kv_off[b + 1] - kv_off[b];
+        const int64_t np = ceil_div(q_len, kFwdPairRows);
+        for (int64_t t = 0; t < np; ++t) {
+            int first, n, na, nb;
+            pair_stream(q_len, kv_len, t, causal, window, first, n, na, nb);
+            const int64_t c = 2 * (int64_t(na) + nb) + 2;
+            total += c;
+            if (q_len <= kFwdBM && na >= 2) split += c;
+        }
+    }
+    return split > 0 && 2 * split >= total;
+}
+
 int64_t count_shared_kv_dkdv_items(const int32_t* u_off, int32_t U, int32_t H) {
     int64_t n = 0;
     for (int32_t u = 0; u < U; ++u) n += ceil_div(u_off[u + 1] - u_off[u], kBwdBN) * H;

@@ -162,3 +162,21 @@ def test_full_size_workload_sampled(name):
     # whole-output sanity at full size: finite everywhere
     for k in ("O", "dQ", "dK", "dV"):
         assert torch.isfinite(g[k]).all(), k
+
+
+@pytest.mark.parametrize("mode", ["softmax", "gelu_tanh", "silu"])
+@pytest.mark.parametrize("causal,bias", [(False, False), (True, True)])
+@pytest.mark.parametrize("long_len,split", [(300, 1), (3000, 0)])
+def test_split_forward_both_kernels(mode, causal, bias, long_len, split):
+    """One-tile query sequences over several key tiles (split items) next to a longer
+    sequence: with a short neighbour the forward runs the kernel with split items on the
+    mixed list, with a long one the plain kernel runs the short sequences unsplit."""
+    from jagged_sequence_attention_gb300 import jfa
+    rng = np.random.default_rng(12)
+    q = rng.integers(1, 129, size=14).tolist() + [128, 1, long_len]
+    kv = rng.integers(129, 1200, size=14).tolist() + [129, 4000, long_len]
+    std = 1.0 if mode == "softmax" else 0.5
+    b = wl.make_custom(q, kv, H=2, D=128, mode=mode, causal=causal, bias=bias, value_std=std,
+                       device="cuda", seed=13)
+    g, _ = check_full(b)
+    assert jfa.jfa_plan_info(g["plan"])["fwd_split"] == split
