@@ -68,7 +68,9 @@ struct KvCfg {
     static constexpr int kRelTab = kCols + 32;
     static constexpr int kWarpMisc = 2 * kCols + 32 + kRelTab + 32;
     static constexpr int kMiscBytes = 16 + kCompWarps * kWarpMisc * 4;
-    static constexpr int kSmemNeed = kOffMisc + kMiscBytes + 1024;
+    // per compute warp: a 2 KB buffer through which the epilogue's stores are regrouped
+    static constexpr int kOffStage = (kOffMisc + kMiscBytes + 127) / 128 * 128;
+    static constexpr int kSmemNeed = kOffStage + kCompWarps * 2048 + 1024;
     // At least 120 KB so that exactly one CTA fits on an SM: it allocates all 512 TMEM columns.
     static constexpr int kSmemBytes = kSmemNeed > 120 * 1024 ? kSmemNeed : 120 * 1024;
     static constexpr int kDSteps = D / 16;   // contraction over head_dim
@@ -731,21 +733,24 @@ __global__ void __launch_bounds__(320, 1)
             // Epilogue: dV and dK (times scale) of this key row, the warpgroup's half of D.
             if (!warp_wait(KV_ACC_FULL, item_it & 1)) { ok = false; break; }
             tc_fence_after();
+            {
+                uint32_t* stage_w = reinterpret_cast<uint32_t*>(smem + C::kOffStage) + warp * 512;
+                const uint32_t valid = __ballot_sync(0xffffffffu, key_valid);
+                // this warp's first key row (kv0 + key0) * H + h, then rows H * D elements apart
+                const size_t off0 = ((size_t(kv0) + size_t(nt * C::BN + (warp & 3) * 32)) * size_t(p.H) + size_t(h)) * D +
+                                    size_t(wg * C::kEpiCols);
+                const size_t stride = size_t(p.H) * D;
 #pragma unroll
-            for (int cc = 0; cc < C::kEpiCols / 32; ++cc) {
-                const uint32_t col = uint32_t(wg * C::kEpiCols + 32 * cc);
-                uint32_t rr[32];
-                float v[32];
-                tmem_ld32(tmem + lane_base + C::kTmDV + col, rr);
-                tmem_ld_wait(rr);
+                for (int cc = 0; cc < C::kEpiCols / 32; ++cc) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(rr[e]);
-                if (key_valid) store_bf16_row(dv_row + 32 * cc, v, 32, 1.f);
-                tmem_ld32(tmem + lane_base + C::kTmDK + col, rr);
-                tmem_ld_wait(rr);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(rr[e]);
-                if (key_valid) store_bf16_row(dk_row + 32 * cc, v, 32, p.scale);
+                    for (int t = 0; t < 2; ++t) {  // dV, then dK
+                        uint32_t rr[32];
+                        tmem_ld32(tmem + lane_base + (t ? C::kTmDK : C::kTmDV) + uint32_t(wg * C::kEpiCols + 32 * cc), rr);
+                        tmem_ld_wait(rr);
+                        store_chunk_bf16(stage_w, rr, t ? p.scale : 1.f, lane, valid,
+                                         reinterpret_cast<__nv_bfloat16*>(t ? p.dK : p.dV) + off0 + 32 * cc, stride);
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
