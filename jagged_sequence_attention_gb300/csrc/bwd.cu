@@ -734,7 +734,7 @@ __global__ void __launch_bounds__(320, 1)
             if (!warp_wait(KV_ACC_FULL, item_it & 1)) { ok = false; break; }
             tc_fence_after();
             {
-                uint32_t* stage_w = reinterpret_cast<uint32_t*>(smem + C::kOffStage) + warp * 512;
+                const uint32_t stage_w = sbase + uint32_t(C::kOffStage + warp * 2048);
                 const uint32_t valid = __ballot_sync(0xffffffffu, key_valid);
                 // this warp's first key row (kv0 + key0) * H + h, then rows H * D elements apart
                 const size_t off0 = ((size_t(kv0) + size_t(nt * C::BN + (warp & 3) * 32)) * size_t(p.H) + size_t(h)) * D +

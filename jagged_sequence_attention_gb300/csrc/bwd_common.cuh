@@ -22,36 +22,6 @@ __device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float* 
     }
 }
 
-// Writes a warp's 32 x 32 fp32 chunk (lane = row, raw = the row's 32 values as bits),
-// each times `mul`, as bf16 to 32 global rows of 64 bytes: row r at dst + r * stride
-// (elements; 16-byte aligned), skipped unless bit r of valid is set.  Each lane stores its row's four 16-byte
-// pieces in the warp's 2 KB staging buffer `stg` (piece q of row r at slot q ^ ((r >> 1) &
-// 3), so that any eight consecutive rows cover all 32 banks), then every global store
-// instruction writes eight whole 64-byte rows.  Stored straight from registers, each
-// instruction would instead touch 32 rows, one 16-byte piece of each: four times the
-// cache-line transactions.
-__device__ __forceinline__ void store_chunk_bf16(uint32_t* stg, const uint32_t (&raw)[32], float mul, int lane,
-                                                 uint32_t valid, __nv_bfloat16* dst, size_t stride) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u;
-        u.x = pack_bf16x2(__uint_as_float(raw[8 * q + 0]) * mul, __uint_as_float(raw[8 * q + 1]) * mul);
-        u.y = pack_bf16x2(__uint_as_float(raw[8 * q + 2]) * mul, __uint_as_float(raw[8 * q + 3]) * mul);
-        u.z = pack_bf16x2(__uint_as_float(raw[8 * q + 4]) * mul, __uint_as_float(raw[8 * q + 5]) * mul);
-        u.w = pack_bf16x2(__uint_as_float(raw[8 * q + 6]) * mul, __uint_as_float(raw[8 * q + 7]) * mul);
-        *reinterpret_cast<uint4*>(stg + lane * 16 + ((q ^ ((lane >> 1) & 3)) << 2)) = u;
-    }
-    __syncwarp();
-    const int piece = lane & 3;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int r = (lane >> 2) + 8 * k;
-        const uint4 u = *reinterpret_cast<const uint4*>(stg + r * 16 + ((piece ^ ((r >> 1) & 3)) << 2));
-        if ((valid >> r) & 1u) *reinterpret_cast<uint4*>(dst + size_t(r) * stride + 8 * piece) = u;
-    }
-    __syncwarp();
-}
-
 // Zero-fills n bf16 values (n a multiple of 8) of a 16-byte aligned global row.
 __device__ __forceinline__ void zero_bf16_row(__nv_bfloat16* dst, int n) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);

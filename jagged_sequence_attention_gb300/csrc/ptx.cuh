@@ -319,10 +319,48 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Writes a warp's 32 x 32 fp32 chunk (lane = row, raw = the row's 32 values as bits),
+// each times `mul`, as bf16 to 32 global rows of 64 bytes: row r at dst + r * stride
+// (elements; 16-byte aligned), skipped unless bit r of valid is set.  Each lane stores its
+// row's four 16-byte pieces in the warp's 2 KB staging buffer at shared address stg
+// (piece q of row r at slot q ^ ((r >> 1) & 3), so that any eight consecutive rows cover
+// all 32 banks), then every global store instruction writes eight whole 64-byte rows.
+// Stored straight from registers, each instruction would instead touch 32 rows, one
+// 16-byte piece of each: four times the cache-line transactions.
+__device__ __forceinline__ void store_chunk_bf16(uint32_t stg, const uint32_t (&raw)[32], float mul, int lane,
+                                                 uint32_t valid, __nv_bfloat16* dst, size_t stride) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        st_shared_v4(stg + uint32_t(lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)),
+                     pack_bf16x2(__uint_as_float(raw[8 * q + 0]) * mul, __uint_as_float(raw[8 * q + 1]) * mul),
+                     pack_bf16x2(__uint_as_float(raw[8 * q + 2]) * mul, __uint_as_float(raw[8 * q + 3]) * mul),
+                     pack_bf16x2(__uint_as_float(raw[8 * q + 4]) * mul, __uint_as_float(raw[8 * q + 5]) * mul),
+                     pack_bf16x2(__uint_as_float(raw[8 * q + 6]) * mul, __uint_as_float(raw[8 * q + 7]) * mul));
+    }
+    __syncwarp();
+    const int piece = lane & 3;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = (lane >> 2) + 8 * k;
+        const uint4 u = ld_shared_v4(stg + uint32_t(r * 64 + ((piece ^ ((r >> 1) & 3)) << 4)));
+        if ((valid >> r) & 1u) *reinterpret_cast<uint4*>(dst + size_t(r) * stride + 8 * piece) = u;
+    }
+    __syncwarp();
 }
 
 // Packed dual fp32 arithmetic (fma/add on a pair of floats, one instruction).
