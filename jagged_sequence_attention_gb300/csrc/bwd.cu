@@ -532,6 +532,12 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 __syncwarp();
 
+                // A 32-column chunk masked for every key row of the warp (query rows past the
+                // sequence's end, or all before the causal diagonal, or no valid key row) has
+                // P^T = 0: it skips the exponent and writes zeros (steps with no masked
+                // column never test this).
+                const bool zc[2] = {!full && __all_sync(0xffffffffu, hi <= 0 || lo >= 32),
+                                    !full && __all_sync(0xffffffffu, hi <= 32 || lo >= NC)};
                 if (!warp_wait(KV_S_FULL, g & 1)) { ok = false; break; }
                 tc_fence_after();
                 float pv[NC];
@@ -567,6 +573,12 @@ __global__ void __launch_bounds__(320, 1)
                         }
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) pk[c >> 1] = pack_bf16x2(pv[32 * k + c], pv[32 * k + c + 1]);
+                    } else if (zc[k]) {
+                        // P^T = 0 (GDPA: act' = 0 too), so dS^T of the chunk comes out 0
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) pk[c] = 0u;
+#pragma unroll
+                        for (int c = 32 * k; c < 32 * k + 32; ++c) pv[c] = 0.f;
                     } else if (softmax) {
                         // exponent = xs * s + (bias - lse): the staged addend already holds
                         // the bias of a warp-constant chunk; other chunks add it per element
