@@ -455,17 +455,24 @@ __global__ void __launch_bounds__(320, 1)
                 bias_w[lane] = p.bias[h * 32 + lane] * (softmax ? 1.4426950408889634f : 1.0f);
                 __syncwarp();
             }
-            // Row terms (lse in log2 units, Delta) of this warpgroup's query columns:
-            // lane l holds columns c0 + l and c0 + 32 + l, fetched one step ahead.
-            float nl[2] = {0.f, 0.f}, nd[2] = {0.f, 0.f};
+            // Row terms (lse, Delta) of this warpgroup's query columns: lane l holds columns
+            // c0 + l and c0 + 32 + l, loaded one step ahead as they are (bit k of rv: column
+            // valid).  Nothing reads the loaded registers until that step, so the load's
+            // latency is never waited for.
+            float rl[2] = {0.f, 0.f}, rd[2] = {0.f, 0.f};
+            uint32_t rv = 0;
             auto fetch = [&](int fq0, int fq_len, int qrow0) {
+                rv = 0;
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int c = qrow0 + c0 + 32 * k + lane;
-                    const bool v = softmax && c < fq_len;
+                    const bool v = c < fq_len;
                     const size_t ridx = (size_t(fq0) + size_t(v ? c : 0)) * size_t(p.H) + size_t(h);
-                    nl[k] = v ? -p.lse[ridx] * 1.4426950408889634f : 0.f;
-                    nd[k] = v ? -p.delta[ridx] : 0.f;
+                    if constexpr (softmax) {
+                        rl[k] = p.lse[ridx];
+                        rd[k] = p.delta[ridx];
+                    }
+                    rv |= uint32_t(v) << k;
                 }
             };
             {
@@ -478,10 +485,12 @@ __global__ void __launch_bounds__(320, 1)
                 int sb, sq0, sq_len, qrow0;  // the step's query sequence and first query row
                 step_q(i, sb, sq0, sq_len, qrow0);
                 const int diag = kv_len - sq_len;
-                const float cur_nl0 = nl[0], cur_nl1 = nl[1];
+                // -lse in log2 units and -Delta of this step's columns (0 past the end)
+                const float cur_nl0 = (softmax && (rv & 1u)) ? -rl[0] * 1.4426950408889634f : 0.f;
+                const float cur_nl1 = (softmax && (rv & 2u)) ? -rl[1] * 1.4426950408889634f : 0.f;
                 __syncwarp();
-                del_s[lane] = nd[0];
-                del_s[32 + lane] = nd[1];
+                del_s[lane] = (softmax && (rv & 1u)) ? -rd[0] : 0.f;
+                del_s[32 + lane] = (softmax && (rv & 2u)) ? -rd[1] : 0.f;
                 if (i + 1 < n) {
                     int fb, fq0, fql, fr0;
                     step_q(i + 1, fb, fq0, fql, fr0);
