@@ -28,7 +28,7 @@
 // dK/dV CTA = 10 warps: 0-7 compute (warpgroup g owns query columns [64g, 64g+64) of
 // a step; thread = key row = TMEM lane) and write the dK/dV epilogue, 8 TMA producer,
 // 9 MMA issuer.  TMEM: dV [0,128), dK [128,256), S^T/P^T [256,384), dP^T/dS^T
-// [384,512).  Issue order per step: dK(i), S(i+1), dP(i+1), dV(i+1); each product
+// [384,512).  Issue order per step: S(i+1), dK(i), dP(i+1), dV(i+1); each product
 // that must wait for a TMEM region to be consumed finds another product queued
 // ahead of it.  P^T and dS^T are signalled per 32-column chunk, so dV and dK start on
 // the first chunk while the second is being formed.
@@ -354,8 +354,12 @@ __global__ void __launch_bounds__(320, 1)
             if (!issue_s(g0) || !issue_dp(g0) || !issue_dv(g0, true)) { ok = false; break; }
             for (int i = 0; i < n && ok; ++i) {
                 const uint32_t g = g0 + uint32_t(i);
+                // S^T(i+1) goes ahead of dK(i): it needs only dV(i) to have read P^T, so it runs
+                // while the compute warps form dS^T(i), and their next P^T phase starts as soon
+                // as dS^T(i) is done instead of after dK(i) and S^T(i+1) have run.
+                if (i + 1 < n && !issue_s(g + 1)) { ok = false; break; }
                 if (!issue_dk(g, i == 0)) { ok = false; break; }
-                if (i + 1 < n && (!issue_s(g + 1) || !issue_dp(g + 1) || !issue_dv(g + 1, false))) {
+                if (i + 1 < n && (!issue_dp(g + 1) || !issue_dv(g + 1, false))) {
                     ok = false;
                     break;
                 }
