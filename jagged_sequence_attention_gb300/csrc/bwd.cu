@@ -547,8 +547,10 @@ __global__ void __launch_bounds__(320, 1)
 
                 // A 32-column chunk masked for every key row of the warp (query rows past the
                 // sequence's end, or all before the causal diagonal, or no valid key row) has
-                // P^T = 0: it skips the exponent and writes zeros (steps with no masked
-                // column never test this).
+                // P^T = dS^T = 0: it skips the exponent or activation and writes zeros (steps
+                // with no masked column never test this).  Softmax zeroes P and forms dS^T = 0
+                // on the common path; GDPA also skips the chunk's loads and dS^T arithmetic.
+                // Each is the faster of the two forms for its mode.
                 const bool zc[2] = {!full && __all_sync(0xffffffffu, hi <= 0 || lo >= 32),
                                     !full && __all_sync(0xffffffffu, hi <= 32 || lo >= NC)};
                 if (!warp_wait(KV_S_FULL, g & 1)) { ok = false; break; }
@@ -557,10 +559,19 @@ __global__ void __launch_bounds__(320, 1)
                 {
                     uint32_t (&ra)[32] = *reinterpret_cast<uint32_t(*)[32]>(pv);
                     uint32_t (&rb)[32] = *reinterpret_cast<uint32_t(*)[32]>(pv + 32);
-                    tmem_ld32(tX, ra);
-                    tmem_ld32(tX + 32u, rb);
-                    tmem_ld_wait(ra);
-                    tmem_ld_wait(rb);
+                    if constexpr (GDPA) {  // GDPA: a zero chunk is not even loaded
+                        if (!zc[0]) tmem_ld32(tX, ra);
+                        if (!zc[1]) tmem_ld32(tX + 32u, rb);
+                        if (!(zc[0] && zc[1])) {
+                            tmem_ld_wait(ra);
+                            tmem_ld_wait(rb);
+                        }
+                    } else {
+                        tmem_ld32(tX, ra);
+                        tmem_ld32(tX + 32u, rb);
+                        tmem_ld_wait(ra);
+                        tmem_ld_wait(rb);
+                    }
                 }
                 // P^T = exp2(xs * s + bias - lse) (softmax; pv keeps P) or act(scale * s +
                 // bias) (GDPA; pv keeps act' for dS), one 32-column chunk at a time: each
@@ -587,11 +598,12 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) pk[c >> 1] = pack_bf16x2(pv[32 * k + c], pv[32 * k + c + 1]);
                     } else if (zc[k]) {
-                        // P^T = 0 (GDPA: act' = 0 too), so dS^T of the chunk comes out 0
 #pragma unroll
                         for (int c = 0; c < 16; ++c) pk[c] = 0u;
+                        if constexpr (softmax) {  // P^T = 0, so dS^T of the chunk comes out 0
 #pragma unroll
-                        for (int c = 32 * k; c < 32 * k + 32; ++c) pv[c] = 0.f;
+                            for (int c = 32 * k; c < 32 * k + 32; ++c) pv[c] = 0.f;
+                        }
                     } else if (softmax) {
                         // exponent = xs * s + (bias - lse): the staged addend already holds
                         // the bias of a warp-constant chunk; other chunks add it per element
@@ -659,6 +671,19 @@ __global__ void __launch_bounds__(320, 1)
                 // time, packed over the warpgroup's own dP^T columns (already read).
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
+                    if constexpr (GDPA) {
+                        if (zc[k]) {  // dS^T = 0: written without reading dP^T
+                            uint32_t pd[16];
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) pd[c] = 0u;
+                            tmem_st16(tY + 16u * k, pd);
+                            tmem_st_wait();
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar(KV_DS_FULL + k));
+                            continue;
+                        }
+                    }
                     float dp[32];
                     {
                         uint32_t (&ra)[32] = *reinterpret_cast<uint32_t(*)[32]>(dp);
