@@ -104,37 +104,19 @@ void assign_lpt(std::vector<Costed>& all, int32_t n_groups_b, int32_t H, int32_t
                 int32_t* cta_off, int64_t* cta_cost) {
     const int32_t B = n_groups_b;
     // Group-major order: groups by total cost (largest first, ties by sequence and
-    // head), then items by cost inside the group, equal costs keeping (sequence, head,
-    // tile) order, so the plan is deterministic.  Items are bucketed by group (a
-    // counting pass), the groups sorted, and each group's items stably sorted.
-    const size_t G = size_t(B) * size_t(H);
-    std::vector<int64_t> group_cost(G, 0);
-    std::vector<int32_t> group_start(G + 1, 0);
-    for (const Costed& c : all) {
-        const size_t g = size_t(c.w.b) * size_t(H) + size_t(c.w.h);
-        group_cost[g] += c.cost;
-        group_start[g + 1]++;
-    }
-    for (size_t g = 0; g < G; ++g) group_start[g + 1] += group_start[g];
-    std::vector<Costed> bucketed(all.size());
-    {
-        std::vector<int32_t> fill(group_start.begin(), group_start.end() - 1);
-        for (const Costed& c : all) bucketed[size_t(fill[size_t(c.w.b) * size_t(H) + size_t(c.w.h)]++)] = c;
-    }
-    std::vector<int32_t> groups;
-    groups.reserve(G);
-    for (size_t g = 0; g < G; ++g)
-        if (group_start[g + 1] > group_start[g]) groups.push_back(int32_t(g));
-    std::sort(groups.begin(), groups.end(), [&](int32_t a, int32_t b) {
-        if (group_cost[size_t(a)] != group_cost[size_t(b)]) return group_cost[size_t(a)] > group_cost[size_t(b)];
-        return a < b;
+    // head), then items by cost inside the group; the sort is stable so equal keys
+    // keep (sequence, head, tile) order and the plan is deterministic.
+    std::vector<int64_t> group_cost(size_t(B) * size_t(H), 0);
+    for (const Costed& c : all) group_cost[size_t(c.w.b) * size_t(H) + size_t(c.w.h)] += c.cost;
+    auto gkey = [&](const Costed& c) { return size_t(c.w.b) * size_t(H) + size_t(c.w.h); };
+    std::stable_sort(all.begin(), all.end(), [&](const Costed& a, const Costed& b) {
+        const size_t ga = gkey(a), gb = gkey(b);
+        if (ga != gb) {
+            if (group_cost[ga] != group_cost[gb]) return group_cost[ga] > group_cost[gb];
+            return ga < gb;
+        }
+        return a.cost > b.cost;
     });
-    size_t pos = 0;
-    for (int32_t g : groups) {
-        auto first = bucketed.begin() + group_start[size_t(g)], last = bucketed.begin() + group_start[size_t(g) + 1];
-        std::stable_sort(first, last, [](const Costed& a, const Costed& b) { return a.cost > b.cost; });
-        for (auto it = first; it != last; ++it) all[pos++] = *it;
-    }
 
     // Greedy: each item goes to the currently least-loaded CTA (ties: lowest index).
     using Slot = std::pair<int64_t, int32_t>;
