@@ -41,6 +41,19 @@ def test_reference_arm_prints_one_contract_line():
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
 
 
+def test_reference_arm_under_two_ranks_prints_once():
+    """Launched as two ranks, rank 0 alone runs the oracle and prints; the other rank exits 0."""
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", "29541", os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--workload", "tiny", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a GPU")
 def test_our_arm_fails_loudly_without_a_gpu():
     r = run_bench("--workload", "tiny", "--steps", "1", "--warmup", "3", timeout=300)
