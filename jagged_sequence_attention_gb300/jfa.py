@@ -401,6 +401,47 @@ def plan_for(batch, stream=None) -> Plan:
                            window=getattr(batch, "window", None))
 
 
+class JaggedAttention(torch.autograd.Function):
+    """The forward and backward passes as one torch.autograd function (argument marshalling
+    only: both passes run in the library's kernels, on the current stream).
+
+    Q [T_q, H, D], K, V [T_kv, H, D] (bf16 or fp32, contiguous); bias: the bucket table
+    [H, 32], or with dense set the dense per-pair bias [H, P] (fp32), or None.  Returns O in
+    Q's dtype.  The bias gradient is computed only when the bias requires one."""
+
+    @staticmethod
+    def forward(ctx, Q, K, V, bias, plan, scale, dense):
+        O, lse = jfa_fwd(plan, Q, K, V, None if dense else bias, scale, dense_bias=bias if dense else None)
+        ctx.plan, ctx.scale, ctx.dense = plan, scale, dense
+        ctx.save_for_backward(Q, K, V, O, lse, bias)
+        return O
+
+    @staticmethod
+    def backward(ctx, dO):
+        Q, K, V, O, lse, bias = ctx.saved_tensors
+        dO = dO.to(Q.dtype).contiguous()
+        table, dense = (None, bias) if ctx.dense else (bias, None)
+        if bias is not None and ctx.needs_input_grad[3]:
+            dQ, dK, dV, dbias = jfa_bwd_ex(ctx.plan, Q, K, V, O, dO, lse, table, ctx.scale, dense_bias=dense)
+        else:
+            (dQ, dK, dV), dbias = jfa_bwd(ctx.plan, Q, K, V, O, dO, lse, table, ctx.scale, dense_bias=dense), None
+        return dQ, dK, dV, dbias, None, None, None
+
+
+def jagged_attention(Q, K, V, q_offsets=None, kv_offsets=None, bias=None, mode="softmax", causal=False,
+                     window=None, scale=None, plan=None, dense_bias=False, kv_index=None):
+    """Differentiable jagged attention.  Builds the plan from the offsets (kv_index: shared
+    key/value, query set b attending to user kv_index[b]) unless one is given; a plan can be
+    reused while the batch's shape is the same.  See JaggedAttention for the tensors."""
+    if plan is None:
+        H, D = int(Q.shape[1]), int(Q.shape[2])
+        if kv_index is not None:
+            plan = jfa_plan_create_shared_kv(q_offsets, kv_offsets, kv_index, H, D, mode, causal, window=window)
+        else:
+            plan = jfa_plan_create(q_offsets, kv_offsets, H, D, mode, causal, window=window)
+    return JaggedAttention.apply(Q, K, V, bias, plan, scale, bool(dense_bias))
+
+
 def attention(batch, with_backward=True, stream=None, out_dtype=None, bias_grad=False):
     """Run forward (and backward) for a workloads.Batch on the GPU: returns dict of tensors
     (with bias_grad, also "dbias", the gradient of the batch's bias table)."""
