@@ -87,3 +87,21 @@ def test_autograd_dense_bias_gradient():
     torch.cuda.synchronize()
     assert torch.equal(O.detach(), direct["O"])
     assert torch.equal(dense.grad, direct["dbias"])
+
+
+def test_autograd_shared_key_value():
+    # query sets 0..4 over two users; dK and dV sum over each user's query sets
+    from jagged_sequence_attention_gb300 import jfa
+    users = [300, 129]
+    kv_map = [0, 1, 0, 0, 1]
+    q = [40, 7, 128, 1, 64]
+    b = wl.make_shared_kv(q, users, kv_map, H=2, D=128, bias=True, seed=34, device="cuda")
+    Q, K, V = leaf(b.Q), leaf(b.K), leaf(b.V)
+    O = jfa.jagged_attention(Q, K, V, b.q_off, b.kv_off, bias=b.bias, scale=b.scale, kv_index=b.kv_map)
+    O.backward(b.dO)
+    torch.cuda.synchronize()
+    direct = jfa.attention(b, with_backward=True, out_dtype=b.Q.dtype)
+    torch.cuda.synchronize()
+    assert torch.equal(O.detach(), direct["O"])
+    for got, key in ((Q.grad, "dQ"), (K.grad, "dK"), (V.grad, "dV")):
+        assert torch.equal(got, direct[key]), key
