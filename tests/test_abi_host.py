@@ -217,3 +217,21 @@ def test_binding_refuses_non_contiguous_tensors():
         jfa._ptr(t.t())
     assert e.value.status == jfa.JFA_ERR_INVALID_ARG
     assert jfa._ptr(None) is None
+
+
+def test_planning_without_a_gpu_fails_loudly():
+    # no CPU fallback: with no CUDA device, plan creation (and so every call and the autograd
+    # form) raises -- the library's NO_DEVICE, or CUDA's own error when the binding asks for the
+    # current stream first -- instead of computing anything on the host
+    import torch
+    from jagged_sequence_attention_gb300 import jfa
+    if torch.cuda.is_available():
+        pytest.skip("checks the behaviour without a GPU")
+    with pytest.raises((jfa.JFAError, RuntimeError)) as e:
+        jfa.jfa_plan_create([0, 3, 5], [0, 4, 9], 2, 64)
+    if isinstance(e.value, jfa.JFAError):
+        assert e.value.status == jfa.JFA_ERR_NO_DEVICE
+    Q = torch.zeros(5, 2, 64, dtype=torch.bfloat16, requires_grad=True)
+    K = torch.zeros(9, 2, 64, dtype=torch.bfloat16, requires_grad=True)
+    with pytest.raises((jfa.JFAError, RuntimeError)):
+        jfa.jagged_attention(Q, K, K, [0, 3, 5], [0, 4, 9])
