@@ -24,8 +24,9 @@
  *  - Q, O, dO, dQ are [T_q, H, D] row-major (token-major), T_q = q_offsets[B];
  *    K, V, dK, dV are [T_kv, H, D], T_kv = kv_offsets[B].  Contiguous, 16-byte
  *    aligned DEVICE pointers owned by the caller.  lse is fp32 [T_q, H].
- *  - Element type: JFA_BF16 (bfloat16, head_dim 64 or 128) or JFA_F32 (float,
- *    head_dim 32 or 64; the tensor cores compute in TF32).  Accumulation is fp32.
+ *  - Element type: JFA_BF16 (bfloat16, head_dim 64 or 128; tensor-core products)
+ *    or JFA_F32 (float, head_dim 32 or 64; plain fp32 arithmetic on the CUDA cores,
+ *    no TF32 rounding).  Accumulation is fp32.
  *  - Values must be finite: a key/value row of a neighbouring sequence is read
  *    (and multiplied by an exact zero weight) at jagged tile edges.
  *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
@@ -217,7 +218,7 @@ jfa_status jfa_bwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
  *     dbias is set (jfa_bwd_workspace_size otherwise), 256-byte aligned.
  *   The result is the same on every run: each CTA and warp sums its part in a fixed
  *   order, and a last kernel adds the parts in a fixed order.
- * Errors: those of jfa_bwd; INVALID_ARG for a dbias without JFA_BIAS_RELPOS32, a
+ * Errors: those of jfa_bwd; INVALID_ARG for a dbias with bias_kind JFA_BIAS_NONE, a
  * misaligned dbias or too small a workspace.
  */
 size_t jfa_bwd_ex_workspace_size(jfa_plan plan, int32_t dtype, int32_t bias_kind);
@@ -244,10 +245,14 @@ jfa_status jfa_bwd_ex(jfa_plan plan, int32_t dtype, const void* Q, const void* K
  *   no cudaMalloc, no cudaFree, no allocating library routine.  The plan's timing
  *   hook, when a caller has switched it on, creates CUDA events as it does for
  *   jfa_bwd; it is off by default.
- *   Set-up: the first call on a device, with that device current, looks up the
- *   array's device address and keeps it for later calls.  That look-up can load
- *   the library's module on the device, so make the first call before any stream
- *   capture.
+ *   Set-up: the first call in a CUDA context (normally the device's primary
+ *   context, made current by cudaSetDevice) looks up the array's device address
+ *   and keeps it, keyed by the context's unique id, for later calls in that
+ *   context.  A new context -- the primary context re-created after
+ *   cudaDeviceReset, or a caller's own driver-API context -- gets a fresh look-up,
+ *   and the array's contents do not survive a reset.  The look-up can load the
+ *   library's module on the device, so make the first call in each context before
+ *   any stream capture.
  *   Every call on a device uses the same array.  A call rewrites the row terms
  *   held there before reading them.  With JFA_F32 it also clears the dQ
  *   accumulator on its stream before adding anything in.  So no call depends on

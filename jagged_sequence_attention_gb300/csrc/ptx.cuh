@@ -114,12 +114,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Order this thread's generic-proxy shared-memory writes before later async-proxy
-// reads (tcgen05.mma operands, TMA stores).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05 / TMEM
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -159,36 +153,10 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
         : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T-or-not, per the instruction descriptor.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
+// Element format codes of the kind::f16 instruction descriptor.
+enum : uint32_t { kFmtF16 = 0, kFmtBF16 = 1 };
 
-// D[tmem] (+)= A[tmem] * B[smem]: A (M rows in TMEM lanes, 16-bit elements packed two
-// per 32-bit column along K) read from Tensor Memory at a_tmem.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-
-// Element format codes of the kind::f16 / kind::tf32 instruction descriptor.
-enum : uint32_t { kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2 };
-
-// Instruction descriptor (32 bits) for dense kind::f16 / kind::tf32 with an fp32
+// Instruction descriptor (32 bits) for dense kind::f16 with an fp32
 // accumulator: [4,6) D format (1 = f32), [7,10) A format, [10,13) B format,
 // bit 15 A is MN-major, bit 16 B is MN-major, [17,23) N>>3, [24,29) M>>4.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t fmt, int M, int N, bool a_mn, bool b_mn) {
@@ -261,13 +229,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : JFA_R8(0), JFA_R8(8), JFA_R8(16), JFA_R8(24)
         : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : JFA_R8(0), JFA_R8(8)
-        : "r"(taddr));
-}
 #undef JFA_R8
 #define JFA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
                   "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
@@ -307,10 +268,6 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 
 // ---------------------------------------------------------------- misc
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -389,16 +346,6 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
     return d;
 }
 
-// Register budget of the calling warpgroup (all its warps execute it).
-template <int N>
-__device__ __forceinline__ void reg_alloc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void reg_dealloc() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
@@ -416,20 +363,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
     float y;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-__device__ __forceinline__ float tanh_approx(float x) {
-    float y;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128-byte-swizzled
-// block whose rows are 128 bytes (the layout TMA SWIZZLE_128B writes and the
-// SWIZZLE_128B descriptor reads): 8-row groups of 1024 bytes, chunk XOR (row mod 8).
-__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
-    return uint32_t(row >> 3) * 1024u + uint32_t(row & 7) * 128u +
-           uint32_t((chunk ^ (row & 7)) << 4);
 }
 
 }  // namespace jfa

@@ -16,18 +16,9 @@ __device__ __forceinline__ int relpos_bucket(int r) {
     return r >= 46340 ? 31 : b;
 }
 
-// For 32 consecutive columns whose relative positions run from r_hi down to
-// r_hi - 31: true when all of them are >= 0 and fall in one bucket (the bucket is
-// non-decreasing in r), so the chunk's bias is the single value bucket(r_hi).
-__device__ __forceinline__ bool chunk_bucket_const(int r_hi, int& bucket) {
-    const int r_lo = r_hi - 31;
-    bucket = relpos_bucket(r_hi);
-    return r_lo >= 0 && relpos_bucket(r_lo) == bucket;
-}
-
-// Warp-level form of the test above.  In the callers, the 32 lanes' windows for one
-// chunk tile a range of 63 relative positions [lo, lo + 62] (consecutive rows or keys
-// shift the window by one).  The bucket of |r| is monotone on a range that does not
+// Warp-level test of whether a 32-column chunk's bias is one value.  In the callers,
+// the 32 lanes' windows for one chunk tile a range of 63 relative positions
+// [lo, lo + 62] (consecutive rows or keys shift the window by one).  The bucket of |r| is monotone on a range that does not
 // cross 0, so every lane's chunk is constant exactly when the whole range lies on one
 // side of 0 and its two ends share a bucket; then all lanes share that bucket.  Each
 // lane evaluates one chunk (the caller passes lane k the range of chunk k); returns the

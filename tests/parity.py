@@ -209,3 +209,39 @@ def sampled_parity(batch, gpu, samples, with_backward=True):
         for k in ("dQ", "dK", "dV"):
             m[f"{k}_rel_frob"] = rel_frob(cat(got[k]), cat(ref[k]))
     return m
+
+
+def causal_row_blocks(L, n):
+    """Boundaries 0 = i_0 < ... < i_n = L giving blocks of about equal causal cost (a
+    row i costs about i + 1 keys, so block k ends near L sqrt(k / n))."""
+    cuts = sorted(set([0, L] + [int(round(L * np.sqrt(k / n))) for k in range(1, n)]))
+    return [(a, b) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+
+
+def causal_head_oracle(Q, K, V, dO, bias_h, scale, n_blocks=48):
+    """Oracle O, lse, dQ, dK, dV ([L, D] / [L]) of one causal self-attention head given as
+    fp64 [L, D] arrays, computed block by block so that the oracle, which parallelises
+    over (sequence, head) problems, uses every core on one long sequence.
+
+    The split is exact.  In causal self-attention (q_len = kv_len), rows [i0, i1) see
+    only keys [0, i1).  As a sub-problem with q_len' = i1 - i0 and kv_len' = i1, the
+    bottom-right alignment puts local row r at position r + i0, so it sees the same
+    keys, at the same relative positions, as global row i0 + r: O, lse and dQ of the
+    block's rows come out exactly, and dK, dV (sums over rows) are the sums of the
+    blocks' contributions."""
+    L, D = Q.shape
+    blocks = causal_row_blocks(L, n_blocks)
+    q_off = wl.offsets([b - a for a, b in blocks])
+    kv_off = wl.offsets([b for _, b in blocks])
+    cat = lambda X, sl: np.concatenate([X[s] for s in sl])[:, None, :]  # noqa: E731
+    rows = [slice(a, b) for a, b in blocks]
+    keys = [slice(0, b) for _, b in blocks]
+    Qc, dOc, Kc, Vc = cat(Q, rows), cat(dO, rows), cat(K, keys), cat(V, keys)
+    O, LSE = oracle.fwd(q_off, kv_off, Qc, Kc, Vc, causal=True, bias=bias_h, scale=scale)
+    dQ, dKc, dVc = oracle.bwd(q_off, kv_off, Qc, Kc, Vc, dOc, causal=True, bias=bias_h, scale=scale)
+    dK = np.zeros((L, D))
+    dV = np.zeros((L, D))
+    for k, (_, b) in enumerate(blocks):
+        dK[:b] += dKc[kv_off[k]:kv_off[k + 1], 0]
+        dV[:b] += dVc[kv_off[k]:kv_off[k + 1], 0]
+    return {"O": O[:, 0], "lse": LSE[:, 0], "dQ": dQ[:, 0], "dK": dK, "dV": dV}

@@ -52,6 +52,18 @@ def test_library_exports_every_declared_symbol(jfa):
     assert set(jfa.EXPORTED) <= exported
 
 
+def test_binding_constants_match_the_header(jfa):
+    """The binding restates a few of the header's numbers; they must agree."""
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+JFA_STATIC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", text)
+    assert m, "JFA_STATIC_SCRATCH_BYTES not found in the header"
+    assert jfa.JFA_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+    body = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    enums = dict((k, int(v)) for k, v in re.findall(r"\b(JFA_[A-Z0-9_]+)\s*=\s*(\d+)", body))
+    for name, value in enums.items():
+        assert getattr(jfa, name) == value, name
+
+
 def test_status_strings(jfa):
     for s in range(8):
         assert jfa.jfa_status_string(s) and jfa.jfa_status_string(s) != "unknown status"
