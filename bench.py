@@ -62,10 +62,17 @@ def flops_of(batch):
     return fwd, 2.5 * fwd
 
 
-def algorithmic_bytes(batch, elem=2):
+def algorithmic_bytes(batch, elem=2, fused=False):
     """Compulsory HBM bytes of one launch of each tensor-core kernel: every input it
-    reads and every output it writes, once."""
+    reads and every output it writes, once.  The fused backward reads Q, dO, K, V and
+    writes dK, dV and dQ (its fp32 dQ accumulator is implementation traffic, not
+    algorithmic)."""
     Tq, Tkv, H, D = int(batch.q_off[-1]), int(batch.kv_off[-1]), batch.H, batch.D
+    if fused:
+        return {
+            "fwd": elem * H * D * (2 * Tq + 2 * Tkv) + 4 * H * Tq,         # Q,K,V -> O; lse
+            "bwd_main": elem * H * D * (3 * Tq + 4 * Tkv) + 8 * H * Tq,    # Q,dO,K,V -> dQ,dK,dV; lse,Delta
+        }
     return {
         "fwd": elem * H * D * (2 * Tq + 2 * Tkv) + 4 * H * Tq,             # Q,K,V -> O; lse
         "bwd_main": elem * H * D * (2 * Tq + 4 * Tkv) + 8 * H * Tq,        # Q,dO,K,V -> dK,dV; lse,Delta
@@ -73,11 +80,14 @@ def algorithmic_bytes(batch, elem=2):
     }
 
 
-def kernel_flops(fwd_flop):
+def kernel_flops(fwd_flop, fused=False):
     """Algorithmic FLOPs per launch of each tensor-core kernel.  The backward's five
-    products (S, dP, dV, dK, dQ; 2.5x the forward's two) split as: dK/dV kernel S, dP,
-    dV, dK (2x), dQ kernel the dQ product (0.5x); its recomputed S and dP are not
-    algorithmic work and are not counted."""
+    products (S, dP, dV, dK, dQ; 2.5x the forward's two) all run in the fused backward
+    kernel; on the two-pass backward they split as: dK/dV kernel S, dP, dV, dK (2x), dQ
+    kernel the dQ product (0.5x), whose recomputed S and dP are not algorithmic work and
+    are not counted."""
+    if fused:
+        return {"fwd": fwd_flop, "bwd_main": 2.5 * fwd_flop}
     return {"fwd": fwd_flop, "bwd_main": 2.0 * fwd_flop, "bwd_dq": 0.5 * fwd_flop}
 
 
@@ -299,12 +309,15 @@ def main():
         batch = wl.broadcast(batch)
     fl_f, fl_b = flops_of(batch)
     job_flop = fl_f + fl_b  # summed over ranks below: the work all ranks processed
-    kbytes = algorithmic_bytes(batch)
     cfg.update({"tokens": int(batch.q_off[-1]), "kv_tokens": int(batch.kv_off[-1]),
                 "unpadded_fwd_flop": fl_f, "unpadded_bwd_flop": fl_b})
 
     stream = torch.cuda.current_stream()
     plan = jfa.plan_for(batch)
+    # jfa_bwd on bf16 inputs (no dense bias, no bias gradient) runs the fused backward
+    fused = batch.Q.dtype == torch.bfloat16 and jfa.jfa_plan_info(plan)["bwd_fused"] == 1
+    kbytes = algorithmic_bytes(batch, fused=fused)
+    cfg["backward"] = "fused dK/dV/dQ kernel" if fused else "dK/dV kernel + dQ kernel"
     O = torch.empty_like(batch.Q)
     lse = torch.empty((batch.Q.shape[0], batch.H), dtype=torch.float32, device=dev)
     dQ, dK, dV = torch.empty_like(batch.Q), torch.empty_like(batch.K), torch.empty_like(batch.V)
@@ -359,8 +372,10 @@ def main():
 
     # dominant kernel: the largest share of device time among the tensor-core kernels
     per = {k: (v[0] / v[1] if v[1] else 0.0, v[1], v[0]) for k, v in kt.items()}
-    kflop = kernel_flops(fl_f)
-    kname_of = {"fwd": "jfa_fwd_kernel", "bwd_main": "jfa_bwd_dkdv_kernel", "bwd_dq": "jfa_bwd_dq_kernel"}
+    kflop = kernel_flops(fl_f, fused)
+    kname_of = {"fwd": "jfa_fwd_kernel", "bwd_main": "jfa_bwd_fused_kernel" if fused else "jfa_bwd_dkdv_kernel"}
+    if not fused:
+        kname_of["bwd_dq"] = "jfa_bwd_dq_kernel"
     dom = max(kname_of, key=lambda k: per[k][2])
     dom_ms = per[dom][0]
     achieved = kflop[dom] / (dom_ms / 1e3) / 1e12 if dom_ms > 0 else 0.0

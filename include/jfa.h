@@ -160,7 +160,12 @@ jfa_status jfa_plan_destroy(jfa_plan plan);
  * jfa_plan_create_shared_kv), and 1 when the forward runs the kernel with split items
  * (sequences of one query tile whose key range is split in two halves that are merged
  * at the end; chosen when such items carry at least half the forward's tensor-core
- * products and the plan has no window), else 0.  n may be smaller than 19.
+ * products and the plan has no window), else 0, and 1 when jfa_bwd on JFA_BF16 inputs
+ * (without a dense bias or a bias gradient) may run the fused backward, in which every
+ * key tile also adds its part of dQ into an fp32 accumulator held in the workspace, else
+ * 0.  The planner chooses the fused form when the backward's key tiles visit few query
+ * tiles on average (short sequences), unless jfa_plan_set_deterministic chose the
+ * two-pass form; see jfa_plan_set_deterministic.  n may be smaller than 20.
  */
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
 
@@ -181,7 +186,8 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
                    float* lse, void* stream);
 
 /* Bytes of device workspace jfa_bwd needs for this plan and dtype: fp32 row terms
- * [T_q,H], and for JFA_F32 also an fp32 dQ accumulator [T_q,H,D]; 0 on a bad plan. */
+ * [T_q,H], and an fp32 dQ accumulator [T_q,H,D] for JFA_F32 and for plans whose bf16
+ * backward may be fused (jfa_plan_info fact 19); 0 on a bad plan. */
 size_t jfa_bwd_workspace_size(jfa_plan plan, int32_t dtype);
 
 /*
@@ -229,8 +235,10 @@ jfa_status jfa_bwd_ex(jfa_plan plan, int32_t dtype, const void* Q, const void* K
 
 /* Size of the library-held scratch array that jfa_bwd_static_scratch uses on each
  * GPU (64 MiB).  A plan fits when jfa_bwd_workspace_size(plan, dtype) is at most
- * this: T_q * H up to about 16.7 million (token, head) rows for JFA_BF16, and
- * about 258,000 for JFA_F32 at head_dim 64. */
+ * this.  With an fp32 dQ accumulator in the scratch (JFA_F32, and JFA_BF16 on a fused
+ * backward) that is T_q * H up to about 130,000 (token, head) rows at head_dim 128 and
+ * 258,000 at head_dim 64; with row terms alone (shared key/value plans on JFA_BF16),
+ * about 16.7 million. */
 #define JFA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 
 /*
@@ -254,8 +262,9 @@ jfa_status jfa_bwd_ex(jfa_plan plan, int32_t dtype, const void* Q, const void* K
  *   library's module on the device, so make the first call in each context before
  *   any stream capture.
  *   Every call on a device uses the same array.  A call rewrites the row terms
- *   held there before reading them.  With JFA_F32 it also clears the dQ
- *   accumulator on its stream before adding anything in.  So no call depends on
+ *   held there before reading them.  Where the scratch holds a dQ accumulator
+ *   (JFA_F32, and JFA_BF16 on a fused backward) it also clears that on its stream
+ *   before adding anything in.  So no call depends on
  *   what an earlier call left there.  Calls that may overlap on the GPU race on the
  *   array and corrupt each other's gradients: order them on one stream, or by
  *   events.
@@ -269,6 +278,28 @@ jfa_status jfa_bwd_static_scratch(jfa_plan plan, int32_t dtype, const void* Q, c
                                   const void* V, const void* O, int32_t o_dtype, const void* dO,
                                   const float* lse, int32_t bias_kind, const float* bias_table,
                                   float scale, void* dQ, void* dK, void* dV, void* stream);
+
+/*
+ * The bf16 backward has two forms (the articles leave the backward's accumulation open;
+ * see jfa_bwd):
+ *   fused: one kernel over key tiles forms dK, dV and each key tile's part of dQ, adding
+ *     the parts into an fp32 accumulator in the workspace with reduce-adds at L2, and a
+ *     conversion pass writes dQ.  The order of the additions varies from run to run, so
+ *     dQ can differ in its last bit between runs; dK and dV do not.
+ *   two-pass: a second kernel over query tiles recomputes S and dP and accumulates dQ
+ *     on chip, with no atomics: every result is the same bit for bit on every run, at
+ *     1.4x the tensor-core work of the backward.
+ * By default (enable = 0) the planner picks the faster form for the batch: fused when
+ * the key tiles visit few query tiles on average (short sequences, where it saves the
+ * second pass), two-pass otherwise (long sequences, where the reduce-adds cost more than
+ * the recomputation).  enable = 1 always runs the two-pass form.  Shared key/value plans
+ * (unless their merged view is used), a dense bias and bias gradients always run the
+ * two-pass form.  The choice changes jfa_bwd_workspace_size (the fused backward needs the
+ * fp32 accumulator); query it after this call.  jfa_plan_info fact 19 reports the form.
+ * fp32 inputs are unaffected.
+ * Errors: INVALID_ARG for a null plan or enable not 0 or 1.
+ */
+jfa_status jfa_plan_set_deterministic(jfa_plan plan, int32_t enable);
 
 /* Synchronises `stream`, then reads and clears the plan's device status word, which
  * the kernels set when a pipeline wait times out (TIMEOUT) or a bounds check fires

@@ -251,6 +251,15 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
         build_worklist(qo.data(), ko.data(), B, H, causal, window, kPassBwdKV, p->bwd_grid, bi.data(), bo.data(),
                        nullptr);
     build_worklist(qo.data(), kvv.data(), B, H, causal, window, kPassBwdQ, p->dq_grid, qi.data(), qio.data(), nullptr);
+    {
+        // Backward form: the fused kernel saves the whole dQ pass but pays more per step
+        // (dQ's reduce-adds and their drain), so it wins while key tiles visit few query
+        // tiles (short sequences) and loses on long ones.
+        int64_t total_steps = 0;
+        if (!kv_map)
+            for (int64_t i = 0; i < p->n_bwd_items; ++i) total_steps += bi[size_t(i)].n_inner;
+        p->fused_pref = !kv_map && p->n_bwd_items > 0 && total_steps <= kFusedMaxMeanSteps * p->n_bwd_items;
+    }
     std::vector<int64_t> po(size_t(B) + 1, 0);  // pair offsets of a dense bias
     for (int32_t b = 0; b < B; ++b)
         po[size_t(b) + 1] = po[size_t(b)] + int64_t(qo[size_t(b) + 1] - qo[size_t(b)]) * int64_t(kvv[size_t(b) + 1] - kvv[size_t(b)]);
@@ -415,13 +424,20 @@ jfa_status jfa_plan_destroy(jfa_plan plan) {
 
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
     if (!plan || !info || n < 0) return JFA_ERR_INVALID_ARG;
-    const int64_t v[19] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
+    const int64_t v[20] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
                            plan->mode,     plan->causal,  plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items,
                            plan->bwd_grid, plan->num_sms, plan->n_dq_items,  plan->dq_grid,  plan->window,
                            plan->n_pairs,  plan->shared_kv ? plan->U : -1,
                            plan->merged ? int64_t(plan->merged->B) : -1,
-                           plan->fwd_split ? 1 : 0};
-    for (int32_t i = 0; i < n && i < 19; ++i) info[i] = v[i];
+                           plan->fwd_split ? 1 : 0,
+                           fused_backward(plan) ? 1 : 0};
+    for (int32_t i = 0; i < n && i < 20; ++i) info[i] = v[i];
+    return JFA_OK;
+}
+
+jfa_status jfa_plan_set_deterministic(jfa_plan plan, int32_t enable) {
+    if (!plan || (enable != 0 && enable != 1)) return JFA_ERR_INVALID_ARG;
+    plan->deterministic = enable != 0;
     return JFA_OK;
 }
 
@@ -518,8 +534,10 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
 size_t jfa_bwd_workspace_size(jfa_plan plan, int32_t dtype) {
     if (!plan || (dtype != JFA_BF16 && dtype != JFA_F32)) return 0;
     const size_t rows = size_t(plan->Tq) * size_t(plan->H);
-    // row terms; fp32 inputs also accumulate dQ in fp32 before converting it
-    return round_up(rows * 4, 256) + (dtype == JFA_F32 ? round_up(rows * size_t(plan->D) * 4, 256) : 0);
+    // row terms; fp32 inputs, and bf16 inputs on the fused backward, also accumulate dQ in
+    // fp32 before converting it
+    const bool acc = dtype == JFA_F32 || fused_backward(plan);
+    return round_up(rows * 4, 256) + (acc ? round_up(rows * size_t(plan->D) * 4, 256) : 0);
 }
 
 // Bytes of the partial table gradients: one [H][32] table per (CTA, compute warp) of
@@ -590,9 +608,13 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
     }
     if (plan->Tkv == 0 && plan->Tq == 0) return JFA_OK;
     const size_t rows = size_t(plan->Tq) * size_t(plan->H);
+    // bf16 inputs without a dense bias or a bias gradient: dK, dV and dQ in one kernel that
+    // adds dQ into an fp32 accumulator (bwd_fused.cu)
+    const bool fused = dtype == JFA_BF16 && !plan->deterministic && v->fused_pref && !dense && !dbias;
     float* delta = static_cast<float*>(workspace);
-    float* dq_acc = dtype == JFA_F32 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * 4, 256))
-                                     : nullptr;
+    float* dq_acc = (dtype == JFA_F32 || fused)
+                        ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * 4, 256))
+                        : nullptr;
     float* dbias_part = (dbias && !dense) ? reinterpret_cast<float*>(static_cast<char*>(workspace) + base) : nullptr;
 
     cudaError_t e = cudaSuccess;
@@ -644,7 +666,8 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
     }
     if (v->n_bwd_items > 0) {
         KernelTimer tm(plan, 2, st);
-        e = dtype == JFA_BF16 ? launch_bwd_main(dtype, plan->D, mq, mk, mv, mdo, p, v->bwd_grid, st)
+        e = dtype == JFA_BF16 ? (fused ? launch_bwd_fused(plan->D, mq, mk, mv, mdo, p, v->bwd_grid, st)
+                                       : launch_bwd_main(dtype, plan->D, mq, mk, mv, mdo, p, v->bwd_grid, st))
                               : launch_bwd_f32(plan->D, Q, K, V, dO, p, v->n_bwd_items, st);
         tm.done();
         if (e != cudaSuccess) return JFA_ERR_CUDA;
@@ -656,7 +679,7 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
         }
         p.dbias_part = nullptr;  // the dQ pass does not take part
     }
-    if (dtype == JFA_BF16 && v->n_dq_items > 0) {
+    if (dtype == JFA_BF16 && !fused && v->n_dq_items > 0) {
         // dQ per query tile, written directly (also the zero rows of tiles that see no key)
         p.items = v->d_dq_items;
         p.cta_off = v->d_dq_cta_off;
@@ -667,7 +690,7 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
         tm.done();
         if (e != cudaSuccess) return JFA_ERR_CUDA;
     }
-    if (dtype == JFA_F32 && plan->Tq > 0) {
+    if ((dtype == JFA_F32 || fused) && plan->Tq > 0) {
         KernelTimer tm(plan, 3, st);
         e = launch_bwd_post(dtype, plan->D, dq_acc, dQ, plan->Tq, plan->H, scale, st);
         tm.done();

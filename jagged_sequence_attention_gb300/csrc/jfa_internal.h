@@ -158,7 +158,7 @@ struct BwdParams {
     const float* bias;
     const float* lse;    // [T_q,H] (softmax)
     const float* delta;  // [T_q,H] rowsum(dO*O) (softmax)
-    float* dq_acc;       // [T_q,H,D] fp32, zeroed by the preprocess kernel (fp32 inputs only)
+    float* dq_acc;       // [T_q,H,D] fp32, zeroed first (fp32 inputs; bf16 inputs on the fused backward)
     void* dQ;            // [T_q,H,D] (bf16 inputs: written by the dQ kernel)
     void* dK;
     void* dV;
@@ -216,6 +216,18 @@ cudaError_t launch_bwd_dq(int dtype, int D, const CUtensorMap& tmQ, const CUtens
                           int grid, cudaStream_t st);
 cudaError_t launch_bwd_post(int dtype, int D, const float* dq_acc, void* dQ, int64_t Tq, int H,
                             float scale, cudaStream_t st);
+// bf16 inputs, fused backward (bwd_fused.cu): dK, dV and the key tile's part of dQ, added
+// into p.dq_acc (zeroed first) for launch_bwd_post to scale and convert.
+cudaError_t launch_bwd_fused(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st);
+// Whether jfa_bwd on bf16 inputs runs the fused backward for this plan (without a dense
+// bias or a bias gradient): plans whose dK/dV items visit at most kFusedMaxMeanSteps
+// query tiles on average (not shared key/value plans), unless the caller asked for the
+// deterministic two-pass backward.  On GB300 the fused kernel measured faster on the
+// short-sequence workloads (1 to 4 query tiles per key tile) and 1.2x slower on 32K-token
+// causal sequences (about 90).
+constexpr int64_t kFusedMaxMeanSteps = 6;
+inline bool fused_backward(const jfa_plan_t* plan);
 
 // fp32 element type: CUDA-core kernels, one CTA per work item (f32.cu).
 cudaError_t launch_fwd_f32(int D, const void* Q, const void* K, const void* V, const FwdParams& p, int64_t n_items,
@@ -264,8 +276,14 @@ struct jfa_plan_t {
     int64_t n_fwd_items, n_bwd_items, n_dq_items;
     int fwd_grid, bwd_grid, dq_grid;
     bool fwd_split;  // forward kernel with split items (prefer_split_forward)
+    bool deterministic = false;  // jfa_plan_set_deterministic: the two-pass bf16 backward
+    bool fused_pref = false;     // the planner's choice of the fused bf16 backward
     // optional per-kernel timing (jfa_plan_set_timing)
     bool timing;
     std::vector<cudaEvent_t> ev_pool;                 // reusable events
     std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> ev_pending;  // kind, (start, stop)
 };
+
+inline bool jfa::fused_backward(const jfa_plan_t* plan) {
+    return !plan->deterministic && (plan->fused_pref || (plan->merged && plan->merged->fused_pref));
+}

@@ -114,6 +114,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before later async-proxy
+// reads (tcgen05.mma operands).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05 / TMEM
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -318,6 +324,14 @@ __device__ __forceinline__ void store_chunk_bf16(uint32_t stg, const uint32_t (&
         if ((valid >> r) & 1u) *reinterpret_cast<uint4*>(dst + size_t(r) * stride + 8 * piece) = u;
     }
     __syncwarp();
+}
+
+// Adds four consecutive fp32 values (bits in v) to global memory at a 16-byte aligned
+// address, as one vector reduction performed at L2.
+__device__ __forceinline__ void red_add_v4(float* addr, uint4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(__uint_as_float(v.x)),
+                 "f"(__uint_as_float(v.y)), "f"(__uint_as_float(v.z)), "f"(__uint_as_float(v.w))
+                 : "memory");
 }
 
 // Packed dual fp32 arithmetic (fma/add on a pair of floats, one instruction).

@@ -1,7 +1,8 @@
 // jfa_bwd_static_scratch: the backward pass with its scratch held by the library.
 //
-// jfa_bwd needs scratch: the softmax row terms [T_q, H], and for fp32 inputs an fp32
-// dQ accumulator [T_q, H, D] into which every key/value tile adds its share.
+// jfa_bwd needs scratch: the softmax row terms [T_q, H], and (for fp32 inputs, and bf16
+// inputs on the fused backward) an fp32 dQ accumulator [T_q, H, D] into which every
+// key/value tile adds its share.
 // Callers of jfa_bwd must pass that scratch in, which some cannot do.  Such callers include
 // host code that owns no device allocator (the memory it works in was handed to it
 // by another runtime), and programs whose device memory is all reserved by a pool
@@ -21,8 +22,8 @@
 // device, so make it before any stream capture.
 //
 // The launches themselves are those of jfa_bwd, given the array as its workspace:
-// the preprocess writes every row term before a later kernel reads one and, for
-// fp32 inputs, clears the dQ accumulator on the stream before anything adds to it.
+// the preprocess writes every row term before a later kernel reads one and clears
+// the dQ accumulator, where there is one, on the stream before anything adds to it.
 // So a call never depends on what an earlier call left in the array.
 #include <cuda.h>
 #include <cuda_runtime.h>

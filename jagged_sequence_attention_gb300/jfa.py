@@ -32,7 +32,7 @@ EXPORTED = ["jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_pl
             "jfa_bwd", "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build",
             "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times", "jfa_bwd_static_scratch",
             "jfa_partition_sequences", "jfa_bwd_ex_workspace_size", "jfa_bwd_ex", "jfa_plan_create_shared_kv",
-            "jfa_partition_users"]
+            "jfa_partition_users", "jfa_plan_set_deterministic"]
 
 
 class JFAError(RuntimeError):
@@ -72,13 +72,14 @@ def lib():
         L.jfa_worklist_size.argtypes = [vp, vp, i32, i32, i32, i32, i32, P(i64)]
         L.jfa_worklist_build.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
         L.jfa_plan_set_timing.argtypes = [vp, i32]
+        L.jfa_plan_set_deterministic.argtypes = [vp, i32]
         L.jfa_plan_kernel_times.argtypes = [vp, vp, vp]
         L.jfa_status_string.argtypes = [i32]
         L.jfa_status_string.restype = ctypes.c_char_p
         for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
                      "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build", "jfa_plan_set_timing",
                      "jfa_plan_kernel_times", "jfa_bwd_static_scratch", "jfa_partition_sequences", "jfa_bwd_ex",
-                     "jfa_plan_create_shared_kv", "jfa_partition_users"):
+                     "jfa_plan_create_shared_kv", "jfa_partition_users", "jfa_plan_set_deterministic"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -192,7 +193,7 @@ def jfa_plan_destroy(plan: Plan):
 
 INFO_KEYS = ["T_q", "T_kv", "B", "H", "D", "mode", "causal", "fwd_items", "fwd_grid", "bwd_items", "bwd_grid",
              "num_sms", "dq_items", "dq_grid", "window", "pairs", "users", "merged",
-             "fwd_split"]
+             "fwd_split", "bwd_fused"]
 
 
 def jfa_plan_info(plan: Plan) -> dict:
@@ -309,6 +310,13 @@ def jfa_plan_device_status(plan: Plan, stream=None) -> int:
 KERNEL_KINDS = ["fwd", "bwd_pre", "bwd_main", "bwd_post", "bwd_dq"]
 
 
+def jfa_plan_set_deterministic(plan: Plan, enable: bool = True):
+    """enable: always the two-pass bf16 backward, the same bit for bit on every run; off
+    (the default): the planner's choice, the fused backward on short sequences (whose dQ
+    can differ in its last bit between runs), the two-pass one on long ones."""
+    _check("jfa_plan_set_deterministic", lib().jfa_plan_set_deterministic(plan.handle, int(bool(enable))))
+
+
 def jfa_plan_set_timing(plan: Plan, enable: bool = True):
     _check("jfa_plan_set_timing", lib().jfa_plan_set_timing(plan.handle, int(bool(enable))))
 
@@ -392,13 +400,18 @@ def jfa_worklist_build(q_offsets, kv_offsets, H: int, causal: bool, pass_: int, 
 # --------------------------------------------------------------------------- convenience
 
 
-def plan_for(batch, stream=None) -> Plan:
-    """The plan of a workloads.Batch: shared key/value when it has a query-set-to-user map."""
+def plan_for(batch, stream=None, deterministic=False) -> Plan:
+    """The plan of a workloads.Batch: shared key/value when it has a query-set-to-user map.
+    deterministic: the two-pass backward (see jfa_plan_set_deterministic)."""
     if getattr(batch, "kv_map", None) is not None:
-        return jfa_plan_create_shared_kv(batch.q_off, batch.kv_off, batch.kv_map, batch.H, batch.D, batch.mode,
+        plan = jfa_plan_create_shared_kv(batch.q_off, batch.kv_off, batch.kv_map, batch.H, batch.D, batch.mode,
                                          batch.causal, stream, window=getattr(batch, "window", None))
-    return jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal, stream,
-                           window=getattr(batch, "window", None))
+    else:
+        plan = jfa_plan_create(batch.q_off, batch.kv_off, batch.H, batch.D, batch.mode, batch.causal, stream,
+                               window=getattr(batch, "window", None))
+    if deterministic:
+        jfa_plan_set_deterministic(plan, True)
+    return plan
 
 
 class JaggedAttention(torch.autograd.Function):
@@ -429,23 +442,27 @@ class JaggedAttention(torch.autograd.Function):
 
 
 def jagged_attention(Q, K, V, q_offsets=None, kv_offsets=None, bias=None, mode="softmax", causal=False,
-                     window=None, scale=None, plan=None, dense_bias=False, kv_index=None):
+                     window=None, scale=None, plan=None, dense_bias=False, kv_index=None, deterministic=False):
     """Differentiable jagged attention.  Builds the plan from the offsets (kv_index: shared
     key/value, query set b attending to user kv_index[b]) unless one is given; a plan can be
-    reused while the batch's shape is the same.  See JaggedAttention for the tensors."""
+    reused while the batch's shape is the same.  deterministic: a new plan runs the two-pass
+    backward (see jfa_plan_set_deterministic).  See JaggedAttention for the tensors."""
     if plan is None:
         H, D = int(Q.shape[1]), int(Q.shape[2])
         if kv_index is not None:
             plan = jfa_plan_create_shared_kv(q_offsets, kv_offsets, kv_index, H, D, mode, causal, window=window)
         else:
             plan = jfa_plan_create(q_offsets, kv_offsets, H, D, mode, causal, window=window)
+        if deterministic:
+            jfa_plan_set_deterministic(plan, True)
     return JaggedAttention.apply(Q, K, V, bias, plan, scale, bool(dense_bias))
 
 
-def attention(batch, with_backward=True, stream=None, out_dtype=None, bias_grad=False):
+def attention(batch, with_backward=True, stream=None, out_dtype=None, bias_grad=False, deterministic=False):
     """Run forward (and backward) for a workloads.Batch on the GPU: returns dict of tensors
-    (with bias_grad, also "dbias", the gradient of the batch's bias table)."""
-    plan = plan_for(batch, stream)
+    (with bias_grad, also "dbias", the gradient of the batch's bias table).  deterministic:
+    the two-pass backward (see jfa_plan_set_deterministic)."""
+    plan = plan_for(batch, stream, deterministic)
     dense = getattr(batch, "dense", None)
     O, lse = jfa_fwd(plan, batch.Q, batch.K, batch.V, batch.bias, batch.scale, stream=stream, out_dtype=out_dtype,
                      dense_bias=dense)

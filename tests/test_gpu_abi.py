@@ -86,8 +86,10 @@ def test_timing_hook_counts_launches(jfa):
         O, lse = jfa.jfa_fwd(p, b.Q, b.K, b.V)
         jfa.jfa_bwd(p, b.Q, b.K, b.V, O, b.dO, lse)
     t = jfa.jfa_plan_kernel_times(p)
-    # bf16: the dQ pass replaces the fp32 accumulator conversion
-    assert {k: v[1] for k, v in t.items()} == {"fwd": 3, "bwd_pre": 3, "bwd_main": 3, "bwd_post": 0, "bwd_dq": 3}
+    # bf16 on a fused backward: the main kernel adds dQ into an fp32 accumulator that the
+    # conversion pass scales and writes; the dQ pass does not run
+    assert jfa.jfa_plan_info(p)["bwd_fused"] == 1
+    assert {k: v[1] for k, v in t.items()} == {"fwd": 3, "bwd_pre": 3, "bwd_main": 3, "bwd_post": 3, "bwd_dq": 0}
     assert all(v[0] > 0 for v in t.values() if v[1])
     assert all(v[1] == 0 for v in jfa.jfa_plan_kernel_times(p).values())
 

@@ -99,6 +99,7 @@ def test_deterministic_and_same_gradients_as_jfa_bwd():
     from jagged_sequence_attention_gb300 import jfa
     b = wl.make_custom(LENS, LENS, H=2, D=128, causal=True, bias=True, device="cuda", seed=38)
     plan = jfa.jfa_plan_create(b.q_off, b.kv_off, b.H, b.D, b.mode, b.causal)
+    jfa.jfa_plan_set_deterministic(plan, True)  # jfa_bwd then runs the two-pass form, as jfa_bwd_ex does
     O, lse = jfa.jfa_fwd(plan, b.Q, b.K, b.V, b.bias, b.scale)
     g1 = jfa.jfa_bwd_ex(plan, b.Q, b.K, b.V, O, b.dO, lse, b.bias, b.scale)
     g2 = jfa.jfa_bwd_ex(plan, b.Q, b.K, b.V, O, b.dO, lse, b.bias, b.scale)
