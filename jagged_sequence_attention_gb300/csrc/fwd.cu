@@ -10,14 +10,18 @@
 // The GDPA mode (aihot.vn, "Generalized Dot-Product Attention (GDPA)") swaps the
 // online softmax for an elementwise GELU/SiLU with no normalisation.
 //
-// CTA = 10 warps, persistent, one CTA per SM, work list from the planner.  Two query
+// CTA = 18 warps, persistent, one CTA per SM, work list from the planner.  Two query
 // tiles (A: rows 256p..256p+127, B: the next 128) share every K/V tile, so each K/V
-// byte loaded feeds two products, and two softmax warpgroups ping-pong around the
-// tensor core:
-//   warps 0-3  tile A softmax/activation, correction, epilogue (thread = row = lane)
-//   warps 4-7  tile B, the same
-//   warp 8     TMA producer: Q_A, Q_B once per item; K_j, V_j through 2-stage rings
-//   warp 9     tcgen05.mma issuer and TMEM owner
+// byte loaded feeds two products, and the two tiles' softmax warps ping-pong around the
+// tensor core.  Two warps share each row (thread = row = TMEM lane): one takes score
+// columns [0, 64) and O columns [0, D/2), the other the rest, so a tile's softmax runs
+// on two warps per scheduler; they exchange row maxima and sums through shared memory.
+//   warps 0-3   tile A, columns [0, 64): softmax/activation, correction, epilogue
+//   warps 4-7   tile B, columns [0, 64)
+//   warps 8-11  tile A, columns [64, 128)
+//   warps 12-15 tile B, columns [64, 128)
+//   warp 16     TMA producer: Q_A, Q_B once per item; K_j, V_j through 2-stage rings
+//   warp 17     tcgen05.mma issuer and TMEM owner
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [384,384+D).
 // P is written back over its own S columns as packed bf16 (64 columns; GDPA adds the
 // rounding remainder in the next 64) and read by O += P V straight from TMEM.  The
@@ -43,13 +47,16 @@ struct FwdCfg {
     static constexpr int kOffK = kOffQ + 2 * kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffBar = kOffV + kStages * kKVBytes;
-    static constexpr int kNumBars = 24;
+    static constexpr int kNumBars = 32;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    // softmax warps: 2 tiles x 2 column halves x 4 row quarters
+    static constexpr int kSoftWarps = 16;
     // tmem slot + abort flag; per softmax warp: the head's bias row (32) and a tile's
     // bias-by-relative-position table (160)
     static constexpr int kBiasRow = 32, kBiasTab = 160;
-    // ... and, for split items, warpgroup 1's row max and sum (two buffers of 2 x BM floats)
-    static constexpr int kMiscBytes = 16 + 8 * (kBiasRow + kBiasTab) * 4 + 2 * 2 * BM * 4;
+    // ... for split items, tile 1's row max and two partial sums (two buffers of 3 x BM
+    // floats), and the pair exchanges (two buffers of 2 halves x 8 pairs x 32 floats)
+    static constexpr int kMiscBytes = 16 + kSoftWarps * (kBiasRow + kBiasTab) * 4 + 2 * 3 * BM * 4 + 2 * 2 * 8 * 32 * 4;
     static constexpr int kSmemNeed = kOffMisc + kMiscBytes + 1024;
     // At least 120 KB so that exactly one CTA fits on an SM: the CTA allocates all
     // 512 TMEM columns.
@@ -60,8 +67,8 @@ struct FwdCfg {
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kIdescQK = make_idesc(kFmtBF16, BM, BN, false, false);
     static constexpr uint32_t kIdescPV = make_idesc(kFmtBF16, BM, D, false, true);
-    static constexpr int kThreads = 320;
-    static constexpr int kProdWarp = 8, kMmaWarp = 9;
+    static constexpr int kThreads = (kSoftWarps + 2) * 32;
+    static constexpr int kProdWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
     __host__ __device__ static constexpr uint32_t tmem_s(int x) { return x ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t tmem_o(int x) { return x ? 384u : 256u; }
 };
@@ -84,7 +91,8 @@ enum {
     B_O_DONE = 14,   // +tile: a P V product of the tile finished
     B_O_EMPTY = 16,  // +tile: the tile's epilogue has read O
     B_DRAIN = 18,
-    B_COMBINE = 19,  // split item: warpgroup 1's last P V done and its row max/sum written
+    B_COMBINE = 19,  // split item: tile 1's last P V done and its row max/sums written
+    B_XCH = 20,      // +pair: the two warps of a row group have written their exchange values
 };
 
 template <typename T>
@@ -115,7 +123,7 @@ __device__ __forceinline__ void store_row<float>(float* dst, const float* v, int
 // SPLIT: the work list holds split items (one-tile sequences, see below); without it the
 // split code compiles away and the kernel is the plain two-tile pipeline.
 template <int D, typename OT, bool GDPA, bool WIN, bool DENSE, bool SPLIT>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(576, 1)
     jfa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using C = FwdCfg<D>;
@@ -142,12 +150,13 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(bar(B_V_FULL + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
             mbar_init(bar(B_S_FULL + s), 1);
-            mbar_init(bar(B_P_FULL + s), 4);
+            mbar_init(bar(B_P_FULL + s), 8);
             mbar_init(bar(B_O_DONE + s), 1);
-            mbar_init(bar(B_O_EMPTY + s), 4);
+            mbar_init(bar(B_O_EMPTY + s), 8);
         }
         mbar_init(bar(B_DRAIN), 1);
-        mbar_init(bar(B_COMBINE), 4);
+        mbar_init(bar(B_COMBINE), 8);
+        for (int q = 0; q < 8; ++q) mbar_init(bar(B_XCH + q), 2);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -381,15 +390,37 @@ __global__ void __launch_bounds__(320, 1)
         mbar_wait_bounded(bar(B_DRAIN), 0, nullptr);
     } else {
         // ------------------------------------------------------------ softmax / epilogue
-        const int x = warp >> 2;               // query tile of this warpgroup
+        // Two warps share each 32-row group of a tile: the warp with hf = 0 takes score
+        // columns [0, 64) and O columns [0, D/2), the one with hf = 1 the rest.  They
+        // exchange their partial row max (softmax) each step and their partial row sums at
+        // the end through shared memory, behind a bounded wait on their pair's barrier.
+        const int x = (warp >> 2) & 1;         // query tile of this warp
+        const int hf = warp >> 3;              // column half
+        const int pair = warp & 7;             // the two warps holding these rows
         const int t = (warp & 3) * 32 + lane;  // row in the tile == TMEM lane
+        constexpr int HC = C::BN / 2;          // score columns per thread
+        constexpr int OC = D / 2;              // O columns per thread
         const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::tmem_s(x);
-        const uint32_t tO = tmem + lane_base + C::tmem_o(x);
+        const uint32_t tSt = tmem + lane_base + C::tmem_s(x);  // the tile's S columns
+        const uint32_t tS = tSt + uint32_t(HC * hf);           // this warp's half
+        const uint32_t tO = tmem + lane_base + C::tmem_o(x) + uint32_t(OC * hf);
         constexpr bool softmax = !GDPA;
         uint32_t s_cnt = 0;
         uint32_t split_cnt = 0;  // split items seen (phase of B_COMBINE, exchange buffer)
-        float* comb_s = bias_s + 8 * (C::kBiasRow + C::kBiasTab);  // [2][max(BM), sum(BM)]
+        uint32_t x_cnt = 0;      // exchanges with the partner warp (phase of its barrier)
+        float* comb_s = bias_s + C::kSoftWarps * (C::kBiasRow + C::kBiasTab);  // [2][m, l0, l1][BM]
+        float* xch_s = comb_s + 2 * 3 * C::BM;                                  // [2][2][8][32]
+        // The partner warp's value of a per-row float this warp also passes in.
+        auto exchange = [&](float v, float& other) -> bool {
+            float* buf = xch_s + (x_cnt & 1) * 512 + pair * 32;
+            buf[hf * 256 + lane] = v;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_XCH + pair));
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_XCH + pair), x_cnt & 1, abort_flag));
+            ++x_cnt;
+            if (ok) other = buf[(hf ^ 1) * 256 + lane];
+            return ok;
+        };
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
             const int4 w = p.items[it];
@@ -397,16 +428,16 @@ __global__ void __launch_bounds__(320, 1)
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
             const int kb = p.kv_map ? p.kv_map[b] : b;
             const int kv_len = p.kv_off[kb + 1] - p.kv_off[kb];
-            // Split item (a one-tile sequence with two or more key tiles): both
-            // warpgroups take tile 0's rows, warpgroup x one half of its key range (the first
-            // (na + 1) / 2 key tiles, or the rest) with its own max, sum and O; warpgroup 0
-            // combines the two at the end.  The tile loop is the same in both cases.
+            // Split item (a one-tile sequence with two or more key tiles): both tiles'
+            // warps take tile 0's rows, tile x one half of its key range (the first
+            // (na + 1) / 2 key tiles, or the rest) with its own max, sum and O; tile 0's
+            // warps combine the two at the end.  The tile loop is the same in both cases.
             int kfa, na;
             key_tile_range(q_len, kv_len, 2 * pr, p.causal, window, kfa, na);
             const bool split = SPLIT && q_len <= C::BM && na >= 2;
             const int tile = split ? 2 * pr : 2 * pr + x;
             if (tile * C::BM >= q_len) continue;  // tile B of a short last pair
-            int kf, n;  // this warpgroup's key tiles [kf, kf + n)
+            int kf, n;  // this tile's key tiles [kf, kf + n)
             if (split) {
                 kf = kfa + (x ? (na + 1) / 2 : 0);
                 n = x ? na / 2 : (na + 1) / 2;
@@ -441,8 +472,9 @@ __global__ void __launch_bounds__(320, 1)
                     float z[32];
 #pragma unroll
                     for (int d = 0; d < 32; ++d) z[d] = 0.f;
-                    for (int c = 0; c < D / 32; ++c) store_row<OT>(reinterpret_cast<OT*>(p.O) + orow * D + c * 32, z, 32);
-                    if (p.lse) p.lse[orow] = -INFINITY;
+                    for (int c = 0; c < OC / 32; ++c)
+                        store_row<OT>(reinterpret_cast<OT*>(p.O) + orow * D + OC * hf + c * 32, z, 32);
+                    if (p.lse && hf == 0) p.lse[orow] = -INFINITY;
                 }
                 continue;
             }
@@ -453,6 +485,11 @@ __global__ void __launch_bounds__(320, 1)
                     break;
                 }
                 tc_fence_after();
+                // this warp's two chunks: 32-column chunks kk = 2 hf + k of the tile, loaded
+                // at once and kept in registers through both passes
+                uint32_t sr[2][32];
+                tmem_ld32(tS, sr[0]);
+                tmem_ld32(tS + 32u, sr[1]);
                 const int col0 = (kf + j) * C::BN;
                 int lim = kv_len - col0;  // subtraction scheme: columns >= lim are masked
                 if (p.causal) lim = min(lim, row + diag + 1 - col0);
@@ -467,19 +504,18 @@ __global__ void __launch_bounds__(320, 1)
                 // from a table of the bias by relative position built for this tile.
                 // Lane k tests chunk k for the whole warp: over the warp's rows, chunk k
                 // spans relative positions rbase(lane 0) - 32k - 31 .. + 62.
-                uint32_t cmask = (1u << (C::BN / 32)) - 1;  // bit k: chunk k has a constant bias
-                float cb[C::BN / 32];
-#pragma unroll
-                for (int k = 0; k < C::BN / 32; ++k) cb[k] = 0.f;
+                uint32_t hmask = 3u;  // bit k: this warp's chunk k (tile chunk 2 hf + k) has a constant bias
+                float cb[2] = {0.f, 0.f};
                 if (p.bias) {
                     const int rb0 = __shfl_sync(0xffffffffu, rbase, 0);
                     int bk = 0;
-                    cmask = warp_const_chunks(lane < C::BN / 32, rb0 - 32 * lane - 31, bk) & cmask;
+                    const int kl = 2 * hf + (lane & 1);  // lanes 0, 1 test this warp's chunks
+                    hmask = warp_const_chunks(lane < 2, rb0 - 32 * kl - 31, bk) & 3u;
                     const float bv = btab[bk];
 #pragma unroll
-                    for (int k = 0; k < C::BN / 32; ++k) cb[k] = __shfl_sync(0xffffffffu, bv, k);
+                    for (int k = 0; k < 2; ++k) cb[k] = __shfl_sync(0xffffffffu, bv, k);
                 }
-                if (cmask != (1u << (C::BN / 32)) - 1) {
+                if (hmask != 3u) {
                     // rtab[i] = bias(r) for r = (lane 0's rbase) - 127 + i, i in [0, 160):
                     // element (lane, c) reads rtab[lane + 127 - c].
                     const int r0 = __shfl_sync(0xffffffffu, rbase, 0) - (C::BN - 1);
@@ -490,193 +526,160 @@ __global__ void __launch_bounds__(320, 1)
                     __syncwarp();
                 }
                 const float* rrow = rtab + lane + (C::BN - 1);  // rrow[-c] = bias of column c
-                // Scaled, biased and masked scores of chunk k, minus `shift`.
-                auto chunk_x = [&](const uint32_t (&r)[32], int k, float shift, float (&v)[32]) {
+                // In place: the scores of this warp's chunk k (tile chunk kk) become the
+                // scaled, biased and masked scores minus `shift` (masked: -inf).
+                auto to_x = [&](uint32_t (&r)[32], int k, float shift) {
+                    const int kk = 2 * hf + k;
                     if constexpr (DENSE) {
                         // per-element bias, read only inside the row's allowed columns
                         const float bs = softmax ? 1.4426950408889634f : 1.0f;
-                        const int lk = lim - 32 * k, lok = lo - 32 * k;
-                        const float* src = drow + col0 + 32 * k;
+                        const int lk = lim - 32 * kk, lok = lo - 32 * kk;
+                        const float* src = drow + col0 + 32 * kk;
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const bool in = i >= lok && i < lk;
                             const float bv = in ? __ldg(src + i) : 0.f;
-                            v[i] = in ? fmaf(__uint_as_float(r[i]), xs, fmaf(bv, bs, -shift)) : -INFINITY;
+                            r[i] = __float_as_uint(in ? fmaf(__uint_as_float(r[i]), xs, fmaf(bv, bs, -shift)) : -INFINITY);
                         }
                         return;
                     }
-                    if (cmask & (1u << k)) {
+                    if (hmask & (1u << k)) {
                         const float2 sc = make_float2(xs, xs), add = make_float2(cb[k] - shift, cb[k] - shift);
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
                             const float2 t2 = fma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sc, add);
-                            v[i] = t2.x;
-                            v[i + 1] = t2.y;
+                            r[i] = __float_as_uint(t2.x);
+                            r[i + 1] = __float_as_uint(t2.y);
                         }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = fmaf(__uint_as_float(r[i]), xs, rrow[-(32 * k + i)] - shift);
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = __float_as_uint(fmaf(__uint_as_float(r[i]), xs, rrow[-(32 * kk + i)] - shift));
                     }
                     if (!full) {
-                        const int lk = lim - 32 * k, lok = lo - 32 * k;
+                        const int lk = lim - 32 * kk, lok = lo - 32 * kk;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = (i >= lok && i < lk) ? v[i] : -INFINITY;
+                        for (int i = 0; i < 32; ++i) r[i] = (i >= lok && i < lk) ? r[i] : __float_as_uint(-INFINITY);
                     }
                 };
-                // S streams from TMEM in 32-column chunks; the load of chunk k+1 is in
-                // flight while chunk k is processed.  P of chunk k (and, for GDPA, its
-                // rounding remainder) is written over chunk k's own columns: P at
-                // [32k, 32k+16), remainder at [32k+16, 32k+32), two bf16 per column.
-                uint32_t ra[32], rb[32];
-                bool need_rescale = false;
-                float alpha = 1.f;
+                tmem_ld_wait(sr[0]);
+                tmem_ld_wait(sr[1]);
                 if constexpr (softmax) {
-                    // pass 1: an upper bound of the row max from the raw scores (one FMNMX
-                    // per element): xs * max(s) + the chunk's bias (constant, or the
-                    // head's largest).  Any m >= the true max gives the same P / l.
-                    // Fast tiles (no column masked, every chunk's bias one value) take a
-                    // branch-free copy of both passes; the rest take the general one.
-                    const bool fast = !DENSE && full && cmask == (1u << (C::BN / 32)) - 1;
+                    // pass 1: an upper bound of this half's row max from the raw scores (one
+                    // FMNMX per element): xs * max(s) + the chunk's bias (constant, or the
+                    // head's largest); the exact max for a dense bias.  Any m >= the true max
+                    // gives the same P / l.  The partner's half completes the row.
+                    const bool fast = !DENSE && full && hmask == 3u;
                     float mx = -INFINITY;
-                    tmem_ld32(tS, ra);
-                    tmem_ld_wait(ra);
-                    if (fast) {
 #pragma unroll
-                        for (int k = 0; k < C::BN / 32; ++k) {
-                            uint32_t (&cur)[32] = (k & 1) ? rb : ra;
-                            uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
-                            if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
-                            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2)
-                                m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
-                            mx = fmaxf(mx, fmaf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), xs, cb[k]));
-                            if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
-                        }
-                    } else {
-#pragma unroll
-                    for (int k = 0; k < C::BN / 32; ++k) {
-                        uint32_t (&cur)[32] = (k & 1) ? rb : ra;
-                        uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
-                        if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
+                    for (int k = 0; k < 2; ++k) {
+                        const int kk = 2 * hf + k;
                         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                         if (DENSE) {
-                            // no cheap bound on a dense bias: the exact max of x
-                            float v[32];
-                            chunk_x(cur, k, 0.f, v);
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2) m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], v[i], v[i + 1]);
-                            mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-                        } else if (full) {
+                            to_x(sr[k], k, 0.f);  // exact x, kept for pass 2
 #pragma unroll
                             for (int i = 0; i < 32; i += 2)
-                                m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
+                                m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(sr[k][i]), __uint_as_float(sr[k][i + 1]));
+                            mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                            continue;
+                        }
+                        if (fast || full) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2)
+                                m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(sr[k][i]), __uint_as_float(sr[k][i + 1]));
                         } else {
-                            const int lk = lim - 32 * k, lok = lo - 32 * k;
+                            const int lk = lim - 32 * kk, lok = lo - 32 * kk;
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
-                                m4[i & 3] = fmaxf(m4[i & 3], (i >= lok && i < lk) ? __uint_as_float(cur[i]) : -INFINITY);
+                                m4[i & 3] = fmaxf(m4[i & 3], (i >= lok && i < lk) ? __uint_as_float(sr[k][i]) : -INFINITY);
                         }
-                        if (!DENSE) {
-                            const float mk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                            mx = fmaxf(mx, fmaf(mk, xs, (cmask & (1u << k)) ? cb[k] : bmax));
-                        }
-                        if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
+                        const float mk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                        mx = fmaxf(mx, fmaf(mk, xs, (hmask & (1u << k)) ? cb[k] : bmax));
                     }
-                    }
-                    // Lazy rescaling: keep the running max unless it grows by more
-                    // than 2^8; both O and l use the same stale max, so the final
-                    // O / l is unchanged.
+                    float mo;
+                    if (!exchange(mx, mo)) { ok = false; break; }
+                    mx = fmaxf(mx, mo);
+                    // Lazy rescaling: keep the running max unless it grows by more than 2^8;
+                    // both O and l use the same stale max, so the final O / l is unchanged.
                     float m_new = m;
                     if (mx > m + 8.f) m_new = mx;
                     const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                    alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_use);
-                    if (m_new != m) need_rescale = (j > 0);
+                    const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_use);
+                    const bool need_rescale = (m_new != m) && j > 0;
                     m = m_new;
                     // O of this tile is stable here: S_x(j) was issued after P_x(j-1) V
                     // completed, and P V of step j waits for this tile's P.
                     if (__any_sync(0xffffffffu, need_rescale)) {
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t r[32];
-                            tmem_ld32(tO + c * 32u, r);
+#pragma unroll 1
+                        for (int c = 0; c < OC / 8; ++c) {
+                            uint32_t r[8];
+                            tmem_ld8(tO + c * 8u, r);
                             tmem_ld_wait(r);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                            tmem_st32(tO + c * 32u, r);
+                            for (int i = 0; i < 8; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st8(tO + c * 8u, r);
                         }
                     }
                     // pass 2: P = exp2(x - m) (packed FMA folds in -m), packed row sum,
-                    // P -> TMEM
+                    // P -> the chunk's first 16 TMEM columns
                     float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                     make_float2(0.f, 0.f)};
-                    tmem_ld32(tS, ra);
-                    tmem_ld_wait(ra);
-                    if (fast) {
-                        const float2 xs2 = make_float2(xs, xs);
 #pragma unroll
-                        for (int k = 0; k < C::BN / 32; ++k) {
-                            uint32_t (&cur)[32] = (k & 1) ? rb : ra;
-                            uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
-                            if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
-                            const float2 add = make_float2(cb[k] - m_use, cb[k] - m_use);
-                            uint32_t pk[16];
+                    for (int k = 0; k < 2; ++k) {
+                        const int kk = 2 * hf + k;
+                        uint32_t pk[16];
+                        if (fast) {
+                            const float2 xs2 = make_float2(xs, xs), add = make_float2(cb[k] - m_use, cb[k] - m_use);
 #pragma unroll
                             for (int i = 0; i < 32; i += 2) {
-                                const float2 t2 = fma2(make_float2(__uint_as_float(cur[i]), __uint_as_float(cur[i + 1])), xs2, add);
+                                const float2 t2 = fma2(make_float2(__uint_as_float(sr[k][i]), __uint_as_float(sr[k][i + 1])), xs2, add);
                                 const float2 e2 = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
                                 rs[(i >> 1) & 3] = add2(rs[(i >> 1) & 3], e2);
                                 pk[i >> 1] = pack_bf16x2(e2.x, e2.y);
                             }
-                            tmem_st16(tS + 32u * k, pk);
-                            if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
-                        }
-                    } else {
+                        } else {
+                            if (DENSE) {
+                                const float2 sh = make_float2(-m_use, -m_use);
 #pragma unroll
-                    for (int k = 0; k < C::BN / 32; ++k) {
-                        uint32_t (&cur)[32] = (k & 1) ? rb : ra;
-                        uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
-                        if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
-                        float v[32];
-                        chunk_x(cur, k, m_use, v);
-                        uint32_t pk[16];
+                                for (int i = 0; i < 32; i += 2) {
+                                    const float2 t2 = add2(make_float2(__uint_as_float(sr[k][i]), __uint_as_float(sr[k][i + 1])), sh);
+                                    sr[k][i] = __float_as_uint(t2.x);
+                                    sr[k][i + 1] = __float_as_uint(t2.y);
+                                }
+                            } else {
+                                to_x(sr[k], k, m_use);
+                            }
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const float2 e2 = make_float2(ex2_approx(v[i]), ex2_approx(v[i + 1]));
-                            rs[(i >> 1) & 3] = add2(rs[(i >> 1) & 3], e2);
-                            pk[i >> 1] = pack_bf16x2(e2.x, e2.y);
+                            for (int i = 0; i < 32; i += 2) {
+                                const float2 e2 = make_float2(ex2_approx(__uint_as_float(sr[k][i])), ex2_approx(__uint_as_float(sr[k][i + 1])));
+                                rs[(i >> 1) & 3] = add2(rs[(i >> 1) & 3], e2);
+                                pk[i >> 1] = pack_bf16x2(e2.x, e2.y);
+                            }
                         }
-                        tmem_st16(tS + 32u * k, pk);
-                        if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
-                    }
+                        tmem_st16(tSt + 32u * kk, pk);
                     }
                     const float2 r01 = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
                     l = l * alpha + (r01.x + r01.y);
                 } else {
                     // GDPA: P = act(x), one pass; remainder P - bf16(P) beside it.
                     const bool gelu = p.mode == JFA_GDPA_GELU_TANH;
-                    tmem_ld32(tS, ra);
-                    tmem_ld_wait(ra);
 #pragma unroll
-                    for (int k = 0; k < C::BN / 32; ++k) {
-                        uint32_t (&cur)[32] = (k & 1) ? rb : ra;
-                        uint32_t (&nxt)[32] = (k & 1) ? ra : rb;
-                        if (k + 1 < C::BN / 32) tmem_ld32(tS + 32u * (k + 1), nxt);
-                        float v[32];
-                        chunk_x(cur, k, 0.f, v);
+                    for (int k = 0; k < 2; ++k) {
+                        const int kk = 2 * hf + k;
+                        to_x(sr[k], k, 0.f);
                         uint32_t pk[16], pl[16];
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
                             // masked entries are -inf here: contribute exactly 0
-                            const float a0 = v[i] == -INFINITY ? 0.f : gdpa_act(gelu, v[i]);
-                            const float a1 = v[i + 1] == -INFINITY ? 0.f : gdpa_act(gelu, v[i + 1]);
+                            const float v0 = __uint_as_float(sr[k][i]), v1 = __uint_as_float(sr[k][i + 1]);
+                            const float a0 = v0 == -INFINITY ? 0.f : gdpa_act(gelu, v0);
+                            const float a1 = v1 == -INFINITY ? 0.f : gdpa_act(gelu, v1);
                             const uint32_t u = pack_bf16x2(a0, a1);
                             pk[i >> 1] = u;
                             pl[i >> 1] = pack_bf16x2(a0 - __uint_as_float(u << 16), a1 - __uint_as_float(u & 0xffff0000u));
                         }
-                        tmem_st16(tS + 32u * k, pk);
-                        tmem_st16(tS + 32u * k + 16u, pl);
-                        if (k + 1 < C::BN / 32) tmem_ld_wait(nxt);
+                        tmem_st16(tSt + 32u * kk, pk);
+                        tmem_st16(tSt + 32u * kk + 16u, pl);
                     }
                 }
                 tmem_st_wait();
@@ -693,38 +696,45 @@ __global__ void __launch_bounds__(320, 1)
             }
             tc_fence_after();
             if (split) {
-                // Warpgroup 1 hands over its row max and sum; warpgroup 0 combines both halves:
+                // Tile 1's warps hand over the row max and their partial sums; tile 0's warps
+                // combine both halves of the key range over their O columns:
                 // O = (O0 2^(m0-m) + O1 2^(m1-m)) / (l0 2^(m0-m) + l1 2^(m1-m)), m = max(m0, m1)
-                // (GDPA: O = O0 + O1), then releases both O accumulators.
-                float* comb = comb_s + (split_cnt & 1) * 2 * C::BM;
+                // (GDPA: O = O0 + O1), then release both O accumulators.
+                float* comb = comb_s + (split_cnt & 1) * 3 * C::BM;
                 ++split_cnt;
                 if (x == 1) {
-                    comb[t] = m;
-                    comb[C::BM + t] = l;
+                    if (hf == 0) comb[t] = m;
+                    comb[(1 + hf) * C::BM + t] = l;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B_COMBINE));
                     continue;
+                }
+                float l0 = l;
+                if constexpr (softmax) {
+                    float lo2;
+                    if (!exchange(l, lo2)) { ok = false; break; }
+                    l0 = l + lo2;
                 }
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_COMBINE), (split_cnt - 1) & 1, abort_flag))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                float c0 = 1.f, c1 = 1.f, mm = m, ll = l;
+                float c0 = 1.f, c1 = 1.f, mm = m, ll = l0;
                 if constexpr (softmax) {
-                    const float m1 = comb[t], l1 = comb[C::BM + t];
+                    const float m1 = comb[t], l1 = comb[C::BM + t] + comb[2 * C::BM + t];
                     mm = fmaxf(m, m1);
                     const float a0 = m == -INFINITY ? 0.f : ex2_approx(m - mm);
                     const float a1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
-                    ll = fmaf(l, a0, l1 * a1);
+                    ll = fmaf(l0, a0, l1 * a1);
                     const float inv = ll > 0.f ? 1.f / ll : 0.f;
                     c0 = a0 * inv;
                     c1 = a1 * inv;
                 }
-                const uint32_t tO1 = tmem + lane_base + C::tmem_o(1);
-                OT* orow_p = reinterpret_cast<OT*>(p.O) + orow * D;
+                const uint32_t tO1 = tmem + lane_base + C::tmem_o(1) + uint32_t(OC * hf);
+                OT* orow_p = reinterpret_cast<OT*>(p.O) + orow * D + OC * hf;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < OC / 32; ++c) {
                     uint32_t r0[32], r1[32];
                     float v[32];
                     tmem_ld32(tO + c * 32u, r0);
@@ -741,15 +751,21 @@ __global__ void __launch_bounds__(320, 1)
                     mbar_arrive(bar(B_O_EMPTY + 0));
                     mbar_arrive(bar(B_O_EMPTY + 1));
                 }
-                if (row_valid && softmax && p.lse)
+                if (row_valid && softmax && p.lse && hf == 0)
                     p.lse[orow] = ll > 0.f ? (mm + __log2f(ll)) * 0.6931471805599453f : -INFINITY;
                 continue;
             }
             {
-                const float inv = (softmax && l > 0.f) ? 1.f / l : (softmax ? 0.f : 1.f);
-                OT* orow_p = reinterpret_cast<OT*>(p.O) + orow * D;
+                float lt = l;  // the row's sum over both halves (softmax)
+                if constexpr (softmax) {
+                    float lo2;
+                    if (!exchange(l, lo2)) { ok = false; break; }
+                    lt = l + lo2;
+                }
+                const float inv = (softmax && lt > 0.f) ? 1.f / lt : (softmax ? 0.f : 1.f);
+                OT* orow_p = reinterpret_cast<OT*>(p.O) + orow * D + OC * hf;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < OC / 32; ++c) {
                     uint32_t r[32];
                     float v[32];
                     tmem_ld32(tO + c * 32u, r);
@@ -758,12 +774,12 @@ __global__ void __launch_bounds__(320, 1)
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * inv;
                     if (row_valid) store_row<OT>(orow_p + c * 32, v, 32);
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_O_EMPTY + x));
+                if (row_valid && softmax && p.lse && hf == 0)
+                    p.lse[orow] = lt > 0.f ? (m + __log2f(lt)) * 0.6931471805599453f : -INFINITY;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_O_EMPTY + x));
-            if (row_valid && softmax && p.lse)
-                p.lse[orow] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
         if (!ok) fail();
     }
