@@ -480,16 +480,8 @@ __global__ void __launch_bounds__(576, 1)
             }
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_S_FULL + x), s_cnt & 1, abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // this warp's two chunks: 32-column chunks kk = 2 hf + k of the tile, loaded
-                // at once and kept in registers through both passes
-                uint32_t sr[2][32];
-                tmem_ld32(tS, sr[0]);
-                tmem_ld32(tS + 32u, sr[1]);
+                // The step's masks and bias lookups depend on its position only, so they are
+                // formed while the tensor core computes its scores.
                 const int col0 = (kf + j) * C::BN;
                 int lim = kv_len - col0;  // subtraction scheme: columns >= lim are masked
                 if (p.causal) lim = min(lim, row + diag + 1 - col0);
@@ -526,6 +518,16 @@ __global__ void __launch_bounds__(576, 1)
                     __syncwarp();
                 }
                 const float* rrow = rtab + lane + (C::BN - 1);  // rrow[-c] = bias of column c
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_S_FULL + x), s_cnt & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // this warp's two chunks: 32-column chunks kk = 2 hf + k of the tile, loaded
+                // at once and kept in registers through both passes
+                uint32_t sr[2][32];
+                tmem_ld32(tS, sr[0]);
+                tmem_ld32(tS + 32u, sr[1]);
                 // In place: the scores of this warp's chunk k (tile chunk kk) become the
                 // scaled, biased and masked scores minus `shift` (masked: -inf).
                 auto to_x = [&](uint32_t (&r)[32], int k, float shift) {
@@ -622,8 +624,7 @@ __global__ void __launch_bounds__(576, 1)
                     }
                     // pass 2: P = exp2(x - m) (packed FMA folds in -m), packed row sum,
                     // P -> the chunk's first 16 TMEM columns
-                    float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                    make_float2(0.f, 0.f)};
+                    float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
                         const int kk = 2 * hf + k;
@@ -634,7 +635,7 @@ __global__ void __launch_bounds__(576, 1)
                             for (int i = 0; i < 32; i += 2) {
                                 const float2 t2 = fma2(make_float2(__uint_as_float(sr[k][i]), __uint_as_float(sr[k][i + 1])), xs2, add);
                                 const float2 e2 = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
-                                rs[(i >> 1) & 3] = add2(rs[(i >> 1) & 3], e2);
+                                rs[(i >> 1) & 1] = add2(rs[(i >> 1) & 1], e2);
                                 pk[i >> 1] = pack_bf16x2(e2.x, e2.y);
                             }
                         } else {
@@ -652,13 +653,13 @@ __global__ void __launch_bounds__(576, 1)
 #pragma unroll
                             for (int i = 0; i < 32; i += 2) {
                                 const float2 e2 = make_float2(ex2_approx(__uint_as_float(sr[k][i])), ex2_approx(__uint_as_float(sr[k][i + 1])));
-                                rs[(i >> 1) & 3] = add2(rs[(i >> 1) & 3], e2);
+                                rs[(i >> 1) & 1] = add2(rs[(i >> 1) & 1], e2);
                                 pk[i >> 1] = pack_bf16x2(e2.x, e2.y);
                             }
                         }
                         tmem_st16(tSt + 32u * kk, pk);
                     }
-                    const float2 r01 = add2(add2(rs[0], rs[1]), add2(rs[2], rs[3]));
+                    const float2 r01 = add2(rs[0], rs[1]);
                     l = l * alpha + (r01.x + r01.y);
                 } else {
                     // GDPA: P = act(x), one pass; remainder P - bf16(P) beside it.
