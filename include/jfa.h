@@ -301,6 +301,22 @@ jfa_status jfa_bwd_static_scratch(jfa_plan plan, int32_t dtype, const void* Q, c
  */
 jfa_status jfa_plan_set_deterministic(jfa_plan plan, int32_t enable);
 
+/*
+ * Test hook for the kernels' own checks (not a counterpart of anything in the articles).
+ * Every kernel checks each work item it reads against the plan -- sequence, head and
+ * tile inside the batch, inner count equal to the one the tile ranges give -- before it
+ * touches anything the item indexes.  It skips an item that fails and sets the status
+ * that jfa_plan_device_status reports as JFA_ERR_DEVICE_BOUNDS.  The planner never writes
+ * such an item; this call overwrites work item `index` of a pass (0 forward, 1 backward
+ * dK/dV, 2 backward dQ; numbering as jfa_plan_info facts 7, 9, 12) in the plan's device
+ * memory so that a test can plant one.  The lists are the plan's own (a shared key/value
+ * plan's merged view keeps its lists).  Synchronises.  A plan holding a changed item gives
+ * wrong results for that item's rows until it is destroyed.
+ *   item: int32[4] (sequence, head, tile, inner count), host memory.
+ * Errors: INVALID_ARG for a bad pass, an index outside the list or a null pointer; CUDA.
+ */
+jfa_status jfa_plan_set_work_item(jfa_plan plan, int32_t pass, int64_t index, const int32_t* item);
+
 /* Synchronises `stream`, then reads and clears the plan's device status word, which
  * the kernels set when a pipeline wait times out (TIMEOUT) or a bounds check fires
  * (DEVICE_BOUNDS).  Returns JFA_OK when no kernel reported anything. */

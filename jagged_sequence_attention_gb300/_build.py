@@ -89,6 +89,45 @@ def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines, sources=("fwd.cu",), verbose: bool = False) -> str:
+    """A test build of the library: `sources` compiled again with the extra -D `defines`,
+    linked with the main build's objects for the other sources, as _build/lib<name>.so.
+    Returns its path.  The main library is built first if needed."""
+    build()
+    out_dir = os.path.join(BUILD, name)
+    os.makedirs(out_dir, exist_ok=True)
+    lib = os.path.join(BUILD, f"lib{name}.so")
+    extra = [f"-D{d}" for d in defines]
+    stamp = os.path.join(out_dir, "stamp")
+    dig = _digest(extra) + ",".join(sources)
+    if os.path.exists(lib) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == dig:
+                return lib
+    nvcc = _nvcc()
+    objs = []
+    for src in SOURCES:
+        base = os.path.splitext(src)[0] + ".o"
+        if src in sources:
+            obj = os.path.join(out_dir, base)
+            cmd = [nvcc] + _flags(extra) + ["-c", os.path.join(CSRC, src), "-o", obj]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"compile failed: {src}\n{r.stdout}\n{r.stderr}")
+            objs.append(obj)
+        else:
+            objs.append(os.path.join(BUILD, base))
+    tmp = lib + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"], capture_output=True,
+                       text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib)
+    with open(stamp, "w") as f:
+        f.write(dig)
+    return lib
+
+
 if __name__ == "__main__":
     v = "-v" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas" in sys.argv else []

@@ -435,6 +435,15 @@ jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
     return JFA_OK;
 }
 
+jfa_status jfa_plan_set_work_item(jfa_plan plan, int32_t pass, int64_t index, const int32_t* item) {
+    if (!plan || !item || pass < kPassFwd || pass > kPassBwdQ || index < 0) return JFA_ERR_INVALID_ARG;
+    const int64_t n = pass == kPassFwd ? plan->n_fwd_items : pass == kPassBwdKV ? plan->n_bwd_items : plan->n_dq_items;
+    if (index >= n) return JFA_ERR_INVALID_ARG;
+    int4* list = pass == kPassFwd ? plan->d_fwd_items : pass == kPassBwdKV ? plan->d_bwd_items : plan->d_dq_items;
+    const int4 w = make_int4(item[0], item[1], item[2], item[3]);
+    return cudaMemcpy(list + index, &w, sizeof(w), cudaMemcpyHostToDevice) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
 jfa_status jfa_plan_set_deterministic(jfa_plan plan, int32_t enable) {
     if (!plan || (enable != 0 && enable != 1)) return JFA_ERR_INVALID_ARG;
     plan->deterministic = enable != 0;
@@ -523,6 +532,8 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
         p.n_pairs = plan->n_pairs;
     }
     p.kv_map = v->d_kv_map;
+    p.n_seq = v->B;
+    p.n_kv = v->U;
     KernelTimer tm(plan, 0, static_cast<cudaStream_t>(stream));
     cudaError_t e = dtype == JFA_BF16
                         ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, v->fwd_grid, v->fwd_split, static_cast<cudaStream_t>(stream))
@@ -663,6 +674,9 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
         p.steps = v->d_steps;
         p.step_off = v->d_step_off;
         p.ktile_off = v->d_ktile_off;
+        p.kv_map = v->d_kv_map;
+        p.n_seq = v->B;
+        p.n_kv = v->U;
     }
     if (v->n_bwd_items > 0) {
         KernelTimer tm(plan, 2, st);

@@ -150,9 +150,14 @@ __global__ void __launch_bounds__(320, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t kv_it = 0, item_it = 0;
+            uint32_t k_extra = 0;  // 1: the last step's K load went out but its V load did not
             bool ok = true;
             for (int it = it_begin; it < it_end && ok; ++it) {
                 const int4 w = p.items[it];
+                if (!dq_item_ok(w, p)) {  // not an item of this plan: skipped by every role
+                    atomicOr(p.status, kStatusBounds);
+                    continue;
+                }
                 const int n = w.w;
                 if (n == 0) continue;
                 const int b = w.x, h = w.y, tq = w.z;
@@ -181,7 +186,11 @@ __global__ void __launch_bounds__(320, 1)
                     for (int cb = 0; cb < C::kCB; ++cb)
                         tma_load_2d(sK + kst * C::kKVTile + cb * C::BN * 128, &tmK, bar(DQ_K_FULL + kst),
                                     h * D + cb * C::kBoxCols, y);
-                    if (!mbar_wait_bounded(bar(DQ_V_EMPTY + st), ph ^ 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_bounded(bar(DQ_V_EMPTY + st), ph ^ 1, abort_flag)) {
+                        k_extra = 1;
+                        ok = false;
+                        break;
+                    }
                     mbar_arrive_expect_tx(bar(DQ_V_FULL + st), C::kKVTile);
 #pragma unroll
                     for (int cb = 0; cb < C::kCB; ++cb)
@@ -195,16 +204,8 @@ __global__ void __launch_bounds__(320, 1)
                 mbar_wait_bounded(bar(DQ_Q_FULL), (item_it - 1) & 1, nullptr);
                 mbar_wait_bounded(bar(DQ_DO_FULL), (item_it - 1) & 1, nullptr);
             }
-            for (uint32_t s = 0; s < 3; ++s)
-                if (kv_it > s) {
-                    const uint32_t last = ((kv_it - 1 - s) / 3) * 3 + s;  // last index with K stage s
-                    mbar_wait_bounded(bar(DQ_K_FULL + s), (last / 3) & 1, nullptr);
-                }
-            for (uint32_t s = 0; s < 2; ++s)
-                if (kv_it > s) {
-                    const uint32_t last = ((kv_it - 1 - s) / 2) * 2 + s;
-                    mbar_wait_bounded(bar(DQ_V_FULL + s), (last >> 1) & 1, nullptr);
-                }
+            drain_ring(bar(DQ_K_FULL), kv_it + k_extra, 3);
+            drain_ring(bar(DQ_V_FULL), kv_it, 2);
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -279,7 +280,9 @@ __global__ void __launch_bounds__(320, 1)
             return true;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const int n = p.items[it].w;
+            const int4 wi = p.items[it];
+            if (!dq_item_ok(wi, p)) continue;
+            const int n = wi.w;
             if (n == 0) continue;
             if (!warp_wait(DQ_Q_FULL, item_it & 1) || !warp_wait(DQ_DO_FULL, item_it & 1)) { ok = false; break; }
             tc_fence_after();
@@ -320,6 +323,7 @@ __global__ void __launch_bounds__(320, 1)
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
             const int4 w = p.items[it];
+            if (!dq_item_ok(w, p)) continue;
             const int n = w.w, b = w.x, h = w.y, tq = w.z;
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
             const int kb = p.kv_map ? p.kv_map[b] : b;

@@ -182,9 +182,14 @@ __global__ void __launch_bounds__(320, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t step_it = 0, item_it = 0;
+            uint32_t q_extra = 0;  // 1: the last step's Q load went out but its dO load did not
             bool ok = true;
             for (int it = it_begin; it < it_end && ok; ++it) {
                 const int4 w = p.items[it];
+                if (!kv_item_ok(w, p, false)) {  // not an item of this plan: skipped by every role
+                    atomicOr(p.status, kStatusBounds);
+                    continue;
+                }
                 const int n = w.w;
                 if (n == 0) continue;
                 const int b = w.x, h = w.y, nt = w.z;
@@ -210,7 +215,11 @@ __global__ void __launch_bounds__(320, 1)
                     for (int cb = 0; cb < C::kCB; ++cb)
                         tma_load_2d(sQ + st * C::kQTile + cb * C::BM * 128, &tmQ, bar(FU_Q_FULL + st),
                                     h * D + cb * C::kBoxCols, y);
-                    if (!mbar_wait_bounded(bar(FU_DO_EMPTY), (step_it & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_bounded(bar(FU_DO_EMPTY), (step_it & 1) ^ 1, abort_flag)) {
+                        q_extra = 1;
+                        ok = false;
+                        break;
+                    }
                     mbar_arrive_expect_tx(bar(FU_DO_FULL), C::kQTile);
 #pragma unroll
                     for (int cb = 0; cb < C::kCB; ++cb)
@@ -223,12 +232,8 @@ __global__ void __launch_bounds__(320, 1)
                 mbar_wait_bounded(bar(FU_K_FULL), (item_it - 1) & 1, nullptr);
                 mbar_wait_bounded(bar(FU_V_FULL), (item_it - 1) & 1, nullptr);
             }
-            for (uint32_t s = 0; s < 2; ++s)
-                if (step_it > s) {
-                    const uint32_t last = ((step_it - 1 - s) / 2) * 2 + s;
-                    mbar_wait_bounded(bar(FU_Q_FULL + s), (last >> 1) & 1, nullptr);
-                }
-            if (step_it > 0) mbar_wait_bounded(bar(FU_DO_FULL), (step_it - 1) & 1, nullptr);
+            drain_ring(bar(FU_Q_FULL), step_it + q_extra, 2);
+            drain_ring(bar(FU_DO_FULL), step_it, 1);
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -332,7 +337,9 @@ __global__ void __launch_bounds__(320, 1)
             return true;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const int n = p.items[it].w;
+            const int4 wi = p.items[it];
+            if (!kv_item_ok(wi, p, false)) continue;
+            const int n = wi.w;
             if (n == 0) continue;
             if (!warp_wait(FU_K_FULL, item_it & 1) || !warp_wait(FU_V_FULL, item_it & 1)) { ok = false; break; }
             tc_fence_after();
@@ -427,6 +434,7 @@ __global__ void __launch_bounds__(320, 1)
 
         for (int it = it_begin; it < it_end && ok; ++it) {
             const int4 w = p.items[it];
+            if (!kv_item_ok(w, p, false)) continue;
             const int n = w.w, b = w.x, h = w.y, nt = w.z;
             const int kv0 = p.kv_off[b], kv_len = p.kv_off[b + 1] - kv0;
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;

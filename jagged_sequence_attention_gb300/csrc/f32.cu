@@ -51,6 +51,10 @@ __global__ void __launch_bounds__(kF32Rows) jfa_fwd_f32_kernel(const float* __re
     __shared__ float sV[kF32Inner][D];
     __shared__ float sB[32];
     const int4 w = p.items[blockIdx.x >> 1];
+    if (!fwd_item_ok(w, p, p.window)) {  // not an item of this plan (the whole CTA returns)
+        if (threadIdx.x == 0 && (blockIdx.x & 1) == 0) atomicOr(p.status, kStatusBounds);
+        return;
+    }
     const int b = w.x, h = w.y, mt = 2 * w.z + int(blockIdx.x & 1);
     const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
     const int kb = p.kv_map ? p.kv_map[b] : b;  // key/value sequence (shared: the user)
@@ -154,6 +158,10 @@ __global__ void __launch_bounds__(kF32Rows) jfa_bwd_f32_kernel(const float* __re
     __shared__ float sDiag[kDiags];
     __shared__ float sDB[32];  // the item's table gradient, bucket t owned by thread t
     const int4 w = p.items[blockIdx.x];
+    if (!kv_item_ok(w, p, p.steps != nullptr)) {  // not an item of this plan (the whole CTA returns)
+        if (threadIdx.x == 0) atomicOr(p.status, kStatusBounds);
+        return;
+    }
     // b: the key/value sequence of the item (shared key/value: the user)
     const int b = w.x, h = w.y, nt = w.z, n = w.w;
     const int k0 = p.kv_off[b], kv_len = p.kv_off[b + 1] - k0;

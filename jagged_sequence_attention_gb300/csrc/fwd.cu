@@ -93,6 +93,7 @@ enum {
     B_DRAIN = 18,
     B_COMBINE = 19,  // split item: tile 1's last P V done and its row max/sums written
     B_XCH = 20,      // +pair: the two warps of a row group have written their exchange values
+    B_NEVER = 28,    // nothing arrives here (the timeout test's stall, test builds only)
 };
 
 template <typename T>
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(576, 1)
         mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_COMBINE), 8);
         for (int q = 0; q < 8; ++q) mbar_init(bar(B_XCH + q), 2);
+        mbar_init(bar(B_NEVER), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -186,9 +188,14 @@ __global__ void __launch_bounds__(576, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t kv_it = 0, item_it = 0;
+            uint32_t k_extra = 0;  // 1: the last step's K load went out but its V load did not
             bool ok = true;
             for (int it = it_begin; it < it_end && ok; ++it) {
                 const int4 w = p.items[it];
+                if (!fwd_item_ok(w, p, window)) {  // not an item of this plan: skipped by every role
+                    atomicOr(p.status, kStatusBounds);
+                    continue;
+                }
                 const int n = w.w;
                 if (n == 0) continue;
                 const int b = w.x, h = w.y, pr = w.z;
@@ -220,7 +227,11 @@ __global__ void __launch_bounds__(576, 1)
                     for (int cb = 0; cb < C::kCB; ++cb)
                         tma_load_2d(sK + st * C::kKVBytes + cb * C::BN * 128, &tmK, bar(B_K_FULL + st),
                                     h * D + cb * C::kBoxCols, y);
-                    if (!mbar_wait_bounded(bar(B_V_EMPTY + st), ph ^ 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_bounded(bar(B_V_EMPTY + st), ph ^ 1, abort_flag)) {
+                        k_extra = 1;
+                        ok = false;
+                        break;
+                    }
                     mbar_arrive_expect_tx(bar(B_V_FULL + st), C::kKVBytes);
 #pragma unroll
                     for (int cb = 0; cb < C::kCB; ++cb)
@@ -231,13 +242,8 @@ __global__ void __launch_bounds__(576, 1)
             if (!ok) fail();
             // Drain: wait until every load this thread issued has landed.
             if (item_it > 0) mbar_wait_bounded(bar(B_Q_FULL), (item_it - 1) & 1, nullptr);
-            for (uint32_t s = 0; s < 2; ++s) {
-                if (kv_it > s) {
-                    const uint32_t last = ((kv_it - 1 - s) / 2) * 2 + s;  // last index with stage s
-                    mbar_wait_bounded(bar(B_K_FULL + s), (last >> 1) & 1, nullptr);
-                    mbar_wait_bounded(bar(B_V_FULL + s), (last >> 1) & 1, nullptr);
-                }
-            }
+            drain_ring(bar(B_K_FULL), kv_it + k_extra, 2);
+            drain_ring(bar(B_V_FULL), kv_it, 2);
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -249,6 +255,12 @@ __global__ void __launch_bounds__(576, 1)
         uint32_t kv_it = 0, item_it = 0;
         uint32_t pv_cnt0 = 0, pv_cnt1 = 0, items_x0 = 0, items_x1 = 0;
         bool ok = true;
+#ifdef JFA_TEST_STALL_MMA
+        // Test builds only (the bounded-wait test): before its first product the issuer waits
+        // on a barrier that nothing arrives on, so that this pipeline wait runs out and every
+        // role of the CTA winds down and reports the timeout.
+        if (it_begin < it_end && !wwait(B_NEVER, 0)) ok = false;
+#endif
         // Descriptors of every operand tile, built once; each MMA below adds a
         // compile-time byte offset to the low half.
         const SDesc dQ0 = sdesc_sw128(sQ, 16, 1024), dQ1 = sdesc_sw128(sQ + C::kQBytes, 16, 1024);
@@ -304,6 +316,7 @@ __global__ void __launch_bounds__(576, 1)
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
             const int4 w = p.items[it];
+            if (!fwd_item_ok(w, p, window)) continue;
             const int n = w.w;
             if (n == 0) continue;
             const int b = w.x, pr = w.z;
@@ -416,7 +429,15 @@ __global__ void __launch_bounds__(576, 1)
             buf[hf * 256 + lane] = v;
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_XCH + pair));
-            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_XCH + pair), x_cnt & 1, abort_flag));
+            // The partner is normally a few hundred cycles away at most: spin inline (a call
+            // to the parked slow-path wait would save this warp's live scores around it),
+            // bounded by an iteration count and the CTA's abort flag.
+            bool done = false;
+            for (uint32_t spin = 0; spin < (1u << 26) && !done; ++spin) {
+                done = mbar_try_wait(bar(B_XCH + pair), x_cnt & 1);
+                if (!done && (spin & 1023u) == 1023u && *abort_flag) break;
+            }
+            const bool ok = __all_sync(0xffffffffu, done);
             ++x_cnt;
             if (ok) other = buf[(hf ^ 1) * 256 + lane];
             return ok;
@@ -424,6 +445,7 @@ __global__ void __launch_bounds__(576, 1)
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
             const int4 w = p.items[it];
+            if (!fwd_item_ok(w, p, window)) continue;
             const int b = w.x, h = w.y, pr = w.z;
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
             const int kb = p.kv_map ? p.kv_map[b] : b;
@@ -625,6 +647,14 @@ __global__ void __launch_bounds__(576, 1)
                     // pass 2: P = exp2(x - m) (packed FMA folds in -m), packed row sum,
                     // P -> the chunk's first 16 TMEM columns
                     float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    if (!DENSE) {
+                        // the raw scores again (cheaper than keeping 64 registers live across
+                        // the exchange and the rescale)
+                        tmem_ld32(tS, sr[0]);
+                        tmem_ld32(tS + 32u, sr[1]);
+                        tmem_ld_wait(sr[0]);
+                        tmem_ld_wait(sr[1]);
+                    }
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
                         const int kk = 2 * hf + k;

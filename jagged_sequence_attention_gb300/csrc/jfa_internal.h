@@ -142,6 +142,8 @@ struct FwdParams {
     // Shared key/value: kv_map[b] is query set b's key/value sequence (its user), whose
     // rows are kv_off[u] .. kv_off[u+1]; nullptr: sequence b's own.
     const int32_t* kv_map = nullptr;
+    int n_seq = 0;  // query sequences (entries of q_off minus one)
+    int n_kv = 0;   // key/value sequences (entries of kv_off minus one)
 };
 
 struct BwdParams {
@@ -179,7 +181,53 @@ struct BwdParams {
     const int2* steps = nullptr;
     const int32_t* step_off = nullptr;
     const int32_t* ktile_off = nullptr;
+    int n_seq = 0;  // query sequences (entries of q_off minus one)
+    int n_kv = 0;   // key/value sequences (entries of kv_off minus one)
 };
+
+// Work-item checks.  Every kernel checks each item it reads against the plan before it
+// touches anything the item indexes: the sequence, head and tile must lie inside the
+// batch and the inner count must be the one the tile ranges give.  The planner never
+// writes an item that fails; a kernel that meets one skips it (every role of the CTA
+// takes the same decision from the same item) and sets kStatusBounds, which
+// jfa_plan_device_status reports as JFA_ERR_DEVICE_BOUNDS.
+__device__ inline bool fwd_item_ok(const int4 w, const FwdParams& p, int window) {
+    if (w.x < 0 || w.x >= p.n_seq || w.y < 0 || w.y >= p.H || w.z < 0 || w.w < 0) return false;
+    const int kb = p.kv_map ? p.kv_map[w.x] : w.x;
+    if (kb < 0 || kb >= p.n_kv) return false;
+    const int q_len = p.q_off[w.x + 1] - p.q_off[w.x], kv_len = p.kv_off[kb + 1] - p.kv_off[kb];
+    if (int64_t(w.z) * kFwdPairRows >= int64_t(q_len)) return false;
+    int f0, ns, na, nb;
+    pair_stream(q_len, kv_len, w.z, p.causal, window, f0, ns, na, nb);
+    return w.w == ns;
+}
+
+// dQ pass: query tile w.z of sequence w.x, visiting the forward's key-tile range.
+__device__ inline bool dq_item_ok(const int4 w, const BwdParams& p) {
+    if (w.x < 0 || w.x >= p.n_seq || w.y < 0 || w.y >= p.H || w.z < 0 || w.w < 0) return false;
+    const int kb = p.kv_map ? p.kv_map[w.x] : w.x;
+    if (kb < 0 || kb >= p.n_kv) return false;
+    const int q_len = p.q_off[w.x + 1] - p.q_off[w.x], kv_len = p.kv_off[kb + 1] - p.kv_off[kb];
+    if (int64_t(w.z) * kFwdBM >= int64_t(q_len)) return false;
+    return w.w == fwd_tiles_of(q_len, kv_len, w.z, p.causal, p.window);
+}
+
+// dK/dV pass: key tile w.z of sequence w.x (shared key/value: of user w.x, visiting the
+// steps the planner listed for it).
+__device__ inline bool kv_item_ok(const int4 w, const BwdParams& p, bool shared) {
+    if (w.x < 0 || w.x >= p.n_kv || w.y < 0 || w.y >= p.H || w.z < 0 || w.w < 0) return false;
+    if (shared) {
+        if (w.z >= p.ktile_off[w.x + 1] - p.ktile_off[w.x]) return false;
+        const int g = p.ktile_off[w.x] + w.z;
+        return w.w == p.step_off[g + 1] - p.step_off[g];
+    }
+    if (w.x >= p.n_seq) return false;
+    const int q_len = p.q_off[w.x + 1] - p.q_off[w.x], kv_len = p.kv_off[w.x + 1] - p.kv_off[w.x];
+    if (int64_t(w.z) * kBwdBN >= int64_t(kv_len)) return false;
+    int first, n;
+    query_tile_range(q_len, kv_len, w.z, p.causal, p.window, first, n);
+    return w.w == n;
+}
 
 // Host planner (plan.cpp).  Returns JFA_OK or an error for bad offsets.
 jfa_status validate_offsets(const int32_t* q_off, const int32_t* kv_off, int32_t B);

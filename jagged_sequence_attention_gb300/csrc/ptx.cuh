@@ -10,11 +10,18 @@
 
 namespace jfa {
 
-// Spin-wait limit for every mbarrier wait in the kernels (nanoseconds of
+// Spin-wait limit for every pipeline mbarrier wait in the kernels (nanoseconds of
 // %globaltimer).  A correct pipeline never waits longer than one tile's work; the
 // limit only turns a logic error into an error status instead of a hang.
 #ifndef JFA_WAIT_TIMEOUT_NS
 #define JFA_WAIT_TIMEOUT_NS 2000000000ull
+#endif
+// Limit of the waits with which a role, before its CTA exits, lets its own TMA loads and
+// tensor-core products finish (drains).  Those always complete; the limit is kept apart
+// from the pipeline's, and never shortened, so that a role that gave up on the pipeline
+// still waits for everything it issued before shared memory and TMEM are released.
+#ifndef JFA_DRAIN_TIMEOUT_NS
+#define JFA_DRAIN_TIMEOUT_NS 2000000000ull
 #endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -79,16 +86,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Bounded wait for the phase with the given parity to complete.  Returns false if
 // the wait gave up: after JFA_WAIT_TIMEOUT_NS, or as soon as another role of the
-// CTA raised *abort_flag (pass nullptr to ignore the flag, e.g. when draining).
+// CTA raised *abort_flag.  A drain passes nullptr: it ignores the flag and waits up to
+// JFA_DRAIN_TIMEOUT_NS.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                             const volatile int* abort_flag) {
+    const uint64_t limit = abort_flag ? JFA_WAIT_TIMEOUT_NS : JFA_DRAIN_TIMEOUT_NS;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
             if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (abort_flag && *abort_flag) return false;
-        if (globaltimer_ns() - t0 > JFA_WAIT_TIMEOUT_NS) return false;
+        if (globaltimer_ns() - t0 > limit) return false;
     }
 }
 
@@ -96,6 +105,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   const volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, abort_flag);
+}
+
+// Drain of a ring of `stages` full barriers (at bar0, 8 bytes apart) after `count` loads
+// were issued into it in order, stage i % stages for load i: waits for the last load of
+// each stage.
+__device__ __forceinline__ void drain_ring(uint32_t bar0, uint32_t count, uint32_t stages) {
+    for (uint32_t s = 0; s < stages; ++s)
+        if (count > s) {
+            const uint32_t last = ((count - 1 - s) / stages) * stages + s;
+            mbar_wait_bounded(bar0 + 8u * s, (last / stages) & 1, nullptr);
+        }
 }
 
 // ---------------------------------------------------------------- TMA

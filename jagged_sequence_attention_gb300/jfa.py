@@ -32,7 +32,7 @@ EXPORTED = ["jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_pl
             "jfa_bwd", "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build",
             "jfa_status_string", "jfa_plan_set_timing", "jfa_plan_kernel_times", "jfa_bwd_static_scratch",
             "jfa_partition_sequences", "jfa_bwd_ex_workspace_size", "jfa_bwd_ex", "jfa_plan_create_shared_kv",
-            "jfa_partition_users", "jfa_plan_set_deterministic"]
+            "jfa_partition_users", "jfa_plan_set_deterministic", "jfa_plan_set_work_item"]
 
 
 class JFAError(RuntimeError):
@@ -50,39 +50,47 @@ def lib():
     if _lib is None:
         if not os.path.exists(_LIB_PATH):
             raise RuntimeError(f"libjfa.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
-        L = ctypes.CDLL(_LIB_PATH)
-        vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
-        P = ctypes.POINTER
-        L.jfa_plan_create.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, P(vp)]
-        L.jfa_plan_create_ex.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, P(vp)]
-        L.jfa_plan_create_shared_kv.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, P(vp)]
-        L.jfa_plan_destroy.argtypes = [vp]
-        L.jfa_plan_info.argtypes = [vp, P(i64), i32]
-        L.jfa_fwd.argtypes = [vp, i32, vp, vp, vp, i32, vp, f32, vp, i32, vp, vp]
-        L.jfa_bwd_workspace_size.argtypes = [vp, i32]
-        L.jfa_bwd_workspace_size.restype = sz
-        L.jfa_bwd.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
-        L.jfa_bwd_ex_workspace_size.argtypes = [vp, i32, i32]
-        L.jfa_bwd_ex_workspace_size.restype = sz
-        L.jfa_bwd_ex.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, vp, sz, vp]
-        L.jfa_bwd_static_scratch.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp]
-        L.jfa_plan_device_status.argtypes = [vp, vp]
-        L.jfa_partition_sequences.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp]
-        L.jfa_partition_users.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp]
-        L.jfa_worklist_size.argtypes = [vp, vp, i32, i32, i32, i32, i32, P(i64)]
-        L.jfa_worklist_build.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
-        L.jfa_plan_set_timing.argtypes = [vp, i32]
-        L.jfa_plan_set_deterministic.argtypes = [vp, i32]
-        L.jfa_plan_kernel_times.argtypes = [vp, vp, vp]
-        L.jfa_status_string.argtypes = [i32]
-        L.jfa_status_string.restype = ctypes.c_char_p
-        for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
-                     "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build", "jfa_plan_set_timing",
-                     "jfa_plan_kernel_times", "jfa_bwd_static_scratch", "jfa_partition_sequences", "jfa_bwd_ex",
-                     "jfa_plan_create_shared_kv", "jfa_partition_users", "jfa_plan_set_deterministic"):
-            getattr(L, name).restype = i32
-        _lib = L
+        _lib = load_library(_LIB_PATH)
     return _lib
+
+
+def load_library(path):
+    """A build of the library at `path` (the main one, or a test build) with the C-ABI's
+    argument and result types declared."""
+    L = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    P = ctypes.POINTER
+    L.jfa_plan_create.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, P(vp)]
+    L.jfa_plan_create_ex.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, P(vp)]
+    L.jfa_plan_create_shared_kv.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, P(vp)]
+    L.jfa_plan_destroy.argtypes = [vp]
+    L.jfa_plan_info.argtypes = [vp, P(i64), i32]
+    L.jfa_fwd.argtypes = [vp, i32, vp, vp, vp, i32, vp, f32, vp, i32, vp, vp]
+    L.jfa_bwd_workspace_size.argtypes = [vp, i32]
+    L.jfa_bwd_workspace_size.restype = sz
+    L.jfa_bwd.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, sz, vp]
+    L.jfa_bwd_ex_workspace_size.argtypes = [vp, i32, i32]
+    L.jfa_bwd_ex_workspace_size.restype = sz
+    L.jfa_bwd_ex.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp, vp, sz, vp]
+    L.jfa_bwd_static_scratch.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, vp]
+    L.jfa_plan_device_status.argtypes = [vp, vp]
+    L.jfa_partition_sequences.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp]
+    L.jfa_partition_users.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp]
+    L.jfa_worklist_size.argtypes = [vp, vp, i32, i32, i32, i32, i32, P(i64)]
+    L.jfa_worklist_build.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    L.jfa_plan_set_timing.argtypes = [vp, i32]
+    L.jfa_plan_set_deterministic.argtypes = [vp, i32]
+    L.jfa_plan_set_work_item.argtypes = [vp, i32, i64, vp]
+    L.jfa_plan_kernel_times.argtypes = [vp, vp, vp]
+    L.jfa_status_string.argtypes = [i32]
+    L.jfa_status_string.restype = ctypes.c_char_p
+    for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_info", "jfa_fwd", "jfa_bwd",
+                 "jfa_plan_device_status", "jfa_worklist_size", "jfa_worklist_build", "jfa_plan_set_timing",
+                 "jfa_plan_kernel_times", "jfa_bwd_static_scratch", "jfa_partition_sequences", "jfa_bwd_ex",
+                 "jfa_plan_create_shared_kv", "jfa_partition_users", "jfa_plan_set_deterministic",
+                 "jfa_plan_set_work_item"):
+        getattr(L, name).restype = i32
+    return L
 
 
 def jfa_status_string(status: int) -> str:
@@ -308,6 +316,14 @@ def jfa_plan_device_status(plan: Plan, stream=None) -> int:
 
 
 KERNEL_KINDS = ["fwd", "bwd_pre", "bwd_main", "bwd_post", "bwd_dq"]
+
+
+def jfa_plan_set_work_item(plan: Plan, pass_: int, index: int, item):
+    """Test hook: overwrite work item `index` of pass 0 (forward), 1 (dK/dV) or 2 (dQ) with
+    the four ints of `item` (see include/jfa.h)."""
+    buf = np.ascontiguousarray(np.asarray(item, dtype=np.int32).reshape(4))
+    _check("jfa_plan_set_work_item", lib().jfa_plan_set_work_item(plan.handle, int(pass_), int(index),
+                                                                    buf.ctypes.data_as(ctypes.c_void_p)))
 
 
 def jfa_plan_set_deterministic(plan: Plan, enable: bool = True):
