@@ -207,17 +207,41 @@ def oracle_sample(batch, target_seconds=15.0):
     return cpu, seqs
 
 
-def run_oracle_once(cpu_batch):
+def run_oracle_once(cpu_batch, results=None):
+    """Times one forward + backward of the oracle on a CPU batch; with a dict `results`, also
+    leaves the outputs there (O, lse, dQ, dK, dV as fp64 arrays)."""
     import oracle
     f64 = lambda t: t.detach().to(torch.float32).numpy().astype(np.float64)  # noqa: E731
     b = None if cpu_batch.bias is None else f64(cpu_batch.bias)
     t0 = time.perf_counter()
-    oracle.fwd(cpu_batch.q_off, cpu_batch.kv_off, f64(cpu_batch.Q), f64(cpu_batch.K), f64(cpu_batch.V),
-               mode=cpu_batch.mode, causal=cpu_batch.causal, bias=b, scale=cpu_batch.scale, window=cpu_batch.window)
-    oracle.bwd(cpu_batch.q_off, cpu_batch.kv_off, f64(cpu_batch.Q), f64(cpu_batch.K), f64(cpu_batch.V),
-               f64(cpu_batch.dO), mode=cpu_batch.mode, causal=cpu_batch.causal, bias=b, scale=cpu_batch.scale,
-               window=cpu_batch.window)
-    return time.perf_counter() - t0
+    O, lse = oracle.fwd(cpu_batch.q_off, cpu_batch.kv_off, f64(cpu_batch.Q), f64(cpu_batch.K), f64(cpu_batch.V),
+                        mode=cpu_batch.mode, causal=cpu_batch.causal, bias=b, scale=cpu_batch.scale,
+                        window=cpu_batch.window)
+    dQ, dK, dV = oracle.bwd(cpu_batch.q_off, cpu_batch.kv_off, f64(cpu_batch.Q), f64(cpu_batch.K), f64(cpu_batch.V),
+                            f64(cpu_batch.dO), mode=cpu_batch.mode, causal=cpu_batch.causal, bias=b,
+                            scale=cpu_batch.scale, window=cpu_batch.window)
+    el = time.perf_counter() - t0
+    if results is not None:
+        results.update(O=O, lse=lse, dQ=dQ, dK=dK, dV=dV)
+    return el
+
+
+def sample_errors(got, ref, softmax):
+    """Errors of the benchmarked launch's outputs on the oracle's sample (the tolerances of the
+    parity tests: forward max-abs <= 1e-2 beyond a bf16 output's own rounding and relative
+    Frobenius <= 5e-3; dQ, dK, dV relative Frobenius <= 1e-2)."""
+    rel = lambda a, r: float(np.linalg.norm(a - r) / max(np.linalg.norm(r), 1e-30))  # noqa: E731
+    e = {"O_max_abs": float(np.abs(got["O"] - ref["O"]).max()),
+         "O_max_abs_beyond_rounding": float((np.abs(got["O"] - ref["O"]) - np.abs(ref["O"]) * 2.0 ** -8).max()),
+         "O_rel_frob": rel(got["O"], ref["O"])}
+    for k in ("dQ", "dK", "dV"):
+        e[f"{k}_rel_frob"] = rel(got[k], ref[k])
+    if softmax:
+        fin = np.isfinite(ref["lse"])
+        e["lse_max_abs"] = float(np.abs(got["lse"][fin] - ref["lse"][fin]).max()) if fin.any() else 0.0
+    e["within_tolerance"] = bool(e["O_max_abs_beyond_rounding"] <= 1e-2 and e["O_rel_frob"] <= 5e-3 and
+                                 max(e["dQ_rel_frob"], e["dK_rel_frob"], e["dV_rel_frob"]) <= 1e-2)
+    return e
 
 
 def oracle_cores(cpu_batch):
@@ -359,6 +383,15 @@ def main():
     status = jfa.jfa_plan_device_status(plan)
     if status != 0:
         raise RuntimeError(f"device status after timing: {jfa.jfa_status_string(status)}")
+    # The timed launch's outputs for the oracle's sample (the shortest sequences, all heads),
+    # kept for the error report beside the CPU baseline (plain batches).
+    sampled_rows = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and batch.kv_map is None:
+        _, sample_seqs = oracle_sample(batch, args.cpu_seconds)
+        qi = np.concatenate([np.arange(batch.q_off[b], batch.q_off[b + 1]) for b in sample_seqs])
+        ki = np.concatenate([np.arange(batch.kv_off[b], batch.kv_off[b + 1]) for b in sample_seqs])
+        sel = lambda t, idx: t[torch.as_tensor(idx, device=t.device)].float().cpu().numpy().astype(np.float64)  # noqa: E731
+        sampled_rows = {"O": sel(O, qi), "lse": sel(lse, qi), "dQ": sel(dQ, qi), "dK": sel(dK, ki), "dV": sel(dV, ki)}
     if dist:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -512,11 +545,16 @@ def main():
         cpu, seqs = oracle_sample(wl.broadcast(batch), args.cpu_seconds)
         cf, cb = flops_of(cpu)
         run_oracle_once(wl.subset(cpu, [0], [0]))
-        t = run_oracle_once(cpu)
+        ref = {}
+        t = run_oracle_once(cpu, ref)
         line["cpu_baseline"] = {"value": (cf + cb) / t / 1e12, "unit": UNIT, "cores": oracle_cores(cpu),
                                 "kind": "oracle", "seconds": t,
                                 "sample": f"{len(seqs)} shortest sequences (lengths "
                                           f"{sorted(batch.q_lens[seqs].tolist())}), all {cpu.H} heads, fwd+bwd fp64"}
+        if sampled_rows is not None:
+            # the benchmarked launch's own outputs for the same sequences, against the oracle
+            line["parity_sample"] = {"sample": line["cpu_baseline"]["sample"],
+                                     **sample_errors(sampled_rows, ref, batch.mode == "softmax")}
 
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -40,9 +40,11 @@ def max_abs(got, ref):
     return float(np.max(np.abs(got - ref))) if got.size else 0.0
 
 
-def run_gpu(batch, with_backward=True, out_dtype=torch.float32):
+def run_gpu(batch, with_backward=True, out_dtype=torch.float32, deterministic=False):
+    """The batch through the C-ABI (deterministic: the two-pass bf16 backward, whatever the
+    planner would choose)."""
     from jagged_sequence_attention_gb300 import jfa
-    out = jfa.attention(batch, with_backward=with_backward, out_dtype=out_dtype)
+    out = jfa.attention(batch, with_backward=with_backward, out_dtype=out_dtype, deterministic=deterministic)
     torch.cuda.synchronize()
     status = jfa.jfa_plan_device_status(out["plan"])
     out["status"] = status

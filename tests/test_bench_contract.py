@@ -59,3 +59,20 @@ def test_our_arm_fails_loudly_without_a_gpu():
     r = run_bench("--workload", "tiny", "--steps", "1", "--warmup", "3", timeout=300)
     assert r.returncode != 0
     assert not any(ln.strip().startswith("{") for ln in r.stdout.splitlines())
+
+
+def test_sample_errors_apply_the_parity_tolerances():
+    """The bench line's error report on the oracle's sample uses the parity tests' bounds."""
+    import numpy as np
+    import bench
+    rng = np.random.default_rng(0)
+    ref = {k: rng.standard_normal((50, 2, 8)) for k in ("O", "dQ", "dK", "dV")}
+    ref["lse"] = rng.standard_normal((50, 2))
+    got = {k: v.copy() for k, v in ref.items()}
+    e = bench.sample_errors(got, ref, True)
+    assert e["within_tolerance"] and e["O_max_abs"] == 0.0 and e["dK_rel_frob"] == 0.0
+    got["dQ"] = ref["dQ"] * 2.0  # a dQ counted twice
+    assert not bench.sample_errors(got, ref, True)["within_tolerance"]
+    got = {k: v.copy() for k, v in ref.items()}
+    got["O"] = ref["O"] + 0.05  # beyond the forward's max-abs bound
+    assert not bench.sample_errors(got, ref, True)["within_tolerance"]

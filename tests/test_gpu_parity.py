@@ -26,9 +26,13 @@ def _lib():
     _build.build()
 
 
-def check_full(batch, with_backward=True, out_dtype=torch.float32):
-    g = parity.run_gpu(batch, with_backward, out_dtype=out_dtype)
+def check_full(batch, with_backward=True, out_dtype=torch.float32, form="planner"):
+    """form: "planner" (the plan's own choice of bf16 backward) or "two_pass" (forced)."""
+    g = parity.run_gpu(batch, with_backward, out_dtype=out_dtype, deterministic=form == "two_pass")
     assert g["status"] == 0, g["status"]
+    if form == "two_pass":
+        from jagged_sequence_attention_gb300 import jfa
+        assert jfa.jfa_plan_info(g["plan"])["bwd_fused"] == 0
     r = parity.run_oracle(batch, with_backward)
     m = parity.compare(g, r, softmax=batch.mode == "softmax", with_backward=with_backward)
     print(batch.name, m)
@@ -49,10 +53,11 @@ def pick_sequences(batch, k_random=4, seed=0):
 
 
 @pytest.mark.parametrize("name", ["causal_bias", "cross", "gdpa_gelu", "gdpa_silu"])
-@pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_workload_slice_full(name, out):
+@pytest.mark.parametrize("out,form", [("f32", "planner"), ("bf16", "planner"), ("f32", "two_pass")])
+def test_workload_slice_full(name, out, form):
     full = wl.make(name, device="cuda")
-    check_full(wl.subset(full, pick_sequences(full)), out_dtype=torch.float32 if out == "f32" else torch.bfloat16)
+    check_full(wl.subset(full, pick_sequences(full)), out_dtype=torch.float32 if out == "f32" else torch.bfloat16,
+               form=form)
 
 
 def test_long_causal_scaled_down_full():
@@ -63,27 +68,31 @@ def test_long_causal_scaled_down_full():
     check_full(wl.make_custom(lens, lens, H=8, D=128, causal=True, bias=True, device="cuda", seed=77))
 
 
+@pytest.mark.parametrize("form", ["planner", "two_pass"])
 @pytest.mark.parametrize("mode", ["softmax", "gelu_tanh", "silu"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("bias", [False, True])
-def test_edge_lengths(mode, causal, bias):
+def test_edge_lengths(mode, causal, bias, form):
     # empty sequences, single tokens, tile boundaries +-1, q > kv and q < kv, a kv tail
     # inside a tile, and the last sequence ending at the end of the buffers
     q = [0, 1, 127, 128, 129, 3, 0, 5, 1, 200, 64]
     kv = [4, 1, 127, 128, 129, 0, 0, 300, 257, 130, 1]
     std = 1.0 if mode == "softmax" else 0.5
     check_full(wl.make_custom(q, kv, H=2, D=128, mode=mode, causal=causal, bias=bias, value_std=std,
-                              device="cuda", seed=11))
+                              device="cuda", seed=11), form=form)
 
 
-@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 64), (torch.float32, 32), (torch.float32, 64)])
-def test_other_head_dims(dtype, D):
+@pytest.mark.parametrize("dtype,D,form", [(torch.bfloat16, 64, "planner"), (torch.bfloat16, 64, "two_pass"),
+                                          (torch.float32, 32, "planner"), (torch.float32, 64, "planner")])
+def test_other_head_dims(dtype, D, form):
     check_full(wl.make_custom([7, 130, 64, 1], [200, 5, 64, 129], H=3, D=D, dtype=dtype, causal=True, bias=True,
-                              device="cuda", seed=12))
+                              device="cuda", seed=12), form=form)
 
 
-def test_guard_bands_untouched():
-    """Rows past the last offset of every output buffer keep their canary values."""
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_guard_bands_untouched(deterministic):
+    """Rows past the last offset of every output buffer keep their canary values (both bf16
+    backward forms: the fused one adds into an accumulator, the two-pass one writes rows)."""
     from jagged_sequence_attention_gb300 import jfa
     b = wl.make_custom([5, 130, 77], [129, 3, 200], H=2, D=128, causal=True, bias=True, device="cuda", seed=13)
     Tq, Tkv, pad = int(b.q_off[-1]), int(b.kv_off[-1]), 37
@@ -97,6 +106,8 @@ def test_guard_bands_untouched():
     O = O.float()
     lse = torch.full((Tq + pad, b.H), canary, dtype=torch.float32, device="cuda")
     plan = jfa.jfa_plan_create(b.q_off, b.kv_off, b.H, b.D, b.mode, b.causal)
+    jfa.jfa_plan_set_deterministic(plan, deterministic)
+    assert jfa.jfa_plan_info(plan)["bwd_fused"] == (0 if deterministic else 1)
     jfa.jfa_fwd(plan, b.Q, b.K, b.V, b.bias, b.scale, O=O, lse=lse)
     jfa.jfa_bwd(plan, b.Q, b.K, b.V, O, b.dO, lse, b.bias, b.scale, dQ=dQ, dK=dK, dV=dV)
     torch.cuda.synchronize()
