@@ -64,9 +64,9 @@ def flops_of(batch):
 
 def algorithmic_bytes(batch, elem=2, fused=False):
     """Compulsory HBM bytes of one launch of each tensor-core kernel: every input it
-    reads and every output it writes, once.  The fused backward reads Q, dO, K, V and
-    writes dK, dV and dQ (its fp32 dQ accumulator is implementation traffic, not
-    algorithmic)."""
+    reads and every output it writes, once.  A one-kernel backward (fused or
+    short-query) reads Q, dO, K, V and writes dK, dV and dQ (the fused form's fp32 dQ
+    accumulator is implementation traffic, not algorithmic)."""
     Tq, Tkv, H, D = int(batch.q_off[-1]), int(batch.kv_off[-1]), batch.H, batch.D
     if fused:
         return {
@@ -82,8 +82,8 @@ def algorithmic_bytes(batch, elem=2, fused=False):
 
 def kernel_flops(fwd_flop, fused=False):
     """Algorithmic FLOPs per launch of each tensor-core kernel.  The backward's five
-    products (S, dP, dV, dK, dQ; 2.5x the forward's two) all run in the fused backward
-    kernel; on the two-pass backward they split as: dK/dV kernel S, dP, dV, dK (2x), dQ
+    products (S, dP, dV, dK, dQ; 2.5x the forward's two) all run in a one-kernel backward
+    (fused or short-query); on the two-pass backward they split as: dK/dV kernel S, dP, dV, dK (2x), dQ
     kernel the dQ product (0.5x), whose recomputed S and dP are not algorithmic work and
     are not counted."""
     if fused:
@@ -338,10 +338,15 @@ def main():
 
     stream = torch.cuda.current_stream()
     plan = jfa.plan_for(batch)
-    # jfa_bwd on bf16 inputs (no dense bias, no bias gradient) runs the fused backward
-    fused = batch.Q.dtype == torch.bfloat16 and jfa.jfa_plan_info(plan)["bwd_fused"] == 1
-    kbytes = algorithmic_bytes(batch, fused=fused)
-    cfg["backward"] = "fused dK/dV/dQ kernel" if fused else "dK/dV kernel + dQ kernel"
+    # The backward form jfa_bwd runs on bf16 inputs: short-query (no bias, every query set
+    # in one tile), else fused (no dense bias, no bias gradient), else two-pass.
+    info = jfa.jfa_plan_info(plan)
+    bf16 = batch.Q.dtype == torch.bfloat16
+    short_q = bf16 and info["bwd_short"] > 0 and batch.bias is None
+    fused = bf16 and not short_q and info["bwd_fused"] == 1
+    kbytes = algorithmic_bytes(batch, fused=fused or short_q)
+    cfg["backward"] = ("short-query dQ/dK/dV kernel" if short_q else
+                       "fused dK/dV/dQ kernel" if fused else "dK/dV kernel + dQ kernel")
     O = torch.empty_like(batch.Q)
     lse = torch.empty((batch.Q.shape[0], batch.H), dtype=torch.float32, device=dev)
     dQ, dK, dV = torch.empty_like(batch.Q), torch.empty_like(batch.K), torch.empty_like(batch.V)
@@ -405,20 +410,30 @@ def main():
 
     # dominant kernel: the largest share of device time among the tensor-core kernels
     per = {k: (v[0] / v[1] if v[1] else 0.0, v[1], v[0]) for k, v in kt.items()}
-    kflop = kernel_flops(fl_f, fused)
-    kname_of = {"fwd": "jfa_fwd_kernel", "bwd_main": "jfa_bwd_fused_kernel" if fused else "jfa_bwd_dkdv_kernel"}
-    if not fused:
+    kflop = kernel_flops(fl_f, fused or short_q)
+    kname_of = {"fwd": "jfa_fwd_kernel", "bwd_main": ("jfa_bwd_short_kernel" if short_q else
+                                                      "jfa_bwd_fused_kernel" if fused else "jfa_bwd_dkdv_kernel")}
+    if not (fused or short_q):
         kname_of["bwd_dq"] = "jfa_bwd_dq_kernel"
     dom = max(kname_of, key=lambda k: per[k][2])
     dom_ms = per[dom][0]
     achieved = kflop[dom] / (dom_ms / 1e3) / 1e12 if dom_ms > 0 else 0.0
     kname = kname_of[dom]
-    roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
-                "peak_kind": f"bf16 dense, sustained, {peaks['source']}", "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops_sustained"],
-                "traffic": measured_traffic(kname, args.workload),
-                "algorithmic_bytes_per_launch": kbytes[dom],
-                "flop_per_launch": kflop[dom]}
+    # The roof that binds the dominant kernel: the one its algorithmic rate comes closer to
+    # (tensor FLOP/s on the long sequences, HBM bytes/s on the short-query shapes).
+    gbs = kbytes[dom] / (dom_ms / 1e3) / 1e9 if dom_ms > 0 else 0.0
+    frac_t = achieved / peaks["bf16_tflops_sustained"]
+    frac_b = gbs / peaks["hbm_gbs"]
+    if frac_b > frac_t:
+        roofline = {"bound": "hbm", "kernel": kname, "achieved": gbs, "peak": peaks["hbm_gbs"],
+                    "peak_kind": f"HBM copy, {peaks['source']}", "unit": "GB/s", "frac": frac_b,
+                    "tensor_frac": frac_t}
+    else:
+        roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
+                    "peak_kind": f"bf16 dense, sustained, {peaks['source']}", "unit": "TFLOP/s", "frac": frac_t,
+                    "hbm_frac": frac_b}
+    roofline.update({"traffic": measured_traffic(kname, args.workload),
+                     "algorithmic_bytes_per_launch": kbytes[dom], "flop_per_launch": kflop[dom]})
     kernels = {k: {"ms_per_launch": v[0], "launches": v[1], "share": v[2] / max(1e-9, sum(x[2] for x in per.values())),
                    **({"tflops": kflop[k] / (v[0] / 1e3) / 1e12,
                        "gbs": kbytes[k] / (v[0] / 1e3) / 1e9} if k in kflop and v[0] > 0 else {})}

@@ -136,8 +136,9 @@ const char* jfa_status_string(int32_t s) {
 
 jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H,
                              int32_t causal, int32_t window, int32_t pass, int64_t* n_items) {
-    if (!n_items || H < 1 || pass < kPassFwd || pass > kPassBwdQ) return JFA_ERR_INVALID_ARG;
+    if (!n_items || H < 1 || pass < kPassFwd || pass > kPassBwdShort) return JFA_ERR_INVALID_ARG;
     if (window < -1 || (window >= 0 && causal != 1)) return JFA_ERR_INVALID_ARG;
+    if (pass == kPassBwdShort && (causal != 0 || window >= 0)) return JFA_ERR_INVALID_ARG;
     jfa_status s = validate_offsets(q_offsets, kv_offsets, B);
     if (s != JFA_OK) return s;
     *n_items = count_items(q_offsets, kv_offsets, B, H, causal, pass);
@@ -147,8 +148,9 @@ jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets
 jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B, int32_t H,
                               int32_t causal, int32_t window, int32_t pass, int32_t n_ctas, int32_t* items,
                               int32_t* cta_offsets, int64_t* cta_cost) {
-    if (H < 1 || n_ctas < 1 || !cta_offsets || pass < kPassFwd || pass > kPassBwdQ) return JFA_ERR_INVALID_ARG;
+    if (H < 1 || n_ctas < 1 || !cta_offsets || pass < kPassFwd || pass > kPassBwdShort) return JFA_ERR_INVALID_ARG;
     if (window < -1 || (window >= 0 && causal != 1)) return JFA_ERR_INVALID_ARG;
+    if (pass == kPassBwdShort && (causal != 0 || window >= 0)) return JFA_ERR_INVALID_ARG;
     jfa_status s = validate_offsets(q_offsets, kv_offsets, B);
     if (s != JFA_OK) return s;
     const int64_t n = count_items(q_offsets, kv_offsets, B, H, causal, pass);
@@ -260,6 +262,18 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
             for (int64_t i = 0; i < p->n_bwd_items; ++i) total_steps += bi[size_t(i)].n_inner;
         p->fused_pref = !kv_map && p->n_bwd_items > 0 && total_steps <= kFusedMaxMeanSteps * p->n_bwd_items;
     }
+    // Short-query backward: one (sequence, head) item per query set, when each fits one tile.
+    p->short_bq = short_query_rows(qo.data(), B, D, causal, window, kv_map != nullptr);
+    std::vector<WorkItem> si(1);
+    std::vector<int32_t> sio(2, 0);
+    if (p->short_bq > 0) {
+        p->n_short_items = count_items(qo.data(), ko.data(), B, H, 0, kPassBwdShort);
+        p->short_grid = int(std::max<int64_t>(
+            1, std::min<int64_t>(int64_t(p->num_sms) * short_ctas_per_sm(D, p->short_bq), p->n_short_items)));
+        si.resize(size_t(std::max<int64_t>(1, p->n_short_items)));
+        sio.resize(size_t(p->short_grid) + 1);
+        build_worklist(qo.data(), ko.data(), B, H, 0, -1, kPassBwdShort, p->short_grid, si.data(), sio.data(), nullptr);
+    }
     std::vector<int64_t> po(size_t(B) + 1, 0);  // pair offsets of a dense bias
     for (int32_t b = 0; b < B; ++b)
         po[size_t(b) + 1] = po[size_t(b)] + int64_t(qo[size_t(b) + 1] - qo[size_t(b)]) * int64_t(kvv[size_t(b) + 1] - kvv[size_t(b)]);
@@ -286,6 +300,8 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
     const size_t o_sp = cur; cur += round_up(steps.size() * 8, 256);
     const size_t o_so = cur; cur += round_up(step_off.size() * 4, 256);
     const size_t o_ko = cur; cur += round_up(ktile_off.size() * 4, 256);
+    const size_t o_si = cur; cur += round_up(si.size() * 16, 256);
+    const size_t o_sio = cur; cur += round_up(sio.size() * 4, 256);
     if (cudaMalloc(&p->dev_block, cur) != cudaSuccess) {
         delete p;
         return JFA_ERR_CUDA;
@@ -305,6 +321,8 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
     p->d_steps = kv_map ? reinterpret_cast<int2*>(base + o_sp) : nullptr;
     p->d_step_off = kv_map ? reinterpret_cast<int32_t*>(base + o_so) : nullptr;
     p->d_ktile_off = kv_map ? reinterpret_cast<int32_t*>(base + o_ko) : nullptr;
+    p->d_short_items = reinterpret_cast<int4*>(base + o_si);
+    p->d_short_cta_off = reinterpret_cast<int32_t*>(base + o_sio);
     auto up = [&](void* dst, const void* src, size_t bytes) {
         return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st) == cudaSuccess;
     };
@@ -315,7 +333,8 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
               up(p->d_dq_items, qi.data(), qi.size() * 16) && up(p->d_dq_cta_off, qio.data(), qio.size() * 4) &&
               up(p->d_pair_off, po.data(), po.size() * 8) && up(base + o_map, map_h.data(), map_h.size() * 4) &&
               up(base + o_sp, steps.data(), steps.size() * 8) && up(base + o_so, step_off.data(), step_off.size() * 4) &&
-              up(base + o_ko, ktile_off.data(), ktile_off.size() * 4);
+              up(base + o_ko, ktile_off.data(), ktile_off.size() * 4) &&
+              up(base + o_si, si.data(), si.size() * 16) && up(base + o_sio, sio.data(), sio.size() * 4);
     // The host vectors are pageable: the copies above are staged before returning,
     // but keep the stream ordered before the vectors go out of scope.
     if (!ok || cudaStreamSynchronize(st) != cudaSuccess) {
@@ -424,22 +443,29 @@ jfa_status jfa_plan_destroy(jfa_plan plan) {
 
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
     if (!plan || !info || n < 0) return JFA_ERR_INVALID_ARG;
-    const int64_t v[20] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
+    const int64_t v[21] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
                            plan->mode,     plan->causal,  plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items,
                            plan->bwd_grid, plan->num_sms, plan->n_dq_items,  plan->dq_grid,  plan->window,
                            plan->n_pairs,  plan->shared_kv ? plan->U : -1,
                            plan->merged ? int64_t(plan->merged->B) : -1,
                            plan->fwd_split ? 1 : 0,
-                           fused_backward(plan) ? 1 : 0};
-    for (int32_t i = 0; i < n && i < 20; ++i) info[i] = v[i];
+                           fused_backward(plan) ? 1 : 0,
+                           short_backward(plan, JFA_BIAS_NONE, false) ? plan->short_bq : 0};
+    for (int32_t i = 0; i < n && i < 21; ++i) info[i] = v[i];
     return JFA_OK;
 }
 
 jfa_status jfa_plan_set_work_item(jfa_plan plan, int32_t pass, int64_t index, const int32_t* item) {
-    if (!plan || !item || pass < kPassFwd || pass > kPassBwdQ || index < 0) return JFA_ERR_INVALID_ARG;
-    const int64_t n = pass == kPassFwd ? plan->n_fwd_items : pass == kPassBwdKV ? plan->n_bwd_items : plan->n_dq_items;
+    if (!plan || !item || pass < kPassFwd || pass > kPassBwdShort || index < 0) return JFA_ERR_INVALID_ARG;
+    const int64_t n = pass == kPassFwd     ? plan->n_fwd_items
+                      : pass == kPassBwdKV ? plan->n_bwd_items
+                      : pass == kPassBwdQ  ? plan->n_dq_items
+                                           : plan->n_short_items;
     if (index >= n) return JFA_ERR_INVALID_ARG;
-    int4* list = pass == kPassFwd ? plan->d_fwd_items : pass == kPassBwdKV ? plan->d_bwd_items : plan->d_dq_items;
+    int4* list = pass == kPassFwd     ? plan->d_fwd_items
+                 : pass == kPassBwdKV ? plan->d_bwd_items
+                 : pass == kPassBwdQ  ? plan->d_dq_items
+                                      : plan->d_short_items;
     const int4 w = make_int4(item[0], item[1], item[2], item[3]);
     return cudaMemcpy(list + index, &w, sizeof(w), cudaMemcpyHostToDevice) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
@@ -619,9 +645,12 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
     }
     if (plan->Tkv == 0 && plan->Tq == 0) return JFA_OK;
     const size_t rows = size_t(plan->Tq) * size_t(plan->H);
+    // bf16 inputs without a bias or a bias gradient, every query set in one tile: dQ, dK and
+    // dV in one kernel over (sequence, head) items, dQ held in TMEM (bwd_short.cu)
+    const bool short_q = dtype == JFA_BF16 && short_backward(v, bias_kind, dbias != nullptr);
     // bf16 inputs without a dense bias or a bias gradient: dK, dV and dQ in one kernel that
     // adds dQ into an fp32 accumulator (bwd_fused.cu)
-    const bool fused = dtype == JFA_BF16 && !plan->deterministic && v->fused_pref && !dense && !dbias;
+    const bool fused = dtype == JFA_BF16 && !short_q && !plan->deterministic && v->fused_pref && !dense && !dbias;
     float* delta = static_cast<float*>(workspace);
     float* dq_acc = (dtype == JFA_F32 || fused)
                         ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * 4, 256))
@@ -638,11 +667,12 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
     CUtensorMap mq, mk, mv, mdo;
     BwdParams p;
     if (v->n_bwd_items > 0 || (dtype == JFA_BF16 && v->n_dq_items > 0)) {
+        const int q_box = short_q ? v->short_bq : kBwdBM;  // Q and dO rows per load
         if (dtype == JFA_BF16 &&
-            ((s = make_map(&mq, dtype, Q, plan->Tq, plan->H, plan->D, plan->dev_block, kBwdBM)) != JFA_OK ||
+            ((s = make_map(&mq, dtype, Q, plan->Tq, plan->H, plan->D, plan->dev_block, q_box)) != JFA_OK ||
              (s = make_map(&mk, dtype, K, plan->Tkv, plan->H, plan->D, plan->dev_block, kBwdBN)) != JFA_OK ||
              (s = make_map(&mv, dtype, V, plan->Tkv, plan->H, plan->D, plan->dev_block, kBwdBN)) != JFA_OK ||
-             (s = make_map(&mdo, dtype, dO, plan->Tq, plan->H, plan->D, plan->dev_block, kBwdBM)) != JFA_OK))
+             (s = make_map(&mdo, dtype, dO, plan->Tq, plan->H, plan->D, plan->dev_block, q_box)) != JFA_OK))
             return s;
         p.items = v->d_bwd_items;
         p.cta_off = v->d_bwd_cta_off;
@@ -677,6 +707,18 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
         p.kv_map = v->d_kv_map;
         p.n_seq = v->B;
         p.n_kv = v->U;
+    }
+    if (short_q) {
+        // one kernel writes dQ, dK and dV (also the zero rows of sequences without a query
+        // or a key)
+        p.items = v->d_short_items;
+        p.cta_off = v->d_short_cta_off;
+        KernelTimer tm(plan, 2, st);
+        e = v->n_short_items > 0
+                ? launch_bwd_short(plan->D, v->short_bq, mq, mk, mv, mdo, p, v->short_grid, st)
+                : cudaSuccess;
+        tm.done();
+        return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
     }
     if (v->n_bwd_items > 0) {
         KernelTimer tm(plan, 2, st);

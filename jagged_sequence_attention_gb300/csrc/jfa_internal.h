@@ -23,8 +23,8 @@ constexpr int kBwdBN = 128;
 constexpr int kBwdBM = 128;
 
 // Work-list passes: forward query-tile pairs, backward key tiles (dK/dV), backward
-// query tiles (dQ).
-enum : int { kPassFwd = 0, kPassBwdKV = 1, kPassBwdQ = 2 };
+// query tiles (dQ), and the short-query backward's (sequence, head) items.
+enum : int { kPassFwd = 0, kPassBwdKV = 1, kPassBwdQ = 2, kPassBwdShort = 3 };
 
 // Kernel kinds of the timing hook: forward, backward preprocess, backward dK/dV (or
 // the fp32 main kernel), fp32 dQ conversion, bf16 dQ.
@@ -229,6 +229,15 @@ __device__ inline bool kv_item_ok(const int4 w, const BwdParams& p, bool shared)
     return w.w == n;
 }
 
+// Short-query backward: item (sequence w.x, head w.y, 0, key tiles of the sequence) of a
+// sequence with at most bq query rows (no shared key/value, no causal mask or window).
+__device__ inline bool short_item_ok(const int4 w, const BwdParams& p, int bq) {
+    if (w.x < 0 || w.x >= p.n_seq || w.x >= p.n_kv || w.y < 0 || w.y >= p.H || w.z != 0 || w.w < 0) return false;
+    const int q_len = p.q_off[w.x + 1] - p.q_off[w.x], kv_len = p.kv_off[w.x + 1] - p.kv_off[w.x];
+    if (q_len > bq) return false;
+    return w.w == (kv_len + kBwdBN - 1) / kBwdBN;
+}
+
 // Host planner (plan.cpp).  Returns JFA_OK or an error for bad offsets.
 jfa_status validate_offsets(const int32_t* q_off, const int32_t* kv_off, int32_t B);
 int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
@@ -268,6 +277,15 @@ cudaError_t launch_bwd_post(int dtype, int D, const float* dq_acc, void* dQ, int
 // into p.dq_acc (zeroed first) for launch_bwd_post to scale and convert.
 cudaError_t launch_bwd_fused(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st);
+// bf16 inputs, short-query backward (bwd_short.cu): dQ, dK and dV in one kernel over
+// (sequence, head) items of plans whose query sets have at most bq (64 or 128) rows.
+cudaError_t launch_bwd_short(int D, int bq, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st);
+// CTAs of that kernel an SM holds (2 at D = 64 with 64-row query tiles), 0 if unsupported.
+int short_ctas_per_sm(int D, int bq);
+// Query-tile rows of the short-query backward for a plan (0: the form does not apply):
+// every query set fits one tile, no shared key/value, no causal mask, no window.
+int short_query_rows(const int32_t* q_off, int32_t B, int32_t D, int32_t causal, int32_t window, bool shared_kv);
 // Whether jfa_bwd on bf16 inputs runs the fused backward for this plan (without a dense
 // bias or a bias gradient): plans whose dK/dV items visit at most kFusedMaxMeanSteps
 // query tiles on average (not shared key/value plans), unless the caller asked for the
@@ -326,11 +344,25 @@ struct jfa_plan_t {
     bool fwd_split;  // forward kernel with split items (prefer_split_forward)
     bool deterministic = false;  // jfa_plan_set_deterministic: the two-pass bf16 backward
     bool fused_pref = false;     // the planner's choice of the fused bf16 backward
+    // short-query backward: query-tile rows (0: not applicable) and its work list
+    int short_bq = 0;
+    int64_t n_short_items = 0;
+    int short_grid = 1;
+    int4* d_short_items = nullptr;
+    int32_t* d_short_cta_off = nullptr;
     // optional per-kernel timing (jfa_plan_set_timing)
     bool timing;
     std::vector<cudaEvent_t> ev_pool;                 // reusable events
     std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> ev_pending;  // kind, (start, stop)
 };
+
+namespace jfa {
+// Whether jfa_bwd on bf16 inputs with this bias (and no bias gradient) runs the
+// short-query backward.
+inline bool short_backward(const jfa_plan_t* plan, int32_t bias_kind, bool dbias) {
+    return !plan->deterministic && plan->short_bq > 0 && bias_kind == JFA_BIAS_NONE && !dbias;
+}
+}  // namespace jfa
 
 inline bool jfa::fused_backward(const jfa_plan_t* plan) {
     return !plan->deterministic && (plan->fused_pref || (plan->merged && plan->merged->fused_pref));

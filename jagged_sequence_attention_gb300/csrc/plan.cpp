@@ -68,6 +68,14 @@ void build_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t
                     query_tile_range(q_len, kv_len, t, causal, window, first, n);
                     out->push_back({{b, h, int32_t(t), int32_t(n)}, 4 * int64_t(n) + 2});
                 }
+        } else if (pass == kPassBwdShort) {
+            // Short-query backward: one item per (sequence, head) with a query or a key,
+            // visiting all of the sequence's key tiles, five products each (a sequence
+            // without queries only has its dK/dV rows zeroed).
+            if (q_len == 0 && kv_len == 0) continue;
+            const int64_t n = ceil_div(kv_len, kBwdBN);
+            for (int32_t h = 0; h < H; ++h)
+                out->push_back({{b, h, 0, int32_t(n)}, (q_len > 0 ? 5 * n : n) + 2});
         } else {
             // Backward dQ: one item per 128-row query tile (also when it sees no key, so
             // that its dQ rows are written); it visits the forward's key-tile range, three
@@ -88,6 +96,11 @@ int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int3
                     int32_t causal, int32_t pass) {
     (void)causal;
     int64_t n = 0;
+    if (pass == kPassBwdShort) {
+        for (int32_t b = 0; b < B; ++b)
+            if (q_off[b + 1] > q_off[b] || kv_off[b + 1] > kv_off[b]) n += H;
+        return n;
+    }
     for (int32_t b = 0; b < B; ++b) {
         const int64_t len = pass == kPassBwdKV ? kv_off[b + 1] - kv_off[b] : q_off[b + 1] - q_off[b];
         const int64_t tile = pass == kPassFwd ? kFwdPairRows : pass == kPassBwdKV ? kBwdBN : kFwdBM;
@@ -211,6 +224,19 @@ bool prefer_split_forward(const int32_t* q_off, const int32_t* kv_off, int32_t B
         }
     }
     return split > 0 && 2 * split >= total;
+}
+
+// The short-query backward keeps a whole query set in one tile of 64 or 128 rows and its
+// dQ in TMEM across the key tiles.  Its TMEM budget (S^T, dP^T/dV, dK and dQ columns)
+// fits a 64-row tile at head_dim 64 in 256 columns, so two CTAs share an SM; other
+// tiles take all 512.
+int short_query_rows(const int32_t* q_off, int32_t B, int32_t D, int32_t causal, int32_t window, bool shared_kv) {
+    if (shared_kv || causal || window >= 0 || (D != 64 && D != 128)) return 0;
+    int32_t max_q = 0;
+    for (int32_t b = 0; b < B; ++b) max_q = std::max(max_q, q_off[b + 1] - q_off[b]);
+    if (max_q == 0) return 0;
+    if (D == 64 && max_q <= 64) return 64;
+    return max_q <= 128 ? 128 : 0;
 }
 
 int64_t count_shared_kv_dkdv_items(const int32_t* u_off, int32_t U, int32_t H) {

@@ -247,3 +247,20 @@ def test_planning_without_a_gpu_fails_loudly():
     K = torch.zeros(9, 2, 64, dtype=torch.bfloat16, requires_grad=True)
     with pytest.raises((jfa.JFAError, RuntimeError)):
         jfa.jagged_attention(Q, K, K, [0, 3, 5], [0, 4, 9])
+
+
+def test_worklist_of_the_short_query_pass(jfa):
+    # pass 3: one item per (sequence, head) with a query or a key, visiting all of the
+    # sequence's key tiles; the pass has no causal or windowed form
+    q = [0, 3, 0, 64, 1]
+    kv = [0, 0, 129, 256, 1000]
+    qo, ko = np.cumsum([0] + q), np.cumsum([0] + kv)
+    items, offs, cost = jfa.jfa_worklist_build(qo, ko, 2, False, 3, 3)
+    got = sorted(map(tuple, items.tolist()))
+    want = sorted((s, h, 0, -(-kv[s] // 128)) for s in range(5) for h in range(2) if q[s] or kv[s])
+    assert got == want
+    assert offs[0] == 0 and offs[-1] == len(want)
+    # LPT: every CTA within one item's cost of the least loaded one
+    assert cost.max() - cost.min() <= 5 * 8 + 2
+    with pytest.raises(jfa.JFAError):
+        jfa.jfa_worklist_build(qo, ko, 2, True, 3, 3)

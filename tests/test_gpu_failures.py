@@ -5,8 +5,8 @@
   and reports it.  The planner never writes such an item, so the tests plant one with
   jfa_plan_set_work_item -- a sequence or head outside the batch, a tile past the
   sequence, or an inner count other than the one the tile ranges give -- in each pass's
-  list, for the two-pass and the fused bf16 backward, the fp32 kernels and a shared
-  key/value plan.  Every planted item is caught by the check before any access it would
+  list, for the two-pass, the fused and the short-query bf16 backward, the fp32 kernels
+  and a shared key/value plan.  Every planted item is caught by the check before any access it would
   steer.
 - Bounded waits (JFA_ERR_TIMEOUT).  A test build of the forward kernel
   (JFA_TEST_STALL_MMA, pipeline waits limited to 20 ms) makes its tensor-core issuer wait
@@ -117,6 +117,23 @@ def test_planted_work_item_is_skipped_and_reported(jfa, case):
     _check_normal_call_is_right(b)
 
 
+@pytest.mark.parametrize("kind", ["sequence", "tile", "count"])
+def test_planted_item_in_the_short_query_backward(jfa, kind):
+    # query sets of one tile, no causal mask: jfa_bwd runs the short-query kernel (pass 3)
+    b = wl.make_custom([40, 7, 64], [300, 129, 1000], H=2, D=64, causal=False, device="cuda", seed=540)
+    plan = jfa.plan_for(b)
+    assert jfa.jfa_plan_info(plan)["bwd_short"] == 64
+    O, lse = jfa.jfa_fwd(plan, b.Q, b.K, b.V, None, b.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert jfa.jfa_plan_device_status(plan) == jfa.JFA_OK
+    seq = [b.B + 5, 0, 0, 1] if kind == "sequence" else [0, 0, 1, 3] if kind == "tile" else [0, 0, 0, 2]
+    jfa.jfa_plan_set_work_item(plan, 3, 0, seq)
+    jfa.jfa_bwd(plan, b.Q, b.K, b.V, O, b.dO, lse, None, b.scale)
+    torch.cuda.synchronize()
+    assert jfa.jfa_plan_device_status(plan) == jfa.JFA_ERR_DEVICE_BOUNDS
+    _check_normal_call_is_right(b)
+
+
 def test_planted_item_on_a_shared_key_value_plan(jfa):
     b = wl.make_shared_kv([40, 7, 128, 1, 64], [300, 129], [0, 1, 0, 0, 1], H=2, D=128, causal=True, bias=True,
                           seed=520, device="cuda")
@@ -134,7 +151,7 @@ def test_planted_item_on_a_shared_key_value_plan(jfa):
 def test_set_work_item_argument_errors(jfa):
     b = wl.make_custom([40], [40], H=1, D=128, device="cuda", seed=521)
     plan = jfa.plan_for(b)
-    for pass_, index in ((3, 0), (0, -1), (0, 10**6)):
+    for pass_, index in ((4, 0), (-1, 0), (0, -1), (0, 10**6), (3, 10**6)):
         with pytest.raises(jfa.JFAError) as e:
             jfa.jfa_plan_set_work_item(plan, pass_, index, [0, 0, 0, 1])
         assert e.value.status == jfa.JFA_ERR_INVALID_ARG

@@ -93,6 +93,28 @@ def test_static_scratch_equal_to_jfa_bwd_across_alternating_problems(jfa, mode, 
                 assert bool(((gf - rf).abs() <= rf.abs() * 2.0 ** -7 + 1e-6).all()), (k, name)
 
 
+@pytest.mark.parametrize("mode", ["softmax", "silu"])
+def test_static_scratch_on_the_short_query_backward(jfa, mode):
+    # query sets of one tile without a causal mask or a bias: the short-query kernel, which
+    # keeps only row terms in the scratch and adds nothing, so every output is equal bit
+    # for bit to jfa_bwd's, across calls on alternating problems
+    probs = [_problem(jfa, [40, 1, 64, 0, 17], [300, 129, 1000, 77, 0], mode, False, False, 781, H=2, D=64),
+             _problem(jfa, [128, 5, 90], [700, 1, 256], mode, False, False, 782, H=2, D=128)]
+    assert jfa.jfa_plan_info(probs[0][1])["bwd_short"] == 64 and jfa.jfa_plan_info(probs[1][1])["bwd_short"] == 128
+    outs = []
+    for k in range(4):
+        b, plan, O, lse, _ = probs[k % 2]
+        got = tuple(torch.full_like(t, float("nan")) for t in (b.Q, b.K, b.V))
+        assert _static_call(jfa, plan, b, jfa.JFA_BF16, O, jfa.JFA_F32, lse, *got) == jfa.JFA_OK
+        outs.append(got)
+    torch.cuda.synchronize()
+    for k, got in enumerate(outs):
+        b, plan, _, _, ref = probs[k % 2]
+        assert jfa.jfa_plan_device_status(plan) == jfa.JFA_OK
+        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+            assert torch.equal(g, r), (k, name)
+
+
 def test_static_scratch_fp32_consecutive_calls_clear_the_accumulator(jfa):
     # fp32 inputs keep the dQ accumulator in the shared array: a second call that did not
     # clear it would return about twice the first call's dQ.
