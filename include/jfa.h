@@ -165,7 +165,11 @@ jfa_status jfa_plan_destroy(jfa_plan plan);
  * key tile also adds its part of dQ into an fp32 accumulator held in the workspace, else
  * 0.  The planner chooses the fused form when the backward's key tiles visit few query
  * tiles on average (short sequences), unless jfa_plan_set_deterministic chose the
- * two-pass form; see jfa_plan_set_deterministic.  n may be smaller than 20.
+ * two-pass form; see jfa_plan_set_deterministic.  Fact 20 is the query-tile rows (64 or
+ * 128) of the short-query backward when jfa_bwd on JFA_BF16 inputs without a bias runs
+ * it for this plan, else 0: one kernel per (sequence, head) for batches whose query sets
+ * all fit one tile, with no causal mask, window or shared key/value (it then takes the
+ * place of the fused form for calls without a bias).  n may be smaller than 21.
  */
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
 
@@ -280,7 +284,7 @@ jfa_status jfa_bwd_static_scratch(jfa_plan plan, int32_t dtype, const void* Q, c
                                   float scale, void* dQ, void* dK, void* dV, void* stream);
 
 /*
- * The bf16 backward has two forms (the articles leave the backward's accumulation open;
+ * The bf16 backward has three forms (the articles leave the backward's accumulation open;
  * see jfa_bwd):
  *   fused: one kernel over key tiles forms dK, dV and each key tile's part of dQ, adding
  *     the parts into an fp32 accumulator in the workspace with reduce-adds at L2, and a
@@ -289,13 +293,19 @@ jfa_status jfa_bwd_static_scratch(jfa_plan plan, int32_t dtype, const void* Q, c
  *   two-pass: a second kernel over query tiles recomputes S and dP and accumulates dQ
  *     on chip, with no atomics: every result is the same bit for bit on every run, at
  *     1.4x the tensor-core work of the backward.
- * By default (enable = 0) the planner picks the faster form for the batch: fused when
- * the key tiles visit few query tiles on average (short sequences, where it saves the
- * second pass), two-pass otherwise (long sequences, where the reduce-adds cost more than
- * the recomputation).  enable = 1 always runs the two-pass form.  Shared key/value plans
+ *   short-query: when every query set fits one tile of 64 or 128 rows (64 at head_dim
+ *     64) and the plan has no causal mask, window or shared key/value, and the call has no
+ *     bias: one kernel per (sequence, head) keeps the query set on chip while the key
+ *     tiles stream past, and sums dQ in TMEM.  No atomics: the same bits on every run.
+ * By default (enable = 0) the planner picks the faster form for the batch: short-query
+ * where it applies; else fused when the key tiles visit few query tiles on average (short
+ * sequences, where it saves the second pass); two-pass otherwise (long sequences, where
+ * the reduce-adds cost more than the recomputation).  enable = 1 always runs the two-pass
+ * form.  Shared key/value plans
  * (unless their merged view is used), a dense bias and bias gradients always run the
  * two-pass form.  The choice changes jfa_bwd_workspace_size (the fused backward needs the
- * fp32 accumulator); query it after this call.  jfa_plan_info fact 19 reports the form.
+ * fp32 accumulator); query it after this call.  jfa_plan_info facts 19 and 20 report the
+ * form.
  * fp32 inputs are unaffected.
  * Errors: INVALID_ARG for a null plan or enable not 0 or 1.
  */
@@ -308,7 +318,8 @@ jfa_status jfa_plan_set_deterministic(jfa_plan plan, int32_t enable);
  * touches anything the item indexes.  It skips an item that fails and sets the status
  * that jfa_plan_device_status reports as JFA_ERR_DEVICE_BOUNDS.  The planner never writes
  * such an item; this call overwrites work item `index` of a pass (0 forward, 1 backward
- * dK/dV, 2 backward dQ; numbering as jfa_plan_info facts 7, 9, 12) in the plan's device
+ * dK/dV, 2 backward dQ, 3 the short-query backward; numbering as jfa_plan_info facts 7, 9,
+ * 12, and for pass 3 as jfa_worklist_build's pass 3 on the plan's offsets) in the plan's device
  * memory so that a test can plant one.  The lists are the plan's own (a shared key/value
  * plan's merged view keeps its lists).  Synchronises.  A plan holding a changed item gives
  * wrong results for that item's rows until it is destroyed.
@@ -325,12 +336,15 @@ jfa_status jfa_plan_device_status(jfa_plan plan, void* stream);
 /* Host-only planner, usable without a GPU (the same code jfa_plan_create runs).
  * pass 0 = forward (pairs of 128-row query tiles), 1 = backward dK/dV (key/value
  * tiles of 128 rows, visiting 128-row query tiles), 2 = backward dQ (128-row query
- * tiles).  jfa_worklist_size gives the number of work items; jfa_worklist_build
- * writes items as int32 quadruples (sequence, head, tile index, inner tiles
- * visited) grouped by CTA, cta_offsets[n_ctas+1] delimiting each CTA's items, and
- * optionally each CTA's total cost in units of tensor-core products.  window as in
- * jfa_plan_create_ex (-1: none).  With a window the inner tiles are a band: a
- * forward pair streams the union of its two query tiles' key ranges. */
+ * tiles), 3 = the short-query backward (one item (sequence, head, 0, key tiles) per
+ * sequence with a query or a key; causal must be 0 and window -1).  jfa_worklist_size
+ * gives the number of work items; jfa_worklist_build writes items as int32 quadruples
+ * (sequence, head, tile index, inner tiles visited) grouped by CTA, cta_offsets[n_ctas+1]
+ * delimiting each CTA's items, and optionally each CTA's total cost in units of
+ * tensor-core products.  window as in jfa_plan_create_ex (-1: none).  With a window the
+ * inner tiles are a band: a forward pair streams the union of its two query tiles' key
+ * ranges.  Errors: INVALID_ARG for bad offsets, H < 1, n_ctas < 1, an unknown pass, or
+ * pass 3 with a causal mask or a window. */
 jfa_status jfa_worklist_size(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
                              int32_t H, int32_t causal, int32_t window, int32_t pass, int64_t* n_items);
 jfa_status jfa_worklist_build(const int32_t* q_offsets, const int32_t* kv_offsets, int32_t B,
