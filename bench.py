@@ -411,7 +411,8 @@ def main():
     # dominant kernel: the largest share of device time among the tensor-core kernels
     per = {k: (v[0] / v[1] if v[1] else 0.0, v[1], v[0]) for k, v in kt.items()}
     kflop = kernel_flops(fl_f, fused or short_q)
-    kname_of = {"fwd": "jfa_fwd_kernel", "bwd_main": ("jfa_bwd_short_kernel" if short_q else
+    fwd_short = bf16 and info["fwd_short"] > 0 and batch.bias is None
+    kname_of = {"fwd": "jfa_fwd_short_kernel" if fwd_short else "jfa_fwd_kernel", "bwd_main": ("jfa_bwd_short_kernel" if short_q else
                                                       "jfa_bwd_fused_kernel" if fused else "jfa_bwd_dkdv_kernel")}
     if not (fused or short_q):
         kname_of["bwd_dq"] = "jfa_bwd_dq_kernel"

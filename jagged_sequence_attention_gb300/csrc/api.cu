@@ -269,7 +269,9 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
     if (p->short_bq > 0) {
         p->n_short_items = count_items(qo.data(), ko.data(), B, H, 0, kPassBwdShort);
         p->short_grid = int(std::max<int64_t>(
-            1, std::min<int64_t>(int64_t(p->num_sms) * short_ctas_per_sm(D, p->short_bq), p->n_short_items)));
+            1, std::min<int64_t>(int64_t(p->num_sms) * std::min(short_ctas_per_sm(D, p->short_bq),
+                                                                 short_fwd_ctas_per_sm(D, p->short_bq)),
+                                 p->n_short_items)));
         si.resize(size_t(std::max<int64_t>(1, p->n_short_items)));
         sio.resize(size_t(p->short_grid) + 1);
         build_worklist(qo.data(), ko.data(), B, H, 0, -1, kPassBwdShort, p->short_grid, si.data(), sio.data(), nullptr);
@@ -443,15 +445,16 @@ jfa_status jfa_plan_destroy(jfa_plan plan) {
 
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
     if (!plan || !info || n < 0) return JFA_ERR_INVALID_ARG;
-    const int64_t v[21] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
+    const int64_t v[22] = {plan->Tq,       plan->Tkv,     plan->B,           plan->H,        plan->D,
                            plan->mode,     plan->causal,  plan->n_fwd_items, plan->fwd_grid, plan->n_bwd_items,
                            plan->bwd_grid, plan->num_sms, plan->n_dq_items,  plan->dq_grid,  plan->window,
                            plan->n_pairs,  plan->shared_kv ? plan->U : -1,
                            plan->merged ? int64_t(plan->merged->B) : -1,
                            plan->fwd_split ? 1 : 0,
                            fused_backward(plan) ? 1 : 0,
-                           short_backward(plan, JFA_BIAS_NONE, false) ? plan->short_bq : 0};
-    for (int32_t i = 0; i < n && i < 21; ++i) info[i] = v[i];
+                           short_backward(plan, JFA_BIAS_NONE, false) ? plan->short_bq : 0,
+                           short_forward(plan, JFA_BIAS_NONE) ? plan->short_bq : 0};
+    for (int32_t i = 0; i < n && i < 22; ++i) info[i] = v[i];
     return JFA_OK;
 }
 
@@ -531,9 +534,13 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
         (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(bias_table) & 3u))
         return JFA_ERR_INVALID_ARG;
     if (plan->Tq == 0 || v->n_fwd_items == 0) return JFA_OK;
+    // bf16 GDPA without a bias, every query set in one tile: the transposed short-query
+    // forward over (sequence, head) items (fwd_short.cu)
+    const bool short_q = dtype == JFA_BF16 && short_forward(v, bias_kind);
     CUtensorMap mq, mk, mv;
     if (dtype == JFA_BF16 &&
-        ((s = make_map(&mq, dtype, Q, plan->Tq, plan->H, plan->D, plan->dev_block)) != JFA_OK ||
+        ((s = make_map(&mq, dtype, Q, plan->Tq, plan->H, plan->D, plan->dev_block, short_q ? v->short_bq : 128)) !=
+             JFA_OK ||
          (s = make_map(&mk, dtype, K, plan->Tkv, plan->H, plan->D, plan->dev_block)) != JFA_OK ||
          (s = make_map(&mv, dtype, V, plan->Tkv, plan->H, plan->D, plan->dev_block)) != JFA_OK))
         return s;
@@ -561,9 +568,17 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
     p.n_seq = v->B;
     p.n_kv = v->U;
     KernelTimer tm(plan, 0, static_cast<cudaStream_t>(stream));
-    cudaError_t e = dtype == JFA_BF16
-                        ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, v->fwd_grid, v->fwd_split, static_cast<cudaStream_t>(stream))
-                        : launch_fwd_f32(plan->D, Q, K, V, p, v->n_fwd_items, static_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (short_q) {
+        p.items = v->d_short_items;
+        p.cta_off = v->d_short_cta_off;
+        e = launch_fwd_short(o_dtype, plan->D, v->short_bq, mq, mk, mv, p, v->short_grid,
+                             static_cast<cudaStream_t>(stream));
+    } else {
+        e = dtype == JFA_BF16 ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, v->fwd_grid, v->fwd_split,
+                                           static_cast<cudaStream_t>(stream))
+                              : launch_fwd_f32(plan->D, Q, K, V, p, v->n_fwd_items, static_cast<cudaStream_t>(stream));
+    }
     tm.done();
     return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }

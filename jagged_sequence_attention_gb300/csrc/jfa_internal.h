@@ -238,6 +238,14 @@ __device__ inline bool short_item_ok(const int4 w, const BwdParams& p, int bq) {
     return w.w == (kv_len + kBwdBN - 1) / kBwdBN;
 }
 
+// Short-query GDPA forward: the same items, checked against the forward's parameters.
+__device__ inline bool short_fwd_item_ok(const int4 w, const FwdParams& p, int bq) {
+    if (w.x < 0 || w.x >= p.n_seq || w.x >= p.n_kv || w.y < 0 || w.y >= p.H || w.z != 0 || w.w < 0) return false;
+    const int q_len = p.q_off[w.x + 1] - p.q_off[w.x], kv_len = p.kv_off[w.x + 1] - p.kv_off[w.x];
+    if (q_len > bq) return false;
+    return w.w == (kv_len + kFwdBN - 1) / kFwdBN;
+}
+
 // Host planner (plan.cpp).  Returns JFA_OK or an error for bad offsets.
 jfa_status validate_offsets(const int32_t* q_off, const int32_t* kv_off, int32_t B);
 int64_t count_items(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t H,
@@ -283,6 +291,11 @@ cudaError_t launch_bwd_short(int D, int bq, const CUtensorMap& tmQ, const CUtens
                              const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st);
 // CTAs of that kernel an SM holds (2 at D = 64 with 64-row query tiles), 0 if unsupported.
 int short_ctas_per_sm(int D, int bq);
+// bf16 inputs, GDPA modes, short-query forward (fwd_short.cu): O over the same (sequence,
+// head) items and grid as launch_bwd_short, scores formed transposed (keys on the lanes).
+cudaError_t launch_fwd_short(int o_dtype, int D, int bq, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                             const CUtensorMap& tmV, const FwdParams& p, int grid, cudaStream_t st);
+int short_fwd_ctas_per_sm(int D, int bq);
 // Query-tile rows of the short-query backward for a plan (0: the form does not apply):
 // every query set fits one tile, no shared key/value, no causal mask, no window.
 int short_query_rows(const int32_t* q_off, int32_t B, int32_t D, int32_t causal, int32_t window, bool shared_kv);
@@ -357,6 +370,10 @@ struct jfa_plan_t {
 };
 
 namespace jfa {
+// Whether jfa_fwd on bf16 inputs with this bias runs the short-query GDPA forward.
+inline bool short_forward(const jfa_plan_t* plan, int32_t bias_kind) {
+    return plan->short_bq > 0 && plan->mode != JFA_SOFTMAX && bias_kind == JFA_BIAS_NONE;
+}
 // Whether jfa_bwd on bf16 inputs with this bias (and no bias gradient) runs the
 // short-query backward.
 inline bool short_backward(const jfa_plan_t* plan, int32_t bias_kind, bool dbias) {

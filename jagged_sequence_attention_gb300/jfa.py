@@ -201,7 +201,7 @@ def jfa_plan_destroy(plan: Plan):
 
 INFO_KEYS = ["T_q", "T_kv", "B", "H", "D", "mode", "causal", "fwd_items", "fwd_grid", "bwd_items", "bwd_grid",
              "num_sms", "dq_items", "dq_grid", "window", "pairs", "users", "merged",
-             "fwd_split", "bwd_fused", "bwd_short"]
+             "fwd_split", "bwd_fused", "bwd_short", "fwd_short"]
 
 
 def jfa_plan_info(plan: Plan) -> dict:

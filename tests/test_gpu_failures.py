@@ -43,7 +43,8 @@ def jfa():
 def _check_normal_call_is_right(b):
     g = parity.run_gpu(b)
     assert g["status"] == 0
-    parity.assert_within(parity.compare(g, parity.run_oracle(b)), softmax=b.mode == "softmax")
+    softmax = b.mode == "softmax"
+    parity.assert_within(parity.compare(g, parity.run_oracle(b), softmax=softmax), softmax=softmax)
 
 
 def _bad_item(kind, b, item):
@@ -129,6 +130,18 @@ def test_planted_item_in_the_short_query_backward(jfa, kind):
     seq = [b.B + 5, 0, 0, 1] if kind == "sequence" else [0, 0, 1, 3] if kind == "tile" else [0, 0, 0, 2]
     jfa.jfa_plan_set_work_item(plan, 3, 0, seq)
     jfa.jfa_bwd(plan, b.Q, b.K, b.V, O, b.dO, lse, None, b.scale)
+    torch.cuda.synchronize()
+    assert jfa.jfa_plan_device_status(plan) == jfa.JFA_ERR_DEVICE_BOUNDS
+    _check_normal_call_is_right(b)
+
+
+def test_planted_item_in_the_short_query_gdpa_forward(jfa):
+    b = wl.make_custom([40, 7, 64], [300, 129, 1000], H=2, D=64, mode="silu", causal=False, value_std=0.5,
+                       device="cuda", seed=545)
+    plan = jfa.plan_for(b)
+    assert jfa.jfa_plan_info(plan)["fwd_short"] == 64
+    jfa.jfa_plan_set_work_item(plan, 3, 0, [0, 0, 0, 5])  # an inner count the sequence does not have
+    jfa.jfa_fwd(plan, b.Q, b.K, b.V, None, b.scale, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert jfa.jfa_plan_device_status(plan) == jfa.JFA_ERR_DEVICE_BOUNDS
     _check_normal_call_is_right(b)
