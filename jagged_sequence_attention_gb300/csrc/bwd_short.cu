@@ -105,7 +105,9 @@ __device__ __forceinline__ uint32_t packed_col_nc(int s) {
     return uint32_t(NC * (s / (NC / 16)) + 8 * (s % (NC / 16)));
 }
 
-template <int D, int BQ, bool GDPA>
+// MODE: JFA_SOFTMAX, JFA_GDPA_GELU_TANH or JFA_GDPA_SILU (a template parameter, so that the
+// activation pass is straight-line code).
+template <int D, int BQ, int MODE>
 __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
     jfa_bwd_short_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -322,8 +324,8 @@ __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
         float* lse_s = misc_f + warp * 2 * NC;  // -lse (log2 units) per column
         float* del_s = lse_s + NC;              // -Delta per column
         const uint32_t stg = sbase + uint32_t(C::kOffStage + warp * 2048);
-        constexpr bool softmax = !GDPA;
-        const bool gelu = p.mode == JFA_GDPA_GELU_TANH;
+        constexpr bool GDPA = MODE != JFA_SOFTMAX, softmax = !GDPA;
+        constexpr bool gelu = MODE == JFA_GDPA_GELU_TANH;
         const float xs = softmax ? p.scale_log2 : p.scale;
         const size_t row_stride = size_t(p.H) * D;  // elements between consecutive token rows
         uint32_t kv_it = 0;
@@ -421,13 +423,12 @@ __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
 #pragma unroll
                             for (int c = 0; c < 32; c += 2) {
                                 const int cc = 32 * k + c;
-                                float a0, a1, d0, d1;
-                                gdpa_act_grad(gelu, pv[cc] * xs, a0, d0);
-                                gdpa_act_grad(gelu, pv[cc + 1] * xs, a1, d1);
+                                float2 a, d;
+                                gdpa_act_grad2<gelu>(make_float2(pv[cc], pv[cc + 1]), xs, a, d);
                                 const bool v0 = full || cc < hi, v1 = full || cc + 1 < hi;
-                                pk[c >> 1] = pack_bf16x2(v0 ? a0 : 0.f, v1 ? a1 : 0.f);
-                                pv[cc] = v0 ? d0 : 0.f;
-                                pv[cc + 1] = v1 ? d1 : 0.f;
+                                pk[c >> 1] = pack_bf16x2(v0 ? a.x : 0.f, v1 ? a.y : 0.f);
+                                pv[cc] = v0 ? d.x : 0.f;
+                                pv[cc + 1] = v1 ? d.y : 0.f;
                             }
                         }
                     }
@@ -536,18 +537,18 @@ __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
     if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmCols);
 }
 
-template <int D, int BQ, bool GDPA>
+template <int D, int BQ, int MODE>
 cudaError_t launch_short_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
     using C = ShCfg<D, BQ>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(jfa_bwd_short_kernel<D, BQ, GDPA>,
+        cudaError_t e = cudaFuncSetAttribute(jfa_bwd_short_kernel<D, BQ, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_short_kernel<D, BQ, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
+    jfa_bwd_short_kernel<D, BQ, MODE><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
     return cudaGetLastError();
 }
 
@@ -560,18 +561,20 @@ int short_ctas_per_sm(int D, int bq) {
     return 0;
 }
 
+template <int D, int BQ>
+static cudaError_t launch_short_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                  const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
+    if (p.mode == JFA_SOFTMAX) return launch_short_t<D, BQ, JFA_SOFTMAX>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    if (p.mode == JFA_GDPA_GELU_TANH)
+        return launch_short_t<D, BQ, JFA_GDPA_GELU_TANH>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    return launch_short_t<D, BQ, JFA_GDPA_SILU>(tmQ, tmK, tmV, tmdO, p, grid, st);
+}
+
 cudaError_t launch_bwd_short(int D, int bq, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
-    const bool sm = p.mode == JFA_SOFTMAX;
-    if (D == 64 && bq == 64)
-        return sm ? launch_short_t<64, 64, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                  : launch_short_t<64, 64, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
-    if (D == 64 && bq == 128)
-        return sm ? launch_short_t<64, 128, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                  : launch_short_t<64, 128, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
-    if (D == 128 && bq == 128)
-        return sm ? launch_short_t<128, 128, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                  : launch_short_t<128, 128, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    if (D == 64 && bq == 64) return launch_short_m<64, 64>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    if (D == 64 && bq == 128) return launch_short_m<64, 128>(tmQ, tmK, tmV, tmdO, p, grid, st);
+    if (D == 128 && bq == 128) return launch_short_m<128, 128>(tmQ, tmK, tmV, tmdO, p, grid, st);
     return cudaErrorInvalidValue;
 }
 

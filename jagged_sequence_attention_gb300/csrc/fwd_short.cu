@@ -93,7 +93,9 @@ enum {
     FS_DRAIN = 18,
 };
 
-template <int D, int BQ, typename OT>
+// GELU: the activation is tanh-GELU, else SiLU (a template parameter, so that the activation
+// pass is straight-line code).
+template <int D, int BQ, typename OT, bool GELU>
 __global__ void __launch_bounds__(FsCfg<D, BQ>::kThreads, FsCfg<D, BQ>::kCtasPerSm)
     jfa_fwd_short_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -279,7 +281,6 @@ __global__ void __launch_bounds__(FsCfg<D, BQ>::kThreads, FsCfg<D, BQ>::kCtasPer
         const int r = quarter * 32 + lane;  // key row of a tile; head-dim row in the epilogue
         const int c0 = wg * NC;
         const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-        const bool gelu = p.mode == JFA_GDPA_GELU_TANH;
         const size_t row_stride = size_t(p.H) * D;
         uint32_t kv_it = 0, item_it = 0;
         bool ok = true;
@@ -330,11 +331,13 @@ __global__ void __launch_bounds__(FsCfg<D, BQ>::kThreads, FsCfg<D, BQ>::kCtasPer
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
                         const int cc = 32 * k + c;
-                        const float a0 = full || cc < hi ? gdpa_act(gelu, sv[c] * p.scale) : 0.f;
-                        const float a1 = full || cc + 1 < hi ? gdpa_act(gelu, sv[c + 1] * p.scale) : 0.f;
-                        const uint32_t u = pack_bf16x2(a0, a1);
+                        float2 a = gdpa_act2<GELU>(make_float2(sv[c], sv[c + 1]), p.scale);
+                        if (!full) a = make_float2(cc < hi ? a.x : 0.f, cc + 1 < hi ? a.y : 0.f);
+                        const uint32_t u = pack_bf16x2(a.x, a.y);
                         pk[k][c >> 1] = u;
-                        pl[k][c >> 1] = pack_bf16x2(a0 - __uint_as_float(u << 16), a1 - __uint_as_float(u & 0xffff0000u));
+                        const float2 rem =
+                            add2(a, make_float2(-__uint_as_float(u << 16), -__uint_as_float(u & 0xffff0000u)));
+                        pl[k][c >> 1] = pack_bf16x2(rem.x, rem.y);
                     }
                 }
                 // the S^T buffer is read: the tile after next may score into it
@@ -392,19 +395,26 @@ __global__ void __launch_bounds__(FsCfg<D, BQ>::kThreads, FsCfg<D, BQ>::kCtasPer
     if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmCols);
 }
 
-template <int D, int BQ, typename OT>
-cudaError_t launch_fs_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
+template <int D, int BQ, typename OT, bool GELU>
+cudaError_t launch_fs_a(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
                         int grid, cudaStream_t st) {
     using C = FsCfg<D, BQ>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(jfa_fwd_short_kernel<D, BQ, OT>,
+        cudaError_t e = cudaFuncSetAttribute(jfa_fwd_short_kernel<D, BQ, OT, GELU>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_fwd_short_kernel<D, BQ, OT><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, p);
+    jfa_fwd_short_kernel<D, BQ, OT, GELU><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
+}
+
+template <int D, int BQ, typename OT>
+cudaError_t launch_fs_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
+                        int grid, cudaStream_t st) {
+    return p.mode == JFA_GDPA_GELU_TANH ? launch_fs_a<D, BQ, OT, true>(tmQ, tmK, tmV, p, grid, st)
+                                        : launch_fs_a<D, BQ, OT, false>(tmQ, tmK, tmV, p, grid, st);
 }
 
 template <typename OT>

@@ -52,6 +52,49 @@ __device__ __forceinline__ float gdpa_act(bool gelu, float x) {
     return x * sigmoid_acc(x);
 }
 
+// gdpa_act on two elements (s0, s1) of the raw score, x = scale * s, with the products and
+// sums on the paired fp32 pipe (one instruction per pair); the exponents and reciprocals
+// stay per element.
+template <bool GELU>
+__device__ __forceinline__ float2 gdpa_act2(float2 s, float scale) {
+    const float2 x = mul2(s, make_float2(scale, scale));
+    float2 z;
+    if (GELU) {
+        const float2 t = fma2(mul2(x, x), make_float2(-0.10294324f, -0.10294324f), make_float2(-2.3022082f, -2.3022082f));
+        z = mul2(x, t);  // gelu_sigmoid_arg of each element
+    } else {
+        z = mul2(x, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+    }
+    const float2 d = add2(make_float2(ex2_approx(z.x), ex2_approx(z.y)), make_float2(1.f, 1.f));
+    return mul2(x, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
+// gdpa_act_grad on two elements of the raw score (x = scale * s), paired as gdpa_act2.
+template <bool GELU>
+__device__ __forceinline__ void gdpa_act_grad2(float2 s, float scale, float2& a, float2& da) {
+    const float2 x = mul2(s, make_float2(scale, scale));
+    if (GELU) {
+        const float2 x2 = mul2(x, x);
+        const float2 z = mul2(x, fma2(x2, make_float2(-0.10294324f, -0.10294324f), make_float2(-2.3022082f, -2.3022082f)));
+        const float2 d = add2(make_float2(ex2_approx(z.x), ex2_approx(z.y)), make_float2(1.f, 1.f));
+        const float2 sg = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+        a = mul2(x, sg);
+        // gelu' = s + 2 a (1 - s) (k0 + 3 k1 x^2)
+        const float2 oms = add2(make_float2(1.f, 1.f), make_float2(-sg.x, -sg.y));
+        const float2 poly = fma2(x2, make_float2(3.f * 0.035677408136300125f, 3.f * 0.035677408136300125f),
+                                 make_float2(0.7978845608028654f, 0.7978845608028654f));
+        da = fma2(mul2(add2(a, a), oms), poly, sg);
+    } else {
+        const float2 z = mul2(x, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+        const float2 d = add2(make_float2(ex2_approx(z.x), ex2_approx(z.y)), make_float2(1.f, 1.f));
+        const float2 sg = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+        a = mul2(x, sg);
+        // silu' = s (1 + x (1 - s))
+        const float2 oms = add2(make_float2(1.f, 1.f), make_float2(-sg.x, -sg.y));
+        da = mul2(sg, fma2(x, oms, make_float2(1.f, 1.f)));
+    }
+}
+
 __device__ __forceinline__ void gdpa_act_grad(bool gelu, float x, float& a, float& da) {
     if (gelu) {
         const float k0 = 0.7978845608028654f, k1 = 0.035677408136300125f;
