@@ -68,15 +68,18 @@ def algorithmic_bytes(batch, elem=2, fused=False):
     short-query) reads Q, dO, K, V and writes dK, dV and dQ (the fused form's fp32 dQ
     accumulator is implementation traffic, not algorithmic)."""
     Tq, Tkv, H, D = int(batch.q_off[-1]), int(batch.kv_off[-1]), batch.H, batch.D
+    # softmax row terms: the forward writes lse, the backward reads lse and Delta (GDPA has none)
+    sm = batch.mode == "softmax"
+    lse_b, rows_b = (4 * H * Tq, 8 * H * Tq) if sm else (0, 0)
     if fused:
         return {
-            "fwd": elem * H * D * (2 * Tq + 2 * Tkv) + 4 * H * Tq,         # Q,K,V -> O; lse
-            "bwd_main": elem * H * D * (3 * Tq + 4 * Tkv) + 8 * H * Tq,    # Q,dO,K,V -> dQ,dK,dV; lse,Delta
+            "fwd": elem * H * D * (2 * Tq + 2 * Tkv) + lse_b,          # Q,K,V -> O; lse
+            "bwd_main": elem * H * D * (3 * Tq + 4 * Tkv) + rows_b,    # Q,dO,K,V -> dQ,dK,dV; lse,Delta
         }
     return {
-        "fwd": elem * H * D * (2 * Tq + 2 * Tkv) + 4 * H * Tq,             # Q,K,V -> O; lse
-        "bwd_main": elem * H * D * (2 * Tq + 4 * Tkv) + 8 * H * Tq,        # Q,dO,K,V -> dK,dV; lse,Delta
-        "bwd_dq": elem * H * D * (3 * Tq + 2 * Tkv) + 8 * H * Tq,          # Q,dO,K,V -> dQ; lse,Delta
+        "fwd": elem * H * D * (2 * Tq + 2 * Tkv) + lse_b,              # Q,K,V -> O; lse
+        "bwd_main": elem * H * D * (2 * Tq + 4 * Tkv) + rows_b,        # Q,dO,K,V -> dK,dV; lse,Delta
+        "bwd_dq": elem * H * D * (3 * Tq + 2 * Tkv) + rows_b,          # Q,dO,K,V -> dQ; lse,Delta
     }
 
 

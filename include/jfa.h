@@ -169,7 +169,11 @@ jfa_status jfa_plan_destroy(jfa_plan plan);
  * 128) of the short-query backward when jfa_bwd on JFA_BF16 inputs without a bias runs
  * it for this plan, else 0: one kernel per (sequence, head) for batches whose query sets
  * all fit one tile, with no causal mask, window or shared key/value (it then takes the
- * place of the fused form for calls without a bias).  n may be smaller than 21.
+ * place of the fused form for calls without a bias).  Fact 21 is the same query-tile rows
+ * when jfa_fwd on JFA_BF16 inputs without a bias runs the short-query GDPA forward for this
+ * plan (GDPA modes only), else 0: the scores formed transposed, with the keys on the
+ * tensor-core accumulator's lanes, so that short query sets leave none of them on padding
+ * rows.  n may be smaller than 22.
  */
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
 
