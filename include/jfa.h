@@ -181,7 +181,9 @@ jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
  * Forward pass.
  *   Q [T_q,H,D], K, V [T_kv,H,D] (dtype); bias_table fp32 [H,32] when bias_kind is
  *   JFA_BIAS_RELPOS32, the dense bias fp32 [H,P] when it is JFA_BIAS_DENSE (see
- *   jfa_bias_kind), else ignored; scale multiplies <q,k> (typically 1/sqrt(D)).
+ *   jfa_bias_kind), else ignored; scale multiplies <q,k> (typically 1/sqrt(D)); in
+ *   SOFTMAX mode it must be finite and positive (the kernels bound each row's maximum by
+ *   scale times the row's largest raw score), else INVALID_ARG.
  *   O [T_q,H,D] is written for every row covered by the offsets, in o_dtype:
  *   JFA_F32 (the fp32 accumulator, no output rounding) or JFA_BF16 (rounded to
  *   nearest even); with dtype JFA_F32, o_dtype must be JFA_F32.

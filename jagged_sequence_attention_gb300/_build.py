@@ -22,7 +22,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libjfa.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "plan.cpp", "fwd.cu", "fwd_short.cu", "bwd.cu", "bwd_dq.cu", "bwd_fused.cu", "bwd_short.cu", "f32.cu", "static_scratch.cu"]
+SOURCES = ["api.cu", "plan.cpp", "fwd.cu", "fwd_short.cu", "fwd_pack.cu", "bwd.cu", "bwd_dq.cu", "bwd_fused.cu", "bwd_short.cu", "f32.cu", "static_scratch.cu"]
 
 
 def _nvcc() -> str:

@@ -264,17 +264,25 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
     }
     // Short-query backward: one (sequence, head) item per query set, when each fits one tile.
     p->short_bq = short_query_rows(qo.data(), B, D, causal, window, kv_map != nullptr);
-    std::vector<WorkItem> si(1);
-    std::vector<int32_t> sio(2, 0);
+    // The forward's kernel holds a different number of CTAs per SM (one for the softmax
+    // kernel with two key tiles per score tile), so it has its own grouping of the items.
+    std::vector<WorkItem> si(1), sfi(1);
+    std::vector<int32_t> sio(2, 0), sfo(2, 0);
     if (p->short_bq > 0) {
         p->n_short_items = count_items(qo.data(), ko.data(), B, H, 0, kPassBwdShort);
-        p->short_grid = int(std::max<int64_t>(
-            1, std::min<int64_t>(int64_t(p->num_sms) * std::min(short_ctas_per_sm(D, p->short_bq),
-                                                                 short_fwd_ctas_per_sm(D, p->short_bq)),
-                                 p->n_short_items)));
+        auto grid_of = [&](int per_sm) {
+            return int(std::max<int64_t>(1, std::min<int64_t>(int64_t(p->num_sms) * per_sm, p->n_short_items)));
+        };
+        p->short_grid = grid_of(short_ctas_per_sm(D, p->short_bq));
+        const bool pack = mode == JFA_SOFTMAX;  // (applies at D = 64 with 64-row tiles only)
+        p->short_fwd_grid = grid_of(pack ? 1 : short_fwd_ctas_per_sm(D, p->short_bq));
         si.resize(size_t(std::max<int64_t>(1, p->n_short_items)));
+        sfi.resize(si.size());
         sio.resize(size_t(p->short_grid) + 1);
+        sfo.resize(size_t(p->short_fwd_grid) + 1);
         build_worklist(qo.data(), ko.data(), B, H, 0, -1, kPassBwdShort, p->short_grid, si.data(), sio.data(), nullptr);
+        build_worklist(qo.data(), ko.data(), B, H, 0, -1, kPassBwdShort, p->short_fwd_grid, sfi.data(), sfo.data(),
+                       nullptr);
     }
     std::vector<int64_t> po(size_t(B) + 1, 0);  // pair offsets of a dense bias
     for (int32_t b = 0; b < B; ++b)
@@ -304,6 +312,8 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
     const size_t o_ko = cur; cur += round_up(ktile_off.size() * 4, 256);
     const size_t o_si = cur; cur += round_up(si.size() * 16, 256);
     const size_t o_sio = cur; cur += round_up(sio.size() * 4, 256);
+    const size_t o_sfi = cur; cur += round_up(sfi.size() * 16, 256);
+    const size_t o_sfo = cur; cur += round_up(sfo.size() * 4, 256);
     if (cudaMalloc(&p->dev_block, cur) != cudaSuccess) {
         delete p;
         return JFA_ERR_CUDA;
@@ -325,6 +335,8 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
     p->d_ktile_off = kv_map ? reinterpret_cast<int32_t*>(base + o_ko) : nullptr;
     p->d_short_items = reinterpret_cast<int4*>(base + o_si);
     p->d_short_cta_off = reinterpret_cast<int32_t*>(base + o_sio);
+    p->d_sfwd_items = reinterpret_cast<int4*>(base + o_sfi);
+    p->d_sfwd_cta_off = reinterpret_cast<int32_t*>(base + o_sfo);
     auto up = [&](void* dst, const void* src, size_t bytes) {
         return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st) == cudaSuccess;
     };
@@ -336,7 +348,8 @@ static jfa_status plan_create_impl(const std::vector<int32_t>& qo, const std::ve
               up(p->d_pair_off, po.data(), po.size() * 8) && up(base + o_map, map_h.data(), map_h.size() * 4) &&
               up(base + o_sp, steps.data(), steps.size() * 8) && up(base + o_so, step_off.data(), step_off.size() * 4) &&
               up(base + o_ko, ktile_off.data(), ktile_off.size() * 4) &&
-              up(base + o_si, si.data(), si.size() * 16) && up(base + o_sio, sio.data(), sio.size() * 4);
+              up(base + o_si, si.data(), si.size() * 16) && up(base + o_sio, sio.data(), sio.size() * 4) &&
+              up(base + o_sfi, sfi.data(), sfi.size() * 16) && up(base + o_sfo, sfo.data(), sfo.size() * 4);
     // The host vectors are pageable: the copies above are staged before returning,
     // but keep the stream ordered before the vectors go out of scope.
     if (!ok || cudaStreamSynchronize(st) != cudaSuccess) {
@@ -459,16 +472,18 @@ jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n) {
 }
 
 jfa_status jfa_plan_set_work_item(jfa_plan plan, int32_t pass, int64_t index, const int32_t* item) {
-    if (!plan || !item || pass < kPassFwd || pass > kPassBwdShort || index < 0) return JFA_ERR_INVALID_ARG;
+    // pass 4: the short-query forward's list (pass 3's items, grouped for its grid)
+    if (!plan || !item || pass < kPassFwd || pass > kPassBwdShort + 1 || index < 0) return JFA_ERR_INVALID_ARG;
     const int64_t n = pass == kPassFwd     ? plan->n_fwd_items
                       : pass == kPassBwdKV ? plan->n_bwd_items
                       : pass == kPassBwdQ  ? plan->n_dq_items
                                            : plan->n_short_items;
     if (index >= n) return JFA_ERR_INVALID_ARG;
-    int4* list = pass == kPassFwd     ? plan->d_fwd_items
-                 : pass == kPassBwdKV ? plan->d_bwd_items
-                 : pass == kPassBwdQ  ? plan->d_dq_items
-                                      : plan->d_short_items;
+    int4* list = pass == kPassFwd         ? plan->d_fwd_items
+                 : pass == kPassBwdKV     ? plan->d_bwd_items
+                 : pass == kPassBwdQ      ? plan->d_dq_items
+                 : pass == kPassBwdShort  ? plan->d_short_items
+                                          : plan->d_sfwd_items;
     const int4 w = make_int4(item[0], item[1], item[2], item[3]);
     return cudaMemcpy(list + index, &w, sizeof(w), cudaMemcpyHostToDevice) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
@@ -530,6 +545,8 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
     const bool softmax = plan->mode == JFA_SOFTMAX;
     if (plan->Tq > 0 && (!Q || !O || (softmax && !lse))) return JFA_ERR_INVALID_ARG;
     if (plan->Tkv > 0 && (!K || !V)) return JFA_ERR_INVALID_ARG;
+    // softmax: each row's maximum is bounded by scale times its largest raw score
+    if (softmax && !(scale > 0.f && scale < INFINITY)) return JFA_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(bias_table) & 3u))
         return JFA_ERR_INVALID_ARG;
@@ -570,10 +587,11 @@ jfa_status jfa_fwd(jfa_plan plan, int32_t dtype, const void* Q, const void* K, c
     KernelTimer tm(plan, 0, static_cast<cudaStream_t>(stream));
     cudaError_t e;
     if (short_q) {
-        p.items = v->d_short_items;
-        p.cta_off = v->d_short_cta_off;
-        e = launch_fwd_short(o_dtype, plan->D, v->short_bq, mq, mk, mv, p, v->short_grid,
-                             static_cast<cudaStream_t>(stream));
+        p.items = v->d_sfwd_items;
+        p.cta_off = v->d_sfwd_cta_off;
+        e = softmax ? launch_fwd_pack(o_dtype, mq, mk, mv, p, v->short_fwd_grid, static_cast<cudaStream_t>(stream))
+                    : launch_fwd_short(o_dtype, plan->D, v->short_bq, mq, mk, mv, p, v->short_fwd_grid,
+                                       static_cast<cudaStream_t>(stream));
     } else {
         e = dtype == JFA_BF16 ? launch_fwd(dtype, o_dtype, plan->D, mq, mk, mv, p, v->fwd_grid, v->fwd_split,
                                            static_cast<cudaStream_t>(stream))

@@ -296,6 +296,10 @@ int short_ctas_per_sm(int D, int bq);
 cudaError_t launch_fwd_short(int o_dtype, int D, int bq, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                              const CUtensorMap& tmV, const FwdParams& p, int grid, cudaStream_t st);
 int short_fwd_ctas_per_sm(int D, int bq);
+// bf16 inputs, softmax, head_dim 64, query sets of at most 64 rows (fwd_pack.cu): the
+// short-query forward with two key tiles per score tile, one CTA per SM.
+cudaError_t launch_fwd_pack(int o_dtype, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                            const FwdParams& p, int grid, cudaStream_t st);
 // Query-tile rows of the short-query backward for a plan (0: the form does not apply):
 // every query set fits one tile, no shared key/value, no causal mask, no window.
 int short_query_rows(const int32_t* q_off, int32_t B, int32_t D, int32_t causal, int32_t window, bool shared_kv);
@@ -363,6 +367,10 @@ struct jfa_plan_t {
     int short_grid = 1;
     int4* d_short_items = nullptr;
     int32_t* d_short_cta_off = nullptr;
+    // the short-query forward's list: the same items, grouped for its own grid
+    int short_fwd_grid = 1;
+    int4* d_sfwd_items = nullptr;
+    int32_t* d_sfwd_cta_off = nullptr;
     // optional per-kernel timing (jfa_plan_set_timing)
     bool timing;
     std::vector<cudaEvent_t> ev_pool;                 // reusable events
@@ -370,9 +378,12 @@ struct jfa_plan_t {
 };
 
 namespace jfa {
-// Whether jfa_fwd on bf16 inputs with this bias runs the short-query GDPA forward.
+// Whether jfa_fwd on bf16 inputs with this bias runs a short-query forward: the transposed
+// GDPA kernel, or for softmax at head_dim 64 with query sets of at most 64 rows the kernel
+// with two key tiles per score tile.
 inline bool short_forward(const jfa_plan_t* plan, int32_t bias_kind) {
-    return plan->short_bq > 0 && plan->mode != JFA_SOFTMAX && bias_kind == JFA_BIAS_NONE;
+    return plan->short_bq > 0 && bias_kind == JFA_BIAS_NONE &&
+           (plan->mode != JFA_SOFTMAX || (plan->D == 64 && plan->short_bq == 64));
 }
 // Whether jfa_bwd on bf16 inputs with this bias (and no bias gradient) runs the
 // short-query backward.

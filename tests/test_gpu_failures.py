@@ -140,7 +140,20 @@ def test_planted_item_in_the_short_query_gdpa_forward(jfa):
                        device="cuda", seed=545)
     plan = jfa.plan_for(b)
     assert jfa.jfa_plan_info(plan)["fwd_short"] == 64
-    jfa.jfa_plan_set_work_item(plan, 3, 0, [0, 0, 0, 5])  # an inner count the sequence does not have
+    jfa.jfa_plan_set_work_item(plan, 4, 0, [0, 0, 0, 5])  # an inner count the sequence does not have
+    jfa.jfa_fwd(plan, b.Q, b.K, b.V, None, b.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert jfa.jfa_plan_device_status(plan) == jfa.JFA_ERR_DEVICE_BOUNDS
+    _check_normal_call_is_right(b)
+
+
+@pytest.mark.parametrize("kind", ["sequence", "count"])
+def test_planted_item_in_the_packed_softmax_forward(jfa, kind):
+    b = wl.make_custom([40, 7, 64], [300, 129, 1000], H=2, D=64, causal=False, device="cuda", seed=546)
+    plan = jfa.plan_for(b)
+    assert jfa.jfa_plan_info(plan)["fwd_short"] == 64
+    item = [b.B + 1, 0, 0, 3] if kind == "sequence" else [2, 1, 0, 2]  # sequence 2 has 8 key tiles
+    jfa.jfa_plan_set_work_item(plan, 4, 0, item)
     jfa.jfa_fwd(plan, b.Q, b.K, b.V, None, b.scale, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert jfa.jfa_plan_device_status(plan) == jfa.JFA_ERR_DEVICE_BOUNDS
@@ -164,7 +177,7 @@ def test_planted_item_on_a_shared_key_value_plan(jfa):
 def test_set_work_item_argument_errors(jfa):
     b = wl.make_custom([40], [40], H=1, D=128, device="cuda", seed=521)
     plan = jfa.plan_for(b)
-    for pass_, index in ((4, 0), (-1, 0), (0, -1), (0, 10**6), (3, 10**6)):
+    for pass_, index in ((5, 0), (-1, 0), (0, -1), (0, 10**6), (3, 10**6), (4, 10**6)):
         with pytest.raises(jfa.JFAError) as e:
             jfa.jfa_plan_set_work_item(plan, pass_, index, [0, 0, 0, 1])
         assert e.value.status == jfa.JFA_ERR_INVALID_ARG
