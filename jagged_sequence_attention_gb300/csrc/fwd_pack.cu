@@ -283,25 +283,38 @@ __global__ void __launch_bounds__(FpCfg::kThreads, 1)
                 const uint32_t tS = tmem + lane_base + C::kTmS + st * 128u;
                 // valid keys of this lane's tile 2u + half: [0, hi)
                 const int hi = row_ok ? min(C::BN, max(0, kv_len - (2 * u + half) * C::BN)) : 0;
-                const bool full = __all_sync(0xffffffffu, hi == C::BN);
+                // Masking is per lane where each lane's tile is wholly valid or wholly masked
+                // (a query row past the set's end, a tile past the sequence's end): such a lane
+                // gets m = -inf and an exponent argument of -inf, so P = 0 with no per-element
+                // select.  Only a sequence's last, partial key tile is masked per element, and a
+                // warp with no valid key at all only writes zeros.
+                const bool partial = __any_sync(0xffffffffu, hi > 0 && hi < C::BN);
+                const bool none = __all_sync(0xffffffffu, hi == 0);
                 if (!warp_wait(FP_S_FULL + st, (g >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 // pass 1: the tile's row maximum
                 float mx = -INFINITY;
+                if (!none) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t v[32];
-                    tmem_ld32(tS + 32u * k, v);
-                    tmem_ld_wait(v);
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t v[32];
+                        tmem_ld32(tS + 32u * k, v);
+                        tmem_ld_wait(v);
+                        if (partial) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const int cc = 32 * k + c;
-                        const float a = (full || cc < hi) ? __uint_as_float(v[c]) : -INFINITY;
-                        const float a1 = (full || cc + 1 < hi) ? __uint_as_float(v[c + 1]) : -INFINITY;
-                        mx = fmax3(mx, a, a1);
+                            for (int c = 0; c < 32; c += 2) {
+                                const int cc = 32 * k + c;
+                                const float a = cc < hi ? __uint_as_float(v[c]) : -INFINITY;
+                                const float a1 = cc + 1 < hi ? __uint_as_float(v[c + 1]) : -INFINITY;
+                                mx = fmax3(mx, a, a1);
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 32; c += 2) mx = fmax3(mx, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+                        }
                     }
                 }
-                const float m_tile = mx * xs;
+                const float m_tile = hi > 0 ? mx * xs : -INFINITY;
                 // P' may be rewritten, and O is stable, once the previous product is done
                 if (g > 0 && !warp_wait(FP_P_FREE, (g - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
@@ -325,33 +338,41 @@ __global__ void __launch_bounds__(FpCfg::kThreads, 1)
                 }
                 if (grow) m_use = m_tile;
                 // pass 2: P = 2^(x s - m) over the lane's key tile, into its half of P'; zeros
-                // into the other half
-                const float2 nm = make_float2(-m_use, -m_use), xs2 = make_float2(xs, xs);
+                // into the other half (and into both for a warp with no valid key)
+                const float nmv = hi > 0 ? -m_use : -INFINITY;
+                const float2 nm = make_float2(nmv, nmv), xs2 = make_float2(xs, xs);
                 float2 sum2 = make_float2(0.f, 0.f);
+                uint32_t z[16];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t v[32];
-                    tmem_ld32(tS + 32u * k, v);
-                    tmem_ld_wait(v);
-                    uint32_t pk[16];
+                for (int c = 0; c < 16; ++c) z[c] = 0u;
+                if (!none) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const int cc = 32 * k + c;
-                        const float2 e = fma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), xs2, nm);
-                        const float p0 = (full || cc < hi) ? ex2_approx(e.x) : 0.f;
-                        const float p1 = (full || cc + 1 < hi) ? ex2_approx(e.y) : 0.f;
-                        sum2 = add2(sum2, make_float2(p0, p1));
-                        pk[c >> 1] = pack_bf16x2(p0, p1);
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t v[32];
+                        tmem_ld32(tS + 32u * k, v);
+                        tmem_ld_wait(v);
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const float2 e =
+                                fma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), xs2, nm);
+                            float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
+                            if (partial) {
+                                const int cc = 32 * k + c;
+                                p0 = cc < hi ? p0 : 0.f;
+                                p1 = cc + 1 < hi ? p1 : 0.f;
+                            }
+                            sum2 = add2(sum2, make_float2(p0, p1));
+                            pk[c >> 1] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(tP + uint32_t(64 * half + 16 * k), pk);
                     }
-                    tmem_st16(tP + uint32_t(64 * half + 16 * k), pk);
-                }
-                {
-                    uint32_t z[16];
+                } else {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) z[c] = 0u;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) tmem_st16(tP + uint32_t(64 * (1 - half) + 16 * k), z);
+                    for (int k = 0; k < 4; ++k) tmem_st16(tP + uint32_t(64 * half + 16 * k), z);
                 }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tmem_st16(tP + uint32_t(64 * (1 - half) + 16 * k), z);
                 l += sum2.x + sum2.y;
                 tmem_st_wait();
                 tc_fence_before();
