@@ -170,10 +170,11 @@ jfa_status jfa_plan_destroy(jfa_plan plan);
  * it for this plan, else 0: one kernel per (sequence, head) for batches whose query sets
  * all fit one tile, with no causal mask, window or shared key/value (it then takes the
  * place of the fused form for calls without a bias).  Fact 21 is the same query-tile rows
- * when jfa_fwd on JFA_BF16 inputs without a bias runs the short-query GDPA forward for this
- * plan (GDPA modes only), else 0: the scores formed transposed, with the keys on the
- * tensor-core accumulator's lanes, so that short query sets leave none of them on padding
- * rows.  n may be smaller than 22.
+ * when jfa_fwd on JFA_BF16 inputs without a bias runs a short-query forward for this plan,
+ * else 0: in GDPA modes the scores formed transposed, with the keys on the tensor-core
+ * accumulator's lanes; in SOFTMAX mode (head_dim 64, query sets of at most 64 rows) two key
+ * tiles per score tile, one per half of the lanes.  Either way short query sets leave no
+ * lane on padding rows.  n may be smaller than 22.
  */
 jfa_status jfa_plan_info(jfa_plan plan, int64_t* info, int32_t n);
 
@@ -324,8 +325,9 @@ jfa_status jfa_plan_set_deterministic(jfa_plan plan, int32_t enable);
  * touches anything the item indexes.  It skips an item that fails and sets the status
  * that jfa_plan_device_status reports as JFA_ERR_DEVICE_BOUNDS.  The planner never writes
  * such an item; this call overwrites work item `index` of a pass (0 forward, 1 backward
- * dK/dV, 2 backward dQ, 3 the short-query backward; numbering as jfa_plan_info facts 7, 9,
- * 12, and for pass 3 as jfa_worklist_build's pass 3 on the plan's offsets) in the plan's device
+ * dK/dV, 2 backward dQ, 3 the short-query backward, 4 the short-query forward; numbering as
+ * jfa_plan_info facts 7, 9, 12, and for passes 3 and 4 as jfa_worklist_build's pass 3 on the
+ * plan's offsets, grouped for each kernel's own grid) in the plan's device
  * memory so that a test can plant one.  The lists are the plan's own (a shared key/value
  * plan's merged view keeps its lists).  Synchronises.  A plan holding a changed item gives
  * wrong results for that item's rows until it is destroyed.
