@@ -104,10 +104,21 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def kernel_digest():
+# The source file of each tensor-core kernel; its digest also covers the shared headers.
+KERNEL_SOURCE = {
+    "jfa_fwd_kernel": "fwd.cu", "jfa_fwd_short_kernel": "fwd_short.cu", "jfa_fwd_pack_kernel": "fwd_pack.cu",
+    "jfa_bwd_dkdv_kernel": "bwd.cu", "jfa_bwd_dq_kernel": "bwd_dq.cu", "jfa_bwd_fused_kernel": "bwd_fused.cu",
+    "jfa_bwd_short_kernel": "bwd_short.cu",
+}
+
+
+def kernel_digest(kernel):
+    """Digest of the sources a kernel is built from: its own .cu file and every header in
+    csrc (a measurement stays valid while these are unchanged)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "jagged_sequence_attention_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = [KERNEL_SOURCE[kernel]] + sorted(n for n in os.listdir(csrc) if n.endswith((".h", ".cuh")))
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -122,7 +133,7 @@ def measured_traffic(kernel, workload):
     with open(p) as f:
         d = json.load(f)
     e = d.get(f"{kernel}/{workload}")
-    if not e or e.get("kernel_digest") != kernel_digest():
+    if not e or kernel not in KERNEL_SOURCE or e.get("kernel_digest") != kernel_digest(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
