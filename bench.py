@@ -358,9 +358,18 @@ def main():
     bf16 = batch.Q.dtype == torch.bfloat16
     short_q = bf16 and info["bwd_short"] > 0 and batch.bias is None
     fused = bf16 and not short_q and info["bwd_fused"] == 1
-    kbytes = algorithmic_bytes(batch, fused=fused or short_q)
-    cfg["backward"] = ("short-query dQ/dK/dV kernel" if short_q else
+    # one backward kernel forms dQ, dK and dV: short-query, fused, and the fp32 path
+    one_kernel_bwd = fused or short_q or not bf16
+    kbytes = algorithmic_bytes(batch, elem=2 if bf16 else 4, fused=one_kernel_bwd)
+    cfg["backward"] = ("fp32 CUDA-core kernel (dQ by atomics) + dQ conversion" if not bf16 else
+                       "short-query dQ/dK/dV kernel" if short_q else
                        "fused dK/dV/dQ kernel" if fused else "dK/dV kernel + dQ kernel")
+    cfg["forward"] = {"jfa_fwd_kernel": "query-tile kernel", "jfa_fwd_short_kernel": "short-query GDPA kernel",
+                      "jfa_fwd_pack_kernel": "short-query softmax kernel (two key tiles per score tile)",
+                      "jfa_fwd_f32_kernel": "fp32 CUDA-core kernel"}[
+        "jfa_fwd_f32_kernel" if not bf16 else
+        ("jfa_fwd_pack_kernel" if batch.mode == "softmax" else "jfa_fwd_short_kernel")
+        if (info["fwd_short"] > 0 and batch.bias is None) else "jfa_fwd_kernel"]
     O = torch.empty_like(batch.Q)
     lse = torch.empty((batch.Q.shape[0], batch.H), dtype=torch.float32, device=dev)
     dQ, dK, dV = torch.empty_like(batch.Q), torch.empty_like(batch.K), torch.empty_like(batch.V)
@@ -424,11 +433,14 @@ def main():
 
     # dominant kernel: the largest share of device time among the tensor-core kernels
     per = {k: (v[0] / v[1] if v[1] else 0.0, v[1], v[0]) for k, v in kt.items()}
-    kflop = kernel_flops(fl_f, fused or short_q)
+    kflop = kernel_flops(fl_f, one_kernel_bwd)
     fwd_short = bf16 and info["fwd_short"] > 0 and batch.bias is None
-    kname_of = {"fwd": "jfa_fwd_short_kernel" if fwd_short else "jfa_fwd_kernel", "bwd_main": ("jfa_bwd_short_kernel" if short_q else
+    fwd_kernel = ("jfa_fwd_f32_kernel" if not bf16 else
+                  ("jfa_fwd_pack_kernel" if batch.mode == "softmax" else "jfa_fwd_short_kernel") if fwd_short else
+                  "jfa_fwd_kernel")
+    kname_of = {"fwd": fwd_kernel, "bwd_main": "jfa_bwd_f32_kernel" if not bf16 else ("jfa_bwd_short_kernel" if short_q else
                                                       "jfa_bwd_fused_kernel" if fused else "jfa_bwd_dkdv_kernel")}
-    if not (fused or short_q):
+    if bf16 and not (fused or short_q):
         kname_of["bwd_dq"] = "jfa_bwd_dq_kernel"
     dom = max(kname_of, key=lambda k: per[k][2])
     dom_ms = per[dom][0]
