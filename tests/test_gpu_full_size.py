@@ -82,3 +82,23 @@ def test_ikbo_cross_full_batch():
         m = parity.compare(g, ref)
         print("ikbo_cross", o_dtype, m)
         parity.assert_within(m)
+
+
+def test_cross_full_batch():
+    """The whole cross-attention workload (512 query sets of up to 64 rows over key/value
+    histories of up to 16K rows) against the oracle, every output compared: the short-query
+    forward with two key tiles per score tile and the short-query backward, as the benchmark
+    launches them (bf16 O) and with fp32 O."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from jagged_sequence_attention_gb300 import jfa
+    batch = wl.make("cross", device="cuda")
+    ref = parity.run_oracle(batch)
+    for o_dtype in (torch.float32, torch.bfloat16):
+        g = parity.run_gpu(batch, out_dtype=o_dtype)
+        assert g["status"] == 0
+        info = jfa.jfa_plan_info(g["plan"])
+        assert info["fwd_short"] == 64 and info["bwd_short"] == 64
+        m = parity.compare(g, ref)
+        print("cross", o_dtype, m)
+        parity.assert_within(m)
