@@ -319,8 +319,9 @@ KERNEL_KINDS = ["fwd", "bwd_pre", "bwd_main", "bwd_post", "bwd_dq"]
 
 
 def jfa_plan_set_work_item(plan: Plan, pass_: int, index: int, item):
-    """Test hook: overwrite work item `index` of pass 0 (forward), 1 (dK/dV), 2 (dQ) or 3 (the
-    short-query backward) with the four ints of `item` (see include/jfa.h)."""
+    """Test hook: overwrite work item `index` of pass 0 (forward), 1 (dK/dV), 2 (dQ), 3 (the
+    short-query backward) or 4 (the short-query forward) with the four ints of `item` (see
+    include/jfa.h)."""
     buf = np.ascontiguousarray(np.asarray(item, dtype=np.int32).reshape(4))
     _check("jfa_plan_set_work_item", lib().jfa_plan_set_work_item(plan.handle, int(pass_), int(index),
                                                                     buf.ctypes.data_as(ctypes.c_void_p)))
