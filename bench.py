@@ -205,8 +205,10 @@ def oracle_sample(batch, target_seconds=15.0):
     """The shortest sequences of the batch (all heads), as a CPU batch: a bounded sample
     of the same workload for the oracle."""
     order = np.argsort(batch.q_lens * batch.kv_lens)
-    # ~40 GFLOP of fp64 work per 15 s on the host cores is the planning figure
-    budget = 2.7e9 * target_seconds
+    # planning figure: the oracle's measured rate on the GPU box's host cores, about 28 GFLOP/s
+    # of fp64 work (a 4,269-token causal sequence, all 8 heads, forward and backward: 130 GFLOP
+    # in 4.6 s)
+    budget = 28e9 * target_seconds
     seqs, tot = [], 0.0
     for b in order:
         f = 3.5 * 4.0 * batch.D * batch.H * allowed_pairs([batch.q_lens[b]], [batch.kv_lens[b]], batch.causal,
@@ -313,7 +315,8 @@ def main():
                 dist.barrier()
             return
         batch = wl.broadcast(wl.make(args.workload, device="cpu"))
-        cpu, seqs = oracle_sample(batch, args.cpu_seconds)
+        # each timed step is one run of the sample: keep all K steps within about 2.5 minutes
+        cpu, seqs = oracle_sample(batch, min(args.cpu_seconds, 150.0 / max(1, args.steps)))
         fl_f, fl_b = flops_of(cpu)
         # the oracle's one warm-up effect is loading its library: one tiny call does that
         run_oracle_once(wl.subset(cpu, [0], [0]))
