@@ -280,7 +280,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--broadcast", action="store_true",
                     help="shared key/value workloads: run the plain path on an explicit broadcast copy of each "
                          "query set's user rows (the copies the in-kernel broadcast avoids; copy not timed)")
