@@ -201,6 +201,14 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- reference (oracle)
 
 
+def lengths_text(lens):
+    """The sample's query lengths: listed when few, else their count, range and total."""
+    lens = sorted(int(x) for x in lens)
+    if len(lens) <= 8:
+        return f"lengths {lens}"
+    return f"lengths {lens[0]}..{lens[-1]}, {sum(lens)} tokens"
+
+
 def oracle_sample(batch, target_seconds=15.0):
     """The shortest sequences of the batch (all heads), as a CPU batch: a bounded sample
     of the same workload for the oracle."""
@@ -323,7 +331,7 @@ def main():
         times = [run_oracle_once(cpu) for _ in range(args.steps)]
         t = sum(times) / len(times)
         v = (fl_f + fl_b) / t / 1e12
-        sample = (f"{len(seqs)} shortest sequences of the workload (lengths {sorted(batch.q_lens[seqs].tolist())}), "
+        sample = (f"{len(seqs)} shortest sequences of the workload ({lengths_text(batch.q_lens[seqs])}), "
                   f"all {cpu.H} heads, forward+backward in fp64")
         cfg.update({"tokens": int(batch.q_off[-1]), "sample_tokens": int(cpu.q_off[-1])})
         line = {"metric": METRIC, "value": v, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
@@ -594,8 +602,8 @@ def main():
         t = run_oracle_once(cpu, ref)
         line["cpu_baseline"] = {"value": (cf + cb) / t / 1e12, "unit": UNIT, "cores": oracle_cores(cpu),
                                 "kind": "oracle", "seconds": t,
-                                "sample": f"{len(seqs)} shortest sequences (lengths "
-                                          f"{sorted(batch.q_lens[seqs].tolist())}), all {cpu.H} heads, fwd+bwd fp64"}
+                                "sample": f"{len(seqs)} shortest sequences ({lengths_text(batch.q_lens[seqs])}), "
+                                          f"all {cpu.H} heads, fwd+bwd fp64"}
         if sampled_rows is not None:
             # the benchmarked launch's own outputs for the same sequences, against the oracle
             line["parity_sample"] = {"sample": line["cpu_baseline"]["sample"],
