@@ -96,7 +96,7 @@ struct FuCfg {
 enum {
     FU_K_FULL = 0,
     FU_V_FULL = 1,
-    FU_KV_EMPTY = 2,
+    FU_K_EMPTY = 2,  // the item's last dQ product is done: K may be overwritten
     FU_Q_FULL = 3,   // +stage
     FU_Q_EMPTY = 5,  // +stage
     FU_DO_FULL = 7,
@@ -111,6 +111,7 @@ enum {
     FU_ACC_FULL = 18,
     FU_ACC_EMPTY = 19,
     FU_DRAIN = 20,
+    FU_V_EMPTY = 21,  // the item's last dP product is done: V may be overwritten
 };
 
 template <int D, bool GDPA>
@@ -134,7 +135,8 @@ __global__ void __launch_bounds__(320, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(FU_K_FULL), 1);
         mbar_init(bar(FU_V_FULL), 1);
-        mbar_init(bar(FU_KV_EMPTY), 1);
+        mbar_init(bar(FU_K_EMPTY), 1);
+        mbar_init(bar(FU_V_EMPTY), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(FU_Q_FULL + s), 1);
             mbar_init(bar(FU_Q_EMPTY + s), 1);
@@ -181,9 +183,47 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == C::kProdWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t step_it = 0, item_it = 0;
-            uint32_t q_extra = 0;  // 1: the last step's Q load went out but its dO load did not
+            // Loads issued so far, per buffer (the drain below waits for each one's last).
+            // An item's loads go out in the order in which their buffers come free at the
+            // end of the previous item: its first Q tile (a ring stage freed a step
+            // earlier), V (after the last dP), its first dO tile (after the last dV), and K
+            // (after the last dQ), so that only K's load stands between one item's last
+            // product and the next item's first.
+            uint32_t n_q = 0, n_do = 0, n_k = 0, n_v = 0;
             bool ok = true;
+            auto load_q = [&](int h, int y) -> bool {
+                const uint32_t st = n_q & 1, ph = (n_q >> 1) & 1;
+                if (!mbar_wait_bounded(bar(FU_Q_EMPTY + st), ph ^ 1, abort_flag)) return false;
+                mbar_arrive_expect_tx(bar(FU_Q_FULL + st), C::kQTile);
+#pragma unroll
+                for (int cb = 0; cb < C::kCB; ++cb)
+                    tma_load_2d(sQ + st * C::kQTile + cb * C::BM * 128, &tmQ, bar(FU_Q_FULL + st),
+                                h * D + cb * C::kBoxCols, y);
+                ++n_q;
+                return true;
+            };
+            auto load_do = [&](int h, int y) -> bool {
+                if (!mbar_wait_bounded(bar(FU_DO_EMPTY), (n_do & 1) ^ 1, abort_flag)) return false;
+                mbar_arrive_expect_tx(bar(FU_DO_FULL), C::kQTile);
+#pragma unroll
+                for (int cb = 0; cb < C::kCB; ++cb)
+                    tma_load_2d(sDO + cb * C::BM * 128, &tmdO, bar(FU_DO_FULL), h * D + cb * C::kBoxCols, y);
+                ++n_do;
+                return true;
+            };
+            // K or V of key rows [y, y + BN)
+            auto load_kv = [&](bool is_k, int h, int y) -> bool {
+                uint32_t& cnt = is_k ? n_k : n_v;
+                if (!mbar_wait_bounded(bar(is_k ? FU_K_EMPTY : FU_V_EMPTY), (cnt & 1) ^ 1, abort_flag)) return false;
+                const uint32_t full = bar(is_k ? FU_K_FULL : FU_V_FULL);
+                mbar_arrive_expect_tx(full, C::kKVTile);
+#pragma unroll
+                for (int cb = 0; cb < C::kCB; ++cb)
+                    tma_load_2d((is_k ? sK : sV) + cb * C::BN * 128, is_k ? &tmK : &tmV, full,
+                                h * D + cb * C::kBoxCols, y);
+                ++cnt;
+                return true;
+            };
             for (int it = it_begin; it < it_end && ok; ++it) {
                 const int4 w = p.items[it];
                 if (!kv_item_ok(w, p, false)) {  // not an item of this plan: skipped by every role
@@ -196,44 +236,22 @@ __global__ void __launch_bounds__(320, 1)
                 const int q0 = p.q_off[b], kv0 = p.kv_off[b];
                 int first_qt, nq;  // query tiles [first_qt, first_qt + n) see this key tile
                 query_tile_range(p.q_off[b + 1] - q0, p.kv_off[b + 1] - kv0, nt, p.causal, p.window, first_qt, nq);
-                if (!mbar_wait_bounded(bar(FU_KV_EMPTY), (item_it & 1) ^ 1, abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(bar(FU_K_FULL), C::kKVTile);
-#pragma unroll
-                for (int cb = 0; cb < C::kCB; ++cb)
-                    tma_load_2d(sK + cb * C::BN * 128, &tmK, bar(FU_K_FULL), h * D + cb * C::kBoxCols, kv0 + nt * C::BN);
-                mbar_arrive_expect_tx(bar(FU_V_FULL), C::kKVTile);
-#pragma unroll
-                for (int cb = 0; cb < C::kCB; ++cb)
-                    tma_load_2d(sV + cb * C::BN * 128, &tmV, bar(FU_V_FULL), h * D + cb * C::kBoxCols, kv0 + nt * C::BN);
-                ++item_it;
-                for (int i = 0; i < n; ++i, ++step_it) {
-                    const uint32_t st = step_it & 1, ph = (step_it >> 1) & 1;
+                const int y0 = q0 + first_qt * C::BM, ykv = kv0 + nt * C::BN;
+                if (!load_q(h, y0) || !load_kv(false, h, ykv) || !load_do(h, y0) || !load_kv(true, h, ykv)) {
+                    ok = false;
+                    break;
+                }
+                for (int i = 1; i < n; ++i) {
                     const int y = q0 + (first_qt + i) * C::BM;
-                    if (!mbar_wait_bounded(bar(FU_Q_EMPTY + st), ph ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(bar(FU_Q_FULL + st), C::kQTile);
-#pragma unroll
-                    for (int cb = 0; cb < C::kCB; ++cb)
-                        tma_load_2d(sQ + st * C::kQTile + cb * C::BM * 128, &tmQ, bar(FU_Q_FULL + st),
-                                    h * D + cb * C::kBoxCols, y);
-                    if (!mbar_wait_bounded(bar(FU_DO_EMPTY), (step_it & 1) ^ 1, abort_flag)) {
-                        q_extra = 1;
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar(FU_DO_FULL), C::kQTile);
-#pragma unroll
-                    for (int cb = 0; cb < C::kCB; ++cb)
-                        tma_load_2d(sDO + cb * C::BM * 128, &tmdO, bar(FU_DO_FULL), h * D + cb * C::kBoxCols, y);
+                    if (!load_q(h, y) || !load_do(h, y)) { ok = false; break; }
                 }
             }
             if (!ok) fail();
             // Drain: wait until every load this thread issued has landed.
-            if (item_it > 0) {
-                mbar_wait_bounded(bar(FU_K_FULL), (item_it - 1) & 1, nullptr);
-                mbar_wait_bounded(bar(FU_V_FULL), (item_it - 1) & 1, nullptr);
-            }
-            drain_ring(bar(FU_Q_FULL), step_it + q_extra, 2);
-            drain_ring(bar(FU_DO_FULL), step_it, 1);
+            if (n_k > 0) mbar_wait_bounded(bar(FU_K_FULL), (n_k - 1) & 1, nullptr);
+            if (n_v > 0) mbar_wait_bounded(bar(FU_V_FULL), (n_v - 1) & 1, nullptr);
+            drain_ring(bar(FU_Q_FULL), n_q, 2);
+            drain_ring(bar(FU_DO_FULL), n_do, 1);
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -268,8 +286,9 @@ __global__ void __launch_bounds__(320, 1)
             __syncwarp();
             return true;
         };
-        // dP^T(g) = V dO^T into Y, once every compute warp has drained dQ(g-1) out of Y.
-        auto issue_dp = [&](uint32_t g) -> bool {
+        // dP^T(g) = V dO^T into Y, once every compute warp has drained dQ(g-1) out of Y;
+        // after an item's last one, V is released to the next item's load.
+        auto issue_dp = [&](uint32_t g, bool last) -> bool {
             if (!warp_wait(FU_DO_FULL, g & 1)) return false;
             if (g > 0 && !warp_wait(FU_DQ_EMPTY, (g - 1) & 1)) return false;
             tc_fence_after();
@@ -277,6 +296,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                 for (int s = 0; s < C::kDSteps; ++s) mma_ss(tmem + C::kTmY, dVa, koff(s), dOk, koff(s), C::kIdescS, s > 0);
                 tc_commit(bar(FU_DP_FULL));
+                if (last) tc_commit(bar(FU_V_EMPTY));
             }
             __syncwarp();
             return true;
@@ -344,12 +364,12 @@ __global__ void __launch_bounds__(320, 1)
             if (!warp_wait(FU_K_FULL, item_it & 1) || !warp_wait(FU_V_FULL, item_it & 1)) { ok = false; break; }
             tc_fence_after();
             const uint32_t g0 = step_it;
-            if (!issue_s(g0) || !issue_dp(g0) || !issue_dv(g0, true)) { ok = false; break; }
+            if (!issue_s(g0) || !issue_dp(g0, n == 1) || !issue_dv(g0, true)) { ok = false; break; }
             for (int i = 0; i < n && ok; ++i) {
                 const uint32_t g = g0 + uint32_t(i);
                 if (i + 1 < n && !issue_s(g + 1)) { ok = false; break; }
                 if (!issue_dk_dq(g, i == 0)) { ok = false; break; }
-                if (i + 1 < n && (!issue_dp(g + 1) || !issue_dv(g + 1, false))) {
+                if (i + 1 < n && (!issue_dp(g + 1, i + 2 == n) || !issue_dv(g + 1, false))) {
                     ok = false;
                     break;
                 }
@@ -357,7 +377,7 @@ __global__ void __launch_bounds__(320, 1)
             if (!ok) break;
             if (elect_one()) {
                 tc_commit(bar(FU_ACC_FULL));
-                tc_commit(bar(FU_KV_EMPTY));
+                tc_commit(bar(FU_K_EMPTY));
             }
             __syncwarp();
             step_it += uint32_t(n);
