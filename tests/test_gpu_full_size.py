@@ -1,6 +1,6 @@
 """Full-size backward parity: complete outputs of benchmark-size launches against the
 oracle (aihot GEM article, "Jagged Sequence Flash Attention": the efficient backward
-pass on jagged tensors).
+pass on jagged tensors; "Generalized Dot-Product Attention (GDPA)" for the GDPA batches).
 
 The sampled full-size tests elsewhere compare suffix rows only, so the dK/dV they check
 belong to keys that few query tiles see.  Here every row and every key of one head of
@@ -101,4 +101,61 @@ def test_cross_full_batch():
         assert info["fwd_short"] == 64 and info["bwd_short"] == 64
         m = parity.compare(g, ref)
         print("cross", o_dtype, m)
+        parity.assert_within(m)
+
+
+def _full_batch(name, expect):
+    """A named workload's whole batch against the oracle, every output of every sequence
+    and head compared, once with O in fp32 (plain bounds) and once with O in bf16 (the
+    launch the benchmark times; the bound allows for O's own rounding).  `expect`: plan
+    facts that pin the kernels the benchmark runs on this workload."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from jagged_sequence_attention_gb300 import jfa
+    batch = wl.make(name, device="cuda")
+    softmax = batch.mode == "softmax"
+    ref = parity.run_oracle(batch)
+    for o_dtype in (torch.float32, torch.bfloat16):
+        g = parity.run_gpu(batch, out_dtype=o_dtype)
+        assert g["status"] == 0
+        info = jfa.jfa_plan_info(g["plan"])
+        for k, v in expect.items():
+            assert info[k] == v, (k, info[k], v)
+        m = parity.compare(g, ref, softmax=softmax)
+        print(name, o_dtype, m)
+        parity.assert_within(m, softmax=softmax)
+
+
+def test_causal_bias_full_batch():
+    """256 causal sequences of 32 to 2,048 tokens with the relative-position bias, 8 heads:
+    the query-tile forward and the fused backward (every key tile's part of dQ added into
+    the fp32 accumulator)."""
+    _full_batch("causal_bias", {"bwd_fused": 1, "bwd_short": 0, "fwd_short": 0})
+
+
+@pytest.mark.parametrize("name", ["gdpa_gelu", "gdpa_silu"])
+def test_gdpa_full_batch(name):
+    """1,024 query sets of 1 to 128 rows over 64 to 4,096 keys, 4 heads, no normalisation:
+    the transposed short-query forward and the short-query backward."""
+    _full_batch(name, {"bwd_short": 128, "fwd_short": 128})
+
+
+def test_long_causal_shortest_sequence_all_heads_in_full(long_causal):
+    """The shortest sequence of the long causal workload, every head, every row and key,
+    from the benchmark's whole-batch launch (bf16 O, and fp32 O)."""
+    batch = long_causal
+    b = int(np.argmin(batch.q_lens))
+    q0, q1 = int(batch.q_off[b]), int(batch.q_off[b + 1])
+    assert (int(batch.kv_off[b]), int(batch.kv_off[b + 1])) == (q0, q1)  # self-attention: same rows
+    runs = {}
+    for o_dtype in (torch.float32, torch.bfloat16):
+        g = parity.run_gpu(batch, out_dtype=o_dtype)
+        assert g["status"] == 0
+        runs[o_dtype] = {k: g[k][q0:q1] for k in ("O", "lse", "dQ", "dK", "dV")}
+        del g
+        torch.cuda.empty_cache()
+    ref = parity.run_oracle(wl.subset(batch, [b]))
+    for o_dtype, got in runs.items():
+        m = parity.compare(got, ref)
+        print("long_causal shortest", b, q1 - q0, o_dtype, m)
         parity.assert_within(m)
