@@ -697,7 +697,7 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
         tm.done();
         if (e != cudaSuccess) return JFA_ERR_CUDA;
     }
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mdq;
     BwdParams p;
     if (v->n_bwd_items > 0 || (dtype == JFA_BF16 && v->n_dq_items > 0)) {
         const int q_box = short_q ? v->short_bq : kBwdBM;  // Q and dO rows per load
@@ -706,6 +706,9 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
              (s = make_map(&mk, dtype, K, plan->Tkv, plan->H, plan->D, plan->dev_block, kBwdBN)) != JFA_OK ||
              (s = make_map(&mv, dtype, V, plan->Tkv, plan->H, plan->D, plan->dev_block, kBwdBN)) != JFA_OK ||
              (s = make_map(&mdo, dtype, dO, plan->Tq, plan->H, plan->D, plan->dev_block, q_box)) != JFA_OK))
+            return s;
+        // the fused backward's dQ accumulator, [T_q, H*D] fp32 in 32 x 32 boxes (reduce-adds)
+        if (fused && (s = make_map(&mdq, JFA_F32, dq_acc, plan->Tq, plan->H, plan->D, plan->dev_block, 32)) != JFA_OK)
             return s;
         p.items = v->d_bwd_items;
         p.cta_off = v->d_bwd_cta_off;
@@ -755,7 +758,7 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
     }
     if (v->n_bwd_items > 0) {
         KernelTimer tm(plan, 2, st);
-        e = dtype == JFA_BF16 ? (fused ? launch_bwd_fused(plan->D, mq, mk, mv, mdo, p, v->bwd_grid, st)
+        e = dtype == JFA_BF16 ? (fused ? launch_bwd_fused(plan->D, mq, mk, mv, mdo, mdq, p, v->bwd_grid, st)
                                        : launch_bwd_main(dtype, plan->D, mq, mk, mv, mdo, p, v->bwd_grid, st))
                               : launch_bwd_f32(plan->D, Q, K, V, dO, p, v->n_bwd_items, st);
         tm.done();

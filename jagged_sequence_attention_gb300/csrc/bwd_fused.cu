@@ -9,7 +9,7 @@
 // buffer); a conversion pass scales it and writes dQ in bf16.  Compared with a second
 // pass over query tiles, which recomputes S and dP to form dQ on chip, it issues five
 // products per tile pair instead of seven, and moves 64 KB of fp32 reduce-adds per tile
-// pair instead (L2 absorbs them at about 6.7 TB/s on GB300).
+// pair instead (L2 absorbs them at about 7 TB/s on GB300).
 //
 // Persistent over (sequence, head, 128-row key tile).  K and V stay in shared memory;
 // 128-row query tiles stream through a two-stage Q ring and a one-stage dO buffer.
@@ -22,9 +22,9 @@
 //   dK  += dS^T Q_i     (A = the dS tile read K-major)
 //   dQ_i = dS K         (A = the same dS tile read MN-major; into TMEM Y, whose dP^T the
 //                        compute warps have read), then drained by the compute warps:
-//                        TMEM -> registers -> a transpose through the dS tile ->
-//                        red.global.add.v4.f32, four query rows x 128 bytes per
-//                        instruction
+//                        TMEM -> registers (Y released) -> 32 x 32 fp32 boxes staged in
+//                        the dS tile -> TMA tensor reduce-adds into the accumulator, so
+//                        the compute warps issue no per-element global traffic
 // TMEM: dV [0,128), dK [128,256), X [256,384), Y [384,512).
 // Issue order per step: S(i+1), dK(i), dQ(i), dP(i+1), dV(i+1).  dP(i+1) waits for the
 // drain of dQ(i) out of Y; the compute warps drain dQ(i) after forming step i+1's row
@@ -118,7 +118,7 @@ template <int D, bool GDPA>
 __global__ void __launch_bounds__(320, 1)
     jfa_bwd_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                         const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
     using C = FuCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(320, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmdO);
+        tma_prefetch_desc(&tmDQ);
     }
     tc_fence_before();
     __syncthreads();
@@ -414,41 +415,45 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t step_it = 0, item_it = 0;
         bool ok = true;
 
-        // dQ(g) of query rows [qrow0, qrow0 + 128) of a sequence (rows from dq_q0, dq_len
-        // of them): TMEM Y -> registers -> 32 x 32 transposes through this warp's staging ->
-        // reduce-adds of four rows x 128 bytes per instruction.  Rows past the sequence
-        // end hold exact zeros (their dS is 0) and are skipped, so nothing is added
-        // outside the accumulator.
-        // dq_item: the accumulator row of the item's sequence start, at this warpgroup's columns.
-        const int row_stride = p.H * D;  // floats between consecutive rows of the accumulator
-        auto drain = [&](uint32_t g, float* dq_item, int dq_len, int qrow0) -> bool {
+        // dQ(g) of query rows [qrow0, qrow0 + 128) of a sequence whose first row is dq_y0 (of
+        // dq_len rows), at accumulator column dq_x0 (this warpgroup's half of head h):
+        // TMEM Y -> registers, after which Y is released for the next dP; then, 32 columns
+        // at a time, this warp's 32 rows go through its staging (the 128-byte-swizzled box
+        // layout) and a TMA reduce-add into the accumulator.  The box covers all 32 rows: rows
+        // past the sequence end hold zeros (their dS is 0), and adding a zero leaves any value
+        // of the accumulator as it is (it starts at +0, so no sum in it is ever -0); rows past
+        // the accumulator's end are clipped by the tensor map.  A warp whose rows all lie past
+        // the end adds nothing.
+        auto drain = [&](uint32_t g, int dq_x0, int dq_y0, int dq_len, int qrow0) -> bool {
             if (!warp_wait(FU_DQK_DONE, g & 1)) return false;
             tc_fence_after();
             const int wrow0 = qrow0 + (warp & 3) * 32;  // this warp's first query row
-            const int rows_left = dq_len - wrow0;        // of its 32, the valid ones
-            // lane's row within each group of four, and its 16-byte piece of the 128-byte row
-            float* acc_lane = dq_item + size_t(wrow0 + (lane >> 3)) * size_t(row_stride) + 4 * (lane & 7);
+            uint32_t v[C::kDrainChunks][32];
 #pragma unroll
-            for (int k = 0; k < C::kDrainChunks; ++k) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + C::kTmY + uint32_t(wg * (D / 2) + 32 * k), v);
-                tmem_ld_wait(v);
+            for (int k = 0; k < C::kDrainChunks; ++k)
+                tmem_ld32(tmem + lane_base + C::kTmY + uint32_t(wg * (D / 2) + 32 * k), v[k]);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_v4(stg + uint32_t(lane * 128 + ((q ^ (lane & 7)) << 4)), v[4 * q], v[4 * q + 1],
-                                 v[4 * q + 2], v[4 * q + 3]);
-                __syncwarp();
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int rr = 4 * j + (lane >> 3), q = lane & 7;
-                    const uint4 u = ld_shared_v4(stg + uint32_t(rr * 128 + ((q ^ (rr & 7)) << 4)));
-                    if (rr < rows_left) red_add_v4(acc_lane + size_t(4 * j) * size_t(row_stride) + 32 * k, u);
-                }
-                __syncwarp();
-            }
+            for (int k = 0; k < C::kDrainChunks; ++k) tmem_ld_wait(v[k]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(FU_DQ_EMPTY));
+#pragma unroll
+            for (int k = 0; k < C::kDrainChunks; ++k) {
+                if (k > 0) {  // the previous box has left the staging
+                    if (lane == 0) bulk_wait_read();
+                    __syncwarp();
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_shared_v4(stg + uint32_t(lane * 128 + ((q ^ (lane & 7)) << 4)), v[k][4 * q], v[k][4 * q + 1],
+                                 v[k][4 * q + 2], v[k][4 * q + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && wrow0 < dq_len) {
+                    tma_reduce_add_2d(&tmDQ, stg, dq_x0 + 32 * k, dq_y0 + wrow0);
+                    bulk_commit();
+                }
+            }
             return true;
         };
 
@@ -460,7 +465,7 @@ __global__ void __launch_bounds__(320, 1)
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
             int first_qt, nq;  // query tiles [first_qt, first_qt + n) see this key tile
             query_tile_range(q_len, kv_len, nt, p.causal, p.window, first_qt, nq);
-            float* dq_item = p.dq_acc + (size_t(q0) * size_t(p.H) + size_t(h)) * D + size_t(wg * (D / 2));
+            const int dq_x0 = h * D + wg * (D / 2);  // accumulator column of this warpgroup's half
             const int j = nt * C::BN + r;  // key row within the sequence
             const bool key_valid = j < kv_len;
             const size_t krow = (size_t(kv0) + size_t(key_valid ? j : 0)) * size_t(p.H) + size_t(h);
@@ -548,7 +553,7 @@ __global__ void __launch_bounds__(320, 1)
 
                 // dQ of the previous step, now that its products have had this step's set-up
                 // to run; Y must be free before dP of this step is issued.
-                if (i > 0 && !drain(g - 1, dq_item, q_len, qrow0 - C::BM)) { ok = false; break; }
+                if (i > 0 && !drain(g - 1, dq_x0, q0, q_len, qrow0 - C::BM)) { ok = false; break; }
 
                 // A 32-column chunk masked for every key row of the warp has P^T = dS = 0:
                 // softmax zeroes P and forms dS = 0 on the common path; GDPA also skips the
@@ -649,6 +654,10 @@ __global__ void __launch_bounds__(320, 1)
 
                 if (!warp_wait(FU_DP_FULL, g & 1)) { ok = false; break; }
                 tc_fence_after();
+                // This warp's rows of the dS tile are its dQ staging: the last box must have
+                // left it (long since, in practice) before dS is written there.
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
                 // dS = P^T (dP^T - Delta) (softmax) or act' dP^T (GDPA), 32 columns at a time,
                 // into this thread's row of the dS tile (pieces 4k .. 4k+3 of the row).
 #pragma unroll
@@ -699,7 +708,7 @@ __global__ void __launch_bounds__(320, 1)
             }
             if (!ok) break;
             // dQ of the item's last step
-            if (!drain(step_it + uint32_t(n) - 1, dq_item, q_len, (first_qt + n - 1) * C::BM)) { ok = false; break; }
+            if (!drain(step_it + uint32_t(n) - 1, dq_x0, q0, q_len, (first_qt + n - 1) * C::BM)) { ok = false; break; }
             // Epilogue: dV and dK (times scale) of this key row, the warpgroup's half of D.
             if (!warp_wait(FU_ACC_FULL, item_it & 1)) { ok = false; break; }
             tc_fence_after();
@@ -728,6 +737,9 @@ __global__ void __launch_bounds__(320, 1)
             ++item_it;
         }
         if (!ok) fail();
+        // Every dQ reduce-add this warp issued has completed before the CTA exits.
+        if (lane == 0) bulk_wait_done();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -738,7 +750,8 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D, bool GDPA>
 cudaError_t launch_fused_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                           const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
+                           const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const BwdParams& p, int grid,
+                           cudaStream_t st) {
     using C = FuCfg<D>;
     static bool configured = false;
     if (!configured) {
@@ -747,21 +760,22 @@ cudaError_t launch_fused_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_fused_kernel<D, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
+    jfa_bwd_fused_kernel<D, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, tmDQ, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_fused(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
+                             const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const BwdParams& p, int grid,
+                             cudaStream_t st) {
     const bool sm = p.mode == JFA_SOFTMAX;
     if (D == 128)
-        return sm ? launch_fused_t<128, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                  : launch_fused_t<128, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
+        return sm ? launch_fused_t<128, false>(tmQ, tmK, tmV, tmdO, tmDQ, p, grid, st)
+                  : launch_fused_t<128, true>(tmQ, tmK, tmV, tmdO, tmDQ, p, grid, st);
     if (D == 64)
-        return sm ? launch_fused_t<64, false>(tmQ, tmK, tmV, tmdO, p, grid, st)
-                  : launch_fused_t<64, true>(tmQ, tmK, tmV, tmdO, p, grid, st);
+        return sm ? launch_fused_t<64, false>(tmQ, tmK, tmV, tmdO, tmDQ, p, grid, st)
+                  : launch_fused_t<64, true>(tmQ, tmK, tmV, tmdO, tmDQ, p, grid, st);
     return cudaErrorInvalidValue;
 }
 
