@@ -292,6 +292,9 @@ def main():
     ap.add_argument("--broadcast", action="store_true",
                     help="shared key/value workloads: run the plain path on an explicit broadcast copy of each "
                          "query set's user rows (the copies the in-kernel broadcast avoids; copy not timed)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="plans in deterministic mode (jfa_plan_set_deterministic): the two-pass bf16 backward, "
+                         "the same bits on every run, whatever form the planner would choose")
     ap.add_argument("--partition", action="store_true",
                     help="strong scaling: one batch, its sequences split across the ranks by the LPT partition "
                          "(default: weak scaling, each rank its own batch of the workload)")
@@ -313,7 +316,7 @@ def main():
     w = wl.WORKLOADS[args.workload]
     cfg = {"workload": args.workload, "description": w.description, "B": w.B, "H": w.H, "D": w.D,
            "mode": w.mode, "causal": w.causal, "bias": w.bias, "window": w.window, "seed": wl.seed_of(w),
-           "users": w.users, "broadcast": bool(args.broadcast and w.users),
+           "users": w.users, "broadcast": bool(args.broadcast and w.users), "deterministic": bool(args.deterministic),
            "l2": "inputs larger than L2 (no flush needed)",
            "parallelism": f"dp{world} (" + ("LPT partition of one batch" if args.partition else "independent batches") + ")"}
 
@@ -362,7 +365,7 @@ def main():
                 "unpadded_fwd_flop": fl_f, "unpadded_bwd_flop": fl_b})
 
     stream = torch.cuda.current_stream()
-    plan = jfa.plan_for(batch)
+    plan = jfa.plan_for(batch, deterministic=args.deterministic)
     # The backward form jfa_bwd runs on bf16 inputs: short-query (no bias, every query set
     # in one tile), else fused (no dense bias, no bias gradient), else two-pass.
     info = jfa.jfa_plan_info(plan)
@@ -539,7 +542,8 @@ def main():
                 ev_do.record(s_in)
             p2 = jfa.plan_for(wl.Batch(batch.name, q_off, kv_off, b["Q"], b["K"], b["V"], b["dO"], b["bias"],
                                        batch.scale, batch.mode, batch.causal, batch.H, batch.D,
-                                       window=batch.window, kv_map=batch.kv_map), stream=s_plan)
+                                       window=batch.window, kv_map=batch.kv_map), stream=s_plan,
+                              deterministic=args.deterministic)
             plans.append(p2)
             stream.wait_event(ev_qkv)
             jfa.jfa_fwd(p2, b["Q"], b["K"], b["V"], b["bias"], batch.scale, O=b["O"], lse=b["lse"], stream=stream)
