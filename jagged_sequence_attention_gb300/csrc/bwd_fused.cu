@@ -27,8 +27,8 @@
 //                        the compute warps issue no per-element global traffic
 // TMEM: dV [0,128), dK [128,256), X [256,384), Y [384,512).
 // Issue order per step: S(i+1), dK(i), dQ(i), dP(i+1), dV(i+1).  dP(i+1) waits for the
-// drain of dQ(i) out of Y; the compute warps drain dQ(i) after forming step i+1's row
-// terms and before its P^T phase, so S(i+1) and the drain overlap dK(i) and dQ(i).
+// drain of dQ(i) out of Y; the compute warps drain dQ(i) after step i+1's P^T phase, so
+// that dK(i) and dQ(i) run on the tensor core while P^T(i+1) is formed.
 //
 // CTA = 10 warps: 0-7 compute (thread = key row = TMEM lane; warpgroup g owns query
 // columns [64g, 64g+64) of a step, and in the drain, head-dim columns [g D/2, (g+1) D/2)
@@ -428,25 +428,24 @@ __global__ void __launch_bounds__(320, 1)
             if (!warp_wait(FU_DQK_DONE, g & 1)) return false;
             tc_fence_after();
             const int wrow0 = qrow0 + (warp & 3) * 32;  // this warp's first query row
-            uint32_t v[C::kDrainChunks][32];
-#pragma unroll
-            for (int k = 0; k < C::kDrainChunks; ++k)
-                tmem_ld32(tmem + lane_base + C::kTmY + uint32_t(wg * (D / 2) + 32 * k), v[k]);
-#pragma unroll
-            for (int k = 0; k < C::kDrainChunks; ++k) tmem_ld_wait(v[k]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(FU_DQ_EMPTY));
 #pragma unroll
             for (int k = 0; k < C::kDrainChunks; ++k) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + C::kTmY + uint32_t(wg * (D / 2) + 32 * k), v);
+                tmem_ld_wait(v);
+                if (k + 1 == C::kDrainChunks) {  // the last read of Y: release it for the next dP
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(FU_DQ_EMPTY));
+                }
                 if (k > 0) {  // the previous box has left the staging
                     if (lane == 0) bulk_wait_read();
                     __syncwarp();
                 }
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    st_shared_v4(stg + uint32_t(lane * 128 + ((q ^ (lane & 7)) << 4)), v[k][4 * q], v[k][4 * q + 1],
-                                 v[k][4 * q + 2], v[k][4 * q + 3]);
+                    st_shared_v4(stg + uint32_t(lane * 128 + ((q ^ (lane & 7)) << 4)), v[4 * q], v[4 * q + 1],
+                                 v[4 * q + 2], v[4 * q + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && wrow0 < dq_len) {
@@ -551,10 +550,6 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 __syncwarp();
 
-                // dQ of the previous step, now that its products have had this step's set-up
-                // to run; Y must be free before dP of this step is issued.
-                if (i > 0 && !drain(g - 1, dq_x0, q0, q_len, qrow0 - C::BM)) { ok = false; break; }
-
                 // A 32-column chunk masked for every key row of the warp has P^T = dS = 0:
                 // softmax zeroes P and forms dS = 0 on the common path; GDPA also skips the
                 // chunk's loads and dS arithmetic.
@@ -652,10 +647,15 @@ __global__ void __launch_bounds__(320, 1)
                     if (lane == 0) mbar_arrive(bar(FU_P_FULL + k));
                 }
 
+                // dQ of the previous step, drained once this step's P^T is out, so that dK and dQ
+                // of the previous step run on the tensor core during the P^T phase; Y must be
+                // free before dP of this step is issued.
+                if (i > 0 && !drain(g - 1, dq_x0, q0, q_len, qrow0 - C::BM)) { ok = false; break; }
+
                 if (!warp_wait(FU_DP_FULL, g & 1)) { ok = false; break; }
                 tc_fence_after();
                 // This warp's rows of the dS tile are its dQ staging: the last box must have
-                // left it (long since, in practice) before dS is written there.
+                // left it before dS is written there.
                 if (lane == 0) bulk_wait_read();
                 __syncwarp();
                 // dS = P^T (dP^T - Delta) (softmax) or act' dP^T (GDPA), 32 columns at a time,
