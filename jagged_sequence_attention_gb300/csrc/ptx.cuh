@@ -376,14 +376,6 @@ __device__ __forceinline__ void store_chunk_bf16(uint32_t stg, const uint32_t (&
     __syncwarp();
 }
 
-// Adds four consecutive fp32 values (bits in v) to global memory at a 16-byte aligned
-// address, as one vector reduction performed at L2.
-__device__ __forceinline__ void red_add_v4(float* addr, uint4 v) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(__uint_as_float(v.x)),
-                 "f"(__uint_as_float(v.y)), "f"(__uint_as_float(v.z)), "f"(__uint_as_float(v.w))
-                 : "memory");
-}
-
 // Packed dual fp32 arithmetic (fma/add on a pair of floats, one instruction).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     float2 d;
