@@ -121,7 +121,7 @@ __device__ __forceinline__ void store_row<float>(float* dst, const float* v, int
 // WIN: a sliding window may be set (p.window >= 0).  Without it the window arithmetic
 // folds away at compile time, so the plain causal and non-causal paths carry none of it.
 // DENSE: the bias is the dense per-pair array p.dense (read per element, both passes).
-// SPLIT: the work list holds split items (one-tile sequences, see below); without it the
+// SPLIT: the work list holds split items (fwd_split_item, see below); without it the
 // split code compiles away and the kernel is the plain two-tile pipeline.
 template <int D, typename OT, bool GDPA, bool WIN, bool DENSE, bool SPLIT>
 __global__ void __launch_bounds__(576, 1)
@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(576, 1)
                         tma_load_2d(sQ + tq * C::kQBytes + cb * C::BM * 128, &tmQ, bar(B_Q_FULL),
                                     h * D + cb * C::kBoxCols, q0 + (2 * pr + tq) * C::BM);
                 ++item_it;
-                // A split item (a one-tile sequence with two or more key tiles) streams the two
-                // halves of its key range interleaved: tile 0's half at even steps, tile 1's at odd.
-                const bool split = SPLIT && q_len <= C::BM && na >= 2;
+                // A split item (fwd_split_item) streams the two halves of its key range
+                // interleaved: tile 0's half at even steps, tile 1's at odd.
+                const bool split = SPLIT && fwd_split_item(q_len, pr, na);
                 const int half0 = (na + 1) / 2;
                 for (int j = 0; j < n; ++j, ++kv_it) {
                     const uint32_t st = kv_it & 1, ph = (kv_it >> 1) & 1;
@@ -329,11 +329,10 @@ __global__ void __launch_bounds__(576, 1)
             key_tile_range(q_len, kv_len, 2 * pr + 1, p.causal, window, fb, nx1);
             pair_stream(q_len, kv_len, pr, p.causal, window, f0, ns, na2, nb2);
             const int off0 = fa - f0, off1 = fb - f0;
-            // A split item (a one-tile sequence, q_len <= 128, with two or more key tiles): both
-            // tiles' products read query tile 0; tile 0 takes the even stream steps, tile 1 the
-            // odd.  (Short-query batches consist of such items; a long sequence's odd last tile is
-            // not split, which measured faster.)
-            const bool split = SPLIT && q_len <= C::BM && nx0 >= 2;
+            // A split item (fwd_split_item: a pair holding one query tile with two or more key
+            // tiles; a longer sequence's odd last tile only with a long key range): both tiles'
+            // products read query tile 0; tile 0 takes the even stream steps, tile 1 the odd.
+            const bool split = SPLIT && fwd_split_item(q_len, pr, nx0);
             if (!wwait(B_Q_FULL, item_it & 1)) { ok = false; break; }
             if (!split) {
                 auto act0 = [&](int j) { return j >= off0 && j < off0 + nx0; };
@@ -450,13 +449,13 @@ __global__ void __launch_bounds__(576, 1)
             const int q0 = p.q_off[b], q_len = p.q_off[b + 1] - q0;
             const int kb = p.kv_map ? p.kv_map[b] : b;
             const int kv_len = p.kv_off[kb + 1] - p.kv_off[kb];
-            // Split item (a one-tile sequence with two or more key tiles): both tiles'
+            // Split item (fwd_split_item): both tiles'
             // warps take tile 0's rows, tile x one half of its key range (the first
             // (na + 1) / 2 key tiles, or the rest) with its own max, sum and O; tile 0's
             // warps combine the two at the end.  The tile loop is the same in both cases.
             int kfa, na;
             key_tile_range(q_len, kv_len, 2 * pr, p.causal, window, kfa, na);
-            const bool split = SPLIT && q_len <= C::BM && na >= 2;
+            const bool split = SPLIT && fwd_split_item(q_len, pr, na);
             const int tile = split ? 2 * pr : 2 * pr + x;
             if (tile * C::BM >= q_len) continue;  // tile B of a short last pair
             int kf, n;  // this tile's key tiles [kf, kf + n)

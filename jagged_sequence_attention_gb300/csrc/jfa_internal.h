@@ -97,6 +97,17 @@ __host__ __device__ inline void pair_stream(int64_t q_len, int64_t kv_len, int64
     }
 }
 
+// A forward pair item (query tiles 2t and 2t+1) whose pair holds a single tile (2t + 1 is past
+// the sequence end) that visits na >= 2 key tiles can be split: its key range is cut in two
+// halves run as the pair's two tiles over the same query rows and merged at the end.  The
+// split kernel splits such an item when the sequence is one tile, and for the last, odd tile
+// of a longer sequence when its key range has at least kSplitMinTiles tiles: halving a long
+// chain pays for the merge, a short one does not.
+constexpr int kSplitMinTiles = 16;
+__host__ __device__ inline bool fwd_split_item(int64_t q_len, int64_t t, int na) {
+    return (2 * t + 1) * kFwdBM >= q_len && na >= 2 && (q_len <= kFwdBM || na >= kSplitMinTiles);
+}
+
 // Query tiles (kBwdBM rows) that see key tile nt (kBwdBN keys): [first, first + count).
 // Row i sees key j when j <= i' (causal) and j >= i' - W (window), i' = i + kv_len - q_len.
 __host__ __device__ inline void query_tile_range(int64_t q_len, int64_t kv_len, int64_t nt, int causal, int window,

@@ -201,16 +201,18 @@ void build_shared_kv_dkdv(const int32_t* q_off, const int32_t* u_off, const int3
     assign_lpt(all, U, H, n_ctas, items, cta_off, nullptr);
 }
 
-// The forward's split items: a sequence with a single query tile (q_len <= 128) that
+// The forward's split items (fwd_split_item): a pair holding a single query tile that
 // visits two key tiles or more has no second tile to overlap its softmax with, so the
 // kernel splits its key range into two halves run as if they were the two tiles of a
-// pair and merges the halves' (max, sum, O) at the end.  Code for that costs the plain
-// two-tile pipeline some speed even where no item splits, so the plan picks the kernel
-// with split items only when they carry at least half the forward's products.  The
-// sliding-window forward has no split form.
+// pair and merges the halves' (max, sum, O) at the end.  The plan picks the kernel with
+// split items when one-tile sequences' split items carry at least half the forward's
+// products, or when a longer sequence's last tile has a long key range to split (on the
+// long causal workload that kernel ran its forward 47.1 -> 46.7 ms).  The sliding-window
+// forward has no split form.
 bool prefer_split_forward(const int32_t* q_off, const int32_t* kv_off, int32_t B, int32_t causal, int32_t window) {
     if (window >= 0) return false;
-    int64_t split = 0, total = 0;
+    int64_t split = 0, total = 0;  // products of one-tile sequences' split items, of all items
+    bool long_split = false;        // a longer sequence's last tile is split
     for (int32_t b = 0; b < B; ++b) {
         const int64_t q_len = q_off[b + 1] - q_off[b];
         const int64_t kv_len = kv_off[b + 1] - kv_off[b];
@@ -220,10 +222,15 @@ bool prefer_split_forward(const int32_t* q_off, const int32_t* kv_off, int32_t B
             pair_stream(q_len, kv_len, t, causal, window, first, n, na, nb);
             const int64_t c = 2 * (int64_t(na) + nb) + 2;
             total += c;
-            if (q_len <= kFwdBM && na >= 2) split += c;
+            if (fwd_split_item(q_len, t, na)) {
+                if (q_len <= kFwdBM)
+                    split += c;
+                else
+                    long_split = true;
+            }
         }
     }
-    return split > 0 && 2 * split >= total;
+    return (split > 0 && 2 * split >= total) || long_split;
 }
 
 // The short-query backward keeps a whole query set in one tile of 64 or 128 rows and its

@@ -191,3 +191,17 @@ def test_split_forward_both_kernels(mode, causal, bias, long_len, split):
                        device="cuda", seed=13)
     g, _ = check_full(b)
     assert jfa.jfa_plan_info(g["plan"])["fwd_split"] == split
+
+
+@pytest.mark.parametrize("lens,split", [([2100, 600, 129, 256], 1), ([600, 1700, 129, 256], 0)])
+def test_split_forward_long_odd_tile(lens, split):
+    """The last, odd query tile of a longer causal sequence: split (its key range cut in two
+    halves run as the pair's two tiles, then merged) when it visits 16 key tiles or more
+    (2,100 tokens: 17 tiles), not otherwise (600 tokens: 5 tiles; 1,700 tokens: 14 tiles, an
+    even count, has no such tile); the other sequences keep their plain pairs.  Full outputs
+    and gradients against the oracle."""
+    from jagged_sequence_attention_gb300 import jfa
+    b = wl.make_custom(lens, lens, H=2, D=128, mode="softmax", causal=True, bias=True, device="cuda", seed=14)
+    for o_dtype in (torch.float32, torch.bfloat16):
+        g, _ = check_full(b, out_dtype=o_dtype)
+        assert jfa.jfa_plan_info(g["plan"])["fwd_split"] == split
