@@ -697,7 +697,7 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
         tm.done();
         if (e != cudaSuccess) return JFA_ERR_CUDA;
     }
-    CUtensorMap mq, mk, mv, mdo, mdq;
+    CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
     BwdParams p;
     if (v->n_bwd_items > 0 || (dtype == JFA_BF16 && v->n_dq_items > 0)) {
         const int q_box = short_q ? v->short_bq : kBwdBM;  // Q and dO rows per load
@@ -709,6 +709,10 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
             return s;
         // the fused backward's dQ accumulator, [T_q, H*D] fp32 in 32 x 32 boxes (reduce-adds)
         if (fused && (s = make_map(&mdq, JFA_F32, dq_acc, plan->Tq, plan->H, plan->D, plan->dev_block, 32)) != JFA_OK)
+            return s;
+        // and its dK, dV outputs, [T_kv, H*D] bf16 in 32-row boxes (stores of whole warps' rows)
+        if (fused && ((s = make_map(&mdk, JFA_BF16, dK, plan->Tkv, plan->H, plan->D, plan->dev_block, 32)) != JFA_OK ||
+                      (s = make_map(&mdv, JFA_BF16, dV, plan->Tkv, plan->H, plan->D, plan->dev_block, 32)) != JFA_OK))
             return s;
         p.items = v->d_bwd_items;
         p.cta_off = v->d_bwd_cta_off;
@@ -758,7 +762,7 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
     }
     if (v->n_bwd_items > 0) {
         KernelTimer tm(plan, 2, st);
-        e = dtype == JFA_BF16 ? (fused ? launch_bwd_fused(plan->D, mq, mk, mv, mdo, mdq, p, v->bwd_grid, st)
+        e = dtype == JFA_BF16 ? (fused ? launch_bwd_fused(plan->D, mq, mk, mv, mdo, mdq, mdk, mdv, p, v->bwd_grid, st)
                                        : launch_bwd_main(dtype, plan->D, mq, mk, mv, mdo, p, v->bwd_grid, st))
                               : launch_bwd_f32(plan->D, Q, K, V, dO, p, v->n_bwd_items, st);
         tm.done();

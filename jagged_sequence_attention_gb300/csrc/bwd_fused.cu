@@ -118,7 +118,8 @@ template <int D, bool GDPA>
 __global__ void __launch_bounds__(320, 1)
     jfa_bwd_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                         const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+                         const __grid_constant__ CUtensorMap tmDV, const BwdParams p) {
     using C = FuCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -166,6 +167,8 @@ __global__ void __launch_bounds__(320, 1)
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmdO);
         tma_prefetch_desc(&tmDQ);
+        tma_prefetch_desc(&tmDK);
+        tma_prefetch_desc(&tmDV);
     }
     tc_fence_before();
     __syncthreads();
@@ -713,20 +716,58 @@ __global__ void __launch_bounds__(320, 1)
             if (!warp_wait(FU_ACC_FULL, item_it & 1)) { ok = false; break; }
             tc_fence_after();
             {
-                const uint32_t stage_w = sbase + uint32_t(C::kOffStage + warp * 2048);
                 const uint32_t valid = __ballot_sync(0xffffffffu, key_valid);
-                const size_t off0 = ((size_t(kv0) + size_t(nt * C::BN + (warp & 3) * 32)) * size_t(p.H) + size_t(h)) * D +
-                                    size_t(wg * C::kEpiCols);
-                const size_t stride = size_t(p.H) * D;
-#pragma unroll
-                for (int cc = 0; cc < C::kEpiCols / 32; ++cc) {
+                if (D == 128 && valid == 0xffffffffu) {
+                    // Every key row of the warp lies in the sequence: each accumulator's 32 rows x
+                    // 64 columns are packed into the staging (the 128-byte-swizzled box layout)
+                    // and written by one TMA store.  (A box cannot skip rows, so a warp holding
+                    // the sequence's end, whose later rows belong to the next sequence, takes the
+                    // row-by-row path below.)
+                    const int ky = kv0 + nt * C::BN + (warp & 3) * 32;  // the warp's first key row
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {  // dV, then dK
-                        uint32_t rr[32];
-                        tmem_ld32(tmem + lane_base + (t ? C::kTmDK : C::kTmDV) + uint32_t(wg * C::kEpiCols + 32 * cc), rr);
-                        tmem_ld_wait(rr);
-                        store_chunk_bf16(stage_w, rr, t ? p.scale : 1.f, lane, valid,
-                                         reinterpret_cast<__nv_bfloat16*>(t ? p.dK : p.dV) + off0 + 32 * cc, stride);
+                        const float mul = t ? p.scale : 1.f;
+                        uint32_t w[32];  // bf16 pairs of columns (2k, 2k + 1)
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            uint32_t rr[32];
+                            tmem_ld32(tmem + lane_base + (t ? C::kTmDK : C::kTmDV) + uint32_t(wg * 64 + 32 * cc), rr);
+                            tmem_ld_wait(rr);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                w[16 * cc + i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * mul,
+                                                             __uint_as_float(rr[2 * i + 1]) * mul);
+                        }
+                        if (lane == 0) bulk_wait_read();  // the staging's previous box has been read
+                        __syncwarp();
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            st_shared_v4(stg + uint32_t(lane * 128 + ((q ^ (lane & 7)) << 4)), w[4 * q], w[4 * q + 1],
+                                         w[4 * q + 2], w[4 * q + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(t ? &tmDK : &tmDV, stg, h * D + wg * 64, ky);
+                            bulk_commit();
+                        }
+                    }
+                } else {
+                    const uint32_t stage_w = sbase + uint32_t(C::kOffStage + warp * 2048);
+                    const size_t off0 =
+                        ((size_t(kv0) + size_t(nt * C::BN + (warp & 3) * 32)) * size_t(p.H) + size_t(h)) * D +
+                        size_t(wg * C::kEpiCols);
+                    const size_t stride = size_t(p.H) * D;
+#pragma unroll
+                    for (int cc = 0; cc < C::kEpiCols / 32; ++cc) {
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {  // dV, then dK
+                            uint32_t rr[32];
+                            tmem_ld32(tmem + lane_base + (t ? C::kTmDK : C::kTmDV) + uint32_t(wg * C::kEpiCols + 32 * cc),
+                                      rr);
+                            tmem_ld_wait(rr);
+                            store_chunk_bf16(stage_w, rr, t ? p.scale : 1.f, lane, valid,
+                                             reinterpret_cast<__nv_bfloat16*>(t ? p.dK : p.dV) + off0 + 32 * cc, stride);
+                        }
                     }
                 }
             }
@@ -750,8 +791,8 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D, bool GDPA>
 cudaError_t launch_fused_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                           const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const BwdParams& p, int grid,
-                           cudaStream_t st) {
+                           const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const CUtensorMap& tmDK,
+                           const CUtensorMap& tmDV, const BwdParams& p, int grid, cudaStream_t st) {
     using C = FuCfg<D>;
     static bool configured = false;
     if (!configured) {
@@ -760,22 +801,22 @@ cudaError_t launch_fused_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_fused_kernel<D, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, tmDQ, p);
+    jfa_bwd_fused_kernel<D, GDPA><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, tmDQ, tmDK, tmDV, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_fused(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const BwdParams& p, int grid,
-                             cudaStream_t st) {
+                             const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const CUtensorMap& tmDK,
+                             const CUtensorMap& tmDV, const BwdParams& p, int grid, cudaStream_t st) {
     const bool sm = p.mode == JFA_SOFTMAX;
     if (D == 128)
-        return sm ? launch_fused_t<128, false>(tmQ, tmK, tmV, tmdO, tmDQ, p, grid, st)
-                  : launch_fused_t<128, true>(tmQ, tmK, tmV, tmdO, tmDQ, p, grid, st);
+        return sm ? launch_fused_t<128, false>(tmQ, tmK, tmV, tmdO, tmDQ, tmDK, tmDV, p, grid, st)
+                  : launch_fused_t<128, true>(tmQ, tmK, tmV, tmdO, tmDQ, tmDK, tmDV, p, grid, st);
     if (D == 64)
-        return sm ? launch_fused_t<64, false>(tmQ, tmK, tmV, tmdO, tmDQ, p, grid, st)
-                  : launch_fused_t<64, true>(tmQ, tmK, tmV, tmdO, tmDQ, p, grid, st);
+        return sm ? launch_fused_t<64, false>(tmQ, tmK, tmV, tmdO, tmDQ, tmDK, tmDV, p, grid, st)
+                  : launch_fused_t<64, true>(tmQ, tmK, tmV, tmdO, tmDQ, tmDK, tmDV, p, grid, st);
     return cudaErrorInvalidValue;
 }
 

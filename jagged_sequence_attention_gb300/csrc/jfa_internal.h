@@ -294,10 +294,11 @@ cudaError_t launch_bwd_post(int dtype, int D, const float* dq_acc, void* dQ, int
                             float scale, cudaStream_t st);
 // bf16 inputs, fused backward (bwd_fused.cu): dK, dV and the key tile's part of dQ, added
 // into the fp32 accumulator (zeroed first; tmDQ: its [T_q, H*D] view in 32 x 32 boxes,
-// 128-byte swizzle) for launch_bwd_post to scale and convert.
+// 128-byte swizzle) for launch_bwd_post to scale and convert.  tmDK, tmDV: the [T_kv, H*D]
+// bf16 outputs in 32-row x 64-column boxes, 128-byte swizzle (stores of whole boxes).
 cudaError_t launch_bwd_fused(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const BwdParams& p, int grid,
-                             cudaStream_t st);
+                             const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const CUtensorMap& tmDK,
+                             const CUtensorMap& tmDV, const BwdParams& p, int grid, cudaStream_t st);
 // bf16 inputs, short-query backward (bwd_short.cu): dQ, dK and dV in one kernel over
 // (sequence, head) items of plans whose query sets have at most bq (64 or 128) rows.
 cudaError_t launch_bwd_short(int D, int bq, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
