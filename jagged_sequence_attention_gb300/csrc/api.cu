@@ -40,10 +40,10 @@ inline size_t elem_bytes(int dtype) { return dtype == JFA_F32 ? 4 : 2; }
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// 2-D view [rows, H*D] of a token-major [T, H, D] tensor, box = 128 bytes x box_rows,
-// 128-byte swizzle, zero fill beyond the last row.
+// 2-D view [rows, H*D] of a token-major [T, H, D] tensor, box = box_bytes (128 or 64) x
+// box_rows, swizzled over the box row (128- or 64-byte swizzle), zero fill beyond the last row.
 jfa_status make_map(CUtensorMap* map, int dtype, const void* base, int64_t rows, int H, int D,
-                    const void* dummy, int box_rows = 128) {
+                    const void* dummy, int box_rows = 128, int box_bytes = 128) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return JFA_ERR_CUDA;
     const size_t E = elem_bytes(dtype);
@@ -53,11 +53,12 @@ jfa_status make_map(CUtensorMap* map, int dtype, const void* base, int64_t rows,
     }
     cuuint64_t dims[2] = {cuuint64_t(H) * cuuint64_t(D), cuuint64_t(rows)};
     cuuint64_t strides[1] = {cuuint64_t(H) * cuuint64_t(D) * E};
-    cuuint32_t box[2] = {cuuint32_t(128 / E), cuuint32_t(box_rows)};
+    cuuint32_t box[2] = {cuuint32_t(box_bytes / int(E)), cuuint32_t(box_rows)};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = enc(map, dtype == JFA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? JFA_OK : JFA_ERR_CUDA;
 }
@@ -750,12 +751,16 @@ static jfa_status bwd_impl(jfa_plan plan, int32_t dtype, const void* Q, const vo
     }
     if (short_q) {
         // one kernel writes dQ, dK and dV (also the zero rows of sequences without a query
-        // or a key)
+        // or a key); dK and dV of whole warps' rows by TMA stores of 32 x 32 boxes
+        if (v->n_short_items > 0 &&
+            ((s = make_map(&mdk, dtype, dK, plan->Tkv, plan->H, plan->D, plan->dev_block, 32, 64)) != JFA_OK ||
+             (s = make_map(&mdv, dtype, dV, plan->Tkv, plan->H, plan->D, plan->dev_block, 32, 64)) != JFA_OK))
+            return s;
         p.items = v->d_short_items;
         p.cta_off = v->d_short_cta_off;
         KernelTimer tm(plan, 2, st);
         e = v->n_short_items > 0
-                ? launch_bwd_short(plan->D, v->short_bq, mq, mk, mv, mdo, p, v->short_grid, st)
+                ? launch_bwd_short(plan->D, v->short_bq, mq, mk, mv, mdo, mdk, mdv, p, v->short_grid, st)
                 : cudaSuccess;
         tm.done();
         return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;

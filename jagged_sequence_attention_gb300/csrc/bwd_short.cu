@@ -111,6 +111,7 @@ template <int D, int BQ, int MODE>
 __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
     jfa_bwd_short_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                         const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                          const BwdParams p) {
     using C = ShCfg<D, BQ>;
     extern __shared__ uint8_t smem_raw[];
@@ -154,6 +155,8 @@ __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmdO);
+        tma_prefetch_desc(&tmDK);
+        tma_prefetch_desc(&tmDV);
     }
     tc_fence_before();
     __syncthreads();
@@ -482,10 +485,17 @@ __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(SH_DS_FULL));
 
-                // Epilogue of the tile: dV as soon as its product is done, then dK (times scale).
+                // Epilogue of the tile: dV as soon as its product is done, then dK (times scale),
+                // 32 columns at a time through the staging.  A warp whose 32 key rows all lie in
+                // the sequence writes an accumulator's first chunk with one TMA store of the
+                // staged box and any second chunk (head_dim 128) row by row: with one 2 KB
+                // staging per warp a second box would wait for the first to be read, which
+                // measured slower.  A warp holding the sequence's end stores row by row (a box
+                // cannot skip the rows that belong to the next sequence).  Before the staging is
+                // written, the lane that issued the previous box waits until it has been read.
                 const uint32_t valid = __ballot_sync(0xffffffffu, key_valid);
-                const size_t off0 =
-                    (size_t(kv0 + t * C::BN + quarter * 32) * size_t(p.H) + size_t(h)) * D + size_t(wg * C::kEpiCols);
+                const int ky = kv0 + t * C::BN + quarter * 32;  // the warp's first key row
+                const size_t off0 = (size_t(ky) * size_t(p.H) + size_t(h)) * D + size_t(wg * C::kEpiCols);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {  // dV, then dK
                     if (!warp_wait(u ? SH_ACC_FULL : SH_DV_FULL, kv_it & 1)) { ok = false; break; }
@@ -495,10 +505,22 @@ __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
                         uint32_t rr[32];
                         tmem_ld32(tmem + lane_base + (u ? C::kTmZ : C::kTmY) + uint32_t(wg * C::kEpiCols + 32 * cc), rr);
                         tmem_ld_wait(rr);
-                        if (valid)
+                        if (!valid) continue;
+                        if (lane == 0) bulk_wait_read();
+                        __syncwarp();
+                        if (valid == 0xffffffffu && cc == 0) {
+                            stage_chunk_bf16(stg, rr, u ? p.scale : 1.f, lane);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(u ? &tmDK : &tmDV, stg, h * D + wg * C::kEpiCols + 32 * cc, ky);
+                                bulk_commit();
+                            }
+                        } else {
                             store_chunk_bf16(stg, rr, u ? p.scale : 1.f, lane, valid,
                                              reinterpret_cast<__nv_bfloat16*>(u ? p.dK : p.dV) + off0 + 32 * cc,
                                              row_stride);
+                        }
                     }
                 }
                 if (!ok) break;
@@ -519,6 +541,8 @@ __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
                         uint32_t rr[32];
                         tmem_ld32(tmem + lane_base + C::kTmW + uint32_t(wg * C::kEpiCols + 32 * cc), rr);
                         tmem_ld_wait(rr);
+                        if (lane == 0) bulk_wait_read();
+                        __syncwarp();
                         store_chunk_bf16(stg, rr, p.scale, lane, valid,
                                          reinterpret_cast<__nv_bfloat16*>(p.dQ) + off0 + 32 * cc, row_stride);
                     }
@@ -529,6 +553,9 @@ __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
             if (lane == 0) mbar_arrive(bar(SH_DQ_EMPTY));
         }
         if (!ok) fail();
+        // Every store this warp's lane issued has completed before the CTA exits.
+        if (lane == 0) bulk_wait_done();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -539,7 +566,8 @@ __global__ void __launch_bounds__(320, ShCfg<D, BQ>::kCtasPerSm)
 
 template <int D, int BQ, int MODE>
 cudaError_t launch_short_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                           const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
+                           const CUtensorMap& tmdO, const CUtensorMap& tmDK, const CUtensorMap& tmDV, const BwdParams& p,
+                           int grid, cudaStream_t st) {
     using C = ShCfg<D, BQ>;
     static bool configured = false;
     if (!configured) {
@@ -548,7 +576,7 @@ cudaError_t launch_short_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_short_kernel<D, BQ, MODE><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, p);
+    jfa_bwd_short_kernel<D, BQ, MODE><<<grid, C::kThreads, C::kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO, tmDK, tmDV, p);
     return cudaGetLastError();
 }
 
@@ -563,18 +591,20 @@ int short_ctas_per_sm(int D, int bq) {
 
 template <int D, int BQ>
 static cudaError_t launch_short_m(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                  const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
-    if (p.mode == JFA_SOFTMAX) return launch_short_t<D, BQ, JFA_SOFTMAX>(tmQ, tmK, tmV, tmdO, p, grid, st);
+                                  const CUtensorMap& tmdO, const CUtensorMap& tmDK, const CUtensorMap& tmDV,
+                                  const BwdParams& p, int grid, cudaStream_t st) {
+    if (p.mode == JFA_SOFTMAX) return launch_short_t<D, BQ, JFA_SOFTMAX>(tmQ, tmK, tmV, tmdO, tmDK, tmDV, p, grid, st);
     if (p.mode == JFA_GDPA_GELU_TANH)
-        return launch_short_t<D, BQ, JFA_GDPA_GELU_TANH>(tmQ, tmK, tmV, tmdO, p, grid, st);
-    return launch_short_t<D, BQ, JFA_GDPA_SILU>(tmQ, tmK, tmV, tmdO, p, grid, st);
+        return launch_short_t<D, BQ, JFA_GDPA_GELU_TANH>(tmQ, tmK, tmV, tmdO, tmDK, tmDV, p, grid, st);
+    return launch_short_t<D, BQ, JFA_GDPA_SILU>(tmQ, tmK, tmV, tmdO, tmDK, tmDV, p, grid, st);
 }
 
 cudaError_t launch_bwd_short(int D, int bq, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st) {
-    if (D == 64 && bq == 64) return launch_short_m<64, 64>(tmQ, tmK, tmV, tmdO, p, grid, st);
-    if (D == 64 && bq == 128) return launch_short_m<64, 128>(tmQ, tmK, tmV, tmdO, p, grid, st);
-    if (D == 128 && bq == 128) return launch_short_m<128, 128>(tmQ, tmK, tmV, tmdO, p, grid, st);
+                             const CUtensorMap& tmdO, const CUtensorMap& tmDK, const CUtensorMap& tmDV,
+                             const BwdParams& p, int grid, cudaStream_t st) {
+    if (D == 64 && bq == 64) return launch_short_m<64, 64>(tmQ, tmK, tmV, tmdO, tmDK, tmDV, p, grid, st);
+    if (D == 64 && bq == 128) return launch_short_m<64, 128>(tmQ, tmK, tmV, tmdO, tmDK, tmDV, p, grid, st);
+    if (D == 128 && bq == 128) return launch_short_m<128, 128>(tmQ, tmK, tmV, tmdO, tmDK, tmDV, p, grid, st);
     return cudaErrorInvalidValue;
 }
 

@@ -301,8 +301,10 @@ cudaError_t launch_bwd_fused(int D, const CUtensorMap& tmQ, const CUtensorMap& t
                              const CUtensorMap& tmDV, const BwdParams& p, int grid, cudaStream_t st);
 // bf16 inputs, short-query backward (bwd_short.cu): dQ, dK and dV in one kernel over
 // (sequence, head) items of plans whose query sets have at most bq (64 or 128) rows.
+// tmDK, tmDV: the [T_kv, H*D] bf16 outputs in 32 x 32 boxes, 64-byte swizzle (stores).
 cudaError_t launch_bwd_short(int D, int bq, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             const CUtensorMap& tmdO, const BwdParams& p, int grid, cudaStream_t st);
+                             const CUtensorMap& tmdO, const CUtensorMap& tmDK, const CUtensorMap& tmDV,
+                             const BwdParams& p, int grid, cudaStream_t st);
 // CTAs of that kernel an SM holds (2 at D = 64 with 64-row query tiles), 0 if unsupported.
 int short_ctas_per_sm(int D, int bq);
 // bf16 inputs, GDPA modes, short-query forward (fwd_short.cu): O over the same (sequence,

@@ -354,16 +354,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
-// Writes a warp's 32 x 32 fp32 chunk (lane = row, raw = the row's 32 values as bits),
-// each times `mul`, as bf16 to 32 global rows of 64 bytes: row r at dst + r * stride
-// (elements; 16-byte aligned), skipped unless bit r of valid is set.  Each lane stores its
-// row's four 16-byte pieces in the warp's 2 KB staging buffer at shared address stg
-// (piece q of row r at slot q ^ ((r >> 1) & 3), so that any eight consecutive rows cover
-// all 32 banks), then every global store instruction writes eight whole 64-byte rows.
-// Stored straight from registers, each instruction would instead touch 32 rows, one
-// 16-byte piece of each: four times the cache-line transactions.
-__device__ __forceinline__ void store_chunk_bf16(uint32_t stg, const uint32_t (&raw)[32], float mul, int lane,
-                                                 uint32_t valid, __nv_bfloat16* dst, size_t stride) {
+// Packs a warp's 32 x 32 fp32 chunk (lane = row, raw = the row's 32 values as bits), each
+// times `mul`, as bf16 into the warp's 2 KB staging buffer at shared address stg: row r's
+// 16-byte piece q at byte 64 r + 16 (q ^ ((r >> 1) & 3)), so that any eight consecutive rows
+// cover all 32 banks.  That is also the box layout of a tensor map with 64-byte box rows and
+// 64-byte swizzle (16-byte chunks XORed with bits 7-8 of the address; stg 512-byte aligned).
+__device__ __forceinline__ void stage_chunk_bf16(uint32_t stg, const uint32_t (&raw)[32], float mul, int lane) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         st_shared_v4(stg + uint32_t(lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)),
@@ -373,6 +369,16 @@ __device__ __forceinline__ void store_chunk_bf16(uint32_t stg, const uint32_t (&
                      pack_bf16x2(__uint_as_float(raw[8 * q + 6]) * mul, __uint_as_float(raw[8 * q + 7]) * mul));
     }
     __syncwarp();
+}
+
+// Writes a warp's 32 x 32 fp32 chunk (as stage_chunk_bf16) as bf16 to 32 global rows of 64
+// bytes: row r at dst + r * stride (elements; 16-byte aligned), skipped unless bit r of valid
+// is set.  The rows go through the staging, so every global store instruction writes eight
+// whole 64-byte rows.  Stored straight from registers, each instruction would instead touch
+// 32 rows, one 16-byte piece of each: four times the cache-line transactions.
+__device__ __forceinline__ void store_chunk_bf16(uint32_t stg, const uint32_t (&raw)[32], float mul, int lane,
+                                                 uint32_t valid, __nv_bfloat16* dst, size_t stride) {
+    stage_chunk_bf16(stg, raw, mul, lane);
     const int piece = lane & 3;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
