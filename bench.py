@@ -16,6 +16,7 @@ bounded sample of the same workload.  Under torchrun each rank runs its own batc
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -226,8 +227,10 @@ def oracle_sample(batch, target_seconds=15.0):
         seqs.append(int(b))
         tot += f
     sub = wl.subset(batch, seqs)
-    cpu = wl.Batch(sub.name, sub.q_off, sub.kv_off, sub.Q.cpu(), sub.K.cpu(), sub.V.cpu(), sub.dO.cpu(),
-                   None if sub.bias is None else sub.bias.cpu(), sub.scale, sub.mode, sub.causal, sub.H, sub.D)
+    # the same problem (window and all) with its tensors on the host
+    cpu = dataclasses.replace(sub, Q=sub.Q.cpu(), K=sub.K.cpu(), V=sub.V.cpu(), dO=sub.dO.cpu(),
+                              bias=None if sub.bias is None else sub.bias.cpu(),
+                              dense=None if sub.dense is None else sub.dense.cpu())
     return cpu, seqs
 
 

@@ -76,3 +76,25 @@ def test_sample_errors_apply_the_parity_tolerances():
     got = {k: v.copy() for k, v in ref.items()}
     got["O"] = ref["O"] + 0.05  # beyond the forward's max-abs bound
     assert not bench.sample_errors(got, ref, True)["within_tolerance"]
+
+
+def test_oracle_sample_is_the_same_problem():
+    """The bench's oracle sample (its CPU baseline and parity check) keeps every property of
+    the workload: on a sliding-window batch it must compute windowed attention."""
+    import dataclasses
+    import numpy as np
+    import bench
+    from jagged_sequence_attention_gb300 import workloads as wl
+    b = wl.make_custom([40, 90, 70], [40, 90, 70], H=2, D=32, dtype=torch.float32, causal=True, bias=True,
+                       window=16, device="cpu", seed=21)
+    cpu, seqs = bench.oracle_sample(b, 1.0)
+    assert cpu.window == 16 and cpu.causal and cpu.bias is not None
+    got = {}
+    bench.run_oracle_once(cpu, got)
+    plain = {}
+    bench.run_oracle_once(dataclasses.replace(cpu, window=None), plain)
+    sub = wl.subset(b, seqs)
+    ref = {}
+    bench.run_oracle_once(sub, ref)
+    assert np.array_equal(got["O"], ref["O"]) and np.array_equal(got["dQ"], ref["dQ"])
+    assert not np.allclose(got["O"], plain["O"])  # the window changes the result
