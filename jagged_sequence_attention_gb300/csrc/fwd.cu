@@ -52,11 +52,13 @@ struct FwdCfg {
     // softmax warps: 2 tiles x 2 column halves x 4 row quarters
     static constexpr int kSoftWarps = 16;
     // tmem slot + abort flag; per softmax warp: the head's bias row (32) and a tile's
-    // bias-by-relative-position table (160)
+    // bias-by-relative-position table (160), with a copy shifted by one entry (so that every
+    // lane reads its column pairs as aligned 8-byte loads)
     static constexpr int kBiasRow = 32, kBiasTab = 160;
+    static constexpr int kWarpBias = kBiasRow + 2 * kBiasTab;
     // ... for split items, tile 1's row max and two partial sums (two buffers of 3 x BM
     // floats), and the pair exchanges (two buffers of 2 halves x 8 pairs x 32 floats)
-    static constexpr int kMiscBytes = 16 + kSoftWarps * (kBiasRow + kBiasTab) * 4 + 2 * 3 * BM * 4 + 2 * 2 * 8 * 32 * 4;
+    static constexpr int kMiscBytes = 16 + kSoftWarps * kWarpBias * 4 + 2 * 3 * BM * 4 + 2 * 2 * 8 * 32 * 4;
     static constexpr int kSmemNeed = kOffMisc + kMiscBytes + 1024;
     // At least 120 KB so that exactly one CTA fits on an SM: the CTA allocates all
     // 512 TMEM columns.
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(576, 1)
         uint32_t s_cnt = 0;
         uint32_t split_cnt = 0;  // split items seen (phase of B_COMBINE, exchange buffer)
         uint32_t x_cnt = 0;      // exchanges with the partner warp (phase of its barrier)
-        float* comb_s = bias_s + C::kSoftWarps * (C::kBiasRow + C::kBiasTab);  // [2][m, l0, l1][BM]
+        float* comb_s = bias_s + C::kSoftWarps * C::kWarpBias;  // [2][m, l0, l1][BM]
         float* xch_s = comb_s + 2 * 3 * C::BM;                                  // [2][2][8][32]
         // The partner warp's value of a per-row float this warp also passes in.
         auto exchange = [&](float v, float& other) -> bool {
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(576, 1)
                        size_t(row_valid ? row : 0) * size_t(kv_len);
             // Each warp keeps its own copy of the head's bias row (log2 units for
             // softmax) and its maximum, so no cross-warp barrier is needed.
-            float* btab = bias_s + warp * (C::kBiasRow + C::kBiasTab);
+            float* btab = bias_s + warp * C::kWarpBias;
             float* rtab = btab + C::kBiasRow;
             float bmax = 0.f;
             if (p.bias) {
@@ -529,16 +531,23 @@ __global__ void __launch_bounds__(576, 1)
                     for (int k = 0; k < 2; ++k) cb[k] = __shfl_sync(0xffffffffu, bv, k);
                 }
                 if (hmask != 3u) {
-                    // rtab[i] = bias(r) for r = (lane 0's rbase) - 127 + i, i in [0, 160):
-                    // element (lane, c) reads rtab[lane + 127 - c].
+                    // rtab[i] = bias(r) for r = (lane 0's rbase) - 127 + i, i in [0, 160): element
+                    // (lane, c) is rtab[lane + 127 - c]; and rtab[160 + i] = rtab[i + 1].
                     const int r0 = __shfl_sync(0xffffffffu, rbase, 0) - (C::BN - 1);
                     __syncwarp();
 #pragma unroll
-                    for (int m2 = 0; m2 < C::kBiasTab / 32; ++m2)
-                        rtab[lane + 32 * m2] = btab[relpos_bucket(r0 + lane + 32 * m2)];
+                    for (int m2 = 0; m2 < C::kBiasTab / 32; ++m2) {
+                        const int i = lane + 32 * m2;
+                        const float v = btab[relpos_bucket(r0 + i)];
+                        rtab[i] = v;
+                        if (i > 0) rtab[C::kBiasTab + i - 1] = v;
+                    }
                     __syncwarp();
                 }
-                const float* rrow = rtab + lane + (C::BN - 1);  // rrow[-c] = bias of column c
+                // Columns (c, c + 1), c even, as one aligned float2 (bias of c + 1, bias of c) at
+                // rpair - c: even lanes read the table at lane + 126 - c, odd lanes the shifted
+                // copy at lane + 125 - c.
+                const float* rpair = (lane & 1) ? rtab + C::kBiasTab + lane + (C::BN - 3) : rtab + lane + (C::BN - 2);
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(B_S_FULL + x), s_cnt & 1, abort_flag))) {
                     ok = false;
                     break;
@@ -575,9 +584,15 @@ __global__ void __launch_bounds__(576, 1)
                             r[i + 1] = __float_as_uint(t2.y);
                         }
                     } else {
+                        const float2 sc = make_float2(xs, xs), ns = make_float2(-shift, -shift);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(fmaf(__uint_as_float(r[i]), xs, rrow[-(32 * kk + i)] - shift));
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 bb = *reinterpret_cast<const float2*>(rpair - (32 * kk + i));
+                            const float2 t2 = fma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sc,
+                                                   add2(make_float2(bb.y, bb.x), ns));
+                            r[i] = __float_as_uint(t2.x);
+                            r[i + 1] = __float_as_uint(t2.y);
+                        }
                     }
                     if (!full) {
                         const int lk = lim - 32 * kk, lok = lo - 32 * kk;
@@ -658,11 +673,24 @@ __global__ void __launch_bounds__(576, 1)
                     for (int k = 0; k < 2; ++k) {
                         const int kk = 2 * hf + k;
                         uint32_t pk[16];
-                        if (fast) {
+                        if (!DENSE && full && (hmask & (1u << k))) {
                             const float2 xs2 = make_float2(xs, xs), add = make_float2(cb[k] - m_use, cb[k] - m_use);
 #pragma unroll
                             for (int i = 0; i < 32; i += 2) {
                                 const float2 t2 = fma2(make_float2(__uint_as_float(sr[k][i]), __uint_as_float(sr[k][i + 1])), xs2, add);
+                                const float2 e2 = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
+                                rs[(i >> 1) & 1] = add2(rs[(i >> 1) & 1], e2);
+                                pk[i >> 1] = pack_bf16x2(e2.x, e2.y);
+                            }
+                        } else if (!DENSE && full) {
+                            // no column masked, bias per element: the same single loop with the
+                            // bias pair read from the table
+                            const float2 xs2 = make_float2(xs, xs), nm = make_float2(-m_use, -m_use);
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                const float2 bb = *reinterpret_cast<const float2*>(rpair - (32 * kk + i));
+                                const float2 t2 = fma2(make_float2(__uint_as_float(sr[k][i]), __uint_as_float(sr[k][i + 1])), xs2,
+                                                       add2(make_float2(bb.y, bb.x), nm));
                                 const float2 e2 = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
                                 rs[(i >> 1) & 1] = add2(rs[(i >> 1) & 1], e2);
                                 pk[i >> 1] = pack_bf16x2(e2.x, e2.y);
