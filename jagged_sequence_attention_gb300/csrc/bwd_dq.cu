@@ -25,6 +25,15 @@ namespace jfa {
 
 namespace {
 
+// relpos_bucket_start(b) for every bucket, looked up with a warp-uniform index
+struct BucketStarts {
+    int v[32];
+    constexpr BucketStarts() : v() {
+        for (int b = 0; b < 32; ++b) v[b] = relpos_bucket_start(b);
+    }
+};
+__constant__ BucketStarts kBucketStart = BucketStarts();
+
 template <int D>
 struct QCfg {
     static constexpr int BM = kFwdBM;  // query rows (TMEM lanes)
@@ -363,17 +372,28 @@ __global__ void __launch_bounds__(320, 1)
                 const int rb = row + diag - col0;  // relative position of local column 0
                 // Lane k tests chunk k for the whole warp: over the warp's rows, chunk k
                 // spans relative positions rb(lane 0) - 32k - 31 .. + 62.
-                bool cconst[2] = {true, true};
-                float cbias[2] = {0.f, 0.f};
+                // A chunk that is not one bucket but exactly two (the warp's positions all >= 0,
+                // its lowest one bucket below its highest) takes its bias per lane from a column
+                // threshold: columns c <= rb - start(upper bucket) are in the upper bucket.
+                bool cconst[2] = {true, true}, two[2] = {false, false};
+                float cbias[2] = {0.f, 0.f}, clow[2] = {0.f, 0.f};
+                int cstart[2] = {0, 0};
                 if (p.bias) {
                     const int rb0 = __shfl_sync(0xffffffffu, rb, 0);
                     int bk = 0;
-                    const uint32_t cm = warp_const_chunks(lane < 2, rb0 - 32 * lane - 31, bk);
-                    const float bv = bias_w[bk];
+                    const int lo_k = rb0 - 32 * lane - 31;  // lane k < 2: chunk k's lowest position
+                    const uint32_t cm = warp_const_chunks(lane < 2, lo_k, bk);
+                    const uint32_t tm =
+                        __ballot_sync(0xffffffffu, lane < 2 && lo_k >= 0 && relpos_bucket(lo_k) == bk - 1);
+                    const float bv = bias_w[bk], bv_low = bias_w[bk > 0 ? bk - 1 : 0];
+                    const int st = kBucketStart.v[lane < 2 ? bk : 0];
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
                         cconst[k] = (cm >> k) & 1u;
+                        two[k] = (tm >> k) & 1u;
                         cbias[k] = __shfl_sync(0xffffffffu, bv, k);
+                        clow[k] = __shfl_sync(0xffffffffu, bv_low, k);
+                        cstart[k] = __shfl_sync(0xffffffffu, st, k);
                     }
                 }
                 const uint32_t tS = tmem + lane_base + sb * 128u + uint32_t(c0);
@@ -418,6 +438,16 @@ __global__ void __launch_bounds__(320, 1)
                             const float2 add = make_float2(cbias[k] - lse_row, cbias[k] - lse_row);
 #pragma unroll
                             for (int c = 32 * k; c < 32 * k + 32; c += 2) {
+                                const float2 e = fma2(make_float2(pv[c], pv[c + 1]), xs2, add);
+                                pv[c] = ex2_approx(e.x);
+                                pv[c + 1] = ex2_approx(e.y);
+                            }
+                        } else if (two[k]) {
+                            const float ahi = cbias[k] - lse_row, alo = clow[k] - lse_row;
+                            const int t = rb - cstart[k];  // columns c <= t: the upper bucket
+#pragma unroll
+                            for (int c = 32 * k; c < 32 * k + 32; c += 2) {
+                                const float2 add = make_float2(c <= t ? ahi : alo, c + 1 <= t ? ahi : alo);
                                 const float2 e = fma2(make_float2(pv[c], pv[c + 1]), xs2, add);
                                 pv[c] = ex2_approx(e.x);
                                 pv[c + 1] = ex2_approx(e.y);

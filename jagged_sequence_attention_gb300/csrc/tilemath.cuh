@@ -16,6 +16,20 @@ __device__ __forceinline__ int relpos_bucket(int r) {
     return r >= 46340 ? 31 : b;
 }
 
+// The first relative position of bucket b or above: the smallest r >= 0 with
+// (1 + r)^2 >= 2^b (b <= 31), by an exact integer search.
+__host__ __device__ constexpr int relpos_bucket_start(int b) {
+    long long lo = 0, hi = 46340;
+    while (lo < hi) {
+        const long long mid = (lo + hi) / 2;
+        if ((1 + mid) * (1 + mid) >= (1LL << b))
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return int(lo);
+}
+
 // Warp-level test of whether a 32-column chunk's bias is one value.  In the callers,
 // the 32 lanes' windows for one chunk tile a range of 63 relative positions
 // [lo, lo + 62] (consecutive rows or keys shift the window by one).  The bucket of |r| is monotone on a range that does not
