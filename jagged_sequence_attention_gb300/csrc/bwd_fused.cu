@@ -419,10 +419,12 @@ __global__ void __launch_bounds__(320, 1)
         bool ok = true;
 
         // dQ(g) of query rows [qrow0, qrow0 + 128) of a sequence whose first row is dq_y0 (of
-        // dq_len rows), at accumulator column dq_x0 (this warpgroup's half of head h):
-        // TMEM Y -> registers, after which Y is released for the next dP; then, 32 columns
-        // at a time, this warp's 32 rows go through its staging (the 128-byte-swizzled box
-        // layout) and a TMA reduce-add into the accumulator.  The box covers all 32 rows: rows
+        // dq_len rows), at accumulator column dq_x0 (this warpgroup's half of head h), 32
+        // columns at a time: TMEM Y -> registers -> this warp's staging (the 128-byte-swizzled
+        // box layout) -> a TMA reduce-add into the accumulator.  Y is released for the next dP
+        // once its last columns are read.  The staging was last read by a box before this
+        // warp wrote its dS rows there, which waited for that, so only a second box waits.
+        // The box covers all 32 rows: rows
         // past the sequence end hold zeros (their dS is 0), and adding a zero leaves any value
         // of the accumulator as it is (it starts at +0, so no sum in it is ever -0); rows past
         // the accumulator's end are clipped by the tensor map.  A warp whose rows all lie past
