@@ -25,6 +25,17 @@ namespace jfa {
 
 namespace {
 
+// Every start is the first position of its bucket or above: (1 + s)^2 >= 2^b, and s - 1 is
+// below it (s^2 < 2^b); checked here when the library is built.
+constexpr bool bucket_starts_hold() {
+    for (int b = 0; b < 32; ++b) {
+        const long long st = relpos_bucket_start(b);
+        if ((1 + st) * (1 + st) < (1LL << b) || (st > 0 && st * st >= (1LL << b))) return false;
+    }
+    return true;
+}
+static_assert(bucket_starts_hold(), "relative-position bucket starts");
+
 // relpos_bucket_start(b) for every bucket, looked up with a warp-uniform index
 struct BucketStarts {
     int v[32];
